@@ -1,0 +1,421 @@
+"""Throughput of the collapse-safe CE forward+backward on one GB300 (or N replicas).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload pages|chunked|mid|linear]
+
+One step = ce_forward + ce_backward over one batch of the workload (default: the pages'
+shape, T=16384 rows x V=128256 bf16 logits, mean over non-ignored rows, 10% of rows with
+the target raised by 17..50 above the row max, 1% ignored).  Inputs are resident in HBM
+before the timed region; the 4.2 GB logits are ~33x the 129 MB L2, so every pass streams
+from HBM with no flush needed.  `value` is whole-job tokens/s (all ranks); `e2e` is the same
+metric with the step's inputs copied from pinned host memory and the loss read back inside
+the timed region.  `--impl reference` times the fp64 CPU oracle on a bounded row sample.
+
+Under torchrun (--gpus N > 1) each rank runs an independent replica on its own batch
+(rows are independent: no data-path collective); the timed region is bracketed by a
+barrier and the max over ranks is taken.  Rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import gen  # noqa: E402
+
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+PROFILE_DIR = os.path.join(ROOT, "profiles")
+
+
+# ------------------------------------------------------------------------------- distributed plumbing
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
+
+
+def init_dist(world, backend):
+    if world > 1:
+        import torch.distributed as dist
+        if not dist.is_initialized():
+            dist.init_process_group(backend)
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    if world == 1:
+        return float(x)
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, world: int, device=None) -> float:
+    if world == 1:
+        return float(x)
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------------------- peaks, clocks, profiles
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(path))
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS,
+                "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, period_ms: int = 50):
+        self.gpu = gpu_index
+        self.period = period_ms
+        self.proc = None
+        self.out = None
+
+    def __enter__(self):
+        try:
+            self.out = open(os.devnull if False else f"/tmp/vce_clocks_{os.getpid()}.csv", "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", f"-lms", str(self.period)],
+                                         stdout=self.out, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        if self.out:
+            self.out.close()
+
+    def summary(self):
+        path = f"/tmp/vce_clocks_{os.getpid()}.csv"
+        if self.proc is None or not os.path.exists(path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        rows = []
+        for line in open(path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append({"sm": float(parts[1]), "max": float(parts[2]), "power": float(parts[3]),
+                             "active": parts[4], "hw": parts[5], "hwt": parts[6], "swt": parts[7], "pcap": parts[8]})
+            except ValueError:
+                continue
+        os.remove(path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        loaded = [r for r in rows if r["power"] > 200] or rows
+        reasons = set()
+        for r in loaded:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"), ("swt", "sw_thermal_slowdown"),
+                              ("pcap", "sw_power_cap")):
+                if r[key].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in loaded), "sm_max_mhz": max(r["max"] for r in rows),
+                "reasons": sorted(reasons), "samples": len(loaded),
+                "power_w_max": max(r["power"] for r in rows)}
+
+
+def kernel_source_hash(files):
+    h = hashlib.sha256()
+    for f in files:
+        h.update(open(os.path.join(ROOT, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(name, files):
+    """DRAM bytes per launch from a committed ncu summary, if it matches the current source."""
+    path = os.path.join(PROFILE_DIR, f"{name}.json")
+    try:
+        d = json.load(open(path))
+    except Exception:
+        return None
+    if d.get("source_hash") != kernel_source_hash(files):
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------------------------- workloads
+
+class CEWorkload:
+    """The pages' shape (default) or the mid shape: ce_forward + ce_backward."""
+
+    KERNEL_FILES = ["vocab_cross_entropy_gb300/csrc/ce.cu", "vocab_cross_entropy_gb300/csrc/vce_device.cuh"]
+
+    def __init__(self, problem, device):
+        import vocab_cross_entropy_gb300 as vce
+        self.vce = vce
+        self.p = problem
+        self.dev = device
+        T, V = problem.T, problem.V
+        self.host = torch.empty((T, V), dtype=torch.int16, pin_memory=True)
+        problem.full(out=self.host.numpy().view(np.uint16))
+        self.host_bf16 = self.host.view(torch.bfloat16)
+        self.labels_host = torch.from_numpy(problem.labels).pin_memory()
+        self.logits = self.host_bf16.to(device)
+        self.labels = self.labels_host.to(device)
+        self.loss_rows = torch.empty(T, dtype=torch.float32, device=device)
+        self.loss_out = torch.empty(1, dtype=torch.float32, device=device)
+        self.stats = torch.empty(T, 4, dtype=torch.float32, device=device)
+        self.status = torch.empty(1, dtype=torch.int32, device=device)
+        self.go = torch.ones(1, dtype=torch.float32, device=device)
+        self.grad = torch.empty((T, V), dtype=torch.bfloat16, device=device)
+        self.loss_host = torch.empty(1, dtype=torch.float32, pin_memory=True)
+        self.n_valid = int(np.sum(problem.labels != problem.ignore_index))
+        self.launches_per_step = 3            # k_ce_fwd, k_ce_reduce, k_ce_bwd
+
+    def fwd(self, stream):
+        self.vce.ce_forward(self.logits, self.labels, loss_rows=self.loss_rows, loss_out=self.loss_out,
+                            row_stats=self.stats, status=self.status, stream=stream)
+
+    def bwd(self, stream):
+        self.vce.ce_backward(self.logits, self.labels, self.stats, self.go, grad_logits=self.grad, stream=stream)
+
+    def step(self, stream):
+        self.fwd(stream)
+        self.bwd(stream)
+
+    def e2e_step(self, stream):
+        self.logits.copy_(self.host_bf16, non_blocking=True)
+        self.labels.copy_(self.labels_host, non_blocking=True)
+        self.step(stream)
+        self.loss_host.copy_(self.loss_out, non_blocking=True)
+
+    @property
+    def h2d_bytes(self):
+        return self.p.T * self.p.V * 2 + self.p.T * 8
+
+    d2h_bytes = 4
+
+    def tokens(self):
+        return self.p.T
+
+    def bytes_fwd(self):
+        T, V = self.p.T, self.p.V
+        return self.n_valid * V * 2 + T * (8 + 4 + 16)
+
+    def bytes_bwd(self):
+        T, V = self.p.T, self.p.V
+        return self.n_valid * V * 2 + T * V * 2 + T * (8 + 16)
+
+    def describe(self):
+        p = self.p
+        return {"workload": f"{p.name}: CE fwd+bwd, T={p.T} rows x V={p.V} bf16 logits, mean over non-ignored "
+                            f"rows, {len(p.margin_rows)} raised-target rows, {len(p.ignore_rows)} ignored",
+                "T": p.T, "V": p.V, "logits": "bf16", "grad": "bf16", "math": "f32",
+                "l2": "no flush: inputs (%.2f GB logits) larger than the 129 MB L2" % (p.T * p.V * 2 / 1e9)}
+
+
+# ------------------------------------------------------------------------------- timing
+
+def time_steps(fn, steps, stream, world, device, per_launch=None):
+    """Time `steps` calls of fn(stream) with CUDA events on `stream`; max over ranks."""
+    barrier(world)
+    torch.cuda.synchronize(device)
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(steps):
+        fn(stream)
+    end.record(stream)
+    end.synchronize()
+    torch.cuda.synchronize(device)
+    barrier(world)
+    ms = start.elapsed_time(end)
+    return max_over_ranks(ms, world, device)
+
+
+def time_kernel(workload, steps, stream):
+    """Average duration of the forward and backward launches, events on the launching stream."""
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+            torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    torch.cuda.synchronize()
+    for a, b, c in evs:
+        a.record(stream)
+        workload.fwd(stream)
+        b.record(stream)
+        workload.bwd(stream)
+        c.record(stream)
+    torch.cuda.synchronize()
+    f = [a.elapsed_time(b) for a, b, _ in evs]
+    g = [b.elapsed_time(c) for _, b, c in evs]
+    return statistics.mean(f), statistics.mean(g)
+
+
+def cpu_oracle_baseline(problem, budget_s=12.0, max_rows=4096):
+    """The fp64 oracle as it stands, on a row sample of the same workload (host cores)."""
+    from oracle import ce_oracle as O
+    N = int(np.sum(problem.labels != problem.ignore_index))
+    rng = np.random.default_rng(123)
+    order = rng.permutation(problem.T)
+    done = 0
+    t0 = time.perf_counter()
+    block = 64
+    while done < max_rows and time.perf_counter() - t0 < budget_s:
+        rows = np.sort(order[done: done + block])
+        z = O.widen(problem.rows(rows), problem.dtype)
+        fwd = O.ce_rows(z, problem.labels[rows])
+        O.ce_grad_rows(z, problem.labels[rows], fwd, O.row_scale(fwd["valid"], "sum", 1.0 / N))
+        done += len(rows)
+    dt = time.perf_counter() - t0
+    return {"value": done / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{done} random rows of the same T={problem.T}, V={problem.V} matrix (input generation "
+                      f"included), fp64 numpy forward+backward, single thread, {dt:.1f} s"}
+
+
+# ------------------------------------------------------------------------------- main
+
+def run_ours(args, rank, local_rank, world):
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    init_dist(world, "nccl")
+    problem = {"pages": gen.pages, "mid": gen.mid}[args.workload](seed=1003 + rank if args.workload == "pages"
+                                                                  else 1002 + rank)
+    w = CEWorkload(problem, device)
+    stream = torch.cuda.current_stream(device)
+    for _ in range(args.warmup):
+        w.step(stream)
+    torch.cuda.synchronize(device)
+    with ClockSampler(local_rank) as clk:
+        ms = time_steps(w.step, args.steps, stream, world, device)
+    clocks = clk.summary()
+    fwd_ms, bwd_ms = time_kernel(w, max(10, min(args.steps, 50)), stream)
+    e2e_steps = max(3, min(args.e2e_steps, args.steps))
+    for _ in range(2):
+        w.e2e_step(stream)
+    e2e_ms = time_steps(w.e2e_step, e2e_steps, stream, world, device)
+    status = w.vce.vce_get_status(w.status)
+    if status != 0:
+        raise RuntimeError(f"device status {status}")
+
+    tokens_all = sum_over_ranks(w.tokens(), world, device)
+    ms_step = ms / args.steps
+    value = tokens_all / (ms_step / 1e3)
+    e2e_value = tokens_all / (e2e_ms / e2e_steps / 1e3)
+    peaks = measured_peaks()
+    bwd_bytes = w.bytes_bwd()
+    achieved = bwd_bytes / (bwd_ms / 1e3) / 1e9
+    traffic = profiled_traffic(f"k_ce_bwd_{args.workload}", CEWorkload.KERNEL_FILES)
+    out = {
+        "metric": "CE fwd+bwd tokens/s at T=16384,V=128256 bf16; HBM GB/s vs ~8 TB/s",
+        "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": dict(w.describe(), parallelism=f"replicas{world}"),
+        "hbm_gbs_step": round((w.bytes_fwd() + bwd_bytes) * world / (ms_step / 1e3) / 1e9, 1),
+        "kernels_ms": {"ce_forward": round(fwd_ms, 5), "ce_backward": round(bwd_ms, 5)},
+        "roofline": {"bound": "hbm", "kernel": "k_ce_bwd", "achieved": round(achieved, 1),
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                     "peak_source": peaks["source"], "algorithmic_bytes_per_launch": bwd_bytes,
+                     "traffic": traffic},
+        "roofline_fwd": {"bound": "hbm", "kernel": "k_ce_fwd",
+                         "achieved": round(w.bytes_fwd() / (fwd_ms / 1e3) / 1e9, 1), "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": round(w.bytes_fwd() / (fwd_ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4)},
+        "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": w.h2d_bytes,
+                "d2h_bytes_per_step": w.d2h_bytes, "steps": e2e_steps},
+        "gpu_launches": w.launches_per_step * args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_oracle_baseline(problem)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
+def run_reference(args, rank, world):
+    """The oracle (fp64, CPU) as the reference arm: rank 0 alone, bounded samples per step."""
+    if rank != 0:
+        return
+    problem = {"pages": gen.pages, "mid": gen.mid}[args.workload]()
+    from oracle import ce_oracle as O
+    N = int(np.sum(problem.labels != problem.ignore_index))
+    rows_per_step = 64
+    rng = np.random.default_rng(7)
+
+    def one_step():
+        rows = np.sort(rng.choice(problem.T, rows_per_step, replace=False))
+        z = O.widen(problem.rows(rows), problem.dtype)
+        fwd = O.ce_rows(z, problem.labels[rows])
+        O.ce_grad_rows(z, problem.labels[rows], fwd, O.row_scale(fwd["valid"], "sum", 1.0 / N))
+
+    for _ in range(args.warmup):
+        one_step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        one_step()
+    dt = time.perf_counter() - t0
+    value = rows_per_step * args.steps / dt
+    out = {
+        "impl": "reference", "metric": "CE fwd+bwd tokens/s at T=16384,V=128256 bf16; HBM GB/s vs ~8 TB/s",
+        "value": round(value, 2), "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{problem.name}: CE fwd+bwd T={problem.T} V={problem.V} bf16 logits, "
+                               f"{rows_per_step} sampled rows per step", "T": problem.T, "V": problem.V},
+        "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{rows_per_step} random rows per step of the same matrix, fp64 numpy"},
+        "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=["pages", "mid"], default="pages")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank, local_rank, world = dist_env()
+    if world != args.gpus and world > 1:
+        print(f"warning: WORLD_SIZE={world} but --gpus {args.gpus}", file=sys.stderr)
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, local_rank, world)
+
+
+if __name__ == "__main__":
+    main()

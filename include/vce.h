@@ -1,0 +1,177 @@
+/*
+ * vce.h -- C ABI of the GB300 vocabulary cross-entropy library (libvce.so).
+ *
+ * Softmax cross-entropy over a [T, V] logits matrix that stays accurate at large
+ * target margins, its gradient, the merge of vocabulary-chunked statistics, and a
+ * fused linear cross-entropy (declared in vce_linear.h), as hand-written sm_103a
+ * CUDA kernels.
+ *
+ * Sources of the operations (the web pages this library restates):
+ *   [TT]  torchtitan PR #5723, "[loss] fix softmax collapse with improved ce perf":
+ *         Numerics (target-excluded log-sum-exp and softplus NLL; the p_t = 1/4
+ *         branch of the target gradient; ignored labels), Memory/perf (the
+ *         compiled form: column mask, one read of the logits in forward, per-row
+ *         statistics saved, the gradient rebuilt in one fused backward pass;
+ *         bf16 input upcast inside the op).
+ *   [MC]  Megatron-core API docs, core.tensor_parallel.cross_entropy:
+ *         vocab_parallel_cross_entropy(vocab_parallel_logits, target,
+ *         label_smoothing, tp_group) and the VocabParallelCrossEntropy helpers
+ *         (calculate_logits_max, gather_predicted_logits: target mask, local
+ *         target ids, predicted logit zero for targets owned elsewhere).
+ *   [CCE] apple/ml-cross-entropy issue #14: linear_cross_entropy(e, c, targets)
+ *         (classifier weight only, no bias), impl="cce_exact" (no gradient
+ *         filtering) and use_kahan (compensated accumulation of dc and de).
+ *
+ * Conventions common to every call:
+ *   - Every pointer is a DEVICE pointer owned by the caller unless stated "host".
+ *     The library allocates and frees nothing; scratch space is an explicit
+ *     caller-provided workspace where a call needs one.
+ *   - Every call only enqueues work on the caller's stream `s` and returns; it
+ *     never synchronises.  Inputs must stay valid until that work has run.
+ *   - Logits are read only (const): the input is never written [TT, Memory/perf].
+ *   - Matrices are row-major with a leading dimension `ld` (elements between the
+ *     starts of consecutive rows, ld >= number of columns).  Rows need not be
+ *     16-byte aligned; 16-byte aligned rows take the vectorised path.
+ *   - Labels are int64.  A label equal to ignore_index marks an ignored row: its
+ *     loss and gradient are exactly +0.0, whatever its logits hold (even +-inf).
+ *     Any other label outside [0, V) is an error: the device writes VCE_ERR_LABEL
+ *     into *status, that row's loss becomes NaN (and so does a reduced loss), its
+ *     gradient is 0.  No call traps or asserts on the device.
+ *   - Per-row losses and reduced losses are fp32 whatever the logits dtype.
+ *   - Return value: VCE_OK, or a negative host-detected error (nothing was
+ *     enqueued in that case).  Device-detected errors go to *status; read it after
+ *     the stream has run (vce_get_status does that).
+ */
+#ifndef VCE_H
+#define VCE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* vce_stream_t; /* the same handle as cudaStream_t; NULL = legacy stream */
+
+#define VCE_ABI_VERSION 1
+#define VCE_ROW_STATS 4     /* floats per row of row_stats */
+#define VCE_CHUNK_STATS 4   /* floats per (chunk, row) of chunk statistics */
+#define VCE_MAX_CHUNKS 64   /* most column chunks ce_merge_chunks accepts */
+
+typedef enum { VCE_F32 = 0, VCE_BF16 = 1 } vce_dtype;
+typedef enum { VCE_RED_NONE = 0, VCE_RED_SUM = 1, VCE_RED_MEAN = 2 } vce_reduction;
+
+enum {
+    VCE_OK = 0,
+    VCE_ERR_LABEL = 1,        /* device-detected: a label neither ignore_index nor in [0, V) */
+    VCE_ERR_NULL = -1,        /* a required pointer is NULL */
+    VCE_ERR_DTYPE = -2,       /* unknown or unsupported dtype / reduction */
+    VCE_ERR_SHAPE = -3,       /* a size is negative, zero where it must not be, or overflows */
+    VCE_ERR_LD = -4,          /* a leading dimension is smaller than the row length */
+    VCE_ERR_ALIGN = -5,       /* a pointer is not aligned to its element size (16 B for stats) */
+    VCE_ERR_WORKSPACE = -6,   /* workspace missing or smaller than required */
+    VCE_ERR_CUDA = -7,        /* a CUDA runtime call failed (launch, memset, attribute query) */
+    VCE_ERR_ARG = -8,         /* any other invalid argument (chunk count, chunk layout) */
+    VCE_ERR_DEVICE = -9       /* the current device is not an sm_100-family GPU */
+};
+
+/* Library ABI version (VCE_ABI_VERSION of the build). */
+int vce_abi_version(void);
+
+/* Static text for a status code; never NULL. */
+const char* vce_status_string(int status);
+
+/* Floats per row of the row_stats buffer (= VCE_ROW_STATS). */
+size_t vce_row_stats_floats(void);
+
+/*
+ * Waits for stream `s`, then copies the device status word to *host_out.
+ * Returns VCE_OK or VCE_ERR_CUDA / VCE_ERR_NULL.
+ */
+int vce_get_status(const int32_t* status, vce_stream_t s, int32_t* host_out);
+
+/*
+ * ce_forward -- per-row NLL and the statistics its gradient needs.  [TT, Numerics;
+ * Memory/perf, compiled forward]  For row i with label t:
+ *     L'_i = log sum_{j != t} exp(z_ij)          (target left out by a column test)
+ *     x_i  = L'_i - z_it
+ *     loss_rows[i] = softplus(x_i) = -log softmax(z_i)_t
+ * in one read of the row (running max and rescaled sum-exp), fp32 arithmetic on
+ * bf16 or fp32 input.  Reduction SUM writes sum_i loss_i to *loss_out; MEAN writes
+ * that sum divided by N, the number of non-ignored rows (NaN when N = 0), summed
+ * in a fixed order (bitwise reproducible); NONE leaves loss_out untouched (may be NULL).
+ *
+ *   logits     [T, ld] of dtype `dt` (VCE_F32 or VCE_BF16), element-aligned
+ *   T, V, ld   rows, vocabulary size (>= 1), leading dimension (>= V); T may be 0
+ *   labels     [T] int64;  ignore_index: label value of ignored rows (e.g. -100)
+ *   loss_rows  [T] fp32, written
+ *   loss_out   [1] fp32, written for SUM / MEAN
+ *   row_stats  [T * VCE_ROW_STATS] fp32, 16-byte aligned, written; per row
+ *              (L', sigmoid(x) = 1 - p_t, target-gradient coefficient, row weight).
+ *              The target coefficient is p_t - 1 when p_t < 1/4 (x > ln 3), else
+ *              -(1 - p_t) [TT, Numerics].  The row weight is 1/N (MEAN), 1 (SUM,
+ *              NONE) or 0 (ignored / invalid row).  Consumed by ce_backward.
+ *   status     [1] int32, set to 0 by this call, VCE_ERR_LABEL on a bad label
+ */
+int ce_forward(const void* logits, vce_dtype dt, int64_t T, int64_t V, int64_t ld,
+               const int64_t* labels, int64_t ignore_index, vce_reduction red,
+               float* loss_rows, float* loss_out, float* row_stats, int32_t* status,
+               vce_stream_t s);
+
+/*
+ * ce_backward -- gradient of the reduced loss w.r.t. the logits, rebuilt in one
+ * pass from the logits and row_stats.  [TT, Numerics; Memory/perf, compiled backward]
+ *     grad_ij = c_i * exp(z_ij - L'_i) * sigmoid(x_i)          (j != t)
+ *     grad_it = c_i * (p_t - 1) if p_t < 1/4, else -c_i * (1 - p_t)
+ * with c_i = grad_output[0] * weight_i (SUM, MEAN) or grad_output[i] * weight_i
+ * (NONE).  Ignored rows are written as +0.0.  fp32 math, bf16 output rounded to
+ * nearest even.
+ *
+ *   logits, dt, T, V, ld, labels, ignore_index, red: as given to ce_forward
+ *   row_stats    [T * VCE_ROW_STATS] from ce_forward (or ce_merge_chunks)
+ *   grad_output  fp32 [1] (SUM, MEAN) or [T] (NONE)
+ *   grad_logits  [T, ld_grad] of dtype grad_dt (VCE_F32 or VCE_BF16), written;
+ *                it must not overlap the logits
+ */
+int ce_backward(const void* logits, vce_dtype dt, int64_t T, int64_t V, int64_t ld,
+                const int64_t* labels, int64_t ignore_index, vce_reduction red,
+                const float* row_stats, const float* grad_output,
+                void* grad_logits, vce_dtype grad_dt, int64_t ld_grad, vce_stream_t s);
+
+/*
+ * ce_merge_chunks -- CE forward (+ backward) over logits held as k column chunks
+ * in separate buffers, the single-GPU form of the vocabulary-parallel CE [MC,
+ * vocab_parallel_cross_entropy; TT, Numerics: the owner of the target drops it].
+ * Chunk c covers global columns [off_c, off_c + width[c]), off_c = sum of the
+ * earlier widths, V = sum of all widths.  Three device steps:
+ *   1. per chunk and row, over the chunk's non-target columns: the max m_c, the
+ *      sum s_c of exp(z - m_c), and the target logit if the chunk owns the target
+ *      (off_c <= t < off_c + width[c]); written to chunk_stats_ws as
+ *      [k][T][VCE_CHUNK_STATS] = (m_c, s_c, z_t or 0, owner 1.0/0.0);
+ *   2. per row: M = max_c m_c, S = sum_c s_c exp(m_c - M) (chunks with m_c = -inf
+ *      skipped), then loss, row_stats and the reduction exactly as ce_forward;
+ *   3. if chunk_grads != NULL: every chunk's gradient as ce_backward, with c_i from
+ *      grad_output, read on the device when step 3 runs.
+ *
+ *   k                        1 .. VCE_MAX_CHUNKS
+ *   chunk_logits             host array [k] of device pointers [T, chunk_ld[c]]
+ *   chunk_width, chunk_ld    host arrays [k]: columns (>= 1) and leading dimensions
+ *   chunk_grads              host array [k] of device pointers, or NULL (forward only)
+ *   chunk_grad_ld            host array [k], or NULL for chunk_grad_ld = chunk_width
+ *   chunk_stats_ws           [k * T * VCE_CHUNK_STATS] fp32, 16-byte aligned, scratch
+ *   other arguments          as ce_forward / ce_backward
+ */
+int ce_merge_chunks(int k, const void* const* chunk_logits, const int64_t* chunk_width,
+                    const int64_t* chunk_ld, vce_dtype dt, int64_t T,
+                    const int64_t* labels, int64_t ignore_index, vce_reduction red,
+                    float* loss_rows, float* loss_out, float* row_stats,
+                    const float* grad_output, void* const* chunk_grads,
+                    const int64_t* chunk_grad_ld, vce_dtype grad_dt,
+                    float* chunk_stats_ws, int32_t* status, vce_stream_t s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VCE_H */

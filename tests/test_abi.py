@@ -1,0 +1,63 @@
+"""The C-ABI library: it builds, loads without a GPU and exports every symbol its headers declare."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        src = open(h).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        for m in re.finditer(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b([a-z_][a-z0-9_]*)\s*\(", src, flags=re.M):
+            if not m.group(0).lstrip().startswith(("typedef", "#", "return")):
+                names.add(m.group(1))
+    return names
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from vocab_cross_entropy_gb300 import build
+    path = build.build()
+    return ctypes.CDLL(path)
+
+
+def test_headers_declare_the_boundary():
+    names = declared_functions()
+    for n in ("ce_forward", "ce_backward", "ce_merge_chunks", "vce_get_status", "vce_status_string"):
+        assert n in names, n
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [n for n in sorted(declared_functions()) if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_host_only_calls(lib):
+    lib.vce_status_string.restype = ctypes.c_char_p
+    assert lib.vce_abi_version() == 1
+    assert lib.vce_row_stats_floats() == 4
+    assert b"label" in lib.vce_status_string(1)
+    assert lib.vce_status_string(12345) == b"unknown status"
+
+
+def test_argument_errors_need_no_gpu(lib):
+    # checks that fail before any CUDA call: bad dtype, bad reduction, null status, ld < V
+    P = ctypes.c_void_p
+    i64 = ctypes.c_int64
+    f = lib.ce_forward
+    f.argtypes = [P, ctypes.c_int, i64, i64, i64, P, i64, ctypes.c_int, P, P, P, P, P]
+    x = P(0x1000)
+    assert f(x, 7, 4, 8, 8, x, -100, 2, x, x, x, x, None) == -2
+    assert f(x, 1, 4, 8, 8, x, -100, 5, x, x, x, x, None) == -2
+    assert f(x, 1, 4, 8, 8, x, -100, 2, x, x, x, None, None) == -1
+    assert f(x, 1, 4, 8, 7, x, -100, 2, x, x, x, x, None) == -4
+    assert f(x, 1, 4, 0, 8, x, -100, 2, x, x, x, x, None) == -3
+    m = lib.ce_merge_chunks
+    assert m(0, None, None, None, 1, 4, None, -100, 2, None, None, None, None, None, None, 1, None, None,
+             None) == -8

@@ -1,0 +1,289 @@
+"""Parity of the CUDA CE forward/backward (through the C ABI) with the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import gen
+from oracle import ce_oracle as O
+from tests import _grading as G
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def vce():
+    if not torch.cuda.is_available():
+        pytest.fail("GPU tests need CUDA")
+    import vocab_cross_entropy_gb300 as v
+    return v
+
+
+TORCH_DT = {"f32": torch.float32, "bf16": torch.bfloat16}
+
+
+def to_device(storage, dtype):
+    t = torch.from_numpy(np.ascontiguousarray(storage))
+    if dtype == "bf16":
+        t = t.view(torch.int16).view(torch.bfloat16)
+    return t.cuda()
+
+
+def host_values(t):
+    if t.dtype == torch.bfloat16:
+        return O.widen(G.bf16_tensor_bits(t), "bf16")
+    return t.detach().cpu().numpy().astype(np.float64)
+
+
+def grade_grad(grad_t, want, rows_raised_target=None, labels=None, what="grad"):
+    if grad_t.dtype == torch.bfloat16:
+        G.check_grad_bf16(G.bf16_tensor_bits(grad_t), want, what)
+    else:
+        got = grad_t.cpu().numpy().astype(np.float64)
+        G.check_grad_f32(got, want, what)
+        if rows_raised_target is not None and len(rows_raised_target):
+            r = rows_raised_target
+            G.check_target_entries(got[r, labels[r]], want[r, labels[r]], what + " (raised targets)")
+
+
+def run_ce(vce, logits, labels_np, reduction="mean", grad_output=1.0, grad_dtype=None, ignore_index=-100):
+    labels = torch.from_numpy(labels_np).cuda()
+    loss_out, loss_rows, stats, status = vce.ce_forward(logits, labels, ignore_index, reduction)
+    T = logits.shape[0]
+    go = torch.full((T,) if reduction == "none" else (1,), 0.0, dtype=torch.float32, device="cuda")
+    go[:] = torch.as_tensor(grad_output, dtype=torch.float32)
+    grad = vce.ce_backward(logits, labels, stats, go, ignore_index, reduction, grad_dtype=grad_dtype)
+    torch.cuda.synchronize()
+    return loss_out, loss_rows, stats, status, grad
+
+
+def full_check(vce, p, reduction="mean", grad_output=1.0, grad_dtype=None, block=512):
+    """Whole-matrix parity for a problem the oracle finishes in seconds."""
+    storage = p.full()
+    logits = to_device(storage, p.dtype)
+    before = logits.clone()
+    loss_out, loss_rows, stats, status, grad = run_ce(vce, logits, p.labels, reduction, grad_output, grad_dtype)
+    assert vce.vce_get_status(status) == 0
+    assert torch.equal(logits, before)   # the input is never written
+    z = O.widen(storage, p.dtype)
+    ref = O.ce(z, p.labels, reduction, grad_output)
+    G.check_loss_rows(loss_rows.cpu().numpy(), ref["loss_rows"], ref["valid"])
+    if reduction != "none":
+        G.check_reduced(loss_out.item(), ref["loss_out"])
+    grade_grad(grad, ref["grad"], p.margin_rows, p.labels)
+    st = stats.cpu().numpy().astype(np.float64)
+    v = ref["valid"]
+    fin = v & np.isfinite(ref["lse_nt"])
+    assert np.all(np.abs(st[fin, 0] - ref["lse_nt"][fin]) <= 1e-5 * np.maximum(1, np.abs(ref["lse_nt"][fin])))
+    assert np.all(st[~v] == 0)
+    return grad, stats
+
+
+def test_tiny_config_full(vce):
+    full_check(vce, gen.tiny())
+
+
+def test_mid_config_full(vce):
+    p = gen.mid()
+    storage = p.full()
+    logits = to_device(storage, "bf16")
+    loss_out, loss_rows, stats, status, grad = run_ce(vce, logits, p.labels)
+    assert vce.vce_get_status(status) == 0
+    lr = loss_rows.cpu().numpy()
+    gbits = G.bf16_tensor_bits(grad)
+    losses = []
+    for r0 in range(0, p.T, 512):
+        z = O.widen(storage[r0:r0 + 512], "bf16")
+        fwd = O.ce_rows(z, p.labels[r0:r0 + 512])
+        c = O.row_scale(fwd["valid"], "sum", 1.0 / (p.T - p.n_ignore))
+        want = O.ce_grad_rows(z, p.labels[r0:r0 + 512], fwd, c)
+        G.check_loss_rows(lr[r0:r0 + 512], fwd["loss"], fwd["valid"])
+        G.check_grad_bf16(gbits[r0:r0 + 512], want, f"grad rows {r0}+")
+        losses.append(fwd["loss"])
+    valid = p.labels != p.ignore_index
+    G.check_reduced(loss_out.item(), np.concatenate(losses)[valid].sum() / valid.sum())
+
+
+@pytest.mark.parametrize("reduction", ["sum", "none"])
+@pytest.mark.parametrize("dtype,gdt", [("bf16", torch.float32), ("f32", torch.bfloat16), ("f32", None)])
+def test_reductions_and_grad_dtypes(vce, reduction, dtype, gdt):
+    p = gen.custom(96, 3000, dtype, seed=41, std=2.5, n_margin=12, margin=(17.0, 50.0), n_ignore=6)
+    go = np.linspace(0.25, 2.0, 96) if reduction == "none" else 0.75
+    full_check(vce, p, reduction, go, gdt)
+
+
+@pytest.mark.parametrize("V", [1, 2, 3, 7, 9, 1001, 4097, 33333])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_odd_vocab_sizes(vce, V, dtype):
+    p = gen.custom(19, V, dtype, seed=V, std=2.0, n_margin=3 if V > 1 else 0, n_ignore=2)
+    full_check(vce, p)
+
+
+def test_single_row(vce):
+    full_check(vce, gen.custom(1, 5000, "bf16", seed=2, n_margin=1))
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_padded_ld_and_unaligned_rows(vce, dtype):
+    """A view with ld > V whose rows start off the 16-byte grid (head/tail path and scalar path)."""
+    p = gen.custom(33, 1000, dtype, seed=17, n_margin=4, n_ignore=3)
+    storage = p.full()
+    big = np.zeros((33, 1013), storage.dtype)
+    big[:, 3:1003] = storage
+    base = to_device(big, dtype)
+    logits = base[:, 3:1003]
+    labels = torch.from_numpy(p.labels).cuda()
+    loss_out, loss_rows, stats, status = vce.ce_forward(logits, labels)
+    go = torch.ones(1, device="cuda")
+    gbase = torch.full((33, 1011), 7.0, dtype=TORCH_DT[dtype], device="cuda")
+    grad = vce.ce_backward(logits, labels, stats, go, grad_logits=gbase[:, 1:1001])
+    torch.cuda.synchronize()
+    ref = O.ce(O.widen(storage, dtype), p.labels, "mean")
+    G.check_loss_rows(loss_rows.cpu().numpy(), ref["loss_rows"], ref["valid"])
+    grade_grad(gbase[:, 1:1001], ref["grad"], p.margin_rows, p.labels)
+    assert torch.all(gbase[:, :1] == 7) and torch.all(gbase[:, 1001:] == 7)   # nothing written outside
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_output_phase_differs_from_input(vce, dtype):
+    p = gen.custom(17, 999, dtype, seed=18, n_margin=3, n_ignore=2)
+    storage = p.full()
+    logits = to_device(storage, dtype)
+    labels = torch.from_numpy(p.labels).cuda()
+    _, loss_rows, stats, status = vce.ce_forward(logits, labels)
+    gbase = torch.full((17, 1003), 3.0, dtype=TORCH_DT[dtype], device="cuda")
+    gview = gbase[:, 1:1000]
+    vce.ce_backward(logits, labels, stats, torch.ones(1, device="cuda"), grad_logits=gview)
+    torch.cuda.synchronize()
+    ref = O.ce(O.widen(storage, dtype), p.labels, "mean")
+    grade_grad(gview, ref["grad"], p.margin_rows, p.labels)
+    assert torch.all(gbase[:, 0] == 3) and torch.all(gbase[:, 1000:] == 3)
+
+
+def test_non_finite_rows(vce):
+    z = np.array([
+        [np.inf, -np.inf, 3.0, 1.0],      # ignored row holding +-inf: exactly zero
+        [-np.inf, -np.inf, -np.inf, -np.inf],   # ignored
+        [-np.inf, 2.0, -np.inf, -np.inf],  # every non-target -inf: loss 0, gradient 0
+        [0.0, -np.inf, np.log(3.0), -np.inf],   # -inf target: loss +inf
+        [1.0, -np.inf, 2.0, 0.5],
+    ], np.float32)
+    labels = np.array([-100, -100, 1, 1, 2])
+    for dtype in ("f32", "bf16"):
+        storage = z if dtype == "f32" else (z.view(np.uint32) >> 16).astype(np.uint16)
+        logits = to_device(storage, dtype)
+        loss_out, loss_rows, stats, status, grad = run_ce(vce, logits, labels, "sum")
+        ref = O.ce(O.widen(storage, dtype), labels, "sum")
+        lr = loss_rows.cpu().numpy()
+        assert lr[0] == 0 and lr[1] == 0 and lr[2] == 0 and lr[3] == np.inf
+        assert abs(lr[4] - ref["loss_rows"][4]) <= 1e-4 * ref["loss_rows"][4]
+        g = host_values(grad)
+        assert np.all(g[:3] == 0)
+        np.testing.assert_allclose(g[3:], ref["grad"][3:], rtol=1e-2 if dtype == "bf16" else 1e-5, atol=1e-7)
+
+
+def test_all_rows_ignored(vce):
+    p = gen.custom(8, 100, "bf16", seed=3)
+    labels = np.full(8, -100)
+    logits = to_device(p.full(), "bf16")
+    loss_out, loss_rows, stats, status, grad = run_ce(vce, logits, labels, "mean")
+    assert np.isnan(loss_out.item())
+    assert torch.all(loss_rows == 0) and torch.all(grad == 0)
+
+
+def test_invalid_label_sets_status(vce):
+    p = gen.custom(8, 100, "f32", seed=4)
+    labels = p.labels.copy()
+    labels[3] = 100
+    labels[5] = -7
+    logits = to_device(p.full(), "f32")
+    loss_out, loss_rows, stats, status, grad = run_ce(vce, logits, labels, "mean")
+    assert vce.vce_get_status(status) == 1
+    lr = loss_rows.cpu().numpy()
+    assert np.isnan(lr[3]) and np.isnan(lr[5]) and np.isnan(loss_out.item())
+    assert torch.all(grad[3] == 0) and torch.all(grad[5] == 0)
+    # a clean call resets the status word
+    _, _, _, status2, _ = run_ce(vce, logits, p.labels, "mean")
+    assert vce.vce_get_status(status2) == 0
+
+
+def test_host_argument_errors(vce):
+    import ctypes
+    lib = vce.lib
+    x = torch.zeros(4, 8, device="cuda")
+    lab = torch.zeros(4, dtype=torch.int64, device="cuda")
+    out = torch.zeros(4, device="cuda")
+    st = torch.zeros(4, 4, device="cuda")
+    s = torch.zeros(1, dtype=torch.int32, device="cuda")
+    P = ctypes.c_void_p
+    args = lambda **kw: [P(kw.get("x", x.data_ptr())), kw.get("dt", 0), kw.get("T", 4), kw.get("V", 8),
+                         kw.get("ld", 8), P(lab.data_ptr()), -100, kw.get("red", 2), P(out.data_ptr()),
+                         P(out.data_ptr()), P(kw.get("st", st.data_ptr())), P(s.data_ptr()), None]
+    assert lib.ce_forward(*args()) == 0
+    assert lib.ce_forward(*args(dt=5)) == -2
+    assert lib.ce_forward(*args(red=9)) == -2
+    assert lib.ce_forward(*args(V=0)) == -3
+    assert lib.ce_forward(*args(ld=7)) == -4
+    assert lib.ce_forward(*args(x=x.data_ptr() + 2)) == -5
+    assert lib.ce_forward(*args(st=st.data_ptr() + 4)) == -5
+    assert lib.ce_forward(*args(T=1 << 62, ld=1 << 3)) == -3
+    torch.cuda.synchronize()
+
+
+def test_repeatable_bitwise(vce):
+    p = gen.custom(64, 20000, "bf16", seed=8, n_margin=6, n_ignore=3)
+    logits = to_device(p.full(), "bf16")
+    a = run_ce(vce, logits, p.labels)
+    b = run_ce(vce, logits, p.labels)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1]) and torch.equal(a[4], b[4])
+
+
+def test_autograd_wrapper(vce):
+    p = gen.custom(32, 700, "bf16", seed=9, n_margin=4, n_ignore=2)
+    storage = p.full()
+    logits = to_device(storage, "bf16").requires_grad_(True)
+    loss = vce.cross_entropy(logits, torch.from_numpy(p.labels).cuda())
+    (2.0 * loss).backward()
+    ref = O.ce(O.widen(storage, "bf16"), p.labels, "mean", grad_output=2.0)
+    G.check_reduced(loss.item(), ref["loss_out"])
+    G.check_grad_bf16(G.bf16_tensor_bits(logits.grad), ref["grad"])
+
+
+# ------------------------------------------------------------------ the pages' shape, as the bench runs it
+
+@pytest.fixture(scope="module")
+def pages_data():
+    p = gen.pages()
+    storage = p.full()
+    return p, storage
+
+
+def test_pages_shape_sampled(vce, pages_data):
+    p, storage = pages_data
+    logits = to_device(storage, "bf16")
+    labels = torch.from_numpy(p.labels).cuda()
+    loss_out, loss_rows, stats, status = vce.ce_forward(logits, labels)
+    grad = vce.ce_backward(logits, labels, stats, torch.ones(1, device="cuda"))
+    torch.cuda.synchronize()
+    assert vce.vce_get_status(status) == 0
+    rng = np.random.default_rng(0)
+    valid = p.labels != p.ignore_index
+    N = int(valid.sum())
+    rows = np.unique(np.concatenate([p.margin_rows, rng.choice(p.T, 256, replace=False), [0, p.T - 1]]))
+    lr = loss_rows.cpu().numpy()
+    idx = torch.from_numpy(rows).cuda()
+    gbits = G.bf16_tensor_bits(grad.index_select(0, idx))
+    for k in range(0, len(rows), 256):
+        rr = rows[k:k + 256]
+        z = O.widen(storage[rr], "bf16")
+        fwd = O.ce_rows(z, p.labels[rr])
+        want = O.ce_grad_rows(z, p.labels[rr], fwd, O.row_scale(fwd["valid"], "sum", 1.0 / N))
+        G.check_loss_rows(lr[rr], fwd["loss"], fwd["valid"], "pages loss")
+        G.check_grad_bf16(gbits[k:k + 256], want, "pages grad")
+    # ignored rows: exactly zero gradient; reduction consistent with the per-row losses
+    ig = torch.from_numpy(p.ignore_rows).cuda()
+    assert torch.all(grad.index_select(0, ig) == 0) and np.all(lr[p.ignore_rows] == 0)
+    G.check_reduced(loss_out.item(), float(np.sum(lr[valid].astype(np.float64)) / N))
+    # collapse regime: every raised-target row has a positive loss and a negative target gradient
+    assert np.all(lr[p.margin_rows] > 0)
+    tg = grad[torch.from_numpy(p.margin_rows).cuda(), torch.from_numpy(p.labels[p.margin_rows]).cuda()]
+    assert torch.all(tg < 0)

@@ -1,0 +1,225 @@
+"""Python binding of libvce.so, the GB300 vocabulary cross-entropy library.
+
+Argument marshalling only: every step of the computation runs in the library's CUDA
+kernels.  Tensors are torch CUDA tensors (torch supplies device memory and streams);
+each function passes raw pointers to the C entry point of the same name in
+``include/vce.h`` and raises ``VceError`` on a non-zero return.  There is no CPU
+fallback: importing works without a GPU, calling a compute entry point needs one.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = ["VceError", "lib", "library_path", "ce_forward", "ce_backward", "ce_merge_chunks",
+           "linear_ce_workspace_bytes", "linear_ce_fwd_bwd", "vce_get_status", "vce_status_string",
+           "vce_abi_version", "cross_entropy", "IGNORE_INDEX", "F32", "BF16", "RED"]
+
+IGNORE_INDEX = -100
+F32, BF16 = 0, 1
+RED = {"none": 0, "sum": 1, "mean": 2}
+ROW_STATS = 4
+CHUNK_STATS = 4
+_DT = {torch.float32: F32, torch.bfloat16: BF16}
+
+library_path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libvce.so")
+
+
+class VceError(RuntimeError):
+    def __init__(self, fn, code):
+        self.code = code
+        super().__init__(f"{fn} failed: {code} ({vce_status_string(code)})")
+
+
+def _load():
+    if not os.path.exists(library_path):
+        raise ImportError(f"{library_path} is not built: run `python -m vocab_cross_entropy_gb300.build` "
+                          "(or __graft_entry__.build()) first; this library has no fallback path")
+    L = ctypes.CDLL(library_path)
+    p, i64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+    L.vce_abi_version.restype = i32
+    L.vce_status_string.argtypes = [i32]
+    L.vce_status_string.restype = ctypes.c_char_p
+    L.vce_row_stats_floats.restype = sz
+    L.vce_get_status.argtypes = [p, p, p]
+    L.ce_forward.argtypes = [p, i32, i64, i64, i64, p, i64, i32, p, p, p, p, p]
+    L.ce_backward.argtypes = [p, i32, i64, i64, i64, p, i64, i32, p, p, p, i32, i64, p]
+    L.ce_merge_chunks.argtypes = [i32, p, p, p, i32, i64, p, i64, i32, p, p, p, p, p, p, i32, p, p, p]
+    if hasattr(L, "linear_ce_fwd_bwd"):
+        L.linear_ce_workspace_bytes.argtypes = [i64, i64, i64]
+        L.linear_ce_workspace_bytes.restype = sz
+        L.linear_ce_fwd_bwd.argtypes = [p, p, i64, i64, i64, p, i64, i32, p, p, p, p, p, i32, p, sz, p, p]
+    for name in ("ce_forward", "ce_backward", "ce_merge_chunks", "linear_ce_fwd_bwd", "vce_get_status"):
+        if hasattr(L, name):
+            getattr(L, name).restype = i32
+    return L
+
+
+lib = _load()
+
+
+def vce_abi_version() -> int:
+    return lib.vce_abi_version()
+
+
+def vce_status_string(code: int) -> str:
+    return lib.vce_status_string(int(code)).decode()
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(fn, rc):
+    if rc != 0:
+        raise VceError(fn, rc)
+
+
+def _dtype(t):
+    try:
+        return _DT[t.dtype]
+    except KeyError:
+        raise TypeError(f"unsupported dtype {t.dtype}; use float32 or bfloat16") from None
+
+
+def _ld(t):
+    if t.dim() != 2 or t.stride(1) != 1:
+        raise ValueError("expected a 2-D tensor with unit column stride")
+    return t.stride(0)
+
+
+def vce_get_status(status, stream=None) -> int:
+    """Wait for the stream and return the device status word (0 = ok, 1 = bad label)."""
+    out = ctypes.c_int32(0)
+    _check("vce_get_status", lib.vce_get_status(_ptr(status), _stream(stream), ctypes.byref(out)))
+    return out.value
+
+
+def ce_forward(logits, labels, ignore_index=IGNORE_INDEX, reduction="mean", *, loss_rows=None, loss_out=None,
+               row_stats=None, status=None, stream=None):
+    """Per-row loss, reduced loss and row statistics.  Returns (loss_out, loss_rows, row_stats, status)."""
+    T, V = logits.shape
+    dev = logits.device
+    loss_rows = torch.empty(T, dtype=torch.float32, device=dev) if loss_rows is None else loss_rows
+    row_stats = torch.empty(T, ROW_STATS, dtype=torch.float32, device=dev) if row_stats is None else row_stats
+    status = torch.empty(1, dtype=torch.int32, device=dev) if status is None else status
+    if reduction != "none" and loss_out is None:
+        loss_out = torch.empty(1, dtype=torch.float32, device=dev)
+    _check("ce_forward", lib.ce_forward(_ptr(logits), _dtype(logits), T, V, _ld(logits), _ptr(labels),
+                                        int(ignore_index), RED[reduction], _ptr(loss_rows), _ptr(loss_out),
+                                        _ptr(row_stats), _ptr(status), _stream(stream)))
+    return loss_out, loss_rows, row_stats, status
+
+
+def ce_backward(logits, labels, row_stats, grad_output, ignore_index=IGNORE_INDEX, reduction="mean", *,
+                grad_logits=None, grad_dtype=None, stream=None):
+    """Gradient of the reduced loss w.r.t. the logits.  Returns grad_logits."""
+    T, V = logits.shape
+    if grad_logits is None:
+        grad_logits = torch.empty(T, V, dtype=grad_dtype or logits.dtype, device=logits.device)
+    _check("ce_backward", lib.ce_backward(_ptr(logits), _dtype(logits), T, V, _ld(logits), _ptr(labels),
+                                          int(ignore_index), RED[reduction], _ptr(row_stats), _ptr(grad_output),
+                                          _ptr(grad_logits), _dtype(grad_logits), _ld(grad_logits),
+                                          _stream(stream)))
+    return grad_logits
+
+
+def ce_merge_chunks(chunks, labels, ignore_index=IGNORE_INDEX, reduction="mean", *, grad_output=None,
+                    chunk_grads=None, grad_dtype=None, want_grad=True, loss_rows=None, loss_out=None,
+                    row_stats=None, chunk_stats=None, status=None, stream=None):
+    """CE over column chunks (list of [T, w_c] tensors).
+
+    Returns (loss_out, loss_rows, row_stats, chunk_grads or None, chunk_stats [k, T, 4], status).
+    """
+    k = len(chunks)
+    T = chunks[0].shape[0]
+    dev = chunks[0].device
+    dt = _dtype(chunks[0])
+    if any(_dtype(c) != dt or c.shape[0] != T for c in chunks):
+        raise ValueError("chunks must share dtype and row count")
+    loss_rows = torch.empty(T, dtype=torch.float32, device=dev) if loss_rows is None else loss_rows
+    row_stats = torch.empty(T, ROW_STATS, dtype=torch.float32, device=dev) if row_stats is None else row_stats
+    chunk_stats = torch.empty(k, T, CHUNK_STATS, dtype=torch.float32, device=dev) if chunk_stats is None else chunk_stats
+    status = torch.empty(1, dtype=torch.int32, device=dev) if status is None else status
+    if reduction != "none" and loss_out is None:
+        loss_out = torch.empty(1, dtype=torch.float32, device=dev)
+    if want_grad and chunk_grads is None:
+        chunk_grads = [torch.empty(T, c.shape[1], dtype=grad_dtype or c.dtype, device=dev) for c in chunks]
+    if want_grad and grad_output is None:
+        grad_output = torch.ones(T if reduction == "none" else 1, dtype=torch.float32, device=dev)
+    P = ctypes.c_void_p * k
+    I = ctypes.c_int64 * k
+    in_ptrs = P(*[c.data_ptr() for c in chunks])
+    widths = I(*[c.shape[1] for c in chunks])
+    lds = I(*[_ld(c) for c in chunks])
+    g_ptrs = P(*[g.data_ptr() for g in chunk_grads]) if want_grad else None
+    g_lds = I(*[_ld(g) for g in chunk_grads]) if want_grad else None
+    gdt = _dtype(chunk_grads[0]) if want_grad else F32
+    _check("ce_merge_chunks", lib.ce_merge_chunks(
+        k, in_ptrs, widths, lds, dt, T, _ptr(labels), int(ignore_index), RED[reduction], _ptr(loss_rows),
+        _ptr(loss_out), _ptr(row_stats), _ptr(grad_output), g_ptrs, g_lds, gdt, _ptr(chunk_stats),
+        _ptr(status), _stream(stream)))
+    return loss_out, loss_rows, row_stats, (chunk_grads if want_grad else None), chunk_stats, status
+
+
+def linear_ce_workspace_bytes(T, D, V) -> int:
+    return int(lib.linear_ce_workspace_bytes(T, D, V))
+
+
+def linear_ce_fwd_bwd(E, W, labels, ignore_index=IGNORE_INDEX, reduction="mean", *, grad_output=None,
+                      grad_dtype=None, dE=None, dW=None, loss_rows=None, loss_out=None, workspace=None,
+                      status=None, stream=None):
+    """Fused linear-CE: loss of softmax(E W^T) and the gradients dE, dW.
+
+    Returns (loss_out, loss_rows, dE, dW, status).
+    """
+    T, D = E.shape
+    V = W.shape[0]
+    dev = E.device
+    gdt = grad_dtype or E.dtype
+    dE = torch.empty(T, D, dtype=gdt, device=dev) if dE is None else dE
+    dW = torch.empty(V, D, dtype=gdt, device=dev) if dW is None else dW
+    loss_rows = torch.empty(T, dtype=torch.float32, device=dev) if loss_rows is None else loss_rows
+    if reduction != "none" and loss_out is None:
+        loss_out = torch.empty(1, dtype=torch.float32, device=dev)
+    if grad_output is None:
+        grad_output = torch.ones(T if reduction == "none" else 1, dtype=torch.float32, device=dev)
+    status = torch.empty(1, dtype=torch.int32, device=dev) if status is None else status
+    need = linear_ce_workspace_bytes(T, D, V)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    _check("linear_ce_fwd_bwd", lib.linear_ce_fwd_bwd(
+        _ptr(E), _ptr(W), T, D, V, _ptr(labels), int(ignore_index), RED[reduction], _ptr(grad_output),
+        _ptr(loss_rows), _ptr(loss_out), _ptr(dE), _ptr(dW), _dtype(dE), _ptr(workspace), workspace.numel(),
+        _ptr(status), _stream(stream)))
+    return loss_out, loss_rows, dE, dW, status
+
+
+class _CrossEntropy(torch.autograd.Function):
+    """Autograd wrapper: forward = ce_forward, backward = ce_backward (bf16 input is not upcast)."""
+
+    @staticmethod
+    def forward(ctx, logits, labels, ignore_index, reduction):
+        loss_out, loss_rows, row_stats, status = ce_forward(logits, labels, ignore_index, reduction)
+        ctx.save_for_backward(logits, labels, row_stats)
+        ctx.ignore_index, ctx.reduction = ignore_index, reduction
+        return loss_rows if reduction == "none" else loss_out.reshape(())
+
+    @staticmethod
+    def backward(ctx, grad):
+        logits, labels, row_stats = ctx.saved_tensors
+        go = grad.reshape(-1).to(torch.float32).contiguous()
+        g = ce_backward(logits, labels, row_stats, go, ctx.ignore_index, ctx.reduction)
+        return g, None, None, None
+
+
+def cross_entropy(logits, labels, ignore_index=IGNORE_INDEX, reduction="mean"):
+    """Collapse-safe softmax cross-entropy of [T, V] float32/bfloat16 CUDA logits with autograd."""
+    return _CrossEntropy.apply(logits, labels, ignore_index, reduction)

@@ -1,0 +1,567 @@
+// Softmax cross-entropy over [T, V] logits: forward row statistics, the reduction, the
+// rebuilt gradient, and the vocabulary-chunked variant with its on-device merge.
+//
+// Method: torchtitan PR #5723 "[loss] fix softmax collapse with improved ce perf"
+//   Numerics  - NLL = softplus(logsumexp_{j != t} z_j - z_t), the target dropped before
+//               the sum; target gradient p_t - 1 below p_t = 1/4, else -p_non_target;
+//               ignored labels finite, then zeroed by the label mask.
+//   Memory/perf (compiled form) - the target removed by a column test so the sum is one
+//               read of the logits; only per-row statistics saved; the gradient rebuilt
+//               in one fused backward pass; bf16 input upcast inside the op.
+// Vocabulary chunks: Megatron-core core.tensor_parallel.cross_entropy (per-shard
+//   calculate_logits_max / gather_predicted_logits, all-reduce over the TP group),
+//   here merged on one device.
+//
+// Kernels (all stream the rows once, 16-byte vector accesses on the aligned body of
+// each row, scalar accesses on an unaligned head and tail):
+//   k_ce_fwd        one row per block iteration: (max, sum-exp) over j != t, z_t,
+//                   then loss and row statistics
+//   k_ce_reduce     one block: fixed-order fp64 sum of the losses, N, and 1/N weights
+//   k_ce_bwd        one (chunk, row) segment per block iteration: the gradient
+//   k_ce_chunk_fwd  one (chunk, row) segment per block iteration: chunk statistics
+//   k_ce_merge      one row per thread: merge the chunk statistics, then as k_ce_fwd
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <algorithm>
+
+#include "vce.h"
+#include "vce_device.cuh"
+#include "vce_host.h"
+
+namespace vce {
+namespace {
+
+constexpr int kUnroll = 4;
+
+// ------------------------------------------------------------------------------------------
+// Row segment streaming (forward): thread-partial (m, s) over the segment's columns except
+// the local target column `tl` (tl < 0 or >= w: no target here).  The thread that meets the
+// target column stores its value to *zt_out.
+
+template <typename S, int NT>
+__device__ __forceinline__ void fwd_segment(const S* __restrict__ row, int64_t w, int64_t tl, float& m,
+                                            float& s, float& mb, float* zt_out) {
+    constexpr int G = Elt<S>::kGroup;
+    const int tid = threadIdx.x;
+    const uintptr_t a = reinterpret_cast<uintptr_t>(row);
+    int64_t h = (int64_t)(((16 - (a & 15)) & 15) / sizeof(S));   // elements before 16-B alignment
+    if (h > w) h = w;
+    const int64_t nvec = (w - h) / G;
+    const int64_t tail0 = h + nvec * G;
+
+    // unaligned head and tail, one element per thread
+    for (int64_t j = tid; j < h; j += NT) {
+        float v = Elt<S>::load1(row + j);
+        if (j == tl) { *zt_out = v; v = -kInf; }
+        ms_push1(v, m, s, mb);
+    }
+    for (int64_t j = tail0 + tid; j < w; j += NT) {
+        float v = Elt<S>::load1(row + j);
+        if (j == tl) { *zt_out = v; v = -kInf; }
+        ms_push1(v, m, s, mb);
+    }
+
+    const uint4* vp = reinterpret_cast<const uint4*>(row + h);
+    for (int64_t v0 = tid; v0 < nvec; v0 += (int64_t)NT * kUnroll) {
+        uint4 r[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int64_t vi = v0 + (int64_t)u * NT;
+            if (vi < nvec) r[u] = ld_stream16(vp + vi);
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int64_t vi = v0 + (int64_t)u * NT;
+            if (vi < nvec) {
+                float v[G];
+                Elt<S>::unpack(r[u], v);
+                const uint64_t rel = (uint64_t)(tl - (h + vi * G));
+                if (rel < (uint64_t)G) {   // the target's group: mask it out (column test)
+#pragma unroll
+                    for (int k = 0; k < G; ++k)
+                        if (rel == (uint64_t)k) { *zt_out = v[k]; v[k] = -kInf; }
+                }
+                ms_push<G>(v, m, s, mb);
+            }
+        }
+    }
+}
+
+// Block-wide merge of the thread pairs; the result is valid in thread 0.
+template <int NT>
+__device__ __forceinline__ void ms_block_reduce(float& m, float& s, float* sm_m, float* sm_s) {
+    constexpr int NW = NT / 32;
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    ms_warp_reduce(m, s);
+    if (lane == 0) { sm_m[wid] = m; sm_s[wid] = s; }
+    __syncthreads();
+    if (wid == 0) {
+        m = lane < NW ? sm_m[lane] : -kInf;
+        s = lane < NW ? sm_s[lane] : 0.f;
+        ms_warp_reduce(m, s);
+    }
+}
+
+__device__ __forceinline__ void flag_label_error(int32_t* status) {
+    if (status) atomicCAS(status, 0, (int32_t)VCE_ERR_LABEL);
+}
+
+// ------------------------------------------------------------------------------------------
+
+template <typename S, int NT>
+__global__ void __launch_bounds__(NT) k_ce_fwd(const S* __restrict__ logits, int64_t T, int64_t V, int64_t ld,
+                                               const int64_t* __restrict__ labels, int64_t ignore_index,
+                                               float* __restrict__ loss_rows, float4* __restrict__ row_stats,
+                                               int32_t* status) {
+    __shared__ float sm_m[NT / 32], sm_s[NT / 32];
+    __shared__ float sm_zt;
+    for (int64_t row = blockIdx.x; row < T; row += gridDim.x) {
+        const int64_t t = labels[row];
+        const bool ignored = (t == ignore_index);
+        if (ignored || t < 0 || t >= V) {   // no read of the row: loss 0 (ignored) or NaN (bad label)
+            if (threadIdx.x == 0) {
+                loss_rows[row] = ignored ? 0.f : __int_as_float(0x7FC00000);
+                row_stats[row] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (!ignored) flag_label_error(status);
+            }
+            continue;
+        }
+        float m = -kInf, s = 0.f, mb = 0.f;
+        fwd_segment<S, NT>(logits + row * ld, V, t, m, s, mb, &sm_zt);
+        ms_block_reduce<NT>(m, s, sm_m, sm_s);   // contains the barrier that publishes sm_zt
+        if (threadIdx.x == 0) {
+            float loss;
+            row_stats[row] = ce_row_finish(m, s, sm_zt, &loss);
+            loss_rows[row] = loss;
+        }
+        __syncthreads();
+    }
+}
+
+// Fixed-order reduction of the per-row losses (one block).  Rows with a bad label add NaN.
+// MEAN also writes each valid row's weight 1/N into its statistics.
+template <int NT>
+__global__ void __launch_bounds__(NT) k_ce_reduce(const float* __restrict__ loss_rows, const int64_t* __restrict__ labels,
+                                                  int64_t T, int64_t V, int64_t ignore_index, int red,
+                                                  float* loss_out, float4* row_stats) {
+    __shared__ double sm_a[NT / 32];
+    __shared__ long long sm_n[NT / 32];
+    __shared__ float sm_inv;
+    double acc = 0.0;
+    long long n = 0;
+    for (int64_t i = threadIdx.x; i < T; i += NT) {
+        const int64_t t = labels[i];
+        if (t != ignore_index) {
+            acc += (double)loss_rows[i];
+            n += (t >= 0 && t < V) ? 1 : 0;
+        }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        acc += __shfl_xor_sync(0xFFFFFFFFu, acc, off);
+        n += __shfl_xor_sync(0xFFFFFFFFu, n, off);
+    }
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    if (lane == 0) { sm_a[wid] = acc; sm_n[wid] = n; }
+    __syncthreads();
+    if (wid == 0) {
+        acc = lane < NT / 32 ? sm_a[lane] : 0.0;
+        n = lane < NT / 32 ? sm_n[lane] : 0;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            acc += __shfl_xor_sync(0xFFFFFFFFu, acc, off);
+            n += __shfl_xor_sync(0xFFFFFFFFu, n, off);
+        }
+        if (lane == 0) {
+            if (red == VCE_RED_MEAN) {
+                *loss_out = (float)(acc / (double)n);   // 0/0 = NaN when every row is ignored
+                sm_inv = n > 0 ? (float)(1.0 / (double)n) : 0.f;
+            } else {
+                *loss_out = (float)acc;
+            }
+        }
+    }
+    if (red != VCE_RED_MEAN) return;
+    __syncthreads();
+    const float inv = sm_inv;
+    for (int64_t i = threadIdx.x; i < T; i += NT) {
+        const int64_t t = labels[i];
+        if (t != ignore_index && t >= 0 && t < V) row_stats[i].w = inv;
+    }
+}
+
+// ------------------------------------------------------------------------------------------
+// Backward: one row segment.  grad = coef * 2^(z*log2e - bias) off target, gt at the target.
+
+template <typename S, typename O, int NT>
+__device__ __forceinline__ void bwd_segment(const S* __restrict__ row, O* __restrict__ grow, int64_t w, int64_t tl,
+                                            float coef, float bias, float gt, bool zero) {
+    constexpr int G = Elt<S>::kGroup;
+    const int tid = threadIdx.x;
+    const uintptr_t a = reinterpret_cast<uintptr_t>(row);
+    int64_t h = (int64_t)(((16 - (a & 15)) & 15) / sizeof(S));
+    if (h > w) h = w;
+    const bool out_ok = ((reinterpret_cast<uintptr_t>(grow + h)) % GroupStore<O, G>::kAlign) == 0;
+    if (!out_ok) h = w;   // input and output phases differ: the whole segment goes scalar
+    const int64_t nvec = (w - h) / G;
+    const int64_t tail0 = h + nvec * G;
+
+    auto one = [&](int64_t j) {
+        float g = 0.f;
+        if (!zero) {
+            const float z = Elt<S>::load1(row + j);
+            g = (j == tl) ? gt : coef * ex2(fmaf(z, kLog2e, -bias));
+        }
+        Elt<O>::store1(grow + j, g);
+    };
+    for (int64_t j = tid; j < h; j += NT) one(j);
+    for (int64_t j = tail0 + tid; j < w; j += NT) one(j);
+
+    const uint4* vp = reinterpret_cast<const uint4*>(row + h);
+    O* gp = grow + h;
+    if (zero) {
+        const float g[G] = {};
+        for (int64_t vi = tid; vi < nvec; vi += NT) GroupStore<O, G>::run(gp + vi * G, g);
+        return;
+    }
+    for (int64_t v0 = tid; v0 < nvec; v0 += (int64_t)NT * kUnroll) {
+        uint4 r[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int64_t vi = v0 + (int64_t)u * NT;
+            if (vi < nvec) r[u] = ld_stream16(vp + vi);
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int64_t vi = v0 + (int64_t)u * NT;
+            if (vi < nvec) {
+                float v[G];
+                Elt<S>::unpack(r[u], v);
+#pragma unroll
+                for (int k = 0; k < G; ++k) v[k] = coef * ex2(fmaf(v[k], kLog2e, -bias));
+                const uint64_t rel = (uint64_t)(tl - (h + vi * G));
+                if (rel < (uint64_t)G) {
+#pragma unroll
+                    for (int k = 0; k < G; ++k)
+                        if (rel == (uint64_t)k) v[k] = gt;
+                }
+                GroupStore<O, G>::run(gp + vi * G, v);
+            }
+        }
+    }
+}
+
+struct SegTable {
+    int k;
+    int64_t T;
+    const void* in[VCE_MAX_CHUNKS];
+    void* out[VCE_MAX_CHUNKS];
+    int64_t width[VCE_MAX_CHUNKS];
+    int64_t off[VCE_MAX_CHUNKS];
+    int64_t ld_in[VCE_MAX_CHUNKS];
+    int64_t ld_out[VCE_MAX_CHUNKS];
+};
+
+// Items are (chunk, row) pairs, row-major over chunks so neighbouring blocks read the same row.
+template <typename S, typename O, int NT>
+__global__ void __launch_bounds__(NT) k_ce_bwd(const __grid_constant__ SegTable tab, const int64_t* __restrict__ labels,
+                                               const float4* __restrict__ row_stats,
+                                               const float* __restrict__ grad_output, int go_per_row) {
+    const int64_t items = tab.T * tab.k;
+    for (int64_t it = blockIdx.x; it < items; it += gridDim.x) {
+        const int64_t row = it / tab.k;
+        const int c = (int)(it - row * tab.k);
+        const float4 st = row_stats[row];
+        const bool zero = (st.w == 0.f);   // ignored row or bad label: +0.0 by selection
+        const float cg = zero ? 0.f : grad_output[go_per_row ? row : 0] * st.w;
+        const float coef = cg * st.y;                      // c * (1 - p_t)
+        const float bias = (st.x == -kInf) ? 0.f : st.x * kLog2e;
+        const float gt = cg * st.z;
+        const int64_t tl = zero ? -1 : labels[row] - tab.off[c];
+        const S* in = reinterpret_cast<const S*>(tab.in[c]) + row * tab.ld_in[c];
+        O* out = reinterpret_cast<O*>(tab.out[c]) + row * tab.ld_out[c];
+        bwd_segment<S, O, NT>(in, out, tab.width[c], tl, coef, bias, gt, zero);
+    }
+}
+
+// ------------------------------------------------------------------------------------------
+// Vocabulary chunks: per-(chunk, row) statistics, then a per-row merge.
+
+template <typename S, int NT>
+__global__ void __launch_bounds__(NT) k_ce_chunk_fwd(const __grid_constant__ SegTable tab,
+                                                     const int64_t* __restrict__ labels, int64_t ignore_index,
+                                                     float4* __restrict__ chunk_stats) {
+    __shared__ float sm_m[NT / 32], sm_s[NT / 32];
+    __shared__ float sm_zt;
+    const int64_t items = tab.T * tab.k;
+    for (int64_t it = blockIdx.x; it < items; it += gridDim.x) {
+        const int64_t row = it / tab.k;
+        const int c = (int)(it - row * tab.k);
+        const int64_t t = labels[row];
+        const int64_t w = tab.width[c];
+        const int64_t tl = (t == ignore_index) ? -1 : t - tab.off[c];
+        const bool owner = (tl >= 0 && tl < w);
+        if (threadIdx.x == 0) sm_zt = 0.f;
+        __syncthreads();
+        float m = -kInf, s = 0.f, mb = 0.f;
+        fwd_segment<S, NT>(reinterpret_cast<const S*>(tab.in[c]) + row * tab.ld_in[c], w, owner ? tl : -1, m, s, mb,
+                           &sm_zt);
+        ms_block_reduce<NT>(m, s, sm_m, sm_s);
+        if (threadIdx.x == 0)
+            chunk_stats[(int64_t)c * tab.T + row] = make_float4(m, s, owner ? sm_zt : 0.f, owner ? 1.f : 0.f);
+        __syncthreads();
+    }
+}
+
+__global__ void k_ce_merge(const float4* __restrict__ chunk_stats, int k, int64_t T, int64_t V,
+                           const int64_t* __restrict__ labels, int64_t ignore_index, float* __restrict__ loss_rows,
+                           float4* __restrict__ row_stats, int32_t* status) {
+    for (int64_t row = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; row < T; row += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t t = labels[row];
+        const bool ignored = (t == ignore_index);
+        if (ignored || t < 0 || t >= V) {
+            loss_rows[row] = ignored ? 0.f : __int_as_float(0x7FC00000);
+            row_stats[row] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (!ignored) flag_label_error(status);
+            continue;
+        }
+        float M = -kInf, S = 0.f, zt = 0.f;
+        for (int c = 0; c < k; ++c) {
+            const float4 cs = chunk_stats[(int64_t)c * T + row];
+            ms_merge(M, S, cs.x, cs.y);
+            if (cs.w != 0.f) zt = cs.z;
+        }
+        float loss;
+        row_stats[row] = ce_row_finish(M, S, zt, &loss);
+        loss_rows[row] = loss;
+    }
+}
+
+// ------------------------------------------------------------------------------------------
+// host side
+
+int pick_threads(int64_t row_bytes) {
+    if (row_bytes <= 8 * 1024) return 128;
+    if (row_bytes <= 64 * 1024) return 256;
+    return 512;
+}
+
+template <typename K>
+int grid_for(K kernel, int nt, int64_t items) {
+    const int sms = device_sm_count();
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, nt, 0) != cudaSuccess || per_sm < 1)
+        per_sm = 1;
+    const int64_t g = std::min<int64_t>(items, (int64_t)sms * per_sm);
+    return (int)std::max<int64_t>(g, 1);
+}
+
+template <typename S, int NT>
+cudaError_t launch_fwd(const void* logits, int64_t T, int64_t V, int64_t ld, const int64_t* labels, int64_t ig,
+                       float* loss_rows, float* row_stats, int32_t* status, cudaStream_t s) {
+    auto kern = k_ce_fwd<S, NT>;
+    kern<<<grid_for(kern, NT, T), NT, 0, s>>>(reinterpret_cast<const S*>(logits), T, V, ld, labels, ig, loss_rows,
+                                              reinterpret_cast<float4*>(row_stats), status);
+    return cudaGetLastError();
+}
+
+template <typename S, typename O, int NT>
+cudaError_t launch_bwd(const SegTable& tab, const int64_t* labels, const float* row_stats, const float* go,
+                       int go_per_row, cudaStream_t s) {
+    auto kern = k_ce_bwd<S, O, NT>;
+    kern<<<grid_for(kern, NT, tab.T * tab.k), NT, 0, s>>>(tab, labels, reinterpret_cast<const float4*>(row_stats), go,
+                                                           go_per_row);
+    return cudaGetLastError();
+}
+
+template <typename S, int NT>
+cudaError_t launch_chunk_fwd(const SegTable& tab, const int64_t* labels, int64_t ig, float* ws, cudaStream_t s) {
+    auto kern = k_ce_chunk_fwd<S, NT>;
+    kern<<<grid_for(kern, NT, tab.T * tab.k), NT, 0, s>>>(tab, labels, ig, reinterpret_cast<float4*>(ws));
+    return cudaGetLastError();
+}
+
+template <typename S>
+cudaError_t dispatch_fwd(int nt, const void* logits, int64_t T, int64_t V, int64_t ld, const int64_t* labels,
+                         int64_t ig, float* lr, float* rs, int32_t* st, cudaStream_t s) {
+    if (nt == 128) return launch_fwd<S, 128>(logits, T, V, ld, labels, ig, lr, rs, st, s);
+    if (nt == 256) return launch_fwd<S, 256>(logits, T, V, ld, labels, ig, lr, rs, st, s);
+    return launch_fwd<S, 512>(logits, T, V, ld, labels, ig, lr, rs, st, s);
+}
+
+template <typename S, typename O>
+cudaError_t dispatch_bwd2(int nt, const SegTable& tab, const int64_t* labels, const float* rs, const float* go,
+                          int per_row, cudaStream_t s) {
+    if (nt == 128) return launch_bwd<S, O, 128>(tab, labels, rs, go, per_row, s);
+    if (nt == 256) return launch_bwd<S, O, 256>(tab, labels, rs, go, per_row, s);
+    return launch_bwd<S, O, 512>(tab, labels, rs, go, per_row, s);
+}
+
+cudaError_t dispatch_bwd(vce_dtype dt, vce_dtype gdt, int nt, const SegTable& tab, const int64_t* labels,
+                         const float* rs, const float* go, int per_row, cudaStream_t s) {
+    if (dt == VCE_BF16 && gdt == VCE_BF16) return dispatch_bwd2<uint16_t, uint16_t>(nt, tab, labels, rs, go, per_row, s);
+    if (dt == VCE_BF16 && gdt == VCE_F32) return dispatch_bwd2<uint16_t, float>(nt, tab, labels, rs, go, per_row, s);
+    if (dt == VCE_F32 && gdt == VCE_BF16) return dispatch_bwd2<float, uint16_t>(nt, tab, labels, rs, go, per_row, s);
+    return dispatch_bwd2<float, float>(nt, tab, labels, rs, go, per_row, s);
+}
+
+template <typename S>
+cudaError_t dispatch_chunk_fwd(int nt, const SegTable& tab, const int64_t* labels, int64_t ig, float* ws,
+                               cudaStream_t s) {
+    if (nt == 128) return launch_chunk_fwd<S, 128>(tab, labels, ig, ws, s);
+    if (nt == 256) return launch_chunk_fwd<S, 256>(tab, labels, ig, ws, s);
+    return launch_chunk_fwd<S, 512>(tab, labels, ig, ws, s);
+}
+
+cudaError_t launch_reduce(const float* loss_rows, const int64_t* labels, int64_t T, int64_t V, int64_t ig, int red,
+                          float* loss_out, float* row_stats, cudaStream_t s) {
+    k_ce_reduce<1024><<<1, 1024, 0, s>>>(loss_rows, labels, T, V, ig, red, loss_out,
+                                         reinterpret_cast<float4*>(row_stats));
+    return cudaGetLastError();
+}
+
+int check_common(vce_dtype dt, vce_reduction red, int64_t T) {
+    if (dt != VCE_F32 && dt != VCE_BF16) return VCE_ERR_DTYPE;
+    if (red != VCE_RED_NONE && red != VCE_RED_SUM && red != VCE_RED_MEAN) return VCE_ERR_DTYPE;
+    if (T < 0) return VCE_ERR_SHAPE;
+    return VCE_OK;
+}
+
+}  // namespace
+}  // namespace vce
+
+using namespace vce;
+
+extern "C" int ce_forward(const void* logits, vce_dtype dt, int64_t T, int64_t V, int64_t ld, const int64_t* labels,
+                          int64_t ignore_index, vce_reduction red, float* loss_rows, float* loss_out, float* row_stats,
+                          int32_t* status, vce_stream_t s) {
+    int rc = check_common(dt, red, T);
+    if (rc) return rc;
+    if (V < 1) return VCE_ERR_SHAPE;
+    if (ld < V) return VCE_ERR_LD;
+    if (!status || (red != VCE_RED_NONE && !loss_out)) return VCE_ERR_NULL;
+    const size_t es = dt == VCE_BF16 ? 2 : 4;
+    if (T > 0) {
+        if (!logits || !labels || !loss_rows || !row_stats) return VCE_ERR_NULL;
+        if (!fits_bytes(T, ld, es)) return VCE_ERR_SHAPE;
+        if (!aligned(logits, es) || !aligned(labels, 8) || !aligned(loss_rows, 4) || !aligned(row_stats, 16))
+            return VCE_ERR_ALIGN;
+    }
+    if (red != VCE_RED_NONE && !aligned(loss_out, 4)) return VCE_ERR_ALIGN;
+    if ((rc = require_sm100())) return rc;
+    if (cudaMemsetAsync(status, 0, sizeof(int32_t), s) != cudaSuccess) return VCE_ERR_CUDA;
+    if (T > 0) {
+        const int nt = pick_threads(V * (int64_t)es);
+        cudaError_t e = dt == VCE_BF16 ? dispatch_fwd<uint16_t>(nt, logits, T, V, ld, labels, ignore_index, loss_rows,
+                                                                row_stats, status, s)
+                                       : dispatch_fwd<float>(nt, logits, T, V, ld, labels, ignore_index, loss_rows,
+                                                             row_stats, status, s);
+        if (e != cudaSuccess) return VCE_ERR_CUDA;
+    }
+    if (red != VCE_RED_NONE &&
+        launch_reduce(loss_rows, labels, T, V, ignore_index, red, loss_out, row_stats, s) != cudaSuccess)
+        return VCE_ERR_CUDA;
+    return VCE_OK;
+}
+
+extern "C" int ce_backward(const void* logits, vce_dtype dt, int64_t T, int64_t V, int64_t ld, const int64_t* labels,
+                           int64_t ignore_index, vce_reduction red, const float* row_stats, const float* grad_output,
+                           void* grad_logits, vce_dtype grad_dt, int64_t ld_grad, vce_stream_t s) {
+    (void)ignore_index;   // ignored rows carry weight 0 in row_stats
+    int rc = check_common(dt, red, T);
+    if (rc) return rc;
+    if (grad_dt != VCE_F32 && grad_dt != VCE_BF16) return VCE_ERR_DTYPE;
+    if (V < 1) return VCE_ERR_SHAPE;
+    if (ld < V || ld_grad < V) return VCE_ERR_LD;
+    if (T == 0) return VCE_OK;
+    if (!logits || !labels || !row_stats || !grad_output || !grad_logits) return VCE_ERR_NULL;
+    const size_t es = dt == VCE_BF16 ? 2 : 4, gs = grad_dt == VCE_BF16 ? 2 : 4;
+    if (!fits_bytes(T, ld, es) || !fits_bytes(T, ld_grad, gs)) return VCE_ERR_SHAPE;
+    if (!aligned(logits, es) || !aligned(grad_logits, gs) || !aligned(labels, 8) || !aligned(row_stats, 16) ||
+        !aligned(grad_output, 4))
+        return VCE_ERR_ALIGN;
+    if ((rc = require_sm100())) return rc;
+    SegTable tab{};
+    tab.k = 1;
+    tab.T = T;
+    tab.in[0] = logits;
+    tab.out[0] = grad_logits;
+    tab.width[0] = V;
+    tab.off[0] = 0;
+    tab.ld_in[0] = ld;
+    tab.ld_out[0] = ld_grad;
+    const int nt = pick_threads(V * (int64_t)es);
+    if (dispatch_bwd(dt, grad_dt, nt, tab, labels, row_stats, grad_output, red == VCE_RED_NONE, s) != cudaSuccess)
+        return VCE_ERR_CUDA;
+    return VCE_OK;
+}
+
+extern "C" int ce_merge_chunks(int k, const void* const* chunk_logits, const int64_t* chunk_width,
+                               const int64_t* chunk_ld, vce_dtype dt, int64_t T, const int64_t* labels,
+                               int64_t ignore_index, vce_reduction red, float* loss_rows, float* loss_out,
+                               float* row_stats, const float* grad_output, void* const* chunk_grads,
+                               const int64_t* chunk_grad_ld, vce_dtype grad_dt, float* chunk_stats_ws,
+                               int32_t* status, vce_stream_t s) {
+    int rc = check_common(dt, red, T);
+    if (rc) return rc;
+    if (k < 1 || k > VCE_MAX_CHUNKS) return VCE_ERR_ARG;
+    if (!chunk_logits || !chunk_width || !chunk_ld || !status) return VCE_ERR_NULL;
+    if (red != VCE_RED_NONE && !loss_out) return VCE_ERR_NULL;
+    if (chunk_grads && grad_dt != VCE_F32 && grad_dt != VCE_BF16) return VCE_ERR_DTYPE;
+    const size_t es = dt == VCE_BF16 ? 2 : 4, gs = grad_dt == VCE_BF16 ? 2 : 4;
+    SegTable tab{};
+    tab.k = k;
+    tab.T = T;
+    int64_t V = 0, max_w = 0;
+    for (int c = 0; c < k; ++c) {
+        const int64_t w = chunk_width[c];
+        if (w < 1) return VCE_ERR_SHAPE;
+        if (chunk_ld[c] < w) return VCE_ERR_LD;
+        const int64_t gld = chunk_grad_ld ? chunk_grad_ld[c] : w;
+        if (chunk_grads && gld < w) return VCE_ERR_LD;
+        if (T > 0) {
+            if (!chunk_logits[c] || (chunk_grads && !chunk_grads[c])) return VCE_ERR_NULL;
+            if (!fits_bytes(T, chunk_ld[c], es) || (chunk_grads && !fits_bytes(T, gld, gs))) return VCE_ERR_SHAPE;
+            if (!aligned(chunk_logits[c], es) || (chunk_grads && !aligned(chunk_grads[c], gs))) return VCE_ERR_ALIGN;
+        }
+        tab.in[c] = chunk_logits[c];
+        tab.out[c] = chunk_grads ? chunk_grads[c] : nullptr;
+        tab.width[c] = w;
+        tab.off[c] = V;
+        tab.ld_in[c] = chunk_ld[c];
+        tab.ld_out[c] = gld;
+        if (V > INT64_MAX - w) return VCE_ERR_SHAPE;
+        V += w;
+        max_w = std::max(max_w, w);
+    }
+    if (T > 0) {
+        if (!labels || !loss_rows || !row_stats || !chunk_stats_ws || (chunk_grads && !grad_output))
+            return VCE_ERR_NULL;
+        if (!aligned(labels, 8) || !aligned(loss_rows, 4) || !aligned(row_stats, 16) || !aligned(chunk_stats_ws, 16))
+            return VCE_ERR_ALIGN;
+        if (!fits_bytes(T, (int64_t)k * VCE_CHUNK_STATS, 4)) return VCE_ERR_SHAPE;
+    }
+    if ((rc = require_sm100())) return rc;
+    if (cudaMemsetAsync(status, 0, sizeof(int32_t), s) != cudaSuccess) return VCE_ERR_CUDA;
+    if (T > 0) {
+        const int nt = pick_threads(max_w * (int64_t)es);
+        cudaError_t e = dt == VCE_BF16 ? dispatch_chunk_fwd<uint16_t>(nt, tab, labels, ignore_index, chunk_stats_ws, s)
+                                       : dispatch_chunk_fwd<float>(nt, tab, labels, ignore_index, chunk_stats_ws, s);
+        if (e != cudaSuccess) return VCE_ERR_CUDA;
+        const int mt = 256;
+        const int mg = (int)std::min<int64_t>((T + mt - 1) / mt, (int64_t)device_sm_count() * 8);
+        k_ce_merge<<<mg, mt, 0, s>>>(reinterpret_cast<const float4*>(chunk_stats_ws), k, T, V, labels, ignore_index,
+                                     loss_rows, reinterpret_cast<float4*>(row_stats), status);
+        if (cudaGetLastError() != cudaSuccess) return VCE_ERR_CUDA;
+    }
+    if (red != VCE_RED_NONE &&
+        launch_reduce(loss_rows, labels, T, V, ignore_index, red, loss_out, row_stats, s) != cudaSuccess)
+        return VCE_ERR_CUDA;
+    if (chunk_grads && T > 0) {
+        const int nt = pick_threads(max_w * (int64_t)es);
+        if (dispatch_bwd(dt, grad_dt, nt, tab, labels, row_stats, grad_output, red == VCE_RED_NONE, s) != cudaSuccess)
+            return VCE_ERR_CUDA;
+    }
+    return VCE_OK;
+}

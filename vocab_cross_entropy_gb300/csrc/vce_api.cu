@@ -1,0 +1,76 @@
+// Library-wide entry points (version, status text, status read-back) and the cached
+// device queries the launchers use.
+#include <cuda_runtime.h>
+
+#include <atomic>
+
+#include "vce.h"
+#include "vce_host.h"
+
+namespace vce {
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_sms[kMaxDevices];
+std::atomic<int> g_arch[kMaxDevices];   // 0 unknown, 1 ok, -1 not sm_100-family
+
+int current_device() {
+    int d = 0;
+    if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDevices) return -1;
+    return d;
+}
+}  // namespace
+
+int device_sm_count() {
+    const int d = current_device();
+    if (d < 0) return 1;
+    int n = g_sms[d].load(std::memory_order_relaxed);
+    if (n > 0) return n;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, d) != cudaSuccess || n < 1) n = 1;
+    g_sms[d].store(n, std::memory_order_relaxed);
+    return n;
+}
+
+int require_sm100() {
+    const int d = current_device();
+    if (d < 0) return VCE_ERR_CUDA;
+    int a = g_arch[d].load(std::memory_order_relaxed);
+    if (a == 0) {
+        int major = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, d) != cudaSuccess) return VCE_ERR_CUDA;
+        a = (major == 10) ? 1 : -1;
+        g_arch[d].store(a, std::memory_order_relaxed);
+    }
+    return a == 1 ? VCE_OK : VCE_ERR_DEVICE;
+}
+
+}  // namespace vce
+
+extern "C" int vce_abi_version(void) { return VCE_ABI_VERSION; }
+
+extern "C" size_t vce_row_stats_floats(void) { return VCE_ROW_STATS; }
+
+extern "C" const char* vce_status_string(int status) {
+    switch (status) {
+        case VCE_OK: return "ok";
+        case VCE_ERR_LABEL: return "a label is neither ignore_index nor in [0, V)";
+        case VCE_ERR_NULL: return "a required pointer is NULL";
+        case VCE_ERR_DTYPE: return "unknown or unsupported dtype or reduction";
+        case VCE_ERR_SHAPE: return "invalid or overflowing size";
+        case VCE_ERR_LD: return "leading dimension smaller than the row length";
+        case VCE_ERR_ALIGN: return "misaligned pointer";
+        case VCE_ERR_WORKSPACE: return "workspace missing or too small";
+        case VCE_ERR_CUDA: return "a CUDA runtime call failed";
+        case VCE_ERR_ARG: return "invalid argument";
+        case VCE_ERR_DEVICE: return "the current device is not an sm_100-family GPU";
+        default: return "unknown status";
+    }
+}
+
+extern "C" int vce_get_status(const int32_t* status, vce_stream_t s, int32_t* host_out) {
+    if (!status || !host_out) return VCE_ERR_NULL;
+    if (cudaMemcpyAsync(host_out, status, sizeof(int32_t), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return VCE_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return VCE_ERR_CUDA;
+    return VCE_OK;
+}

@@ -1,0 +1,23 @@
+// Host-side helpers shared by the library's entry points: argument checks and cached
+// device properties.
+#pragma once
+
+#include <stddef.h>
+#include <stdint.h>
+
+namespace vce {
+
+inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// rows * ld * esize bytes (the extent of a [rows, ld] matrix) fits in int64.
+inline bool fits_bytes(int64_t rows, int64_t ld, size_t esize) {
+    if (rows < 0 || ld < 0) return false;
+    if (rows == 0 || ld == 0) return true;
+    const int64_t lim = INT64_MAX / (int64_t)esize;
+    return ld <= lim / rows;
+}
+
+int device_sm_count();     // SMs of the current device (cached per device)
+int require_sm100();       // VCE_OK when the current device is an sm_100-family GPU
+
+}  // namespace vce
