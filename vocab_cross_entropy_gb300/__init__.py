@@ -57,15 +57,28 @@ def _load():
     return L
 
 
-lib = _load()
+_lib = None
+
+
+def _get():
+    global _lib
+    if _lib is None:
+        _lib = _load()
+    return _lib
+
+
+def __getattr__(name):   # `lib` is loaded on first use, so the build module imports without it
+    if name == "lib":
+        return _get()
+    raise AttributeError(name)
 
 
 def vce_abi_version() -> int:
-    return lib.vce_abi_version()
+    return _get().vce_abi_version()
 
 
 def vce_status_string(code: int) -> str:
-    return lib.vce_status_string(int(code)).decode()
+    return _get().vce_status_string(int(code)).decode()
 
 
 def _ptr(t):
@@ -98,7 +111,7 @@ def _ld(t):
 def vce_get_status(status, stream=None) -> int:
     """Wait for the stream and return the device status word (0 = ok, 1 = bad label)."""
     out = ctypes.c_int32(0)
-    _check("vce_get_status", lib.vce_get_status(_ptr(status), _stream(stream), ctypes.byref(out)))
+    _check("vce_get_status", _get().vce_get_status(_ptr(status), _stream(stream), ctypes.byref(out)))
     return out.value
 
 
@@ -112,7 +125,7 @@ def ce_forward(logits, labels, ignore_index=IGNORE_INDEX, reduction="mean", *, l
     status = torch.empty(1, dtype=torch.int32, device=dev) if status is None else status
     if reduction != "none" and loss_out is None:
         loss_out = torch.empty(1, dtype=torch.float32, device=dev)
-    _check("ce_forward", lib.ce_forward(_ptr(logits), _dtype(logits), T, V, _ld(logits), _ptr(labels),
+    _check("ce_forward", _get().ce_forward(_ptr(logits), _dtype(logits), T, V, _ld(logits), _ptr(labels),
                                         int(ignore_index), RED[reduction], _ptr(loss_rows), _ptr(loss_out),
                                         _ptr(row_stats), _ptr(status), _stream(stream)))
     return loss_out, loss_rows, row_stats, status
@@ -124,7 +137,7 @@ def ce_backward(logits, labels, row_stats, grad_output, ignore_index=IGNORE_INDE
     T, V = logits.shape
     if grad_logits is None:
         grad_logits = torch.empty(T, V, dtype=grad_dtype or logits.dtype, device=logits.device)
-    _check("ce_backward", lib.ce_backward(_ptr(logits), _dtype(logits), T, V, _ld(logits), _ptr(labels),
+    _check("ce_backward", _get().ce_backward(_ptr(logits), _dtype(logits), T, V, _ld(logits), _ptr(labels),
                                           int(ignore_index), RED[reduction], _ptr(row_stats), _ptr(grad_output),
                                           _ptr(grad_logits), _dtype(grad_logits), _ld(grad_logits),
                                           _stream(stream)))
@@ -162,7 +175,7 @@ def ce_merge_chunks(chunks, labels, ignore_index=IGNORE_INDEX, reduction="mean",
     g_ptrs = P(*[g.data_ptr() for g in chunk_grads]) if want_grad else None
     g_lds = I(*[_ld(g) for g in chunk_grads]) if want_grad else None
     gdt = _dtype(chunk_grads[0]) if want_grad else F32
-    _check("ce_merge_chunks", lib.ce_merge_chunks(
+    _check("ce_merge_chunks", _get().ce_merge_chunks(
         k, in_ptrs, widths, lds, dt, T, _ptr(labels), int(ignore_index), RED[reduction], _ptr(loss_rows),
         _ptr(loss_out), _ptr(row_stats), _ptr(grad_output), g_ptrs, g_lds, gdt, _ptr(chunk_stats),
         _ptr(status), _stream(stream)))
@@ -170,7 +183,7 @@ def ce_merge_chunks(chunks, labels, ignore_index=IGNORE_INDEX, reduction="mean",
 
 
 def linear_ce_workspace_bytes(T, D, V) -> int:
-    return int(lib.linear_ce_workspace_bytes(T, D, V))
+    return int(_get().linear_ce_workspace_bytes(T, D, V))
 
 
 def linear_ce_fwd_bwd(E, W, labels, ignore_index=IGNORE_INDEX, reduction="mean", *, grad_output=None,
@@ -195,7 +208,7 @@ def linear_ce_fwd_bwd(E, W, labels, ignore_index=IGNORE_INDEX, reduction="mean",
     need = linear_ce_workspace_bytes(T, D, V)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
-    _check("linear_ce_fwd_bwd", lib.linear_ce_fwd_bwd(
+    _check("linear_ce_fwd_bwd", _get().linear_ce_fwd_bwd(
         _ptr(E), _ptr(W), T, D, V, _ptr(labels), int(ignore_index), RED[reduction], _ptr(grad_output),
         _ptr(loss_rows), _ptr(loss_out), _ptr(dE), _ptr(dW), _dtype(dE), _ptr(workspace), workspace.numel(),
         _ptr(status), _stream(stream)))
