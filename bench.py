@@ -308,6 +308,10 @@ def run_ours(args, rank, local_rank, world):
     init_dist(world, "nccl")
     problem = {"pages": gen.pages, "mid": gen.mid}[args.workload](seed=1003 + rank if args.workload == "pages"
                                                                   else 1002 + rank)
+    if args.rows:
+        problem = gen.CEProblem(problem.name + f"[{args.rows} rows]", args.rows, problem.V, problem.dtype,
+                                problem.seed, problem.std, round(0.10 * args.rows) if problem.n_margin else 0,
+                                problem.margin_lo, problem.margin_hi, round(problem.n_ignore * args.rows / problem.T))
     w = CEWorkload(problem, device)
     stream = torch.cuda.current_stream(device)
     for _ in range(args.warmup):
@@ -405,6 +409,8 @@ def main(argv=None):
     ap.add_argument("--workload", choices=["pages", "mid"], default="pages")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--rows", type=int, default=None,
+                    help="profiling only: draw the first ROWS rows of the workload instead of all T")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
