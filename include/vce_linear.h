@@ -1,0 +1,67 @@
+/*
+ * vce_linear.h -- fused linear cross-entropy of the GB300 vocabulary CE library.
+ *
+ * Source: apple/ml-cross-entropy issue #14 (Cut Cross-Entropy):
+ * linear_cross_entropy(e, c, targets) computes the cross-entropy of softmax(e c^T)
+ * from the embeddings e and the classifier weight c (no bias) without storing the
+ * logits; impl="cce_exact" disables gradient filtering so the gradients are the plain
+ * CE gradients; use_kahan keeps the accumulation of dc and de compensated.  The CE
+ * numerics are those of ce_forward / ce_backward in vce.h (torchtitan PR #5723).
+ *
+ * Conventions as in vce.h: device pointers owned by the caller, asynchronous on the
+ * caller's stream, negative return = host-detected argument error (nothing enqueued),
+ * device-detected errors in *status.
+ */
+#ifndef VCE_LINEAR_H
+#define VCE_LINEAR_H
+
+#include "vce.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/*
+ * Bytes of workspace linear_ce_fwd_bwd needs for these sizes; 0 if the sizes are
+ * invalid (T, V >= 1; D >= 8 and a multiple of 8).  For T=8192, D=4096, V=128256 it is
+ * about 2.6 GB (E^T, W^T, per-tile statistics, one vocabulary chunk of the gradient in
+ * two layouts and two bf16 halves, and the compensated dE accumulator pair).
+ */
+size_t linear_ce_workspace_bytes(int64_t T, int64_t D, int64_t V);
+
+/*
+ * linear_ce_fwd_bwd -- loss and gradients of CE(softmax(E W^T), labels) in one call.
+ *   z = E W^T is formed 128 x 256 tiles at a time on the tensor cores (bf16 operands,
+ *   fp32 accumulators) and never stored as a [T, V] matrix.
+ *   loss_rows[i] = softplus(logsumexp_{j != t} z_ij - z_it), reduction as ce_forward.
+ *   With G = dloss/dz (softmax - onehot scaled by c_i, the target entry by the p_t = 1/4
+ *   branch, ignored rows 0):
+ *       dE = G W   [T, D],       dW = G^T E   [V, D].
+ *   G enters the two gradient GEMMs as an exact-to-16-bits pair of bf16 terms
+ *   (G = G_hi + G_lo), every product sum is accumulated in fp32, and the partial dE of
+ *   successive vocabulary chunks is merged with a two-sum compensated fp32 pair.
+ *
+ *   E            [T, D] bf16 row-major, 16-byte aligned
+ *   W            [V, D] bf16 row-major, 16-byte aligned
+ *   labels       [T] int64; ignore_index marks ignored rows
+ *   red          VCE_RED_MEAN, VCE_RED_SUM or VCE_RED_NONE
+ *   grad_output  fp32 [1] (SUM, MEAN) or [T] (NONE): upstream gradient of the loss
+ *   loss_rows    [T] fp32, written;  loss_out [1] fp32, written for SUM / MEAN
+ *   dE, dW       [T, D] and [V, D] of dtype grad_dt (VCE_BF16 or VCE_F32), 16-byte
+ *                aligned, written (bf16 rounded to nearest even from fp32)
+ *   workspace    >= linear_ce_workspace_bytes(T, D, V) bytes, 256-byte aligned,
+ *                scratch owned by the caller, contents undefined on return
+ *   status       [1] int32: 0, VCE_ERR_LABEL, or 101..104 when a device-side wait of
+ *                the GEMM pipeline gave up (the outputs are then undefined)
+ */
+int linear_ce_fwd_bwd(const void* E, const void* W, int64_t T, int64_t D, int64_t V,
+                      const int64_t* labels, int64_t ignore_index, vce_reduction red,
+                      const float* grad_output, float* loss_rows, float* loss_out,
+                      void* dE, void* dW, vce_dtype grad_dt,
+                      void* workspace, size_t workspace_bytes, int32_t* status, vce_stream_t s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VCE_LINEAR_H */

@@ -1,0 +1,115 @@
+"""Parity of the fused linear-CE (linear_ce_fwd_bwd through the C ABI) with the fp64 oracle.
+
+dE and dW are sums over T or V products; they are graded as bf16 outputs against the
+oracle rounded once to bf16 (one ulp), except that an entry whose sum cancels (small
+|sum| against sum |terms|) may instead be within 2^-14 * sum |terms| of the fp64 value,
+the accumulation error an fp32 sum of these lengths can carry.
+"""
+import numpy as np
+import pytest
+import torch
+
+import gen
+from oracle import ce_oracle as O
+from oracle import rounding as R
+from tests import _grading as G
+from tests.test_ce_gpu import vce  # noqa: F401  (fixture)
+
+pytestmark = pytest.mark.gpu
+
+SUM_ATOL_REL = 2.0 ** -14
+
+
+def dev_bf16(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
+
+
+def host(t):
+    if t.dtype == torch.bfloat16:
+        return G.bf16_tensor_bits(t)
+    return t.cpu().numpy()
+
+
+def grade_sum(got, want, abs_terms, what):
+    """bf16 bits (or fp32 values) of a GEMM output vs the fp64 oracle and its sum of |terms|."""
+    if got.dtype == np.uint16:
+        d = R.bf16_ulp_distance(got, want)
+        val = O.widen(got, "bf16")
+        ok = (d <= 1) | (np.abs(val - want) <= SUM_ATOL_REL * abs_terms)
+        info = f"{what}: {np.sum(d > 1)} of {d.size} beyond 1 ulp, {np.sum(~ok)} beyond the cancellation bound"
+    else:
+        err = np.abs(got.astype(np.float64) - want)
+        ok = (err <= 1e-6 + 1e-4 * np.abs(want)) | (err <= SUM_ATOL_REL * abs_terms)
+        info = f"{what}: {np.sum(~ok)} of {err.size} out of tolerance"
+    assert ok.all(), info
+    return info
+
+
+def run_lce(vce, p, reduction="mean", grad_output=1.0, grad_dtype=torch.bfloat16):
+    Eb, Wb = p.E(), p.W()
+    E, W = dev_bf16(Eb), dev_bf16(Wb)
+    labels = torch.from_numpy(p.labels).cuda()
+    go = torch.empty(p.T if reduction == "none" else 1, device="cuda")
+    go[:] = torch.as_tensor(grad_output, dtype=torch.float32)
+    E0, W0 = E.clone(), W.clone()
+    loss_out, loss_rows, dE, dW, status = vce.linear_ce_fwd_bwd(E, W, labels, reduction=reduction, grad_output=go,
+                                                                grad_dtype=grad_dtype)
+    torch.cuda.synchronize()
+    assert vce.vce_get_status(status) == 0
+    assert torch.equal(E, E0) and torch.equal(W, W0)
+    return Eb, Wb, loss_out, loss_rows, dE, dW
+
+
+def full_check(vce, p, reduction="mean", grad_output=1.0, grad_dtype=torch.bfloat16):
+    Eb, Wb, loss_out, loss_rows, dE, dW = run_lce(vce, p, reduction, grad_output, grad_dtype)
+    E, W = O.widen(Eb, "bf16"), O.widen(Wb, "bf16")
+    ref = O.linear_ce(E, W, p.labels, reduction, grad_output)
+    G.check_loss_rows(loss_rows.cpu().numpy(), ref["loss_rows"], ref["valid"])
+    if reduction != "none":
+        G.check_reduced(loss_out.item(), ref["loss_out"])
+    aG = np.abs(ref["grad"])
+    grade_sum(host(dE), ref["dE"], aG @ np.abs(W), "dE")
+    grade_sum(host(dW), ref["dW"], aG.T @ np.abs(E), "dW")
+
+
+def test_pages_toy_shape(vce):
+    """T=8191, D=128, V=32: the Cut Cross-Entropy issue's toy, checked in full."""
+    full_check(vce, gen.linear_small())
+
+
+@pytest.mark.parametrize("T,D,V", [(300, 192, 1000), (128, 64, 256), (1, 8, 1), (257, 128, 513), (1024, 512, 40000)])
+def test_ragged_shapes(vce, T, D, V):
+    full_check(vce, gen.linear_custom(T, D, V, seed=T + V, n_ignore=min(3, T - 1)))
+
+
+@pytest.mark.parametrize("reduction", ["sum", "none"])
+def test_reductions(vce, reduction):
+    p = gen.linear_custom(200, 128, 700, seed=3, n_ignore=5)
+    full_check(vce, p, reduction, np.linspace(0.5, 2.0, 200) if reduction == "none" else 0.5)
+
+
+def test_fp32_gradients(vce):
+    full_check(vce, gen.linear_custom(256, 128, 3000, seed=4, n_ignore=4), grad_dtype=torch.float32)
+
+
+def test_raised_targets_do_not_collapse(vce):
+    """Rows whose target logit dominates: loss ~e^-m stays nonzero, exactly as the oracle."""
+    p = gen.linear_custom(64, 64, 500, seed=9, w_std=0.3)
+    Eb, Wb = p.E(), p.W()
+    E, W = O.widen(Eb, "bf16"), O.widen(Wb, "bf16")
+    # point W's target rows along E's rows: z_t = |e|^2 / 2 ~ 32, far above the other logits
+    Wm = Wb.copy()
+    for i in range(0, 64, 4):
+        Wm[p.labels[i]] = R.bf16_bits(R.round_bf16(0.5 * E[i]))
+    p.W = lambda out=None, threads=None: Wm
+    full_check(vce, p, "sum")
+
+
+def test_invalid_label(vce):
+    p = gen.linear_custom(64, 64, 100, seed=2)
+    p.labels = p.labels.copy()
+    p.labels[5] = 100
+    E, W = dev_bf16(p.E()), dev_bf16(p.W())
+    out = vce.linear_ce_fwd_bwd(E, W, torch.from_numpy(p.labels).cuda())
+    assert vce.vce_get_status(out[4]) == 1
+    assert np.isnan(out[1][5].item())

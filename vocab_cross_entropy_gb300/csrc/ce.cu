@@ -429,6 +429,22 @@ int check_common(vce_dtype dt, vce_reduction red, int64_t T) {
 }
 
 }  // namespace
+
+cudaError_t launch_stats_merge(const float* part, int k, int64_t T, int64_t V, const int64_t* labels,
+                               int64_t ignore_index, float* loss_rows, float* row_stats, int32_t* status,
+                               cudaStream_t s) {
+    const int mt = 256;
+    const int mg = (int)std::max<int64_t>(1, std::min<int64_t>((T + mt - 1) / mt, (int64_t)device_sm_count() * 8));
+    k_ce_merge<<<mg, mt, 0, s>>>(reinterpret_cast<const float4*>(part), k, T, V, labels, ignore_index, loss_rows,
+                                 reinterpret_cast<float4*>(row_stats), status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_loss_reduce(const float* loss_rows, const int64_t* labels, int64_t T, int64_t V,
+                               int64_t ignore_index, int red, float* loss_out, float* row_stats, cudaStream_t s) {
+    return launch_reduce(loss_rows, labels, T, V, ignore_index, red, loss_out, row_stats, s);
+}
+
 }  // namespace vce
 
 using namespace vce;

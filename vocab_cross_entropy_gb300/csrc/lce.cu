@@ -1,0 +1,461 @@
+// Fused linear cross-entropy: loss, dE and dW of softmax(E W^T) without storing the logits.
+//
+// Method: apple/ml-cross-entropy issue #14 (Cut Cross-Entropy): linear_cross_entropy(e, c,
+// targets) with the classifier weight only; impl="cce_exact" (no gradient filtering, so the
+// result is the plain CE gradient); use_kahan (dc = dW and de = dE kept in compensated
+// precision).  The CE numerics are those of torchtitan PR #5723 (target-excluded
+// log-sum-exp, softplus NLL, the p_t = 1/4 branch of the target gradient).
+//
+// Steps, all on the tensor cores through tc_gemm.cuh (bf16 operands, fp32 accumulators):
+//   0. E^T and W^T (K-major operands for the two gradient GEMMs)
+//   1. z = E W^T tile by tile (128 rows x 256 vocabulary columns, K = D); the epilogue keeps
+//      per-row (max, sum-exp) over the tile's non-target columns and the target logit, one
+//      partial per (row, vocabulary tile); a merge gives L', x, the loss and row_stats.
+//   2. per vocabulary chunk of Vc columns:
+//        G = c (softmax - onehot) of the recomputed z tile, split G = G_hi + G_lo in bf16
+//            (a 16-bit significand in total), written as [T, Vc] and [Vc, T];
+//        dW[chunk] = G^T E      (K = 2T: G_hi^T E + G_lo^T E; one complete reduction)
+//        dE      += G W[chunk]  (K = 2Vc), merged across chunks with a two-sum
+//                               compensated fp32 accumulator pair (sum, compensation).
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+#include <stdint.h>
+
+#include <algorithm>
+
+#include "tc_gemm.cuh"
+#include "vce.h"
+#include "vce_device.cuh"
+#include "vce_host.h"
+#include "vce_linear.h"
+
+namespace vce {
+namespace {
+
+using tc::BM;
+using tc::BN;
+using tc::BK;
+
+constexpr int64_t kChunkCols = 16384;   // vocabulary columns per gradient chunk (a multiple of BN)
+
+inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline int64_t round_up(int64_t a, int64_t b) { return cdiv(a, b) * b; }
+
+// ------------------------------------------------------------------------------------------
+// epilogues
+
+// Step 1: per (row, vocabulary tile): (max, sum-exp) over non-target columns < V, target logit.
+struct EpiStats {
+    struct Params {
+        const int64_t* labels;
+        int64_t ignore_index, T, V;
+        float4* part;   // [tiles_n][T]
+    };
+    struct Row {
+        float m, s, mb, zt;
+        int64_t t;
+        bool own;
+    };
+    __device__ __forceinline__ static void begin(const Params& p, Row& r, int row, int) {
+        r.m = -kInf;
+        r.s = 0.f;
+        r.mb = 0.f;
+        r.zt = 0.f;
+        r.own = false;
+        r.t = row < p.T ? p.labels[row] : p.ignore_index;
+        if (r.t == p.ignore_index) r.t = -1;
+    }
+    __device__ __forceinline__ static void consume(const Params& p, Row& r, int, int col0, const uint32_t (&acc)[32]) {
+        float v[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(acc[k]);
+        if ((int64_t)col0 + 32 > p.V) {   // vocabulary tail: columns past V are not logits
+#pragma unroll
+            for (int k = 0; k < 32; ++k)
+                if ((int64_t)col0 + k >= p.V) v[k] = -kInf;
+        }
+        const uint64_t rel = (uint64_t)(r.t - col0);
+        if (rel < 32) {   // the target column: take it out of the sum (column test)
+#pragma unroll
+            for (int k = 0; k < 32; ++k)
+                if (rel == (uint64_t)k) {
+                    r.zt = v[k];
+                    r.own = true;
+                    v[k] = -kInf;
+                }
+        }
+        ms_push<32>(v, r.m, r.s, r.mb);
+    }
+    __device__ __forceinline__ static void end(const Params& p, Row& r, int row, int tn) {
+        if (row < p.T) p.part[(int64_t)tn * p.T + row] = make_float4(r.m, r.s, r.own ? r.zt : 0.f, r.own ? 1.f : 0.f);
+    }
+};
+
+// Step 2a: G = c * (softmax - onehot) on the chunk's columns, as bf16 hi + lo, both layouts.
+struct EpiGrad {
+    struct Params {
+        const int64_t* labels;
+        int64_t T, width, col_off;   // rows, chunk width, chunk's first global column
+        const float4* row_stats;
+        const float* grad_output;
+        int go_per_row;
+        uint16_t *g_hi, *g_lo;       // [T_pad][ldg]
+        uint16_t *gt_hi, *gt_lo;     // [width_pad][ldt]
+        int64_t ldg, ldt;
+    };
+    struct Row {
+        float coef, bias, gt;
+        int64_t tl;
+        bool zero;
+    };
+    __device__ __forceinline__ static void begin(const Params& p, Row& r, int row, int) {
+        r.zero = true;
+        r.coef = r.bias = r.gt = 0.f;
+        r.tl = -1;
+        if (row < p.T) {
+            const float4 st = p.row_stats[row];
+            if (st.w != 0.f) {
+                const float c = p.grad_output[p.go_per_row ? row : 0] * st.w;
+                r.zero = false;
+                r.coef = c * st.y;
+                r.bias = (st.x == -kInf) ? 0.f : st.x * kLog2e;
+                r.gt = c * st.z;
+                r.tl = p.labels[row] - p.col_off;
+            }
+        }
+    }
+    __device__ __forceinline__ static void consume(const Params& p, Row& r, int row, int col0,
+                                                   const uint32_t (&acc)[32]) {
+        uint32_t hi[16], lo[16];
+#pragma unroll
+        for (int k = 0; k < 32; k += 2) {
+            float g[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int col = col0 + k + e;
+                float x = r.coef * ex2(fmaf(__uint_as_float(acc[k + e]), kLog2e, -r.bias));
+                if (col == r.tl) x = r.gt;
+                if (r.zero || col >= p.width) x = 0.f;
+                g[e] = x;
+            }
+            const uint32_t h = pack_bf16x2(g[0], g[1]);
+            const float r0 = g[0] - bf16_lo(h), r1 = g[1] - bf16_hi(h);
+            hi[k / 2] = h;
+            lo[k / 2] = pack_bf16x2(r0, r1);
+        }
+        // row-major [T_pad][ldg]: 64 contiguous bytes per thread
+        uint4* dh = reinterpret_cast<uint4*>(p.g_hi + (int64_t)row * p.ldg + col0);
+        uint4* dl = reinterpret_cast<uint4*>(p.g_lo + (int64_t)row * p.ldg + col0);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            dh[q] = make_uint4(hi[4 * q], hi[4 * q + 1], hi[4 * q + 2], hi[4 * q + 3]);
+            dl[q] = make_uint4(lo[4 * q], lo[4 * q + 1], lo[4 * q + 2], lo[4 * q + 3]);
+        }
+        // transposed [width_pad][ldt]: for each column the warp writes 32 consecutive rows
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+            const uint32_t h = hi[k / 2], l = lo[k / 2];
+            const uint16_t hv = (k & 1) ? (uint16_t)(h >> 16) : (uint16_t)(h & 0xFFFFu);
+            const uint16_t lv = (k & 1) ? (uint16_t)(l >> 16) : (uint16_t)(l & 0xFFFFu);
+            p.gt_hi[(int64_t)(col0 + k) * p.ldt + row] = hv;
+            p.gt_lo[(int64_t)(col0 + k) * p.ldt + row] = lv;
+        }
+    }
+    __device__ __forceinline__ static void end(const Params&, Row&, int, int) {}
+};
+
+// Step 2b: dW rows of the chunk, stored once (bf16 round-to-nearest-even or fp32).
+struct EpiStore {
+    struct Params {
+        void* out;
+        int64_t ld, rows, cols, row_off;
+        int bf16;
+    };
+    struct Row {};
+    __device__ __forceinline__ static void begin(const Params&, Row&, int, int) {}
+    __device__ __forceinline__ static void consume(const Params& p, Row&, int row, int col0, const uint32_t (&acc)[32]) {
+        if (row >= p.rows || col0 >= p.cols) return;
+        const int64_t base = (p.row_off + row) * p.ld + col0;
+        const int n = (p.cols - col0) < 32 ? (int)(p.cols - col0) : 32;
+        if (p.bf16) {
+            uint16_t* o = reinterpret_cast<uint16_t*>(p.out) + base;
+            if (n == 32) {
+                uint32_t w[16];
+#pragma unroll
+                for (int k = 0; k < 16; ++k) w[k] = pack_bf16x2(__uint_as_float(acc[2 * k]), __uint_as_float(acc[2 * k + 1]));
+                uint4* d = reinterpret_cast<uint4*>(o);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) d[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+            } else {
+                for (int k = 0; k < n; ++k) o[k] = to_bf16(__uint_as_float(acc[k]));
+            }
+        } else {
+            float* o = reinterpret_cast<float*>(p.out) + base;
+            if (n == 32) {
+                uint4* d = reinterpret_cast<uint4*>(o);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) d[q] = make_uint4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
+            } else {
+                for (int k = 0; k < n; ++k) o[k] = __uint_as_float(acc[k]);
+            }
+        }
+    }
+    __device__ __forceinline__ static void end(const Params&, Row&, int, int) {}
+};
+
+// Step 2c: dE partial of one chunk added into (sum, compensation) with a two-sum; the first
+// chunk initialises the pair, the last writes sum + compensation to the output.
+struct EpiKahan {
+    struct Params {
+        float *sum, *comp;   // [rows][cols]
+        int64_t rows, cols;
+        int first, last;
+        void* out;
+        int bf16;
+    };
+    struct Row {};
+    __device__ __forceinline__ static void begin(const Params&, Row&, int, int) {}
+    __device__ __forceinline__ static void consume(const Params& p, Row&, int row, int col0, const uint32_t (&acc)[32]) {
+        if (row >= p.rows || col0 >= p.cols) return;
+        const int64_t base = (int64_t)row * p.cols + col0;
+        const int n = (p.cols - col0) < 32 ? (int)(p.cols - col0) : 32;
+        float s[32], c[32];
+        if (p.first) {
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+                s[k] = __uint_as_float(acc[k]);
+                c[k] = 0.f;
+            }
+        } else {
+            for (int k = 0; k < n; ++k) {
+                const float x = __uint_as_float(acc[k]);
+                const float a = p.sum[base + k];
+                const float t = a + x;
+                const float bp = t - a;
+                const float e = (a - (t - bp)) + (x - bp);   // exact rounding error of a + x
+                s[k] = t;
+                c[k] = p.comp[base + k] + e;
+            }
+        }
+        if (p.last) {
+            if (p.bf16) {
+                uint16_t* o = reinterpret_cast<uint16_t*>(p.out) + base;
+                for (int k = 0; k < n; ++k) o[k] = to_bf16(s[k] + c[k]);
+            } else {
+                float* o = reinterpret_cast<float*>(p.out) + base;
+                for (int k = 0; k < n; ++k) o[k] = s[k] + c[k];
+            }
+        } else {
+            for (int k = 0; k < n; ++k) {
+                p.sum[base + k] = s[k];
+                p.comp[base + k] = c[k];
+            }
+        }
+    }
+    __device__ __forceinline__ static void end(const Params&, Row&, int, int) {}
+};
+
+// ------------------------------------------------------------------------------------------
+// transpose [R, C] (ld_in) -> [C, ld_out] with zero padding for R <= r < ld_out
+
+__global__ void k_transpose_bf16(const uint16_t* __restrict__ in, int64_t R, int64_t C, int64_t ld_in,
+                                 uint16_t* __restrict__ out, int64_t R_pad, int64_t ld_out) {
+    __shared__ uint16_t tile[64][65];
+    const int64_t r0 = (int64_t)blockIdx.y * 64, c0 = (int64_t)blockIdx.x * 64;
+    for (int i = threadIdx.y; i < 64; i += blockDim.y) {
+        const int64_t r = r0 + i, c = c0 + threadIdx.x;
+        tile[i][threadIdx.x] = (r < R && c < C) ? in[r * ld_in + c] : (uint16_t)0;
+    }
+    __syncthreads();
+    for (int i = threadIdx.y; i < 64; i += blockDim.y) {
+        const int64_t c = c0 + i, r = r0 + threadIdx.x;
+        if (c < C && r < R_pad) out[c * ld_out + r] = tile[threadIdx.x][i];
+    }
+}
+
+// ------------------------------------------------------------------------------------------
+// host side
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// 2-D bf16 map over a row-major [outer, inner] matrix with row pitch ld elements; box
+// box_rows x 64 elements (128 B, the swizzle span).  Loads past the extents read zeros.
+bool make_map(CUtensorMap* m, const void* base, int64_t inner, int64_t outer, int64_t ld, int box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
+    cuuint64_t strides[1] = {(cuuint64_t)(ld * 2)};
+    cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+    cuuint32_t es[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <class Epi>
+cudaError_t run_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b, const tc::GemmArgs& g,
+                     const typename Epi::Params& ep, cudaStream_t s) {
+    auto kern = tc::k_tc_gemm<Epi>;
+    static bool attr_set = false;   // per process; the attribute is per function, not per device
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    const int64_t tiles = (int64_t)g.tiles_m * g.tiles_n;
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(tiles, device_sm_count()));
+    kern<<<grid, tc::kThreads, tc::SMEM_BYTES, s>>>(a0, a1, b, g, ep);
+    return cudaGetLastError();
+}
+
+struct Layout {
+    int64_t T, D, V, T_pad, V_pad, Vc, tiles_v;
+    size_t off_et, off_wt, off_part, off_stats, off_ghi, off_glo, off_gthi, off_gtlo, off_sum, off_comp, total;
+};
+
+bool layout(int64_t T, int64_t D, int64_t V, Layout* L) {
+    if (T < 1 || D < 8 || V < 1 || (D % 8) != 0) return false;
+    if (T > (1 << 30) || V > (1ll << 31) || D > (1 << 20)) return false;
+    L->T = T;
+    L->D = D;
+    L->V = V;
+    L->T_pad = round_up(T, BM);
+    L->tiles_v = cdiv(V, BN);
+    L->V_pad = L->tiles_v * BN;
+    L->Vc = std::min<int64_t>(kChunkCols, L->V_pad);
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t o = off;
+        off += (bytes + 255) & ~size_t(255);
+        return o;
+    };
+    L->off_et = take((size_t)D * L->T_pad * 2);
+    L->off_wt = take((size_t)D * L->V_pad * 2);
+    L->off_part = take((size_t)L->tiles_v * T * 16);
+    L->off_stats = take((size_t)T * 16);
+    L->off_ghi = take((size_t)L->T_pad * L->Vc * 2);
+    L->off_glo = take((size_t)L->T_pad * L->Vc * 2);
+    L->off_gthi = take((size_t)L->Vc * L->T_pad * 2);
+    L->off_gtlo = take((size_t)L->Vc * L->T_pad * 2);
+    L->off_sum = take((size_t)T * D * 4);
+    L->off_comp = take((size_t)T * D * 4);
+    L->total = off;
+    return true;
+}
+
+}  // namespace
+}  // namespace vce
+
+using namespace vce;
+
+extern "C" size_t linear_ce_workspace_bytes(int64_t T, int64_t D, int64_t V) {
+    Layout L;
+    return layout(T, D, V, &L) ? L.total : 0;
+}
+
+extern "C" int linear_ce_fwd_bwd(const void* E, const void* W, int64_t T, int64_t D, int64_t V, const int64_t* labels,
+                                 int64_t ignore_index, vce_reduction red, const float* grad_output, float* loss_rows,
+                                 float* loss_out, void* dE, void* dW, vce_dtype grad_dt, void* workspace,
+                                 size_t workspace_bytes, int32_t* status, vce_stream_t s) {
+    if (red != VCE_RED_NONE && red != VCE_RED_SUM && red != VCE_RED_MEAN) return VCE_ERR_DTYPE;
+    if (grad_dt != VCE_BF16 && grad_dt != VCE_F32) return VCE_ERR_DTYPE;
+    Layout L;
+    if (!layout(T, D, V, &L)) return VCE_ERR_SHAPE;
+    if (!E || !W || !labels || !grad_output || !loss_rows || !dE || !dW || !status) return VCE_ERR_NULL;
+    if (red != VCE_RED_NONE && !loss_out) return VCE_ERR_NULL;
+    if (!workspace || workspace_bytes < L.total) return VCE_ERR_WORKSPACE;
+    const size_t gs = grad_dt == VCE_BF16 ? 2 : 4;
+    if (!aligned(E, 16) || !aligned(W, 16) || !aligned(workspace, 256) || !aligned(labels, 8) ||
+        !aligned(loss_rows, 4) || !aligned(grad_output, 4) || !aligned(dE, 16) || !aligned(dW, 16) ||
+        (loss_out && !aligned(loss_out, 4)))
+        return VCE_ERR_ALIGN;
+    (void)gs;
+    int rc = require_sm100();
+    if (rc) return rc;
+
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    uint16_t* Et = reinterpret_cast<uint16_t*>(ws + L.off_et);
+    uint16_t* Wt = reinterpret_cast<uint16_t*>(ws + L.off_wt);
+    float* part = reinterpret_cast<float*>(ws + L.off_part);
+    float* stats = reinterpret_cast<float*>(ws + L.off_stats);
+    uint16_t* ghi = reinterpret_cast<uint16_t*>(ws + L.off_ghi);
+    uint16_t* glo = reinterpret_cast<uint16_t*>(ws + L.off_glo);
+    uint16_t* gthi = reinterpret_cast<uint16_t*>(ws + L.off_gthi);
+    uint16_t* gtlo = reinterpret_cast<uint16_t*>(ws + L.off_gtlo);
+    float* dsum = reinterpret_cast<float*>(ws + L.off_sum);
+    float* dcomp = reinterpret_cast<float*>(ws + L.off_comp);
+
+    if (cudaMemsetAsync(status, 0, sizeof(int32_t), s) != cudaSuccess) return VCE_ERR_CUDA;
+
+    // 0. transposes
+    {
+        dim3 blk(64, 8);
+        k_transpose_bf16<<<dim3((unsigned)cdiv(D, 64), (unsigned)cdiv(L.T_pad, 64)), blk, 0, s>>>(
+            static_cast<const uint16_t*>(E), T, D, D, Et, L.T_pad, L.T_pad);
+        k_transpose_bf16<<<dim3((unsigned)cdiv(D, 64), (unsigned)cdiv(L.V_pad, 64)), blk, 0, s>>>(
+            static_cast<const uint16_t*>(W), V, D, D, Wt, L.V_pad, L.V_pad);
+        if (cudaGetLastError() != cudaSuccess) return VCE_ERR_CUDA;
+    }
+
+    CUtensorMap mE, mW, mEt, mWt, mGhi, mGlo, mGthi, mGtlo;
+    if (!make_map(&mE, E, D, T, D, BM) || !make_map(&mW, W, D, V, D, BN) || !make_map(&mEt, Et, L.T_pad, D, L.T_pad, BN) ||
+        !make_map(&mWt, Wt, L.V_pad, D, L.V_pad, BN) || !make_map(&mGhi, ghi, L.Vc, L.T_pad, L.Vc, BM) ||
+        !make_map(&mGlo, glo, L.Vc, L.T_pad, L.Vc, BM) || !make_map(&mGthi, gthi, L.T_pad, L.Vc, L.T_pad, BM) ||
+        !make_map(&mGtlo, gtlo, L.T_pad, L.Vc, L.T_pad, BM))
+        return VCE_ERR_CUDA;
+
+    const int nkD = (int)cdiv(D, BK);
+    const int tiles_t = (int)(L.T_pad / BM);
+
+    // 1. forward statistics over the whole vocabulary
+    {
+        tc::GemmArgs g{tiles_t, (int)L.tiles_v, nkD, nkD, 0, 0, 0, status};
+        EpiStats::Params ep{labels, ignore_index, T, V, reinterpret_cast<float4*>(part)};
+        if (run_gemm<EpiStats>(mE, mE, mW, g, ep, s) != cudaSuccess) return VCE_ERR_CUDA;
+        if (launch_stats_merge(part, (int)L.tiles_v, T, V, labels, ignore_index, loss_rows, stats, status, s) !=
+            cudaSuccess)
+            return VCE_ERR_CUDA;
+        if (red != VCE_RED_NONE &&
+            launch_loss_reduce(loss_rows, labels, T, V, ignore_index, red, loss_out, stats, s) != cudaSuccess)
+            return VCE_ERR_CUDA;
+    }
+
+    // 2. gradients, one vocabulary chunk at a time
+    const int64_t nchunks = cdiv(L.V_pad, L.Vc);
+    for (int64_t ci = 0; ci < nchunks; ++ci) {
+        const int64_t off = ci * L.Vc;
+        const int64_t width = std::min<int64_t>(L.Vc, V - off);
+        const int64_t width_pad = round_up(width, BN);
+        {
+            tc::GemmArgs g{tiles_t, (int)(width_pad / BN), nkD, nkD, 0, 0, (int)off, status};
+            EpiGrad::Params ep{labels, T, width, off, reinterpret_cast<const float4*>(stats), grad_output,
+                               red == VCE_RED_NONE, ghi, glo, gthi, gtlo, L.Vc, L.T_pad};
+            if (run_gemm<EpiGrad>(mE, mE, mW, g, ep, s) != cudaSuccess) return VCE_ERR_CUDA;
+        }
+        {   // dW[off : off + width] = G^T E, K = 2 T_pad (hi then lo)
+            const int nkT = (int)(L.T_pad / BK);
+            tc::GemmArgs g{(int)(width_pad / BM), (int)cdiv(D, BN), 2 * nkT, nkT, 0, 0, 0, status};
+            EpiStore::Params ep{dW, D, width, D, off, grad_dt == VCE_BF16};
+            if (run_gemm<EpiStore>(mGthi, mGtlo, mEt, g, ep, s) != cudaSuccess) return VCE_ERR_CUDA;
+        }
+        {   // dE += G W[off : off + width], K = 2 width (hi then lo)
+            const int nkc = (int)cdiv(width, BK);
+            tc::GemmArgs g{tiles_t, (int)cdiv(D, BN), 2 * nkc, nkc, (int)off, 0, 0, status};
+            EpiKahan::Params ep{dsum, dcomp, T, D, ci == 0, ci == nchunks - 1, dE, grad_dt == VCE_BF16};
+            if (run_gemm<EpiKahan>(mGhi, mGlo, mWt, g, ep, s) != cudaSuccess) return VCE_ERR_CUDA;
+        }
+    }
+    return VCE_OK;
+}

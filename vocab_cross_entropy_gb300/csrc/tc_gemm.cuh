@@ -1,0 +1,319 @@
+// A persistent, warp-specialised bf16 GEMM on the sm_100-family tensor cores:
+//     acc[m, n] = sum_k A[m, k] * B[n, k]      (both operands K-major, fp32 accumulators)
+// with a caller-supplied epilogue that consumes each 128 x 256 accumulator tile from
+// tensor memory.  Hand-written PTX for the TMA loads (cp.async.bulk.tensor), the
+// mbarrier pipeline and the tcgen05 MMA / TMEM instructions.
+//
+//   warp 0 (one lane)  TMA producer: A tile 128 x 64 and B tile 256 x 64 per stage
+//   warp 1 (one lane)  MMA issuer:   4 x tcgen05.mma (M=128, N=256, K=16) per stage
+//   warp 2             TMEM allocation / release (512 columns = two accumulators)
+//   warps 4..7         epilogue: tcgen05.ld 32 lanes x 32 columns at a time, one
+//                      accumulator row per thread
+// The accumulator is double buffered so the epilogue of tile i overlaps the MMAs of
+// tile i+1.  Shared-memory tiles use the 128-byte swizzle that TMA writes and the MMA
+// descriptors read.  Every wait is bounded: a wait that exceeds kWaitNs sets an error
+// code, every role stops, in-flight copies are drained (bounded) and TMEM is released.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace vce {
+namespace tc {
+
+constexpr int BM = 128, BN = 256, BK = 64;
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;   // 16 KB
+constexpr int B_BYTES = BN * BK * 2;   // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int TMEM_COLS = 2 * BN;      // two fp32 accumulators of 128 lanes x 256 columns
+constexpr int kThreads = 256;
+constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s: far beyond any legitimate wait
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+
+// error codes written to the kernel's error word when a wait gives up
+enum { kErrWaitEmpty = 101, kErrWaitFull = 102, kErrWaitAccFree = 103, kErrWaitAccFull = 104 };
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for the phase of `bar` with the given parity to complete.  Gives up after kWaitNs or
+// as soon as another role of the block has given up; returns false then.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          int32_t* err, int code) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer() - t0 > kWaitNs) {
+            *abort_flag = 1;
+            if (err) atomicCAS(err, 0, code);
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            smem_u32(dst)),
+        "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
+}
+
+// ---- tcgen05 ------------------------------------------------------------------------------
+
+__device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// D[tmem] (+)= A[smem] * B[smem]^T, bf16 inputs, fp32 accumulate, one thread issues.
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive on `bar` once every tcgen05.mma issued so far by this thread has completed.
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane (lane = 32 * (warp % 4) + lane id).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Shared-memory matrix descriptor: K-major operand, rows of 64 bf16 (128 B) written by TMA
+// with the 128-byte swizzle; 8-row groups 1024 B apart (stride byte offset).  The leading
+// byte offset is unused for this layout.  Bits 46-47 hold the descriptor version (1).
+__device__ __forceinline__ uint64_t desc_kmajor_sw128(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)1 << 16;
+    d |= (uint64_t)(1024 >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, both K-major, M x N.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// ---- the kernel ---------------------------------------------------------------------------
+
+struct GemmArgs {
+    int tiles_m, tiles_n;   // output tiles (BM x BN)
+    int nk;                 // K blocks (of BK) per tile
+    int nk_a0;              // the first nk_a0 blocks read A0, the rest A1 (K restarts at 0 for A1)
+    int b_x0;               // B's K coordinate of block kb is b_x0 + (kb mod nk_a0) * BK
+    int a_y0, b_y0;         // row offsets of the A and B tiles
+    int32_t* err;           // error word (wait timeouts)
+};
+
+template <class Epi>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_tc_gemm(const __grid_constant__ CUtensorMap mapA0, const __grid_constant__ CUtensorMap mapA1,
+              const __grid_constant__ CUtensorMap mapB, const GemmArgs g, const typename Epi::Params ep) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* smA = smem;
+    uint8_t* smB = smem + STAGES * A_BYTES;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+    uint64_t* empty = full + STAGES;
+    uint64_t* acc_full = empty + STAGES;
+    uint64_t* acc_free = acc_full + 2;
+    uint64_t* drain = acc_free + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&acc_full[a], 1);
+            mbar_init(&acc_free[a], 4 * 32);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        prefetch_map(&mapA0);
+        prefetch_map(&mapA1);
+        prefetch_map(&mapB);
+    }
+    if (warp == 2) {
+        tmem_alloc(tmem_slot, TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int ntiles = g.tiles_m * g.tiles_n;
+
+    if (warp == 0 && lane == 0) {
+        // ---------------- TMA producer
+        int stage = 0;
+        uint32_t phase = 0;
+        int issued = 0;   // stages whose copies were issued and not yet known complete
+        for (int tile = blockIdx.x; tile < ntiles && !*abort_flag; tile += gridDim.x) {
+            const int tm = tile % g.tiles_m, tn = tile / g.tiles_m;
+            for (int kb = 0; kb < g.nk; ++kb) {
+                if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, g.err, kErrWaitEmpty)) break;
+                mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
+                const bool second = kb >= g.nk_a0;
+                const int ka = second ? kb - g.nk_a0 : kb;
+                tma_load_2d(smA + stage * A_BYTES, second ? &mapA1 : &mapA0, &full[stage], ka * BK,
+                            g.a_y0 + tm * BM);
+                tma_load_2d(smB + stage * B_BYTES, &mapB, &full[stage], g.b_x0 + ka * BK, g.b_y0 + tn * BN);
+                issued = issued < STAGES ? issued + 1 : STAGES;
+                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+            }
+        }
+        if (*abort_flag) {
+            // drain: wait (bounded) for the copies of the last `issued` stages so no TMA write
+            // lands in shared memory after the block has exited
+            for (int i = 0; i < issued; ++i) {
+                if (--stage < 0) { stage = STAGES - 1; phase ^= 1u; }
+                const uint64_t t0 = globaltimer();
+                while (!mbar_try_wait(&full[stage], phase) && globaltimer() - t0 < kWaitNs) {
+                }
+            }
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ---------------- MMA issuer
+        constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
+        int stage = 0;
+        uint32_t phase = 0;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        const uint32_t a0 = smem_u32(smA), b0 = smem_u32(smB);
+        for (int tile = blockIdx.x; tile < ntiles && !*abort_flag; tile += gridDim.x) {
+            if (!mbar_wait(&acc_free[acc], acc_phase ^ 1u, abort_flag, g.err, kErrWaitAccFree)) break;
+            tc_fence_after();
+            const uint32_t d = tmem_base + (uint32_t)(acc * BN);
+            bool ok = true;
+            for (int kb = 0; kb < g.nk; ++kb) {
+                if (!mbar_wait(&full[stage], phase, abort_flag, g.err, kErrWaitFull)) { ok = false; break; }
+                tc_fence_after();
+                const uint64_t ad = desc_kmajor_sw128(a0 + stage * A_BYTES);
+                const uint64_t bd = desc_kmajor_sw128(b0 + stage * B_BYTES);
+#pragma unroll
+                for (int k = 0; k < BK / 16; ++k)   // advance 16 elements = 32 B = 2 descriptor units
+                    mma_bf16(d, ad + 2 * k, bd + 2 * k, idesc, (kb | k) != 0);
+                mma_commit(&empty[stage]);
+                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+            }
+            if (!ok) break;
+            mma_commit(&acc_full[acc]);
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1u;
+        }
+        // every MMA this thread issued has finished before TMEM can be released
+        mma_commit(drain);
+        const uint64_t t0 = globaltimer();
+        while (!mbar_try_wait(drain, 0) && globaltimer() - t0 < kWaitNs) {
+        }
+    } else if (warp >= 4) {
+        // ---------------- epilogue: thread = accumulator row
+        const int sub = warp & 3;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+            if (!mbar_wait(&acc_full[acc], acc_phase, abort_flag, g.err, kErrWaitAccFull)) break;
+            tc_fence_after();
+            const int tm = tile % g.tiles_m, tn = tile / g.tiles_m;
+            const int row = tm * BM + sub * 32 + lane;
+            typename Epi::Row st;
+            Epi::begin(ep, st, row, tn);
+            const uint32_t t0 = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(sub * 32) << 16);
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld32(t0 + (uint32_t)(c * 32), r);
+                tmem_wait_ld();
+                Epi::consume(ep, st, row, tn * BN + c * 32, r);
+            }
+            Epi::end(ep, st, row, tn);
+            tc_fence_before();
+            mbar_arrive(&acc_free[acc]);
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1u;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 2) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+}  // namespace tc
+}  // namespace vce

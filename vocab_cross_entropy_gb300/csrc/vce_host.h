@@ -2,6 +2,7 @@
 // device properties.
 #pragma once
 
+#include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
 
@@ -19,5 +20,13 @@ inline bool fits_bytes(int64_t rows, int64_t ld, size_t esize) {
 
 int device_sm_count();     // SMs of the current device (cached per device)
 int require_sm100();       // VCE_OK when the current device is an sm_100-family GPU
+
+// Per-row merge of k partial (max, sum-exp, target, owner) statistics laid out [k][T] as
+// float4, then the row finish (loss, row_stats); and the fixed-order loss reduction.
+cudaError_t launch_stats_merge(const float* part, int k, int64_t T, int64_t V, const int64_t* labels,
+                               int64_t ignore_index, float* loss_rows, float* row_stats, int32_t* status,
+                               cudaStream_t s);
+cudaError_t launch_loss_reduce(const float* loss_rows, const int64_t* labels, int64_t T, int64_t V,
+                               int64_t ignore_index, int red, float* loss_out, float* row_stats, cudaStream_t s);
 
 }  // namespace vce
