@@ -58,6 +58,7 @@ typedef struct CUstream_st* vce_stream_t; /* the same handle as cudaStream_t; NU
 #define VCE_ROW_STATS 4     /* floats per row of row_stats */
 #define VCE_CHUNK_STATS 4   /* floats per (chunk, row) of chunk statistics */
 #define VCE_MAX_CHUNKS 64   /* most column chunks ce_merge_chunks accepts */
+#define VCE_NOALLOC_MAX_CHUNK_ROWS 262144   /* most k * T for ce_merge_chunks_noalloc (4 MiB) */
 
 typedef enum { VCE_F32 = 0, VCE_BF16 = 1 } vce_dtype;
 typedef enum { VCE_RED_NONE = 0, VCE_RED_SUM = 1, VCE_RED_MEAN = 2 } vce_reduction;
@@ -73,7 +74,8 @@ enum {
     VCE_ERR_WORKSPACE = -6,   /* workspace missing or smaller than required */
     VCE_ERR_CUDA = -7,        /* a CUDA runtime call failed (launch, memset, attribute query) */
     VCE_ERR_ARG = -8,         /* any other invalid argument (chunk count, chunk layout) */
-    VCE_ERR_DEVICE = -9       /* the current device is not an sm_100-family GPU */
+    VCE_ERR_DEVICE = -9,      /* the current device is not an sm_100-family GPU */
+    VCE_ERR_SCRATCH_LIMIT = -10 /* k * T exceeds VCE_NOALLOC_MAX_CHUNK_ROWS (ce_merge_chunks_noalloc) */
 };
 
 /* Library ABI version (VCE_ABI_VERSION of the build). */
@@ -169,6 +171,35 @@ int ce_merge_chunks(int k, const void* const* chunk_logits, const int64_t* chunk
                     const float* grad_output, void* const* chunk_grads,
                     const int64_t* chunk_grad_ld, vce_dtype grad_dt,
                     float* chunk_stats_ws, int32_t* status, vce_stream_t s);
+
+/*
+ * ce_merge_chunks_noalloc -- ce_merge_chunks for callers that cannot allocate device memory.
+ * None of the pages has a counterpart: this entry point exists for callers that have no
+ * way to provide the per-call chunk_stats_ws scratch, such as a host program driving the
+ * library through this C ABI without a device memory manager of its own, or an engine
+ * whose device memory is a single arena reserved at start-up that no op may carve from.
+ *
+ * Same arguments, steps and results as ce_merge_chunks, without chunk_stats_ws: the
+ * per-(chunk, row) statistics live in a fixed array in device memory that the library
+ * defines (VCE_NOALLOC_MAX_CHUNK_ROWS entries of 16 bytes = 4 MiB, held on every GPU that
+ * loads the library until the process exits).  The call allocates and frees nothing.
+ *
+ *   - k * T must not exceed VCE_NOALLOC_MAX_CHUNK_ROWS; larger sizes return
+ *     VCE_ERR_SCRATCH_LIMIT and enqueue nothing.
+ *   - The first call on each device looks up the array's device address on that device
+ *     (cudaGetSymbolAddress, with that device current); make that first call before
+ *     capturing any stream.  A failed lookup returns VCE_ERR_CUDA.
+ *   - Every call on a device uses the same array and leaves its contents behind.  Calls
+ *     whose work can overlap on the GPU (different streams without ordering, or different
+ *     host threads) race on it and give undefined results; order them on one stream.
+ */
+int ce_merge_chunks_noalloc(int k, const void* const* chunk_logits, const int64_t* chunk_width,
+                            const int64_t* chunk_ld, vce_dtype dt, int64_t T,
+                            const int64_t* labels, int64_t ignore_index, vce_reduction red,
+                            float* loss_rows, float* loss_out, float* row_stats,
+                            const float* grad_output, void* const* chunk_grads,
+                            const int64_t* chunk_grad_ld, vce_dtype grad_dt,
+                            int32_t* status, vce_stream_t s);
 
 #ifdef __cplusplus
 }

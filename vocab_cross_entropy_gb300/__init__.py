@@ -13,7 +13,7 @@ import os
 
 import torch
 
-__all__ = ["VceError", "lib", "library_path", "ce_forward", "ce_backward", "ce_merge_chunks",
+__all__ = ["VceError", "lib", "library_path", "ce_forward", "ce_backward", "ce_merge_chunks", "ce_merge_chunks_noalloc",
            "linear_ce_workspace_bytes", "linear_ce_fwd_bwd", "vce_get_status", "vce_status_string",
            "vce_abi_version", "cross_entropy", "IGNORE_INDEX", "F32", "BF16", "RED"]
 
@@ -47,11 +47,13 @@ def _load():
     L.ce_forward.argtypes = [p, i32, i64, i64, i64, p, i64, i32, p, p, p, p, p]
     L.ce_backward.argtypes = [p, i32, i64, i64, i64, p, i64, i32, p, p, p, i32, i64, p]
     L.ce_merge_chunks.argtypes = [i32, p, p, p, i32, i64, p, i64, i32, p, p, p, p, p, p, i32, p, p, p]
+    L.ce_merge_chunks_noalloc.argtypes = [i32, p, p, p, i32, i64, p, i64, i32, p, p, p, p, p, p, i32, p, p]
     if hasattr(L, "linear_ce_fwd_bwd"):
         L.linear_ce_workspace_bytes.argtypes = [i64, i64, i64]
         L.linear_ce_workspace_bytes.restype = sz
         L.linear_ce_fwd_bwd.argtypes = [p, p, i64, i64, i64, p, i64, i32, p, p, p, p, p, i32, p, sz, p, p]
-    for name in ("ce_forward", "ce_backward", "ce_merge_chunks", "linear_ce_fwd_bwd", "vce_get_status"):
+    for name in ("ce_forward", "ce_backward", "ce_merge_chunks", "ce_merge_chunks_noalloc", "linear_ce_fwd_bwd",
+                 "vce_get_status"):
         if hasattr(L, name):
             getattr(L, name).restype = i32
     return L
@@ -180,6 +182,33 @@ def ce_merge_chunks(chunks, labels, ignore_index=IGNORE_INDEX, reduction="mean",
         _ptr(loss_out), _ptr(row_stats), _ptr(grad_output), g_ptrs, g_lds, gdt, _ptr(chunk_stats),
         _ptr(status), _stream(stream)))
     return loss_out, loss_rows, row_stats, (chunk_grads if want_grad else None), chunk_stats, status
+
+
+NOALLOC_MAX_CHUNK_ROWS = 262144
+
+
+def ce_merge_chunks_noalloc(chunks, labels, ignore_index=IGNORE_INDEX, reduction="mean", *, grad_output,
+                            chunk_grads, loss_rows, loss_out, row_stats, status, stream=None):
+    """ce_merge_chunks without a scratch workspace, for callers that cannot allocate device memory.
+
+    Every output buffer is the caller's (this wrapper allocates nothing); chunk_grads may be
+    None for a forward-only call.  The statistics go to an array the library keeps in device
+    memory (k * T <= NOALLOC_MAX_CHUNK_ROWS).  Returns None; raises VceError on a non-zero return.
+    """
+    k = len(chunks)
+    T = chunks[0].shape[0]
+    dt = _dtype(chunks[0])
+    P = ctypes.c_void_p * k
+    I = ctypes.c_int64 * k
+    in_ptrs = P(*[c.data_ptr() for c in chunks])
+    widths = I(*[c.shape[1] for c in chunks])
+    lds = I(*[_ld(c) for c in chunks])
+    g_ptrs = P(*[g.data_ptr() for g in chunk_grads]) if chunk_grads is not None else None
+    g_lds = I(*[_ld(g) for g in chunk_grads]) if chunk_grads is not None else None
+    gdt = _dtype(chunk_grads[0]) if chunk_grads is not None else F32
+    _check("ce_merge_chunks_noalloc", _get().ce_merge_chunks_noalloc(
+        k, in_ptrs, widths, lds, dt, T, _ptr(labels), int(ignore_index), RED[reduction], _ptr(loss_rows),
+        _ptr(loss_out), _ptr(row_stats), _ptr(grad_output), g_ptrs, g_lds, gdt, _ptr(status), _stream(stream)))
 
 
 def linear_ce_workspace_bytes(T, D, V) -> int:

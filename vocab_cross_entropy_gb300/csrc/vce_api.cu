@@ -63,6 +63,7 @@ extern "C" const char* vce_status_string(int status) {
         case VCE_ERR_CUDA: return "a CUDA runtime call failed";
         case VCE_ERR_ARG: return "invalid argument";
         case VCE_ERR_DEVICE: return "the current device is not an sm_100-family GPU";
+        case VCE_ERR_SCRATCH_LIMIT: return "k * T exceeds the built-in scratch of ce_merge_chunks_noalloc";
         default: return "unknown status";
     }
 }
