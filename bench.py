@@ -177,7 +177,8 @@ def profiled_traffic(name, files):
 class CEWorkload:
     """The pages' shape (default) or the mid shape: ce_forward + ce_backward."""
 
-    KERNEL_FILES = ["vocab_cross_entropy_gb300/csrc/ce.cu", "vocab_cross_entropy_gb300/csrc/vce_device.cuh"]
+    KERNEL_FILES = ["vocab_cross_entropy_gb300/csrc/ce_bwd.cu", "vocab_cross_entropy_gb300/csrc/ce_segments.h",
+                    "vocab_cross_entropy_gb300/csrc/vce_device.cuh"]
 
     def __init__(self, problem, device):
         import vocab_cross_entropy_gb300 as vce
@@ -243,6 +244,100 @@ class CEWorkload:
                 "l2": "no flush: inputs (%.2f GB logits) larger than the 129 MB L2" % (p.T * p.V * 2 / 1e9)}
 
 
+class ChunkedWorkload(CEWorkload):
+    """The pages' matrix as 8 column chunks in separate buffers: one ce_merge_chunks call per step."""
+
+    def __init__(self, problem, device):
+        super().__init__(problem, device)
+        bounds = gen.chunk_bounds(problem.V, gen.CHUNKS)
+        self.chunks = [self.logits[:, o:o + w].contiguous() for o, w in bounds]
+        self.grads = [torch.empty_like(c) for c in self.chunks]
+        del self.grad
+        self.logits = None
+        self.cstats = torch.empty(len(self.chunks), problem.T, 4, dtype=torch.float32, device=device)
+        self.launches_per_step = 4            # k_ce_chunk_fwd, k_ce_merge, k_ce_reduce, k_ce_bwd
+
+    def step(self, stream):
+        self.vce.ce_merge_chunks(self.chunks, self.labels, grad_output=self.go, chunk_grads=self.grads,
+                                 loss_rows=self.loss_rows, loss_out=self.loss_out, row_stats=self.stats,
+                                 chunk_stats=self.cstats, status=self.status, stream=stream)
+
+    def e2e_step(self, stream):
+        for c, o_w in zip(self.chunks, gen.chunk_bounds(self.p.V, gen.CHUNKS)):
+            o, w = o_w
+            c.copy_(self.host_bf16[:, o:o + w], non_blocking=True)
+        self.labels.copy_(self.labels_host, non_blocking=True)
+        self.step(stream)
+        self.loss_host.copy_(self.loss_out, non_blocking=True)
+
+    def describe(self):
+        d = super().describe()
+        d["workload"] = d["workload"].replace("CE fwd+bwd", f"CE fwd+bwd over {gen.CHUNKS} column chunks of "
+                                                            f"{gen.CHUNK_WIDTH} in separate buffers")
+        return d
+
+
+class LinearWorkload:
+    """Fused linear-CE: E [8192, 4096], W [128256, 4096] bf16; one linear_ce_fwd_bwd call per step."""
+
+    def __init__(self, problem, device):
+        import vocab_cross_entropy_gb300 as vce
+        self.vce = vce
+        self.p = problem
+        T, D, V = problem.T, problem.D, problem.V
+        self.E_host = torch.empty((T, D), dtype=torch.int16, pin_memory=True)
+        problem.E(out=self.E_host.numpy().view(np.uint16))
+        self.W_host = torch.empty((V, D), dtype=torch.int16, pin_memory=True)
+        problem.W(out=self.W_host.numpy().view(np.uint16))
+        self.E = self.E_host.view(torch.bfloat16).to(device)
+        self.W = self.W_host.view(torch.bfloat16).to(device)
+        self.labels_host = torch.from_numpy(problem.labels).pin_memory()
+        self.labels = self.labels_host.to(device)
+        self.dE = torch.empty((T, D), dtype=torch.bfloat16, device=device)
+        self.dW = torch.empty((V, D), dtype=torch.bfloat16, device=device)
+        self.ws = torch.empty(vce.linear_ce_workspace_bytes(T, D, V), dtype=torch.uint8, device=device)
+        self.loss_rows = torch.empty(T, dtype=torch.float32, device=device)
+        self.loss_out = torch.empty(1, dtype=torch.float32, device=device)
+        self.status = torch.empty(1, dtype=torch.int32, device=device)
+        self.go = torch.ones(1, dtype=torch.float32, device=device)
+        self.loss_host = torch.empty(1, dtype=torch.float32, pin_memory=True)
+        nchunks = -(-V // 16384)
+        self.launches_per_step = 2 + 3 + 3 * nchunks     # transposes, stats GEMM + merge + reduce, 3 GEMMs/chunk
+
+    def step(self, stream):
+        self.vce.linear_ce_fwd_bwd(self.E, self.W, self.labels, grad_output=self.go, dE=self.dE, dW=self.dW,
+                                   loss_rows=self.loss_rows, loss_out=self.loss_out, workspace=self.ws,
+                                   status=self.status, stream=stream)
+
+    def e2e_step(self, stream):
+        self.E.copy_(self.E_host.view(torch.bfloat16), non_blocking=True)
+        self.W.copy_(self.W_host.view(torch.bfloat16), non_blocking=True)
+        self.labels.copy_(self.labels_host, non_blocking=True)
+        self.step(stream)
+        self.loss_host.copy_(self.loss_out, non_blocking=True)
+
+    @property
+    def h2d_bytes(self):
+        p = self.p
+        return (p.T + p.V) * p.D * 2 + p.T * 8
+
+    d2h_bytes = 4
+
+    def tokens(self):
+        return self.p.T
+
+    def flops(self):
+        p = self.p
+        return 8.0 * p.T * p.V * p.D
+
+    def describe(self):
+        p = self.p
+        return {"workload": f"{p.name}: fused linear-CE fwd+bwd, E [{p.T}, {p.D}] x W [{p.V}, {p.D}] bf16, mean over "
+                            f"non-ignored rows ({len(p.ignore_rows)} ignored), dE and dW bf16",
+                "T": p.T, "D": p.D, "V": p.V, "operands": "bf16", "accumulate": "f32",
+                "l2": "no flush: W (%.2f GB) larger than the 129 MB L2" % (p.V * p.D * 2 / 1e9)}
+
+
 # ------------------------------------------------------------------------------- timing
 
 def time_steps(fn, steps, stream, world, device, per_launch=None):
@@ -302,17 +397,12 @@ def cpu_oracle_baseline(problem, budget_s=12.0, max_rows=4096):
 
 # ------------------------------------------------------------------------------- main
 
-def run_ours(args, rank, local_rank, world):
-    device = torch.device("cuda", local_rank)
-    torch.cuda.set_device(device)
-    init_dist(world, "nccl")
-    problem = {"pages": gen.pages, "mid": gen.mid}[args.workload](seed=1003 + rank if args.workload == "pages"
-                                                                  else 1002 + rank)
-    if args.rows:
-        problem = gen.CEProblem(problem.name + f"[{args.rows} rows]", args.rows, problem.V, problem.dtype,
-                                problem.seed, problem.std, round(0.10 * args.rows) if problem.n_margin else 0,
-                                problem.margin_lo, problem.margin_hi, round(problem.n_ignore * args.rows / problem.T))
-    w = CEWorkload(problem, device)
+def run_linear(args, rank, local_rank, world, device):
+    problem = gen.linear(seed=1005 + rank)
+    if args.vocab:
+        problem = gen.LinearProblem(f"linear[V={args.vocab}]", problem.T, problem.D, args.vocab, problem.seed,
+                                    problem.n_ignore)
+    w = LinearWorkload(problem, device)
     stream = torch.cuda.current_stream(device)
     for _ in range(args.warmup):
         w.step(stream)
@@ -320,7 +410,60 @@ def run_ours(args, rank, local_rank, world):
     with ClockSampler(local_rank) as clk:
         ms = time_steps(w.step, args.steps, stream, world, device)
     clocks = clk.summary()
-    fwd_ms, bwd_ms = time_kernel(w, max(10, min(args.steps, 50)), stream)
+    e2e_steps = max(3, min(args.e2e_steps, args.steps))
+    w.e2e_step(stream)
+    e2e_ms = time_steps(w.e2e_step, e2e_steps, stream, world, device)
+    status = w.vce.vce_get_status(w.status)
+    if status != 0:
+        raise RuntimeError(f"device status {status}")
+    tokens_all = sum_over_ranks(w.tokens(), world, device)
+    ms_step = ms / args.steps
+    peaks = measured_peaks()
+    achieved = w.flops() / (ms_step / 1e3) / 1e12
+    out = {
+        "metric": "fused linear-CE fwd+bwd tokens/s at T=8192, D=4096, V=128256 bf16; TFLOP/s vs bf16 peak",
+        "value": round(tokens_all / (ms_step / 1e3), 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": dict(w.describe(), parallelism=f"replicas{world}"),
+        "roofline": {"bound": "tensor", "kernel": "linear_ce_fwd_bwd (all launches of one call)",
+                     "achieved": round(achieved, 1), "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                     "frac": round(achieved / peaks["bf16_tflops_sustained"], 4),
+                     "frac_of_burst": round(achieved / peaks["bf16_tflops"], 4), "peak_source": peaks["source"],
+                     "algorithmic_flop_per_call": w.flops(), "executed_flop_per_call": 1.5 * w.flops(),
+                     "traffic": None},
+        "e2e": {"value": round(tokens_all / (e2e_ms / e2e_steps / 1e3), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": w.h2d_bytes, "d2h_bytes_per_step": w.d2h_bytes, "steps": e2e_steps},
+        "gpu_launches": w.launches_per_step * args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
+def run_ours(args, rank, local_rank, world):
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    init_dist(world, "nccl")
+    if args.workload == "linear":
+        return run_linear(args, rank, local_rank, world, device)
+    problem = {"pages": gen.pages, "chunked": gen.pages, "mid": gen.mid}[args.workload](
+        seed=(1002 if args.workload == "mid" else 1003) + rank)
+    if args.rows:
+        problem = gen.CEProblem(problem.name + f"[{args.rows} rows]", args.rows, problem.V, problem.dtype,
+                                problem.seed, problem.std, round(0.10 * args.rows) if problem.n_margin else 0,
+                                problem.margin_lo, problem.margin_hi, round(problem.n_ignore * args.rows / problem.T))
+    w = (ChunkedWorkload if args.workload == "chunked" else CEWorkload)(problem, device)
+    stream = torch.cuda.current_stream(device)
+    for _ in range(args.warmup):
+        w.step(stream)
+    torch.cuda.synchronize(device)
+    with ClockSampler(local_rank) as clk:
+        ms = time_steps(w.step, args.steps, stream, world, device)
+    clocks = clk.summary()
+    chunked = args.workload == "chunked"
+    if not chunked:
+        fwd_ms, bwd_ms = time_kernel(w, max(10, min(args.steps, 50)), stream)
     e2e_steps = max(3, min(args.e2e_steps, args.steps))
     for _ in range(2):
         w.e2e_step(stream)
@@ -335,8 +478,19 @@ def run_ours(args, rank, local_rank, world):
     e2e_value = tokens_all / (e2e_ms / e2e_steps / 1e3)
     peaks = measured_peaks()
     bwd_bytes = w.bytes_bwd()
-    achieved = bwd_bytes / (bwd_ms / 1e3) / 1e9
-    traffic = profiled_traffic(f"k_ce_bwd_{args.workload}", CEWorkload.KERNEL_FILES)
+    if chunked:   # one call launches all four kernels: roofline over the whole call
+        call_bytes = w.bytes_fwd() + bwd_bytes + 2 * w.p.T * gen.CHUNKS * 16
+        achieved = call_bytes / (ms_step / 1e3) / 1e9
+        roof = {"bound": "hbm", "kernel": "ce_merge_chunks (k_ce_chunk_fwd + k_ce_merge + k_ce_reduce + k_ce_bwd)",
+                "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(achieved / peaks["hbm_gbs"], 4), "peak_source": peaks["source"],
+                "algorithmic_bytes_per_launch": call_bytes, "traffic": None}
+    else:
+        achieved = bwd_bytes / (bwd_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "kernel": "k_ce_bwd", "achieved": round(achieved, 1),
+                "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                "peak_source": peaks["source"], "algorithmic_bytes_per_launch": bwd_bytes,
+                "traffic": profiled_traffic(f"k_ce_bwd_{args.workload}", CEWorkload.KERNEL_FILES)}
     out = {
         "metric": "CE fwd+bwd tokens/s at T=16384,V=128256 bf16; HBM GB/s vs ~8 TB/s",
         "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
@@ -344,19 +498,18 @@ def run_ours(args, rank, local_rank, world):
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": dict(w.describe(), parallelism=f"replicas{world}"),
         "hbm_gbs_step": round((w.bytes_fwd() + bwd_bytes) * world / (ms_step / 1e3) / 1e9, 1),
-        "kernels_ms": {"ce_forward": round(fwd_ms, 5), "ce_backward": round(bwd_ms, 5)},
-        "roofline": {"bound": "hbm", "kernel": "k_ce_bwd", "achieved": round(achieved, 1),
-                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
-                     "peak_source": peaks["source"], "algorithmic_bytes_per_launch": bwd_bytes,
-                     "traffic": traffic},
-        "roofline_fwd": {"bound": "hbm", "kernel": "k_ce_fwd",
-                         "achieved": round(w.bytes_fwd() / (fwd_ms / 1e3) / 1e9, 1), "peak": peaks["hbm_gbs"],
-                         "unit": "GB/s", "frac": round(w.bytes_fwd() / (fwd_ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4)},
+        "roofline": roof,
         "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": w.h2d_bytes,
                 "d2h_bytes_per_step": w.d2h_bytes, "steps": e2e_steps},
         "gpu_launches": w.launches_per_step * args.steps,
         "clocks": clocks,
     }
+    if not chunked:
+        out["kernels_ms"] = {"ce_forward": round(fwd_ms, 5), "ce_backward": round(bwd_ms, 5)}
+        out["roofline_fwd"] = {"bound": "hbm", "kernel": "k_ce_fwd",
+                               "achieved": round(w.bytes_fwd() / (fwd_ms / 1e3) / 1e9, 1), "peak": peaks["hbm_gbs"],
+                               "unit": "GB/s",
+                               "frac": round(w.bytes_fwd() / (fwd_ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4)}
     if rank == 0 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_oracle_baseline(problem)
     if rank == 0:
@@ -406,11 +559,13 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["pages", "mid"], default="pages")
+    ap.add_argument("--workload", choices=["pages", "chunked", "mid", "linear"], default="pages")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--rows", type=int, default=None,
                     help="profiling only: draw the first ROWS rows of the workload instead of all T")
+    ap.add_argument("--vocab", type=int, default=None,
+                    help="profiling only: a smaller vocabulary for the linear workload")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

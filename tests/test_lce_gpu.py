@@ -113,3 +113,28 @@ def test_invalid_label(vce):
     out = vce.linear_ce_fwd_bwd(E, W, torch.from_numpy(p.labels).cuda())
     assert vce.vce_get_status(out[4]) == 1
     assert np.isnan(out[1][5].item())
+
+
+def test_full_size_sampled(vce):
+    """E [8192, 4096], W [128256, 4096]: every loss row, sampled dE rows and dW rows vs fp64."""
+    p = gen.linear()
+    Eb, Wb, loss_out, loss_rows, dE, dW = run_lce(vce, p)
+    E, W = O.widen(Eb, "bf16"), O.widen(Wb, "bf16")
+    fwd = O.linear_ce_row_forward(E, W, p.labels, block=512)          # all T rows in fp64
+    G.check_loss_rows(loss_rows.cpu().numpy(), fwd["loss"], fwd["valid"], "full-size loss rows")
+    N = int(fwd["valid"].sum())
+    G.check_reduced(loss_out.item(), float(fwd["loss"][fwd["valid"]].sum()) / N)
+    c = O.row_scale(fwd["valid"], "mean", 1.0)
+    rng = np.random.default_rng(5)
+    aW = np.abs(W)
+    # dE rows: the full gradient row of z, times W
+    rows = np.unique(np.concatenate([rng.choice(p.T, 40, replace=False), p.ignore_rows[:4]]))
+    z = E[rows] @ W.T
+    sub = {k: v[rows] for k, v in fwd.items()}
+    Gr = O.ce_grad_rows(z, p.labels[rows], sub, c[rows])
+    grade_sum(host(dE[torch.from_numpy(rows).cuda()]), Gr @ W, np.abs(Gr) @ aW, "full-size dE rows")
+    # dW rows: one vocabulary column of G over all T rows, times E
+    targets = np.unique(p.labels[fwd["valid"]])
+    cols = np.unique(np.concatenate([rng.choice(p.V, 32, replace=False), rng.choice(targets, 16, replace=False)]))
+    Gc = O.linear_ce_grad_columns(E, W, p.labels, fwd, c, cols)
+    grade_sum(host(dW[torch.from_numpy(cols).cuda()]), Gc.T @ E, np.abs(Gc).T @ np.abs(E), "full-size dW rows")

@@ -16,8 +16,9 @@
 // each row, scalar accesses on an unaligned head and tail):
 //   k_ce_fwd        one row per block iteration: (max, sum-exp) over j != t, z_t,
 //                   then loss and row statistics
+//   k_ce_fwd_ring   the same per row, fed by a bulk-copy ring (rows >= 192 KB, 16-B aligned)
 //   k_ce_reduce     one block: fixed-order fp64 sum of the losses, N, and 1/N weights
-//   k_ce_bwd        one (chunk, row) segment per block iteration: the gradient
+//   k_ce_bwd        (ce_bwd.cu) one (chunk, row) segment per block iteration: the gradient
 //   k_ce_chunk_fwd  one (chunk, row) segment per block iteration: chunk statistics
 //   k_ce_merge      one row per thread: merge the chunk statistics, then as k_ce_fwd
 #include <cuda_runtime.h>
@@ -28,6 +29,8 @@
 #include "vce.h"
 #include "vce_device.cuh"
 #include "vce_host.h"
+#include "ce_segments.h"
+#include "vce_async.cuh"
 
 namespace vce {
 namespace {
@@ -139,6 +142,141 @@ __global__ void __launch_bounds__(NT) k_ce_fwd(const S* __restrict__ logits, int
     }
 }
 
+// ------------------------------------------------------------------------------------------
+// Forward with a bulk-copy ring: one producer thread streams every row of the block's share
+// in 32 KB pieces (cp.async.bulk into a 6-stage shared-memory ring, completion counted on
+// mbarriers) while 16 consumer warps reduce the previous pieces.  Copies never wait for the
+// row-end reduction, so DRAM stays busy across row boundaries.  Used for rows whose start
+// and length are 16-byte multiples and that span at least kRingStages pieces.
+
+constexpr int kRingBytes = 32768;
+constexpr int kRingStages = 6;
+constexpr int kRingWarps = 16;   // consumer warps; one more warp produces
+constexpr int kRingThreads = (kRingWarps + 1) * 32;
+constexpr int kRingSmem = kRingStages * kRingBytes + 128;
+enum { kErrRingEmpty = 111, kErrRingFull = 112, kErrRingReduce = 113 };
+
+template <typename S>
+__global__ void __launch_bounds__(kRingThreads, 1)
+    k_ce_fwd_ring(const S* __restrict__ logits, int64_t T, int64_t V, int64_t ld, const int64_t* __restrict__ labels,
+                  int64_t ignore_index, float* __restrict__ loss_rows, float4* __restrict__ row_stats,
+                  int32_t* status) {
+    constexpr int G = Elt<S>::kGroup;
+    extern __shared__ uint8_t ring_raw[];
+    uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(ring_raw) + 127) & ~uintptr_t(127));
+    __shared__ uint64_t full[kRingStages], empty[kRingStages], red_bar[2];
+    __shared__ float red_m[2][kRingWarps], red_s[2][kRingWarps], red_zt[2];
+    __shared__ int abort_flag;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kRingStages; ++i) {
+            tc::mbar_init(&full[i], 1);
+            tc::mbar_init(&empty[i], kRingWarps);
+        }
+        tc::mbar_init(&red_bar[0], kRingWarps);
+        tc::mbar_init(&red_bar[1], kRingWarps);
+        abort_flag = 0;
+        tc::fence_mbar_init();
+    }
+    __syncthreads();
+    volatile int* abort_v = &abort_flag;
+    const int64_t rb = V * (int64_t)sizeof(S);
+    const int nch = (int)((rb + kRingBytes - 1) / kRingBytes);
+
+    if (warp == kRingWarps) {
+        // ---------------- producer
+        if (lane == 0) {
+            int stage = 0, issued = 0;
+            uint32_t phase = 0;
+            for (int64_t row = blockIdx.x; row < T && !*abort_v; row += gridDim.x) {
+                const int64_t t = labels[row];
+                if (t == ignore_index || t < 0 || t >= V) continue;
+                const uint8_t* src = reinterpret_cast<const uint8_t*>(logits + row * ld);
+                for (int c = 0; c < nch; ++c) {
+                    if (!tc::mbar_wait(&empty[stage], phase ^ 1u, abort_v, status, kErrRingEmpty)) break;
+                    const int64_t left = rb - (int64_t)c * kRingBytes;
+                    const uint32_t bytes = (uint32_t)(left < kRingBytes ? left : kRingBytes);
+                    tc::mbar_arrive_expect_tx(&full[stage], bytes);
+                    tc::bulk_g2s(ring + stage * kRingBytes, src + (int64_t)c * kRingBytes, bytes, &full[stage]);
+                    issued = issued < kRingStages ? issued + 1 : kRingStages;
+                    if (++stage == kRingStages) { stage = 0; phase ^= 1u; }
+                }
+            }
+            if (*abort_v) {   // let copies in flight land before the block exits (bounded)
+                for (int i = 0; i < issued; ++i) {
+                    if (--stage < 0) { stage = kRingStages - 1; phase ^= 1u; }
+                    const uint64_t t0 = tc::globaltimer();
+                    while (!tc::mbar_try_wait(&full[stage], phase) && tc::globaltimer() - t0 < tc::kWaitNs) {
+                    }
+                }
+            }
+        }
+        return;
+    }
+
+    // ---------------- consumers
+    const int tid = threadIdx.x;   // 0 .. kRingWarps*32-1
+    int stage = 0, p = 0;
+    uint32_t phase = 0, red_phase = 0;   // bit p: parity of red_bar[p]'s next completion
+    for (int64_t row = blockIdx.x; row < T; row += gridDim.x) {
+        const int64_t t = labels[row];
+        const bool ignored = (t == ignore_index);
+        if (ignored || t < 0 || t >= V) {
+            if (tid == 0) {
+                loss_rows[row] = ignored ? 0.f : __int_as_float(0x7FC00000);
+                row_stats[row] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (!ignored) flag_label_error(status);
+            }
+            continue;
+        }
+        float m = -kInf, s = 0.f, mb = 0.f;
+        bool ok = true;
+        for (int c = 0; c < nch; ++c) {
+            if (!tc::mbar_wait(&full[stage], phase, abort_v, status, kErrRingFull)) { ok = false; break; }
+            const int64_t left = rb - (int64_t)c * kRingBytes;
+            const int nvec = (int)((left < kRingBytes ? left : kRingBytes) / 16);
+            const uint8_t* buf = ring + stage * kRingBytes;
+            const int64_t col_base = (int64_t)c * (kRingBytes / (int)sizeof(S));
+#pragma unroll 4
+            for (int v = tid; v < nvec; v += kRingWarps * 32) {
+                float x[G];
+                Elt<S>::unpack(tc::lds128(buf + v * 16), x);
+                const uint64_t rel = (uint64_t)(t - (col_base + (int64_t)v * G));
+                if (rel < (uint64_t)G) {
+#pragma unroll
+                    for (int k = 0; k < G; ++k)
+                        if (rel == (uint64_t)k) { red_zt[p] = x[k]; x[k] = -kInf; }
+                }
+                ms_push<G>(x, m, s, mb);
+            }
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&empty[stage]);
+            if (++stage == kRingStages) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        ms_warp_reduce(m, s);
+        __syncwarp();   // orders a lane's red_zt store before lane 0's arrive
+        if (lane == 0) {
+            red_m[p][warp] = m;
+            red_s[p][warp] = s;
+            tc::mbar_arrive(&red_bar[p]);   // release: the partials (and red_zt) are visible to waiters
+        }
+        if (warp == 0) {
+            if (!tc::mbar_wait(&red_bar[p], (red_phase >> p) & 1u, abort_v, status, kErrRingReduce)) break;
+            red_phase ^= 1u << p;
+            m = lane < kRingWarps ? red_m[p][lane] : -kInf;
+            s = lane < kRingWarps ? red_s[p][lane] : 0.f;
+            ms_warp_reduce(m, s);
+            if (lane == 0) {
+                float loss;
+                row_stats[row] = ce_row_finish(m, s, red_zt[p], &loss);
+                loss_rows[row] = loss;
+            }
+        }
+        p ^= 1;
+    }
+}
+
 // Fixed-order reduction of the per-row losses (one block).  Rows with a bad label add NaN.
 // MEAN also writes each valid row's weight 1/N into its statistics.
 template <int NT>
@@ -188,100 +326,6 @@ __global__ void __launch_bounds__(NT) k_ce_reduce(const float* __restrict__ loss
     for (int64_t i = threadIdx.x; i < T; i += NT) {
         const int64_t t = labels[i];
         if (t != ignore_index && t >= 0 && t < V) row_stats[i].w = inv;
-    }
-}
-
-// ------------------------------------------------------------------------------------------
-// Backward: one row segment.  grad = coef * 2^(z*log2e - bias) off target, gt at the target.
-
-template <typename S, typename O, int NT>
-__device__ __forceinline__ void bwd_segment(const S* __restrict__ row, O* __restrict__ grow, int64_t w, int64_t tl,
-                                            float coef, float bias, float gt, bool zero) {
-    constexpr int G = Elt<S>::kGroup;
-    const int tid = threadIdx.x;
-    const uintptr_t a = reinterpret_cast<uintptr_t>(row);
-    int64_t h = (int64_t)(((16 - (a & 15)) & 15) / sizeof(S));
-    if (h > w) h = w;
-    const bool out_ok = ((reinterpret_cast<uintptr_t>(grow + h)) % GroupStore<O, G>::kAlign) == 0;
-    if (!out_ok) h = w;   // input and output phases differ: the whole segment goes scalar
-    const int64_t nvec = (w - h) / G;
-    const int64_t tail0 = h + nvec * G;
-
-    auto one = [&](int64_t j) {
-        float g = 0.f;
-        if (!zero) {
-            const float z = Elt<S>::load1(row + j);
-            g = (j == tl) ? gt : coef * ex2(fmaf(z, kLog2e, -bias));
-        }
-        Elt<O>::store1(grow + j, g);
-    };
-    for (int64_t j = tid; j < h; j += NT) one(j);
-    for (int64_t j = tail0 + tid; j < w; j += NT) one(j);
-
-    const uint4* vp = reinterpret_cast<const uint4*>(row + h);
-    O* gp = grow + h;
-    if (zero) {
-        const float g[G] = {};
-        for (int64_t vi = tid; vi < nvec; vi += NT) GroupStore<O, G>::run(gp + vi * G, g);
-        return;
-    }
-    for (int64_t v0 = tid; v0 < nvec; v0 += (int64_t)NT * kUnroll) {
-        uint4 r[kUnroll];
-#pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-            const int64_t vi = v0 + (int64_t)u * NT;
-            if (vi < nvec) r[u] = ld_stream16(vp + vi);
-        }
-#pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-            const int64_t vi = v0 + (int64_t)u * NT;
-            if (vi < nvec) {
-                float v[G];
-                Elt<S>::unpack(r[u], v);
-#pragma unroll
-                for (int k = 0; k < G; ++k) v[k] = coef * ex2(fmaf(v[k], kLog2e, -bias));
-                const uint64_t rel = (uint64_t)(tl - (h + vi * G));
-                if (rel < (uint64_t)G) {
-#pragma unroll
-                    for (int k = 0; k < G; ++k)
-                        if (rel == (uint64_t)k) v[k] = gt;
-                }
-                GroupStore<O, G>::run(gp + vi * G, v);
-            }
-        }
-    }
-}
-
-struct SegTable {
-    int k;
-    int64_t T;
-    const void* in[VCE_MAX_CHUNKS];
-    void* out[VCE_MAX_CHUNKS];
-    int64_t width[VCE_MAX_CHUNKS];
-    int64_t off[VCE_MAX_CHUNKS];
-    int64_t ld_in[VCE_MAX_CHUNKS];
-    int64_t ld_out[VCE_MAX_CHUNKS];
-};
-
-// Items are (chunk, row) pairs, row-major over chunks so neighbouring blocks read the same row.
-template <typename S, typename O, int NT>
-__global__ void __launch_bounds__(NT) k_ce_bwd(const __grid_constant__ SegTable tab, const int64_t* __restrict__ labels,
-                                               const float4* __restrict__ row_stats,
-                                               const float* __restrict__ grad_output, int go_per_row) {
-    const int64_t items = tab.T * tab.k;
-    for (int64_t it = blockIdx.x; it < items; it += gridDim.x) {
-        const int64_t row = it / tab.k;
-        const int c = (int)(it - row * tab.k);
-        const float4 st = row_stats[row];
-        const bool zero = (st.w == 0.f);   // ignored row or bad label: +0.0 by selection
-        const float cg = zero ? 0.f : grad_output[go_per_row ? row : 0] * st.w;
-        const float coef = cg * st.y;                      // c * (1 - p_t)
-        const float bias = (st.x == -kInf) ? 0.f : st.x * kLog2e;
-        const float gt = cg * st.z;
-        const int64_t tl = zero ? -1 : labels[row] - tab.off[c];
-        const S* in = reinterpret_cast<const S*>(tab.in[c]) + row * tab.ld_in[c];
-        O* out = reinterpret_cast<O*>(tab.out[c]) + row * tab.ld_out[c];
-        bwd_segment<S, O, NT>(in, out, tab.width[c], tl, coef, bias, gt, zero);
     }
 }
 
@@ -341,37 +385,12 @@ __global__ void k_ce_merge(const float4* __restrict__ chunk_stats, int k, int64_
 // ------------------------------------------------------------------------------------------
 // host side
 
-int pick_threads(int64_t row_bytes) {
-    if (row_bytes <= 8 * 1024) return 128;
-    if (row_bytes <= 64 * 1024) return 256;
-    return 512;
-}
-
-template <typename K>
-int grid_for(K kernel, int nt, int64_t items) {
-    const int sms = device_sm_count();
-    int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, nt, 0) != cudaSuccess || per_sm < 1)
-        per_sm = 1;
-    const int64_t g = std::min<int64_t>(items, (int64_t)sms * per_sm);
-    return (int)std::max<int64_t>(g, 1);
-}
-
 template <typename S, int NT>
 cudaError_t launch_fwd(const void* logits, int64_t T, int64_t V, int64_t ld, const int64_t* labels, int64_t ig,
                        float* loss_rows, float* row_stats, int32_t* status, cudaStream_t s) {
     auto kern = k_ce_fwd<S, NT>;
     kern<<<grid_for(kern, NT, T), NT, 0, s>>>(reinterpret_cast<const S*>(logits), T, V, ld, labels, ig, loss_rows,
                                               reinterpret_cast<float4*>(row_stats), status);
-    return cudaGetLastError();
-}
-
-template <typename S, typename O, int NT>
-cudaError_t launch_bwd(const SegTable& tab, const int64_t* labels, const float* row_stats, const float* go,
-                       int go_per_row, cudaStream_t s) {
-    auto kern = k_ce_bwd<S, O, NT>;
-    kern<<<grid_for(kern, NT, tab.T * tab.k), NT, 0, s>>>(tab, labels, reinterpret_cast<const float4*>(row_stats), go,
-                                                           go_per_row);
     return cudaGetLastError();
 }
 
@@ -383,27 +402,31 @@ cudaError_t launch_chunk_fwd(const SegTable& tab, const int64_t* labels, int64_t
 }
 
 template <typename S>
+cudaError_t launch_fwd_ring(const void* logits, int64_t T, int64_t V, int64_t ld, const int64_t* labels, int64_t ig,
+                            float* loss_rows, float* row_stats, int32_t* status, cudaStream_t s) {
+    auto kern = k_ce_fwd_ring<S>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kRingSmem);
+    if (e != cudaSuccess) return e;
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(T, device_sm_count()));
+    kern<<<grid, kRingThreads, kRingSmem, s>>>(reinterpret_cast<const S*>(logits), T, V, ld, labels, ig, loss_rows,
+                                               reinterpret_cast<float4*>(row_stats), status);
+    return cudaGetLastError();
+}
+
+// The ring path needs 16-byte aligned row starts and lengths, and rows of at least
+// kRingStages pieces (so no consumer warp runs more than one row ahead of another).
+bool ring_eligible(const void* logits, int64_t V, int64_t ld, size_t es) {
+    return aligned(logits, 16) && (ld * (int64_t)es) % 16 == 0 && (V * (int64_t)es) % 16 == 0 &&
+           V * (int64_t)es >= (int64_t)kRingStages * kRingBytes;
+}
+
+template <typename S>
 cudaError_t dispatch_fwd(int nt, const void* logits, int64_t T, int64_t V, int64_t ld, const int64_t* labels,
                          int64_t ig, float* lr, float* rs, int32_t* st, cudaStream_t s) {
+    if (ring_eligible(logits, V, ld, sizeof(S))) return launch_fwd_ring<S>(logits, T, V, ld, labels, ig, lr, rs, st, s);
     if (nt == 128) return launch_fwd<S, 128>(logits, T, V, ld, labels, ig, lr, rs, st, s);
     if (nt == 256) return launch_fwd<S, 256>(logits, T, V, ld, labels, ig, lr, rs, st, s);
     return launch_fwd<S, 512>(logits, T, V, ld, labels, ig, lr, rs, st, s);
-}
-
-template <typename S, typename O>
-cudaError_t dispatch_bwd2(int nt, const SegTable& tab, const int64_t* labels, const float* rs, const float* go,
-                          int per_row, cudaStream_t s) {
-    if (nt == 128) return launch_bwd<S, O, 128>(tab, labels, rs, go, per_row, s);
-    if (nt == 256) return launch_bwd<S, O, 256>(tab, labels, rs, go, per_row, s);
-    return launch_bwd<S, O, 512>(tab, labels, rs, go, per_row, s);
-}
-
-cudaError_t dispatch_bwd(vce_dtype dt, vce_dtype gdt, int nt, const SegTable& tab, const int64_t* labels,
-                         const float* rs, const float* go, int per_row, cudaStream_t s) {
-    if (dt == VCE_BF16 && gdt == VCE_BF16) return dispatch_bwd2<uint16_t, uint16_t>(nt, tab, labels, rs, go, per_row, s);
-    if (dt == VCE_BF16 && gdt == VCE_F32) return dispatch_bwd2<uint16_t, float>(nt, tab, labels, rs, go, per_row, s);
-    if (dt == VCE_F32 && gdt == VCE_BF16) return dispatch_bwd2<float, uint16_t>(nt, tab, labels, rs, go, per_row, s);
-    return dispatch_bwd2<float, float>(nt, tab, labels, rs, go, per_row, s);
 }
 
 template <typename S>
@@ -481,38 +504,6 @@ extern "C" int ce_forward(const void* logits, vce_dtype dt, int64_t T, int64_t V
     return VCE_OK;
 }
 
-extern "C" int ce_backward(const void* logits, vce_dtype dt, int64_t T, int64_t V, int64_t ld, const int64_t* labels,
-                           int64_t ignore_index, vce_reduction red, const float* row_stats, const float* grad_output,
-                           void* grad_logits, vce_dtype grad_dt, int64_t ld_grad, vce_stream_t s) {
-    (void)ignore_index;   // ignored rows carry weight 0 in row_stats
-    int rc = check_common(dt, red, T);
-    if (rc) return rc;
-    if (grad_dt != VCE_F32 && grad_dt != VCE_BF16) return VCE_ERR_DTYPE;
-    if (V < 1) return VCE_ERR_SHAPE;
-    if (ld < V || ld_grad < V) return VCE_ERR_LD;
-    if (T == 0) return VCE_OK;
-    if (!logits || !labels || !row_stats || !grad_output || !grad_logits) return VCE_ERR_NULL;
-    const size_t es = dt == VCE_BF16 ? 2 : 4, gs = grad_dt == VCE_BF16 ? 2 : 4;
-    if (!fits_bytes(T, ld, es) || !fits_bytes(T, ld_grad, gs)) return VCE_ERR_SHAPE;
-    if (!aligned(logits, es) || !aligned(grad_logits, gs) || !aligned(labels, 8) || !aligned(row_stats, 16) ||
-        !aligned(grad_output, 4))
-        return VCE_ERR_ALIGN;
-    if ((rc = require_sm100())) return rc;
-    SegTable tab{};
-    tab.k = 1;
-    tab.T = T;
-    tab.in[0] = logits;
-    tab.out[0] = grad_logits;
-    tab.width[0] = V;
-    tab.off[0] = 0;
-    tab.ld_in[0] = ld;
-    tab.ld_out[0] = ld_grad;
-    const int nt = pick_threads(V * (int64_t)es);
-    if (dispatch_bwd(dt, grad_dt, nt, tab, labels, row_stats, grad_output, red == VCE_RED_NONE, s) != cudaSuccess)
-        return VCE_ERR_CUDA;
-    return VCE_OK;
-}
-
 extern "C" int ce_merge_chunks(int k, const void* const* chunk_logits, const int64_t* chunk_width,
                                const int64_t* chunk_ld, vce_dtype dt, int64_t T, const int64_t* labels,
                                int64_t ignore_index, vce_reduction red, float* loss_rows, float* loss_out,
@@ -576,7 +567,7 @@ extern "C" int ce_merge_chunks(int k, const void* const* chunk_logits, const int
         return VCE_ERR_CUDA;
     if (chunk_grads && T > 0) {
         const int nt = pick_threads(max_w * (int64_t)es);
-        if (dispatch_bwd(dt, grad_dt, nt, tab, labels, row_stats, grad_output, red == VCE_RED_NONE, s) != cudaSuccess)
+        if (launch_ce_bwd(dt, grad_dt, nt, tab, labels, row_stats, grad_output, red == VCE_RED_NONE, s) != cudaSuccess)
             return VCE_ERR_CUDA;
     }
     return VCE_OK;

@@ -1,0 +1,47 @@
+// Row segments shared by the CE kernels: a table of up to VCE_MAX_CHUNKS column chunks
+// (input pointer, output pointer, width, global column offset, leading dimensions), passed
+// to kernels by value as a __grid_constant__ parameter, and the launch-shape helpers.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <algorithm>
+
+#include "vce.h"
+#include "vce_host.h"
+
+namespace vce {
+
+struct SegTable {
+    int k;
+    int64_t T;
+    const void* in[VCE_MAX_CHUNKS];
+    void* out[VCE_MAX_CHUNKS];
+    int64_t width[VCE_MAX_CHUNKS];
+    int64_t off[VCE_MAX_CHUNKS];
+    int64_t ld_in[VCE_MAX_CHUNKS];
+    int64_t ld_out[VCE_MAX_CHUNKS];
+};
+
+inline int pick_threads(int64_t row_bytes) {
+    if (row_bytes <= 8 * 1024) return 128;
+    if (row_bytes <= 64 * 1024) return 256;
+    return 512;
+}
+
+template <typename K>
+inline int grid_for(K kernel, int nt, int64_t items) {
+    const int sms = device_sm_count();
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, nt, 0) != cudaSuccess || per_sm < 1)
+        per_sm = 1;
+    const int64_t g = std::min<int64_t>(items, (int64_t)sms * per_sm);
+    return (int)std::max<int64_t>(g, 1);
+}
+
+// The gradient of every (chunk, row) segment of `tab` (ce_bwd.cu).
+cudaError_t launch_ce_bwd(vce_dtype dt, vce_dtype gdt, int nt, const SegTable& tab, const int64_t* labels,
+                          const float* row_stats, const float* grad_output, int go_per_row, cudaStream_t s);
+
+}  // namespace vce

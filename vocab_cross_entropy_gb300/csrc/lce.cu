@@ -66,7 +66,7 @@ struct EpiStats {
         r.t = row < p.T ? p.labels[row] : p.ignore_index;
         if (r.t == p.ignore_index) r.t = -1;
     }
-    __device__ __forceinline__ static void consume(const Params& p, Row& r, int, int col0, const uint32_t (&acc)[32]) {
+    __device__ __forceinline__ static void consume(const Params& p, Row& r, int, int col0, const uint32_t (&acc)[32], uint8_t*) {
         float v[32];
 #pragma unroll
         for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(acc[k]);
@@ -125,8 +125,10 @@ struct EpiGrad {
             }
         }
     }
+    // staging row pitch in uint16: 80 bytes, so 16-byte reads of 8 consecutive rows hit 8 distinct bank quads
+    static constexpr int kStageLd = 40;
     __device__ __forceinline__ static void consume(const Params& p, Row& r, int row, int col0,
-                                                   const uint32_t (&acc)[32]) {
+                                                   const uint32_t (&acc)[32], uint8_t* wsm) {
         uint32_t hi[16], lo[16];
 #pragma unroll
         for (int k = 0; k < 32; k += 2) {
@@ -152,15 +154,29 @@ struct EpiGrad {
             dh[q] = make_uint4(hi[4 * q], hi[4 * q + 1], hi[4 * q + 2], hi[4 * q + 3]);
             dl[q] = make_uint4(lo[4 * q], lo[4 * q + 1], lo[4 * q + 2], lo[4 * q + 3]);
         }
-        // transposed [width_pad][ldt]: for each column the warp writes 32 consecutive rows
+        // transposed [width_pad][ldt]: stage the warp's 32 rows x 32 columns in shared memory,
+        // then each lane writes 64 contiguous bytes (32 rows) of one column
+        uint16_t* sh = reinterpret_cast<uint16_t*>(wsm);          // [32 cols][kStageLd] hi
+        uint16_t* sl = sh + 32 * kStageLd;                         // lo
+        const int lane = threadIdx.x & 31;
 #pragma unroll
         for (int k = 0; k < 32; ++k) {
             const uint32_t h = hi[k / 2], l = lo[k / 2];
-            const uint16_t hv = (k & 1) ? (uint16_t)(h >> 16) : (uint16_t)(h & 0xFFFFu);
-            const uint16_t lv = (k & 1) ? (uint16_t)(l >> 16) : (uint16_t)(l & 0xFFFFu);
-            p.gt_hi[(int64_t)(col0 + k) * p.ldt + row] = hv;
-            p.gt_lo[(int64_t)(col0 + k) * p.ldt + row] = lv;
+            sh[k * kStageLd + lane] = (k & 1) ? (uint16_t)(h >> 16) : (uint16_t)(h & 0xFFFFu);
+            sl[k * kStageLd + lane] = (k & 1) ? (uint16_t)(l >> 16) : (uint16_t)(l & 0xFFFFu);
         }
+        __syncwarp();
+        const int row0 = row - lane;
+        const uint4* rh = reinterpret_cast<const uint4*>(sh + lane * kStageLd);
+        const uint4* rl = reinterpret_cast<const uint4*>(sl + lane * kStageLd);
+        uint4* th = reinterpret_cast<uint4*>(p.gt_hi + (int64_t)(col0 + lane) * p.ldt + row0);
+        uint4* tl = reinterpret_cast<uint4*>(p.gt_lo + (int64_t)(col0 + lane) * p.ldt + row0);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            th[q] = rh[q];
+            tl[q] = rl[q];
+        }
+        __syncwarp();
     }
     __device__ __forceinline__ static void end(const Params&, Row&, int, int) {}
 };
@@ -174,7 +190,7 @@ struct EpiStore {
     };
     struct Row {};
     __device__ __forceinline__ static void begin(const Params&, Row&, int, int) {}
-    __device__ __forceinline__ static void consume(const Params& p, Row&, int row, int col0, const uint32_t (&acc)[32]) {
+    __device__ __forceinline__ static void consume(const Params& p, Row&, int row, int col0, const uint32_t (&acc)[32], uint8_t*) {
         if (row >= p.rows || col0 >= p.cols) return;
         const int64_t base = (p.row_off + row) * p.ld + col0;
         const int n = (p.cols - col0) < 32 ? (int)(p.cols - col0) : 32;
@@ -188,7 +204,9 @@ struct EpiStore {
 #pragma unroll
                 for (int q = 0; q < 4; ++q) d[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
             } else {
-                for (int k = 0; k < n; ++k) o[k] = to_bf16(__uint_as_float(acc[k]));
+#pragma unroll
+                for (int k = 0; k < 32; ++k)
+                    if (k < n) o[k] = to_bf16(__uint_as_float(acc[k]));
             }
         } else {
             float* o = reinterpret_cast<float*>(p.out) + base;
@@ -197,7 +215,9 @@ struct EpiStore {
 #pragma unroll
                 for (int q = 0; q < 8; ++q) d[q] = make_uint4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
             } else {
-                for (int k = 0; k < n; ++k) o[k] = __uint_as_float(acc[k]);
+#pragma unroll
+                for (int k = 0; k < 32; ++k)
+                    if (k < n) o[k] = __uint_as_float(acc[k]);
             }
         }
     }
@@ -216,61 +236,111 @@ struct EpiKahan {
     };
     struct Row {};
     __device__ __forceinline__ static void begin(const Params&, Row&, int, int) {}
-    __device__ __forceinline__ static void consume(const Params& p, Row&, int row, int col0, const uint32_t (&acc)[32]) {
+    // a + x = t + e exactly (Knuth's two-sum); the compensation accumulates e
+    __device__ __forceinline__ static void two_sum(float a, float x, float& t, float& e) {
+        t = a + x;
+        const float bp = t - a;
+        e = (a - (t - bp)) + (x - bp);
+    }
+    __device__ __forceinline__ static void put(const Params& p, int64_t i, float s, float c) {
+        if (p.last) {
+            const float v = s + c;
+            if (p.bf16)
+                reinterpret_cast<uint16_t*>(p.out)[i] = to_bf16(v);
+            else
+                reinterpret_cast<float*>(p.out)[i] = v;
+        } else {
+            p.sum[i] = s;
+            p.comp[i] = c;
+        }
+    }
+    __device__ __forceinline__ static void consume(const Params& p, Row&, int row, int col0, const uint32_t (&acc)[32],
+                                                   uint8_t*) {
         if (row >= p.rows || col0 >= p.cols) return;
         const int64_t base = (int64_t)row * p.cols + col0;
-        const int n = (p.cols - col0) < 32 ? (int)(p.cols - col0) : 32;
-        float s[32], c[32];
-        if (p.first) {
+        if (p.cols - col0 >= 32) {   // full 32-column piece: 16-byte accesses
 #pragma unroll
-            for (int k = 0; k < 32; ++k) {
-                s[k] = __uint_as_float(acc[k]);
-                c[k] = 0.f;
+            for (int q = 0; q < 8; ++q) {
+                float s[4], c[4];
+                const float x[4] = {__uint_as_float(acc[4 * q]), __uint_as_float(acc[4 * q + 1]),
+                                    __uint_as_float(acc[4 * q + 2]), __uint_as_float(acc[4 * q + 3])};
+                if (p.first) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) { s[e] = x[e]; c[e] = 0.f; }
+                } else {
+                    const float4 a = *reinterpret_cast<const float4*>(p.sum + base + 4 * q);
+                    const float4 k = *reinterpret_cast<const float4*>(p.comp + base + 4 * q);
+                    const float av[4] = {a.x, a.y, a.z, a.w}, kv[4] = {k.x, k.y, k.z, k.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        float err;
+                        two_sum(av[e], x[e], s[e], err);
+                        c[e] = kv[e] + err;
+                    }
+                }
+                if (p.last) {
+                    if (p.bf16) {
+                        uint2 w = make_uint2(pack_bf16x2(s[0] + c[0], s[1] + c[1]), pack_bf16x2(s[2] + c[2], s[3] + c[3]));
+                        *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(p.out) + base + 4 * q) = w;
+                    } else {
+                        *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + base + 4 * q) =
+                            make_float4(s[0] + c[0], s[1] + c[1], s[2] + c[2], s[3] + c[3]);
+                    }
+                } else {
+                    *reinterpret_cast<float4*>(p.sum + base + 4 * q) = make_float4(s[0], s[1], s[2], s[3]);
+                    *reinterpret_cast<float4*>(p.comp + base + 4 * q) = make_float4(c[0], c[1], c[2], c[3]);
+                }
             }
-        } else {
-            for (int k = 0; k < n; ++k) {
-                const float x = __uint_as_float(acc[k]);
-                const float a = p.sum[base + k];
-                const float t = a + x;
-                const float bp = t - a;
-                const float e = (a - (t - bp)) + (x - bp);   // exact rounding error of a + x
-                s[k] = t;
-                c[k] = p.comp[base + k] + e;
-            }
+            return;
         }
-        if (p.last) {
-            if (p.bf16) {
-                uint16_t* o = reinterpret_cast<uint16_t*>(p.out) + base;
-                for (int k = 0; k < n; ++k) o[k] = to_bf16(s[k] + c[k]);
-            } else {
-                float* o = reinterpret_cast<float*>(p.out) + base;
-                for (int k = 0; k < n; ++k) o[k] = s[k] + c[k];
+        const int n = (int)(p.cols - col0);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+            if (k >= n) break;
+            const float x = __uint_as_float(acc[k]);
+            float sv = x, cv = 0.f;
+            if (!p.first) {
+                float err;
+                two_sum(p.sum[base + k], x, sv, err);
+                cv = p.comp[base + k] + err;
             }
-        } else {
-            for (int k = 0; k < n; ++k) {
-                p.sum[base + k] = s[k];
-                p.comp[base + k] = c[k];
-            }
+            put(p, base + k, sv, cv);
         }
     }
     __device__ __forceinline__ static void end(const Params&, Row&, int, int) {}
 };
 
 // ------------------------------------------------------------------------------------------
-// transpose [R, C] (ld_in) -> [C, ld_out] with zero padding for R <= r < ld_out
+// transpose [R, C] (ld_in) -> [C, ld_out], rows R <= r < R_pad written as zeros.  64 x 64
+// tiles through shared memory, 16-byte loads and stores (C, ld_in and ld_out multiples of 8,
+// both base pointers 16-byte aligned).
 
-__global__ void k_transpose_bf16(const uint16_t* __restrict__ in, int64_t R, int64_t C, int64_t ld_in,
-                                 uint16_t* __restrict__ out, int64_t R_pad, int64_t ld_out) {
-    __shared__ uint16_t tile[64][65];
+__global__ void __launch_bounds__(256) k_transpose_bf16(const uint16_t* __restrict__ in, int64_t R, int64_t C,
+                                                        int64_t ld_in, uint16_t* __restrict__ out, int64_t R_pad,
+                                                        int64_t ld_out) {
+    __shared__ __align__(16) uint16_t tile[64][72];   // 144-byte rows keep 16-byte alignment
     const int64_t r0 = (int64_t)blockIdx.y * 64, c0 = (int64_t)blockIdx.x * 64;
-    for (int i = threadIdx.y; i < 64; i += blockDim.y) {
-        const int64_t r = r0 + i, c = c0 + threadIdx.x;
-        tile[i][threadIdx.x] = (r < R && c < C) ? in[r * ld_in + c] : (uint16_t)0;
+    const int t = threadIdx.x;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int v = t + h * 256, rr = v >> 3, cv = v & 7;
+        const int64_t r = r0 + rr, c = c0 + cv * 8;
+        uint4 x = make_uint4(0, 0, 0, 0);
+        if (r < R && c < C) x = *reinterpret_cast<const uint4*>(in + r * ld_in + c);
+        *reinterpret_cast<uint4*>(&tile[rr][cv * 8]) = x;
     }
     __syncthreads();
-    for (int i = threadIdx.y; i < 64; i += blockDim.y) {
-        const int64_t c = c0 + i, r = r0 + threadIdx.x;
-        if (c < C && r < R_pad) out[c * ld_out + r] = tile[threadIdx.x][i];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int v = t + h * 256, oc = v >> 3, rv = v & 7;
+        const int64_t c = c0 + oc, r = r0 + rv * 8;
+        if (c < C && r < R_pad) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                w[e] = (uint32_t)tile[rv * 8 + 2 * e][oc] | ((uint32_t)tile[rv * 8 + 2 * e + 1][oc] << 16);
+            *reinterpret_cast<uint4*>(out + c * ld_out + r) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
     }
 }
 
@@ -401,7 +471,7 @@ extern "C" int linear_ce_fwd_bwd(const void* E, const void* W, int64_t T, int64_
 
     // 0. transposes
     {
-        dim3 blk(64, 8);
+        const int blk = 256;
         k_transpose_bf16<<<dim3((unsigned)cdiv(D, 64), (unsigned)cdiv(L.T_pad, 64)), blk, 0, s>>>(
             static_cast<const uint16_t*>(E), T, D, D, Et, L.T_pad, L.T_pad);
         k_transpose_bf16<<<dim3((unsigned)cdiv(D, 64), (unsigned)cdiv(L.V_pad, 64)), blk, 0, s>>>(
@@ -421,7 +491,7 @@ extern "C" int linear_ce_fwd_bwd(const void* E, const void* W, int64_t T, int64_
 
     // 1. forward statistics over the whole vocabulary
     {
-        tc::GemmArgs g{tiles_t, (int)L.tiles_v, nkD, nkD, 0, 0, 0, status};
+        tc::GemmArgs g{tiles_t, (int)L.tiles_v, nkD, nkD, 0, 0, 0, 0, status};
         EpiStats::Params ep{labels, ignore_index, T, V, reinterpret_cast<float4*>(part)};
         if (run_gemm<EpiStats>(mE, mE, mW, g, ep, s) != cudaSuccess) return VCE_ERR_CUDA;
         if (launch_stats_merge(part, (int)L.tiles_v, T, V, labels, ignore_index, loss_rows, stats, status, s) !=
@@ -439,20 +509,20 @@ extern "C" int linear_ce_fwd_bwd(const void* E, const void* W, int64_t T, int64_
         const int64_t width = std::min<int64_t>(L.Vc, V - off);
         const int64_t width_pad = round_up(width, BN);
         {
-            tc::GemmArgs g{tiles_t, (int)(width_pad / BN), nkD, nkD, 0, 0, (int)off, status};
+            tc::GemmArgs g{tiles_t, (int)(width_pad / BN), nkD, nkD, 0, 0, (int)off, 0, status};
             EpiGrad::Params ep{labels, T, width, off, reinterpret_cast<const float4*>(stats), grad_output,
                                red == VCE_RED_NONE, ghi, glo, gthi, gtlo, L.Vc, L.T_pad};
             if (run_gemm<EpiGrad>(mE, mE, mW, g, ep, s) != cudaSuccess) return VCE_ERR_CUDA;
         }
         {   // dW[off : off + width] = G^T E, K = 2 T_pad (hi then lo)
             const int nkT = (int)(L.T_pad / BK);
-            tc::GemmArgs g{(int)(width_pad / BM), (int)cdiv(D, BN), 2 * nkT, nkT, 0, 0, 0, status};
+            tc::GemmArgs g{(int)(width_pad / BM), (int)cdiv(D, BN), 2 * nkT, nkT, 0, 0, 0, 1, status};
             EpiStore::Params ep{dW, D, width, D, off, grad_dt == VCE_BF16};
             if (run_gemm<EpiStore>(mGthi, mGtlo, mEt, g, ep, s) != cudaSuccess) return VCE_ERR_CUDA;
         }
         {   // dE += G W[off : off + width], K = 2 width (hi then lo)
             const int nkc = (int)cdiv(width, BK);
-            tc::GemmArgs g{tiles_t, (int)cdiv(D, BN), 2 * nkc, nkc, (int)off, 0, 0, status};
+            tc::GemmArgs g{tiles_t, (int)cdiv(D, BN), 2 * nkc, nkc, (int)off, 0, 0, 1, status};
             EpiKahan::Params ep{dsum, dcomp, T, D, ci == 0, ci == nchunks - 1, dE, grad_dt == VCE_BF16};
             if (run_gemm<EpiKahan>(mGhi, mGlo, mWt, g, ep, s) != cudaSuccess) return VCE_ERR_CUDA;
         }

@@ -19,6 +19,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "vce_async.cuh"
+
 namespace vce {
 namespace tc {
 
@@ -29,75 +31,11 @@ constexpr int B_BYTES = BN * BK * 2;   // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int TMEM_COLS = 2 * BN;      // two fp32 accumulators of 128 lanes x 256 columns
 constexpr int kThreads = 256;
-constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s: far beyond any legitimate wait
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+constexpr int EPI_WARP_BYTES = 5120;   // per epilogue warp: staging space an epilogue may use
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 4 * EPI_WARP_BYTES + 1024 /*align*/ + 256 /*barriers*/;
 
 // error codes written to the kernel's error word when a wait gives up
 enum { kErrWaitEmpty = 101, kErrWaitFull = 102, kErrWaitAccFree = 103, kErrWaitAccFull = 104 };
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ uint64_t globaltimer() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
-}
-__device__ __forceinline__ void fence_mbar_init() {
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// Wait for the phase of `bar` with the given parity to complete.  Gives up after kWaitNs or
-// as soon as another role of the block has given up; returns false then.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          int32_t* err, int code) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer();
-    while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if (*abort_flag) return false;
-        if (globaltimer() - t0 > kWaitNs) {
-            *abort_flag = 1;
-            if (err) atomicCAS(err, 0, code);
-            return false;
-        }
-    }
-}
-
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-            smem_u32(dst)),
-        "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
-        : "memory");
-}
-
-__device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
-    asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
-}
 
 // ---- tcgen05 ------------------------------------------------------------------------------
 
@@ -171,8 +109,20 @@ struct GemmArgs {
     int nk_a0;              // the first nk_a0 blocks read A0, the rest A1 (K restarts at 0 for A1)
     int b_x0;               // B's K coordinate of block kb is b_x0 + (kb mod nk_a0) * BK
     int a_y0, b_y0;         // row offsets of the A and B tiles
+    int n_fastest;          // tile order: 0 = m fastest (blocks in flight share B tiles),
+                            //             1 = n fastest (blocks in flight share A tiles)
     int32_t* err;           // error word (wait timeouts)
 };
+
+__device__ __forceinline__ void tile_coords(const GemmArgs& g, int tile, int& tm, int& tn) {
+    if (g.n_fastest) {
+        tn = tile % g.tiles_n;
+        tm = tile / g.tiles_n;
+    } else {
+        tm = tile % g.tiles_m;
+        tn = tile / g.tiles_m;
+    }
+}
 
 template <class Epi>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -182,7 +132,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* smA = smem;
     uint8_t* smB = smem + STAGES * A_BYTES;
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+    uint8_t* epi_smem = smem + STAGES * STAGE_BYTES;
+    uint64_t* full = reinterpret_cast<uint64_t*>(epi_smem + 4 * EPI_WARP_BYTES);
     uint64_t* empty = full + STAGES;
     uint64_t* acc_full = empty + STAGES;
     uint64_t* acc_free = acc_full + 2;
@@ -223,7 +174,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t phase = 0;
         int issued = 0;   // stages whose copies were issued and not yet known complete
         for (int tile = blockIdx.x; tile < ntiles && !*abort_flag; tile += gridDim.x) {
-            const int tm = tile % g.tiles_m, tn = tile / g.tiles_m;
+            int tm, tn;
+            tile_coords(g, tile, tm, tn);
             for (int kb = 0; kb < g.nk; ++kb) {
                 if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, g.err, kErrWaitEmpty)) break;
                 mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
@@ -288,7 +240,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
             if (!mbar_wait(&acc_full[acc], acc_phase, abort_flag, g.err, kErrWaitAccFull)) break;
             tc_fence_after();
-            const int tm = tile % g.tiles_m, tn = tile / g.tiles_m;
+            int tm, tn;
+            tile_coords(g, tile, tm, tn);
             const int row = tm * BM + sub * 32 + lane;
             typename Epi::Row st;
             Epi::begin(ep, st, row, tn);
@@ -298,7 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t r[32];
                 tmem_ld32(t0 + (uint32_t)(c * 32), r);
                 tmem_wait_ld();
-                Epi::consume(ep, st, row, tn * BN + c * 32, r);
+                Epi::consume(ep, st, row, tn * BN + c * 32, r, epi_smem + sub * EPI_WARP_BYTES);
             }
             Epi::end(ep, st, row, tn);
             tc_fence_before();
