@@ -42,7 +42,9 @@ constexpr int kUnroll = 4;
 // the local target column `tl` (tl < 0 or >= w: no target here).  The thread that meets the
 // target column stores its value to *zt_out.
 
-template <typename S, int NT>
+// kLazy: sum against a lazily updated reference (ms_push_lazy); otherwise m ends as the exact
+// maximum of the non-target values (ms_push), as the chunk statistics report it.
+template <typename S, int NT, bool kLazy>
 __device__ __forceinline__ void fwd_segment(const S* __restrict__ row, int64_t w, int64_t tl, float& m,
                                             float& s, float& mb, float* zt_out) {
     constexpr int G = Elt<S>::kGroup;
@@ -85,7 +87,10 @@ __device__ __forceinline__ void fwd_segment(const S* __restrict__ row, int64_t w
                     for (int k = 0; k < G; ++k)
                         if (rel == (uint64_t)k) { *zt_out = v[k]; v[k] = -kInf; }
                 }
-                ms_push<G>(v, m, s, mb);
+                if (kLazy)
+                    ms_push_lazy<G>(v, m, s, mb);
+                else
+                    ms_push<G>(v, m, s, mb);
             }
         }
     }
@@ -131,7 +136,7 @@ __global__ void __launch_bounds__(NT) k_ce_fwd(const S* __restrict__ logits, int
             continue;
         }
         float m = -kInf, s = 0.f, mb = 0.f;
-        fwd_segment<S, NT>(logits + row * ld, V, t, m, s, mb, &sm_zt);
+        fwd_segment<S, NT, true>(logits + row * ld, V, t, m, s, mb, &sm_zt);
         ms_block_reduce<NT>(m, s, sm_m, sm_s);   // contains the barrier that publishes sm_zt
         if (threadIdx.x == 0) {
             float loss;
@@ -247,7 +252,7 @@ __global__ void __launch_bounds__(kRingThreads, 1)
                     for (int k = 0; k < G; ++k)
                         if (rel == (uint64_t)k) { red_zt[p] = x[k]; x[k] = -kInf; }
                 }
-                ms_push<G>(x, m, s, mb);
+                ms_push_lazy<G>(x, m, s, mb);
             }
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&empty[stage]);
@@ -349,7 +354,7 @@ __global__ void __launch_bounds__(NT) k_ce_chunk_fwd(const __grid_constant__ Seg
         if (threadIdx.x == 0) sm_zt = 0.f;
         __syncthreads();
         float m = -kInf, s = 0.f, mb = 0.f;
-        fwd_segment<S, NT>(reinterpret_cast<const S*>(tab.in[c]) + row * tab.ld_in[c], w, owner ? tl : -1, m, s, mb,
+        fwd_segment<S, NT, false>(reinterpret_cast<const S*>(tab.in[c]) + row * tab.ld_in[c], w, owner ? tl : -1, m, s, mb,
                            &sm_zt);
         ms_block_reduce<NT>(m, s, sm_m, sm_s);
         if (threadIdx.x == 0)

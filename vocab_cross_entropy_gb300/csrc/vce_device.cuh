@@ -131,10 +131,12 @@ struct GroupStore<float, 8> {      // 2 x 16 B
 
 // ---- (max, sum-exp) pairs ------------------------------------------------------------------
 //
-// A pair (m, s) stands for the multiset sum  s * e^m = sum_k e^{v_k}  with m the largest
-// v_k seen.  The empty set (or a set of -inf only) is (-inf, 0).
+// A pair (m, s) stands for the multiset sum  s * e^m = sum_k e^{v_k}, with m one of the v_k
+// (the largest, for ms_push; a running reference within ~22 of the largest, for
+// ms_push_lazy), so s >= 1 and no term overflows.  The empty set (or a set of -inf only) is
+// (-inf, 0).
 
-// Merge (m2, s2) into (m, s), rescaling both sums to the larger maximum.
+// Merge (m2, s2) into (m, s), rescaling both sums to the larger reference.
 __device__ __forceinline__ void ms_merge(float& m, float& s, float m2, float s2) {
     const float M = fmaxf(m, m2);
     const float a = (m == M) ? 1.f : ex2((m - M) * kLog2e);    // also covers m = m2 = -inf
@@ -162,6 +164,36 @@ __device__ __forceinline__ void ms_push(const float (&v)[G], float& m, float& s,
 #pragma unroll
         for (int k = 0; k + w < G; k += 2 * w) e[k] += e[k + w];
     s += e[0];
+}
+
+// Add G values against a lazily updated reference.  The pair (m, s) only needs m to be one
+// of the values seen (so s >= 1) and no term to overflow, not m to be the exact maximum:
+// the first group of a thread sets m to that group's maximum, and later groups are summed
+// against it unless a term reaches 2^32 (a value ~22 above m), which triggers a rescale to
+// the new maximum.  This drops the per-group max (G-1 FMNMX + a compare) from the common
+// path; the result is the same sum, s rounded in the same fp32 steps up to the reference.
+template <int G>
+__device__ __forceinline__ void ms_push_lazy(const float (&v)[G], float& m, float& s, float& mb) {
+    if (m == -kInf) {   // first finite group of this thread: take its exact maximum as reference
+        float vm = v[0];
+#pragma unroll
+        for (int k = 1; k < G; ++k) vm = fmaxf(vm, v[k]);
+        if (vm == -kInf) return;
+        m = vm;
+        mb = m * kLog2e;
+    }
+    float e[G];
+#pragma unroll
+    for (int k = 0; k < G; ++k) e[k] = ex2(fmaf(v[k], kLog2e, -mb));
+#pragma unroll
+    for (int w = 1; w < G; w *= 2)
+#pragma unroll
+        for (int k = 0; k + w < G; k += 2 * w) e[k] += e[k + w];
+    if (e[0] < 4294967296.f) {   // 2^32: no term can have overflowed
+        s += e[0];
+        return;
+    }
+    ms_push<G>(v, m, s, mb);   // rare: a value far above the reference; redo this group exactly
 }
 
 __device__ __forceinline__ void ms_push1(float v, float& m, float& s, float& mb) {
