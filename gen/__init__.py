@@ -6,8 +6,7 @@ library is measured and checked on, from the counter-based generator in
 ``vce_gen.c``.  Every matrix row is a pure function of (seed, stream, row), so a
 test can regenerate just the rows it checks.
 
-Workloads (sizes and value distributions of the pages' problems; see the design doc
-for the recipe):
+Workloads (sizes and value distributions of the pages' problems):
 
   tiny     T=64,    V=1000,   fp32 logits ~N(0, 3^2), 8 rows with the target
            raised to max(row)+U[20,40], 4 ignored rows

@@ -17,7 +17,7 @@ which is -log p_t exactly.  With x = L' - z_t (L' the target-excluded log-sum-ex
 The page's branch between p_t - 1 and -p_non_target is an fp32 device: in fp64
 both are -sigmoid(x) to ~1e-16, so the oracle takes -sigmoid(x) (stable form).
 
-Readings where the pages leave a step open (each listed in the design doc):
+Readings where the pages leave a step open:
   * ignored rows (label == ignore_index, -100 by default) give loss 0 and gradient
     +0.0 by selection, whatever the logits hold (torchtitan page: "Ignored labels
     act as targets on no shard ... zeroed by the label mask");

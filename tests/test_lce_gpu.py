@@ -3,7 +3,7 @@
 dE and dW are sums over T or V products; they are graded as bf16 outputs against the
 oracle rounded once to bf16 (one ulp), except that an entry whose sum cancels (small
 |sum| against sum |terms|) may instead be within 2^-14 * sum |terms| of the fp64 value,
-the accumulation error an fp32 sum of these lengths can carry (see DESIGN.md).
+the accumulation error an fp32 sum of these lengths can carry.
 """
 import numpy as np
 import pytest
