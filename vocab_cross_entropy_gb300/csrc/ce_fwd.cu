@@ -18,7 +18,7 @@
 //                   then loss and row statistics
 //   k_ce_reduce     one block: fixed-order fp64 sum of the losses, N, and 1/N weights
 //   k_ce_bwd        (ce_bwd.cu) one (chunk, row) segment per block iteration: the gradient
-//   k_ce_chunk_fwd  one (chunk, row) segment per block iteration: chunk statistics
+//   k_ce_chunk_fwd  one (chunk, row) segment per warp: chunk statistics
 //   k_ce_merge      one row per thread: merge the chunk statistics, then as k_ce_fwd
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -44,9 +44,8 @@ constexpr int kUnroll = 4;
 // maximum of the non-target values (ms_push), as the chunk statistics report it.
 template <typename S, int NT, bool kLazy>
 __device__ __forceinline__ void fwd_segment(const S* __restrict__ row, int64_t w, int64_t tl, float& m,
-                                            float& s, float& mb, float* zt_out) {
+                                            float& s, float& mb, float* zt_out, const int tid) {
     constexpr int G = Elt<S>::kGroup;
-    const int tid = threadIdx.x;
     const uintptr_t a = reinterpret_cast<uintptr_t>(row);
     int64_t h = (int64_t)(((16 - (a & 15)) & 15) / sizeof(S));   // elements before 16-B alignment
     if (h > w) h = w;
@@ -136,7 +135,7 @@ __global__ void __launch_bounds__(NT, 1536 / NT) k_ce_fwd(const S* __restrict__ 
             continue;
         }
         float m = -kInf, s = 0.f, mb = 0.f;
-        fwd_segment<S, NT, true>(logits + row * ld, V, t, m, s, mb, &sm_zt);
+        fwd_segment<S, NT, true>(logits + row * ld, V, t, m, s, mb, &sm_zt, threadIdx.x);
         ms_block_reduce<NT>(m, s, sm_m, sm_s);   // contains the barrier that publishes sm_zt
         if (threadIdx.x == 0) {
             float loss;
@@ -202,29 +201,35 @@ __global__ void __launch_bounds__(NT) k_ce_reduce(const float* __restrict__ loss
 // ------------------------------------------------------------------------------------------
 // Vocabulary chunks: per-(chunk, row) statistics, then a per-row merge.
 
-template <typename S, int NT>
-__global__ void __launch_bounds__(NT) k_ce_chunk_fwd(const __grid_constant__ SegTable tab,
-                                                     const int64_t* __restrict__ labels, int64_t ignore_index,
-                                                     float4* __restrict__ chunk_stats) {
-    __shared__ float sm_m[NT / 32], sm_s[NT / 32];
-    __shared__ float sm_zt;
+// One warp per (chunk, row) item, items row-major over chunks: a chunk row (32 KB for the
+// pages' 8 chunks) is too short to amortise block barriers, so each warp streams its item
+// and reduces with shuffles only.  The maximum is exact (ms_push), as the statistics report it.
+constexpr int kChunkThreads = 512;
+
+template <typename S>
+__global__ void __launch_bounds__(kChunkThreads, 2) k_ce_chunk_fwd(const __grid_constant__ SegTable tab,
+                                                                   const int64_t* __restrict__ labels,
+                                                                   int64_t ignore_index,
+                                                                   float4* __restrict__ chunk_stats) {
+    const int lane = threadIdx.x & 31;
     const int64_t items = tab.T * tab.k;
-    for (int64_t it = blockIdx.x; it < items; it += gridDim.x) {
+    const int64_t warps = (int64_t)gridDim.x * (kChunkThreads / 32);
+    for (int64_t it = (int64_t)blockIdx.x * (kChunkThreads / 32) + (threadIdx.x >> 5); it < items; it += warps) {
         const int64_t row = it / tab.k;
         const int c = (int)(it - row * tab.k);
         const int64_t t = labels[row];
         const int64_t w = tab.width[c];
         const int64_t tl = (t == ignore_index) ? -1 : t - tab.off[c];
         const bool owner = (tl >= 0 && tl < w);
-        if (threadIdx.x == 0) sm_zt = 0.f;
-        __syncthreads();
-        float m = -kInf, s = 0.f, mb = 0.f;
-        fwd_segment<S, NT, false>(reinterpret_cast<const S*>(tab.in[c]) + row * tab.ld_in[c], w, owner ? tl : -1, m, s, mb,
-                           &sm_zt);
-        ms_block_reduce<NT>(m, s, sm_m, sm_s);
-        if (threadIdx.x == 0)
-            chunk_stats[(int64_t)c * tab.T + row] = make_float4(m, s, owner ? sm_zt : 0.f, owner ? 1.f : 0.f);
-        __syncthreads();
+        float m = -kInf, s = 0.f, mb = 0.f, zt = 0.f;
+        float zt_found = kInf;   // stays +inf except in the lane that meets the target
+        fwd_segment<S, 32, false>(reinterpret_cast<const S*>(tab.in[c]) + row * tab.ld_in[c], w, owner ? tl : -1, m,
+                                  s, mb, &zt_found, lane);
+        ms_warp_reduce(m, s);
+        const unsigned hit = __ballot_sync(0xFFFFFFFFu, zt_found != kInf);
+        if (hit) zt = __shfl_sync(0xFFFFFFFFu, zt_found, __ffs(hit) - 1);
+        if (lane == 0)
+            chunk_stats[(int64_t)c * tab.T + row] = make_float4(m, s, owner ? zt : 0.f, owner ? 1.f : 0.f);
     }
 }
 
@@ -264,10 +269,12 @@ cudaError_t launch_fwd(const void* logits, int64_t T, int64_t V, int64_t ld, con
     return cudaGetLastError();
 }
 
-template <typename S, int NT>
+template <typename S>
 cudaError_t launch_chunk_fwd(const SegTable& tab, const int64_t* labels, int64_t ig, float* ws, cudaStream_t s) {
-    auto kern = k_ce_chunk_fwd<S, NT>;
-    kern<<<grid_for(kern, NT, tab.T * tab.k), NT, 0, s>>>(tab, labels, ig, reinterpret_cast<float4*>(ws));
+    auto kern = k_ce_chunk_fwd<S>;
+    const int64_t blocks_needed = (tab.T * tab.k + kChunkThreads / 32 - 1) / (kChunkThreads / 32);
+    kern<<<grid_for(kern, kChunkThreads, blocks_needed), kChunkThreads, 0, s>>>(tab, labels, ig,
+                                                                               reinterpret_cast<float4*>(ws));
     return cudaGetLastError();
 }
 
@@ -279,13 +286,6 @@ cudaError_t dispatch_fwd(int nt, const void* logits, int64_t T, int64_t V, int64
     return launch_fwd<S, 512>(logits, T, V, ld, labels, ig, lr, rs, st, s);
 }
 
-template <typename S>
-cudaError_t dispatch_chunk_fwd(int nt, const SegTable& tab, const int64_t* labels, int64_t ig, float* ws,
-                               cudaStream_t s) {
-    if (nt == 128) return launch_chunk_fwd<S, 128>(tab, labels, ig, ws, s);
-    if (nt == 256) return launch_chunk_fwd<S, 256>(tab, labels, ig, ws, s);
-    return launch_chunk_fwd<S, 512>(tab, labels, ig, ws, s);
-}
 
 cudaError_t launch_reduce(const float* loss_rows, const int64_t* labels, int64_t T, int64_t V, int64_t ig, int red,
                           float* loss_out, float* row_stats, cudaStream_t s) {
@@ -402,9 +402,8 @@ extern "C" int ce_merge_chunks(int k, const void* const* chunk_logits, const int
     if ((rc = require_sm100())) return rc;
     if (cudaMemsetAsync(status, 0, sizeof(int32_t), s) != cudaSuccess) return VCE_ERR_CUDA;
     if (T > 0) {
-        const int nt = pick_threads(max_w * (int64_t)es);
-        cudaError_t e = dt == VCE_BF16 ? dispatch_chunk_fwd<uint16_t>(nt, tab, labels, ignore_index, chunk_stats_ws, s)
-                                       : dispatch_chunk_fwd<float>(nt, tab, labels, ignore_index, chunk_stats_ws, s);
+        cudaError_t e = dt == VCE_BF16 ? launch_chunk_fwd<uint16_t>(tab, labels, ignore_index, chunk_stats_ws, s)
+                                       : launch_chunk_fwd<float>(tab, labels, ignore_index, chunk_stats_ws, s);
         if (e != cudaSuccess) return VCE_ERR_CUDA;
         const int mt = 256;
         const int mg = (int)std::min<int64_t>((T + mt - 1) / mt, (int64_t)device_sm_count() * 8);
