@@ -244,6 +244,28 @@ class CEWorkload:
                 "l2": "no flush: inputs (%.2f GB logits) larger than the 129 MB L2" % (p.T * p.V * 2 / 1e9)}
 
 
+class FusedWorkload(CEWorkload):
+    """The pages' shape through ce_forward_backward: one pass over the logits per step."""
+
+    def __init__(self, problem, device):
+        super().__init__(problem, device)
+        self.launches_per_step = 3            # k_ce_count_valid, k_ce_fused, k_ce_reduce
+
+    def step(self, stream):
+        self.vce.ce_forward_backward(self.logits, self.labels, grad_output=self.go, grad_logits=self.grad,
+                                     loss_rows=self.loss_rows, loss_out=self.loss_out, row_stats=self.stats,
+                                     status=self.status, stream=stream)
+
+    def bytes_fused(self):
+        T, V = self.p.T, self.p.V
+        return self.n_valid * V * 2 + T * V * 2 + T * (8 + 4 + 16 + 8)
+
+    def describe(self):
+        d = super().describe()
+        d["workload"] = d["workload"].replace("CE fwd+bwd", "CE fwd+bwd in one pass (ce_forward_backward)")
+        return d
+
+
 class ChunkedWorkload(CEWorkload):
     """The pages' matrix as 8 column chunks in separate buffers: one ce_merge_chunks call per step."""
 
@@ -447,13 +469,13 @@ def run_ours(args, rank, local_rank, world):
     init_dist(world, "nccl")
     if args.workload == "linear":
         return run_linear(args, rank, local_rank, world, device)
-    problem = {"pages": gen.pages, "chunked": gen.pages, "mid": gen.mid}[args.workload](
+    problem = {"pages": gen.pages, "chunked": gen.pages, "fused": gen.pages, "mid": gen.mid}[args.workload](
         seed=(1002 if args.workload == "mid" else 1003) + rank)
     if args.rows:
         problem = gen.CEProblem(problem.name + f"[{args.rows} rows]", args.rows, problem.V, problem.dtype,
                                 problem.seed, problem.std, round(0.10 * args.rows) if problem.n_margin else 0,
                                 problem.margin_lo, problem.margin_hi, round(problem.n_ignore * args.rows / problem.T))
-    w = (ChunkedWorkload if args.workload == "chunked" else CEWorkload)(problem, device)
+    w = {"chunked": ChunkedWorkload, "fused": FusedWorkload}.get(args.workload, CEWorkload)(problem, device)
     stream = torch.cuda.current_stream(device)
     for _ in range(args.warmup):
         w.step(stream)
@@ -461,7 +483,7 @@ def run_ours(args, rank, local_rank, world):
     with ClockSampler(local_rank) as clk:
         ms = time_steps(w.step, args.steps, stream, world, device)
     clocks = clk.summary()
-    chunked = args.workload == "chunked"
+    chunked = args.workload in ("chunked", "fused")
     if not chunked:
         fwd_ms, bwd_ms = time_kernel(w, max(10, min(args.steps, 50)), stream)
     e2e_steps = max(3, min(args.e2e_steps, args.steps))
@@ -478,7 +500,14 @@ def run_ours(args, rank, local_rank, world):
     e2e_value = tokens_all / (e2e_ms / e2e_steps / 1e3)
     peaks = measured_peaks()
     bwd_bytes = w.bytes_bwd()
-    if chunked:   # one call launches all four kernels: roofline over the whole call
+    if args.workload == "fused":   # one call: the fused kernel plus two one-block kernels
+        call_bytes = w.bytes_fused()
+        achieved = call_bytes / (ms_step / 1e3) / 1e9
+        roof = {"bound": "hbm", "kernel": "ce_forward_backward (k_ce_count_valid + k_ce_fused + k_ce_reduce)",
+                "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(achieved / peaks["hbm_gbs"], 4), "peak_source": peaks["source"],
+                "algorithmic_bytes_per_launch": call_bytes, "traffic": None}
+    elif chunked:   # one call launches all four kernels: roofline over the whole call
         call_bytes = w.bytes_fwd() + bwd_bytes + 2 * w.p.T * gen.CHUNKS * 16
         achieved = call_bytes / (ms_step / 1e3) / 1e9
         roof = {"bound": "hbm", "kernel": "ce_merge_chunks (k_ce_chunk_fwd + k_ce_merge + k_ce_reduce + k_ce_bwd)",
@@ -559,7 +588,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["pages", "chunked", "mid", "linear"], default="pages")
+    ap.add_argument("--workload", choices=["pages", "fused", "chunked", "mid", "linear"], default="pages")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--rows", type=int, default=None,

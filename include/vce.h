@@ -142,6 +142,26 @@ int ce_backward(const void* logits, vce_dtype dt, int64_t T, int64_t V, int64_t 
                 void* grad_logits, vce_dtype grad_dt, int64_t ld_grad, vce_stream_t s);
 
 /*
+ * ce_forward_backward -- ce_forward followed by ce_backward in one pass over the logits, for
+ * callers that know grad_output when the forward runs (e.g. a mean loss seeded by 1).
+ * [TT, Numerics; Memory/perf: the forward prepares the backward]  Same arguments, results
+ * and per-row numerics as the two calls (bitwise equal outputs); each row is read from HBM
+ * once and re-read for its gradient from L2, so HBM moves V*e in and V*e_g out per row.
+ * For reduction MEAN, *loss_out holds 1/N while the call's work runs and the mean loss when
+ * it is done.
+ *
+ *   logits, dt, T, V, ld, labels, ignore_index, red: as ce_forward
+ *   grad_output  fp32 [1] (SUM, MEAN) or [T] (NONE), read on the device
+ *   loss_rows, loss_out, row_stats, status: as ce_forward (row_stats carries the weights)
+ *   grad_logits  [T, ld_grad] of dtype grad_dt, written; must not overlap the logits
+ */
+int ce_forward_backward(const void* logits, vce_dtype dt, int64_t T, int64_t V, int64_t ld,
+                        const int64_t* labels, int64_t ignore_index, vce_reduction red,
+                        const float* grad_output, float* loss_rows, float* loss_out,
+                        float* row_stats, void* grad_logits, vce_dtype grad_dt, int64_t ld_grad,
+                        int32_t* status, vce_stream_t s);
+
+/*
  * ce_merge_chunks -- CE forward (+ backward) over logits held as k column chunks
  * in separate buffers, the single-GPU form of the vocabulary-parallel CE [MC,
  * vocab_parallel_cross_entropy; TT, Numerics: the owner of the target drops it].

@@ -13,7 +13,8 @@ import os
 
 import torch
 
-__all__ = ["VceError", "lib", "library_path", "ce_forward", "ce_backward", "ce_merge_chunks", "ce_merge_chunks_noalloc",
+__all__ = ["VceError", "lib", "library_path", "ce_forward", "ce_backward", "ce_forward_backward", "ce_merge_chunks",
+           "ce_merge_chunks_noalloc",
            "linear_ce_workspace_bytes", "linear_ce_fwd_bwd", "vce_get_status", "vce_status_string",
            "vce_abi_version", "cross_entropy", "IGNORE_INDEX", "F32", "BF16", "RED"]
 
@@ -46,13 +47,15 @@ def _load():
     L.vce_get_status.argtypes = [p, p, p]
     L.ce_forward.argtypes = [p, i32, i64, i64, i64, p, i64, i32, p, p, p, p, p]
     L.ce_backward.argtypes = [p, i32, i64, i64, i64, p, i64, i32, p, p, p, i32, i64, p]
+    L.ce_forward_backward.argtypes = [p, i32, i64, i64, i64, p, i64, i32, p, p, p, p, p, i32, i64, p, p]
     L.ce_merge_chunks.argtypes = [i32, p, p, p, i32, i64, p, i64, i32, p, p, p, p, p, p, i32, p, p, p]
     L.ce_merge_chunks_noalloc.argtypes = [i32, p, p, p, i32, i64, p, i64, i32, p, p, p, p, p, p, i32, p, p]
     if hasattr(L, "linear_ce_fwd_bwd"):
         L.linear_ce_workspace_bytes.argtypes = [i64, i64, i64]
         L.linear_ce_workspace_bytes.restype = sz
         L.linear_ce_fwd_bwd.argtypes = [p, p, i64, i64, i64, p, i64, i32, p, p, p, p, p, i32, p, sz, p, p]
-    for name in ("ce_forward", "ce_backward", "ce_merge_chunks", "ce_merge_chunks_noalloc", "linear_ce_fwd_bwd",
+    for name in ("ce_forward", "ce_backward", "ce_forward_backward", "ce_merge_chunks", "ce_merge_chunks_noalloc",
+                 "linear_ce_fwd_bwd",
                  "vce_get_status"):
         if hasattr(L, name):
             getattr(L, name).restype = i32
@@ -144,6 +147,28 @@ def ce_backward(logits, labels, row_stats, grad_output, ignore_index=IGNORE_INDE
                                           _ptr(grad_logits), _dtype(grad_logits), _ld(grad_logits),
                                           _stream(stream)))
     return grad_logits
+
+
+def ce_forward_backward(logits, labels, ignore_index=IGNORE_INDEX, reduction="mean", *, grad_output=None,
+                        grad_logits=None, grad_dtype=None, loss_rows=None, loss_out=None, row_stats=None,
+                        status=None, stream=None):
+    """Forward and gradient in one pass.  Returns (loss_out, loss_rows, row_stats, grad_logits, status)."""
+    T, V = logits.shape
+    dev = logits.device
+    loss_rows = torch.empty(T, dtype=torch.float32, device=dev) if loss_rows is None else loss_rows
+    row_stats = torch.empty(T, ROW_STATS, dtype=torch.float32, device=dev) if row_stats is None else row_stats
+    status = torch.empty(1, dtype=torch.int32, device=dev) if status is None else status
+    if reduction != "none" and loss_out is None:
+        loss_out = torch.empty(1, dtype=torch.float32, device=dev)
+    if grad_output is None:
+        grad_output = torch.ones(T if reduction == "none" else 1, dtype=torch.float32, device=dev)
+    if grad_logits is None:
+        grad_logits = torch.empty(T, V, dtype=grad_dtype or logits.dtype, device=dev)
+    _check("ce_forward_backward", _get().ce_forward_backward(
+        _ptr(logits), _dtype(logits), T, V, _ld(logits), _ptr(labels), int(ignore_index), RED[reduction],
+        _ptr(grad_output), _ptr(loss_rows), _ptr(loss_out), _ptr(row_stats), _ptr(grad_logits),
+        _dtype(grad_logits), _ld(grad_logits), _ptr(status), _stream(stream)))
+    return loss_out, loss_rows, row_stats, grad_logits, status
 
 
 def ce_merge_chunks(chunks, labels, ignore_index=IGNORE_INDEX, reduction="mean", *, grad_output=None,

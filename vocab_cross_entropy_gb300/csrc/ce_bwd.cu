@@ -15,6 +15,7 @@
 
 #include <algorithm>
 
+#include "ce_rows.cuh"
 #include "ce_segments.h"
 #include "vce.h"
 #include "vce_device.cuh"
@@ -22,69 +23,6 @@
 
 namespace vce {
 namespace {
-
-constexpr int kUnroll = 4;
-
-// ------------------------------------------------------------------------------------------
-// Backward: one row segment.  grad = coef * 2^(z*log2e - bias) off target, gt at the target.
-
-template <typename S, typename O, int NT>
-__device__ __forceinline__ void bwd_segment(const S* __restrict__ row, O* __restrict__ grow, int64_t w, int64_t tl,
-                                            float coef, float bias, float gt, bool zero) {
-    constexpr int G = Elt<S>::kGroup;
-    const int tid = threadIdx.x;
-    const uintptr_t a = reinterpret_cast<uintptr_t>(row);
-    int64_t h = (int64_t)(((16 - (a & 15)) & 15) / sizeof(S));
-    if (h > w) h = w;
-    const bool out_ok = ((reinterpret_cast<uintptr_t>(grow + h)) % GroupStore<O, G>::kAlign) == 0;
-    if (!out_ok) h = w;   // input and output phases differ: the whole segment goes scalar
-    const int64_t nvec = (w - h) / G;
-    const int64_t tail0 = h + nvec * G;
-
-    auto one = [&](int64_t j) {
-        float g = 0.f;
-        if (!zero) {
-            const float z = Elt<S>::load1(row + j);
-            g = (j == tl) ? gt : coef * ex2(fmaf(z, kLog2e, -bias));
-        }
-        Elt<O>::store1(grow + j, g);
-    };
-    for (int64_t j = tid; j < h; j += NT) one(j);
-    for (int64_t j = tail0 + tid; j < w; j += NT) one(j);
-
-    const uint4* vp = reinterpret_cast<const uint4*>(row + h);
-    O* gp = grow + h;
-    if (zero) {
-        const float g[G] = {};
-        for (int64_t vi = tid; vi < nvec; vi += NT) GroupStore<O, G>::run(gp + vi * G, g);
-        return;
-    }
-    for (int64_t v0 = tid; v0 < nvec; v0 += (int64_t)NT * kUnroll) {
-        uint4 r[kUnroll];
-#pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-            const int64_t vi = v0 + (int64_t)u * NT;
-            if (vi < nvec) r[u] = ld_stream16(vp + vi);
-        }
-#pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-            const int64_t vi = v0 + (int64_t)u * NT;
-            if (vi < nvec) {
-                float v[G];
-                Elt<S>::unpack(r[u], v);
-#pragma unroll
-                for (int k = 0; k < G; ++k) v[k] = coef * ex2(fmaf(v[k], kLog2e, -bias));
-                const uint64_t rel = (uint64_t)(tl - (h + vi * G));
-                if (rel < (uint64_t)G) {
-#pragma unroll
-                    for (int k = 0; k < G; ++k)
-                        if (rel == (uint64_t)k) v[k] = gt;
-                }
-                GroupStore<O, G>::run(gp + vi * G, v);
-            }
-        }
-    }
-}
 
 // Items are (chunk, row) pairs, row-major over chunks so neighbouring blocks read the same row.
 template <typename S, typename O, int NT>

@@ -28,89 +28,11 @@
 #include "vce.h"
 #include "vce_device.cuh"
 #include "vce_host.h"
+#include "ce_rows.cuh"
 #include "ce_segments.h"
 
 namespace vce {
 namespace {
-
-constexpr int kUnroll = 4;
-
-// ------------------------------------------------------------------------------------------
-// Row segment streaming (forward): thread-partial (m, s) over the segment's columns except
-// the local target column `tl` (tl < 0 or >= w: no target here).  The thread that meets the
-// target column stores its value to *zt_out.
-
-// kLazy: sum against a lazily updated reference (ms_push_lazy); otherwise m ends as the exact
-// maximum of the non-target values (ms_push), as the chunk statistics report it.
-template <typename S, int NT, bool kLazy>
-__device__ __forceinline__ void fwd_segment(const S* __restrict__ row, int64_t w, int64_t tl, float& m,
-                                            float& s, float& mb, float* zt_out, const int tid) {
-    constexpr int G = Elt<S>::kGroup;
-    const uintptr_t a = reinterpret_cast<uintptr_t>(row);
-    int64_t h = (int64_t)(((16 - (a & 15)) & 15) / sizeof(S));   // elements before 16-B alignment
-    if (h > w) h = w;
-    const int64_t nvec = (w - h) / G;
-    const int64_t tail0 = h + nvec * G;
-
-    // unaligned head and tail, one element per thread
-    for (int64_t j = tid; j < h; j += NT) {
-        float v = Elt<S>::load1(row + j);
-        if (j == tl) { *zt_out = v; v = -kInf; }
-        ms_push1(v, m, s, mb);
-    }
-    for (int64_t j = tail0 + tid; j < w; j += NT) {
-        float v = Elt<S>::load1(row + j);
-        if (j == tl) { *zt_out = v; v = -kInf; }
-        ms_push1(v, m, s, mb);
-    }
-
-    const uint4* vp = reinterpret_cast<const uint4*>(row + h);
-    for (int64_t v0 = tid; v0 < nvec; v0 += (int64_t)NT * kUnroll) {
-        uint4 r[kUnroll];
-#pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-            const int64_t vi = v0 + (int64_t)u * NT;
-            if (vi < nvec) r[u] = ld_stream16(vp + vi);
-        }
-#pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-            const int64_t vi = v0 + (int64_t)u * NT;
-            if (vi < nvec) {
-                float v[G];
-                Elt<S>::unpack(r[u], v);
-                const uint64_t rel = (uint64_t)(tl - (h + vi * G));
-                if (rel < (uint64_t)G) {   // the target's group: mask it out (column test)
-#pragma unroll
-                    for (int k = 0; k < G; ++k)
-                        if (rel == (uint64_t)k) { *zt_out = v[k]; v[k] = -kInf; }
-                }
-                if (kLazy)
-                    ms_push_lazy<G>(v, m, s, mb);
-                else
-                    ms_push<G>(v, m, s, mb);
-            }
-        }
-    }
-}
-
-// Block-wide merge of the thread pairs; the result is valid in thread 0.
-template <int NT>
-__device__ __forceinline__ void ms_block_reduce(float& m, float& s, float* sm_m, float* sm_s) {
-    constexpr int NW = NT / 32;
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    ms_warp_reduce(m, s);
-    if (lane == 0) { sm_m[wid] = m; sm_s[wid] = s; }
-    __syncthreads();
-    if (wid == 0) {
-        m = lane < NW ? sm_m[lane] : -kInf;
-        s = lane < NW ? sm_s[lane] : 0.f;
-        ms_warp_reduce(m, s);
-    }
-}
-
-__device__ __forceinline__ void flag_label_error(int32_t* status) {
-    if (status) atomicCAS(status, 0, (int32_t)VCE_ERR_LABEL);
-}
 
 // ------------------------------------------------------------------------------------------
 

@@ -31,6 +31,29 @@ __device__ __forceinline__ uint4 ld_stream16(const void* p) {
     return r;
 }
 
+// 16-byte loads with an L2 policy: kLoadStream as ld_stream16; kLoadKeep marks the lines
+// evict-last (the same row is read again shortly, by the fused forward+backward);
+// kLoadLast marks them evict-first (that second, final read).
+enum { kLoadStream = 0, kLoadKeep = 1, kLoadLast = 2 };
+
+template <int kLoad>
+__device__ __forceinline__ uint64_t l2_policy() {
+    uint64_t pol = 0;
+    if (kLoad == kLoadKeep) asm("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    if (kLoad == kLoadLast) asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+template <int kLoad>
+__device__ __forceinline__ uint4 ld16(const void* p, uint64_t pol) {
+    if (kLoad == kLoadStream) return ld_stream16(p);
+    uint4 r;
+    asm("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+        : "l"(p), "l"(pol));
+    return r;
+}
+
 // Streaming (evict-first) stores for gradients that are not read back by this pass.
 __device__ __forceinline__ void st_stream16(void* p, uint4 v) {
     asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
