@@ -180,15 +180,18 @@ class CEWorkload:
     KERNEL_FILES = ["vocab_cross_entropy_gb300/csrc/ce_bwd.cu", "vocab_cross_entropy_gb300/csrc/ce_segments.h",
                     "vocab_cross_entropy_gb300/csrc/vce_device.cuh"]
 
-    def __init__(self, problem, device):
+    def __init__(self, problem, device, reduction="mean"):
         import vocab_cross_entropy_gb300 as vce
         self.vce = vce
         self.p = problem
         self.dev = device
+        self.red = reduction
         T, V = problem.T, problem.V
-        self.host = torch.empty((T, V), dtype=torch.int16, pin_memory=True)
-        problem.full(out=self.host.numpy().view(np.uint16))
-        self.host_bf16 = self.host.view(torch.bfloat16)
+        self.es = 2 if problem.dtype == "bf16" else 4
+        tdt = torch.bfloat16 if problem.dtype == "bf16" else torch.float32
+        self.host = torch.empty((T, V), dtype=torch.int16 if self.es == 2 else torch.float32, pin_memory=True)
+        problem.full(out=self.host.numpy().view(problem.np_dtype))
+        self.host_bf16 = self.host.view(tdt)          # the host logits in their storage dtype
         self.labels_host = torch.from_numpy(problem.labels).pin_memory()
         self.logits = self.host_bf16.to(device)
         self.labels = self.labels_host.to(device)
@@ -196,18 +199,20 @@ class CEWorkload:
         self.loss_out = torch.empty(1, dtype=torch.float32, device=device)
         self.stats = torch.empty(T, 4, dtype=torch.float32, device=device)
         self.status = torch.empty(1, dtype=torch.int32, device=device)
-        self.go = torch.ones(1, dtype=torch.float32, device=device)
-        self.grad = torch.empty((T, V), dtype=torch.bfloat16, device=device)
-        self.loss_host = torch.empty(1, dtype=torch.float32, pin_memory=True)
+        self.go = (torch.linspace(0.5, 1.5, T, dtype=torch.float32, device=device) if reduction == "none"
+                   else torch.ones(1, dtype=torch.float32, device=device))
+        self.grad = torch.empty((T, V), dtype=tdt, device=device)
+        self.loss_host = torch.empty(T if reduction == "none" else 1, dtype=torch.float32, pin_memory=True)
         self.n_valid = int(np.sum(problem.labels != problem.ignore_index))
-        self.launches_per_step = 3            # k_ce_fwd, k_ce_reduce, k_ce_bwd
+        self.launches_per_step = 2 if reduction == "none" else 3   # k_ce_fwd, (k_ce_reduce,) k_ce_bwd
 
     def fwd(self, stream):
-        self.vce.ce_forward(self.logits, self.labels, loss_rows=self.loss_rows, loss_out=self.loss_out,
-                            row_stats=self.stats, status=self.status, stream=stream)
+        self.vce.ce_forward(self.logits, self.labels, reduction=self.red, loss_rows=self.loss_rows,
+                            loss_out=self.loss_out, row_stats=self.stats, status=self.status, stream=stream)
 
     def bwd(self, stream):
-        self.vce.ce_backward(self.logits, self.labels, self.stats, self.go, grad_logits=self.grad, stream=stream)
+        self.vce.ce_backward(self.logits, self.labels, self.stats, self.go, reduction=self.red,
+                             grad_logits=self.grad, stream=stream)
 
     def step(self, stream):
         self.fwd(stream)
@@ -217,48 +222,53 @@ class CEWorkload:
         self.logits.copy_(self.host_bf16, non_blocking=True)
         self.labels.copy_(self.labels_host, non_blocking=True)
         self.step(stream)
-        self.loss_host.copy_(self.loss_out, non_blocking=True)
+        self.loss_host.copy_(self.loss_rows if self.red == "none" else self.loss_out, non_blocking=True)
 
     @property
     def h2d_bytes(self):
-        return self.p.T * self.p.V * 2 + self.p.T * 8
+        return self.p.T * self.p.V * self.es + self.p.T * 8 + (self.p.T * 4 if self.red == "none" else 0)
 
-    d2h_bytes = 4
+    @property
+    def d2h_bytes(self):
+        return 4 * self.loss_host.numel()
 
     def tokens(self):
         return self.p.T
 
     def bytes_fwd(self):
         T, V = self.p.T, self.p.V
-        return self.n_valid * V * 2 + T * (8 + 4 + 16)
+        return self.n_valid * V * self.es + T * (8 + 4 + 16)
 
     def bytes_bwd(self):
         T, V = self.p.T, self.p.V
-        return self.n_valid * V * 2 + T * V * 2 + T * (8 + 16)
+        return self.n_valid * V * self.es + T * V * self.es + T * (8 + 16) + (T * 4 if self.red == "none" else 0)
 
     def describe(self):
         p = self.p
-        return {"workload": f"{p.name}: CE fwd+bwd, T={p.T} rows x V={p.V} bf16 logits, mean over non-ignored "
-                            f"rows, {len(p.margin_rows)} raised-target rows, {len(p.ignore_rows)} ignored",
-                "T": p.T, "V": p.V, "logits": "bf16", "grad": "bf16", "math": "f32",
-                "l2": "no flush: inputs (%.2f GB logits) larger than the 129 MB L2" % (p.T * p.V * 2 / 1e9)}
+        red = {"mean": "mean over non-ignored rows", "sum": "sum over rows",
+               "none": "per-row losses, per-row grad_output"}[self.red]
+        return {"workload": f"{p.name}: CE fwd+bwd, T={p.T} rows x V={p.V} {p.dtype} logits, {red}, "
+                            f"{len(p.margin_rows)} raised-target rows, {len(p.ignore_rows)} ignored",
+                "T": p.T, "V": p.V, "logits": p.dtype, "grad": p.dtype, "math": "f32", "reduction": self.red,
+                "l2": "no flush: inputs (%.2f GB logits) larger than the 129 MB L2" % (p.T * p.V * self.es / 1e9)}
 
 
 class FusedWorkload(CEWorkload):
     """The pages' shape through ce_forward_backward: one pass over the logits per step."""
 
-    def __init__(self, problem, device):
-        super().__init__(problem, device)
-        self.launches_per_step = 3            # k_ce_count_valid, k_ce_fused, k_ce_reduce
+    def __init__(self, problem, device, reduction="mean"):
+        super().__init__(problem, device, reduction)
+        # k_ce_count_valid (mean only), k_ce_fused, k_ce_reduce (mean/sum)
+        self.launches_per_step = {"mean": 3, "sum": 2, "none": 1}[reduction]
 
     def step(self, stream):
-        self.vce.ce_forward_backward(self.logits, self.labels, grad_output=self.go, grad_logits=self.grad,
-                                     loss_rows=self.loss_rows, loss_out=self.loss_out, row_stats=self.stats,
-                                     status=self.status, stream=stream)
+        self.vce.ce_forward_backward(self.logits, self.labels, reduction=self.red, grad_output=self.go,
+                                     grad_logits=self.grad, loss_rows=self.loss_rows, loss_out=self.loss_out,
+                                     row_stats=self.stats, status=self.status, stream=stream)
 
     def bytes_fused(self):
         T, V = self.p.T, self.p.V
-        return self.n_valid * V * 2 + T * V * 2 + T * (8 + 4 + 16 + 8)
+        return self.n_valid * V * self.es + T * V * self.es + T * (8 + 4 + 16 + 8)
 
     def describe(self):
         d = super().describe()
@@ -269,8 +279,8 @@ class FusedWorkload(CEWorkload):
 class ChunkedWorkload(CEWorkload):
     """The pages' matrix as 8 column chunks in separate buffers: one ce_merge_chunks call per step."""
 
-    def __init__(self, problem, device):
-        super().__init__(problem, device)
+    def __init__(self, problem, device, reduction="mean"):
+        super().__init__(problem, device, reduction)
         bounds = gen.chunk_bounds(problem.V, gen.CHUNKS)
         self.chunks = [self.logits[:, o:o + w].contiguous() for o, w in bounds]
         self.grads = [torch.empty_like(c) for c in self.chunks]
@@ -280,7 +290,8 @@ class ChunkedWorkload(CEWorkload):
         self.launches_per_step = 4            # k_ce_chunk_fwd, k_ce_merge, k_ce_reduce, k_ce_bwd
 
     def step(self, stream):
-        self.vce.ce_merge_chunks(self.chunks, self.labels, grad_output=self.go, chunk_grads=self.grads,
+        self.vce.ce_merge_chunks(self.chunks, self.labels, reduction=self.red, grad_output=self.go,
+                                 chunk_grads=self.grads,
                                  loss_rows=self.loss_rows, loss_out=self.loss_out, row_stats=self.stats,
                                  chunk_stats=self.cstats, status=self.status, stream=stream)
 
@@ -471,11 +482,15 @@ def run_ours(args, rank, local_rank, world):
         return run_linear(args, rank, local_rank, world, device)
     problem = {"pages": gen.pages, "chunked": gen.pages, "fused": gen.pages, "mid": gen.mid}[args.workload](
         seed=(1002 if args.workload == "mid" else 1003) + rank)
+    if args.logits_dtype != problem.dtype:
+        problem = gen.CEProblem(problem.name, problem.T, problem.V, args.logits_dtype, problem.seed, problem.std,
+                                problem.n_margin, problem.margin_lo, problem.margin_hi, problem.n_ignore)
     if args.rows:
         problem = gen.CEProblem(problem.name + f"[{args.rows} rows]", args.rows, problem.V, problem.dtype,
                                 problem.seed, problem.std, round(0.10 * args.rows) if problem.n_margin else 0,
                                 problem.margin_lo, problem.margin_hi, round(problem.n_ignore * args.rows / problem.T))
-    w = {"chunked": ChunkedWorkload, "fused": FusedWorkload}.get(args.workload, CEWorkload)(problem, device)
+    w = {"chunked": ChunkedWorkload, "fused": FusedWorkload}.get(args.workload, CEWorkload)(problem, device,
+                                                                                        args.reduction)
     stream = torch.cuda.current_stream(device)
     for _ in range(args.warmup):
         w.step(stream)
@@ -590,6 +605,9 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=["pages", "fused", "chunked", "mid", "linear"], default="pages")
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--logits-dtype", choices=["bf16", "f32"], default="bf16",
+                    help="storage type of the logits (and gradient) for the CE workloads")
+    ap.add_argument("--reduction", choices=["mean", "sum", "none"], default="mean")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--rows", type=int, default=None,
                     help="profiling only: draw the first ROWS rows of the workload instead of all T")

@@ -287,3 +287,32 @@ def test_pages_shape_sampled(vce, pages_data):
     assert np.all(lr[p.margin_rows] > 0)
     tg = grad[torch.from_numpy(p.margin_rows).cuda(), torch.from_numpy(p.labels[p.margin_rows]).cuda()]
     assert torch.all(tg < 0)
+
+
+@pytest.mark.parametrize("dtype,gdt,reduction", [("f32", torch.float32, "mean"), ("bf16", torch.float32, "none")])
+def test_pages_shape_other_dtypes_sampled(vce, dtype, gdt, reduction):
+    """The pages' shape with fp32 logits, and with bf16 logits, fp32 gradients and per-row losses."""
+    base = gen.pages()
+    p = gen.CEProblem("pages", base.T, base.V, dtype, base.seed, base.std, base.n_margin, base.margin_lo,
+                      base.margin_hi, base.n_ignore)
+    storage = p.full()
+    logits = to_device(storage, dtype)
+    labels = torch.from_numpy(p.labels).cuda()
+    go_np = np.linspace(0.5, 1.5, p.T) if reduction == "none" else np.ones(1)
+    go = torch.from_numpy(go_np.astype(np.float32)).cuda()
+    loss_out, loss_rows, stats, status = vce.ce_forward(logits, labels, reduction=reduction)
+    grad = vce.ce_backward(logits, labels, stats, go, reduction=reduction, grad_dtype=gdt)
+    torch.cuda.synchronize()
+    assert vce.vce_get_status(status) == 0
+    rng = np.random.default_rng(11)
+    rows = np.unique(np.concatenate([p.margin_rows[:200], rng.choice(p.T, 200, replace=False)]))
+    z = O.widen(storage[rows], dtype)
+    fwd = O.ce_rows(z, p.labels[rows])
+    N = int(np.sum(p.labels != p.ignore_index))
+    c = fwd["valid"] * (go_np[rows] if reduction == "none" else 1.0 / N)
+    want = O.ce_grad_rows(z, p.labels[rows], fwd, c)
+    G.check_loss_rows(loss_rows.cpu().numpy()[rows], fwd["loss"], fwd["valid"])
+    got = grad[torch.from_numpy(rows).cuda()].cpu().numpy().astype(np.float64)
+    G.check_grad_f32(got, want)
+    raised = np.isin(rows, p.margin_rows)
+    G.check_target_entries(got[raised, p.labels[rows][raised]], want[raised, p.labels[rows][raised]])
