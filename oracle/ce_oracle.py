@@ -200,6 +200,44 @@ def ce(z, labels, reduction="mean", grad_output=1.0, ignore_index=IGNORE_INDEX, 
 
 
 # ----------------------------------------------------------------------------------------
+# label smoothing (Megatron-core vocab_parallel_cross_entropy: label_smoothing in [0, 1))
+#
+# The page gives the argument and its range only.  Reading taken: the target distribution
+# is the one-hot mixed with the uniform distribution over all V classes,
+#     q = (1 - eps) onehot(t) + eps / V,
+#     loss = -sum_j q_j log p_j = (1 - eps) (-log p_t) + eps (LSE(z) - mean_j z_j),
+#     dloss/dz_j = c (p_j - q_j).
+# -log p_t and p_j are taken from the collapse-safe forms above; LSE(z) over all columns is
+# max(z_t, L') + softplus(-|z_t - L'|).
+
+def ce_smoothed(z, labels, eps, reduction="mean", grad_output=1.0, ignore_index=IGNORE_INDEX, want_grad=True):
+    """CE with label smoothing eps: dict with loss_rows, loss_out, grad (and the plain CE fields)."""
+    z = np.asarray(z, np.float64)
+    V = z.shape[1]
+    out = ce(z, labels, reduction, grad_output, ignore_index, want_grad)
+    valid = out["valid"]
+    x, L = out["x"], out["lse_nt"]
+    zt = out["zt"]
+    with np.errstate(invalid="ignore", over="ignore"):
+        hi = np.maximum(zt, L)
+        lse_all = np.where(np.isneginf(L), zt, np.where(np.isneginf(zt), L, hi + softplus(-np.abs(x))))
+        mean_z = z.mean(axis=1)
+        loss = (1.0 - eps) * out["loss"] + eps * (lse_all - mean_z)
+    loss = np.where(valid, loss, 0.0)
+    out["loss"] = out["loss_rows"] = loss
+    out["loss_out"] = reduce_loss(loss, valid, reduction)
+    if want_grad:
+        g = out["grad"]                     # c (p - onehot), rows of ignored labels are 0
+        c = out["c"]
+        shift = np.where(valid, c * eps / V, 0.0)
+        g = g - shift[:, None]
+        rows = np.nonzero(valid)[0]
+        g[rows, np.asarray(labels, np.int64)[rows]] += c[rows] * eps
+        out["grad"] = g
+    return out
+
+
+# ----------------------------------------------------------------------------------------
 # vocabulary-chunked statistics and their merge (Megatron-core cross_entropy page)
 
 def chunk_stats(z_chunk: np.ndarray, labels: np.ndarray, offset: int, ignore_index=IGNORE_INDEX):
