@@ -142,6 +142,28 @@ int ce_backward(const void* logits, vce_dtype dt, int64_t T, int64_t V, int64_t 
                 void* grad_logits, vce_dtype grad_dt, int64_t ld_grad, vce_stream_t s);
 
 /*
+ * ce_forward_ls / ce_backward_ls -- ce_forward / ce_backward with label smoothing.
+ * [MC, vocab_parallel_cross_entropy: label_smoothing, a factor in [0.0, 1.0), default 0]
+ * The page gives the factor and its range only; the targets here are the one-hot mixed with
+ * the uniform distribution over all V classes, q = (1 - eps) onehot(t) + eps / V:
+ *     loss_i = (1 - eps) softplus(x_i) + eps (LSE(z_i) - mean_j z_ij)      (= -sum_j q_j log p_j)
+ *     grad_ij = c_i (p_ij - eps / V),  grad_it = c_i (p_t - 1 + eps (1 - 1/V))
+ * with the collapse-safe forms of softplus(x) = -log p_t and of p_t - 1 of ce_forward.  The
+ * forward additionally sums each row's logits.  label_smoothing outside [0, 1) (or NaN)
+ * returns VCE_ERR_ARG.  eps = 0 is exactly ce_forward / ce_backward.  Pass the same eps to
+ * both calls.  Other arguments as ce_forward / ce_backward.
+ */
+int ce_forward_ls(const void* logits, vce_dtype dt, int64_t T, int64_t V, int64_t ld,
+                  const int64_t* labels, int64_t ignore_index, float label_smoothing,
+                  vce_reduction red, float* loss_rows, float* loss_out, float* row_stats,
+                  int32_t* status, vce_stream_t s);
+
+int ce_backward_ls(const void* logits, vce_dtype dt, int64_t T, int64_t V, int64_t ld,
+                   const int64_t* labels, int64_t ignore_index, float label_smoothing,
+                   vce_reduction red, const float* row_stats, const float* grad_output,
+                   void* grad_logits, vce_dtype grad_dt, int64_t ld_grad, vce_stream_t s);
+
+/*
  * ce_forward_backward -- ce_forward followed by ce_backward in one pass over the logits, for
  * callers that know grad_output when the forward runs (e.g. a mean loss seeded by 1).
  * [TT, Numerics; Memory/perf: the forward prepares the backward]  Same arguments, results

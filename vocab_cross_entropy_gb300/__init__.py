@@ -13,7 +13,8 @@ import os
 
 import torch
 
-__all__ = ["VceError", "lib", "library_path", "ce_forward", "ce_backward", "ce_forward_backward", "ce_merge_chunks",
+__all__ = ["VceError", "lib", "library_path", "ce_forward", "ce_backward", "ce_forward_ls", "ce_backward_ls",
+           "ce_forward_backward", "ce_merge_chunks",
            "ce_merge_chunks_noalloc",
            "linear_ce_workspace_bytes", "linear_ce_fwd_bwd", "vce_get_status", "vce_status_string",
            "vce_abi_version", "cross_entropy", "IGNORE_INDEX", "F32", "BF16", "RED"]
@@ -48,13 +49,17 @@ def _load():
     L.ce_forward.argtypes = [p, i32, i64, i64, i64, p, i64, i32, p, p, p, p, p]
     L.ce_backward.argtypes = [p, i32, i64, i64, i64, p, i64, i32, p, p, p, i32, i64, p]
     L.ce_forward_backward.argtypes = [p, i32, i64, i64, i64, p, i64, i32, p, p, p, p, p, i32, i64, p, p]
+    f32 = ctypes.c_float
+    L.ce_forward_ls.argtypes = [p, i32, i64, i64, i64, p, i64, f32, i32, p, p, p, p, p]
+    L.ce_backward_ls.argtypes = [p, i32, i64, i64, i64, p, i64, f32, i32, p, p, p, i32, i64, p]
     L.ce_merge_chunks.argtypes = [i32, p, p, p, i32, i64, p, i64, i32, p, p, p, p, p, p, i32, p, p, p]
     L.ce_merge_chunks_noalloc.argtypes = [i32, p, p, p, i32, i64, p, i64, i32, p, p, p, p, p, p, i32, p, p]
     if hasattr(L, "linear_ce_fwd_bwd"):
         L.linear_ce_workspace_bytes.argtypes = [i64, i64, i64]
         L.linear_ce_workspace_bytes.restype = sz
         L.linear_ce_fwd_bwd.argtypes = [p, p, i64, i64, i64, p, i64, i32, p, p, p, p, p, i32, p, sz, p, p]
-    for name in ("ce_forward", "ce_backward", "ce_forward_backward", "ce_merge_chunks", "ce_merge_chunks_noalloc",
+    for name in ("ce_forward", "ce_backward", "ce_forward_ls", "ce_backward_ls", "ce_forward_backward",
+                 "ce_merge_chunks", "ce_merge_chunks_noalloc",
                  "linear_ce_fwd_bwd",
                  "vce_get_status"):
         if hasattr(L, name):
@@ -146,6 +151,36 @@ def ce_backward(logits, labels, row_stats, grad_output, ignore_index=IGNORE_INDE
                                           int(ignore_index), RED[reduction], _ptr(row_stats), _ptr(grad_output),
                                           _ptr(grad_logits), _dtype(grad_logits), _ld(grad_logits),
                                           _stream(stream)))
+    return grad_logits
+
+
+def ce_forward_ls(logits, labels, label_smoothing, ignore_index=IGNORE_INDEX, reduction="mean", *, loss_rows=None,
+                  loss_out=None, row_stats=None, status=None, stream=None):
+    """ce_forward with label smoothing.  Returns (loss_out, loss_rows, row_stats, status)."""
+    T, V = logits.shape
+    dev = logits.device
+    loss_rows = torch.empty(T, dtype=torch.float32, device=dev) if loss_rows is None else loss_rows
+    row_stats = torch.empty(T, ROW_STATS, dtype=torch.float32, device=dev) if row_stats is None else row_stats
+    status = torch.empty(1, dtype=torch.int32, device=dev) if status is None else status
+    if reduction != "none" and loss_out is None:
+        loss_out = torch.empty(1, dtype=torch.float32, device=dev)
+    _check("ce_forward_ls", _get().ce_forward_ls(_ptr(logits), _dtype(logits), T, V, _ld(logits), _ptr(labels),
+                                              int(ignore_index), float(label_smoothing), RED[reduction],
+                                              _ptr(loss_rows), _ptr(loss_out), _ptr(row_stats), _ptr(status),
+                                              _stream(stream)))
+    return loss_out, loss_rows, row_stats, status
+
+
+def ce_backward_ls(logits, labels, row_stats, grad_output, label_smoothing, ignore_index=IGNORE_INDEX,
+                   reduction="mean", *, grad_logits=None, grad_dtype=None, stream=None):
+    """ce_backward with label smoothing.  Returns grad_logits."""
+    T, V = logits.shape
+    if grad_logits is None:
+        grad_logits = torch.empty(T, V, dtype=grad_dtype or logits.dtype, device=logits.device)
+    _check("ce_backward_ls", _get().ce_backward_ls(
+        _ptr(logits), _dtype(logits), T, V, _ld(logits), _ptr(labels), int(ignore_index), float(label_smoothing),
+        RED[reduction], _ptr(row_stats), _ptr(grad_output), _ptr(grad_logits), _dtype(grad_logits),
+        _ld(grad_logits), _stream(stream)))
     return grad_logits
 
 
@@ -270,23 +305,24 @@ def linear_ce_fwd_bwd(E, W, labels, ignore_index=IGNORE_INDEX, reduction="mean",
 
 
 class _CrossEntropy(torch.autograd.Function):
-    """Autograd wrapper: forward = ce_forward, backward = ce_backward (bf16 input is not upcast)."""
+    """Autograd wrapper: forward = ce_forward_ls, backward = ce_backward_ls (bf16 input is not upcast)."""
 
     @staticmethod
-    def forward(ctx, logits, labels, ignore_index, reduction):
-        loss_out, loss_rows, row_stats, status = ce_forward(logits, labels, ignore_index, reduction)
+    def forward(ctx, logits, labels, ignore_index, reduction, label_smoothing):
+        loss_out, loss_rows, row_stats, status = ce_forward_ls(logits, labels, label_smoothing, ignore_index,
+                                                               reduction)
         ctx.save_for_backward(logits, labels, row_stats)
-        ctx.ignore_index, ctx.reduction = ignore_index, reduction
+        ctx.ignore_index, ctx.reduction, ctx.eps = ignore_index, reduction, label_smoothing
         return loss_rows if reduction == "none" else loss_out.reshape(())
 
     @staticmethod
     def backward(ctx, grad):
         logits, labels, row_stats = ctx.saved_tensors
         go = grad.reshape(-1).to(torch.float32).contiguous()
-        g = ce_backward(logits, labels, row_stats, go, ctx.ignore_index, ctx.reduction)
-        return g, None, None, None
+        g = ce_backward_ls(logits, labels, row_stats, go, ctx.eps, ctx.ignore_index, ctx.reduction)
+        return g, None, None, None, None
 
 
-def cross_entropy(logits, labels, ignore_index=IGNORE_INDEX, reduction="mean"):
+def cross_entropy(logits, labels, ignore_index=IGNORE_INDEX, reduction="mean", label_smoothing=0.0):
     """Collapse-safe softmax cross-entropy of [T, V] float32/bfloat16 CUDA logits with autograd."""
-    return _CrossEntropy.apply(logits, labels, ignore_index, reduction)
+    return _CrossEntropy.apply(logits, labels, ignore_index, reduction, float(label_smoothing))

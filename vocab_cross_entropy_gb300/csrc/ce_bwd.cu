@@ -28,7 +28,8 @@ namespace {
 template <typename S, typename O, int NT>
 __global__ void __launch_bounds__(NT) k_ce_bwd(const __grid_constant__ SegTable tab, const int64_t* __restrict__ labels,
                                                const float4* __restrict__ row_stats,
-                                               const float* __restrict__ grad_output, int go_per_row) {
+                                               const float* __restrict__ grad_output, int go_per_row,
+                                               float eps_over_v) {
     const int64_t items = tab.T * tab.k;
     for (int64_t it = blockIdx.x; it < items; it += gridDim.x) {
         const int64_t row = it / tab.k;
@@ -39,38 +40,39 @@ __global__ void __launch_bounds__(NT) k_ce_bwd(const __grid_constant__ SegTable 
         const float coef = cg * st.y;                      // c * (1 - p_t)
         const float bias = (st.x == -kInf) ? 0.f : st.x * kLog2e;
         const float gt = cg * st.z;
+        const float shift = cg * eps_over_v;   // label smoothing: every non-target entry loses c eps / V
         const int64_t tl = zero ? -1 : labels[row] - tab.off[c];
         const S* in = reinterpret_cast<const S*>(tab.in[c]) + row * tab.ld_in[c];
         O* out = reinterpret_cast<O*>(tab.out[c]) + row * tab.ld_out[c];
-        bwd_segment<S, O, NT>(in, out, tab.width[c], tl, coef, bias, gt, zero);
+        bwd_segment<S, O, NT>(in, out, tab.width[c], tl, coef, bias, gt, zero, shift);
     }
 }
 
 template <typename S, typename O, int NT>
 cudaError_t launch_bwd(const SegTable& tab, const int64_t* labels, const float* row_stats, const float* go,
-                       int go_per_row, cudaStream_t s) {
+                       int go_per_row, float eps_over_v, cudaStream_t s) {
     auto kern = k_ce_bwd<S, O, NT>;
     kern<<<grid_for(kern, NT, tab.T * tab.k), NT, 0, s>>>(tab, labels, reinterpret_cast<const float4*>(row_stats), go,
-                                                           go_per_row);
+                                                           go_per_row, eps_over_v);
     return cudaGetLastError();
 }
 
 template <typename S, typename O>
 cudaError_t dispatch_bwd2(int nt, const SegTable& tab, const int64_t* labels, const float* rs, const float* go,
-                          int per_row, cudaStream_t s) {
-    if (nt == 128) return launch_bwd<S, O, 128>(tab, labels, rs, go, per_row, s);
-    if (nt == 256) return launch_bwd<S, O, 256>(tab, labels, rs, go, per_row, s);
-    return launch_bwd<S, O, 512>(tab, labels, rs, go, per_row, s);
+                          int per_row, float eov, cudaStream_t s) {
+    if (nt == 128) return launch_bwd<S, O, 128>(tab, labels, rs, go, per_row, eov, s);
+    if (nt == 256) return launch_bwd<S, O, 256>(tab, labels, rs, go, per_row, eov, s);
+    return launch_bwd<S, O, 512>(tab, labels, rs, go, per_row, eov, s);
 }
 
 }  // namespace
 
 cudaError_t launch_ce_bwd(vce_dtype dt, vce_dtype gdt, int nt, const SegTable& tab, const int64_t* labels,
-                         const float* rs, const float* go, int per_row, cudaStream_t s) {
-    if (dt == VCE_BF16 && gdt == VCE_BF16) return dispatch_bwd2<uint16_t, uint16_t>(nt, tab, labels, rs, go, per_row, s);
-    if (dt == VCE_BF16 && gdt == VCE_F32) return dispatch_bwd2<uint16_t, float>(nt, tab, labels, rs, go, per_row, s);
-    if (dt == VCE_F32 && gdt == VCE_BF16) return dispatch_bwd2<float, uint16_t>(nt, tab, labels, rs, go, per_row, s);
-    return dispatch_bwd2<float, float>(nt, tab, labels, rs, go, per_row, s);
+                         const float* rs, const float* go, int per_row, cudaStream_t s, float eov) {
+    if (dt == VCE_BF16 && gdt == VCE_BF16) return dispatch_bwd2<uint16_t, uint16_t>(nt, tab, labels, rs, go, per_row, eov, s);
+    if (dt == VCE_BF16 && gdt == VCE_F32) return dispatch_bwd2<uint16_t, float>(nt, tab, labels, rs, go, per_row, eov, s);
+    if (dt == VCE_F32 && gdt == VCE_BF16) return dispatch_bwd2<float, uint16_t>(nt, tab, labels, rs, go, per_row, eov, s);
+    return dispatch_bwd2<float, float>(nt, tab, labels, rs, go, per_row, eov, s);
 }
 
 
@@ -78,14 +80,15 @@ cudaError_t launch_ce_bwd(vce_dtype dt, vce_dtype gdt, int nt, const SegTable& t
 
 using namespace vce;
 
-extern "C" int ce_backward(const void* logits, vce_dtype dt, int64_t T, int64_t V, int64_t ld, const int64_t* labels,
-                           int64_t ignore_index, vce_reduction red, const float* row_stats, const float* grad_output,
+extern "C" int ce_backward_ls(const void* logits, vce_dtype dt, int64_t T, int64_t V, int64_t ld,
+                              const int64_t* labels, int64_t ignore_index, float label_smoothing, vce_reduction red, const float* row_stats, const float* grad_output,
                            void* grad_logits, vce_dtype grad_dt, int64_t ld_grad, vce_stream_t s) {
     (void)ignore_index;   // ignored rows carry weight 0 in row_stats
     int rc = VCE_OK;
     if (dt != VCE_F32 && dt != VCE_BF16) return VCE_ERR_DTYPE;
     if (red != VCE_RED_NONE && red != VCE_RED_SUM && red != VCE_RED_MEAN) return VCE_ERR_DTYPE;
     if (T < 0) return VCE_ERR_SHAPE;
+    if (!(label_smoothing >= 0.f && label_smoothing < 1.f)) return VCE_ERR_ARG;
     if (grad_dt != VCE_F32 && grad_dt != VCE_BF16) return VCE_ERR_DTYPE;
     if (V < 1) return VCE_ERR_SHAPE;
     if (ld < V || ld_grad < V) return VCE_ERR_LD;
@@ -107,8 +110,16 @@ extern "C" int ce_backward(const void* logits, vce_dtype dt, int64_t T, int64_t 
     tab.ld_in[0] = ld;
     tab.ld_out[0] = ld_grad;
     const int nt = pick_threads(V * (int64_t)es);
-    if (launch_ce_bwd(dt, grad_dt, nt, tab, labels, row_stats, grad_output, red == VCE_RED_NONE, s) != cudaSuccess)
+    if (launch_ce_bwd(dt, grad_dt, nt, tab, labels, row_stats, grad_output, red == VCE_RED_NONE, s,
+                      label_smoothing / (float)V) != cudaSuccess)
         return VCE_ERR_CUDA;
     return VCE_OK;
 }
 
+
+extern "C" int ce_backward(const void* logits, vce_dtype dt, int64_t T, int64_t V, int64_t ld, const int64_t* labels,
+                           int64_t ignore_index, vce_reduction red, const float* row_stats, const float* grad_output,
+                           void* grad_logits, vce_dtype grad_dt, int64_t ld_grad, vce_stream_t s) {
+    return ce_backward_ls(logits, dt, T, V, ld, labels, ignore_index, 0.f, red, row_stats, grad_output, grad_logits,
+                          grad_dt, ld_grad, s);
+}

@@ -38,12 +38,14 @@ namespace {
 
 // Three blocks of 512 threads per SM (registers capped at 42): the row stream is issue- and
 // latency-bound, and 48 resident warps per SM measured 10% faster than 32 on the pages' shape.
-template <typename S, int NT>
-__global__ void __launch_bounds__(NT, 1536 / NT) k_ce_fwd(const S* __restrict__ logits, int64_t T, int64_t V, int64_t ld,
+// kSmooth: label smoothing eps > 0 (the row's sum of all logits is reduced alongside; two
+// blocks per SM, since the extra sum does not fit in 42 registers).
+template <typename S, int NT, bool kSmooth>
+__global__ void __launch_bounds__(NT, (kSmooth ? 1024 : 1536) / NT) k_ce_fwd(const S* __restrict__ logits, int64_t T, int64_t V, int64_t ld,
                                                const int64_t* __restrict__ labels, int64_t ignore_index,
-                                               float* __restrict__ loss_rows, float4* __restrict__ row_stats,
-                                               int32_t* status) {
-    __shared__ float sm_m[NT / 32], sm_s[NT / 32];
+                                               float eps, float* __restrict__ loss_rows,
+                                               float4* __restrict__ row_stats, int32_t* status) {
+    __shared__ float sm_m[NT / 32], sm_s[NT / 32], sm_sz[NT / 32];
     __shared__ float sm_zt;
     for (int64_t row = blockIdx.x; row < T; row += gridDim.x) {
         const int64_t t = labels[row];
@@ -56,12 +58,23 @@ __global__ void __launch_bounds__(NT, 1536 / NT) k_ce_fwd(const S* __restrict__ 
             }
             continue;
         }
-        float m = -kInf, s = 0.f, mb = 0.f;
-        fwd_segment<S, NT, true>(logits + row * ld, V, t, m, s, mb, &sm_zt, threadIdx.x);
+        float m = -kInf, s = 0.f, mb = 0.f, sz = 0.f;
+        fwd_segment<S, NT, true, kLoadStream, kSmooth>(logits + row * ld, V, t, m, s, mb, &sm_zt, threadIdx.x, &sz);
+        if (kSmooth) {   // block sum of the logits (the barrier below publishes the warp sums)
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) sz += __shfl_xor_sync(0xFFFFFFFFu, sz, off);
+            if ((threadIdx.x & 31) == 0) sm_sz[threadIdx.x >> 5] = sz;
+        }
         ms_block_reduce<NT>(m, s, sm_m, sm_s);   // contains the barrier that publishes sm_zt
         if (threadIdx.x == 0) {
             float loss;
-            row_stats[row] = ce_row_finish(m, s, sm_zt, &loss);
+            if (kSmooth) {
+                float tot = 0.f;
+                for (int w = 0; w < NT / 32; ++w) tot += sm_sz[w];
+                row_stats[row] = ce_row_finish_smoothed(m, s, sm_zt, tot, V, eps, &loss);
+            } else {
+                row_stats[row] = ce_row_finish(m, s, sm_zt, &loss);
+            }
             loss_rows[row] = loss;
         }
         __syncthreads();
@@ -184,10 +197,10 @@ __global__ void k_ce_merge(const float4* __restrict__ chunk_stats, int k, int64_
 
 template <typename S, int NT>
 cudaError_t launch_fwd(const void* logits, int64_t T, int64_t V, int64_t ld, const int64_t* labels, int64_t ig,
-                       float* loss_rows, float* row_stats, int32_t* status, cudaStream_t s) {
-    auto kern = k_ce_fwd<S, NT>;
-    kern<<<grid_for(kern, NT, T), NT, 0, s>>>(reinterpret_cast<const S*>(logits), T, V, ld, labels, ig, loss_rows,
-                                              reinterpret_cast<float4*>(row_stats), status);
+                       float eps, float* loss_rows, float* row_stats, int32_t* status, cudaStream_t s) {
+    auto kern = eps > 0.f ? k_ce_fwd<S, NT, true> : k_ce_fwd<S, NT, false>;
+    kern<<<grid_for(kern, NT, T), NT, 0, s>>>(reinterpret_cast<const S*>(logits), T, V, ld, labels, ig, eps,
+                                              loss_rows, reinterpret_cast<float4*>(row_stats), status);
     return cudaGetLastError();
 }
 
@@ -202,10 +215,10 @@ cudaError_t launch_chunk_fwd(const SegTable& tab, const int64_t* labels, int64_t
 
 template <typename S>
 cudaError_t dispatch_fwd(int nt, const void* logits, int64_t T, int64_t V, int64_t ld, const int64_t* labels,
-                         int64_t ig, float* lr, float* rs, int32_t* st, cudaStream_t s) {
-    if (nt == 128) return launch_fwd<S, 128>(logits, T, V, ld, labels, ig, lr, rs, st, s);
-    if (nt == 256) return launch_fwd<S, 256>(logits, T, V, ld, labels, ig, lr, rs, st, s);
-    return launch_fwd<S, 512>(logits, T, V, ld, labels, ig, lr, rs, st, s);
+                         int64_t ig, float eps, float* lr, float* rs, int32_t* st, cudaStream_t s) {
+    if (nt == 128) return launch_fwd<S, 128>(logits, T, V, ld, labels, ig, eps, lr, rs, st, s);
+    if (nt == 256) return launch_fwd<S, 256>(logits, T, V, ld, labels, ig, eps, lr, rs, st, s);
+    return launch_fwd<S, 512>(logits, T, V, ld, labels, ig, eps, lr, rs, st, s);
 }
 
 
@@ -244,11 +257,12 @@ cudaError_t launch_loss_reduce(const float* loss_rows, const int64_t* labels, in
 
 using namespace vce;
 
-extern "C" int ce_forward(const void* logits, vce_dtype dt, int64_t T, int64_t V, int64_t ld, const int64_t* labels,
-                          int64_t ignore_index, vce_reduction red, float* loss_rows, float* loss_out, float* row_stats,
+extern "C" int ce_forward_ls(const void* logits, vce_dtype dt, int64_t T, int64_t V, int64_t ld,
+                             const int64_t* labels, int64_t ignore_index, float label_smoothing, vce_reduction red, float* loss_rows, float* loss_out, float* row_stats,
                           int32_t* status, vce_stream_t s) {
     int rc = check_common(dt, red, T);
     if (rc) return rc;
+    if (!(label_smoothing >= 0.f && label_smoothing < 1.f)) return VCE_ERR_ARG;
     if (V < 1) return VCE_ERR_SHAPE;
     if (ld < V) return VCE_ERR_LD;
     if (!status || (red != VCE_RED_NONE && !loss_out)) return VCE_ERR_NULL;
@@ -264,9 +278,9 @@ extern "C" int ce_forward(const void* logits, vce_dtype dt, int64_t T, int64_t V
     if (cudaMemsetAsync(status, 0, sizeof(int32_t), s) != cudaSuccess) return VCE_ERR_CUDA;
     if (T > 0) {
         const int nt = pick_threads(V * (int64_t)es);
-        cudaError_t e = dt == VCE_BF16 ? dispatch_fwd<uint16_t>(nt, logits, T, V, ld, labels, ignore_index, loss_rows,
+        cudaError_t e = dt == VCE_BF16 ? dispatch_fwd<uint16_t>(nt, logits, T, V, ld, labels, ignore_index, label_smoothing, loss_rows,
                                                                 row_stats, status, s)
-                                       : dispatch_fwd<float>(nt, logits, T, V, ld, labels, ignore_index, loss_rows,
+                                       : dispatch_fwd<float>(nt, logits, T, V, ld, labels, ignore_index, label_smoothing, loss_rows,
                                                              row_stats, status, s);
         if (e != cudaSuccess) return VCE_ERR_CUDA;
     }
@@ -274,6 +288,12 @@ extern "C" int ce_forward(const void* logits, vce_dtype dt, int64_t T, int64_t V
         launch_reduce(loss_rows, labels, T, V, ignore_index, red, loss_out, row_stats, s) != cudaSuccess)
         return VCE_ERR_CUDA;
     return VCE_OK;
+}
+
+extern "C" int ce_forward(const void* logits, vce_dtype dt, int64_t T, int64_t V, int64_t ld, const int64_t* labels,
+                          int64_t ignore_index, vce_reduction red, float* loss_rows, float* loss_out, float* row_stats,
+                          int32_t* status, vce_stream_t s) {
+    return ce_forward_ls(logits, dt, T, V, ld, labels, ignore_index, 0.f, red, loss_rows, loss_out, row_stats, status, s);
 }
 
 extern "C" int ce_merge_chunks(int k, const void* const* chunk_logits, const int64_t* chunk_width,

@@ -20,9 +20,11 @@ constexpr int kUnroll = 4;
 
 // kLazy: sum against a lazily updated reference (ms_push_lazy); otherwise m ends as the exact
 // maximum of the non-target values (ms_push), as the chunk statistics report it.
-template <typename S, int NT, bool kLazy, int kLoad = kLoadStream>
+// kSumZ: also add every value of the segment (target included) into sz.
+template <typename S, int NT, bool kLazy, int kLoad = kLoadStream, bool kSumZ = false>
 __device__ __forceinline__ void fwd_segment(const S* __restrict__ row, int64_t w, int64_t tl, float& m,
-                                            float& s, float& mb, float* zt_out, const int tid) {
+                                            float& s, float& mb, float* zt_out, const int tid,
+                                            float* sz = nullptr) {
     constexpr int G = Elt<S>::kGroup;
     const uintptr_t a = reinterpret_cast<uintptr_t>(row);
     int64_t h = (int64_t)(((16 - (a & 15)) & 15) / sizeof(S));   // elements before 16-B alignment
@@ -33,11 +35,13 @@ __device__ __forceinline__ void fwd_segment(const S* __restrict__ row, int64_t w
     // unaligned head and tail, one element per thread
     for (int64_t j = tid; j < h; j += NT) {
         float v = Elt<S>::load1(row + j);
+        if (kSumZ) *sz += v;
         if (j == tl) { *zt_out = v; v = -kInf; }
         ms_push1(v, m, s, mb);
     }
     for (int64_t j = tail0 + tid; j < w; j += NT) {
         float v = Elt<S>::load1(row + j);
+        if (kSumZ) *sz += v;
         if (j == tl) { *zt_out = v; v = -kInf; }
         ms_push1(v, m, s, mb);
     }
@@ -57,6 +61,16 @@ __device__ __forceinline__ void fwd_segment(const S* __restrict__ row, int64_t w
             if (vi < nvec) {
                 float v[G];
                 Elt<S>::unpack(r[u], v);
+                if (kSumZ) {
+                    float q[G];
+#pragma unroll
+                    for (int k = 0; k < G; ++k) q[k] = v[k];
+#pragma unroll
+                    for (int wd = 1; wd < G; wd *= 2)
+#pragma unroll
+                        for (int k = 0; k + wd < G; k += 2 * wd) q[k] += q[k + wd];
+                    *sz += q[0];
+                }
                 const uint64_t rel = (uint64_t)(tl - (h + vi * G));
                 if (rel < (uint64_t)G) {   // the target's group: mask it out (column test)
 #pragma unroll
@@ -75,9 +89,11 @@ __device__ __forceinline__ void fwd_segment(const S* __restrict__ row, int64_t w
 // ------------------------------------------------------------------------------------------
 // Backward: one row segment.  grad = coef * 2^(z*log2e - bias) off target, gt at the target.
 
+// Non-target entries are coef * 2^(z log2 e - bias) - shift (shift = c * eps / V under label
+// smoothing, 0 otherwise: fmaf with a zero addend rounds exactly as the product).
 template <typename S, typename O, int NT, int kLoad = kLoadStream>
 __device__ __forceinline__ void bwd_segment(const S* __restrict__ row, O* __restrict__ grow, int64_t w, int64_t tl,
-                                            float coef, float bias, float gt, bool zero) {
+                                            float coef, float bias, float gt, bool zero, float shift = 0.f) {
     constexpr int G = Elt<S>::kGroup;
     const int tid = threadIdx.x;
     const uintptr_t a = reinterpret_cast<uintptr_t>(row);
@@ -92,7 +108,7 @@ __device__ __forceinline__ void bwd_segment(const S* __restrict__ row, O* __rest
         float g = 0.f;
         if (!zero) {
             const float z = Elt<S>::load1(row + j);
-            g = (j == tl) ? gt : coef * ex2(fmaf(z, kLog2e, -bias));
+            g = (j == tl) ? gt : fmaf(coef, ex2(fmaf(z, kLog2e, -bias)), -shift);
         }
         Elt<O>::store1(grow + j, g);
     };
@@ -121,7 +137,7 @@ __device__ __forceinline__ void bwd_segment(const S* __restrict__ row, O* __rest
                 float v[G];
                 Elt<S>::unpack(r[u], v);
 #pragma unroll
-                for (int k = 0; k < G; ++k) v[k] = coef * ex2(fmaf(v[k], kLog2e, -bias));
+                for (int k = 0; k < G; ++k) v[k] = fmaf(coef, ex2(fmaf(v[k], kLog2e, -bias)), -shift);
                 const uint64_t rel = (uint64_t)(tl - (h + vi * G));
                 if (rel < (uint64_t)G) {
 #pragma unroll

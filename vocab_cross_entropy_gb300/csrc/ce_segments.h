@@ -41,7 +41,9 @@ inline int grid_for(K kernel, int nt, int64_t items) {
 }
 
 // The gradient of every (chunk, row) segment of `tab` (ce_bwd.cu).
+// eps_over_v: label smoothing eps / V (0 without smoothing).
 cudaError_t launch_ce_bwd(vce_dtype dt, vce_dtype gdt, int nt, const SegTable& tab, const int64_t* labels,
-                          const float* row_stats, const float* grad_output, int go_per_row, cudaStream_t s);
+                          const float* row_stats, const float* grad_output, int go_per_row, cudaStream_t s,
+                          float eps_over_v = 0.f);
 
 }  // namespace vce

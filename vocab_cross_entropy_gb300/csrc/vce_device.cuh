@@ -269,4 +269,24 @@ __device__ __forceinline__ float4 ce_row_finish(float M, float S, float zt, floa
     return make_float4(lse, pnt, dt, 1.f);
 }
 
+// Label smoothing eps (targets q = (1 - eps) onehot + eps / V): from the same (M, S, z_t) and
+// the row's sum of all logits,
+//   loss = (1 - eps) softplus(x) + eps (LSE(z) - sum_z / V),  LSE(z) = max(z_t, L') + softplus(-|x|),
+// and the target coefficient gains eps (1 - 1/V) (the non-target shift -eps/V is applied by
+// the backward).
+__device__ __forceinline__ float4 ce_row_finish_smoothed(float M, float S, float zt, float sum_z, int64_t V,
+                                                         float eps, float* loss) {
+    float nll;
+    float4 st = ce_row_finish(M, S, zt, &nll);
+    const float L = st.x;
+    float lse_all;
+    if (L == -kInf) lse_all = zt;
+    else if (zt == -kInf) lse_all = L;
+    else lse_all = fmaxf(zt, L) + softplus_f(-fabsf(L - zt));
+    const float inv_v = 1.f / (float)V;
+    *loss = (1.f - eps) * nll + eps * (lse_all - sum_z * inv_v);
+    st.z += eps * (1.f - inv_v);
+    return st;
+}
+
 }  // namespace vce
