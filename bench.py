@@ -180,12 +180,13 @@ class CEWorkload:
     KERNEL_FILES = ["vocab_cross_entropy_gb300/csrc/ce_bwd.cu", "vocab_cross_entropy_gb300/csrc/ce_rows.cuh",
                     "vocab_cross_entropy_gb300/csrc/ce_segments.h", "vocab_cross_entropy_gb300/csrc/vce_device.cuh"]
 
-    def __init__(self, problem, device, reduction="mean"):
+    def __init__(self, problem, device, reduction="mean", label_smoothing=0.0):
         import vocab_cross_entropy_gb300 as vce
         self.vce = vce
         self.p = problem
         self.dev = device
         self.red = reduction
+        self.eps = float(label_smoothing)
         T, V = problem.T, problem.V
         self.es = 2 if problem.dtype == "bf16" else 4
         tdt = torch.bfloat16 if problem.dtype == "bf16" else torch.float32
@@ -207,12 +208,20 @@ class CEWorkload:
         self.launches_per_step = 2 if reduction == "none" else 3   # k_ce_fwd, (k_ce_reduce,) k_ce_bwd
 
     def fwd(self, stream):
-        self.vce.ce_forward(self.logits, self.labels, reduction=self.red, loss_rows=self.loss_rows,
-                            loss_out=self.loss_out, row_stats=self.stats, status=self.status, stream=stream)
+        if self.eps:
+            self.vce.ce_forward_ls(self.logits, self.labels, self.eps, reduction=self.red, loss_rows=self.loss_rows,
+                                   loss_out=self.loss_out, row_stats=self.stats, status=self.status, stream=stream)
+        else:
+            self.vce.ce_forward(self.logits, self.labels, reduction=self.red, loss_rows=self.loss_rows,
+                                loss_out=self.loss_out, row_stats=self.stats, status=self.status, stream=stream)
 
     def bwd(self, stream):
-        self.vce.ce_backward(self.logits, self.labels, self.stats, self.go, reduction=self.red,
-                             grad_logits=self.grad, stream=stream)
+        if self.eps:
+            self.vce.ce_backward_ls(self.logits, self.labels, self.stats, self.go, self.eps, reduction=self.red,
+                                    grad_logits=self.grad, stream=stream)
+        else:
+            self.vce.ce_backward(self.logits, self.labels, self.stats, self.go, reduction=self.red,
+                                 grad_logits=self.grad, stream=stream)
 
     def step(self, stream):
         self.fwd(stream)
@@ -256,6 +265,7 @@ class CEWorkload:
         return {"workload": f"{p.name}: CE fwd+bwd, T={p.T} rows x V={p.V} {p.dtype} logits, {red}, "
                             f"{len(p.margin_rows)} raised-target rows, {len(p.ignore_rows)} ignored",
                 "T": p.T, "V": p.V, "logits": p.dtype, "grad": p.dtype, "math": "f32", "reduction": self.red,
+                "label_smoothing": self.eps,
                 "l2": "no flush: inputs (%.2f GB logits) larger than the 129 MB L2" % (p.T * p.V * self.es / 1e9)}
 
 
@@ -495,8 +505,13 @@ def run_ours(args, rank, local_rank, world):
         problem = gen.CEProblem(problem.name + f"[{args.rows} rows]", args.rows, problem.V, problem.dtype,
                                 problem.seed, problem.std, round(0.10 * args.rows) if problem.n_margin else 0,
                                 problem.margin_lo, problem.margin_hi, round(problem.n_ignore * args.rows / problem.T))
-    w = {"chunked": ChunkedWorkload, "fused": FusedWorkload}.get(args.workload, CEWorkload)(problem, device,
-                                                                                        args.reduction)
+    if args.label_smoothing and args.workload != "pages":
+        raise SystemExit("--label-smoothing applies to the pages workload (ce_forward_ls / ce_backward_ls)")
+    if args.label_smoothing:
+        w = CEWorkload(problem, device, args.reduction, args.label_smoothing)
+    else:
+        w = {"chunked": ChunkedWorkload, "fused": FusedWorkload}.get(args.workload, CEWorkload)(problem, device,
+                                                                                            args.reduction)
     stream = torch.cuda.current_stream(device)
     for _ in range(args.warmup):
         w.step(stream)
@@ -507,9 +522,11 @@ def run_ours(args, rank, local_rank, world):
     chunked = args.workload in ("chunked", "fused")
     if not chunked:
         fwd_ms, bwd_ms = time_kernel(w, max(10, min(args.steps, 50)), stream)
-        for _ in range(3):
-            w.one_pass_step(stream)
-        one_pass_ms = time_steps(w.one_pass_step, args.steps, stream, world, device) / args.steps
+        one_pass_ms = None
+        if not w.eps:
+            for _ in range(3):
+                w.one_pass_step(stream)
+            one_pass_ms = time_steps(w.one_pass_step, args.steps, stream, world, device) / args.steps
     e2e_steps = max(3, min(args.e2e_steps, args.steps))
     for _ in range(2):
         w.e2e_step(stream)
@@ -560,9 +577,10 @@ def run_ours(args, rank, local_rank, world):
     }
     if not chunked:
         out["kernels_ms"] = {"ce_forward": round(fwd_ms, 5), "ce_backward": round(bwd_ms, 5)}
-        out["one_pass"] = {"call": "ce_forward_backward", "value": round(tokens_all / (one_pass_ms / 1e3), 1),
-                           "unit": "tokens/s", "ms_per_step": round(one_pass_ms, 5),
-                           "hbm_gbs": round((w.n_valid + w.p.T) * w.p.V * w.es / (one_pass_ms / 1e3) / 1e9, 1)}
+        if one_pass_ms:
+            out["one_pass"] = {"call": "ce_forward_backward", "value": round(tokens_all / (one_pass_ms / 1e3), 1),
+                               "unit": "tokens/s", "ms_per_step": round(one_pass_ms, 5),
+                               "hbm_gbs": round((w.n_valid + w.p.T) * w.p.V * w.es / (one_pass_ms / 1e3) / 1e9, 1)}
         out["roofline_fwd"] = {"bound": "hbm", "kernel": "k_ce_fwd",
                                "achieved": round(w.bytes_fwd() / (fwd_ms / 1e3) / 1e9, 1), "peak": peaks["hbm_gbs"],
                                "unit": "GB/s",
@@ -621,6 +639,8 @@ def main(argv=None):
     ap.add_argument("--logits-dtype", choices=["bf16", "f32"], default="bf16",
                     help="storage type of the logits (and gradient) for the CE workloads")
     ap.add_argument("--reduction", choices=["mean", "sum", "none"], default="mean")
+    ap.add_argument("--label-smoothing", type=float, default=0.0,
+                    help="pages workload through ce_forward_ls / ce_backward_ls with this eps")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--rows", type=int, default=None,
                     help="profiling only: draw the first ROWS rows of the workload instead of all T")
