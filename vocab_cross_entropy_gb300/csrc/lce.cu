@@ -50,14 +50,14 @@ struct EpiStats {
     struct Params {
         const int64_t* labels;
         int64_t ignore_index, T, V;
-        float4* part;   // [2 tiles_n][T]
+        float4* part;   // [tiles_n][T]
     };
     struct Row {
         float m, s, mb, zt;
         int64_t t;
         bool own;
     };
-    __device__ __forceinline__ static void begin(const Params& p, Row& r, int row, int, int) {
+    __device__ __forceinline__ static void begin(const Params& p, Row& r, int row, int) {
         r.m = -kInf;
         r.s = 0.f;
         r.mb = 0.f;
@@ -87,10 +87,8 @@ struct EpiStats {
         }
         ms_push<32>(v, r.m, r.s, r.mb);
     }
-    // one partial per (row, 128-column half tile): part[(2 tn + half) T + row]
-    __device__ __forceinline__ static void end(const Params& p, Row& r, int row, int tn, int half) {
-        if (row < p.T)
-            p.part[(int64_t)(2 * tn + half) * p.T + row] = make_float4(r.m, r.s, r.own ? r.zt : 0.f, r.own ? 1.f : 0.f);
+    __device__ __forceinline__ static void end(const Params& p, Row& r, int row, int tn) {
+        if (row < p.T) p.part[(int64_t)tn * p.T + row] = make_float4(r.m, r.s, r.own ? r.zt : 0.f, r.own ? 1.f : 0.f);
     }
 };
 
@@ -111,7 +109,7 @@ struct EpiGrad {
         int64_t tl;
         bool zero;
     };
-    __device__ __forceinline__ static void begin(const Params& p, Row& r, int row, int, int) {
+    __device__ __forceinline__ static void begin(const Params& p, Row& r, int row, int) {
         r.zero = true;
         r.coef = r.bias = r.gt = 0.f;
         r.tl = -1;
@@ -156,30 +154,31 @@ struct EpiGrad {
             dh[q] = make_uint4(hi[4 * q], hi[4 * q + 1], hi[4 * q + 2], hi[4 * q + 3]);
             dl[q] = make_uint4(lo[4 * q], lo[4 * q + 1], lo[4 * q + 2], lo[4 * q + 3]);
         }
-        // transposed [width_pad][ldt]: stage the warp's 32 rows x 32 columns in shared memory
-        // (hi, then lo, through the same buffer), then each lane writes 64 contiguous bytes
-        // (32 rows) of one column
-        uint16_t* sh = reinterpret_cast<uint16_t*>(wsm);          // [32 cols][kStageLd]
+        // transposed [width_pad][ldt]: stage the warp's 32 rows x 32 columns in shared memory,
+        // then each lane writes 64 contiguous bytes (32 rows) of one column
+        uint16_t* sh = reinterpret_cast<uint16_t*>(wsm);          // [32 cols][kStageLd] hi
+        uint16_t* sl = sh + 32 * kStageLd;                         // lo
         const int lane = threadIdx.x & 31;
-        const int row0 = row - lane;
 #pragma unroll
-        for (int part = 0; part < 2; ++part) {
-            const uint32_t* src = part == 0 ? hi : lo;
-            uint16_t* dst = part == 0 ? p.gt_hi : p.gt_lo;
-#pragma unroll
-            for (int k = 0; k < 32; ++k) {
-                const uint32_t w = src[k / 2];
-                sh[k * kStageLd + lane] = (k & 1) ? (uint16_t)(w >> 16) : (uint16_t)(w & 0xFFFFu);
-            }
-            __syncwarp();
-            const uint4* rs = reinterpret_cast<const uint4*>(sh + lane * kStageLd);
-            uint4* td = reinterpret_cast<uint4*>(dst + (int64_t)(col0 + lane) * p.ldt + row0);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) td[q] = rs[q];
-            __syncwarp();
+        for (int k = 0; k < 32; ++k) {
+            const uint32_t h = hi[k / 2], l = lo[k / 2];
+            sh[k * kStageLd + lane] = (k & 1) ? (uint16_t)(h >> 16) : (uint16_t)(h & 0xFFFFu);
+            sl[k * kStageLd + lane] = (k & 1) ? (uint16_t)(l >> 16) : (uint16_t)(l & 0xFFFFu);
         }
+        __syncwarp();
+        const int row0 = row - lane;
+        const uint4* rh = reinterpret_cast<const uint4*>(sh + lane * kStageLd);
+        const uint4* rl = reinterpret_cast<const uint4*>(sl + lane * kStageLd);
+        uint4* th = reinterpret_cast<uint4*>(p.gt_hi + (int64_t)(col0 + lane) * p.ldt + row0);
+        uint4* tl = reinterpret_cast<uint4*>(p.gt_lo + (int64_t)(col0 + lane) * p.ldt + row0);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            th[q] = rh[q];
+            tl[q] = rl[q];
+        }
+        __syncwarp();
     }
-    __device__ __forceinline__ static void end(const Params&, Row&, int, int, int) {}
+    __device__ __forceinline__ static void end(const Params&, Row&, int, int) {}
 };
 
 // Step 2b: dW rows of the chunk, stored once (bf16 round-to-nearest-even or fp32).
@@ -190,7 +189,7 @@ struct EpiStore {
         int bf16;
     };
     struct Row {};
-    __device__ __forceinline__ static void begin(const Params&, Row&, int, int, int) {}
+    __device__ __forceinline__ static void begin(const Params&, Row&, int, int) {}
     __device__ __forceinline__ static void consume(const Params& p, Row&, int row, int col0, const uint32_t (&acc)[32], uint8_t*) {
         if (row >= p.rows || col0 >= p.cols) return;
         const int64_t base = (p.row_off + row) * p.ld + col0;
@@ -222,7 +221,7 @@ struct EpiStore {
             }
         }
     }
-    __device__ __forceinline__ static void end(const Params&, Row&, int, int, int) {}
+    __device__ __forceinline__ static void end(const Params&, Row&, int, int) {}
 };
 
 // Step 2c: dE partial of one chunk added into (sum, compensation) with a two-sum; the first
@@ -236,7 +235,7 @@ struct EpiKahan {
         int bf16;
     };
     struct Row {};
-    __device__ __forceinline__ static void begin(const Params&, Row&, int, int, int) {}
+    __device__ __forceinline__ static void begin(const Params&, Row&, int, int) {}
     // a + x = t + e exactly (Knuth's two-sum); the compensation accumulates e
     __device__ __forceinline__ static void two_sum(float a, float x, float& t, float& e) {
         t = a + x;
@@ -308,7 +307,7 @@ struct EpiKahan {
             put(p, base + k, sv, cv);
         }
     }
-    __device__ __forceinline__ static void end(const Params&, Row&, int, int, int) {}
+    __device__ __forceinline__ static void end(const Params&, Row&, int, int) {}
 };
 
 // ------------------------------------------------------------------------------------------
@@ -414,7 +413,7 @@ bool layout(int64_t T, int64_t D, int64_t V, Layout* L) {
     };
     L->off_et = take((size_t)D * L->T_pad * 2);
     L->off_wt = take((size_t)D * L->V_pad * 2);
-    L->off_part = take((size_t)2 * L->tiles_v * T * 16);
+    L->off_part = take((size_t)L->tiles_v * T * 16);
     L->off_stats = take((size_t)T * 16);
     L->off_ghi = take((size_t)L->T_pad * L->Vc * 2);
     L->off_glo = take((size_t)L->T_pad * L->Vc * 2);
@@ -495,7 +494,7 @@ extern "C" int linear_ce_fwd_bwd(const void* E, const void* W, int64_t T, int64_
         tc::GemmArgs g{tiles_t, (int)L.tiles_v, nkD, nkD, 0, 0, 0, 0, status};
         EpiStats::Params ep{labels, ignore_index, T, V, reinterpret_cast<float4*>(part)};
         if (run_gemm<EpiStats>(mE, mE, mW, g, ep, s) != cudaSuccess) return VCE_ERR_CUDA;
-        if (launch_stats_merge(part, 2 * (int)L.tiles_v, T, V, labels, ignore_index, loss_rows, stats, status, s) !=
+        if (launch_stats_merge(part, (int)L.tiles_v, T, V, labels, ignore_index, loss_rows, stats, status, s) !=
             cudaSuccess)
             return VCE_ERR_CUDA;
         if (red != VCE_RED_NONE &&

@@ -7,8 +7,7 @@
 //   warp 0 (one lane)  TMA producer: A tile 128 x 64 and B tile 256 x 64 per stage
 //   warp 1 (one lane)  MMA issuer:   4 x tcgen05.mma (M=128, N=256, K=16) per stage
 //   warp 2             TMEM allocation / release (512 columns = two accumulators)
-//   warps 4..11        epilogue: warp w reads TMEM lanes 32*(w%4).. and the column half
-//                      (w-4)/4 of the tile, two 32-column tcgen05.ld per wait; one
+//   warps 4..7         epilogue: tcgen05.ld 32 lanes x 32 columns at a time, one
 //                      accumulator row per thread
 // The accumulator is double buffered so the epilogue of tile i overlaps the MMAs of
 // tile i+1.  Shared-memory tiles use the 128-byte swizzle that TMA writes and the MMA
@@ -31,10 +30,9 @@ constexpr int A_BYTES = BM * BK * 2;   // 16 KB
 constexpr int B_BYTES = BN * BK * 2;   // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int TMEM_COLS = 2 * BN;      // two fp32 accumulators of 128 lanes x 256 columns
-constexpr int kEpiWarps = 8;                 // two per TMEM lane quarter, one per column half
-constexpr int kThreads = (4 + kEpiWarps) * 32;
-constexpr int EPI_WARP_BYTES = 2560;   // per epilogue warp: staging space an epilogue may use
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + kEpiWarps * EPI_WARP_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+constexpr int kThreads = 256;
+constexpr int EPI_WARP_BYTES = 5120;   // per epilogue warp: staging space an epilogue may use
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 4 * EPI_WARP_BYTES + 1024 /*align*/ + 256 /*barriers*/;
 
 // error codes written to the kernel's error word when a wait gives up
 enum { kErrWaitEmpty = 101, kErrWaitFull = 102, kErrWaitAccFree = 103, kErrWaitAccFull = 104 };
@@ -135,7 +133,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* smA = smem;
     uint8_t* smB = smem + STAGES * A_BYTES;
     uint8_t* epi_smem = smem + STAGES * STAGE_BYTES;
-    uint64_t* full = reinterpret_cast<uint64_t*>(epi_smem + kEpiWarps * EPI_WARP_BYTES);
+    uint64_t* full = reinterpret_cast<uint64_t*>(epi_smem + 4 * EPI_WARP_BYTES);
     uint64_t* empty = full + STAGES;
     uint64_t* acc_full = empty + STAGES;
     uint64_t* acc_free = acc_full + 2;
@@ -151,7 +149,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&acc_full[a], 1);
-            mbar_init(&acc_free[a], kEpiWarps * 32);
+            mbar_init(&acc_free[a], 4 * 32);
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -235,10 +233,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         while (!mbar_try_wait(drain, 0) && globaltimer() - t0 < kWaitNs) {
         }
     } else if (warp >= 4) {
-        // ---------------- epilogue: thread = accumulator row, warp = lane quarter x column half
-        const int sub = warp & 3, half = (warp - 4) >> 2;
-        uint8_t* wsm = epi_smem + (warp - 4) * EPI_WARP_BYTES;
-        constexpr int kChunks = BN / 2 / 32;
+        // ---------------- epilogue: thread = accumulator row
+        const int sub = warp & 3;
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
@@ -248,19 +244,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             tile_coords(g, tile, tm, tn);
             const int row = tm * BM + sub * 32 + lane;
             typename Epi::Row st;
-            Epi::begin(ep, st, row, tn, half);
-            const uint32_t t0 = tmem_base + (uint32_t)(acc * BN + half * (BN / 2)) + ((uint32_t)(sub * 32) << 16);
-            static_assert(kChunks % 2 == 0, "chunks are loaded in pairs");
+            Epi::begin(ep, st, row, tn);
+            const uint32_t t0 = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(sub * 32) << 16);
 #pragma unroll 1
-            for (int c = 0; c < kChunks; c += 2) {
-                uint32_t r0[32], r1[32];
-                tmem_ld32(t0 + (uint32_t)(c * 32), r0);
-                tmem_ld32(t0 + (uint32_t)((c + 1) * 32), r1);
-                tmem_wait_ld();   // the registers of both loads are defined from here on
-                Epi::consume(ep, st, row, tn * BN + half * (BN / 2) + c * 32, r0, wsm);
-                Epi::consume(ep, st, row, tn * BN + half * (BN / 2) + (c + 1) * 32, r1, wsm);
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld32(t0 + (uint32_t)(c * 32), r);
+                tmem_wait_ld();
+                Epi::consume(ep, st, row, tn * BN + c * 32, r, epi_smem + sub * EPI_WARP_BYTES);
             }
-            Epi::end(ep, st, row, tn, half);
+            Epi::end(ep, st, row, tn);
             tc_fence_before();
             mbar_arrive(&acc_free[acc]);
             acc ^= 1;
