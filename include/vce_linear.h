@@ -60,6 +60,17 @@ int linear_ce_fwd_bwd(const void* E, const void* W, int64_t T, int64_t D, int64_
                       void* dE, void* dW, vce_dtype grad_dt,
                       void* workspace, size_t workspace_bytes, int32_t* status, vce_stream_t s);
 
+/*
+ * vce_gemm_bf16 -- the tensor-core GEMM the linear-CE is built on, with a plain fp32 output:
+ *     C[m][n] = sum_k A(m, k) B(n, k)
+ * A is [M, K] row-major (a_mn = 0, K-major) or [K, M] row-major (a_mn = 1, MN-major); B is
+ * [N, K] (b_mn = 0) or [K, N] (b_mn = 1).  bf16 operands, fp32 accumulation, 128 x 256
+ * tiles.  M, N, K multiples of 8; A, B, C 16-byte aligned; C [M, ldc] fp32, ldc >= N and a
+ * multiple of 4.  No page counterpart: it exposes the building block for testing.
+ */
+int vce_gemm_bf16(const void* A, int a_mn, const void* B, int b_mn, int64_t M, int64_t N, int64_t K,
+                  float* C, int64_t ldc, vce_stream_t s);
+
 #ifdef __cplusplus
 }
 #endif

@@ -1,0 +1,33 @@
+"""The tensor-core GEMM building block (vce_gemm_bf16) with K-major and MN-major operands,
+against a float64 matrix product of the same bf16 values."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import ce_oracle as O
+from tests.test_ce_gpu import vce  # noqa: F401  (fixture)
+
+pytestmark = pytest.mark.gpu
+
+
+def _bf16(rng, shape, std=1.0):
+    x = torch.from_numpy((rng.standard_normal(shape) * std).astype(np.float32)).to(torch.bfloat16)
+    bits = x.view(torch.int16).numpy().view(np.uint16)
+    return x, O.widen(bits, "bf16")
+
+
+@pytest.mark.parametrize("a_mn", [False, True])
+@pytest.mark.parametrize("b_mn", [False, True])
+@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (256, 512, 320), (136, 264, 72), (8, 8, 8), (384, 768, 1024)])
+def test_gemm_layouts(vce, a_mn, b_mn, M, N, K):
+    rng = np.random.default_rng(M * 7 + N + K + 2 * a_mn + b_mn)
+    A, A64 = _bf16(rng, (K, M) if a_mn else (M, K))
+    B, B64 = _bf16(rng, (K, N) if b_mn else (N, K), 0.05)
+    C = vce.vce_gemm_bf16(A.cuda(), B.cuda(), a_mn, b_mn)
+    torch.cuda.synchronize()
+    Am = A64.T if a_mn else A64
+    Bm = B64.T if b_mn else B64
+    want = Am @ Bm.T
+    bound = 2.0 ** -20 * (np.abs(Am) @ np.abs(Bm).T) + 1e-30
+    err = np.abs(C.cpu().numpy().astype(np.float64) - want)
+    assert np.all(err <= bound), f"max err/bound {np.max(err / bound):.3g}"

@@ -58,6 +58,8 @@ def _load():
         L.linear_ce_workspace_bytes.argtypes = [i64, i64, i64]
         L.linear_ce_workspace_bytes.restype = sz
         L.linear_ce_fwd_bwd.argtypes = [p, p, i64, i64, i64, p, i64, i32, p, p, p, p, p, i32, p, sz, p, p]
+        L.vce_gemm_bf16.argtypes = [p, i32, p, i32, i64, i64, i64, p, i64, p]
+        L.vce_gemm_bf16.restype = i32
     for name in ("ce_forward", "ce_backward", "ce_forward_ls", "ce_backward_ls", "ce_forward_backward",
                  "ce_merge_chunks", "ce_merge_chunks_noalloc",
                  "linear_ce_fwd_bwd",
@@ -269,6 +271,18 @@ def ce_merge_chunks_noalloc(chunks, labels, ignore_index=IGNORE_INDEX, reduction
     _check("ce_merge_chunks_noalloc", _get().ce_merge_chunks_noalloc(
         k, in_ptrs, widths, lds, dt, T, _ptr(labels), int(ignore_index), RED[reduction], _ptr(loss_rows),
         _ptr(loss_out), _ptr(row_stats), _ptr(grad_output), g_ptrs, g_lds, gdt, _ptr(status), _stream(stream)))
+
+
+def vce_gemm_bf16(A, B, a_mn=False, b_mn=False, *, C=None, stream=None):
+    """C = A(m,k) B(n,k) on the tensor cores; A [M,K] or [K,M] (a_mn), B [N,K] or [K,N] (b_mn), bf16."""
+    M = A.shape[1] if a_mn else A.shape[0]
+    K = A.shape[0] if a_mn else A.shape[1]
+    N = B.shape[1] if b_mn else B.shape[0]
+    if C is None:
+        C = torch.empty(M, N, dtype=torch.float32, device=A.device)
+    _check("vce_gemm_bf16", _get().vce_gemm_bf16(_ptr(A), int(a_mn), _ptr(B), int(b_mn), M, N, K, _ptr(C),
+                                              C.stride(0), _stream(stream)))
+    return C
 
 
 def linear_ce_workspace_bytes(T, D, V) -> int:

@@ -374,10 +374,10 @@ bool make_map(CUtensorMap* m, const void* base, int64_t inner, int64_t outer, in
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <class Epi>
+template <class Epi, bool kAmn = false, bool kBmn = false>
 cudaError_t run_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b, const tc::GemmArgs& g,
                      const typename Epi::Params& ep, cudaStream_t s) {
-    auto kern = tc::k_tc_gemm<Epi>;
+    auto kern = tc::k_tc_gemm<Epi, kAmn, kBmn>;
     static bool attr_set = false;   // per process; the attribute is per function, not per device
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::SMEM_BYTES);
@@ -528,4 +528,28 @@ extern "C" int linear_ce_fwd_bwd(const void* E, const void* W, int64_t T, int64_
         }
     }
     return VCE_OK;
+}
+
+extern "C" int vce_gemm_bf16(const void* A, int a_mn, const void* B, int b_mn, int64_t M, int64_t N, int64_t K,
+                             float* C, int64_t ldc, vce_stream_t s) {
+    if (!A || !B || !C) return VCE_ERR_NULL;
+    if (M < 1 || N < 1 || K < 1 || (M % 8) || (N % 8) || (K % 8) || M > (1 << 30) || N > (1 << 30) || K > (1 << 30))
+        return VCE_ERR_SHAPE;
+    if (ldc < N) return VCE_ERR_LD;
+    if (!aligned(A, 16) || !aligned(B, 16) || !aligned(C, 16) || (ldc % 4)) return VCE_ERR_ALIGN;
+    int rc = require_sm100();
+    if (rc) return rc;
+    CUtensorMap ma, mb;
+    const bool ok_a = a_mn ? make_map(&ma, A, M, K, M, BK) : make_map(&ma, A, K, M, K, BM);
+    const bool ok_b = b_mn ? make_map(&mb, B, N, K, N, BK) : make_map(&mb, B, K, N, K, BN);
+    if (!ok_a || !ok_b) return VCE_ERR_CUDA;
+    const int nk = (int)cdiv(K, BK);
+    tc::GemmArgs g{(int)cdiv(M, BM), (int)cdiv(N, BN), nk, nk, 0, 0, 0, 0, nullptr};
+    EpiStore::Params ep{C, ldc, M, N, 0, 0};
+    cudaError_t e;
+    if (a_mn && b_mn) e = run_gemm<EpiStore, true, true>(ma, ma, mb, g, ep, s);
+    else if (a_mn) e = run_gemm<EpiStore, true, false>(ma, ma, mb, g, ep, s);
+    else if (b_mn) e = run_gemm<EpiStore, false, true>(ma, ma, mb, g, ep, s);
+    else e = run_gemm<EpiStore, false, false>(ma, ma, mb, g, ep, s);
+    return e == cudaSuccess ? VCE_OK : VCE_ERR_CUDA;
 }

@@ -1,10 +1,13 @@
 // A persistent, warp-specialised bf16 GEMM on the sm_100-family tensor cores:
-//     acc[m, n] = sum_k A[m, k] * B[n, k]      (both operands K-major, fp32 accumulators)
+//     acc[m, n] = sum_k A[m, k] * B[n, k]      (fp32 accumulators)
+// Each operand is K-major (global rows run along K) or MN-major (global rows run along M,
+// resp. N), chosen at compile time.
 // with a caller-supplied epilogue that consumes each 128 x 256 accumulator tile from
 // tensor memory.  Hand-written PTX for the TMA loads (cp.async.bulk.tensor), the
 // mbarrier pipeline and the tcgen05 MMA / TMEM instructions.
 //
-//   warp 0 (one lane)  TMA producer: A tile 128 x 64 and B tile 256 x 64 per stage
+//   warp 0 (one lane)  TMA producer: A tile 128 x 64 and B tile 256 x 64 per stage (K-major:
+//                      one box of 64 K x rows; MN-major: boxes of 64 MN x 64 K)
 //   warp 1 (one lane)  MMA issuer:   4 x tcgen05.mma (M=128, N=256, K=16) per stage
 //   warp 2             TMEM allocation / release (512 columns = two accumulators)
 //   warps 4..7         epilogue: tcgen05.ld 32 lanes x 32 columns at a time, one
@@ -96,9 +99,25 @@ __device__ __forceinline__ uint64_t desc_kmajor_sw128(uint32_t saddr) {
     return d;
 }
 
-// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, both K-major, M x N.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+// Shared-memory matrix descriptor: MN-major operand written by TMA as boxes of 64 K-rows x
+// 128 B (64 MN elements) with the 128-byte swizzle.  Swizzle atoms are 8 K-rows x 64 MN:
+// atoms along K are 1024 B apart (stride byte offset), atoms along MN one box (8 KB) apart
+// (leading byte offset).
+__device__ __forceinline__ uint64_t desc_mnmajor_sw128(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)(8192 >> 4) << 16;
+    d |= (uint64_t)(1024 >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, M x N; a_mn / b_mn
+// select MN-major ("transposed") A / B.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn = false, bool b_mn = false) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
+           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 // ---- the kernel ---------------------------------------------------------------------------
@@ -124,7 +143,9 @@ __device__ __forceinline__ void tile_coords(const GemmArgs& g, int tile, int& tm
     }
 }
 
-template <class Epi>
+// kAmn / kBmn: the operand is MN-major; its tensor map then has 64 x 64 boxes over a global
+// [K, M] (resp. [K, N]) matrix, and the tile is loaded as BM/64 (resp. BN/64) boxes.
+template <class Epi, bool kAmn = false, bool kBmn = false>
 __global__ void __launch_bounds__(kThreads, 1)
     k_tc_gemm(const __grid_constant__ CUtensorMap mapA0, const __grid_constant__ CUtensorMap mapA1,
               const __grid_constant__ CUtensorMap mapB, const GemmArgs g, const typename Epi::Params ep) {
@@ -181,9 +202,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
                 const bool second = kb >= g.nk_a0;
                 const int ka = second ? kb - g.nk_a0 : kb;
-                tma_load_2d(smA + stage * A_BYTES, second ? &mapA1 : &mapA0, &full[stage], ka * BK,
-                            g.a_y0 + tm * BM);
-                tma_load_2d(smB + stage * B_BYTES, &mapB, &full[stage], g.b_x0 + ka * BK, g.b_y0 + tn * BN);
+                const CUtensorMap* ma = second ? &mapA1 : &mapA0;
+                if (kAmn) {
+#pragma unroll
+                    for (int h = 0; h < BM / 64; ++h)
+                        tma_load_2d(smA + stage * A_BYTES + h * (64 * BK * 2), ma, &full[stage],
+                                    g.a_y0 + tm * BM + h * 64, ka * BK);
+                } else {
+                    tma_load_2d(smA + stage * A_BYTES, ma, &full[stage], ka * BK, g.a_y0 + tm * BM);
+                }
+                if (kBmn) {
+#pragma unroll
+                    for (int h = 0; h < BN / 64; ++h)
+                        tma_load_2d(smB + stage * B_BYTES + h * (64 * BK * 2), &mapB, &full[stage],
+                                    g.b_y0 + tn * BN + h * 64, g.b_x0 + ka * BK);
+                } else {
+                    tma_load_2d(smB + stage * B_BYTES, &mapB, &full[stage], g.b_x0 + ka * BK, g.b_y0 + tn * BN);
+                }
                 issued = issued < STAGES ? issued + 1 : STAGES;
                 if (++stage == STAGES) { stage = 0; phase ^= 1u; }
             }
@@ -200,7 +235,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1 && lane == 0) {
         // ---------------- MMA issuer
-        constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
+        constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, kAmn, kBmn);
+        // one MMA consumes K = 16: 32 B along a K-major row, or 16 K-rows (2 KB) of an MN-major tile
+        constexpr uint32_t kStepA = kAmn ? (2048 >> 4) : (32 >> 4);
+        constexpr uint32_t kStepB = kBmn ? (2048 >> 4) : (32 >> 4);
         int stage = 0;
         uint32_t phase = 0;
         int acc = 0;
@@ -214,11 +252,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int kb = 0; kb < g.nk; ++kb) {
                 if (!mbar_wait(&full[stage], phase, abort_flag, g.err, kErrWaitFull)) { ok = false; break; }
                 tc_fence_after();
-                const uint64_t ad = desc_kmajor_sw128(a0 + stage * A_BYTES);
-                const uint64_t bd = desc_kmajor_sw128(b0 + stage * B_BYTES);
+                const uint64_t ad = kAmn ? desc_mnmajor_sw128(a0 + stage * A_BYTES) : desc_kmajor_sw128(a0 + stage * A_BYTES);
+                const uint64_t bd = kBmn ? desc_mnmajor_sw128(b0 + stage * B_BYTES) : desc_kmajor_sw128(b0 + stage * B_BYTES);
 #pragma unroll
-                for (int k = 0; k < BK / 16; ++k)   // advance 16 elements = 32 B = 2 descriptor units
-                    mma_bf16(d, ad + 2 * k, bd + 2 * k, idesc, (kb | k) != 0);
+                for (int k = 0; k < BK / 16; ++k)   // advance the start address by one K = 16 step
+                    mma_bf16(d, ad + kStepA * k, bd + kStepB * k, idesc, (kb | k) != 0);
                 mma_commit(&empty[stage]);
                 if (++stage == STAGES) { stage = 0; phase ^= 1u; }
             }
