@@ -6,17 +6,18 @@
 // precision).  The CE numerics are those of torchtitan PR #5723 (target-excluded
 // log-sum-exp, softplus NLL, the p_t = 1/4 branch of the target gradient).
 //
-// Steps, all on the tensor cores through tc_gemm.cuh (bf16 operands, fp32 accumulators):
-//   0. E^T and W^T (K-major operands for the two gradient GEMMs)
+// Steps, all on the tensor cores through tc_gemm.cuh (bf16 operands, fp32 accumulators); every
+// operand is read in its natural row-major layout (K-major or MN-major tiles):
 //   1. z = E W^T tile by tile (128 rows x 256 vocabulary columns, K = D); the epilogue keeps
 //      per-row (max, sum-exp) over the tile's non-target columns and the target logit, one
 //      partial per (row, vocabulary tile); a merge gives L', x, the loss and row_stats.
 //   2. per vocabulary chunk of Vc columns:
 //        G = c (softmax - onehot) of the recomputed z tile, split G = G_hi + G_lo in bf16
-//            (a 16-bit significand in total), written as [T, Vc] and [Vc, T];
-//        dW[chunk] = G^T E      (K = 2T: G_hi^T E + G_lo^T E; one complete reduction)
-//        dE      += G W[chunk]  (K = 2Vc), merged across chunks with a two-sum
-//                               compensated fp32 accumulator pair (sum, compensation).
+//            (a 16-bit significand in total), written once as [T, Vc];
+//        dW[chunk] = G^T E      (A = G MN-major, B = E MN-major, K = 2T: G_hi^T E + G_lo^T E;
+//                                one complete reduction)
+//        dE      += G W[chunk]  (A = G K-major, B = W MN-major, K = 2Vc), merged across chunks
+//                               with a two-sum compensated fp32 accumulator pair.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -92,7 +93,7 @@ struct EpiStats {
     }
 };
 
-// Step 2a: G = c * (softmax - onehot) on the chunk's columns, as bf16 hi + lo, both layouts.
+// Step 2a: G = c * (softmax - onehot) on the chunk's columns, as bf16 hi + lo, row-major.
 struct EpiGrad {
     struct Params {
         const int64_t* labels;
@@ -101,8 +102,7 @@ struct EpiGrad {
         const float* grad_output;
         int go_per_row;
         uint16_t *g_hi, *g_lo;       // [T_pad][ldg]
-        uint16_t *gt_hi, *gt_lo;     // [width_pad][ldt]
-        int64_t ldg, ldt;
+        int64_t ldg;
     };
     struct Row {
         float coef, bias, gt;
@@ -125,10 +125,8 @@ struct EpiGrad {
             }
         }
     }
-    // staging row pitch in uint16: 80 bytes, so 16-byte reads of 8 consecutive rows hit 8 distinct bank quads
-    static constexpr int kStageLd = 40;
     __device__ __forceinline__ static void consume(const Params& p, Row& r, int row, int col0,
-                                                   const uint32_t (&acc)[32], uint8_t* wsm) {
+                                                   const uint32_t (&acc)[32], uint8_t*) {
         uint32_t hi[16], lo[16];
 #pragma unroll
         for (int k = 0; k < 32; k += 2) {
@@ -154,29 +152,6 @@ struct EpiGrad {
             dh[q] = make_uint4(hi[4 * q], hi[4 * q + 1], hi[4 * q + 2], hi[4 * q + 3]);
             dl[q] = make_uint4(lo[4 * q], lo[4 * q + 1], lo[4 * q + 2], lo[4 * q + 3]);
         }
-        // transposed [width_pad][ldt]: stage the warp's 32 rows x 32 columns in shared memory,
-        // then each lane writes 64 contiguous bytes (32 rows) of one column
-        uint16_t* sh = reinterpret_cast<uint16_t*>(wsm);          // [32 cols][kStageLd] hi
-        uint16_t* sl = sh + 32 * kStageLd;                         // lo
-        const int lane = threadIdx.x & 31;
-#pragma unroll
-        for (int k = 0; k < 32; ++k) {
-            const uint32_t h = hi[k / 2], l = lo[k / 2];
-            sh[k * kStageLd + lane] = (k & 1) ? (uint16_t)(h >> 16) : (uint16_t)(h & 0xFFFFu);
-            sl[k * kStageLd + lane] = (k & 1) ? (uint16_t)(l >> 16) : (uint16_t)(l & 0xFFFFu);
-        }
-        __syncwarp();
-        const int row0 = row - lane;
-        const uint4* rh = reinterpret_cast<const uint4*>(sh + lane * kStageLd);
-        const uint4* rl = reinterpret_cast<const uint4*>(sl + lane * kStageLd);
-        uint4* th = reinterpret_cast<uint4*>(p.gt_hi + (int64_t)(col0 + lane) * p.ldt + row0);
-        uint4* tl = reinterpret_cast<uint4*>(p.gt_lo + (int64_t)(col0 + lane) * p.ldt + row0);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            th[q] = rh[q];
-            tl[q] = rl[q];
-        }
-        __syncwarp();
     }
     __device__ __forceinline__ static void end(const Params&, Row&, int, int) {}
 };
@@ -311,40 +286,6 @@ struct EpiKahan {
 };
 
 // ------------------------------------------------------------------------------------------
-// transpose [R, C] (ld_in) -> [C, ld_out], rows R <= r < R_pad written as zeros.  64 x 64
-// tiles through shared memory, 16-byte loads and stores (C, ld_in and ld_out multiples of 8,
-// both base pointers 16-byte aligned).
-
-__global__ void __launch_bounds__(256) k_transpose_bf16(const uint16_t* __restrict__ in, int64_t R, int64_t C,
-                                                        int64_t ld_in, uint16_t* __restrict__ out, int64_t R_pad,
-                                                        int64_t ld_out) {
-    __shared__ __align__(16) uint16_t tile[64][72];   // 144-byte rows keep 16-byte alignment
-    const int64_t r0 = (int64_t)blockIdx.y * 64, c0 = (int64_t)blockIdx.x * 64;
-    const int t = threadIdx.x;
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const int v = t + h * 256, rr = v >> 3, cv = v & 7;
-        const int64_t r = r0 + rr, c = c0 + cv * 8;
-        uint4 x = make_uint4(0, 0, 0, 0);
-        if (r < R && c < C) x = *reinterpret_cast<const uint4*>(in + r * ld_in + c);
-        *reinterpret_cast<uint4*>(&tile[rr][cv * 8]) = x;
-    }
-    __syncthreads();
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const int v = t + h * 256, oc = v >> 3, rv = v & 7;
-        const int64_t c = c0 + oc, r = r0 + rv * 8;
-        if (c < C && r < R_pad) {
-            uint32_t w[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-                w[e] = (uint32_t)tile[rv * 8 + 2 * e][oc] | ((uint32_t)tile[rv * 8 + 2 * e + 1][oc] << 16);
-            *reinterpret_cast<uint4*>(out + c * ld_out + r) = make_uint4(w[0], w[1], w[2], w[3]);
-        }
-    }
-}
-
-// ------------------------------------------------------------------------------------------
 // host side
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -392,7 +333,7 @@ cudaError_t run_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUtenso
 
 struct Layout {
     int64_t T, D, V, T_pad, V_pad, Vc, tiles_v;
-    size_t off_et, off_wt, off_part, off_stats, off_ghi, off_glo, off_gthi, off_gtlo, off_sum, off_comp, total;
+    size_t off_part, off_stats, off_ghi, off_glo, off_sum, off_comp, total;
 };
 
 bool layout(int64_t T, int64_t D, int64_t V, Layout* L) {
@@ -411,14 +352,10 @@ bool layout(int64_t T, int64_t D, int64_t V, Layout* L) {
         off += (bytes + 255) & ~size_t(255);
         return o;
     };
-    L->off_et = take((size_t)D * L->T_pad * 2);
-    L->off_wt = take((size_t)D * L->V_pad * 2);
     L->off_part = take((size_t)L->tiles_v * T * 16);
     L->off_stats = take((size_t)T * 16);
     L->off_ghi = take((size_t)L->T_pad * L->Vc * 2);
     L->off_glo = take((size_t)L->T_pad * L->Vc * 2);
-    L->off_gthi = take((size_t)L->Vc * L->T_pad * 2);
-    L->off_gtlo = take((size_t)L->Vc * L->T_pad * 2);
     L->off_sum = take((size_t)T * D * 4);
     L->off_comp = take((size_t)T * D * 4);
     L->total = off;
@@ -456,34 +393,21 @@ extern "C" int linear_ce_fwd_bwd(const void* E, const void* W, int64_t T, int64_
     if (rc) return rc;
 
     uint8_t* ws = static_cast<uint8_t*>(workspace);
-    uint16_t* Et = reinterpret_cast<uint16_t*>(ws + L.off_et);
-    uint16_t* Wt = reinterpret_cast<uint16_t*>(ws + L.off_wt);
     float* part = reinterpret_cast<float*>(ws + L.off_part);
     float* stats = reinterpret_cast<float*>(ws + L.off_stats);
     uint16_t* ghi = reinterpret_cast<uint16_t*>(ws + L.off_ghi);
     uint16_t* glo = reinterpret_cast<uint16_t*>(ws + L.off_glo);
-    uint16_t* gthi = reinterpret_cast<uint16_t*>(ws + L.off_gthi);
-    uint16_t* gtlo = reinterpret_cast<uint16_t*>(ws + L.off_gtlo);
     float* dsum = reinterpret_cast<float*>(ws + L.off_sum);
     float* dcomp = reinterpret_cast<float*>(ws + L.off_comp);
 
     if (cudaMemsetAsync(status, 0, sizeof(int32_t), s) != cudaSuccess) return VCE_ERR_CUDA;
 
-    // 0. transposes
-    {
-        const int blk = 256;
-        k_transpose_bf16<<<dim3((unsigned)cdiv(D, 64), (unsigned)cdiv(L.T_pad, 64)), blk, 0, s>>>(
-            static_cast<const uint16_t*>(E), T, D, D, Et, L.T_pad, L.T_pad);
-        k_transpose_bf16<<<dim3((unsigned)cdiv(D, 64), (unsigned)cdiv(L.V_pad, 64)), blk, 0, s>>>(
-            static_cast<const uint16_t*>(W), V, D, D, Wt, L.V_pad, L.V_pad);
-        if (cudaGetLastError() != cudaSuccess) return VCE_ERR_CUDA;
-    }
-
-    CUtensorMap mE, mW, mEt, mWt, mGhi, mGlo, mGthi, mGtlo;
-    if (!make_map(&mE, E, D, T, D, BM) || !make_map(&mW, W, D, V, D, BN) || !make_map(&mEt, Et, L.T_pad, D, L.T_pad, BN) ||
-        !make_map(&mWt, Wt, L.V_pad, D, L.V_pad, BN) || !make_map(&mGhi, ghi, L.Vc, L.T_pad, L.Vc, BM) ||
-        !make_map(&mGlo, glo, L.Vc, L.T_pad, L.Vc, BM) || !make_map(&mGthi, gthi, L.T_pad, L.Vc, L.T_pad, BM) ||
-        !make_map(&mGtlo, gtlo, L.T_pad, L.Vc, L.T_pad, BM))
+    // K-major maps (box 64 K x rows) and MN-major maps (box 64 MN x 64 K) over row-major matrices
+    CUtensorMap mE, mW, mEmn, mWmn, mGhi, mGlo, mGhi_mn, mGlo_mn;
+    if (!make_map(&mE, E, D, T, D, BM) || !make_map(&mW, W, D, V, D, BN) || !make_map(&mEmn, E, D, T, D, BK) ||
+        !make_map(&mWmn, W, D, V, D, BK) || !make_map(&mGhi, ghi, L.Vc, L.T_pad, L.Vc, BM) ||
+        !make_map(&mGlo, glo, L.Vc, L.T_pad, L.Vc, BM) || !make_map(&mGhi_mn, ghi, L.Vc, L.T_pad, L.Vc, BK) ||
+        !make_map(&mGlo_mn, glo, L.Vc, L.T_pad, L.Vc, BK))
         return VCE_ERR_CUDA;
 
     const int nkD = (int)cdiv(D, BK);
@@ -511,20 +435,20 @@ extern "C" int linear_ce_fwd_bwd(const void* E, const void* W, int64_t T, int64_
         {
             tc::GemmArgs g{tiles_t, (int)(width_pad / BN), nkD, nkD, 0, 0, (int)off, 0, status};
             EpiGrad::Params ep{labels, T, width, off, reinterpret_cast<const float4*>(stats), grad_output,
-                               red == VCE_RED_NONE, ghi, glo, gthi, gtlo, L.Vc, L.T_pad};
+                               red == VCE_RED_NONE, ghi, glo, L.Vc};
             if (run_gemm<EpiGrad>(mE, mE, mW, g, ep, s) != cudaSuccess) return VCE_ERR_CUDA;
         }
-        {   // dW[off : off + width] = G^T E, K = 2 T_pad (hi then lo)
+        {   // dW[off : off + width] = G^T E: A = G (MN-major), B = E (MN-major), K = 2 T_pad (hi then lo)
             const int nkT = (int)(L.T_pad / BK);
             tc::GemmArgs g{(int)(width_pad / BM), (int)cdiv(D, BN), 2 * nkT, nkT, 0, 0, 0, 1, status};
             EpiStore::Params ep{dW, D, width, D, off, grad_dt == VCE_BF16};
-            if (run_gemm<EpiStore>(mGthi, mGtlo, mEt, g, ep, s) != cudaSuccess) return VCE_ERR_CUDA;
+            if (run_gemm<EpiStore, true, true>(mGhi_mn, mGlo_mn, mEmn, g, ep, s) != cudaSuccess) return VCE_ERR_CUDA;
         }
-        {   // dE += G W[off : off + width], K = 2 width (hi then lo)
+        {   // dE += G W[off : off + width]: A = G (K-major), B = W rows (MN-major), K = 2 width (hi then lo)
             const int nkc = (int)cdiv(width, BK);
             tc::GemmArgs g{tiles_t, (int)cdiv(D, BN), 2 * nkc, nkc, (int)off, 0, 0, 1, status};
             EpiKahan::Params ep{dsum, dcomp, T, D, ci == 0, ci == nchunks - 1, dE, grad_dt == VCE_BF16};
-            if (run_gemm<EpiKahan>(mGhi, mGlo, mWt, g, ep, s) != cudaSuccess) return VCE_ERR_CUDA;
+            if (run_gemm<EpiKahan, false, true>(mGhi, mGlo, mWmn, g, ep, s) != cudaSuccess) return VCE_ERR_CUDA;
         }
     }
     return VCE_OK;
