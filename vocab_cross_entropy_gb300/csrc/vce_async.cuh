@@ -1,6 +1,6 @@
-// Asynchronous-copy and mbarrier helpers (hand-written PTX) shared by the TMA-fed kernels:
+// Asynchronous-copy and mbarrier helpers (hand-written PTX) for the TMA-fed kernels:
 // shared-memory addresses, mbarrier init / arrive / bounded wait, tiled TMA loads
-// (cp.async.bulk.tensor) and plain bulk copies (cp.async.bulk).
+// (cp.async.bulk.tensor).
 #pragma once
 
 #include <cuda.h>
@@ -74,26 +74,6 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
 
 __device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
-}
-
-// 1-D bulk copy global -> shared, completion counted in bytes on `bar`.  Both addresses
-// 16-byte aligned, bytes a multiple of 16.
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            smem_u32(dst)),
-        "l"(src), "r"(bytes), "r"(smem_u32(bar))
-        : "memory");
-}
-
-// Not volatile: the compiler may schedule it freely; the mbarrier waits that precede a reuse
-// of the same shared address carry a memory clobber, so no stale value is reused.
-__device__ __forceinline__ uint4 lds128(const void* p) {
-    uint4 r;
-    asm("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-                 : "r"(smem_u32(p)));
-    return r;
 }
 
 }  // namespace tc
