@@ -71,6 +71,18 @@ int linear_ce_fwd_bwd(const void* E, const void* W, int64_t T, int64_t D, int64_
 int vce_gemm_bf16(const void* A, int a_mn, const void* B, int b_mn, int64_t M, int64_t N, int64_t K,
                   float* C, int64_t ldc, vce_stream_t s);
 
+/*
+ * vce_test_gemm_stall -- test hook for the GEMM's give-up path (no page counterpart).
+ * Runs vce_gemm_bf16's pipeline (A [M,K], B [N,K] K-major) with its producer announcing 16
+ * more bytes per stage than its copies deliver, so no stage ever completes.  Every wait of
+ * the kernel is bounded by wait_ns (1 ms .. 2 s): the waiting role gives up, writes its code
+ * to *status (101 empty-slot, 102 full-slot, 103 accumulator-free, 104 accumulator-full
+ * wait), the other roles stop, copies in flight are drained, tensor memory is released and
+ * the kernel returns; the context stays usable.  C's contents are undefined afterwards.
+ */
+int vce_test_gemm_stall(const void* A, const void* B, int64_t M, int64_t N, int64_t K, float* C,
+                        uint64_t wait_ns, int32_t* status, vce_stream_t s);
+
 #ifdef __cplusplus
 }
 #endif

@@ -31,3 +31,23 @@ def test_gemm_layouts(vce, a_mn, b_mn, M, N, K):
     bound = 2.0 ** -20 * (np.abs(Am) @ np.abs(Bm).T) + 1e-30
     err = np.abs(C.cpu().numpy().astype(np.float64) - want)
     assert np.all(err <= bound), f"max err/bound {np.max(err / bound):.3g}"
+
+
+def test_stalled_pipeline_gives_up_and_the_context_survives(vce):
+    """A stage that never completes: the bounded waits give up with a status code, the kernel
+    returns, and the next GEMM on the same context is correct."""
+    import time
+    rng = np.random.default_rng(5)
+    A, A64 = _bf16(rng, (256, 128))
+    B, B64 = _bf16(rng, (512, 128), 0.05)
+    Ad, Bd = A.cuda(), B.cuda()
+    t0 = time.time()
+    status = vce.vce_test_gemm_stall(Ad, Bd, wait_ns=50_000_000)
+    assert status in (101, 102, 103, 104), status
+    assert "gave up" in vce.vce_status_string(status)
+    assert time.time() - t0 < 60
+    C = vce.vce_gemm_bf16(Ad, Bd)
+    torch.cuda.synchronize()
+    want = A64 @ B64.T
+    bound = 2.0 ** -20 * (np.abs(A64) @ np.abs(B64).T) + 1e-30
+    assert np.all(np.abs(C.cpu().numpy().astype(np.float64) - want) <= bound)

@@ -60,6 +60,8 @@ def _load():
         L.linear_ce_fwd_bwd.argtypes = [p, p, i64, i64, i64, p, i64, i32, p, p, p, p, p, i32, p, sz, p, p]
         L.vce_gemm_bf16.argtypes = [p, i32, p, i32, i64, i64, i64, p, i64, p]
         L.vce_gemm_bf16.restype = i32
+        L.vce_test_gemm_stall.argtypes = [p, p, i64, i64, i64, p, ctypes.c_uint64, p, p]
+        L.vce_test_gemm_stall.restype = i32
     for name in ("ce_forward", "ce_backward", "ce_forward_ls", "ce_backward_ls", "ce_forward_backward",
                  "ce_merge_chunks", "ce_merge_chunks_noalloc",
                  "linear_ce_fwd_bwd",
@@ -283,6 +285,17 @@ def vce_gemm_bf16(A, B, a_mn=False, b_mn=False, *, C=None, stream=None):
     _check("vce_gemm_bf16", _get().vce_gemm_bf16(_ptr(A), int(a_mn), _ptr(B), int(b_mn), M, N, K, _ptr(C),
                                               C.stride(0), _stream(stream)))
     return C
+
+
+def vce_test_gemm_stall(A, B, wait_ns=50_000_000, *, stream=None):
+    """Run the GEMM pipeline with a stage that never completes; returns the device status word."""
+    M, K = A.shape
+    N = B.shape[0]
+    C = torch.empty(M, N, dtype=torch.float32, device=A.device)
+    status = torch.empty(1, dtype=torch.int32, device=A.device)
+    _check("vce_test_gemm_stall", _get().vce_test_gemm_stall(_ptr(A), _ptr(B), M, N, K, _ptr(C), int(wait_ns),
+                                                          _ptr(status), _stream(stream)))
+    return vce_get_status(status, stream)
 
 
 def linear_ce_workspace_bytes(T, D, V) -> int:

@@ -477,3 +477,21 @@ extern "C" int vce_gemm_bf16(const void* A, int a_mn, const void* B, int b_mn, i
     else e = run_gemm<EpiStore, false, false>(ma, ma, mb, g, ep, s);
     return e == cudaSuccess ? VCE_OK : VCE_ERR_CUDA;
 }
+
+extern "C" int vce_test_gemm_stall(const void* A, const void* B, int64_t M, int64_t N, int64_t K, float* C,
+                                   uint64_t wait_ns, int32_t* status, vce_stream_t s) {
+    if (!A || !B || !C || !status) return VCE_ERR_NULL;
+    if (M < 1 || N < 1 || K < 1 || (M % 8) || (N % 8) || (K % 8) || M > (1 << 20) || N > (1 << 20) || K > (1 << 20))
+        return VCE_ERR_SHAPE;
+    if (wait_ns < 1000000ull || wait_ns > 2000000000ull) return VCE_ERR_ARG;   // 1 ms .. 2 s
+    if (!aligned(A, 16) || !aligned(B, 16) || !aligned(C, 16)) return VCE_ERR_ALIGN;
+    int rc = require_sm100();
+    if (rc) return rc;
+    CUtensorMap ma, mb;
+    if (!make_map(&ma, A, K, M, K, BM) || !make_map(&mb, B, K, N, K, BN)) return VCE_ERR_CUDA;
+    if (cudaMemsetAsync(status, 0, sizeof(int32_t), s) != cudaSuccess) return VCE_ERR_CUDA;
+    const int nk = (int)cdiv(K, BK);
+    tc::GemmArgs g{(int)cdiv(M, BM), (int)cdiv(N, BN), nk, nk, 0, 0, 0, 0, status, 16u, wait_ns};
+    EpiStore::Params ep{C, N, M, N, 0, 0};
+    return run_gemm<EpiStore>(ma, ma, mb, g, ep, s) == cudaSuccess ? VCE_OK : VCE_ERR_CUDA;
+}

@@ -131,6 +131,9 @@ struct GemmArgs {
     int n_fastest;          // tile order: 0 = m fastest (blocks in flight share B tiles),
                             //             1 = n fastest (blocks in flight share A tiles)
     int32_t* err;           // error word (wait timeouts)
+    uint32_t tx_extra;      // bytes announced per stage beyond the copies (0; > 0 only to test the
+                            // give-up path: the stage never completes and the waits must time out)
+    uint64_t wait_ns;       // limit of every wait (0: kWaitNs)
 };
 
 __device__ __forceinline__ void tile_coords(const GemmArgs& g, int tile, int& tm, int& tn) {
@@ -188,6 +191,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const int ntiles = g.tiles_m * g.tiles_n;
+    const uint64_t wns = g.wait_ns ? g.wait_ns : kWaitNs;
 
     if (warp == 0 && lane == 0) {
         // ---------------- TMA producer
@@ -198,8 +202,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             int tm, tn;
             tile_coords(g, tile, tm, tn);
             for (int kb = 0; kb < g.nk; ++kb) {
-                if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, g.err, kErrWaitEmpty)) break;
-                mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
+                if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, g.err, kErrWaitEmpty, wns)) break;
+                mbar_arrive_expect_tx(&full[stage], STAGE_BYTES + g.tx_extra);
                 const bool second = kb >= g.nk_a0;
                 const int ka = second ? kb - g.nk_a0 : kb;
                 const CUtensorMap* ma = second ? &mapA1 : &mapA0;
@@ -229,7 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < issued; ++i) {
                 if (--stage < 0) { stage = STAGES - 1; phase ^= 1u; }
                 const uint64_t t0 = globaltimer();
-                while (!mbar_try_wait(&full[stage], phase) && globaltimer() - t0 < kWaitNs) {
+                while (!mbar_try_wait(&full[stage], phase) && globaltimer() - t0 < wns) {
                 }
             }
         }
@@ -245,12 +249,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t acc_phase = 0;
         const uint32_t a0 = smem_u32(smA), b0 = smem_u32(smB);
         for (int tile = blockIdx.x; tile < ntiles && !*abort_flag; tile += gridDim.x) {
-            if (!mbar_wait(&acc_free[acc], acc_phase ^ 1u, abort_flag, g.err, kErrWaitAccFree)) break;
+            if (!mbar_wait(&acc_free[acc], acc_phase ^ 1u, abort_flag, g.err, kErrWaitAccFree, wns)) break;
             tc_fence_after();
             const uint32_t d = tmem_base + (uint32_t)(acc * BN);
             bool ok = true;
             for (int kb = 0; kb < g.nk; ++kb) {
-                if (!mbar_wait(&full[stage], phase, abort_flag, g.err, kErrWaitFull)) { ok = false; break; }
+                if (!mbar_wait(&full[stage], phase, abort_flag, g.err, kErrWaitFull, wns)) { ok = false; break; }
                 tc_fence_after();
                 const uint64_t ad = kAmn ? desc_mnmajor_sw128(a0 + stage * A_BYTES) : desc_kmajor_sw128(a0 + stage * A_BYTES);
                 const uint64_t bd = kBmn ? desc_mnmajor_sw128(b0 + stage * B_BYTES) : desc_kmajor_sw128(b0 + stage * B_BYTES);
@@ -268,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // every MMA this thread issued has finished before TMEM can be released
         mma_commit(drain);
         const uint64_t t0 = globaltimer();
-        while (!mbar_try_wait(drain, 0) && globaltimer() - t0 < kWaitNs) {
+        while (!mbar_try_wait(drain, 0) && globaltimer() - t0 < wns) {
         }
     } else if (warp >= 4) {
         // ---------------- epilogue: thread = accumulator row
@@ -276,7 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
-            if (!mbar_wait(&acc_full[acc], acc_phase, abort_flag, g.err, kErrWaitAccFull)) break;
+            if (!mbar_wait(&acc_full[acc], acc_phase, abort_flag, g.err, kErrWaitAccFull, wns)) break;
             tc_fence_after();
             int tm, tn;
             tile_coords(g, tile, tm, tn);

@@ -64,6 +64,10 @@ extern "C" const char* vce_status_string(int status) {
         case VCE_ERR_ARG: return "invalid argument";
         case VCE_ERR_DEVICE: return "the current device is not an sm_100-family GPU";
         case VCE_ERR_SCRATCH_LIMIT: return "k * T exceeds the built-in scratch of ce_merge_chunks_noalloc";
+        case 101: return "a GEMM pipeline wait for a free shared-memory stage gave up";
+        case 102: return "a GEMM pipeline wait for a loaded shared-memory stage gave up";
+        case 103: return "a GEMM pipeline wait for a free accumulator gave up";
+        case 104: return "a GEMM pipeline wait for a finished accumulator gave up";
         default: return "unknown status";
     }
 }

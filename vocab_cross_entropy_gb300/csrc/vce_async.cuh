@@ -47,16 +47,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Wait for the phase of `bar` with the given parity to complete.  Gives up after kWaitNs or
+// Wait for the phase of `bar` with the given parity to complete.  Gives up after wait_ns or
 // as soon as another role of the block has given up; returns false then.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          int32_t* err, int code) {
+                                          int32_t* err, int code, uint64_t wait_ns = kWaitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
-        if (globaltimer() - t0 > kWaitNs) {
+        if (globaltimer() - t0 > wait_ns) {
             *abort_flag = 1;
             if (err) atomicCAS(err, 0, code);
             return false;
