@@ -32,15 +32,13 @@ __device__ __forceinline__ uint4 ld_stream16(const void* p) {
 }
 
 // 16-byte loads with an L2 policy: kLoadStream as ld_stream16; kLoadKeep marks the lines
-// evict-last (the same row is read again shortly, by the fused forward+backward);
-// kLoadLast marks them evict-first (that second, final read).
-enum { kLoadStream = 0, kLoadKeep = 1, kLoadLast = 2 };
+// evict-last (the same row is read again shortly, by the one-pass forward+backward).
+enum { kLoadStream = 0, kLoadKeep = 1 };
 
 template <int kLoad>
 __device__ __forceinline__ uint64_t l2_policy() {
     uint64_t pol = 0;
     if (kLoad == kLoadKeep) asm("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
-    if (kLoad == kLoadLast) asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
     return pol;
 }
 
