@@ -5,6 +5,7 @@ import torch
 
 import gen
 from oracle import ce_oracle as O
+from oracle import rounding as R
 from tests import _grading as G
 
 pytestmark = pytest.mark.gpu
@@ -316,3 +317,32 @@ def test_pages_shape_other_dtypes_sampled(vce, dtype, gdt, reduction):
     G.check_grad_f32(got, want)
     raised = np.isin(rows, p.margin_rows)
     G.check_target_entries(got[raised, p.labels[rows][raised]], want[raised, p.labels[rows][raised]])
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_non_target_spikes_take_the_rescale_path(vce, dtype):
+    """Non-target values far above the rest (late in the row, and one early) force the forward's
+    running reference to be replaced mid-row; results must still match the oracle."""
+    p = gen.custom(24, 20000, dtype, seed=33, std=2.0, n_margin=4, margin=(17.0, 50.0), n_ignore=2)
+    storage = p.full().copy()
+    z = O.widen(storage, dtype)
+    rng = np.random.default_rng(4)
+    for i in range(p.T):
+        if p.labels[i] == p.ignore_index:
+            continue
+        for bump, pos in ((30.0, 19000), (60.0, 15000), (90.0, 7), (45.0, 12345)):
+            j = (pos + i) % p.V
+            if j == p.labels[i]:
+                continue
+            z[i, j] = z[i].max() + bump + rng.uniform(0, 1)
+    if dtype == "f32":
+        storage = z.astype(np.float32)
+    else:
+        storage = R.bf16_bits(R.round_bf16(z))
+    ref = O.ce(O.widen(storage, dtype), p.labels, "mean")
+    logits = to_device(storage, dtype)
+    loss_out, loss_rows, stats, status, grad = run_ce(vce, logits, p.labels)
+    assert vce.vce_get_status(status) == 0
+    G.check_loss_rows(loss_rows.cpu().numpy(), ref["loss_rows"], ref["valid"])
+    G.check_reduced(loss_out.item(), ref["loss_out"])
+    grade_grad(grad, ref["grad"])
