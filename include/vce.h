@@ -167,14 +167,22 @@ int ce_backward_ls(const void* logits, vce_dtype dt, int64_t T, int64_t V, int64
  * ce_forward_backward -- ce_forward followed by ce_backward in one pass over the logits, for
  * callers that know grad_output when the forward runs (e.g. a mean loss seeded by 1).
  * [TT, Numerics; Memory/perf: the forward prepares the backward]  Same arguments, results
- * and per-row numerics as the two calls (bitwise equal outputs); each row is read from HBM
- * once and re-read for its gradient from L2, so HBM moves V*e in and V*e_g out per row.
- * For reduction MEAN, *loss_out holds 1/N while the call's work runs and the mean loss when
- * it is done.
+ * and per-row numerics as the two calls, with the row's sum of exponentials taken in another
+ * fp32 order (so equal to the two calls up to that rounding, and bitwise reproducible from
+ * run to run).  Each row is read from HBM once: where V, ld and ld_grad are multiples of 8
+ * and logits and grad_logits are 16-byte aligned, a cluster of up to 8 CTAs holds the row in
+ * shared memory between its two passes [MC, VocabParallelCrossEntropy: the vocabulary split
+ * with a (max, sum-exp, target) exchange]; otherwise the gradient pass re-reads the row from
+ * L2.  HBM moves V*e in and V*e_g out per row.  For reduction MEAN, *loss_out holds 1/N
+ * while the call's work runs and the mean loss when it is done.
  *
  *   logits, dt, T, V, ld, labels, ignore_index, red: as ce_forward
  *   grad_output  fp32 [1] (SUM, MEAN) or [T] (NONE), read on the device
- *   loss_rows, loss_out, row_stats, status: as ce_forward (row_stats carries the weights)
+ *   loss_rows, loss_out, row_stats: as ce_forward (row_stats carries the weights)
+ *   status       as ce_forward, or 105..109 when a device-side wait of the shared-memory
+ *                path gave up after 2 s (105 free stage, 106 loaded stage, 107 the cluster's
+ *                row statistics, 108 the warps' partial statistics, 109 a row's gradient
+ *                coefficients); the outputs are then undefined
  *   grad_logits  [T, ld_grad] of dtype grad_dt, written; must not overlap the logits
  */
 int ce_forward_backward(const void* logits, vce_dtype dt, int64_t T, int64_t V, int64_t ld,

@@ -3,12 +3,15 @@
 //
 // Method: torchtitan PR #5723 "[loss] fix softmax collapse with improved ce perf" — the same
 // numerics as ce_forward / ce_backward (Numerics: target-excluded log-sum-exp, softplus NLL,
-// the p_t = 1/4 branch; Memory/perf: "forward also prepares the backward").  Each block takes
-// one row: the forward stream reads it from HBM with an evict-last L2 policy, the block
-// reduces it to the row statistics, and the backward stream re-reads the same row (mostly an
-// L2 hit) to write the gradient.  Measured on the pages' shape: without the evict-last policy
-// the step takes 12% longer; an evict-first policy on the re-read costs 1.4%.  HBM moves V*e bytes in and V*e_g out per row,
-// instead of 2*V*e in and V*e_g out for the two separate calls.
+// the p_t = 1/4 branch; Memory/perf: "forward also prepares the backward").
+//
+// Rows whose layout suits 16-byte bulk copies go to the kernel in ce_ring.cu, which holds each
+// row in shared memory between its passes.  The others come here: each block takes one row,
+// the forward stream reads it from HBM with an evict-last L2 policy, the block reduces it to
+// the row statistics, and the backward stream re-reads the same row (mostly an L2 hit) to
+// write the gradient.  Measured at T=16384, V=128256 bf16: without the evict-last policy the
+// step takes 12% longer; an evict-first policy on the re-read costs 1.4%.  HBM moves V*e bytes
+// in and V*e_g out per row, instead of 2*V*e in and V*e_g out for the two separate calls.
 //
 //   k_ce_count_valid  one block: 1/N for the mean, parked in loss_out[0] until k_ce_reduce
 //                     replaces it by the mean loss
@@ -145,20 +148,25 @@ extern "C" int ce_forward_backward(const void* logits, vce_dtype dt, int64_t T, 
             k_ce_count_valid<1024><<<1, 1024, 0, s>>>(labels, T, V, ignore_index, loss_out);
             if (cudaGetLastError() != cudaSuccess) return VCE_ERR_CUDA;
         }
-        const int nt = pick_threads(V * (int64_t)es);
-        cudaError_t e;
-        if (dt == VCE_BF16 && grad_dt == VCE_BF16)
-            e = dispatch_fused2<uint16_t, uint16_t>(nt, logits, T, V, ld, labels, ignore_index, red, grad_output,
-                                                    loss_out, loss_rows, row_stats, grad_logits, ld_grad, status, s);
-        else if (dt == VCE_BF16)
-            e = dispatch_fused2<uint16_t, float>(nt, logits, T, V, ld, labels, ignore_index, red, grad_output, loss_out,
-                                                 loss_rows, row_stats, grad_logits, ld_grad, status, s);
-        else if (grad_dt == VCE_BF16)
-            e = dispatch_fused2<float, uint16_t>(nt, logits, T, V, ld, labels, ignore_index, red, grad_output, loss_out,
-                                                 loss_rows, row_stats, grad_logits, ld_grad, status, s);
-        else
-            e = dispatch_fused2<float, float>(nt, logits, T, V, ld, labels, ignore_index, red, grad_output, loss_out,
-                                              loss_rows, row_stats, grad_logits, ld_grad, status, s);
+        // The row held in shared memory where the layout allows it, else the L2 re-read.
+        bool launched = false;
+        cudaError_t e = launch_fused_ring(dt, grad_dt, logits, T, V, ld, labels, ignore_index, red, grad_output,
+                                          loss_out, loss_rows, row_stats, grad_logits, ld_grad, status, s, &launched);
+        if (e == cudaSuccess && !launched) {
+            const int nt = pick_threads(V * (int64_t)es);
+            if (dt == VCE_BF16 && grad_dt == VCE_BF16)
+                e = dispatch_fused2<uint16_t, uint16_t>(nt, logits, T, V, ld, labels, ignore_index, red, grad_output,
+                                                        loss_out, loss_rows, row_stats, grad_logits, ld_grad, status, s);
+            else if (dt == VCE_BF16)
+                e = dispatch_fused2<uint16_t, float>(nt, logits, T, V, ld, labels, ignore_index, red, grad_output,
+                                                     loss_out, loss_rows, row_stats, grad_logits, ld_grad, status, s);
+            else if (grad_dt == VCE_BF16)
+                e = dispatch_fused2<float, uint16_t>(nt, logits, T, V, ld, labels, ignore_index, red, grad_output,
+                                                     loss_out, loss_rows, row_stats, grad_logits, ld_grad, status, s);
+            else
+                e = dispatch_fused2<float, float>(nt, logits, T, V, ld, labels, ignore_index, red, grad_output, loss_out,
+                                                  loss_rows, row_stats, grad_logits, ld_grad, status, s);
+        }
         if (e != cudaSuccess) return VCE_ERR_CUDA;
     }
     if (red != VCE_RED_NONE &&

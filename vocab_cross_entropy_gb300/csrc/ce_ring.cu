@@ -1,0 +1,479 @@
+// One-pass cross-entropy forward and backward with every row held on chip between its two
+// passes, so HBM moves exactly one read of the logits and one write of the gradient.
+//
+// Method: torchtitan PR #5723 "[loss] fix softmax collapse with improved ce perf" — the same
+// numerics as ce_forward / ce_backward (Numerics: target-excluded log-sum-exp, softplus NLL,
+// the p_t = 1/4 branch; Memory/perf: "forward also prepares the backward").  The vocabulary
+// split across a thread-block cluster is the single-GPU form of the Megatron-core
+// vocab-parallel cross-entropy (Cross Entropy Loss / VocabParallelCrossEntropy: each part
+// reduces its own columns, the parts exchange (max, sum-exp, target logit), every part
+// writes its own gradient columns).
+//
+// A row of a 128256-entry vocabulary in bf16 (250.5 KB) does not fit one SM's shared memory,
+// so a cluster of C CTAs on C SMs takes it, each CTA a column slice of at most 4 ring stages.
+// Each CTA (one per SM) walks the valid rows of its cluster in order, with three roles:
+//   producer warp   one lane streams each row's slice into a ring of seven 32 KB shared-memory
+//                   stages with bulk asynchronous copies (cp.async.bulk; completion counted
+//                   on a per-stage mbarrier), running ahead into later rows as stages free up
+//   consumer warps  forward of a row over its held stages (per-thread (max, sum-exp) pairs,
+//                   the target masked out by its column), each warp's pair published to shared
+//                   memory; then, while the row's statistics are being finished, the forward
+//                   of the next row over the stages already loaded beside it; then the
+//                   row's gradient from its held stages, releasing each stage to the producer;
+//                   then the rest of the next row's forward
+//   stats warp      per row: merges the consumer warps' pairs, exchanges the slice pair with
+//                   the cluster's other CTAs through distributed shared memory (each CTA stores
+//                   its pair into every peer and arrives on the peer's mbarrier), merges the C
+//                   pairs in rank order (identically in every CTA), finishes the row, and
+//                   publishes the gradient coefficients
+// so the exchange and the row finish run while the consumers stream the next row.  Row
+// hand-offs go through mbarriers only, double-buffered by the parity of the row's index in
+// the CTA's sequence: a slot of one parity is rewritten two rows later, after every reader of
+// it has arrived on a barrier the writer waits for.
+//
+// Every wait is bounded (2 s).  A wait that gives up writes its code to the status word
+// (105 free stage, 106 loaded stage, 107 cluster exchange, 108 warp partials, 109 row
+// coefficients) and sets the CTA's abort flag; the CTA then keeps every arrival (stage
+// releases, exchange, hand-offs) but skips the work and later waits, so no peer or warp is
+// left waiting on it, and the producer waits, again bounded, for its copies in flight before
+// the CTA reaches the closing cluster barrier.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <algorithm>
+#include <atomic>
+
+#include "ce_segments.h"
+#include "vce.h"
+#include "vce_async.cuh"
+#include "vce_device.cuh"
+#include "vce_host.h"
+
+namespace vce {
+namespace ring {
+
+constexpr int kChunk = 32768;          // bytes per stage (one bulk copy)
+constexpr int kStages = 7;
+constexpr int kSliceStages = 4;        // a slice occupies at most this many stages
+constexpr int kConsumerWarps = 16;
+constexpr int kConsumers = kConsumerWarps * 32;
+constexpr int kProducerWarp = kConsumerWarps, kStatsWarp = kConsumerWarps + 1;
+constexpr int kThreads = kConsumers + 64;
+constexpr int kMaxCluster = 8;
+constexpr int kMaxDevices = 64;
+constexpr int kVecPerThread = (kChunk / 16 + kConsumers - 1) / kConsumers;   // 16-B vectors per consumer per stage
+enum { kErrEmpty = 105, kErrFull = 106, kErrExchange = 107, kErrPartials = 108, kErrCoefs = 109 };
+
+struct alignas(16) Ctl {
+    float4 slot[2][kMaxCluster];       // (m, s, z_t, owner) of each CTA of the cluster
+    float4 coefs[2];                   // (coef, bias, target gradient, -) of the row
+    float red_m[2][kConsumerWarps], red_s[2][kConsumerWarps];
+    float zt[2];
+    uint64_t full[kStages];            // stage loaded (producer's expect-tx + the copy's bytes)
+    uint64_t empty[kStages];           // stage released (one arrival per consumer warp)
+    uint64_t xbar[2];                  // cluster pairs stored (one arrival per CTA)
+    uint64_t rbar[2];                  // warp pairs published (one arrival per consumer warp)
+    uint64_t cbar[2];                  // coefficients published (the stats warp)
+    int abort;
+};
+constexpr int kSmemBytes = kStages * kChunk + (int)sizeof(Ctl);
+
+struct Args {
+    const void* logits;
+    int64_t T, V, ld;
+    const int64_t* labels;
+    int64_t ignore_index;
+    int red;
+    const float* grad_output;
+    const float* inv_n;
+    float* loss_rows;
+    float4* row_stats;
+    void* grad;
+    int64_t ld_g;
+    int32_t* status;
+    int64_t slice;                     // columns per CTA (a multiple of 8)
+    uint64_t wait_ns;
+};
+
+// ---- cluster and bulk-copy primitives (inline PTX) -----------------------------------------
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+// The address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t peer_addr(const void* p, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(tc::smem_u32(p)), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void st_peer(uint32_t addr, float4 v) {
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x), "f"(v.y), "f"(v.z),
+                 "f"(v.w)
+                 : "memory");
+}
+__device__ __forceinline__ void arrive_peer(uint32_t bar_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_addr) : "memory");
+}
+__device__ __forceinline__ bool try_wait_cluster(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(tc::smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            tc::smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(tc::smem_u32(bar))
+        : "memory");
+}
+__device__ __forceinline__ uint4 lds16(const void* p) {
+    uint4 r;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "r"(tc::smem_u32(p)));
+    return r;
+}
+
+// Bounded wait on a phase of an mbarrier written by peers of the cluster.
+__device__ __forceinline__ bool wait_exchange(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                              int32_t* err, uint64_t wait_ns) {
+    if (*abort_flag) return false;
+    const uint64_t t0 = tc::globaltimer();
+    while (!try_wait_cluster(bar, parity)) {
+        if (*abort_flag) return false;
+        if (tc::globaltimer() - t0 > wait_ns) {
+            *abort_flag = 1;
+            if (err) atomicCAS(err, 0, (int32_t)kErrExchange);
+            return false;
+        }
+    }
+    return true;
+}
+
+__device__ __forceinline__ bool label_valid(const Args& a, int64_t t) {
+    return t != a.ignore_index && t >= 0 && t < a.V;
+}
+// The first row with a valid label among row, row + stride, ...; T if none.
+__device__ __forceinline__ int64_t next_valid(const Args& a, int64_t row, int64_t stride) {
+    for (; row < a.T; row += stride)
+        if (label_valid(a, a.labels[row])) return row;
+    return a.T;
+}
+
+// ---- the kernel -----------------------------------------------------------------------------
+
+template <typename S, typename O, int C>
+__global__ void __launch_bounds__(kThreads, 1) k_ce_fused_ring(const __grid_constant__ Args a) {
+    constexpr int G = Elt<S>::kGroup;
+    extern __shared__ __align__(128) uint8_t smem[];
+    Ctl& ctl = *reinterpret_cast<Ctl*>(smem + kStages * kChunk);
+    volatile int* abort_flag = &ctl.abort;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = C > 1 ? cluster_rank() : 0;
+    const int64_t cid = blockIdx.x / C, ncl = gridDim.x / C;
+    const int64_t c0 = std::min<int64_t>(a.V, (int64_t)rank * a.slice);
+    const int w = (int)(std::min<int64_t>(a.V, c0 + a.slice) - c0);   // this CTA's columns [c0, c0 + w)
+    const int bytes = w * (int)sizeof(S);
+    const int nchunk = (bytes + kChunk - 1) / kChunk;
+    // chunks of the next row that fit beside a held row (all of them for short slices)
+    const int pre = std::min(nchunk, kStages - nchunk);
+
+    if (threadIdx.x == 0) {
+        for (int st = 0; st < kStages; ++st) {
+            tc::mbar_init(&ctl.full[st], 1);
+            tc::mbar_init(&ctl.empty[st], kConsumerWarps);
+        }
+        for (int p = 0; p < 2; ++p) {
+            tc::mbar_init(&ctl.xbar[p], C);
+            tc::mbar_init(&ctl.rbar[p], kConsumerWarps);
+            tc::mbar_init(&ctl.cbar[p], 1);
+        }
+        ctl.abort = 0;
+        tc::fence_mbar_init();
+    }
+    if (C > 1) cluster_sync();   // peers arrive on these barriers from now on
+    else __syncthreads();
+
+    if (warp == kProducerWarp) {
+        // ---------------- producer ----------------
+        if (lane == 0) {
+            uint32_t q = 0;
+            for (int64_t row = next_valid(a, cid, ncl); row < a.T && !*abort_flag;
+                 row = next_valid(a, row + ncl, ncl)) {
+                const char* src = static_cast<const char*>(a.logits) + (row * a.ld + c0) * (int64_t)sizeof(S);
+                for (int j = 0; j < nchunk; ++j) {
+                    const int st = (int)(q % kStages);
+                    if (!tc::mbar_wait(&ctl.empty[st], ((q / kStages) & 1) ^ 1, abort_flag, a.status, kErrEmpty,
+                                       a.wait_ns))
+                        break;
+                    const uint32_t nb = (uint32_t)min(kChunk, bytes - j * kChunk);
+                    tc::mbar_arrive_expect_tx(&ctl.full[st], nb);
+                    bulk_load(smem + st * kChunk, src + (int64_t)j * kChunk, nb, &ctl.full[st]);
+                    ++q;
+                }
+            }
+            // Copies still in flight (only after an abort) land before the CTA may exit.
+            int never = 0;
+            for (uint32_t p = q > (uint32_t)kStages ? q - kStages : 0; p < q; ++p)
+                tc::mbar_wait(&ctl.full[p % kStages], (p / kStages) & 1, &never, nullptr, 0, a.wait_ns);
+        }
+        __syncwarp();
+    } else if (warp == kStatsWarp) {
+        // ---------------- row statistics ----------------
+        const float w_valid = (a.red == VCE_RED_MEAN) ? *a.inv_n : 1.f;
+        uint32_t e = 0;
+        for (int64_t row = next_valid(a, cid, ncl); row < a.T; row = next_valid(a, row + ncl, ncl), ++e) {
+            const int par = (int)(e & 1);
+            const uint32_t ph = (e >> 1) & 1;
+            tc::mbar_wait(&ctl.rbar[par], ph, abort_flag, a.status, kErrPartials, a.wait_ns);
+            float m = lane < kConsumerWarps ? ctl.red_m[par][lane] : -kInf;
+            float s = lane < kConsumerWarps ? ctl.red_s[par][lane] : 0.f;
+            ms_warp_reduce(m, s);
+            if (lane == 0) {
+                const bool own = (uint64_t)(a.labels[row] - c0) < (uint64_t)w;
+                float M = m, Ssum = s, zt = own ? ctl.zt[par] : 0.f;
+                if (C > 1) {
+                    const float4 mine = make_float4(m, s, zt, own ? 1.f : 0.f);
+                    for (uint32_t r = 0; r < (uint32_t)C; ++r) st_peer(peer_addr(&ctl.slot[par][rank], r), mine);
+                    for (uint32_t r = 0; r < (uint32_t)C; ++r) arrive_peer(peer_addr(&ctl.xbar[par], r));
+                    wait_exchange(&ctl.xbar[par], ph, abort_flag, a.status, a.wait_ns);
+                    M = -kInf;
+                    Ssum = 0.f;
+                    for (int r = 0; r < C; ++r) {   // the same order in every CTA
+                        const float4 o = ctl.slot[par][r];
+                        ms_merge(M, Ssum, o.x, o.y);
+                        if (o.w != 0.f) zt = o.z;
+                    }
+                }
+                float loss;
+                float4 st4 = ce_row_finish(M, Ssum, zt, &loss);
+                st4.w = w_valid;
+                const float c = a.grad_output[a.red == VCE_RED_NONE ? row : 0] * w_valid;
+                ctl.coefs[par] = make_float4(c * st4.y, (st4.x == -kInf) ? 0.f : st4.x * kLog2e, c * st4.z, 0.f);
+                tc::mbar_arrive(&ctl.cbar[par]);
+                if (rank == 0) {
+                    a.row_stats[row] = st4;
+                    a.loss_rows[row] = loss;
+                }
+            }
+            __syncwarp();
+        }
+    } else {
+        // ---------------- consumers ----------------
+        const int tid = threadIdx.x;
+
+        // Rows whose label is ignore_index or invalid: gradient +0.0 by selection, logits unread.
+        for (int64_t row = cid; row < a.T; row += ncl) {
+            const int64_t t = a.labels[row];
+            if (label_valid(a, t)) continue;
+            if (rank == 0 && tid == 0) {
+                a.loss_rows[row] = (t == a.ignore_index) ? 0.f : __int_as_float(0x7FC00000);
+                a.row_stats[row] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (t != a.ignore_index) atomicCAS(a.status, 0, (int32_t)VCE_ERR_LABEL);
+            }
+            O* grow = static_cast<O*>(a.grad) + row * a.ld_g + c0;
+            const float zero[G] = {};
+            for (int vi = tid; vi < w / G; vi += kConsumers) GroupStore<O, G>::run(grow + vi * G, zero);
+        }
+
+        // Forward over chunks [j0, j1) of the row whose first chunk is ring chunk q0; tl is the
+        // target's local column (outside [0, w): not in this slice).
+        auto forward = [&](uint32_t q0, int j0, int j1, int tl, int par, float& m, float& s, float& mb) {
+            for (int j = j0; j < j1; ++j) {
+                const uint32_t p = q0 + j;
+                const int st = (int)(p % kStages);
+                if (!tc::mbar_wait(&ctl.full[st], (p / kStages) & 1, abort_flag, a.status, kErrFull, a.wait_ns))
+                    continue;
+                const uint4* buf = reinterpret_cast<const uint4*>(smem + st * kChunk);
+                const int nvec = min(kChunk, bytes - j * kChunk) / 16;
+                const int col0 = j * (kChunk / (int)sizeof(S));
+                uint4 r[kVecPerThread];
+#pragma unroll
+                for (int u = 0; u < kVecPerThread; ++u) {
+                    const int vi = tid + u * kConsumers;
+                    if (vi < nvec) r[u] = lds16(buf + vi);
+                }
+#pragma unroll
+                for (int u = 0; u < kVecPerThread; ++u) {
+                    const int vi = tid + u * kConsumers;
+                    if (vi < nvec) {
+                        float v[G];
+                        Elt<S>::unpack(r[u], v);
+                        const uint32_t rel = (uint32_t)(tl - (col0 + vi * G));
+                        if (rel < (uint32_t)G) {
+#pragma unroll
+                            for (int k = 0; k < G; ++k)
+                                if (rel == (uint32_t)k) { ctl.zt[par] = v[k]; v[k] = -kInf; }
+                        }
+                        ms_push_lazy<G>(v, m, s, mb);
+                    }
+                }
+            }
+        };
+        // This warp's pair of the row, for the stats warp.
+        auto publish = [&](int par, float m, float s) {
+            ms_warp_reduce(m, s);
+            if (lane == 0) {
+                ctl.red_m[par][warp] = m;
+                ctl.red_s[par][warp] = s;
+            }
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&ctl.rbar[par]);
+        };
+        auto target_col = [&](int64_t row) { return (int)(a.labels[row] - c0); };
+
+        uint32_t q = 0, e = 0;   // ring chunk of the current row's first chunk; row index in the sequence
+        int64_t row = next_valid(a, cid, ncl);
+        if (row < a.T) {
+            float m = -kInf, s = 0.f, mb = 0.f;
+            forward(q, 0, nchunk, target_col(row), 0, m, s, mb);
+            publish(0, m, s);
+        }
+        while (row < a.T) {
+            const int par = (int)(e & 1);
+            const int64_t nxt = next_valid(a, row + ncl, ncl);
+            const int tl = target_col(row);
+            const int tl2 = nxt < a.T ? target_col(nxt) : -1;
+            float m2 = -kInf, s2 = 0.f, mb2 = 0.f;
+            if (nxt < a.T) forward(q + nchunk, 0, pre, tl2, par ^ 1, m2, s2, mb2);
+
+            // the row's gradient, each stage released once this warp is done with it
+            tc::mbar_wait(&ctl.cbar[par], (e >> 1) & 1, abort_flag, a.status, kErrCoefs, a.wait_ns);
+            const float4 cf = ctl.coefs[par];
+            O* grow = static_cast<O*>(a.grad) + row * a.ld_g + c0;
+            for (int j = 0; j < nchunk; ++j) {
+                const int st = (int)((q + j) % kStages);
+                const uint4* buf = reinterpret_cast<const uint4*>(smem + st * kChunk);
+                const int nvec = min(kChunk, bytes - j * kChunk) / 16;
+                const int col0 = j * (kChunk / (int)sizeof(S));
+                O* gcol = grow + col0;
+                if (!*abort_flag) {
+                    uint4 r[kVecPerThread];
+#pragma unroll
+                    for (int u = 0; u < kVecPerThread; ++u) {
+                        const int vi = tid + u * kConsumers;
+                        if (vi < nvec) r[u] = lds16(buf + vi);
+                    }
+#pragma unroll
+                    for (int u = 0; u < kVecPerThread; ++u) {
+                        const int vi = tid + u * kConsumers;
+                        if (vi < nvec) {
+                            float v[G];
+                            Elt<S>::unpack(r[u], v);
+#pragma unroll
+                            for (int k = 0; k < G; ++k) v[k] = cf.x * ex2(fmaf(v[k], kLog2e, -cf.y));
+                            const uint32_t rel = (uint32_t)(tl - (col0 + vi * G));
+                            if (rel < (uint32_t)G) {
+#pragma unroll
+                                for (int k = 0; k < G; ++k)
+                                    if (rel == (uint32_t)k) v[k] = cf.z;
+                            }
+                            GroupStore<O, G>::run(gcol + vi * G, v);
+                        }
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&ctl.empty[st]);
+            }
+            q += nchunk;
+
+            if (nxt < a.T) {
+                forward(q, pre, nchunk, tl2, par ^ 1, m2, s2, mb2);
+                publish(par ^ 1, m2, s2);
+            }
+            row = nxt;
+            ++e;
+        }
+    }
+    if (C > 1) cluster_sync();   // no CTA leaves while a peer may still write into its shared memory
+}
+
+template <typename S, typename O, int C>
+cudaError_t launch(const Args& args, int sms, cudaStream_t s, bool* launched) {
+    auto kern = k_ce_fused_ring<S, O, C>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int clusters = sms;
+    if (C > 1) {   // clusters that fit at once, queried once per device
+        static std::atomic<int> fit[kMaxDevices];
+        int dev = 0;
+        e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        if (dev < 0 || dev >= kMaxDevices) return cudaSuccess;
+        clusters = fit[dev].load() - 1;
+        if (clusters < 0) {
+            cfg.gridDim = dim3(C * (sms / C));
+            e = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
+            if (e != cudaSuccess) return e;
+            fit[dev].store(clusters + 1);
+        }
+        if (clusters < 1) return cudaSuccess;   // no room for one cluster: not launched
+    }
+    clusters = (int)std::min<int64_t>(clusters, args.T);
+    cfg.gridDim = dim3(C * clusters);
+    e = cudaLaunchKernelEx(&cfg, kern, args);
+    if (e == cudaSuccess) *launched = true;
+    return e;
+}
+
+template <typename S, typename O>
+cudaError_t launch_c(int C, const Args& args, int sms, cudaStream_t s, bool* launched) {
+    switch (C) {
+        case 1: return launch<S, O, 1>(args, sms, s, launched);
+        case 2: return launch<S, O, 2>(args, sms, s, launched);
+        case 4: return launch<S, O, 4>(args, sms, s, launched);
+        default: return launch<S, O, 8>(args, sms, s, launched);
+    }
+}
+
+}  // namespace ring
+
+cudaError_t launch_fused_ring(vce_dtype dt, vce_dtype gdt, const void* logits, int64_t T, int64_t V, int64_t ld,
+                              const int64_t* labels, int64_t ignore_index, int red, const float* grad_output,
+                              const float* inv_n, float* loss_rows, float* row_stats, void* grad, int64_t ld_g,
+                              int32_t* status, cudaStream_t s, bool* launched) {
+    using namespace ring;
+    *launched = false;
+    // 16-byte rows and slices: every row and slice starts on a 16-byte boundary, and each slice
+    // is whole 16-byte vectors of input and output.
+    if (T < 1 || V % 8 || ld % 8 || ld_g % 8 || !aligned(logits, 16) || !aligned(grad, 16)) return cudaSuccess;
+    const int64_t es = dt == VCE_BF16 ? 2 : 4;
+    int C = 1;
+    int64_t slice = V;
+    for (; C <= kMaxCluster; C *= 2) {
+        slice = ((V + C - 1) / C + 7) / 8 * 8;
+        if (slice * es <= (int64_t)kSliceStages * kChunk) break;
+    }
+    if (C > kMaxCluster) return cudaSuccess;   // rows too long for an 8-CTA cluster
+    Args args{logits, T,   V,    ld,   labels, ignore_index, red,   grad_output, inv_n,
+              loss_rows, reinterpret_cast<float4*>(row_stats), grad, ld_g, status, slice, tc::kWaitNs};
+    const int sms = device_sm_count();
+    if (dt == VCE_BF16 && gdt == VCE_BF16) return launch_c<uint16_t, uint16_t>(C, args, sms, s, launched);
+    if (dt == VCE_BF16) return launch_c<uint16_t, float>(C, args, sms, s, launched);
+    if (gdt == VCE_BF16) return launch_c<float, uint16_t>(C, args, sms, s, launched);
+    return launch_c<float, float>(C, args, sms, s, launched);
+}
+
+}  // namespace vce

@@ -46,4 +46,13 @@ cudaError_t launch_ce_bwd(vce_dtype dt, vce_dtype gdt, int nt, const SegTable& t
                           const float* row_stats, const float* grad_output, int go_per_row, cudaStream_t s,
                           float eps_over_v = 0.f);
 
+// One-pass forward+backward with each row held in shared memory between its two passes
+// (ce_ring.cu).  Sets *launched when it enqueued the kernel; leaves it false, enqueuing
+// nothing, when the shape or layout does not fit (rows or leading dimensions not multiples of
+// 8 elements, pointers not 16-byte aligned, rows too long for an 8-CTA cluster).
+cudaError_t launch_fused_ring(vce_dtype dt, vce_dtype gdt, const void* logits, int64_t T, int64_t V, int64_t ld,
+                              const int64_t* labels, int64_t ignore_index, int red, const float* grad_output,
+                              const float* inv_n, float* loss_rows, float* row_stats, void* grad, int64_t ld_g,
+                              int32_t* status, cudaStream_t s, bool* launched);
+
 }  // namespace vce
