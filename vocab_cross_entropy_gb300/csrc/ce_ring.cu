@@ -62,9 +62,24 @@ constexpr int kThreads = kConsumers + 64;
 constexpr int kMaxCluster = 8;
 constexpr int kMaxDevices = 64;
 constexpr int kVecPerThread = (kChunk / 16 + kConsumers - 1) / kConsumers;   // 16-B vectors per consumer per stage
+// Longest sleep of one poll of an incomplete mbarrier phase: the waiting warps (the producer on a
+// free stage, the stats warp on the partials, consumers on data) leave the issue slots to the
+// working ones and wake when the phase completes.
+constexpr uint32_t kSuspendRole = 10000, kSuspendConsumer = 10000;
+static_assert((kConsumerWarps & (kConsumerWarps - 1)) == 0 && kConsumerWarps <= 32, "warp partials merge in one warp");
+static_assert(kVecPerThread * kConsumers * 16 == kChunk, "every consumer takes the same whole vectors of a stage");
 enum { kErrEmpty = 105, kErrFull = 106, kErrExchange = 107, kErrPartials = 108, kErrCoefs = 109 };
 
+// A valid row of the CTA's sequence: its index and its target's column local to the slice.
+struct RowInfo {
+    int64_t row;
+    int tl;
+    int pad;
+};
+constexpr int kInfoSlots = 16;         // > the rows the producer can run ahead (kStages, at one chunk a row)
+
 struct alignas(16) Ctl {
+    RowInfo info[kInfoSlots];          // by the row's index in the sequence, mod kInfoSlots
     float4 slot[2][kMaxCluster];       // (m, s, z_t, owner) of each CTA of the cluster
     float4 coefs[2];                   // (coef, bias, target gradient, -) of the row
     float red_m[2][kConsumerWarps], red_s[2][kConsumerWarps];
@@ -119,14 +134,14 @@ __device__ __forceinline__ void st_peer(uint32_t addr, float4 v) {
 __device__ __forceinline__ void arrive_peer(uint32_t bar_addr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_addr) : "memory");
 }
-__device__ __forceinline__ bool try_wait_cluster(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ bool try_wait_cluster(uint64_t* bar, uint32_t parity, uint32_t suspend_ns) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(tc::smem_u32(bar)), "r"(parity)
+        : "r"(tc::smem_u32(bar)), "r"(parity), "r"(suspend_ns)
         : "memory");
     return ok != 0;
 }
@@ -150,7 +165,7 @@ __device__ __forceinline__ bool wait_exchange(uint64_t* bar, uint32_t parity, vo
                                               int32_t* err, uint64_t wait_ns) {
     if (*abort_flag) return false;
     const uint64_t t0 = tc::globaltimer();
-    while (!try_wait_cluster(bar, parity)) {
+    while (!try_wait_cluster(bar, parity, kSuspendRole)) {
         if (*abort_flag) return false;
         if (tc::globaltimer() - t0 > wait_ns) {
             *abort_flag = 1;
@@ -171,11 +186,83 @@ __device__ __forceinline__ int64_t next_valid(const Args& a, int64_t row, int64_
     return a.T;
 }
 
+// ---- per-stage work ---------------------------------------------------------------------------
+//
+// A consumer thread takes the 16-byte vectors tid + u * kConsumers (u < kVecPerThread) of a
+// stage; rel0 = (the target's column) - (the column of the thread's first vector).  kFull: the
+// stage is whole, so no vector needs a bound check.
+
+// 16 bytes of -inf in the storage format (vectors past a partial stage's end).
+template <typename S>
+__device__ __forceinline__ uint4 neg_inf16();
+template <>
+__device__ __forceinline__ uint4 neg_inf16<uint16_t>() { return make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u); }
+template <>
+__device__ __forceinline__ uint4 neg_inf16<float>() { return make_uint4(0xFF800000u, 0xFF800000u, 0xFF800000u, 0xFF800000u); }
+
+// Whether the target column falls in one of this thread's vectors of the stage.
+template <typename S>
+__device__ __forceinline__ bool holds_target(int rel0) {
+    constexpr int G = Elt<S>::kGroup, Span = kConsumers * G;
+    return rel0 >= 0 && rel0 < kVecPerThread * Span && (rel0 % Span) < G;
+}
+
+// Forward over one loaded stage.  kTarget: this thread holds the target, whose value goes to
+// *zt and is left out of the sum.
+template <typename S, bool kFull, bool kTarget>
+__device__ __forceinline__ void fwd_stage(const uint4* buf, int nvec, int rel0, int tid, float& m, float& s,
+                                          float& mb, float* zt) {
+    constexpr int G = Elt<S>::kGroup, U = kVecPerThread;
+    float v[U][G];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const int vi = tid + u * kConsumers;
+        Elt<S>::unpack((kFull || vi < nvec) ? lds16(buf + vi) : neg_inf16<S>(), v[u]);
+    }
+    if (kTarget) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const uint32_t rel = (uint32_t)(rel0 - u * kConsumers * G);
+#pragma unroll
+            for (int k = 0; k < G; ++k)
+                if (rel == (uint32_t)k) { *zt = v[u][k]; v[u][k] = -kInf; }
+        }
+    }
+    ms_push_lazy_batch<U, G>(v, m, s, mb);
+}
+
+// Gradient of one held stage: coef * 2^(z log2 e - bias) for every column, then the thread
+// holding the target overwrites that entry with gt (its own later store to the same address).
+template <typename S, typename O, bool kFull>
+__device__ __forceinline__ void bwd_stage(const uint4* buf, int nvec, O* gcol, int rel0, int tid, float coef,
+                                          float bias, float gt) {
+    constexpr int G = Elt<S>::kGroup, U = kVecPerThread;
+    uint4 r[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const int vi = tid + u * kConsumers;
+        if (kFull || vi < nvec) r[u] = lds16(buf + vi);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const int vi = tid + u * kConsumers;
+        if (kFull || vi < nvec) {
+            float v[G];
+            Elt<S>::unpack(r[u], v);
+#pragma unroll
+            for (int k = 0; k < G; ++k) v[k] = coef * ex2(fmaf(v[k], kLog2e, -bias));
+            GroupStore<O, G>::run(gcol + vi * G, v);
+        }
+    }
+    if (holds_target<S>(rel0)) Elt<O>::store1(gcol + tid * G + rel0, gt);
+}
+
 // ---- the kernel -----------------------------------------------------------------------------
 
 template <typename S, typename O, int C>
 __global__ void __launch_bounds__(kThreads, 1) k_ce_fused_ring(const __grid_constant__ Args a) {
     constexpr int G = Elt<S>::kGroup;
+    constexpr int kFullVec = kChunk / 16;
     extern __shared__ __align__(128) uint8_t smem[];
     Ctl& ctl = *reinterpret_cast<Ctl*>(smem + kStages * kChunk);
     volatile int* abort_flag = &ctl.abort;
@@ -199,23 +286,36 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_fused_ring(const __grid_cons
             tc::mbar_init(&ctl.rbar[p], kConsumerWarps);
             tc::mbar_init(&ctl.cbar[p], 1);
         }
+        for (int i = 0; i < kInfoSlots; ++i) ctl.info[i] = RowInfo{-1, -1, 0};
         ctl.abort = 0;
         tc::fence_mbar_init();
     }
     if (C > 1) cluster_sync();   // peers arrive on these barriers from now on
     else __syncthreads();
 
+    // The number of valid rows of this cluster (each warp counts for itself).
+    auto count_valid = [&]() {
+        int n = 0;
+        for (int64_t row = cid + (int64_t)lane * ncl; row < a.T; row += 32 * ncl) n += label_valid(a, a.labels[row]);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) n += __shfl_xor_sync(0xFFFFFFFFu, n, off);
+        return n;
+    };
+
     if (warp == kProducerWarp) {
         // ---------------- producer ----------------
         if (lane == 0) {
-            uint32_t q = 0;
+            uint32_t q = 0, e = 0;
             for (int64_t row = next_valid(a, cid, ncl); row < a.T && !*abort_flag;
-                 row = next_valid(a, row + ncl, ncl)) {
+                 row = next_valid(a, row + ncl, ncl), ++e) {
+                // the row's index and target column, for the other roles (published by the first
+                // chunk's barrier arrival)
+                ctl.info[e % kInfoSlots] = RowInfo{row, (int)(a.labels[row] - c0), 0};
                 const char* src = static_cast<const char*>(a.logits) + (row * a.ld + c0) * (int64_t)sizeof(S);
                 for (int j = 0; j < nchunk; ++j) {
                     const int st = (int)(q % kStages);
                     if (!tc::mbar_wait(&ctl.empty[st], ((q / kStages) & 1) ^ 1, abort_flag, a.status, kErrEmpty,
-                                       a.wait_ns))
+                                       a.wait_ns, kSuspendRole))
                         break;
                     const uint32_t nb = (uint32_t)min(kChunk, bytes - j * kChunk);
                     tc::mbar_arrive_expect_tx(&ctl.full[st], nb);
@@ -232,16 +332,22 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_fused_ring(const __grid_cons
     } else if (warp == kStatsWarp) {
         // ---------------- row statistics ----------------
         const float w_valid = (a.red == VCE_RED_MEAN) ? *a.inv_n : 1.f;
-        uint32_t e = 0;
-        for (int64_t row = next_valid(a, cid, ncl); row < a.T; row = next_valid(a, row + ncl, ncl), ++e) {
-            const int par = (int)(e & 1);
+        const int nv = count_valid();
+        for (int e = 0; e < nv; ++e) {
+            const int par = e & 1;
             const uint32_t ph = (e >> 1) & 1;
-            tc::mbar_wait(&ctl.rbar[par], ph, abort_flag, a.status, kErrPartials, a.wait_ns);
+            tc::mbar_wait(&ctl.rbar[par], ph, abort_flag, a.status, kErrPartials, a.wait_ns, kSuspendRole);
             float m = lane < kConsumerWarps ? ctl.red_m[par][lane] : -kInf;
             float s = lane < kConsumerWarps ? ctl.red_s[par][lane] : 0.f;
-            ms_warp_reduce(m, s);
+#pragma unroll
+            for (int off = kConsumerWarps / 2; off > 0; off >>= 1) {   // lanes 0..kConsumerWarps-1 into lane 0
+                const float m2 = __shfl_xor_sync(0xFFFFFFFFu, m, off);
+                const float s2 = __shfl_xor_sync(0xFFFFFFFFu, s, off);
+                ms_merge(m, s, m2, s2);
+            }
             if (lane == 0) {
-                const bool own = (uint64_t)(a.labels[row] - c0) < (uint64_t)w;
+                const RowInfo ri = ctl.info[e % kInfoSlots];
+                const bool own = (uint32_t)ri.tl < (uint32_t)w;
                 float M = m, Ssum = s, zt = own ? ctl.zt[par] : 0.f;
                 if (C > 1) {
                     const float4 mine = make_float4(m, s, zt, own ? 1.f : 0.f);
@@ -256,15 +362,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_fused_ring(const __grid_cons
                         if (o.w != 0.f) zt = o.z;
                     }
                 }
+                const bool in_range = ri.row >= 0 && ri.row < a.T;   // false only after an abort
                 float loss;
                 float4 st4 = ce_row_finish(M, Ssum, zt, &loss);
                 st4.w = w_valid;
-                const float c = a.grad_output[a.red == VCE_RED_NONE ? row : 0] * w_valid;
+                const float c = in_range ? a.grad_output[a.red == VCE_RED_NONE ? ri.row : 0] * w_valid : 0.f;
                 ctl.coefs[par] = make_float4(c * st4.y, (st4.x == -kInf) ? 0.f : st4.x * kLog2e, c * st4.z, 0.f);
                 tc::mbar_arrive(&ctl.cbar[par]);
-                if (rank == 0) {
-                    a.row_stats[row] = st4;
-                    a.loss_rows[row] = loss;
+                if (rank == 0 && in_range) {
+                    a.row_stats[ri.row] = st4;
+                    a.loss_rows[ri.row] = loss;
                 }
             }
             __syncwarp();
@@ -287,37 +394,26 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_fused_ring(const __grid_cons
             for (int vi = tid; vi < w / G; vi += kConsumers) GroupStore<O, G>::run(grow + vi * G, zero);
         }
 
-        // Forward over chunks [j0, j1) of the row whose first chunk is ring chunk q0; tl is the
-        // target's local column (outside [0, w): not in this slice).
-        auto forward = [&](uint32_t q0, int j0, int j1, int tl, int par, float& m, float& s, float& mb) {
+        // Forward over chunks [j0, j1) of valid row e, whose first chunk is ring chunk q0.  The
+        // row's index and target column are read once its first chunk has landed.
+        auto forward = [&](uint32_t q0, int j0, int j1, int e, RowInfo& ri, float& m, float& s, float& mb) {
             for (int j = j0; j < j1; ++j) {
                 const uint32_t p = q0 + j;
                 const int st = (int)(p % kStages);
-                if (!tc::mbar_wait(&ctl.full[st], (p / kStages) & 1, abort_flag, a.status, kErrFull, a.wait_ns))
-                    continue;
+                const bool ok = tc::mbar_wait(&ctl.full[st], (p / kStages) & 1, abort_flag, a.status, kErrFull,
+                                              a.wait_ns, kSuspendConsumer);
+                if (j == 0) ri = ctl.info[e % kInfoSlots];
+                if (!ok) continue;
                 const uint4* buf = reinterpret_cast<const uint4*>(smem + st * kChunk);
                 const int nvec = min(kChunk, bytes - j * kChunk) / 16;
-                const int col0 = j * (kChunk / (int)sizeof(S));
-                uint4 r[kVecPerThread];
-#pragma unroll
-                for (int u = 0; u < kVecPerThread; ++u) {
-                    const int vi = tid + u * kConsumers;
-                    if (vi < nvec) r[u] = lds16(buf + vi);
-                }
-#pragma unroll
-                for (int u = 0; u < kVecPerThread; ++u) {
-                    const int vi = tid + u * kConsumers;
-                    if (vi < nvec) {
-                        float v[G];
-                        Elt<S>::unpack(r[u], v);
-                        const uint32_t rel = (uint32_t)(tl - (col0 + vi * G));
-                        if (rel < (uint32_t)G) {
-#pragma unroll
-                            for (int k = 0; k < G; ++k)
-                                if (rel == (uint32_t)k) { ctl.zt[par] = v[k]; v[k] = -kInf; }
-                        }
-                        ms_push_lazy<G>(v, m, s, mb);
-                    }
+                const int rel0 = ri.tl - (j * (kChunk / (int)sizeof(S)) + tid * G);
+                float* zt = &ctl.zt[e & 1];
+                if (holds_target<S>(rel0)) {
+                    if (nvec == kFullVec) fwd_stage<S, true, true>(buf, nvec, rel0, tid, m, s, mb, zt);
+                    else fwd_stage<S, false, true>(buf, nvec, rel0, tid, m, s, mb, zt);
+                } else {
+                    if (nvec == kFullVec) fwd_stage<S, true, false>(buf, nvec, rel0, tid, m, s, mb, zt);
+                    else fwd_stage<S, false, false>(buf, nvec, rel0, tid, m, s, mb, zt);
                 }
             }
         };
@@ -331,69 +427,47 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_fused_ring(const __grid_cons
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&ctl.rbar[par]);
         };
-        auto target_col = [&](int64_t row) { return (int)(a.labels[row] - c0); };
 
-        uint32_t q = 0, e = 0;   // ring chunk of the current row's first chunk; row index in the sequence
-        int64_t row = next_valid(a, cid, ncl);
-        if (row < a.T) {
+        const int nv = count_valid();
+        uint32_t q = 0;   // ring chunk of the current row's first chunk
+        RowInfo ri{-1, -1, 0};
+        if (nv > 0) {
             float m = -kInf, s = 0.f, mb = 0.f;
-            forward(q, 0, nchunk, target_col(row), 0, m, s, mb);
+            forward(q, 0, nchunk, 0, ri, m, s, mb);
             publish(0, m, s);
         }
-        while (row < a.T) {
-            const int par = (int)(e & 1);
-            const int64_t nxt = next_valid(a, row + ncl, ncl);
-            const int tl = target_col(row);
-            const int tl2 = nxt < a.T ? target_col(nxt) : -1;
+        for (int e = 0; e < nv; ++e) {
+            const int par = e & 1;
+            const bool more = e + 1 < nv;
+            RowInfo ri2{-1, -1, 0};
             float m2 = -kInf, s2 = 0.f, mb2 = 0.f;
-            if (nxt < a.T) forward(q + nchunk, 0, pre, tl2, par ^ 1, m2, s2, mb2);
+            if (more) forward(q + nchunk, 0, pre, e + 1, ri2, m2, s2, mb2);
 
             // the row's gradient, each stage released once this warp is done with it
-            tc::mbar_wait(&ctl.cbar[par], (e >> 1) & 1, abort_flag, a.status, kErrCoefs, a.wait_ns);
+            tc::mbar_wait(&ctl.cbar[par], (e >> 1) & 1, abort_flag, a.status, kErrCoefs, a.wait_ns, kSuspendConsumer);
             const float4 cf = ctl.coefs[par];
-            O* grow = static_cast<O*>(a.grad) + row * a.ld_g + c0;
+            const bool in_range = ri.row >= 0 && ri.row < a.T;   // false only after an abort
+            O* grow = static_cast<O*>(a.grad) + (in_range ? ri.row : 0) * a.ld_g + c0;
             for (int j = 0; j < nchunk; ++j) {
                 const int st = (int)((q + j) % kStages);
-                const uint4* buf = reinterpret_cast<const uint4*>(smem + st * kChunk);
-                const int nvec = min(kChunk, bytes - j * kChunk) / 16;
-                const int col0 = j * (kChunk / (int)sizeof(S));
-                O* gcol = grow + col0;
-                if (!*abort_flag) {
-                    uint4 r[kVecPerThread];
-#pragma unroll
-                    for (int u = 0; u < kVecPerThread; ++u) {
-                        const int vi = tid + u * kConsumers;
-                        if (vi < nvec) r[u] = lds16(buf + vi);
-                    }
-#pragma unroll
-                    for (int u = 0; u < kVecPerThread; ++u) {
-                        const int vi = tid + u * kConsumers;
-                        if (vi < nvec) {
-                            float v[G];
-                            Elt<S>::unpack(r[u], v);
-#pragma unroll
-                            for (int k = 0; k < G; ++k) v[k] = cf.x * ex2(fmaf(v[k], kLog2e, -cf.y));
-                            const uint32_t rel = (uint32_t)(tl - (col0 + vi * G));
-                            if (rel < (uint32_t)G) {
-#pragma unroll
-                                for (int k = 0; k < G; ++k)
-                                    if (rel == (uint32_t)k) v[k] = cf.z;
-                            }
-                            GroupStore<O, G>::run(gcol + vi * G, v);
-                        }
-                    }
+                if (in_range && !*abort_flag) {
+                    const uint4* buf = reinterpret_cast<const uint4*>(smem + st * kChunk);
+                    const int nvec = min(kChunk, bytes - j * kChunk) / 16;
+                    const int col0 = j * (kChunk / (int)sizeof(S));
+                    const int rel0 = ri.tl - (col0 + tid * G);
+                    if (nvec == kFullVec) bwd_stage<S, O, true>(buf, nvec, grow + col0, rel0, tid, cf.x, cf.y, cf.z);
+                    else bwd_stage<S, O, false>(buf, nvec, grow + col0, rel0, tid, cf.x, cf.y, cf.z);
                 }
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(&ctl.empty[st]);
             }
             q += nchunk;
 
-            if (nxt < a.T) {
-                forward(q, pre, nchunk, tl2, par ^ 1, m2, s2, mb2);
+            if (more) {
+                forward(q, pre, nchunk, e + 1, ri2, m2, s2, mb2);
                 publish(par ^ 1, m2, s2);
             }
-            row = nxt;
-            ++e;
+            ri = ri2;
         }
     }
     if (C > 1) cluster_sync();   // no CTA leaves while a peer may still write into its shared memory

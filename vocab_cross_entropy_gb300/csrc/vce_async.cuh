@@ -47,14 +47,31 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
+// As mbar_try_wait, but while the phase is incomplete the thread may be suspended inside the
+// instruction for up to suspend_ns (it resumes when the phase completes), so a waiting warp
+// does not take issue slots from the warps doing the work.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t* bar, uint32_t parity, uint32_t suspend_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(suspend_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait for the phase of `bar` with the given parity to complete.  Gives up after wait_ns or
-// as soon as another role of the block has given up; returns false then.
+// as soon as another role of the block has given up; returns false then.  suspend_ns > 0
+// lets each poll sleep up to that long while the phase is incomplete.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          int32_t* err, int code, uint64_t wait_ns = kWaitNs) {
+                                          int32_t* err, int code, uint64_t wait_ns = kWaitNs,
+                                          uint32_t suspend_ns = 0) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (suspend_ns ? mbar_try_wait_suspend(bar, parity, suspend_ns) : mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
         if (globaltimer() - t0 > wait_ns) {
             *abort_flag = 1;

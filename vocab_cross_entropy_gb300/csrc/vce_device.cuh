@@ -217,6 +217,44 @@ __device__ __forceinline__ void ms_push_lazy(const float (&v)[G], float& m, floa
     ms_push<G>(v, m, s, mb);   // rare: a value far above the reference; redo this group exactly
 }
 
+// ms_push_lazy over U groups at once: one reference check and one overflow check for all
+// U * G values, so the U groups' exponentials and sums form one block of independent work.
+template <int U, int G>
+__device__ __forceinline__ void ms_push_lazy_batch(const float (&v)[U][G], float& m, float& s, float& mb) {
+    if (m == -kInf) {   // first finite batch of this thread: its exact maximum is the reference
+        float vm = -kInf;
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+#pragma unroll
+            for (int k = 0; k < G; ++k) vm = fmaxf(vm, v[u][k]);
+        if (vm == -kInf) return;
+        m = vm;
+        mb = m * kLog2e;
+    }
+    float t[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        float e[G];
+#pragma unroll
+        for (int k = 0; k < G; ++k) e[k] = ex2(fmaf(v[u][k], kLog2e, -mb));
+#pragma unroll
+        for (int w = 1; w < G; w *= 2)
+#pragma unroll
+            for (int k = 0; k + w < G; k += 2 * w) e[k] += e[k + w];
+        t[u] = e[0];
+    }
+#pragma unroll
+    for (int w = 1; w < U; w *= 2)
+#pragma unroll
+        for (int u = 0; u + w < U; u += 2 * w) t[u] += t[u + w];
+    if (t[0] < 4294967296.f) {   // 2^32: no term can have overflowed
+        s += t[0];
+        return;
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) ms_push<G>(v[u], m, s, mb);   // rare: redo exactly
+}
+
 __device__ __forceinline__ void ms_push1(float v, float& m, float& s, float& mb) {
     if (v > m) {
         s *= ex2((m - v) * kLog2e);
@@ -240,17 +278,15 @@ __device__ __forceinline__ void ms_warp_reduce(float& m, float& s) {
 __device__ __forceinline__ float softplus_f(float x) {
     return x > 0.f ? x + log1pf(expf(-x)) : log1pf(expf(x));
 }
-__device__ __forceinline__ float sigmoid_f(float x) {
-    if (x >= 0.f) return 1.f / (1.f + expf(-x));
-    const float e = expf(x);
-    return e / (1.f + e);
-}
 
 // From the target-excluded pair (M, S) and the target logit zt:
 //   L' = M + log S, x = L' - z_t, loss = softplus(x) = -log p_t,
 //   stats = (L', 1 - p_t = sigmoid(x), target coefficient, weight 1).
 // The target coefficient is p_t - 1 when p_t < 1/4 and -(1 - p_t) otherwise, each a
-// single rounding from sigmoid (torchtitan PR #5723, Numerics).
+// single rounding from sigmoid (torchtitan PR #5723, Numerics).  All three functions of x come
+// from one exponential e = exp(-|x|):  sigmoid(|x|) = 1 / (1 + e),  sigmoid(-|x|) = e / (1 + e),
+// softplus(x) = max(x, 0) + log1p(e)  (each the value of the textbook branch form: 1 / (1 + e^-x)
+// or e^x / (1 + e^x) by the sign of x, and x + log1p(e^-x) or log1p(e^x)).
 __device__ __forceinline__ float4 ce_row_finish(float M, float S, float zt, float* loss) {
     float lse, x;
     if (S > 0.f) {
@@ -261,9 +297,12 @@ __device__ __forceinline__ float4 ce_row_finish(float M, float S, float zt, floa
         lse = -kInf;
         x = -kInf;
     }
-    *loss = softplus_f(x);
-    const float pnt = sigmoid_f(x);
-    const float dt = (x > kLn3) ? (sigmoid_f(-x) - 1.f) : -pnt;
+    const float e = expf(-fabsf(x));
+    const float d = 1.f + e;
+    const float s_abs = 1.f / d, s_neg = e / d;
+    const float pnt = (x >= 0.f) ? s_abs : s_neg;                 // sigmoid(x)
+    *loss = (x > 0.f ? x : 0.f) + log1pf(e);
+    const float dt = (x > kLn3) ? (s_neg - 1.f) : -pnt;           // x > ln 3 > 0: sigmoid(-x) = s_neg
     return make_float4(lse, pnt, dt, 1.f);
 }
 
