@@ -192,6 +192,21 @@ int ce_forward_backward(const void* logits, vce_dtype dt, int64_t T, int64_t V, 
                         int32_t* status, vce_stream_t s);
 
 /*
+ * vce_test_ce_fused_stall -- test hook for the give-up path of ce_forward_backward's
+ * shared-memory kernel (no page counterpart).  Runs that kernel on bf16 logits [T, V]
+ * (ld = V), ignore_index -100, reduction SUM, with its producer announcing 16 more bytes per
+ * stage than its copies deliver, so no stage ever completes.  Every wait is bounded by wait_ns
+ * (1 ms .. 2 s): the waiting warps give up and write their code to *status (105..109, see
+ * ce_forward_backward).  The CTA keeps its barrier arrivals, lets its copies land (bounded)
+ * and returns; the context stays usable.  loss_rows, row_stats and grad_logits are undefined
+ * afterwards.  Returns VCE_ERR_ARG, enqueuing nothing but the status reset, when [T, V] does
+ * not take the shared-memory kernel (V not a multiple of 8, pointers not 16-byte aligned).
+ */
+int vce_test_ce_fused_stall(const void* logits, int64_t T, int64_t V, const int64_t* labels,
+                            const float* grad_output, float* loss_rows, float* row_stats,
+                            void* grad_logits, uint64_t wait_ns, int32_t* status, vce_stream_t s);
+
+/*
  * ce_merge_chunks -- CE forward (+ backward) over logits held as k column chunks
  * in separate buffers, the single-GPU form of the vocabulary-parallel CE [MC,
  * vocab_parallel_cross_entropy; TT, Numerics: the owner of the target drops it].

@@ -149,3 +149,19 @@ def test_fused_pages_shape(vce):
     want = O.ce_grad_rows(z, p.labels[rr], fwd, O.row_scale(fwd["valid"], "sum", 1.0 / N))
     G.check_loss_rows(rows.cpu().numpy()[rr], fwd["loss"], fwd["valid"])
     G.check_grad_bf16(G.bf16_tensor_bits(grad[torch.from_numpy(rr).cuda()]), want)
+
+
+def test_stalled_ring_gives_up_and_the_context_survives(vce):
+    """Stages that never complete (2-CTA clusters): the bounded waits give up with a status code,
+    the kernel returns within seconds, and the next one-pass call on the same context is correct."""
+    import time
+    p = gen.custom(64, 70000, "bf16", seed=23, n_margin=4, n_ignore=2)
+    logits = to_device(p.full(), "bf16")
+    labels = torch.from_numpy(p.labels).cuda()
+    t0 = time.time()
+    status = vce.vce_test_ce_fused_stall(logits, labels, wait_ns=50_000_000)
+    assert 105 <= status <= 109, status
+    assert "gave up" in vce.vce_status_string(status)
+    assert time.time() - t0 < 60
+    storage, out, rows, grad = fused(vce, p)
+    check_against_oracle(p, storage, out, rows, grad)

@@ -62,6 +62,8 @@ def _load():
         L.vce_gemm_bf16.restype = i32
         L.vce_test_gemm_stall.argtypes = [p, p, i64, i64, i64, p, ctypes.c_uint64, p, p]
         L.vce_test_gemm_stall.restype = i32
+        L.vce_test_ce_fused_stall.argtypes = [p, i64, i64, p, p, p, p, p, ctypes.c_uint64, p, p]
+        L.vce_test_ce_fused_stall.restype = i32
     for name in ("ce_forward", "ce_backward", "ce_forward_ls", "ce_backward_ls", "ce_forward_backward",
                  "ce_merge_chunks", "ce_merge_chunks_noalloc",
                  "linear_ce_fwd_bwd",
@@ -295,6 +297,22 @@ def vce_test_gemm_stall(A, B, wait_ns=50_000_000, *, stream=None):
     status = torch.empty(1, dtype=torch.int32, device=A.device)
     _check("vce_test_gemm_stall", _get().vce_test_gemm_stall(_ptr(A), _ptr(B), M, N, K, _ptr(C), int(wait_ns),
                                                           _ptr(status), _stream(stream)))
+    return vce_get_status(status, stream)
+
+
+def vce_test_ce_fused_stall(logits, labels, wait_ns=50_000_000, *, stream=None):
+    """Run the one-pass shared-memory kernel with stages that never complete; returns the device
+    status word."""
+    T, V = logits.shape
+    dev = logits.device
+    go = torch.ones(1, dtype=torch.float32, device=dev)
+    loss_rows = torch.empty(T, dtype=torch.float32, device=dev)
+    row_stats = torch.empty(T, ROW_STATS, dtype=torch.float32, device=dev)
+    grad = torch.empty_like(logits)
+    status = torch.empty(1, dtype=torch.int32, device=dev)
+    _check("vce_test_ce_fused_stall", _get().vce_test_ce_fused_stall(
+        _ptr(logits), T, V, _ptr(labels), _ptr(go), _ptr(loss_rows), _ptr(row_stats), _ptr(grad), int(wait_ns),
+        _ptr(status), _stream(stream)))
     return vce_get_status(status, stream)
 
 

@@ -107,7 +107,8 @@ struct Args {
     int64_t ld_g;
     int32_t* status;
     int64_t slice;                     // columns per CTA (a multiple of 8)
-    uint64_t wait_ns;
+    uint64_t wait_ns;                  // bound of every wait
+    uint32_t tx_extra;                 // 0; > 0 only in the give-up test (a stage never completes)
 };
 
 // ---- cluster and bulk-copy primitives (inline PTX) -----------------------------------------
@@ -318,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_fused_ring(const __grid_cons
                                        a.wait_ns, kSuspendRole))
                         break;
                     const uint32_t nb = (uint32_t)min(kChunk, bytes - j * kChunk);
-                    tc::mbar_arrive_expect_tx(&ctl.full[st], nb);
+                    tc::mbar_arrive_expect_tx(&ctl.full[st], nb + a.tx_extra);
                     bulk_load(smem + st * kChunk, src + (int64_t)j * kChunk, nb, &ctl.full[st]);
                     ++q;
                 }
@@ -527,7 +528,7 @@ cudaError_t launch_c(int C, const Args& args, int sms, cudaStream_t s, bool* lau
 cudaError_t launch_fused_ring(vce_dtype dt, vce_dtype gdt, const void* logits, int64_t T, int64_t V, int64_t ld,
                               const int64_t* labels, int64_t ignore_index, int red, const float* grad_output,
                               const float* inv_n, float* loss_rows, float* row_stats, void* grad, int64_t ld_g,
-                              int32_t* status, cudaStream_t s, bool* launched) {
+                              int32_t* status, cudaStream_t s, bool* launched, uint64_t wait_ns, uint32_t tx_extra) {
     using namespace ring;
     *launched = false;
     // 16-byte rows and slices: every row and slice starts on a 16-byte boundary, and each slice
@@ -542,7 +543,7 @@ cudaError_t launch_fused_ring(vce_dtype dt, vce_dtype gdt, const void* logits, i
     }
     if (C > kMaxCluster) return cudaSuccess;   // rows too long for an 8-CTA cluster
     Args args{logits, T,   V,    ld,   labels, ignore_index, red,   grad_output, inv_n,
-              loss_rows, reinterpret_cast<float4*>(row_stats), grad, ld_g, status, slice, tc::kWaitNs};
+              loss_rows, reinterpret_cast<float4*>(row_stats), grad, ld_g, status, slice, wait_ns, tx_extra};
     const int sms = device_sm_count();
     if (dt == VCE_BF16 && gdt == VCE_BF16) return launch_c<uint16_t, uint16_t>(C, args, sms, s, launched);
     if (dt == VCE_BF16) return launch_c<uint16_t, float>(C, args, sms, s, launched);
@@ -551,3 +552,23 @@ cudaError_t launch_fused_ring(vce_dtype dt, vce_dtype gdt, const void* logits, i
 }
 
 }  // namespace vce
+
+using namespace vce;
+
+extern "C" int vce_test_ce_fused_stall(const void* logits, int64_t T, int64_t V, const int64_t* labels,
+                                       const float* grad_output, float* loss_rows, float* row_stats,
+                                       void* grad_logits, uint64_t wait_ns, int32_t* status, vce_stream_t s) {
+    if (!logits || !labels || !grad_output || !loss_rows || !row_stats || !grad_logits || !status) return VCE_ERR_NULL;
+    if (T < 1 || V < 1) return VCE_ERR_SHAPE;
+    if (wait_ns < 1000000ull || wait_ns > tc::kWaitNs) return VCE_ERR_ARG;
+    if (!aligned(row_stats, 16) || !aligned(labels, 8)) return VCE_ERR_ALIGN;
+    int rc = require_sm100();
+    if (rc) return rc;
+    if (cudaMemsetAsync(status, 0, sizeof(int32_t), s) != cudaSuccess) return VCE_ERR_CUDA;
+    bool launched = false;
+    // 16 bytes announced beyond each copy: no stage ever completes
+    if (launch_fused_ring(VCE_BF16, VCE_BF16, logits, T, V, V, labels, -100, VCE_RED_SUM, grad_output, nullptr,
+                          loss_rows, row_stats, grad_logits, V, status, s, &launched, wait_ns, 16) != cudaSuccess)
+        return VCE_ERR_CUDA;
+    return launched ? VCE_OK : VCE_ERR_ARG;
+}
