@@ -114,7 +114,11 @@ int vce_get_status(const int32_t* status, vce_stream_t s, int32_t* host_out);
  *              The target coefficient is p_t - 1 when p_t < 1/4 (x > ln 3), else
  *              -(1 - p_t) [TT, Numerics].  The row weight is 1/N (MEAN), 1 (SUM,
  *              NONE) or 0 (ignored / invalid row).  Consumed by ce_backward.
- *   status     [1] int32, set to 0 by this call, VCE_ERR_LABEL on a bad label
+ *   status     [1] int32, set to 0 by this call, VCE_ERR_LABEL on a bad label, or
+ *              105 / 106 / 108 / 110 when a bounded device-side wait gave up after 2 s
+ *              (rows of 16-byte multiples stream through a shared-memory stage ring:
+ *              free stage, loaded stage, warp partials, free statistics slots); the
+ *              outputs are then undefined
  */
 int ce_forward(const void* logits, vce_dtype dt, int64_t T, int64_t V, int64_t ld,
                const int64_t* labels, int64_t ignore_index, vce_reduction red,

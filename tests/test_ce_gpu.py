@@ -346,3 +346,56 @@ def test_non_target_spikes_take_the_rescale_path(vce, dtype):
     G.check_loss_rows(loss_rows.cpu().numpy(), ref["loss_rows"], ref["valid"])
     G.check_reduced(loss_out.item(), ref["loss_out"])
     grade_grad(grad, ref["grad"])
+
+
+# ---- ce_forward's shared-memory stage ring (rows of whole 16-byte vectors) ------------------
+
+@pytest.mark.parametrize("T,V,dtype,reduction", [
+    (40, 8, "bf16", "mean"),          # one partial stage per row, many rows per CTA
+    (300, 4096, "f32", "none"),       # one whole stage per row
+    (200, 70000, "bf16", "sum"),      # 4.3 stages per row: partial last stage
+    (24, 128256, "f32", "mean"),      # 15.7 stages per row: the ring wraps within a row
+    (700, 16384, "bf16", "mean"),     # exactly one whole stage; 4-5 rows per CTA
+])
+def test_forward_ring_shapes(vce, T, V, dtype, reduction):
+    p = gen.custom(T, V, dtype, seed=T + V, std=2.0, n_margin=max(1, T // 10), margin=(17.0, 50.0),
+                   n_ignore=max(1, T // 20))
+    full_check(vce, p, reduction, np.linspace(0.5, 1.5, T) if reduction == "none" else 1.0)
+
+
+def test_forward_ring_padded_ld(vce):
+    """ld = V + 8: the padding (80.0, which would dominate the sums) is never read."""
+    p = gen.custom(60, 5000, "bf16", seed=9, n_margin=6, n_ignore=3)
+    storage = p.full()
+    wide = np.zeros((p.T, 5008), dtype=storage.dtype)
+    wide[:, :5000] = storage
+    wide[:, 5000:] = 0x42A0
+    logits = to_device(wide, "bf16")[:, :5000]
+    loss_out, loss_rows, stats, status, grad = run_ce(vce, logits, p.labels)
+    assert vce.vce_get_status(status) == 0
+    ref = O.ce(O.widen(storage, "bf16"), p.labels, "mean")
+    G.check_loss_rows(loss_rows.cpu().numpy(), ref["loss_rows"], ref["valid"])
+    G.check_reduced(loss_out.item(), ref["loss_out"])
+
+
+def test_forward_ring_non_finite_and_bad_labels(vce):
+    """V = 8: -inf entries, a row of all -inf non-targets, ignored and invalid labels."""
+    rng = np.random.default_rng(12)
+    z = rng.normal(0, 2, (6, 8)).astype(np.float32)
+    z[1, :] = -np.inf
+    z[1, 3] = 1.5                       # every non-target -inf: loss 0
+    z[2, 5] = -np.inf                   # the target itself -inf: loss +inf
+    z[4, 0] = -np.inf
+    labels = np.array([2, 3, 5, -100, 7, 9])   # row 5: label 9 >= V
+    for dtype in ("f32", "bf16"):
+        storage = z if dtype == "f32" else (z.view(np.uint32) >> 16).astype(np.uint16)
+        logits = to_device(storage, dtype)
+        lab = torch.from_numpy(labels).cuda()
+        loss_out, loss_rows, stats, status = vce.ce_forward(logits, lab, reduction="none")
+        torch.cuda.synchronize()
+        assert vce.vce_get_status(status) == 1
+        lr = loss_rows.cpu().numpy()
+        ref = O.ce(O.widen(storage, dtype), np.where(labels < 8, labels, -100), "none")
+        assert lr[1] == 0 and lr[2] == np.inf and lr[3] == 0 and np.isnan(lr[5])
+        for r in (0, 4):
+            assert abs(lr[r] - ref["loss_rows"][r]) <= 1e-4 * ref["loss_rows"][r]

@@ -1,0 +1,253 @@
+// CE forward (ce_forward) for rows that suit bulk copies: each row streams through a
+// shared-memory stage ring, so no thread holds global loads in flight.
+//
+// Method: torchtitan PR #5723 "[loss] fix softmax collapse with improved ce perf" (Numerics:
+// target-excluded log-sum-exp, softplus NLL) — the same per-row statistics as k_ce_fwd.
+//
+// One CTA per SM walks the valid rows blockIdx.x, blockIdx.x + gridDim.x, ... with three roles:
+//   producer warp   one lane streams each row into a ring of seven 32 KB stages with bulk
+//                   asynchronous copies (cp.async.bulk), completion counted on per-stage
+//                   mbarriers, and publishes each row's index and target column
+//   consumer warps  per stage, a thread's 4 x 16-byte vectors summed at once into its
+//                   (max, sum-exp) pair (stage::fwd_stage); the stage goes back to the producer
+//                   right away; at the end of a row each warp publishes its pair
+//   stats warp      merges the warps' pairs, finishes the row (loss, row statistics) and frees
+//                   the row's slots; it also writes the outputs of ignored and invalid rows
+// Row hand-offs go through mbarriers double-buffered by the parity of the row's index in the
+// CTA's sequence; consumers wait for the stats warp to free a parity's slots before writing
+// them again, two rows later.  The bf16 row stream of k_ce_fwd is issue-bound (a thread keeps
+// four 16-byte loads in flight and sums them one vector at a time); here the copies need no
+// registers and the sum takes fewer instructions per element.
+//
+// Every wait is bounded (2 s); a wait that gives up writes its code to the status word (105
+// free stage, 106 loaded stage, 108 warp partials, 110 free slots) and sets the CTA's abort
+// flag, after which every role keeps its arrivals but skips the work and later waits.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <algorithm>
+
+#include "ce_segments.h"
+#include "ce_stage.cuh"
+#include "vce.h"
+#include "vce_async.cuh"
+#include "vce_device.cuh"
+#include "vce_host.h"
+
+namespace vce {
+namespace fring {
+
+constexpr int kChunk = 32768;          // bytes per stage (one bulk copy)
+constexpr int kStages = 7;
+constexpr int kConsumerWarps = 16;
+constexpr int kConsumers = kConsumerWarps * 32;
+constexpr int kProducerWarp = kConsumerWarps, kStatsWarp = kConsumerWarps + 1;
+constexpr int kThreads = kConsumers + 64;
+constexpr int kVecPerThread = kChunk / 16 / kConsumers;
+constexpr uint32_t kSuspendNs = 10000;   // longest sleep of one poll of an incomplete phase
+constexpr int kInfoSlots = 16;           // > the rows the producer can run ahead of the stats warp
+static_assert(kVecPerThread * kConsumers * 16 == kChunk, "every consumer takes the same whole vectors of a stage");
+static_assert((kConsumerWarps & (kConsumerWarps - 1)) == 0 && kConsumerWarps <= 32, "warp pairs merge in one warp");
+enum { kErrEmpty = 105, kErrFull = 106, kErrPartials = 108, kErrSlots = 110 };
+
+struct RowInfo {
+    int64_t row;
+    int tl;   // target column
+    int pad;
+};
+
+struct alignas(16) Ctl {
+    RowInfo info[kInfoSlots];          // by the row's index in the sequence, mod kInfoSlots
+    float red_m[2][kConsumerWarps], red_s[2][kConsumerWarps];
+    float zt[2];
+    uint64_t full[kStages];            // stage loaded
+    uint64_t empty[kStages];           // stage released (one arrival per consumer warp)
+    uint64_t rbar[2];                  // warp pairs published (one arrival per consumer warp)
+    uint64_t fbar[2];                  // the parity's slots read by the stats warp
+    int abort;
+};
+constexpr int kSmemBytes = kStages * kChunk + (int)sizeof(Ctl);
+
+struct Args {
+    const void* logits;
+    int64_t T, V, ld;
+    const int64_t* labels;
+    int64_t ignore_index;
+    float* loss_rows;
+    float4* row_stats;
+    int32_t* status;
+    uint64_t wait_ns;
+};
+
+__device__ __forceinline__ bool label_valid(const Args& a, int64_t t) {
+    return t != a.ignore_index && t >= 0 && t < a.V;
+}
+__device__ __forceinline__ int64_t next_valid(const Args& a, int64_t row, int64_t stride) {
+    for (; row < a.T; row += stride)
+        if (label_valid(a, a.labels[row])) return row;
+    return a.T;
+}
+
+template <typename S>
+__global__ void __launch_bounds__(kThreads, 1) k_ce_fwd_ring(const __grid_constant__ Args a) {
+    constexpr int G = Elt<S>::kGroup;
+    extern __shared__ __align__(128) uint8_t smem[];
+    Ctl& ctl = *reinterpret_cast<Ctl*>(smem + kStages * kChunk);
+    volatile int* abort_flag = &ctl.abort;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t stride = gridDim.x;
+    const int64_t bytes = a.V * (int64_t)sizeof(S);
+    const int nchunk = (int)((bytes + kChunk - 1) / kChunk);
+
+    if (threadIdx.x == 0) {
+        for (int st = 0; st < kStages; ++st) {
+            tc::mbar_init(&ctl.full[st], 1);
+            tc::mbar_init(&ctl.empty[st], kConsumerWarps);
+        }
+        for (int p = 0; p < 2; ++p) {
+            tc::mbar_init(&ctl.rbar[p], kConsumerWarps);
+            tc::mbar_init(&ctl.fbar[p], 1);
+        }
+        for (int i = 0; i < kInfoSlots; ++i) ctl.info[i] = RowInfo{-1, -1, 0};
+        ctl.abort = 0;
+        tc::fence_mbar_init();
+    }
+    __syncthreads();
+
+    // The number of valid rows of this CTA (each warp counts for itself).
+    auto count_valid = [&]() {
+        int n = 0;
+        for (int64_t row = blockIdx.x + (int64_t)lane * stride; row < a.T; row += 32 * stride)
+            n += label_valid(a, a.labels[row]);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) n += __shfl_xor_sync(0xFFFFFFFFu, n, off);
+        return n;
+    };
+
+    if (warp == kProducerWarp) {
+        // ---------------- producer ----------------
+        if (lane == 0) {
+            uint32_t q = 0, e = 0;
+            for (int64_t row = next_valid(a, blockIdx.x, stride); row < a.T && !*abort_flag;
+                 row = next_valid(a, row + stride, stride), ++e) {
+                ctl.info[e % kInfoSlots] = RowInfo{row, (int)a.labels[row], 0};   // published with chunk 0
+                const char* src = static_cast<const char*>(a.logits) + row * a.ld * (int64_t)sizeof(S);
+                for (int j = 0; j < nchunk; ++j) {
+                    const int st = (int)(q % kStages);
+                    if (!tc::mbar_wait(&ctl.empty[st], ((q / kStages) & 1) ^ 1, abort_flag, a.status, kErrEmpty,
+                                       a.wait_ns, kSuspendNs))
+                        break;
+                    const uint32_t nb = (uint32_t)std::min<int64_t>(kChunk, bytes - (int64_t)j * kChunk);
+                    tc::mbar_arrive_expect_tx(&ctl.full[st], nb);
+                    tc::bulk_load(smem + st * kChunk, src + (int64_t)j * kChunk, nb, &ctl.full[st]);
+                    ++q;
+                }
+            }
+            // Copies still in flight (only after an abort) land before the CTA may exit.
+            int never = 0;
+            for (uint32_t p = q > (uint32_t)kStages ? q - kStages : 0; p < q; ++p)
+                tc::mbar_wait(&ctl.full[p % kStages], (p / kStages) & 1, &never, nullptr, 0, a.wait_ns);
+        }
+        __syncwarp();
+    } else if (warp == kStatsWarp) {
+        // ---------------- row statistics ----------------
+        if (lane == 0) {   // rows whose label is ignore_index or invalid: the logits are not read
+            for (int64_t row = blockIdx.x; row < a.T; row += stride) {
+                const int64_t t = a.labels[row];
+                if (label_valid(a, t)) continue;
+                a.loss_rows[row] = (t == a.ignore_index) ? 0.f : __int_as_float(0x7FC00000);
+                a.row_stats[row] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (t != a.ignore_index) atomicCAS(a.status, 0, (int32_t)VCE_ERR_LABEL);
+            }
+        }
+        const int nv = count_valid();
+        for (int e = 0; e < nv; ++e) {
+            const int par = e & 1;
+            tc::mbar_wait(&ctl.rbar[par], (e >> 1) & 1, abort_flag, a.status, kErrPartials, a.wait_ns, kSuspendNs);
+            float m = lane < kConsumerWarps ? ctl.red_m[par][lane] : -kInf;
+            float s = lane < kConsumerWarps ? ctl.red_s[par][lane] : 0.f;
+#pragma unroll
+            for (int off = kConsumerWarps / 2; off > 0; off >>= 1) {
+                const float m2 = __shfl_xor_sync(0xFFFFFFFFu, m, off);
+                const float s2 = __shfl_xor_sync(0xFFFFFFFFu, s, off);
+                ms_merge(m, s, m2, s2);
+            }
+            if (lane == 0) {
+                const RowInfo ri = ctl.info[e % kInfoSlots];
+                const float zt = ctl.zt[par];
+                tc::mbar_arrive(&ctl.fbar[par]);   // the parity's slots may be rewritten
+                if (ri.row >= 0 && ri.row < a.T) {  // false only after an abort
+                    float loss;
+                    a.row_stats[ri.row] = ce_row_finish(m, s, zt, &loss);
+                    a.loss_rows[ri.row] = loss;
+                }
+            }
+            __syncwarp();
+        }
+    } else {
+        // ---------------- consumers ----------------
+        const int tid = threadIdx.x;
+        const int nv = count_valid();
+        uint32_t q = 0;   // ring chunk of the current row's first chunk
+        for (int e = 0; e < nv; ++e, q += nchunk) {
+            const int par = e & 1;
+            // the slots of this parity were read for row e - 2
+            if (e >= 2)
+                tc::mbar_wait(&ctl.fbar[par], ((e >> 1) & 1) ^ 1, abort_flag, a.status, kErrSlots, a.wait_ns,
+                              kSuspendNs);
+            float m = -kInf, s = 0.f, mb = 0.f;
+            int tl = -1;
+            for (int j = 0; j < nchunk; ++j) {
+                const uint32_t p = q + j;
+                const int st = (int)(p % kStages);
+                const bool ok = tc::mbar_wait(&ctl.full[st], (p / kStages) & 1, abort_flag, a.status, kErrFull,
+                                              a.wait_ns, kSuspendNs);
+                if (j == 0) tl = ctl.info[e % kInfoSlots].tl;
+                if (ok) {
+                    const uint4* buf = reinterpret_cast<const uint4*>(smem + st * kChunk);
+                    const int nvec = (int)(std::min<int64_t>(kChunk, bytes - (int64_t)j * kChunk) / 16);
+                    const int rel0 = tl - (j * (kChunk / (int)sizeof(S)) + tid * G);
+                    stage::fwd_stage_any<S, kConsumers, kVecPerThread>(buf, nvec, rel0, tid, m, s, mb, &ctl.zt[par]);
+                }
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&ctl.empty[st]);
+            }
+            ms_warp_reduce(m, s);
+            if (lane == 0) {
+                ctl.red_m[par][warp] = m;
+                ctl.red_s[par][warp] = s;
+            }
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&ctl.rbar[par]);
+        }
+    }
+}
+
+template <typename S>
+cudaError_t launch(const Args& args, int sms, cudaStream_t s) {
+    auto kern = k_ce_fwd_ring<S>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    const int grid = (int)std::min<int64_t>(sms, args.T);
+    kern<<<grid, kThreads, kSmemBytes, s>>>(args);
+    return cudaGetLastError();
+}
+
+}  // namespace fring
+
+cudaError_t launch_fwd_ring(vce_dtype dt, const void* logits, int64_t T, int64_t V, int64_t ld, const int64_t* labels,
+                            int64_t ignore_index, float* loss_rows, float* row_stats, int32_t* status, cudaStream_t s,
+                            bool* launched) {
+    using namespace fring;
+    *launched = false;
+    // 16-byte rows: every row starts on a 16-byte boundary and is whole 16-byte vectors.
+    if (T < 1 || V % 8 || ld % 8 || !aligned(logits, 16) || V > (int64_t)1 << 30) return cudaSuccess;
+    Args args{logits, T, V, ld, labels, ignore_index, loss_rows, reinterpret_cast<float4*>(row_stats), status,
+              tc::kWaitNs};
+    const int sms = device_sm_count();
+    const cudaError_t e = dt == VCE_BF16 ? launch<uint16_t>(args, sms, s) : launch<float>(args, sms, s);
+    if (e == cudaSuccess) *launched = true;
+    return e;
+}
+
+}  // namespace vce

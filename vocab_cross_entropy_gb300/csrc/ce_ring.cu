@@ -45,6 +45,7 @@
 
 #include "ce_segments.h"
 #include "vce.h"
+#include "ce_stage.cuh"
 #include "vce_async.cuh"
 #include "vce_device.cuh"
 #include "vce_host.h"
@@ -146,21 +147,6 @@ __device__ __forceinline__ bool try_wait_cluster(uint64_t* bar, uint32_t parity,
         : "memory");
     return ok != 0;
 }
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            tc::smem_u32(dst)),
-        "l"(src), "r"(bytes), "r"(tc::smem_u32(bar))
-        : "memory");
-}
-__device__ __forceinline__ uint4 lds16(const void* p) {
-    uint4 r;
-    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-                 : "r"(tc::smem_u32(p)));
-    return r;
-}
-
 // Bounded wait on a phase of an mbarrier written by peers of the cluster.
 __device__ __forceinline__ bool wait_exchange(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                               int32_t* err, uint64_t wait_ns) {
@@ -185,77 +171,6 @@ __device__ __forceinline__ int64_t next_valid(const Args& a, int64_t row, int64_
     for (; row < a.T; row += stride)
         if (label_valid(a, a.labels[row])) return row;
     return a.T;
-}
-
-// ---- per-stage work ---------------------------------------------------------------------------
-//
-// A consumer thread takes the 16-byte vectors tid + u * kConsumers (u < kVecPerThread) of a
-// stage; rel0 = (the target's column) - (the column of the thread's first vector).  kFull: the
-// stage is whole, so no vector needs a bound check.
-
-// 16 bytes of -inf in the storage format (vectors past a partial stage's end).
-template <typename S>
-__device__ __forceinline__ uint4 neg_inf16();
-template <>
-__device__ __forceinline__ uint4 neg_inf16<uint16_t>() { return make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u); }
-template <>
-__device__ __forceinline__ uint4 neg_inf16<float>() { return make_uint4(0xFF800000u, 0xFF800000u, 0xFF800000u, 0xFF800000u); }
-
-// Whether the target column falls in one of this thread's vectors of the stage.
-template <typename S>
-__device__ __forceinline__ bool holds_target(int rel0) {
-    constexpr int G = Elt<S>::kGroup, Span = kConsumers * G;
-    return rel0 >= 0 && rel0 < kVecPerThread * Span && (rel0 % Span) < G;
-}
-
-// Forward over one loaded stage.  kTarget: this thread holds the target, whose value goes to
-// *zt and is left out of the sum.
-template <typename S, bool kFull, bool kTarget>
-__device__ __forceinline__ void fwd_stage(const uint4* buf, int nvec, int rel0, int tid, float& m, float& s,
-                                          float& mb, float* zt) {
-    constexpr int G = Elt<S>::kGroup, U = kVecPerThread;
-    float v[U][G];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-        const int vi = tid + u * kConsumers;
-        Elt<S>::unpack((kFull || vi < nvec) ? lds16(buf + vi) : neg_inf16<S>(), v[u]);
-    }
-    if (kTarget) {
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const uint32_t rel = (uint32_t)(rel0 - u * kConsumers * G);
-#pragma unroll
-            for (int k = 0; k < G; ++k)
-                if (rel == (uint32_t)k) { *zt = v[u][k]; v[u][k] = -kInf; }
-        }
-    }
-    ms_push_lazy_batch<U, G>(v, m, s, mb);
-}
-
-// Gradient of one held stage: coef * 2^(z log2 e - bias) for every column, then the thread
-// holding the target overwrites that entry with gt (its own later store to the same address).
-template <typename S, typename O, bool kFull>
-__device__ __forceinline__ void bwd_stage(const uint4* buf, int nvec, O* gcol, int rel0, int tid, float coef,
-                                          float bias, float gt) {
-    constexpr int G = Elt<S>::kGroup, U = kVecPerThread;
-    uint4 r[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-        const int vi = tid + u * kConsumers;
-        if (kFull || vi < nvec) r[u] = lds16(buf + vi);
-    }
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-        const int vi = tid + u * kConsumers;
-        if (kFull || vi < nvec) {
-            float v[G];
-            Elt<S>::unpack(r[u], v);
-#pragma unroll
-            for (int k = 0; k < G; ++k) v[k] = coef * ex2(fmaf(v[k], kLog2e, -bias));
-            GroupStore<O, G>::run(gcol + vi * G, v);
-        }
-    }
-    if (holds_target<S>(rel0)) Elt<O>::store1(gcol + tid * G + rel0, gt);
 }
 
 // ---- the kernel -----------------------------------------------------------------------------
@@ -320,7 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_fused_ring(const __grid_cons
                         break;
                     const uint32_t nb = (uint32_t)min(kChunk, bytes - j * kChunk);
                     tc::mbar_arrive_expect_tx(&ctl.full[st], nb + a.tx_extra);
-                    bulk_load(smem + st * kChunk, src + (int64_t)j * kChunk, nb, &ctl.full[st]);
+                    tc::bulk_load(smem + st * kChunk, src + (int64_t)j * kChunk, nb, &ctl.full[st]);
                     ++q;
                 }
             }
@@ -408,14 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_fused_ring(const __grid_cons
                 const uint4* buf = reinterpret_cast<const uint4*>(smem + st * kChunk);
                 const int nvec = min(kChunk, bytes - j * kChunk) / 16;
                 const int rel0 = ri.tl - (j * (kChunk / (int)sizeof(S)) + tid * G);
-                float* zt = &ctl.zt[e & 1];
-                if (holds_target<S>(rel0)) {
-                    if (nvec == kFullVec) fwd_stage<S, true, true>(buf, nvec, rel0, tid, m, s, mb, zt);
-                    else fwd_stage<S, false, true>(buf, nvec, rel0, tid, m, s, mb, zt);
-                } else {
-                    if (nvec == kFullVec) fwd_stage<S, true, false>(buf, nvec, rel0, tid, m, s, mb, zt);
-                    else fwd_stage<S, false, false>(buf, nvec, rel0, tid, m, s, mb, zt);
-                }
+                stage::fwd_stage_any<S, kConsumers, kVecPerThread>(buf, nvec, rel0, tid, m, s, mb, &ctl.zt[e & 1]);
             }
         };
         // This warp's pair of the row, for the stats warp.
@@ -456,8 +364,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_fused_ring(const __grid_cons
                     const int nvec = min(kChunk, bytes - j * kChunk) / 16;
                     const int col0 = j * (kChunk / (int)sizeof(S));
                     const int rel0 = ri.tl - (col0 + tid * G);
-                    if (nvec == kFullVec) bwd_stage<S, O, true>(buf, nvec, grow + col0, rel0, tid, cf.x, cf.y, cf.z);
-                    else bwd_stage<S, O, false>(buf, nvec, grow + col0, rel0, tid, cf.x, cf.y, cf.z);
+                    if (nvec == kFullVec)
+                        stage::bwd_stage<S, O, kConsumers, kVecPerThread, true>(buf, nvec, grow + col0, rel0, tid, cf.x,
+                                                                                cf.y, cf.z);
+                    else
+                        stage::bwd_stage<S, O, kConsumers, kVecPerThread, false>(buf, nvec, grow + col0, rel0, tid, cf.x,
+                                                                                 cf.y, cf.z);
                 }
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(&ctl.empty[st]);

@@ -1,0 +1,102 @@
+// Per-stage row work of the kernels that stream rows through a shared-memory stage ring
+// (ce_ring.cu: one-pass forward + gradient; ce_fwd_ring.cu: forward).  NT consumer threads
+// share a stage; thread tid takes its 16-byte vectors tid + u * NT (u < U).  rel0 is the
+// target's column minus the column of the thread's first vector of the stage.  kFull: the
+// stage is whole (U * NT vectors), so no vector needs a bound check.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "vce_async.cuh"
+#include "vce_device.cuh"
+
+namespace vce {
+namespace stage {
+
+// 16 bytes of -inf in the storage format (vectors past a partial stage's end).
+template <typename S>
+__device__ __forceinline__ uint4 neg_inf16();
+template <>
+__device__ __forceinline__ uint4 neg_inf16<uint16_t>() {
+    return make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
+}
+template <>
+__device__ __forceinline__ uint4 neg_inf16<float>() {
+    return make_uint4(0xFF800000u, 0xFF800000u, 0xFF800000u, 0xFF800000u);
+}
+
+// Whether the target column falls in one of this thread's vectors of the stage.
+template <typename S, int NT, int U>
+__device__ __forceinline__ bool holds_target(int rel0) {
+    constexpr int G = Elt<S>::kGroup, Span = NT * G;
+    return rel0 >= 0 && rel0 < U * Span && (rel0 % Span) < G;
+}
+
+// Forward over one loaded stage: the thread's (max, sum-exp) pair takes its U * G values at
+// once (one reference check, one overflow check).  kTarget: this thread holds the target,
+// whose value goes to *zt and is left out of the sum.
+template <typename S, int NT, int U, bool kFull, bool kTarget>
+__device__ __forceinline__ void fwd_stage(const uint4* buf, int nvec, int rel0, int tid, float& m, float& s,
+                                          float& mb, float* zt) {
+    constexpr int G = Elt<S>::kGroup;
+    float v[U][G];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const int vi = tid + u * NT;
+        Elt<S>::unpack((kFull || vi < nvec) ? tc::lds16(buf + vi) : neg_inf16<S>(), v[u]);
+    }
+    if (kTarget) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const uint32_t rel = (uint32_t)(rel0 - u * NT * G);
+#pragma unroll
+            for (int k = 0; k < G; ++k)
+                if (rel == (uint32_t)k) { *zt = v[u][k]; v[u][k] = -kInf; }
+        }
+    }
+    ms_push_lazy_batch<U, G>(v, m, s, mb);
+}
+
+// The forward of a stage, choosing the instantiation for this thread and stage.
+template <typename S, int NT, int U>
+__device__ __forceinline__ void fwd_stage_any(const uint4* buf, int nvec, int rel0, int tid, float& m, float& s,
+                                              float& mb, float* zt) {
+    const bool full = nvec == U * NT;
+    if (holds_target<S, NT, U>(rel0)) {
+        if (full) fwd_stage<S, NT, U, true, true>(buf, nvec, rel0, tid, m, s, mb, zt);
+        else fwd_stage<S, NT, U, false, true>(buf, nvec, rel0, tid, m, s, mb, zt);
+    } else {
+        if (full) fwd_stage<S, NT, U, true, false>(buf, nvec, rel0, tid, m, s, mb, zt);
+        else fwd_stage<S, NT, U, false, false>(buf, nvec, rel0, tid, m, s, mb, zt);
+    }
+}
+
+// Gradient of one held stage: coef * 2^(z log2 e - bias) for every column, then the thread
+// holding the target overwrites that entry with gt (its own later store to the same address).
+template <typename S, typename O, int NT, int U, bool kFull>
+__device__ __forceinline__ void bwd_stage(const uint4* buf, int nvec, O* gcol, int rel0, int tid, float coef,
+                                          float bias, float gt) {
+    constexpr int G = Elt<S>::kGroup;
+    uint4 r[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const int vi = tid + u * NT;
+        if (kFull || vi < nvec) r[u] = tc::lds16(buf + vi);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const int vi = tid + u * NT;
+        if (kFull || vi < nvec) {
+            float v[G];
+            Elt<S>::unpack(r[u], v);
+#pragma unroll
+            for (int k = 0; k < G; ++k) v[k] = coef * ex2(fmaf(v[k], kLog2e, -bias));
+            GroupStore<O, G>::run(gcol + vi * G, v);
+        }
+    }
+    if (holds_target<S, NT, U>(rel0)) Elt<O>::store1(gcol + tid * G + rel0, gt);
+}
+
+}  // namespace stage
+}  // namespace vce

@@ -73,6 +73,7 @@ extern "C" const char* vce_status_string(int status) {
         case 107: return "a one-pass CE wait for the cluster's row statistics gave up";
         case 108: return "a one-pass CE wait for the warps' partial row statistics gave up";
         case 109: return "a one-pass CE wait for a row's gradient coefficients gave up";
+        case 110: return "a CE forward wait for free statistics slots gave up";
         default: return "unknown status";
     }
 }

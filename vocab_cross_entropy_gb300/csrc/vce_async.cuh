@@ -1,6 +1,6 @@
 // Asynchronous-copy and mbarrier helpers (hand-written PTX) for the TMA-fed kernels:
 // shared-memory addresses, mbarrier init / arrive / bounded wait, tiled TMA loads
-// (cp.async.bulk.tensor).
+// (cp.async.bulk.tensor), untiled bulk copies (cp.async.bulk) and 16-byte shared loads.
 #pragma once
 
 #include <cuda.h>
@@ -87,6 +87,24 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
             smem_u32(dst)),
         "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
         : "memory");
+}
+
+// Untiled bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned) from global
+// to this CTA's shared memory, counted on `bar`'s transaction bytes.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ uint4 lds16(const void* p) {
+    uint4 r;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "r"(smem_u32(p)));
+    return r;
 }
 
 __device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
