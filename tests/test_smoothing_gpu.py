@@ -34,10 +34,11 @@ def grade_smoothed_grad(grad_t, ref, c, eps, V, labels):
     assert ok.all(), f"{np.sum(~ok)} entries out of tolerance"
 
 
+@pytest.mark.parametrize("V", [3001, 3008])   # per-block forward; shared-memory stage ring (16-byte rows)
 @pytest.mark.parametrize("eps", [0.0, 0.1, 0.5])
 @pytest.mark.parametrize("dtype,reduction", [("bf16", "mean"), ("f32", "sum"), ("bf16", "none")])
-def test_smoothing_parity(vce, eps, dtype, reduction):
-    p = gen.custom(64, 3001, dtype, seed=71, std=2.0, n_margin=8, margin=(17.0, 50.0), n_ignore=4)
+def test_smoothing_parity(vce, eps, dtype, reduction, V):
+    p = gen.custom(64, V, dtype, seed=71, std=2.0, n_margin=8, margin=(17.0, 50.0), n_ignore=4)
     storage = p.full()
     logits = to_device(storage, dtype)
     labels = torch.from_numpy(p.labels).cuda()

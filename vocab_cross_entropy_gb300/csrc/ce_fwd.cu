@@ -277,12 +277,11 @@ extern "C" int ce_forward_ls(const void* logits, vce_dtype dt, int64_t T, int64_
     if ((rc = require_sm100())) return rc;
     if (cudaMemsetAsync(status, 0, sizeof(int32_t), s) != cudaSuccess) return VCE_ERR_CUDA;
     if (T > 0) {
-        // Rows streamed through shared memory where the layout allows it (no smoothing), else
-        // one block per row with loads from global memory.
+        // Rows streamed through shared memory where the layout allows it, else one block per
+        // row with loads from global memory.
         bool launched = false;
-        cudaError_t e = cudaSuccess;
-        if (label_smoothing == 0.f)
-            e = launch_fwd_ring(dt, logits, T, V, ld, labels, ignore_index, loss_rows, row_stats, status, s, &launched);
+        cudaError_t e = launch_fwd_ring(dt, logits, T, V, ld, labels, ignore_index, label_smoothing, loss_rows,
+                                        row_stats, status, s, &launched);
         if (e == cudaSuccess && !launched) {
             const int nt = pick_threads(V * (int64_t)es);
             e = dt == VCE_BF16 ? dispatch_fwd<uint16_t>(nt, logits, T, V, ld, labels, ignore_index, label_smoothing,

@@ -58,7 +58,7 @@ struct RowInfo {
 
 struct alignas(16) Ctl {
     RowInfo info[kInfoSlots];          // by the row's index in the sequence, mod kInfoSlots
-    float red_m[2][kConsumerWarps], red_s[2][kConsumerWarps];
+    float red_m[2][kConsumerWarps], red_s[2][kConsumerWarps], red_z[2][kConsumerWarps];
     float zt[2];
     uint64_t full[kStages];            // stage loaded
     uint64_t empty[kStages];           // stage released (one arrival per consumer warp)
@@ -76,6 +76,7 @@ struct Args {
     float* loss_rows;
     float4* row_stats;
     int32_t* status;
+    float eps;                         // label smoothing (k_ce_fwd_ring<S, true> only)
     uint64_t wait_ns;
 };
 
@@ -88,7 +89,8 @@ __device__ __forceinline__ int64_t next_valid(const Args& a, int64_t row, int64_
     return a.T;
 }
 
-template <typename S>
+// kSmooth: label smoothing eps > 0; each row's sum of all logits is reduced alongside the pair.
+template <typename S, bool kSmooth>
 __global__ void __launch_bounds__(kThreads, 1) k_ce_fwd_ring(const __grid_constant__ Args a) {
     constexpr int G = Elt<S>::kGroup;
     extern __shared__ __align__(128) uint8_t smem[];
@@ -172,13 +174,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_fwd_ring(const __grid_consta
                 const float s2 = __shfl_xor_sync(0xFFFFFFFFu, s, off);
                 ms_merge(m, s, m2, s2);
             }
+            float tot = 0.f;   // the row's sum of logits, warps added in a fixed order
+            if (kSmooth && lane == 0)
+                for (int w = 0; w < kConsumerWarps; ++w) tot += ctl.red_z[par][w];
             if (lane == 0) {
                 const RowInfo ri = ctl.info[e % kInfoSlots];
                 const float zt = ctl.zt[par];
                 tc::mbar_arrive(&ctl.fbar[par]);   // the parity's slots may be rewritten
                 if (ri.row >= 0 && ri.row < a.T) {  // false only after an abort
                     float loss;
-                    a.row_stats[ri.row] = ce_row_finish(m, s, zt, &loss);
+                    a.row_stats[ri.row] = kSmooth ? ce_row_finish_smoothed(m, s, zt, tot, a.V, a.eps, &loss)
+                                                  : ce_row_finish(m, s, zt, &loss);
                     a.loss_rows[ri.row] = loss;
                 }
             }
@@ -195,7 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_fwd_ring(const __grid_consta
             if (e >= 2)
                 tc::mbar_wait(&ctl.fbar[par], ((e >> 1) & 1) ^ 1, abort_flag, a.status, kErrSlots, a.wait_ns,
                               kSuspendNs);
-            float m = -kInf, s = 0.f, mb = 0.f;
+            float m = -kInf, s = 0.f, mb = 0.f, sz = 0.f;
             int tl = -1;
             for (int j = 0; j < nchunk; ++j) {
                 const uint32_t p = q + j;
@@ -207,15 +213,21 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_fwd_ring(const __grid_consta
                     const uint4* buf = reinterpret_cast<const uint4*>(smem + st * kChunk);
                     const int nvec = (int)(std::min<int64_t>(kChunk, bytes - (int64_t)j * kChunk) / 16);
                     const int rel0 = tl - (j * (kChunk / (int)sizeof(S)) + tid * G);
-                    stage::fwd_stage_any<S, kConsumers, kVecPerThread>(buf, nvec, rel0, tid, m, s, mb, &ctl.zt[par]);
+                    stage::fwd_stage_any<S, kConsumers, kVecPerThread, kSmooth>(buf, nvec, rel0, tid, m, s, mb,
+                                                                                &ctl.zt[par], &sz);
                 }
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(&ctl.empty[st]);
             }
             ms_warp_reduce(m, s);
+            if (kSmooth) {
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) sz += __shfl_xor_sync(0xFFFFFFFFu, sz, off);
+            }
             if (lane == 0) {
                 ctl.red_m[par][warp] = m;
                 ctl.red_s[par][warp] = s;
+                if (kSmooth) ctl.red_z[par][warp] = sz;
             }
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&ctl.rbar[par]);
@@ -225,7 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_fwd_ring(const __grid_consta
 
 template <typename S>
 cudaError_t launch(const Args& args, int sms, cudaStream_t s) {
-    auto kern = k_ce_fwd_ring<S>;
+    auto kern = args.eps > 0.f ? k_ce_fwd_ring<S, true> : k_ce_fwd_ring<S, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     const int grid = (int)std::min<int64_t>(sms, args.T);
@@ -236,14 +248,14 @@ cudaError_t launch(const Args& args, int sms, cudaStream_t s) {
 }  // namespace fring
 
 cudaError_t launch_fwd_ring(vce_dtype dt, const void* logits, int64_t T, int64_t V, int64_t ld, const int64_t* labels,
-                            int64_t ignore_index, float* loss_rows, float* row_stats, int32_t* status, cudaStream_t s,
-                            bool* launched) {
+                            int64_t ignore_index, float eps, float* loss_rows, float* row_stats, int32_t* status,
+                            cudaStream_t s, bool* launched) {
     using namespace fring;
     *launched = false;
     // 16-byte rows: every row starts on a 16-byte boundary and is whole 16-byte vectors.
     if (T < 1 || V % 8 || ld % 8 || !aligned(logits, 16) || V > (int64_t)1 << 30) return cudaSuccess;
     Args args{logits, T, V, ld, labels, ignore_index, loss_rows, reinterpret_cast<float4*>(row_stats), status,
-              tc::kWaitNs};
+              eps, tc::kWaitNs};
     const int sms = device_sm_count();
     const cudaError_t e = dt == VCE_BF16 ? launch<uint16_t>(args, sms, s) : launch<float>(args, sms, s);
     if (e == cudaSuccess) *launched = true;

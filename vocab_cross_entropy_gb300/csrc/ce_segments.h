@@ -58,12 +58,12 @@ cudaError_t launch_fused_ring(vce_dtype dt, vce_dtype gdt, const void* logits, i
                               int32_t* status, cudaStream_t s, bool* launched, uint64_t wait_ns = 2000000000ull,
                               uint32_t tx_extra = 0);
 
-// CE forward with each row streamed through a shared-memory stage ring (ce_fwd_ring.cu).  Sets
-// *launched when it enqueued the kernel; leaves it false, enqueuing nothing, when the layout
-// does not fit (rows or leading dimension not multiples of 8 elements, logits not 16-byte
-// aligned).
+// CE forward with each row streamed through a shared-memory stage ring (ce_fwd_ring.cu); eps:
+// label smoothing (0: none).  Sets *launched when it enqueued the kernel; leaves it false,
+// enqueuing nothing, when the layout does not fit (rows or leading dimension not multiples of
+// 8 elements, logits not 16-byte aligned).
 cudaError_t launch_fwd_ring(vce_dtype dt, const void* logits, int64_t T, int64_t V, int64_t ld, const int64_t* labels,
-                            int64_t ignore_index, float* loss_rows, float* row_stats, int32_t* status, cudaStream_t s,
-                            bool* launched);
+                            int64_t ignore_index, float eps, float* loss_rows, float* row_stats, int32_t* status,
+                            cudaStream_t s, bool* launched);
 
 }  // namespace vce

@@ -35,16 +35,32 @@ __device__ __forceinline__ bool holds_target(int rel0) {
 
 // Forward over one loaded stage: the thread's (max, sum-exp) pair takes its U * G values at
 // once (one reference check, one overflow check).  kTarget: this thread holds the target,
-// whose value goes to *zt and is left out of the sum.
-template <typename S, int NT, int U, bool kFull, bool kTarget>
+// whose value goes to *zt and is left out of the sum.  kSumZ: the stage's values (target
+// included) are also added to *sz.
+template <typename S, int NT, int U, bool kFull, bool kTarget, bool kSumZ = false>
 __device__ __forceinline__ void fwd_stage(const uint4* buf, int nvec, int rel0, int tid, float& m, float& s,
-                                          float& mb, float* zt) {
+                                          float& mb, float* zt, float* sz = nullptr) {
     constexpr int G = Elt<S>::kGroup;
     float v[U][G];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
         const int vi = tid + u * NT;
         Elt<S>::unpack((kFull || vi < nvec) ? tc::lds16(buf + vi) : neg_inf16<S>(), v[u]);
+    }
+    if (kSumZ) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            if (kFull || tid + u * NT < nvec) {
+                float q[G];
+#pragma unroll
+                for (int k = 0; k < G; ++k) q[k] = v[u][k];
+#pragma unroll
+                for (int w = 1; w < G; w *= 2)
+#pragma unroll
+                    for (int k = 0; k + w < G; k += 2 * w) q[k] += q[k + w];
+                *sz += q[0];
+            }
+        }
     }
     if (kTarget) {
 #pragma unroll
@@ -59,16 +75,16 @@ __device__ __forceinline__ void fwd_stage(const uint4* buf, int nvec, int rel0, 
 }
 
 // The forward of a stage, choosing the instantiation for this thread and stage.
-template <typename S, int NT, int U>
+template <typename S, int NT, int U, bool kSumZ = false>
 __device__ __forceinline__ void fwd_stage_any(const uint4* buf, int nvec, int rel0, int tid, float& m, float& s,
-                                              float& mb, float* zt) {
+                                              float& mb, float* zt, float* sz = nullptr) {
     const bool full = nvec == U * NT;
     if (holds_target<S, NT, U>(rel0)) {
-        if (full) fwd_stage<S, NT, U, true, true>(buf, nvec, rel0, tid, m, s, mb, zt);
-        else fwd_stage<S, NT, U, false, true>(buf, nvec, rel0, tid, m, s, mb, zt);
+        if (full) fwd_stage<S, NT, U, true, true, kSumZ>(buf, nvec, rel0, tid, m, s, mb, zt, sz);
+        else fwd_stage<S, NT, U, false, true, kSumZ>(buf, nvec, rel0, tid, m, s, mb, zt, sz);
     } else {
-        if (full) fwd_stage<S, NT, U, true, false>(buf, nvec, rel0, tid, m, s, mb, zt);
-        else fwd_stage<S, NT, U, false, false>(buf, nvec, rel0, tid, m, s, mb, zt);
+        if (full) fwd_stage<S, NT, U, true, false, kSumZ>(buf, nvec, rel0, tid, m, s, mb, zt, sz);
+        else fwd_stage<S, NT, U, false, false, kSumZ>(buf, nvec, rel0, tid, m, s, mb, zt, sz);
     }
 }
 
