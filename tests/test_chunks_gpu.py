@@ -42,7 +42,10 @@ def chunk_check(vce, p, widths, reduction="mean", grad_output=1.0):
     return loss_rows, grads
 
 
-@pytest.mark.parametrize("widths", [[7, 9, 1, 15], [1000], [1, 1, 998], [333, 334, 333], [64] * 16])
+# widths of whole 16-byte vectors in both dtypes ([1000], [64] * 16, [8] * 4, [4096, 8, 70000]) take
+# the shared-memory stage ring for the chunk statistics; the others take one warp per item
+@pytest.mark.parametrize("widths", [[7, 9, 1, 15], [1000], [1, 1, 998], [333, 334, 333], [64] * 16, [8] * 4,
+                                    [4096, 8, 70000]])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_chunks_small(vce, widths, dtype):
     p = gen.custom(50, sum(widths), dtype, seed=len(widths) * 7 + sum(widths), std=3.0, n_margin=8,

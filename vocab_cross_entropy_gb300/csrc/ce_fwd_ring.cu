@@ -13,9 +13,9 @@
 //                   right away; at the end of a row each warp publishes its pair
 //   stats warp      merges the warps' pairs, finishes the row (loss, row statistics) and frees
 //                   the row's slots; it also writes the outputs of ignored and invalid rows
-// Row hand-offs go through mbarriers double-buffered by the parity of the row's index in the
-// CTA's sequence; consumers wait for the stats warp to free a parity's slots before writing
-// them again, two rows later.  The bf16 row stream of k_ce_fwd is issue-bound (a thread keeps
+// Row hand-offs go through kSlots mbarrier-guarded slots, by the row's index in the CTA's
+// sequence mod kSlots; consumers wait for the stats warp to free a slot before writing it
+// again, kSlots rows later.  The bf16 row stream of k_ce_fwd is issue-bound (a thread keeps
 // four 16-byte loads in flight and sums them one vector at a time); here the copies need no
 // registers and the sum takes fewer instructions per element.
 //
@@ -44,8 +44,9 @@ constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kProducerWarp = kConsumerWarps, kStatsWarp = kConsumerWarps + 1;
 constexpr int kThreads = kConsumers + 64;
 constexpr int kVecPerThread = kChunk / 16 / kConsumers;
-constexpr uint32_t kSuspendNs = 10000;   // longest sleep of one poll of an incomplete phase
-constexpr int kInfoSlots = 16;           // > the rows the producer can run ahead of the stats warp
+constexpr uint32_t kSuspendNs = 0;       // plain polls (a suspend hint measured no faster here)
+constexpr int kSlots = 4;                // hand-off slots: consumers run up to kSlots rows ahead of the stats warp
+constexpr int kInfoSlots = 16;           // > the rows the producer can run ahead of the stats warp (kStages + kSlots)
 static_assert(kVecPerThread * kConsumers * 16 == kChunk, "every consumer takes the same whole vectors of a stage");
 static_assert((kConsumerWarps & (kConsumerWarps - 1)) == 0 && kConsumerWarps <= 32, "warp pairs merge in one warp");
 enum { kErrEmpty = 105, kErrFull = 106, kErrPartials = 108, kErrSlots = 110 };
@@ -58,12 +59,12 @@ struct RowInfo {
 
 struct alignas(16) Ctl {
     RowInfo info[kInfoSlots];          // by the row's index in the sequence, mod kInfoSlots
-    float red_m[2][kConsumerWarps], red_s[2][kConsumerWarps], red_z[2][kConsumerWarps];
-    float zt[2];
+    float red_m[kSlots][kConsumerWarps], red_s[kSlots][kConsumerWarps], red_z[kSlots][kConsumerWarps];
+    float zt[kSlots];
     uint64_t full[kStages];            // stage loaded
     uint64_t empty[kStages];           // stage released (one arrival per consumer warp)
-    uint64_t rbar[2];                  // warp pairs published (one arrival per consumer warp)
-    uint64_t fbar[2];                  // the parity's slots read by the stats warp
+    uint64_t rbar[kSlots];             // warp pairs published (one arrival per consumer warp)
+    uint64_t fbar[kSlots];             // the slot read by the stats warp
     int abort;
 };
 constexpr int kSmemBytes = kStages * kChunk + (int)sizeof(Ctl);
@@ -83,11 +84,6 @@ struct Args {
 __device__ __forceinline__ bool label_valid(const Args& a, int64_t t) {
     return t != a.ignore_index && t >= 0 && t < a.V;
 }
-__device__ __forceinline__ int64_t next_valid(const Args& a, int64_t row, int64_t stride) {
-    for (; row < a.T; row += stride)
-        if (label_valid(a, a.labels[row])) return row;
-    return a.T;
-}
 
 // kSmooth: label smoothing eps > 0; each row's sum of all logits is reduced alongside the pair.
 template <typename S, bool kSmooth>
@@ -106,7 +102,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_fwd_ring(const __grid_consta
             tc::mbar_init(&ctl.full[st], 1);
             tc::mbar_init(&ctl.empty[st], kConsumerWarps);
         }
-        for (int p = 0; p < 2; ++p) {
+        for (int p = 0; p < kSlots; ++p) {
             tc::mbar_init(&ctl.rbar[p], kConsumerWarps);
             tc::mbar_init(&ctl.fbar[p], 1);
         }
@@ -119,6 +115,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_fwd_ring(const __grid_consta
     // The number of valid rows of this CTA (each warp counts for itself).
     auto count_valid = [&]() {
         int n = 0;
+#pragma unroll 4
         for (int64_t row = blockIdx.x + (int64_t)lane * stride; row < a.T; row += 32 * stride)
             n += label_valid(a, a.labels[row]);
 #pragma unroll
@@ -128,24 +125,41 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_fwd_ring(const __grid_consta
 
     if (warp == kProducerWarp) {
         // ---------------- producer ----------------
-        if (lane == 0) {
-            uint32_t q = 0, e = 0;
-            for (int64_t row = next_valid(a, blockIdx.x, stride); row < a.T && !*abort_flag;
-                 row = next_valid(a, row + stride, stride), ++e) {
-                ctl.info[e % kInfoSlots] = RowInfo{row, (int)a.labels[row], 0};   // published with chunk 0
-                const char* src = static_cast<const char*>(a.logits) + row * a.ld * (int64_t)sizeof(S);
-                for (int j = 0; j < nchunk; ++j) {
-                    const int st = (int)(q % kStages);
-                    if (!tc::mbar_wait(&ctl.empty[st], ((q / kStages) & 1) ^ 1, abort_flag, a.status, kErrEmpty,
-                                       a.wait_ns, kSuspendNs))
-                        break;
-                    const uint32_t nb = (uint32_t)std::min<int64_t>(kChunk, bytes - (int64_t)j * kChunk);
-                    tc::mbar_arrive_expect_tx(&ctl.full[st], nb);
-                    tc::bulk_load(smem + st * kChunk, src + (int64_t)j * kChunk, nb, &ctl.full[st]);
-                    ++q;
+        // The warp reads the labels of 32 rows at a time (one per lane) and lane 0 issues the
+        // valid ones in order, so no copy waits on a label load of its own.
+        uint32_t q = 0, e = 0;
+        bool stop = false;
+        for (int64_t base = blockIdx.x; base < a.T && !stop; base += 32 * stride) {
+            const int64_t my = base + (int64_t)lane * stride;
+            const int64_t t_my = my < a.T ? a.labels[my] : 0;
+            uint32_t todo = __ballot_sync(0xFFFFFFFFu, my < a.T && label_valid(a, t_my));
+            while (todo && !stop) {
+                const int b = __ffs(todo) - 1;
+                todo &= todo - 1;
+                const int64_t t = __shfl_sync(0xFFFFFFFFu, t_my, b);
+                if (lane == 0) {
+                    const int64_t row = base + (int64_t)b * stride;
+                    ctl.info[e % kInfoSlots] = RowInfo{row, (int)t, 0};   // published with the first stage
+                    const char* src = static_cast<const char*>(a.logits) + row * a.ld * (int64_t)sizeof(S);
+                    for (int j = 0; j < nchunk; ++j) {
+                        const int st = (int)(q % kStages);
+                        if (!tc::mbar_wait(&ctl.empty[st], ((q / kStages) & 1) ^ 1, abort_flag, a.status, kErrEmpty,
+                                           a.wait_ns, kSuspendNs)) {
+                            stop = true;
+                            break;
+                        }
+                        const uint32_t nb = (uint32_t)std::min<int64_t>(kChunk, bytes - (int64_t)j * kChunk);
+                        tc::mbar_arrive_expect_tx(&ctl.full[st], nb);
+                        tc::bulk_load(smem + st * kChunk, src + (int64_t)j * kChunk, nb, &ctl.full[st]);
+                        ++q;
+                    }
+                    ++e;
+                    stop = stop || *abort_flag;
                 }
+                stop = __shfl_sync(0xFFFFFFFFu, stop, 0);
             }
-            // Copies still in flight (only after an abort) land before the CTA may exit.
+        }
+        if (lane == 0) {   // copies still in flight (only after an abort) land before the CTA may exit
             int never = 0;
             for (uint32_t p = q > (uint32_t)kStages ? q - kStages : 0; p < q; ++p)
                 tc::mbar_wait(&ctl.full[p % kStages], (p / kStages) & 1, &never, nullptr, 0, a.wait_ns);
@@ -153,19 +167,31 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_fwd_ring(const __grid_consta
         __syncwarp();
     } else if (warp == kStatsWarp) {
         // ---------------- row statistics ----------------
-        if (lane == 0) {   // rows whose label is ignore_index or invalid: the logits are not read
-            for (int64_t row = blockIdx.x; row < a.T; row += stride) {
-                const int64_t t = a.labels[row];
-                if (label_valid(a, t)) continue;
+        // Rows whose label is ignore_index or invalid (the logits are not read): one per lane,
+        // four labels loaded before any is used.
+        for (int64_t base = blockIdx.x + (int64_t)lane * stride; base < a.T; base += 4 * 32 * stride) {
+            int64_t tu[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int64_t row = base + (int64_t)u * 32 * stride;
+                tu[u] = row < a.T ? a.labels[row] : 0;
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int64_t row = base + (int64_t)u * 32 * stride;
+                const int64_t t = tu[u];
+                if (row >= a.T || label_valid(a, t)) continue;
                 a.loss_rows[row] = (t == a.ignore_index) ? 0.f : __int_as_float(0x7FC00000);
                 a.row_stats[row] = make_float4(0.f, 0.f, 0.f, 0.f);
                 if (t != a.ignore_index) atomicCAS(a.status, 0, (int32_t)VCE_ERR_LABEL);
             }
         }
+        __syncwarp();
         const int nv = count_valid();
         for (int e = 0; e < nv; ++e) {
-            const int par = e & 1;
-            tc::mbar_wait(&ctl.rbar[par], (e >> 1) & 1, abort_flag, a.status, kErrPartials, a.wait_ns, kSuspendNs);
+            const int par = e % kSlots;
+            tc::mbar_wait(&ctl.rbar[par], (e / kSlots) & 1, abort_flag, a.status, kErrPartials, a.wait_ns,
+                          kSuspendNs);
             float m = lane < kConsumerWarps ? ctl.red_m[par][lane] : -kInf;
             float s = lane < kConsumerWarps ? ctl.red_s[par][lane] : 0.f;
 #pragma unroll
@@ -180,7 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_fwd_ring(const __grid_consta
             if (lane == 0) {
                 const RowInfo ri = ctl.info[e % kInfoSlots];
                 const float zt = ctl.zt[par];
-                tc::mbar_arrive(&ctl.fbar[par]);   // the parity's slots may be rewritten
+                tc::mbar_arrive(&ctl.fbar[par]);   // the slot may be rewritten
                 if (ri.row >= 0 && ri.row < a.T) {  // false only after an abort
                     float loss;
                     a.row_stats[ri.row] = kSmooth ? ce_row_finish_smoothed(m, s, zt, tot, a.V, a.eps, &loss)
@@ -196,10 +222,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_fwd_ring(const __grid_consta
         const int nv = count_valid();
         uint32_t q = 0;   // ring chunk of the current row's first chunk
         for (int e = 0; e < nv; ++e, q += nchunk) {
-            const int par = e & 1;
-            // the slots of this parity were read for row e - 2
-            if (e >= 2)
-                tc::mbar_wait(&ctl.fbar[par], ((e >> 1) & 1) ^ 1, abort_flag, a.status, kErrSlots, a.wait_ns,
+            const int par = e % kSlots;
+            // the slot was read for row e - kSlots
+            if (e >= kSlots)
+                tc::mbar_wait(&ctl.fbar[par], ((e / kSlots) & 1) ^ 1, abort_flag, a.status, kErrSlots, a.wait_ns,
                               kSuspendNs);
             float m = -kInf, s = 0.f, mb = 0.f, sz = 0.f;
             int tl = -1;

@@ -212,6 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_fused_ring(const __grid_cons
     // The number of valid rows of this cluster (each warp counts for itself).
     auto count_valid = [&]() {
         int n = 0;
+#pragma unroll 4
         for (int64_t row = cid + (int64_t)lane * ncl; row < a.T; row += 32 * ncl) n += label_valid(a, a.labels[row]);
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) n += __shfl_xor_sync(0xFFFFFFFFu, n, off);
@@ -297,17 +298,26 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_fused_ring(const __grid_cons
         const int tid = threadIdx.x;
 
         // Rows whose label is ignore_index or invalid: gradient +0.0 by selection, logits unread.
-        for (int64_t row = cid; row < a.T; row += ncl) {
-            const int64_t t = a.labels[row];
-            if (label_valid(a, t)) continue;
-            if (rank == 0 && tid == 0) {
-                a.loss_rows[row] = (t == a.ignore_index) ? 0.f : __int_as_float(0x7FC00000);
-                a.row_stats[row] = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (t != a.ignore_index) atomicCAS(a.status, 0, (int32_t)VCE_ERR_LABEL);
+        // Each warp reads the labels of 32 of the cluster's rows at once and zero-fills the
+        // invalid ones' slices.
+        for (int64_t base = cid + (int64_t)warp * 32 * ncl; base < a.T; base += (int64_t)kConsumerWarps * 32 * ncl) {
+            const int64_t my = base + (int64_t)lane * ncl;
+            const int64_t t_my = my < a.T ? a.labels[my] : 0;
+            uint32_t bad = __ballot_sync(0xFFFFFFFFu, my < a.T && !label_valid(a, t_my));
+            while (bad) {
+                const int b = __ffs(bad) - 1;
+                bad &= bad - 1;
+                const int64_t row = base + (int64_t)b * ncl;
+                const int64_t t = __shfl_sync(0xFFFFFFFFu, t_my, b);
+                if (rank == 0 && lane == 0) {
+                    a.loss_rows[row] = (t == a.ignore_index) ? 0.f : __int_as_float(0x7FC00000);
+                    a.row_stats[row] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (t != a.ignore_index) atomicCAS(a.status, 0, (int32_t)VCE_ERR_LABEL);
+                }
+                O* grow = static_cast<O*>(a.grad) + row * a.ld_g + c0;
+                const float zero[G] = {};
+                for (int vi = lane; vi < w / G; vi += 32) GroupStore<O, G>::run(grow + vi * G, zero);
             }
-            O* grow = static_cast<O*>(a.grad) + row * a.ld_g + c0;
-            const float zero[G] = {};
-            for (int vi = tid; vi < w / G; vi += kConsumers) GroupStore<O, G>::run(grow + vi * G, zero);
         }
 
         // Forward over chunks [j0, j1) of valid row e, whose first chunk is ring chunk q0.  The
