@@ -375,7 +375,7 @@ class LinearWorkload:
         self.go = torch.ones(1, dtype=torch.float32, device=device)
         self.loss_host = torch.empty(1, dtype=torch.float32, pin_memory=True)
         nchunks = -(-V // 16384)
-        self.launches_per_step = 2 + 3 + 3 * nchunks     # transposes, stats GEMM + merge + reduce, 3 GEMMs/chunk
+        self.launches_per_step = 3 + 3 * nchunks     # statistics GEMM + merge + reduce, 3 GEMMs per chunk
 
     def step(self, stream):
         self.vce.linear_ce_fwd_bwd(self.E, self.W, self.labels, grad_output=self.go, dE=self.dE, dW=self.dW,

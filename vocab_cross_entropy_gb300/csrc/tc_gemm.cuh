@@ -84,7 +84,18 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
           "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
         : "r"(taddr));
 }
-__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// Wait until this thread's tcgen05.ld have landed.  r, the destination of the last load, is
+// tied to the wait, so no use of it can be scheduled before the wait.
+__device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[32]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                   "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                   "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
+                   "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]),
+                   "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+                 :
+                 : "memory");
+}
 
 // Shared-memory matrix descriptor: K-major operand, rows of 64 bf16 (128 B) written by TMA
 // with the 128-byte swizzle; 8-row groups 1024 B apart (stride byte offset).  The leading
@@ -285,15 +296,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             int tm, tn;
             tile_coords(g, tile, tm, tn);
             const int row = tm * BM + sub * 32 + lane;
-            typename Epi::Row st;
-            Epi::begin(ep, st, row, tn);
             const uint32_t t0 = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(sub * 32) << 16);
+            uint8_t* stage = epi_smem + sub * EPI_WARP_BYTES;
+            // Two register buffers: the next 32 columns load from TMEM while these are consumed.
+            static_assert((BN / 32) % 2 == 0, "column pieces go in pairs");
+            uint32_t ra[32], rb[32];
+            tmem_ld32(t0, ra);
+            typename Epi::Row st;
+            Epi::begin(ep, st, row, tn);   // its global loads overlap the first TMEM load
 #pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
-                uint32_t r[32];
-                tmem_ld32(t0 + (uint32_t)(c * 32), r);
-                tmem_wait_ld();
-                Epi::consume(ep, st, row, tn * BN + c * 32, r, epi_smem + sub * EPI_WARP_BYTES);
+            for (int c = 0; c < BN / 32; c += 2) {
+                tmem_wait_ld(ra);
+                tmem_ld32(t0 + (uint32_t)((c + 1) * 32), rb);
+                Epi::consume(ep, st, row, tn * BN + c * 32, ra, stage);
+                tmem_wait_ld(rb);
+                if (c + 2 < BN / 32) tmem_ld32(t0 + (uint32_t)((c + 2) * 32), ra);
+                Epi::consume(ep, st, row, tn * BN + (c + 1) * 32, rb, stage);
             }
             Epi::end(ep, st, row, tn);
             tc_fence_before();
