@@ -196,6 +196,19 @@ int ce_forward_backward(const void* logits, vce_dtype dt, int64_t T, int64_t V, 
                         int32_t* status, vce_stream_t s);
 
 /*
+ * ce_forward_backward_ls -- ce_forward_backward with label smoothing: the loss, statistics and
+ * gradient of ce_forward_ls followed by ce_backward_ls (the targets q = (1 - eps) onehot(t) +
+ * eps / V), in the same one pass over the logits.  label_smoothing outside [0, 1) (or NaN)
+ * returns VCE_ERR_ARG; eps = 0 is exactly ce_forward_backward.  Other arguments as
+ * ce_forward_backward.
+ */
+int ce_forward_backward_ls(const void* logits, vce_dtype dt, int64_t T, int64_t V, int64_t ld,
+                           const int64_t* labels, int64_t ignore_index, float label_smoothing,
+                           vce_reduction red, const float* grad_output, float* loss_rows,
+                           float* loss_out, float* row_stats, void* grad_logits, vce_dtype grad_dt,
+                           int64_t ld_grad, int32_t* status, vce_stream_t s);
+
+/*
  * vce_test_ce_fused_stall -- test hook for the give-up path of ce_forward_backward's
  * shared-memory kernel (no page counterpart).  Runs that kernel on bf16 logits [T, V]
  * (ld = V), ignore_index -100, reduction SUM, with its producer announcing 16 more bytes per

@@ -95,3 +95,61 @@ def test_smoothing_pages_shape_sampled(vce):
     ref = O.ce_smoothed(O.widen(storage[rr], "bf16"), p.labels[rr], eps, "sum", grad_output=1.0 / N)
     G.check_loss_rows(rows.cpu().numpy()[rr], ref["loss_rows"], ref["valid"])
     grade_smoothed_grad(grad[torch.from_numpy(rr).cuda()], ref, ref["c"], eps, p.V, p.labels[rr])
+
+
+# ---- the one-pass call (ce_forward_backward_ls) -----------------------------------------------
+
+@pytest.mark.parametrize("V", [3001, 3008, 70000])   # L2 re-read; stage ring, one CTA; 2-CTA cluster
+@pytest.mark.parametrize("eps", [0.1, 0.5])
+@pytest.mark.parametrize("dtype,reduction,gdt", [("bf16", "mean", None), ("f32", "sum", None),
+                                                 ("bf16", "none", torch.float32)])
+def test_one_pass_smoothing_parity(vce, eps, dtype, reduction, gdt, V):
+    T = 32 if V > 10000 else 64
+    p = gen.custom(T, V, dtype, seed=73, std=2.0, n_margin=6, margin=(17.0, 50.0), n_ignore=3)
+    storage = p.full()
+    logits = to_device(storage, dtype)
+    labels = torch.from_numpy(p.labels).cuda()
+    go_np = np.linspace(0.5, 2.0, T) if reduction == "none" else np.array([1.25])
+    go = torch.from_numpy(go_np.astype(np.float32)).cuda()
+    out, rows, stats, grad, status = vce.ce_forward_backward_ls(logits, labels, eps, reduction=reduction,
+                                                               grad_output=go, grad_dtype=gdt)
+    torch.cuda.synchronize()
+    assert vce.vce_get_status(status) == 0
+    ref = O.ce_smoothed(O.widen(storage, dtype), p.labels, eps, reduction, go_np if reduction == "none" else 1.25)
+    G.check_loss_rows(rows.cpu().numpy(), ref["loss_rows"], ref["valid"])
+    if reduction != "none":
+        G.check_reduced(out.item(), ref["loss_out"])
+    grade_smoothed_grad(grad, ref, ref["c"], eps, p.V, p.labels)
+
+
+@pytest.mark.parametrize("V", [3001, 3008])
+def test_one_pass_smoothing_zero_is_the_plain_call(vce, V):
+    p = gen.custom(40, V, "bf16", seed=74, n_margin=4, n_ignore=2)
+    logits = to_device(p.full(), "bf16")
+    labels = torch.from_numpy(p.labels).cuda()
+    a = vce.ce_forward_backward_ls(logits, labels, 0.0)
+    a = tuple(x.clone() for x in a)
+    b = vce.ce_forward_backward(logits, labels)
+    torch.cuda.synchronize()
+    for x, y in zip(a[:4], b[:4]):
+        assert torch.equal(x, y)
+    for bad in (-0.1, 1.0, float("nan")):
+        with pytest.raises(vce.VceError):
+            vce.ce_forward_backward_ls(logits, labels, bad)
+
+
+def test_one_pass_smoothing_pages_shape_sampled(vce):
+    p = gen.pages()
+    storage = p.full()
+    logits = to_device(storage, "bf16")
+    labels = torch.from_numpy(p.labels).cuda()
+    eps = 0.1
+    out, rows, stats, grad, status = vce.ce_forward_backward_ls(logits, labels, eps)
+    torch.cuda.synchronize()
+    assert vce.vce_get_status(status) == 0
+    rng = np.random.default_rng(22)
+    rr = np.unique(np.concatenate([p.margin_rows[:100], rng.choice(p.T, 100, replace=False)]))
+    N = int(np.sum(p.labels != p.ignore_index))
+    ref = O.ce_smoothed(O.widen(storage[rr], "bf16"), p.labels[rr], eps, "sum", grad_output=1.0 / N)
+    G.check_loss_rows(rows.cpu().numpy()[rr], ref["loss_rows"], ref["valid"])
+    grade_smoothed_grad(grad[torch.from_numpy(rr).cuda()], ref, ref["c"], eps, p.V, p.labels[rr])

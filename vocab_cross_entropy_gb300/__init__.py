@@ -14,7 +14,7 @@ import os
 import torch
 
 __all__ = ["VceError", "lib", "library_path", "ce_forward", "ce_backward", "ce_forward_ls", "ce_backward_ls",
-           "ce_forward_backward", "ce_merge_chunks",
+           "ce_forward_backward", "ce_forward_backward_ls", "ce_merge_chunks",
            "ce_merge_chunks_noalloc",
            "linear_ce_workspace_bytes", "linear_ce_fwd_bwd", "vce_get_status", "vce_status_string",
            "vce_abi_version", "cross_entropy", "IGNORE_INDEX", "F32", "BF16", "RED"]
@@ -49,6 +49,8 @@ def _load():
     L.ce_forward.argtypes = [p, i32, i64, i64, i64, p, i64, i32, p, p, p, p, p]
     L.ce_backward.argtypes = [p, i32, i64, i64, i64, p, i64, i32, p, p, p, i32, i64, p]
     L.ce_forward_backward.argtypes = [p, i32, i64, i64, i64, p, i64, i32, p, p, p, p, p, i32, i64, p, p]
+    L.ce_forward_backward_ls.argtypes = [p, i32, i64, i64, i64, p, i64, ctypes.c_float, i32, p, p, p, p, p, i32, i64,
+                                         p, p]
     f32 = ctypes.c_float
     L.ce_forward_ls.argtypes = [p, i32, i64, i64, i64, p, i64, f32, i32, p, p, p, p, p]
     L.ce_backward_ls.argtypes = [p, i32, i64, i64, i64, p, i64, f32, i32, p, p, p, i32, i64, p]
@@ -65,6 +67,7 @@ def _load():
         L.vce_test_ce_fused_stall.argtypes = [p, i64, i64, p, p, p, p, p, ctypes.c_uint64, p, p]
         L.vce_test_ce_fused_stall.restype = i32
     for name in ("ce_forward", "ce_backward", "ce_forward_ls", "ce_backward_ls", "ce_forward_backward",
+                 "ce_forward_backward_ls",
                  "ce_merge_chunks", "ce_merge_chunks_noalloc",
                  "linear_ce_fwd_bwd",
                  "vce_get_status"):
@@ -211,6 +214,27 @@ def ce_forward_backward(logits, labels, ignore_index=IGNORE_INDEX, reduction="me
         _dtype(grad_logits), _ld(grad_logits), _ptr(status), _stream(stream)))
     return loss_out, loss_rows, row_stats, grad_logits, status
 
+
+def ce_forward_backward_ls(logits, labels, label_smoothing, ignore_index=IGNORE_INDEX, reduction="mean", *,
+                           grad_output=None, grad_logits=None, grad_dtype=None, loss_rows=None, loss_out=None,
+                           row_stats=None, status=None, stream=None):
+    """ce_forward_backward with label smoothing.  Returns (loss_out, loss_rows, row_stats, grad_logits, status)."""
+    T, V = logits.shape
+    dev = logits.device
+    loss_rows = torch.empty(T, dtype=torch.float32, device=dev) if loss_rows is None else loss_rows
+    row_stats = torch.empty(T, ROW_STATS, dtype=torch.float32, device=dev) if row_stats is None else row_stats
+    status = torch.empty(1, dtype=torch.int32, device=dev) if status is None else status
+    if reduction != "none" and loss_out is None:
+        loss_out = torch.empty(1, dtype=torch.float32, device=dev)
+    if grad_output is None:
+        grad_output = torch.ones(T if reduction == "none" else 1, dtype=torch.float32, device=dev)
+    if grad_logits is None:
+        grad_logits = torch.empty(T, V, dtype=grad_dtype or logits.dtype, device=dev)
+    _check("ce_forward_backward_ls", _get().ce_forward_backward_ls(
+        _ptr(logits), _dtype(logits), T, V, _ld(logits), _ptr(labels), int(ignore_index), float(label_smoothing),
+        RED[reduction], _ptr(grad_output), _ptr(loss_rows), _ptr(loss_out), _ptr(row_stats), _ptr(grad_logits),
+        _dtype(grad_logits), _ld(grad_logits), _ptr(status), _stream(stream)))
+    return loss_out, loss_rows, row_stats, grad_logits, status
 
 def ce_merge_chunks(chunks, labels, ignore_index=IGNORE_INDEX, reduction="mean", *, grad_output=None,
                     chunk_grads=None, grad_dtype=None, want_grad=True, loss_rows=None, loss_out=None,

@@ -52,14 +52,16 @@ __global__ void __launch_bounds__(NT) k_ce_count_valid(const int64_t* __restrict
 }
 
 // Two 512-thread blocks per SM: both streams inlined need ~60 registers (three blocks would spill).
-template <typename S, typename O, int NT>
+// kSmooth: label smoothing eps > 0 (the row's sum of logits is reduced alongside the pair; the
+// non-target gradient entries lose c eps / V).
+template <typename S, typename O, int NT, bool kSmooth>
 __global__ void __launch_bounds__(NT, 1024 / NT)
     k_ce_fused(const S* __restrict__ logits, int64_t T, int64_t V, int64_t ld, const int64_t* __restrict__ labels,
                int64_t ignore_index, int red, const float* __restrict__ grad_output, const float* __restrict__ inv_n,
                float* __restrict__ loss_rows, float4* __restrict__ row_stats, O* __restrict__ grad, int64_t ld_g,
-               int32_t* status) {
-    __shared__ float sm_m[NT / 32], sm_s[NT / 32];
-    __shared__ float sm_zt, sm_coef, sm_bias, sm_gt;
+               int32_t* status, float eps) {
+    __shared__ float sm_m[NT / 32], sm_s[NT / 32], sm_sz[NT / 32];
+    __shared__ float sm_zt, sm_coef, sm_bias, sm_gt, sm_shift;
     const float w_valid = (red == VCE_RED_MEAN) ? *inv_n : 1.f;
     for (int64_t row = blockIdx.x; row < T; row += gridDim.x) {
         const int64_t t = labels[row];
@@ -75,12 +77,24 @@ __global__ void __launch_bounds__(NT, 1024 / NT)
             bwd_segment<S, O, NT>(in, out, V, -1, 0.f, 0.f, 0.f, true);
             continue;
         }
-        float m = -kInf, s = 0.f, mb = 0.f;
-        fwd_segment<S, NT, true, kLoadKeep>(in, V, t, m, s, mb, &sm_zt, threadIdx.x);
+        float m = -kInf, s = 0.f, mb = 0.f, sz = 0.f;
+        fwd_segment<S, NT, true, kLoadKeep, kSmooth>(in, V, t, m, s, mb, &sm_zt, threadIdx.x, &sz);
+        if (kSmooth) {   // block sum of the logits (the barrier below publishes the warp sums)
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) sz += __shfl_xor_sync(0xFFFFFFFFu, sz, off);
+            if ((threadIdx.x & 31) == 0) sm_sz[threadIdx.x >> 5] = sz;
+        }
         ms_block_reduce<NT>(m, s, sm_m, sm_s);
         if (threadIdx.x == 0) {
             float loss;
-            float4 st = ce_row_finish(m, s, sm_zt, &loss);
+            float4 st;
+            if (kSmooth) {
+                float tot = 0.f;
+                for (int k = 0; k < NT / 32; ++k) tot += sm_sz[k];
+                st = ce_row_finish_smoothed(m, s, sm_zt, tot, V, eps, &loss);
+            } else {
+                st = ce_row_finish(m, s, sm_zt, &loss);
+            }
             st.w = w_valid;
             row_stats[row] = st;
             loss_rows[row] = loss;
@@ -88,9 +102,10 @@ __global__ void __launch_bounds__(NT, 1024 / NT)
             sm_coef = c * st.y;
             sm_bias = (st.x == -kInf) ? 0.f : st.x * kLog2e;
             sm_gt = c * st.z;
+            sm_shift = kSmooth ? c * (eps / (float)V) : 0.f;
         }
         __syncthreads();
-        bwd_segment<S, O, NT>(in, out, V, t, sm_coef, sm_bias, sm_gt, false);
+        bwd_segment<S, O, NT>(in, out, V, t, sm_coef, sm_bias, sm_gt, false, sm_shift);
         __syncthreads();   // sm_* are rewritten by the next row
     }
 }
@@ -98,21 +113,23 @@ __global__ void __launch_bounds__(NT, 1024 / NT)
 template <typename S, typename O, int NT>
 cudaError_t launch_fused(const void* logits, int64_t T, int64_t V, int64_t ld, const int64_t* labels, int64_t ig,
                          int red, const float* go, const float* inv_n, float* loss_rows, float* row_stats, void* grad,
-                         int64_t ld_g, int32_t* status, cudaStream_t s) {
-    auto kern = k_ce_fused<S, O, NT>;
+                         int64_t ld_g, int32_t* status, float eps, cudaStream_t s) {
+    auto kern = eps > 0.f ? k_ce_fused<S, O, NT, true> : k_ce_fused<S, O, NT, false>;
     kern<<<grid_for(kern, NT, T), NT, 0, s>>>(reinterpret_cast<const S*>(logits), T, V, ld, labels, ig, red, go,
                                               inv_n, loss_rows, reinterpret_cast<float4*>(row_stats),
-                                              reinterpret_cast<O*>(grad), ld_g, status);
+                                              reinterpret_cast<O*>(grad), ld_g, status, eps);
     return cudaGetLastError();
 }
 
 template <typename S, typename O>
 cudaError_t dispatch_fused2(int nt, const void* logits, int64_t T, int64_t V, int64_t ld, const int64_t* labels,
                             int64_t ig, int red, const float* go, const float* inv_n, float* lr, float* rs, void* g,
-                            int64_t ldg, int32_t* st, cudaStream_t s) {
-    if (nt == 128) return launch_fused<S, O, 128>(logits, T, V, ld, labels, ig, red, go, inv_n, lr, rs, g, ldg, st, s);
-    if (nt == 256) return launch_fused<S, O, 256>(logits, T, V, ld, labels, ig, red, go, inv_n, lr, rs, g, ldg, st, s);
-    return launch_fused<S, O, 512>(logits, T, V, ld, labels, ig, red, go, inv_n, lr, rs, g, ldg, st, s);
+                            int64_t ldg, int32_t* st, float eps, cudaStream_t s) {
+    if (nt == 128)
+        return launch_fused<S, O, 128>(logits, T, V, ld, labels, ig, red, go, inv_n, lr, rs, g, ldg, st, eps, s);
+    if (nt == 256)
+        return launch_fused<S, O, 256>(logits, T, V, ld, labels, ig, red, go, inv_n, lr, rs, g, ldg, st, eps, s);
+    return launch_fused<S, O, 512>(logits, T, V, ld, labels, ig, red, go, inv_n, lr, rs, g, ldg, st, eps, s);
 }
 
 }  // namespace
@@ -120,14 +137,15 @@ cudaError_t dispatch_fused2(int nt, const void* logits, int64_t T, int64_t V, in
 
 using namespace vce;
 
-extern "C" int ce_forward_backward(const void* logits, vce_dtype dt, int64_t T, int64_t V, int64_t ld,
-                                   const int64_t* labels, int64_t ignore_index, vce_reduction red,
-                                   const float* grad_output, float* loss_rows, float* loss_out, float* row_stats,
-                                   void* grad_logits, vce_dtype grad_dt, int64_t ld_grad, int32_t* status,
-                                   vce_stream_t s) {
+extern "C" int ce_forward_backward_ls(const void* logits, vce_dtype dt, int64_t T, int64_t V, int64_t ld,
+                                      const int64_t* labels, int64_t ignore_index, float label_smoothing,
+                                      vce_reduction red, const float* grad_output, float* loss_rows, float* loss_out,
+                                      float* row_stats, void* grad_logits, vce_dtype grad_dt, int64_t ld_grad,
+                                      int32_t* status, vce_stream_t s) {
     if (dt != VCE_F32 && dt != VCE_BF16) return VCE_ERR_DTYPE;
     if (grad_dt != VCE_F32 && grad_dt != VCE_BF16) return VCE_ERR_DTYPE;
     if (red != VCE_RED_NONE && red != VCE_RED_SUM && red != VCE_RED_MEAN) return VCE_ERR_DTYPE;
+    if (!(label_smoothing >= 0.f && label_smoothing < 1.f)) return VCE_ERR_ARG;
     if (T < 0 || V < 1) return VCE_ERR_SHAPE;
     if (ld < V || ld_grad < V) return VCE_ERR_LD;
     if (!status || (red != VCE_RED_NONE && !loss_out)) return VCE_ERR_NULL;
@@ -148,24 +166,29 @@ extern "C" int ce_forward_backward(const void* logits, vce_dtype dt, int64_t T, 
             k_ce_count_valid<1024><<<1, 1024, 0, s>>>(labels, T, V, ignore_index, loss_out);
             if (cudaGetLastError() != cudaSuccess) return VCE_ERR_CUDA;
         }
+        const float eps = label_smoothing;
         // The row held in shared memory where the layout allows it, else the L2 re-read.
         bool launched = false;
         cudaError_t e = launch_fused_ring(dt, grad_dt, logits, T, V, ld, labels, ignore_index, red, grad_output,
-                                          loss_out, loss_rows, row_stats, grad_logits, ld_grad, status, s, &launched);
+                                          loss_out, loss_rows, row_stats, grad_logits, ld_grad, status, s, &launched,
+                                          eps);
         if (e == cudaSuccess && !launched) {
             const int nt = pick_threads(V * (int64_t)es);
             if (dt == VCE_BF16 && grad_dt == VCE_BF16)
                 e = dispatch_fused2<uint16_t, uint16_t>(nt, logits, T, V, ld, labels, ignore_index, red, grad_output,
-                                                        loss_out, loss_rows, row_stats, grad_logits, ld_grad, status, s);
+                                                        loss_out, loss_rows, row_stats, grad_logits, ld_grad, status,
+                                                        eps, s);
             else if (dt == VCE_BF16)
                 e = dispatch_fused2<uint16_t, float>(nt, logits, T, V, ld, labels, ignore_index, red, grad_output,
-                                                     loss_out, loss_rows, row_stats, grad_logits, ld_grad, status, s);
+                                                     loss_out, loss_rows, row_stats, grad_logits, ld_grad, status,
+                                                     eps, s);
             else if (grad_dt == VCE_BF16)
                 e = dispatch_fused2<float, uint16_t>(nt, logits, T, V, ld, labels, ignore_index, red, grad_output,
-                                                     loss_out, loss_rows, row_stats, grad_logits, ld_grad, status, s);
+                                                     loss_out, loss_rows, row_stats, grad_logits, ld_grad, status,
+                                                     eps, s);
             else
-                e = dispatch_fused2<float, float>(nt, logits, T, V, ld, labels, ignore_index, red, grad_output, loss_out,
-                                                  loss_rows, row_stats, grad_logits, ld_grad, status, s);
+                e = dispatch_fused2<float, float>(nt, logits, T, V, ld, labels, ignore_index, red, grad_output,
+                                                  loss_out, loss_rows, row_stats, grad_logits, ld_grad, status, eps, s);
         }
         if (e != cudaSuccess) return VCE_ERR_CUDA;
     }
@@ -173,4 +196,13 @@ extern "C" int ce_forward_backward(const void* logits, vce_dtype dt, int64_t T, 
         launch_loss_reduce(loss_rows, labels, T, V, ignore_index, red, loss_out, row_stats, s) != cudaSuccess)
         return VCE_ERR_CUDA;
     return VCE_OK;
+}
+
+extern "C" int ce_forward_backward(const void* logits, vce_dtype dt, int64_t T, int64_t V, int64_t ld,
+                                   const int64_t* labels, int64_t ignore_index, vce_reduction red,
+                                   const float* grad_output, float* loss_rows, float* loss_out, float* row_stats,
+                                   void* grad_logits, vce_dtype grad_dt, int64_t ld_grad, int32_t* status,
+                                   vce_stream_t s) {
+    return ce_forward_backward_ls(logits, dt, T, V, ld, labels, ignore_index, 0.f, red, grad_output, loss_rows,
+                                  loss_out, row_stats, grad_logits, grad_dt, ld_grad, status, s);
 }

@@ -82,8 +82,9 @@ constexpr int kInfoSlots = 16;         // > the rows the producer can run ahead 
 struct alignas(16) Ctl {
     RowInfo info[kInfoSlots];          // by the row's index in the sequence, mod kInfoSlots
     float4 slot[2][kMaxCluster];       // (m, s, z_t, owner) of each CTA of the cluster
-    float4 coefs[2];                   // (coef, bias, target gradient, -) of the row
-    float red_m[2][kConsumerWarps], red_s[2][kConsumerWarps];
+    float slot_z[2][kMaxCluster];      // label smoothing: each CTA's sum of its slice's logits
+    float4 coefs[2];                   // (coef, bias, target gradient, non-target shift) of the row
+    float red_m[2][kConsumerWarps], red_s[2][kConsumerWarps], red_z[2][kConsumerWarps];
     float zt[2];
     uint64_t full[kStages];            // stage loaded (producer's expect-tx + the copy's bytes)
     uint64_t empty[kStages];           // stage released (one arrival per consumer warp)
@@ -110,6 +111,7 @@ struct Args {
     int64_t slice;                     // columns per CTA (a multiple of 8)
     uint64_t wait_ns;                  // bound of every wait
     uint32_t tx_extra;                 // 0; > 0 only in the give-up test (a stage never completes)
+    float eps;                         // label smoothing (k_ce_fused_ring<S, O, C, true> only)
 };
 
 // ---- cluster and bulk-copy primitives (inline PTX) -----------------------------------------
@@ -127,6 +129,9 @@ __device__ __forceinline__ uint32_t peer_addr(const void* p, uint32_t rank) {
     uint32_t r;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(tc::smem_u32(p)), "r"(rank));
     return r;
+}
+__device__ __forceinline__ void st_peer1(uint32_t addr, float v) {
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
 __device__ __forceinline__ void st_peer(uint32_t addr, float4 v) {
     asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x), "f"(v.y), "f"(v.z),
@@ -175,7 +180,9 @@ __device__ __forceinline__ int64_t next_valid(const Args& a, int64_t row, int64_
 
 // ---- the kernel -----------------------------------------------------------------------------
 
-template <typename S, typename O, int C>
+// kSmooth: label smoothing eps > 0.  Each row's sum of all logits is reduced beside the pair
+// and exchanged with it; the non-target gradient entries lose c eps / V.
+template <typename S, typename O, int C, bool kSmooth>
 __global__ void __launch_bounds__(kThreads, 1) k_ce_fused_ring(const __grid_constant__ Args a) {
     constexpr int G = Elt<S>::kGroup;
     constexpr int kFullVec = kChunk / 16;
@@ -265,26 +272,36 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_fused_ring(const __grid_cons
             if (lane == 0) {
                 const RowInfo ri = ctl.info[e % kInfoSlots];
                 const bool own = (uint32_t)ri.tl < (uint32_t)w;
-                float M = m, Ssum = s, zt = own ? ctl.zt[par] : 0.f;
+                float sz = 0.f;   // the slice's sum of logits, warps added in a fixed order
+                if (kSmooth)
+                    for (int k = 0; k < kConsumerWarps; ++k) sz += ctl.red_z[par][k];
+                float M = m, Ssum = s, zt = own ? ctl.zt[par] : 0.f, tot = sz;
                 if (C > 1) {
                     const float4 mine = make_float4(m, s, zt, own ? 1.f : 0.f);
-                    for (uint32_t r = 0; r < (uint32_t)C; ++r) st_peer(peer_addr(&ctl.slot[par][rank], r), mine);
+                    for (uint32_t r = 0; r < (uint32_t)C; ++r) {
+                        st_peer(peer_addr(&ctl.slot[par][rank], r), mine);
+                        if (kSmooth) st_peer1(peer_addr(&ctl.slot_z[par][rank], r), sz);
+                    }
                     for (uint32_t r = 0; r < (uint32_t)C; ++r) arrive_peer(peer_addr(&ctl.xbar[par], r));
                     wait_exchange(&ctl.xbar[par], ph, abort_flag, a.status, a.wait_ns);
                     M = -kInf;
                     Ssum = 0.f;
+                    tot = 0.f;
                     for (int r = 0; r < C; ++r) {   // the same order in every CTA
                         const float4 o = ctl.slot[par][r];
                         ms_merge(M, Ssum, o.x, o.y);
                         if (o.w != 0.f) zt = o.z;
+                        if (kSmooth) tot += ctl.slot_z[par][r];
                     }
                 }
                 const bool in_range = ri.row >= 0 && ri.row < a.T;   // false only after an abort
                 float loss;
-                float4 st4 = ce_row_finish(M, Ssum, zt, &loss);
+                float4 st4 = kSmooth ? ce_row_finish_smoothed(M, Ssum, zt, tot, a.V, a.eps, &loss)
+                                     : ce_row_finish(M, Ssum, zt, &loss);
                 st4.w = w_valid;
                 const float c = in_range ? a.grad_output[a.red == VCE_RED_NONE ? ri.row : 0] * w_valid : 0.f;
-                ctl.coefs[par] = make_float4(c * st4.y, (st4.x == -kInf) ? 0.f : st4.x * kLog2e, c * st4.z, 0.f);
+                ctl.coefs[par] = make_float4(c * st4.y, (st4.x == -kInf) ? 0.f : st4.x * kLog2e, c * st4.z,
+                                             kSmooth ? c * (a.eps / (float)a.V) : 0.f);
                 tc::mbar_arrive(&ctl.cbar[par]);
                 if (rank == 0 && in_range) {
                     a.row_stats[ri.row] = st4;
@@ -322,7 +339,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_fused_ring(const __grid_cons
 
         // Forward over chunks [j0, j1) of valid row e, whose first chunk is ring chunk q0.  The
         // row's index and target column are read once its first chunk has landed.
-        auto forward = [&](uint32_t q0, int j0, int j1, int e, RowInfo& ri, float& m, float& s, float& mb) {
+        auto forward = [&](uint32_t q0, int j0, int j1, int e, RowInfo& ri, float& m, float& s, float& mb,
+                           float& sz) {
             for (int j = j0; j < j1; ++j) {
                 const uint32_t p = q0 + j;
                 const int st = (int)(p % kStages);
@@ -333,15 +351,21 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_fused_ring(const __grid_cons
                 const uint4* buf = reinterpret_cast<const uint4*>(smem + st * kChunk);
                 const int nvec = min(kChunk, bytes - j * kChunk) / 16;
                 const int rel0 = ri.tl - (j * (kChunk / (int)sizeof(S)) + tid * G);
-                stage::fwd_stage_any<S, kConsumers, kVecPerThread>(buf, nvec, rel0, tid, m, s, mb, &ctl.zt[e & 1]);
+                stage::fwd_stage_any<S, kConsumers, kVecPerThread, kSmooth>(buf, nvec, rel0, tid, m, s, mb,
+                                                                            &ctl.zt[e & 1], &sz);
             }
         };
         // This warp's pair of the row, for the stats warp.
-        auto publish = [&](int par, float m, float s) {
+        auto publish = [&](int par, float m, float s, float sz) {
             ms_warp_reduce(m, s);
+            if (kSmooth) {
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) sz += __shfl_xor_sync(0xFFFFFFFFu, sz, off);
+            }
             if (lane == 0) {
                 ctl.red_m[par][warp] = m;
                 ctl.red_s[par][warp] = s;
+                if (kSmooth) ctl.red_z[par][warp] = sz;
             }
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&ctl.rbar[par]);
@@ -351,16 +375,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_fused_ring(const __grid_cons
         uint32_t q = 0;   // ring chunk of the current row's first chunk
         RowInfo ri{-1, -1, 0};
         if (nv > 0) {
-            float m = -kInf, s = 0.f, mb = 0.f;
-            forward(q, 0, nchunk, 0, ri, m, s, mb);
-            publish(0, m, s);
+            float m = -kInf, s = 0.f, mb = 0.f, sz = 0.f;
+            forward(q, 0, nchunk, 0, ri, m, s, mb, sz);
+            publish(0, m, s, sz);
         }
         for (int e = 0; e < nv; ++e) {
             const int par = e & 1;
             const bool more = e + 1 < nv;
             RowInfo ri2{-1, -1, 0};
-            float m2 = -kInf, s2 = 0.f, mb2 = 0.f;
-            if (more) forward(q + nchunk, 0, pre, e + 1, ri2, m2, s2, mb2);
+            float m2 = -kInf, s2 = 0.f, mb2 = 0.f, sz2 = 0.f;
+            if (more) forward(q + nchunk, 0, pre, e + 1, ri2, m2, s2, mb2, sz2);
 
             // the row's gradient, each stage released once this warp is done with it
             tc::mbar_wait(&ctl.cbar[par], (e >> 1) & 1, abort_flag, a.status, kErrCoefs, a.wait_ns, kSuspendConsumer);
@@ -376,10 +400,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_fused_ring(const __grid_cons
                     const int rel0 = ri.tl - (col0 + tid * G);
                     if (nvec == kFullVec)
                         stage::bwd_stage<S, O, kConsumers, kVecPerThread, true>(buf, nvec, grow + col0, rel0, tid, cf.x,
-                                                                                cf.y, cf.z);
+                                                                                cf.y, cf.z, cf.w);
                     else
                         stage::bwd_stage<S, O, kConsumers, kVecPerThread, false>(buf, nvec, grow + col0, rel0, tid, cf.x,
-                                                                                 cf.y, cf.z);
+                                                                                 cf.y, cf.z, cf.w);
                 }
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(&ctl.empty[st]);
@@ -387,8 +411,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_fused_ring(const __grid_cons
             q += nchunk;
 
             if (more) {
-                forward(q, pre, nchunk, e + 1, ri2, m2, s2, mb2);
-                publish(par ^ 1, m2, s2);
+                forward(q, pre, nchunk, e + 1, ri2, m2, s2, mb2, sz2);
+                publish(par ^ 1, m2, s2, sz2);
             }
             ri = ri2;
         }
@@ -396,9 +420,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_fused_ring(const __grid_cons
     if (C > 1) cluster_sync();   // no CTA leaves while a peer may still write into its shared memory
 }
 
-template <typename S, typename O, int C>
+template <typename S, typename O, int C, bool kSmooth>
 cudaError_t launch(const Args& args, int sms, cudaStream_t s, bool* launched) {
-    auto kern = k_ce_fused_ring<S, O, C>;
+    auto kern = k_ce_fused_ring<S, O, C, kSmooth>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -435,14 +459,20 @@ cudaError_t launch(const Args& args, int sms, cudaStream_t s, bool* launched) {
     return e;
 }
 
-template <typename S, typename O>
+template <typename S, typename O, bool kSmooth>
 cudaError_t launch_c(int C, const Args& args, int sms, cudaStream_t s, bool* launched) {
     switch (C) {
-        case 1: return launch<S, O, 1>(args, sms, s, launched);
-        case 2: return launch<S, O, 2>(args, sms, s, launched);
-        case 4: return launch<S, O, 4>(args, sms, s, launched);
-        default: return launch<S, O, 8>(args, sms, s, launched);
+        case 1: return launch<S, O, 1, kSmooth>(args, sms, s, launched);
+        case 2: return launch<S, O, 2, kSmooth>(args, sms, s, launched);
+        case 4: return launch<S, O, 4, kSmooth>(args, sms, s, launched);
+        default: return launch<S, O, 8, kSmooth>(args, sms, s, launched);
     }
+}
+
+template <typename S, typename O>
+cudaError_t launch_cs(int C, const Args& args, int sms, cudaStream_t s, bool* launched) {
+    return args.eps > 0.f ? launch_c<S, O, true>(C, args, sms, s, launched)
+                          : launch_c<S, O, false>(C, args, sms, s, launched);
 }
 
 }  // namespace ring
@@ -450,7 +480,8 @@ cudaError_t launch_c(int C, const Args& args, int sms, cudaStream_t s, bool* lau
 cudaError_t launch_fused_ring(vce_dtype dt, vce_dtype gdt, const void* logits, int64_t T, int64_t V, int64_t ld,
                               const int64_t* labels, int64_t ignore_index, int red, const float* grad_output,
                               const float* inv_n, float* loss_rows, float* row_stats, void* grad, int64_t ld_g,
-                              int32_t* status, cudaStream_t s, bool* launched, uint64_t wait_ns, uint32_t tx_extra) {
+                              int32_t* status, cudaStream_t s, bool* launched, float eps, uint64_t wait_ns,
+                              uint32_t tx_extra) {
     using namespace ring;
     *launched = false;
     // 16-byte rows and slices: every row and slice starts on a 16-byte boundary, and each slice
@@ -465,12 +496,12 @@ cudaError_t launch_fused_ring(vce_dtype dt, vce_dtype gdt, const void* logits, i
     }
     if (C > kMaxCluster) return cudaSuccess;   // rows too long for an 8-CTA cluster
     Args args{logits, T,   V,    ld,   labels, ignore_index, red,   grad_output, inv_n,
-              loss_rows, reinterpret_cast<float4*>(row_stats), grad, ld_g, status, slice, wait_ns, tx_extra};
+              loss_rows, reinterpret_cast<float4*>(row_stats), grad, ld_g, status, slice, wait_ns, tx_extra, eps};
     const int sms = device_sm_count();
-    if (dt == VCE_BF16 && gdt == VCE_BF16) return launch_c<uint16_t, uint16_t>(C, args, sms, s, launched);
-    if (dt == VCE_BF16) return launch_c<uint16_t, float>(C, args, sms, s, launched);
-    if (gdt == VCE_BF16) return launch_c<float, uint16_t>(C, args, sms, s, launched);
-    return launch_c<float, float>(C, args, sms, s, launched);
+    if (dt == VCE_BF16 && gdt == VCE_BF16) return launch_cs<uint16_t, uint16_t>(C, args, sms, s, launched);
+    if (dt == VCE_BF16) return launch_cs<uint16_t, float>(C, args, sms, s, launched);
+    if (gdt == VCE_BF16) return launch_cs<float, uint16_t>(C, args, sms, s, launched);
+    return launch_cs<float, float>(C, args, sms, s, launched);
 }
 
 }  // namespace vce
@@ -490,7 +521,7 @@ extern "C" int vce_test_ce_fused_stall(const void* logits, int64_t T, int64_t V,
     bool launched = false;
     // 16 bytes announced beyond each copy: no stage ever completes
     if (launch_fused_ring(VCE_BF16, VCE_BF16, logits, T, V, V, labels, -100, VCE_RED_SUM, grad_output, nullptr,
-                          loss_rows, row_stats, grad_logits, V, status, s, &launched, wait_ns, 16) != cudaSuccess)
+                          loss_rows, row_stats, grad_logits, V, status, s, &launched, 0.f, wait_ns, 16) != cudaSuccess)
         return VCE_ERR_CUDA;
     return launched ? VCE_OK : VCE_ERR_ARG;
 }

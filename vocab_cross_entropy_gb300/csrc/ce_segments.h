@@ -49,14 +49,15 @@ cudaError_t launch_ce_bwd(vce_dtype dt, vce_dtype gdt, int nt, const SegTable& t
 // One-pass forward+backward with each row held in shared memory between its two passes
 // (ce_ring.cu).  Sets *launched when it enqueued the kernel; leaves it false, enqueuing
 // nothing, when the shape or layout does not fit (rows or leading dimensions not multiples of
-// 8 elements, pointers not 16-byte aligned, rows too long for an 8-CTA cluster).  wait_ns
+// 8 elements, pointers not 16-byte aligned, rows too long for an 8-CTA cluster).  eps: label
+// smoothing (0: none).  wait_ns
 // bounds every wait of the kernel; tx_extra > 0 (tests only) announces that many bytes more
 // per stage than each copy delivers, so no stage completes and the waits give up.
 cudaError_t launch_fused_ring(vce_dtype dt, vce_dtype gdt, const void* logits, int64_t T, int64_t V, int64_t ld,
                               const int64_t* labels, int64_t ignore_index, int red, const float* grad_output,
                               const float* inv_n, float* loss_rows, float* row_stats, void* grad, int64_t ld_g,
-                              int32_t* status, cudaStream_t s, bool* launched, uint64_t wait_ns = 2000000000ull,
-                              uint32_t tx_extra = 0);
+                              int32_t* status, cudaStream_t s, bool* launched, float eps = 0.f,
+                              uint64_t wait_ns = 2000000000ull, uint32_t tx_extra = 0);
 
 // CE forward with each row streamed through a shared-memory stage ring (ce_fwd_ring.cu); eps:
 // label smoothing (0: none).  Sets *launched when it enqueued the kernel; leaves it false,

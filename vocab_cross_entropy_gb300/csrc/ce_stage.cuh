@@ -88,11 +88,13 @@ __device__ __forceinline__ void fwd_stage_any(const uint4* buf, int nvec, int re
     }
 }
 
-// Gradient of one held stage: coef * 2^(z log2 e - bias) for every column, then the thread
-// holding the target overwrites that entry with gt (its own later store to the same address).
+// Gradient of one held stage: coef * 2^(z log2 e - bias) - shift for every column (shift =
+// c eps / V under label smoothing, 0 otherwise: a zero addend rounds exactly as the product),
+// then the thread holding the target overwrites that entry with gt (its own later store to
+// the same address).
 template <typename S, typename O, int NT, int U, bool kFull>
 __device__ __forceinline__ void bwd_stage(const uint4* buf, int nvec, O* gcol, int rel0, int tid, float coef,
-                                          float bias, float gt) {
+                                          float bias, float gt, float shift) {
     constexpr int G = Elt<S>::kGroup;
     uint4 r[U];
 #pragma unroll
@@ -107,7 +109,7 @@ __device__ __forceinline__ void bwd_stage(const uint4* buf, int nvec, O* gcol, i
             float v[G];
             Elt<S>::unpack(r[u], v);
 #pragma unroll
-            for (int k = 0; k < G; ++k) v[k] = coef * ex2(fmaf(v[k], kLog2e, -bias));
+            for (int k = 0; k < G; ++k) v[k] = fmaf(coef, ex2(fmaf(v[k], kLog2e, -bias)), -shift);
             GroupStore<O, G>::run(gcol + vi * G, v);
         }
     }
