@@ -255,6 +255,22 @@ int ce_merge_chunks(int k, const void* const* chunk_logits, const int64_t* chunk
                     float* chunk_stats_ws, int32_t* status, vce_stream_t s);
 
 /*
+ * ce_merge_chunks_ls -- ce_merge_chunks with label smoothing (the targets and numerics of
+ * ce_forward_ls / ce_backward_ls).  Step 1 also writes each (chunk, row)'s sum of logits to
+ * chunk_sums_ws [k][T] fp32 (4-byte aligned scratch; required when label_smoothing > 0, may
+ * be NULL otherwise); step 2 adds a row's chunk sums in chunk order.  label_smoothing outside
+ * [0, 1) (or NaN) returns VCE_ERR_ARG; 0 is exactly ce_merge_chunks.  Other arguments as
+ * ce_merge_chunks.
+ */
+int ce_merge_chunks_ls(int k, const void* const* chunk_logits, const int64_t* chunk_width,
+                       const int64_t* chunk_ld, vce_dtype dt, int64_t T,
+                       const int64_t* labels, int64_t ignore_index, float label_smoothing,
+                       vce_reduction red, float* loss_rows, float* loss_out, float* row_stats,
+                       const float* grad_output, void* const* chunk_grads,
+                       const int64_t* chunk_grad_ld, vce_dtype grad_dt,
+                       float* chunk_stats_ws, float* chunk_sums_ws, int32_t* status, vce_stream_t s);
+
+/*
  * ce_merge_chunks_noalloc -- ce_merge_chunks for callers that cannot allocate device memory.
  * None of the pages has a counterpart: this entry point exists for callers that have no
  * way to provide the per-call chunk_stats_ws scratch, such as a host program driving the

@@ -153,3 +153,35 @@ def test_one_pass_smoothing_pages_shape_sampled(vce):
     ref = O.ce_smoothed(O.widen(storage[rr], "bf16"), p.labels[rr], eps, "sum", grad_output=1.0 / N)
     G.check_loss_rows(rows.cpu().numpy()[rr], ref["loss_rows"], ref["valid"])
     grade_smoothed_grad(grad[torch.from_numpy(rr).cuda()], ref, ref["c"], eps, p.V, p.labels[rr])
+
+
+# ---- the chunked call (ce_merge_chunks_ls) ----------------------------------------------------
+
+@pytest.mark.parametrize("widths", [[1000, 2001], [64] * 8, [7, 993, 1]])
+@pytest.mark.parametrize("eps,dtype,reduction", [(0.1, "bf16", "mean"), (0.5, "f32", "none")])
+def test_chunked_smoothing_parity(vce, widths, eps, dtype, reduction):
+    V = sum(widths)
+    p = gen.custom(48, V, dtype, seed=75 + V, std=2.0, n_margin=5, margin=(17.0, 50.0), n_ignore=3)
+    storage = p.full()
+    offs = np.cumsum([0] + list(widths[:-1]))
+    chunks = [to_device(np.ascontiguousarray(storage[:, o:o + w]), dtype) for o, w in zip(offs, widths)]
+    labels = torch.from_numpy(p.labels).cuda()
+    go_np = np.linspace(0.5, 2.0, p.T) if reduction == "none" else np.array([0.75])
+    go = torch.from_numpy(go_np.astype(np.float32)).cuda()
+    out, rows, stats, grads, cstats, status = vce.ce_merge_chunks(chunks, labels, reduction=reduction,
+                                                                  grad_output=go, label_smoothing=eps)
+    torch.cuda.synchronize()
+    assert vce.vce_get_status(status) == 0
+    ref = O.ce_smoothed(O.widen(storage, dtype), p.labels, eps, reduction, go_np if reduction == "none" else 0.75)
+    G.check_loss_rows(rows.cpu().numpy(), ref["loss_rows"], ref["valid"])
+    if reduction != "none":
+        G.check_reduced(out.item(), ref["loss_out"])
+    grade_smoothed_grad(torch.cat(grads, dim=1), ref, ref["c"], eps, p.V, p.labels)
+
+
+def test_chunked_smoothing_rejects_bad_eps(vce):
+    chunks = [torch.zeros(2, 4, device="cuda"), torch.zeros(2, 4, device="cuda")]
+    lab = torch.zeros(2, dtype=torch.int64, device="cuda")
+    for bad in (-0.1, 1.0, float("nan")):
+        with pytest.raises(vce.VceError):
+            vce.ce_merge_chunks(chunks, lab, label_smoothing=bad)

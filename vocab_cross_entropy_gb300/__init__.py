@@ -14,7 +14,7 @@ import os
 import torch
 
 __all__ = ["VceError", "lib", "library_path", "ce_forward", "ce_backward", "ce_forward_ls", "ce_backward_ls",
-           "ce_forward_backward", "ce_forward_backward_ls", "ce_merge_chunks",
+           "ce_forward_backward", "ce_forward_backward_ls", "ce_merge_chunks", "ce_merge_chunks_ls",
            "ce_merge_chunks_noalloc",
            "linear_ce_workspace_bytes", "linear_ce_fwd_bwd", "vce_get_status", "vce_status_string",
            "vce_abi_version", "cross_entropy", "IGNORE_INDEX", "F32", "BF16", "RED"]
@@ -55,6 +55,8 @@ def _load():
     L.ce_forward_ls.argtypes = [p, i32, i64, i64, i64, p, i64, f32, i32, p, p, p, p, p]
     L.ce_backward_ls.argtypes = [p, i32, i64, i64, i64, p, i64, f32, i32, p, p, p, i32, i64, p]
     L.ce_merge_chunks.argtypes = [i32, p, p, p, i32, i64, p, i64, i32, p, p, p, p, p, p, i32, p, p, p]
+    L.ce_merge_chunks_ls.argtypes = [i32, p, p, p, i32, i64, p, i64, ctypes.c_float, i32, p, p, p, p, p, p, i32, p, p,
+                                     p, p]
     L.ce_merge_chunks_noalloc.argtypes = [i32, p, p, p, i32, i64, p, i64, i32, p, p, p, p, p, p, i32, p, p]
     if hasattr(L, "linear_ce_fwd_bwd"):
         L.linear_ce_workspace_bytes.argtypes = [i64, i64, i64]
@@ -67,7 +69,7 @@ def _load():
         L.vce_test_ce_fused_stall.argtypes = [p, i64, i64, p, p, p, p, p, ctypes.c_uint64, p, p]
         L.vce_test_ce_fused_stall.restype = i32
     for name in ("ce_forward", "ce_backward", "ce_forward_ls", "ce_backward_ls", "ce_forward_backward",
-                 "ce_forward_backward_ls",
+                 "ce_forward_backward_ls", "ce_merge_chunks_ls",
                  "ce_merge_chunks", "ce_merge_chunks_noalloc",
                  "linear_ce_fwd_bwd",
                  "vce_get_status"):
@@ -238,8 +240,8 @@ def ce_forward_backward_ls(logits, labels, label_smoothing, ignore_index=IGNORE_
 
 def ce_merge_chunks(chunks, labels, ignore_index=IGNORE_INDEX, reduction="mean", *, grad_output=None,
                     chunk_grads=None, grad_dtype=None, want_grad=True, loss_rows=None, loss_out=None,
-                    row_stats=None, chunk_stats=None, status=None, stream=None):
-    """CE over column chunks (list of [T, w_c] tensors).
+                    row_stats=None, chunk_stats=None, status=None, stream=None, label_smoothing=0.0):
+    """CE over column chunks (list of [T, w_c] tensors); label_smoothing > 0 calls ce_merge_chunks_ls.
 
     Returns (loss_out, loss_rows, row_stats, chunk_grads or None, chunk_stats [k, T, 4], status).
     """
@@ -267,10 +269,17 @@ def ce_merge_chunks(chunks, labels, ignore_index=IGNORE_INDEX, reduction="mean",
     g_ptrs = P(*[g.data_ptr() for g in chunk_grads]) if want_grad else None
     g_lds = I(*[_ld(g) for g in chunk_grads]) if want_grad else None
     gdt = _dtype(chunk_grads[0]) if want_grad else F32
-    _check("ce_merge_chunks", _get().ce_merge_chunks(
-        k, in_ptrs, widths, lds, dt, T, _ptr(labels), int(ignore_index), RED[reduction], _ptr(loss_rows),
-        _ptr(loss_out), _ptr(row_stats), _ptr(grad_output), g_ptrs, g_lds, gdt, _ptr(chunk_stats),
-        _ptr(status), _stream(stream)))
+    if label_smoothing:
+        chunk_sums = torch.empty(k, T, dtype=torch.float32, device=dev)
+        _check("ce_merge_chunks_ls", _get().ce_merge_chunks_ls(
+            k, in_ptrs, widths, lds, dt, T, _ptr(labels), int(ignore_index), float(label_smoothing), RED[reduction],
+            _ptr(loss_rows), _ptr(loss_out), _ptr(row_stats), _ptr(grad_output), g_ptrs, g_lds, gdt,
+            _ptr(chunk_stats), _ptr(chunk_sums), _ptr(status), _stream(stream)))
+    else:
+        _check("ce_merge_chunks", _get().ce_merge_chunks(
+            k, in_ptrs, widths, lds, dt, T, _ptr(labels), int(ignore_index), RED[reduction], _ptr(loss_rows),
+            _ptr(loss_out), _ptr(row_stats), _ptr(grad_output), g_ptrs, g_lds, gdt, _ptr(chunk_stats),
+            _ptr(status), _stream(stream)))
     return loss_out, loss_rows, row_stats, (chunk_grads if want_grad else None), chunk_stats, status
 
 

@@ -141,11 +141,13 @@ __global__ void __launch_bounds__(NT) k_ce_reduce(const float* __restrict__ loss
 // and reduces with shuffles only.  The maximum is exact (ms_push), as the statistics report it.
 constexpr int kChunkThreads = 512;
 
-template <typename S>
+// kSumZ (label smoothing): also each item's sum of logits into chunk_sums [k][T].
+template <typename S, bool kSumZ>
 __global__ void __launch_bounds__(kChunkThreads, 2) k_ce_chunk_fwd(const __grid_constant__ SegTable tab,
                                                                    const int64_t* __restrict__ labels,
                                                                    int64_t ignore_index,
-                                                                   float4* __restrict__ chunk_stats) {
+                                                                   float4* __restrict__ chunk_stats,
+                                                                   float* __restrict__ chunk_sums) {
     const int lane = threadIdx.x & 31;
     const int64_t items = tab.T * tab.k;
     const int64_t warps = (int64_t)gridDim.x * (kChunkThreads / 32);
@@ -158,9 +160,15 @@ __global__ void __launch_bounds__(kChunkThreads, 2) k_ce_chunk_fwd(const __grid_
         const bool owner = (tl >= 0 && tl < w);
         float m = -kInf, s = 0.f, mb = 0.f, zt = 0.f;
         float zt_found = kInf;   // stays +inf except in the lane that meets the target
-        fwd_segment<S, 32, false>(reinterpret_cast<const S*>(tab.in[c]) + row * tab.ld_in[c], w, owner ? tl : -1, m,
-                                  s, mb, &zt_found, lane);
+        float sz = 0.f;
+        fwd_segment<S, 32, false, kLoadStream, kSumZ>(reinterpret_cast<const S*>(tab.in[c]) + row * tab.ld_in[c], w,
+                                                      owner ? tl : -1, m, s, mb, &zt_found, lane, &sz);
         ms_warp_reduce(m, s);
+        if (kSumZ) {
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) sz += __shfl_xor_sync(0xFFFFFFFFu, sz, off);
+            if (lane == 0) chunk_sums[(int64_t)c * tab.T + row] = sz;
+        }
         const unsigned hit = __ballot_sync(0xFFFFFFFFu, zt_found != kInf);
         if (hit) zt = __shfl_sync(0xFFFFFFFFu, zt_found, __ffs(hit) - 1);
         if (lane == 0)
@@ -168,9 +176,12 @@ __global__ void __launch_bounds__(kChunkThreads, 2) k_ce_chunk_fwd(const __grid_
     }
 }
 
+// chunk_sums != NULL: label smoothing eps; the row's sum of logits is the chunks' sums added in
+// chunk order.
 __global__ void k_ce_merge(const float4* __restrict__ chunk_stats, int k, int64_t T, int64_t V,
                            const int64_t* __restrict__ labels, int64_t ignore_index, float* __restrict__ loss_rows,
-                           float4* __restrict__ row_stats, int32_t* status) {
+                           float4* __restrict__ row_stats, int32_t* status, const float* __restrict__ chunk_sums,
+                           float eps) {
     for (int64_t row = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; row < T; row += (int64_t)gridDim.x * blockDim.x) {
         const int64_t t = labels[row];
         const bool ignored = (t == ignore_index);
@@ -187,7 +198,13 @@ __global__ void k_ce_merge(const float4* __restrict__ chunk_stats, int k, int64_
             if (cs.w != 0.f) zt = cs.z;
         }
         float loss;
-        row_stats[row] = ce_row_finish(M, S, zt, &loss);
+        if (chunk_sums) {
+            float tot = 0.f;
+            for (int c = 0; c < k; ++c) tot += chunk_sums[(int64_t)c * T + row];
+            row_stats[row] = ce_row_finish_smoothed(M, S, zt, tot, V, eps, &loss);
+        } else {
+            row_stats[row] = ce_row_finish(M, S, zt, &loss);
+        }
         loss_rows[row] = loss;
     }
 }
@@ -205,11 +222,12 @@ cudaError_t launch_fwd(const void* logits, int64_t T, int64_t V, int64_t ld, con
 }
 
 template <typename S>
-cudaError_t launch_chunk_fwd(const SegTable& tab, const int64_t* labels, int64_t ig, float* ws, cudaStream_t s) {
-    auto kern = k_ce_chunk_fwd<S>;
+cudaError_t launch_chunk_fwd(const SegTable& tab, const int64_t* labels, int64_t ig, float* ws, float* sums,
+                             cudaStream_t s) {
+    auto kern = sums ? k_ce_chunk_fwd<S, true> : k_ce_chunk_fwd<S, false>;
     const int64_t blocks_needed = (tab.T * tab.k + kChunkThreads / 32 - 1) / (kChunkThreads / 32);
     kern<<<grid_for(kern, kChunkThreads, blocks_needed), kChunkThreads, 0, s>>>(tab, labels, ig,
-                                                                               reinterpret_cast<float4*>(ws));
+                                                                               reinterpret_cast<float4*>(ws), sums);
     return cudaGetLastError();
 }
 
@@ -244,7 +262,7 @@ cudaError_t launch_stats_merge(const float* part, int k, int64_t T, int64_t V, c
     const int mt = 256;
     const int mg = (int)std::max<int64_t>(1, std::min<int64_t>((T + mt - 1) / mt, (int64_t)device_sm_count() * 8));
     k_ce_merge<<<mg, mt, 0, s>>>(reinterpret_cast<const float4*>(part), k, T, V, labels, ignore_index, loss_rows,
-                                 reinterpret_cast<float4*>(row_stats), status);
+                                 reinterpret_cast<float4*>(row_stats), status, nullptr, 0.f);
     return cudaGetLastError();
 }
 
@@ -303,14 +321,16 @@ extern "C" int ce_forward(const void* logits, vce_dtype dt, int64_t T, int64_t V
     return ce_forward_ls(logits, dt, T, V, ld, labels, ignore_index, 0.f, red, loss_rows, loss_out, row_stats, status, s);
 }
 
-extern "C" int ce_merge_chunks(int k, const void* const* chunk_logits, const int64_t* chunk_width,
-                               const int64_t* chunk_ld, vce_dtype dt, int64_t T, const int64_t* labels,
-                               int64_t ignore_index, vce_reduction red, float* loss_rows, float* loss_out,
-                               float* row_stats, const float* grad_output, void* const* chunk_grads,
-                               const int64_t* chunk_grad_ld, vce_dtype grad_dt, float* chunk_stats_ws,
-                               int32_t* status, vce_stream_t s) {
+extern "C" int ce_merge_chunks_ls(int k, const void* const* chunk_logits, const int64_t* chunk_width,
+                                  const int64_t* chunk_ld, vce_dtype dt, int64_t T, const int64_t* labels,
+                                  int64_t ignore_index, float label_smoothing, vce_reduction red, float* loss_rows,
+                                  float* loss_out, float* row_stats, const float* grad_output,
+                                  void* const* chunk_grads, const int64_t* chunk_grad_ld, vce_dtype grad_dt,
+                                  float* chunk_stats_ws, float* chunk_sums_ws, int32_t* status, vce_stream_t s) {
     int rc = check_common(dt, red, T);
     if (rc) return rc;
+    if (!(label_smoothing >= 0.f && label_smoothing < 1.f)) return VCE_ERR_ARG;
+    const bool smooth = label_smoothing > 0.f;
     if (k < 1 || k > VCE_MAX_CHUNKS) return VCE_ERR_ARG;
     if (!chunk_logits || !chunk_width || !chunk_ld || !status) return VCE_ERR_NULL;
     if (red != VCE_RED_NONE && !loss_out) return VCE_ERR_NULL;
@@ -344,20 +364,23 @@ extern "C" int ce_merge_chunks(int k, const void* const* chunk_logits, const int
     if (T > 0) {
         if (!labels || !loss_rows || !row_stats || !chunk_stats_ws || (chunk_grads && !grad_output))
             return VCE_ERR_NULL;
-        if (!aligned(labels, 8) || !aligned(loss_rows, 4) || !aligned(row_stats, 16) || !aligned(chunk_stats_ws, 16))
+        if (smooth && !chunk_sums_ws) return VCE_ERR_NULL;
+        if (!aligned(labels, 8) || !aligned(loss_rows, 4) || !aligned(row_stats, 16) || !aligned(chunk_stats_ws, 16) ||
+            (smooth && !aligned(chunk_sums_ws, 4)))
             return VCE_ERR_ALIGN;
         if (!fits_bytes(T, (int64_t)k * VCE_CHUNK_STATS, 4)) return VCE_ERR_SHAPE;
     }
     if ((rc = require_sm100())) return rc;
     if (cudaMemsetAsync(status, 0, sizeof(int32_t), s) != cudaSuccess) return VCE_ERR_CUDA;
     if (T > 0) {
-        cudaError_t e = dt == VCE_BF16 ? launch_chunk_fwd<uint16_t>(tab, labels, ignore_index, chunk_stats_ws, s)
-                                       : launch_chunk_fwd<float>(tab, labels, ignore_index, chunk_stats_ws, s);
+        float* sums = smooth ? chunk_sums_ws : nullptr;
+        cudaError_t e = dt == VCE_BF16 ? launch_chunk_fwd<uint16_t>(tab, labels, ignore_index, chunk_stats_ws, sums, s)
+                                       : launch_chunk_fwd<float>(tab, labels, ignore_index, chunk_stats_ws, sums, s);
         if (e != cudaSuccess) return VCE_ERR_CUDA;
         const int mt = 256;
         const int mg = (int)std::min<int64_t>((T + mt - 1) / mt, (int64_t)device_sm_count() * 8);
         k_ce_merge<<<mg, mt, 0, s>>>(reinterpret_cast<const float4*>(chunk_stats_ws), k, T, V, labels, ignore_index,
-                                     loss_rows, reinterpret_cast<float4*>(row_stats), status);
+                                     loss_rows, reinterpret_cast<float4*>(row_stats), status, sums, label_smoothing);
         if (cudaGetLastError() != cudaSuccess) return VCE_ERR_CUDA;
     }
     if (red != VCE_RED_NONE &&
@@ -365,8 +388,20 @@ extern "C" int ce_merge_chunks(int k, const void* const* chunk_logits, const int
         return VCE_ERR_CUDA;
     if (chunk_grads && T > 0) {
         const int nt = pick_threads(max_w * (int64_t)es);
-        if (launch_ce_bwd(dt, grad_dt, nt, tab, labels, row_stats, grad_output, red == VCE_RED_NONE, s) != cudaSuccess)
+        if (launch_ce_bwd(dt, grad_dt, nt, tab, labels, row_stats, grad_output, red == VCE_RED_NONE, s,
+                          label_smoothing / (float)V) != cudaSuccess)
             return VCE_ERR_CUDA;
     }
     return VCE_OK;
+}
+
+extern "C" int ce_merge_chunks(int k, const void* const* chunk_logits, const int64_t* chunk_width,
+                               const int64_t* chunk_ld, vce_dtype dt, int64_t T, const int64_t* labels,
+                               int64_t ignore_index, vce_reduction red, float* loss_rows, float* loss_out,
+                               float* row_stats, const float* grad_output, void* const* chunk_grads,
+                               const int64_t* chunk_grad_ld, vce_dtype grad_dt, float* chunk_stats_ws,
+                               int32_t* status, vce_stream_t s) {
+    return ce_merge_chunks_ls(k, chunk_logits, chunk_width, chunk_ld, dt, T, labels, ignore_index, 0.f, red,
+                              loss_rows, loss_out, row_stats, grad_output, chunk_grads, chunk_grad_ld, grad_dt,
+                              chunk_stats_ws, nullptr, status, s);
 }
