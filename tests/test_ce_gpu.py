@@ -399,3 +399,23 @@ def test_forward_ring_non_finite_and_bad_labels(vce):
         assert lr[1] == 0 and lr[2] == np.inf and lr[3] == 0 and np.isnan(lr[5])
         for r in (0, 4):
             assert abs(lr[r] - ref["loss_rows"][r]) <= 1e-4 * ref["loss_rows"][r]
+
+
+@pytest.mark.parametrize("dtype,gdt", [("bf16", torch.float32), ("f32", torch.bfloat16), ("bf16", torch.bfloat16)])
+def test_backward_ring_padded_gradient(vce, dtype, gdt):
+    """ce_backward on the stage ring into a wider gradient buffer (ld_grad = V + 8): every entry
+    of the view is written, the padding is not; weight-0 rows come out +0.0."""
+    p = gen.custom(70, 5000, dtype, seed=31, std=2.0, n_margin=7, margin=(17.0, 50.0), n_ignore=6)
+    storage = p.full()
+    logits = to_device(storage, dtype)
+    labels = torch.from_numpy(p.labels).cuda()
+    loss_out, loss_rows, stats, status = vce.ce_forward(logits, labels)
+    gbuf = torch.full((p.T, 5008), 7.0, dtype=gdt, device="cuda")
+    vce.ce_backward(logits, labels, stats, torch.full((1,), 0.5, device="cuda"), grad_logits=gbuf[:, :5000])
+    torch.cuda.synchronize()
+    ref = O.ce(O.widen(storage, dtype), p.labels, "mean", 0.5)
+    grade_grad(gbuf[:, :5000], ref["grad"], p.margin_rows, p.labels)
+    assert torch.all(gbuf[:, 5000:] == 7.0)
+    ign = torch.from_numpy(p.labels == p.ignore_index).cuda()
+    g = gbuf[:, :5000][ign].float()
+    assert torch.all(g == 0) and not torch.any(torch.signbit(g))
