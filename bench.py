@@ -214,7 +214,7 @@ class CEWorkload:
         self.grad = torch.empty((T, V), dtype=tdt, device=device)
         self.loss_host = torch.empty(T if reduction == "none" else 1, dtype=torch.float32, pin_memory=True)
         self.n_valid = int(np.sum(problem.labels != problem.ignore_index))
-        self.launches_per_step = 2 if reduction == "none" else 3   # k_ce_fwd, (k_ce_reduce,) k_ce_bwd
+        self.launches_per_step = 2 if reduction == "none" else 3   # forward kernel, (k_ce_reduce,) backward kernel
 
     def fwd(self, stream):
         if self.eps:
@@ -282,6 +282,15 @@ class CEWorkload:
                 "T": p.T, "V": p.V, "logits": p.dtype, "grad": p.dtype, "math": "f32", "reduction": self.red,
                 "label_smoothing": self.eps,
                 "l2": "no flush: inputs (%.2f GB logits) larger than the 129 MB L2" % (p.T * p.V * self.es / 1e9)}
+
+
+def backward_kernel(V):
+    """The kernel ce_backward runs for contiguous, 16-byte aligned [T, V] logits and gradient."""
+    return "k_ce_bwd_ring" if V % 8 == 0 else "k_ce_bwd"
+
+
+BWD_RING_FILES = ["vocab_cross_entropy_gb300/csrc/ce_bwd_ring.cu", "vocab_cross_entropy_gb300/csrc/ce_stage.cuh",
+                  "vocab_cross_entropy_gb300/csrc/vce_device.cuh", "vocab_cross_entropy_gb300/csrc/vce_async.cuh"]
 
 
 def forward_kernel(V):
@@ -586,11 +595,14 @@ def run_ours(args, rank, local_rank, world):
                 "algorithmic_bytes_per_launch": call_bytes, "traffic": None}
     else:
         achieved = bwd_bytes / (bwd_ms / 1e3) / 1e9
-        roof = {"bound": "hbm", "kernel": "k_ce_bwd", "achieved": round(achieved, 1),
+        bkern = backward_kernel(w.p.V)
+        traffic = None
+        if captured_shape(w):
+            traffic = (profiled_traffic("k_ce_bwd_ring_pages", BWD_RING_FILES) if bkern == "k_ce_bwd_ring"
+                       else profiled_traffic("k_ce_bwd_pages", CEWorkload.KERNEL_FILES))
+        roof = {"bound": "hbm", "kernel": bkern, "achieved": round(achieved, 1),
                 "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
-                "peak_source": peaks["source"], "algorithmic_bytes_per_launch": bwd_bytes,
-                "traffic": (profiled_traffic("k_ce_bwd_pages", CEWorkload.KERNEL_FILES)
-                            if captured_shape(w) else None)}
+                "peak_source": peaks["source"], "algorithmic_bytes_per_launch": bwd_bytes, "traffic": traffic}
     out = {
         "metric": "CE fwd+bwd tokens/s at T=16384,V=128256 bf16; HBM GB/s vs ~8 TB/s",
         "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
