@@ -113,8 +113,8 @@ extern "C" int ce_backward_ls(const void* logits, vce_dtype dt, int64_t T, int64
     // with loads from global memory.
     const float eps_over_v = label_smoothing / (float)V;
     bool launched = false;
-    cudaError_t e = launch_bwd_ring(dt, grad_dt, logits, T, V, ld, labels, row_stats, grad_output,
-                                    red == VCE_RED_NONE, grad_logits, ld_grad, eps_over_v, s, &launched);
+    cudaError_t e = launch_bwd_ring(dt, grad_dt, tab, labels, row_stats, grad_output, red == VCE_RED_NONE, eps_over_v,
+                                    s, &launched);
     if (e == cudaSuccess && !launched) {
         const int nt = pick_threads(V * (int64_t)es);
         e = launch_ce_bwd(dt, grad_dt, nt, tab, labels, row_stats, grad_output, red == VCE_RED_NONE, s, eps_over_v);

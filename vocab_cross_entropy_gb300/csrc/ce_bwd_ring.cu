@@ -1,20 +1,23 @@
-// CE backward (ce_backward) for rows that suit bulk copies: each row streams through a
-// shared-memory stage ring and its gradient is written from there.
+// CE backward (ce_backward, and the gradient step of ce_merge_chunks) for rows that suit bulk
+// copies: each row, or each chunk of a row, streams through a shared-memory stage ring and its
+// gradient is written from there.
 //
 // Method: torchtitan PR #5723 "[loss] fix softmax collapse with improved ce perf" (Numerics:
 // the gradient rebuilt from the logits and the row statistics, the p_t = 1/4 branch) — the same
 // per-element arithmetic as k_ce_bwd (grad = coef * 2^(z log2 e - bias), the target entry gt).
 //
-// One CTA per SM walks the rows blockIdx.x, blockIdx.x + gridDim.x, ... with three roles:
-//   producer warp   reads the row statistics of 32 rows at a time (one per lane); lane 0
-//                   publishes each valid row's coefficients (coef, bias, target gradient,
-//                   smoothing shift) and target column, and streams the row into a ring of seven
-//                   32 KB stages with bulk asynchronous copies (cp.async.bulk)
+// Items are (row, chunk) pairs of a segment table, row-major over its k chunks (k = 1 for a
+// [T, V] matrix).  One CTA per SM walks the items blockIdx.x, blockIdx.x + gridDim.x, ... with
+// three roles:
+//   producer warp   reads the row statistics of 32 items at a time (one per lane); lane 0
+//                   publishes each weighted item's row, chunk, coefficients (coef, bias, target
+//                   gradient, smoothing shift) and target column, and streams the item into a
+//                   ring of seven 32 KB stages with bulk asynchronous copies (cp.async.bulk)
 //   consumer warps  per stage, a thread's 4 x 16-byte vectors to gradient entries stored with
 //                   16-byte streaming stores (stage::bwd_stage); the stage goes back to the
 //                   producer right away
-//   zero warp       writes +0.0 over the gradient rows of weight 0 (ignored or invalid labels),
-//                   whose logits are not read
+//   zero warp       writes +0.0 over the gradient of items of weight 0 (ignored or invalid
+//                   labels), whose logits are not read
 // Every wait is bounded (2 s).  A wait that gives up sets the CTA's abort flag; every role then
 // keeps its arrivals but skips the work and later waits.  ce_backward has no status word, so
 // the gradient is then undefined without a report.
@@ -43,10 +46,11 @@ constexpr int kVecPerThread = kChunk / 16 / kConsumers;
 constexpr int kInfoSlots = 16;         // > the rows the producer can run ahead (kStages, at one stage a row)
 static_assert(kVecPerThread * kConsumers * 16 == kChunk, "every consumer takes the same whole vectors of a stage");
 
-// A valid row of the CTA's sequence: where its gradient goes and how it is formed.
+// A weighted item of the CTA's sequence: where its gradient goes and how it is formed.
 struct RowInfo {
     int64_t row;
-    int tl;                            // target column
+    int tl;                            // target column within the chunk (-1: not in it)
+    int c;                             // chunk
     float coef, bias, gt, shift;
 };
 
@@ -59,9 +63,6 @@ struct alignas(16) Ctl {
 constexpr int kSmemBytes = kStages * kChunk + (int)sizeof(Ctl);
 
 struct Args {
-    const void* logits;
-    void* grad;
-    int64_t T, V, ld, ld_g;
     const int64_t* labels;
     const float4* row_stats;           // (L', 1 - p_t, target coefficient, weight); weight 0: no gradient
     const float* grad_output;
@@ -71,33 +72,34 @@ struct Args {
 };
 
 template <typename S, typename O, bool kShift>
-__global__ void __launch_bounds__(kThreads, 1) k_ce_bwd_ring(const __grid_constant__ Args a) {
+__global__ void __launch_bounds__(kThreads, 1) k_ce_bwd_ring(const __grid_constant__ Args a,
+                                                             const __grid_constant__ SegTable tab) {
     constexpr int G = Elt<S>::kGroup;
+    constexpr int64_t es = sizeof(S);
     extern __shared__ __align__(128) uint8_t smem[];
     Ctl& ctl = *reinterpret_cast<Ctl*>(smem + kStages * kChunk);
     volatile int* abort_flag = &ctl.abort;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t stride = gridDim.x;
-    const int64_t bytes = a.V * (int64_t)sizeof(S);
-    const int nchunk = (int)((bytes + kChunk - 1) / kChunk);
+    const int64_t stride = gridDim.x, items = tab.T * tab.k;
+    auto stages_of = [&](int c) { return (int)((tab.width[c] * es + kChunk - 1) / kChunk); };
 
     if (threadIdx.x == 0) {
         for (int st = 0; st < kStages; ++st) {
             tc::mbar_init(&ctl.full[st], 1);
             tc::mbar_init(&ctl.empty[st], kConsumerWarps);
         }
-        for (int i = 0; i < kInfoSlots; ++i) ctl.info[i] = RowInfo{-1, -1, 0.f, 0.f, 0.f, 0.f};
+        for (int i = 0; i < kInfoSlots; ++i) ctl.info[i] = RowInfo{-1, -1, 0, 0.f, 0.f, 0.f, 0.f};
         ctl.abort = 0;
         tc::fence_mbar_init();
     }
     __syncthreads();
 
-    // The number of rows of this CTA with a nonzero weight (each warp counts for itself).
+    // The number of items of this CTA with a nonzero weight (each warp counts for itself).
     auto count_valid = [&]() {
         int n = 0;
 #pragma unroll 4
-        for (int64_t row = blockIdx.x + (int64_t)lane * stride; row < a.T; row += 32 * stride)
-            n += a.row_stats[row].w != 0.f;
+        for (int64_t it = blockIdx.x + (int64_t)lane * stride; it < items; it += 32 * stride)
+            n += a.row_stats[it / tab.k].w != 0.f;
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) n += __shfl_xor_sync(0xFFFFFFFFu, n, off);
         return n;
@@ -107,9 +109,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_bwd_ring(const __grid_consta
         // ---------------- producer ----------------
         uint32_t q = 0, e = 0;
         bool stop = false;
-        for (int64_t base = blockIdx.x; base < a.T && !stop; base += 32 * stride) {
+        for (int64_t base = blockIdx.x; base < items && !stop; base += 32 * stride) {
             const int64_t my = base + (int64_t)lane * stride;
-            const float4 st_my = my < a.T ? a.row_stats[my] : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float4 st_my = my < items ? a.row_stats[my / tab.k] : make_float4(0.f, 0.f, 0.f, 0.f);
             uint32_t todo = __ballot_sync(0xFFFFFFFFu, st_my.w != 0.f);
             while (todo && !stop) {
                 const int b = __ffs(todo) - 1;
@@ -117,12 +119,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_bwd_ring(const __grid_consta
                 const float sx = __shfl_sync(0xFFFFFFFFu, st_my.x, b), sy = __shfl_sync(0xFFFFFFFFu, st_my.y, b);
                 const float sz = __shfl_sync(0xFFFFFFFFu, st_my.z, b), sw = __shfl_sync(0xFFFFFFFFu, st_my.w, b);
                 if (lane == 0) {
-                    const int64_t row = base + (int64_t)b * stride;
-                    const float c = a.grad_output[a.go_per_row ? row : 0] * sw;
-                    // the row's coefficients, published with its first stage
-                    ctl.info[e % kInfoSlots] = RowInfo{row, (int)a.labels[row], c * sy,
-                                                       (sx == -kInf) ? 0.f : sx * kLog2e, c * sz, c * a.eps_over_v};
-                    const char* src = static_cast<const char*>(a.logits) + row * a.ld * (int64_t)sizeof(S);
+                    const int64_t it = base + (int64_t)b * stride;
+                    const int64_t row = it / tab.k;
+                    const int c = (int)(it - row * tab.k);
+                    const int64_t t = a.labels[row], off = tab.off[c], w = tab.width[c];
+                    const float cg = a.grad_output[a.go_per_row ? row : 0] * sw;
+                    // the item's coefficients, published with its first stage
+                    ctl.info[e % kInfoSlots] = RowInfo{row, (t >= off && t < off + w) ? (int)(t - off) : -1, c,
+                                                       cg * sy, (sx == -kInf) ? 0.f : sx * kLog2e, cg * sz,
+                                                       cg * a.eps_over_v};
+                    const char* src = static_cast<const char*>(tab.in[c]) + row * tab.ld_in[c] * es;
+                    const int64_t bytes = w * es;
+                    const int nchunk = stages_of(c);
                     for (int j = 0; j < nchunk; ++j) {
                         const int st = (int)(q % kStages);
                         if (!tc::mbar_wait(&ctl.empty[st], ((q / kStages) & 1) ^ 1, abort_flag, nullptr, 0,
@@ -148,34 +156,42 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_bwd_ring(const __grid_consta
         }
         __syncwarp();
     } else if (warp == kZeroWarp) {
-        // ---------------- rows of weight 0: gradient +0.0 by selection ----------------
-        for (int64_t base = blockIdx.x; base < a.T; base += 32 * stride) {
+        // ---------------- items of weight 0: gradient +0.0 by selection ----------------
+        for (int64_t base = blockIdx.x; base < items; base += 32 * stride) {
             const int64_t my = base + (int64_t)lane * stride;
-            uint32_t bad = __ballot_sync(0xFFFFFFFFu, my < a.T && a.row_stats[my].w == 0.f);
+            uint32_t bad = __ballot_sync(0xFFFFFFFFu, my < items && a.row_stats[my / tab.k].w == 0.f);
             while (bad) {
                 const int b = __ffs(bad) - 1;
                 bad &= bad - 1;
-                O* grow = static_cast<O*>(a.grad) + (base + (int64_t)b * stride) * a.ld_g;
+                const int64_t it = base + (int64_t)b * stride;
+                const int64_t row = it / tab.k;
+                const int c = (int)(it - row * tab.k);
+                O* grow = static_cast<O*>(tab.out[c]) + row * tab.ld_out[c];
                 const float zero[G] = {};
-                for (int64_t vi = lane; vi < a.V / G; vi += 32) GroupStore<O, G>::run(grow + vi * G, zero);
+                for (int64_t vi = lane; vi < tab.width[c] / G; vi += 32) GroupStore<O, G>::run(grow + vi * G, zero);
             }
         }
     } else {
         // ---------------- consumers ----------------
         const int tid = threadIdx.x;
         const int nv = count_valid();
-        uint32_t q = 0;
-        for (int e = 0; e < nv; ++e, q += nchunk) {
-            RowInfo ri{-1, -1, 0.f, 0.f, 0.f, 0.f};
+        uint32_t q = 0;   // ring chunk of the current item's first stage
+        for (int e = 0; e < nv; ++e) {
+            RowInfo ri{-1, -1, 0, 0.f, 0.f, 0.f, 0.f};
             O* grow = nullptr;
+            int nchunk = 1;
+            int64_t bytes = 0;
             for (int j = 0; j < nchunk; ++j) {
                 const uint32_t p = q + j;
                 const int st = (int)(p % kStages);
                 const bool ok = tc::mbar_wait(&ctl.full[st], (p / kStages) & 1, abort_flag, nullptr, 0, a.wait_ns);
-                if (j == 0) {
+                if (j == 0) {   // the item is known once its first stage has landed
                     ri = ctl.info[e % kInfoSlots];
-                    const bool in_range = ri.row >= 0 && ri.row < a.T;   // false only after an abort
-                    grow = in_range ? static_cast<O*>(a.grad) + ri.row * a.ld_g : nullptr;
+                    const bool in_range = ri.row >= 0 && ri.row < tab.T && ri.c >= 0 && ri.c < tab.k;   // else: aborted
+                    const int c = in_range ? ri.c : 0;
+                    grow = in_range ? static_cast<O*>(tab.out[c]) + ri.row * tab.ld_out[c] : nullptr;
+                    bytes = tab.width[c] * es;
+                    nchunk = stages_of(c);
                 }
                 if (ok && grow && !*abort_flag) {
                     const uint4* buf = reinterpret_cast<const uint4*>(smem + st * kChunk);
@@ -192,38 +208,42 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_bwd_ring(const __grid_consta
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(&ctl.empty[st]);
             }
+            q += nchunk;
         }
     }
 }
 
 template <typename S, typename O>
-cudaError_t launch(const Args& args, cudaStream_t s) {
+cudaError_t launch(const Args& args, const SegTable& tab, cudaStream_t s) {
     auto kern = args.eps_over_v > 0.f ? k_ce_bwd_ring<S, O, true> : k_ce_bwd_ring<S, O, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
-    const int grid = (int)std::min<int64_t>(device_sm_count(), args.T);
-    kern<<<grid, kThreads, kSmemBytes, s>>>(args);
+    const int grid = (int)std::min<int64_t>(device_sm_count(), tab.T * tab.k);
+    kern<<<grid, kThreads, kSmemBytes, s>>>(args, tab);
     return cudaGetLastError();
 }
 
 }  // namespace bring
 
-cudaError_t launch_bwd_ring(vce_dtype dt, vce_dtype gdt, const void* logits, int64_t T, int64_t V, int64_t ld,
-                            const int64_t* labels, const float* row_stats, const float* grad_output, int go_per_row,
-                            void* grad, int64_t ld_g, float eps_over_v, cudaStream_t s, bool* launched) {
+cudaError_t launch_bwd_ring(vce_dtype dt, vce_dtype gdt, const SegTable& tab, const int64_t* labels,
+                            const float* row_stats, const float* grad_output, int go_per_row, float eps_over_v,
+                            cudaStream_t s, bool* launched) {
     using namespace bring;
     *launched = false;
-    // 16-byte rows: every input and output row starts on a 16-byte boundary and is whole
-    // 16-byte vectors.
-    if (T < 1 || V % 8 || ld % 8 || ld_g % 8 || !aligned(logits, 16) || !aligned(grad, 16) || V > (int64_t)1 << 30)
-        return cudaSuccess;
-    const Args args{logits, grad, T, V, ld, ld_g, labels, reinterpret_cast<const float4*>(row_stats), grad_output,
-                    go_per_row, eps_over_v, tc::kWaitNs};
+    const int64_t es = dt == VCE_BF16 ? 2 : 4, gs = gdt == VCE_BF16 ? 2 : 4;
+    if (tab.T < 1) return cudaSuccess;
+    // every input and output chunk row starts on a 16-byte boundary and is whole 16-byte vectors
+    for (int c = 0; c < tab.k; ++c)
+        if (tab.width[c] % 8 || tab.ld_in[c] % 8 || tab.ld_out[c] % 8 || !aligned(tab.in[c], 16) ||
+            !aligned(tab.out[c], 16) || tab.width[c] > ((int64_t)1 << 30) / std::max(es, gs))
+            return cudaSuccess;
+    const Args args{labels, reinterpret_cast<const float4*>(row_stats), grad_output, go_per_row, eps_over_v,
+                    tc::kWaitNs};
     cudaError_t e;
-    if (dt == VCE_BF16 && gdt == VCE_BF16) e = launch<uint16_t, uint16_t>(args, s);
-    else if (dt == VCE_BF16) e = launch<uint16_t, float>(args, s);
-    else if (gdt == VCE_BF16) e = launch<float, uint16_t>(args, s);
-    else e = launch<float, float>(args, s);
+    if (dt == VCE_BF16 && gdt == VCE_BF16) e = launch<uint16_t, uint16_t>(args, tab, s);
+    else if (dt == VCE_BF16) e = launch<uint16_t, float>(args, tab, s);
+    else if (gdt == VCE_BF16) e = launch<float, uint16_t>(args, tab, s);
+    else e = launch<float, float>(args, tab, s);
     if (e == cudaSuccess) *launched = true;
     return e;
 }

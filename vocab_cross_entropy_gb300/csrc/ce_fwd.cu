@@ -387,10 +387,16 @@ extern "C" int ce_merge_chunks_ls(int k, const void* const* chunk_logits, const 
         launch_reduce(loss_rows, labels, T, V, ignore_index, red, loss_out, row_stats, s) != cudaSuccess)
         return VCE_ERR_CUDA;
     if (chunk_grads && T > 0) {
-        const int nt = pick_threads(max_w * (int64_t)es);
-        if (launch_ce_bwd(dt, grad_dt, nt, tab, labels, row_stats, grad_output, red == VCE_RED_NONE, s,
-                          label_smoothing / (float)V) != cudaSuccess)
-            return VCE_ERR_CUDA;
+        // Chunk rows streamed through shared memory where every chunk's layout allows it.
+        const float eps_over_v = label_smoothing / (float)V;
+        bool launched = false;
+        cudaError_t e = launch_bwd_ring(dt, grad_dt, tab, labels, row_stats, grad_output, red == VCE_RED_NONE,
+                                        eps_over_v, s, &launched);
+        if (e == cudaSuccess && !launched) {
+            const int nt = pick_threads(max_w * (int64_t)es);
+            e = launch_ce_bwd(dt, grad_dt, nt, tab, labels, row_stats, grad_output, red == VCE_RED_NONE, s, eps_over_v);
+        }
+        if (e != cudaSuccess) return VCE_ERR_CUDA;
     }
     return VCE_OK;
 }

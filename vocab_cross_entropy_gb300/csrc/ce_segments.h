@@ -59,13 +59,13 @@ cudaError_t launch_fused_ring(vce_dtype dt, vce_dtype gdt, const void* logits, i
                               int32_t* status, cudaStream_t s, bool* launched, float eps = 0.f,
                               uint64_t wait_ns = 2000000000ull, uint32_t tx_extra = 0);
 
-// CE backward with each row streamed through a shared-memory stage ring (ce_bwd_ring.cu): the
-// same gradient entries as launch_ce_bwd over one [T, V] matrix.  Leaves *launched false,
-// enqueuing nothing, unless the input and output rows are whole 16-byte vectors on 16-byte
-// boundaries.
-cudaError_t launch_bwd_ring(vce_dtype dt, vce_dtype gdt, const void* logits, int64_t T, int64_t V, int64_t ld,
-                            const int64_t* labels, const float* row_stats, const float* grad_output, int go_per_row,
-                            void* grad, int64_t ld_g, float eps_over_v, cudaStream_t s, bool* launched);
+// The gradient of every (chunk, row) segment of `tab` with each segment streamed through a
+// shared-memory stage ring (ce_bwd_ring.cu): the same entries as launch_ce_bwd.  Leaves
+// *launched false, enqueuing nothing, unless every input and output chunk row is whole 16-byte
+// vectors on a 16-byte boundary.
+cudaError_t launch_bwd_ring(vce_dtype dt, vce_dtype gdt, const SegTable& tab, const int64_t* labels,
+                            const float* row_stats, const float* grad_output, int go_per_row, float eps_over_v,
+                            cudaStream_t s, bool* launched);
 
 // CE forward with each row streamed through a shared-memory stage ring (ce_fwd_ring.cu); eps:
 // label smoothing (0: none).  Sets *launched when it enqueued the kernel; leaves it false,
