@@ -589,7 +589,9 @@ def run_ours(args, rank, local_rank, world):
     elif chunked:   # one call launches all four kernels: roofline over the whole call
         call_bytes = w.bytes_fwd() + bwd_bytes + 2 * w.p.T * gen.CHUNKS * 16
         achieved = call_bytes / (ms_step / 1e3) / 1e9
-        roof = {"bound": "hbm", "kernel": "ce_merge_chunks (k_ce_chunk_fwd + k_ce_merge + k_ce_reduce + k_ce_bwd)",
+        ring = all(wd % 8 == 0 for _, wd in gen.chunk_bounds(w.p.V, gen.CHUNKS))
+        roof = {"bound": "hbm", "kernel": "ce_merge_chunks (k_ce_chunk_fwd + k_ce_merge + k_ce_reduce + "
+                                          + ("k_ce_bwd_ring" if ring else "k_ce_bwd") + ")",
                 "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": round(achieved / peaks["hbm_gbs"], 4), "peak_source": peaks["source"],
                 "algorithmic_bytes_per_launch": call_bytes, "traffic": None}
