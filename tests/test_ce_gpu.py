@@ -182,8 +182,9 @@ def test_non_finite_rows(vce):
         np.testing.assert_allclose(g[3:], ref["grad"][3:], rtol=1e-2 if dtype == "bf16" else 1e-5, atol=1e-7)
 
 
-def test_all_rows_ignored(vce):
-    p = gen.custom(8, 100, "bf16", seed=3)
+@pytest.mark.parametrize("V", [100, 104])   # per-block kernels; shared-memory stage rings
+def test_all_rows_ignored(vce, V):
+    p = gen.custom(8, V, "bf16", seed=3)
     labels = np.full(8, -100)
     logits = to_device(p.full(), "bf16")
     loss_out, loss_rows, stats, status, grad = run_ce(vce, logits, labels, "mean")
@@ -191,10 +192,11 @@ def test_all_rows_ignored(vce):
     assert torch.all(loss_rows == 0) and torch.all(grad == 0)
 
 
-def test_invalid_label_sets_status(vce):
-    p = gen.custom(8, 100, "f32", seed=4)
+@pytest.mark.parametrize("V", [100, 104])
+def test_invalid_label_sets_status(vce, V):
+    p = gen.custom(8, V, "f32", seed=4)
     labels = p.labels.copy()
-    labels[3] = 100
+    labels[3] = V
     labels[5] = -7
     logits = to_device(p.full(), "f32")
     loss_out, loss_rows, stats, status, grad = run_ce(vce, logits, labels, "mean")

@@ -399,11 +399,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_fused_ring(const __grid_cons
                     const int col0 = j * (kChunk / (int)sizeof(S));
                     const int rel0 = ri.tl - (col0 + tid * G);
                     if (nvec == kFullVec)
-                        stage::bwd_stage<S, O, kConsumers, kVecPerThread, true, kSmooth>(buf, nvec, grow + col0, rel0,
-                                                                                         tid, cf.x, cf.y, cf.z, cf.w);
+                        stage::bwd_stage<S, O, kConsumers, kVecPerThread, true, kSmooth, true>(
+                            buf, nvec, grow + col0, rel0, tid, cf.x, cf.y, cf.z, cf.w);
                     else
-                        stage::bwd_stage<S, O, kConsumers, kVecPerThread, false, kSmooth>(buf, nvec, grow + col0, rel0,
-                                                                                          tid, cf.x, cf.y, cf.z, cf.w);
+                        stage::bwd_stage<S, O, kConsumers, kVecPerThread, false, kSmooth, true>(
+                            buf, nvec, grow + col0, rel0, tid, cf.x, cf.y, cf.z, cf.w);
                 }
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(&ctl.empty[st]);

@@ -150,6 +150,15 @@ struct GroupStore<float, 8> {      // 2 x 16 B
     static constexpr int kAlign = 16;
 };
 
+// Two fp32 FMAs, (a0, a1) * b + c, in one packed instruction (each lane rounds as fmaf).
+__device__ __forceinline__ void ffma2(float a0, float a1, float b, float c, float& d0, float& d1) {
+    asm("{\n\t.reg .b64 pa, pb, pc, pd;\n\t"
+        "mov.b64 pa, {%2, %3};\n\tmov.b64 pb, {%4, %4};\n\tmov.b64 pc, {%5, %5};\n\t"
+        "fma.rn.f32x2 pd, pa, pb, pc;\n\tmov.b64 {%0, %1}, pd;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b), "f"(c));
+}
+
 // ---- (max, sum-exp) pairs ------------------------------------------------------------------
 //
 // A pair (m, s) stands for the multiset sum  s * e^m = sum_k e^{v_k}, with m one of the v_k
