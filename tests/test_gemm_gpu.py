@@ -18,7 +18,8 @@ def _bf16(rng, shape, std=1.0):
 
 @pytest.mark.parametrize("a_mn", [False, True])
 @pytest.mark.parametrize("b_mn", [False, True])
-@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (256, 512, 320), (136, 264, 72), (8, 8, 8), (384, 768, 1024)])
+@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (256, 512, 320), (136, 264, 72), (8, 8, 8), (384, 768, 1024),
+                                   (2560, 4096, 128)])
 def test_gemm_layouts(vce, a_mn, b_mn, M, N, K):
     rng = np.random.default_rng(M * 7 + N + K + 2 * a_mn + b_mn)
     A, A64 = _bf16(rng, (K, M) if a_mn else (M, K))

@@ -24,6 +24,7 @@
 #include <stdint.h>
 
 #include <algorithm>
+#include <atomic>
 
 #include "tc_gemm.cuh"
 #include "vce.h"
@@ -315,17 +316,76 @@ bool make_map(CUtensorMap* m, const void* base, int64_t inner, int64_t outer, in
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+constexpr int kMaxDevices = 64;
+
+// Clusters of two CTAs that fit on the device at once, queried once per device and kernel
+// (0: none fit, the caller then launches single CTAs).
+template <class K>
+int pair_clusters(K kern) {
+    static std::atomic<int> fit[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+    int clusters = fit[dev].load() - 1;
+    if (clusters < 0) {
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3(2 * (device_sm_count() / 2));
+        cfg.blockDim = dim3(tc::kThreads);
+        cfg.dynamicSmemBytes = tc::SMEM_BYTES;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess) {
+            (void)cudaGetLastError();
+            clusters = 0;
+        }
+        fit[dev].store(clusters + 1);
+    }
+    return clusters;
+}
+
+// Runs one GEMM.  With an even tiles_m the grid runs as 2-CTA clusters that share each B tile
+// (k_tc_gemm's kPair); a K-major B is then read through b_half, the same matrix with boxes of
+// BN/2 rows.  Otherwise, or when no 2-CTA cluster fits, one CTA per SM through b.
 template <class Epi, bool kAmn = false, bool kBmn = false>
-cudaError_t run_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b, const tc::GemmArgs& g,
-                     const typename Epi::Params& ep, cudaStream_t s) {
-    auto kern = tc::k_tc_gemm<Epi, kAmn, kBmn>;
-    static bool attr_set = false;   // per process; the attribute is per function, not per device
+cudaError_t run_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b, const CUtensorMap& b_half,
+                     const tc::GemmArgs& g, const typename Epi::Params& ep, cudaStream_t s) {
+    const int64_t tiles = (int64_t)g.tiles_m * g.tiles_n;
+    if (g.tiles_m % 2 == 0) {
+        auto kern = tc::k_tc_gemm<Epi, kAmn, kBmn, true>;
+        static bool attr_set = false;   // per process; the attribute is per function, not per device
+        if (!attr_set) {
+            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::SMEM_BYTES);
+            if (e != cudaSuccess) return e;
+            attr_set = true;
+        }
+        const int fit = pair_clusters(kern);
+        if (fit > 0) {
+            cudaLaunchConfig_t cfg = {};
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = 2;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.gridDim = dim3((unsigned)(2 * std::min<int64_t>(tiles / 2, fit)));
+            cfg.blockDim = dim3(tc::kThreads);
+            cfg.dynamicSmemBytes = tc::SMEM_BYTES;
+            cfg.stream = s;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            return cudaLaunchKernelEx(&cfg, kern, a0, a1, kBmn ? b : b_half, g, ep);
+        }
+    }
+    auto kern = tc::k_tc_gemm<Epi, kAmn, kBmn, false>;
+    static bool attr_set = false;
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::SMEM_BYTES);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    const int64_t tiles = (int64_t)g.tiles_m * g.tiles_n;
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(tiles, device_sm_count()));
     kern<<<grid, tc::kThreads, tc::SMEM_BYTES, s>>>(a0, a1, b, g, ep);
     return cudaGetLastError();
@@ -403,8 +463,9 @@ extern "C" int linear_ce_fwd_bwd(const void* E, const void* W, int64_t T, int64_
     if (cudaMemsetAsync(status, 0, sizeof(int32_t), s) != cudaSuccess) return VCE_ERR_CUDA;
 
     // K-major maps (box 64 K x rows) and MN-major maps (box 64 MN x 64 K) over row-major matrices
-    CUtensorMap mE, mW, mEmn, mWmn, mGhi, mGlo, mGhi_mn, mGlo_mn;
-    if (!make_map(&mE, E, D, T, D, BM) || !make_map(&mW, W, D, V, D, BN) || !make_map(&mEmn, E, D, T, D, BK) ||
+    CUtensorMap mE, mW, mW2, mEmn, mWmn, mGhi, mGlo, mGhi_mn, mGlo_mn;
+    if (!make_map(&mE, E, D, T, D, BM) || !make_map(&mW, W, D, V, D, BN) || !make_map(&mW2, W, D, V, D, BN / 2) ||
+        !make_map(&mEmn, E, D, T, D, BK) ||
         !make_map(&mWmn, W, D, V, D, BK) || !make_map(&mGhi, ghi, L.Vc, L.T_pad, L.Vc, BM) ||
         !make_map(&mGlo, glo, L.Vc, L.T_pad, L.Vc, BM) || !make_map(&mGhi_mn, ghi, L.Vc, L.T_pad, L.Vc, BK) ||
         !make_map(&mGlo_mn, glo, L.Vc, L.T_pad, L.Vc, BK))
@@ -417,7 +478,7 @@ extern "C" int linear_ce_fwd_bwd(const void* E, const void* W, int64_t T, int64_
     {
         tc::GemmArgs g{tiles_t, (int)L.tiles_v, nkD, nkD, 0, 0, 0, 0, status};
         EpiStats::Params ep{labels, ignore_index, T, V, reinterpret_cast<float4*>(part)};
-        if (run_gemm<EpiStats>(mE, mE, mW, g, ep, s) != cudaSuccess) return VCE_ERR_CUDA;
+        if (run_gemm<EpiStats>(mE, mE, mW, mW2, g, ep, s) != cudaSuccess) return VCE_ERR_CUDA;
         if (launch_stats_merge(part, (int)L.tiles_v, T, V, labels, ignore_index, loss_rows, stats, status, s) !=
             cudaSuccess)
             return VCE_ERR_CUDA;
@@ -436,19 +497,19 @@ extern "C" int linear_ce_fwd_bwd(const void* E, const void* W, int64_t T, int64_
             tc::GemmArgs g{tiles_t, (int)(width_pad / BN), nkD, nkD, 0, 0, (int)off, 0, status};
             EpiGrad::Params ep{labels, T, width, off, reinterpret_cast<const float4*>(stats), grad_output,
                                red == VCE_RED_NONE, ghi, glo, L.Vc};
-            if (run_gemm<EpiGrad>(mE, mE, mW, g, ep, s) != cudaSuccess) return VCE_ERR_CUDA;
+            if (run_gemm<EpiGrad>(mE, mE, mW, mW2, g, ep, s) != cudaSuccess) return VCE_ERR_CUDA;
         }
         {   // dW[off : off + width] = G^T E: A = G (MN-major), B = E (MN-major), K = 2 T_pad (hi then lo)
             const int nkT = (int)(L.T_pad / BK);
             tc::GemmArgs g{(int)(width_pad / BM), (int)cdiv(D, BN), 2 * nkT, nkT, 0, 0, 0, 1, status};
             EpiStore::Params ep{dW, D, width, D, off, grad_dt == VCE_BF16};
-            if (run_gemm<EpiStore, true, true>(mGhi_mn, mGlo_mn, mEmn, g, ep, s) != cudaSuccess) return VCE_ERR_CUDA;
+            if (run_gemm<EpiStore, true, true>(mGhi_mn, mGlo_mn, mEmn, mEmn, g, ep, s) != cudaSuccess) return VCE_ERR_CUDA;
         }
         {   // dE += G W[off : off + width]: A = G (K-major), B = W rows (MN-major), K = 2 width (hi then lo)
             const int nkc = (int)cdiv(width, BK);
             tc::GemmArgs g{tiles_t, (int)cdiv(D, BN), 2 * nkc, nkc, (int)off, 0, 0, 1, status};
             EpiKahan::Params ep{dsum, dcomp, T, D, ci == 0, ci == nchunks - 1, dE, grad_dt == VCE_BF16};
-            if (run_gemm<EpiKahan, false, true>(mGhi, mGlo, mWmn, g, ep, s) != cudaSuccess) return VCE_ERR_CUDA;
+            if (run_gemm<EpiKahan, false, true>(mGhi, mGlo, mWmn, mWmn, g, ep, s) != cudaSuccess) return VCE_ERR_CUDA;
         }
     }
     return VCE_OK;
@@ -463,18 +524,19 @@ extern "C" int vce_gemm_bf16(const void* A, int a_mn, const void* B, int b_mn, i
     if (!aligned(A, 16) || !aligned(B, 16) || !aligned(C, 16) || (ldc % 4)) return VCE_ERR_ALIGN;
     int rc = require_sm100();
     if (rc) return rc;
-    CUtensorMap ma, mb;
+    CUtensorMap ma, mb, mb2;
     const bool ok_a = a_mn ? make_map(&ma, A, M, K, M, BK) : make_map(&ma, A, K, M, K, BM);
-    const bool ok_b = b_mn ? make_map(&mb, B, N, K, N, BK) : make_map(&mb, B, K, N, K, BN);
+    const bool ok_b = b_mn ? make_map(&mb, B, N, K, N, BK) && make_map(&mb2, B, N, K, N, BK)
+                           : make_map(&mb, B, K, N, K, BN) && make_map(&mb2, B, K, N, K, BN / 2);
     if (!ok_a || !ok_b) return VCE_ERR_CUDA;
     const int nk = (int)cdiv(K, BK);
     tc::GemmArgs g{(int)cdiv(M, BM), (int)cdiv(N, BN), nk, nk, 0, 0, 0, 0, nullptr};
     EpiStore::Params ep{C, ldc, M, N, 0, 0};
     cudaError_t e;
-    if (a_mn && b_mn) e = run_gemm<EpiStore, true, true>(ma, ma, mb, g, ep, s);
-    else if (a_mn) e = run_gemm<EpiStore, true, false>(ma, ma, mb, g, ep, s);
-    else if (b_mn) e = run_gemm<EpiStore, false, true>(ma, ma, mb, g, ep, s);
-    else e = run_gemm<EpiStore, false, false>(ma, ma, mb, g, ep, s);
+    if (a_mn && b_mn) e = run_gemm<EpiStore, true, true>(ma, ma, mb, mb2, g, ep, s);
+    else if (a_mn) e = run_gemm<EpiStore, true, false>(ma, ma, mb, mb2, g, ep, s);
+    else if (b_mn) e = run_gemm<EpiStore, false, true>(ma, ma, mb, mb2, g, ep, s);
+    else e = run_gemm<EpiStore, false, false>(ma, ma, mb, mb2, g, ep, s);
     return e == cudaSuccess ? VCE_OK : VCE_ERR_CUDA;
 }
 
@@ -487,11 +549,12 @@ extern "C" int vce_test_gemm_stall(const void* A, const void* B, int64_t M, int6
     if (!aligned(A, 16) || !aligned(B, 16) || !aligned(C, 16)) return VCE_ERR_ALIGN;
     int rc = require_sm100();
     if (rc) return rc;
-    CUtensorMap ma, mb;
-    if (!make_map(&ma, A, K, M, K, BM) || !make_map(&mb, B, K, N, K, BN)) return VCE_ERR_CUDA;
+    CUtensorMap ma, mb, mb2;
+    if (!make_map(&ma, A, K, M, K, BM) || !make_map(&mb, B, K, N, K, BN) || !make_map(&mb2, B, K, N, K, BN / 2))
+        return VCE_ERR_CUDA;
     if (cudaMemsetAsync(status, 0, sizeof(int32_t), s) != cudaSuccess) return VCE_ERR_CUDA;
     const int nk = (int)cdiv(K, BK);
     tc::GemmArgs g{(int)cdiv(M, BM), (int)cdiv(N, BN), nk, nk, 0, 0, 0, 0, status, 16u, wait_ns};
     EpiStore::Params ep{C, N, M, N, 0, 0};
-    return run_gemm<EpiStore>(ma, ma, mb, g, ep, s) == cudaSuccess ? VCE_OK : VCE_ERR_CUDA;
+    return run_gemm<EpiStore>(ma, ma, mb, mb2, g, ep, s) == cudaSuccess ? VCE_OK : VCE_ERR_CUDA;
 }

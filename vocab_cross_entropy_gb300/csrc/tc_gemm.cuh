@@ -66,6 +66,36 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64
         : "memory");
 }
 
+// As mma_commit, arriving on the mbarrier at the same shared-memory offset in every CTA of the
+// cluster that `mask` names.
+__device__ __forceinline__ void mma_commit_mc(uint64_t* bar, uint16_t mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            smem_u32(bar)),
+        "h"(mask)
+        : "memory");
+}
+
+// TMA tile load into the same shared-memory offset of every CTA of the cluster that `mask`
+// names, each completing bytes on its own mbarrier at `bar`'s offset.
+__device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y,
+                                               uint16_t mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster "
+        "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+        "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"(mask)
+        : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
 // Arrive on `bar` once every tcgen05.mma issued so far by this thread has completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
@@ -147,8 +177,15 @@ struct GemmArgs {
     uint64_t wait_ns;       // limit of every wait (0: kWaitNs)
 };
 
+// kPair: the grid runs as clusters of two CTAs (blockIdx 2c and 2c + 1) that take tiles 2q and
+// 2q + 1, which are (2p, n) and (2p + 1, n): the two share their B tile.  tiles_m is even.
+template <bool kPair>
 __device__ __forceinline__ void tile_coords(const GemmArgs& g, int tile, int& tm, int& tn) {
-    if (g.n_fastest) {
+    if (kPair && g.n_fastest) {
+        const int q = tile >> 1;
+        tn = q % g.tiles_n;
+        tm = 2 * (q / g.tiles_n) + (tile & 1);
+    } else if (g.n_fastest) {
         tn = tile % g.tiles_n;
         tm = tile / g.tiles_n;
     } else {
@@ -159,7 +196,12 @@ __device__ __forceinline__ void tile_coords(const GemmArgs& g, int tile, int& tm
 
 // kAmn / kBmn: the operand is MN-major; its tensor map then has 64 x 64 boxes over a global
 // [K, M] (resp. [K, N]) matrix, and the tile is loaded as BM/64 (resp. BN/64) boxes.
-template <class Epi, bool kAmn = false, bool kBmn = false>
+// kPair: launched as clusters of two CTAs that compute the two M-neighbours of one B tile
+// (tile_coords).  Each CTA loads its own A tile and one half of the shared B tile, multicast
+// into the same stage of both CTAs (a K-major B map then has boxes of BN/2 rows), so B crosses
+// from L2 once per pair.  A stage is free again once both CTAs' MMAs have read it: every MMA
+// commit arrives on the stage's empty barrier in both CTAs, and empty counts two arrivals.
+template <class Epi, bool kAmn = false, bool kBmn = false, bool kPair = false>
 __global__ void __launch_bounds__(kThreads, 1)
     k_tc_gemm(const __grid_constant__ CUtensorMap mapA0, const __grid_constant__ CUtensorMap mapA1,
               const __grid_constant__ CUtensorMap mapB, const GemmArgs g, const typename Epi::Params ep) {
@@ -180,7 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
+            mbar_init(&empty[s], kPair ? 2 : 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&acc_full[a], 1);
@@ -198,9 +240,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_relinquish();
     }
     tc_fence_before();
-    __syncthreads();
+    if (kPair)
+        cluster_sync_all();   // the peer's copies and commits reach these barriers only once they exist
+    else
+        __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    const uint32_t rank = kPair ? cluster_ctarank() : 0u;
     const int ntiles = g.tiles_m * g.tiles_n;
     const uint64_t wns = g.wait_ns ? g.wait_ns : kWaitNs;
 
@@ -211,7 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int issued = 0;   // stages whose copies were issued and not yet known complete
         for (int tile = blockIdx.x; tile < ntiles && !*abort_flag; tile += gridDim.x) {
             int tm, tn;
-            tile_coords(g, tile, tm, tn);
+            tile_coords<kPair>(g, tile, tm, tn);
             for (int kb = 0; kb < g.nk; ++kb) {
                 if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, g.err, kErrWaitEmpty, wns)) break;
                 mbar_arrive_expect_tx(&full[stage], STAGE_BYTES + g.tx_extra);
@@ -226,7 +272,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 } else {
                     tma_load_2d(smA + stage * A_BYTES, ma, &full[stage], ka * BK, g.a_y0 + tm * BM);
                 }
-                if (kBmn) {
+                if (kPair && kBmn) {
+#pragma unroll
+                    for (int i = 0; i < BN / 128; ++i) {
+                        const int h = (int)rank * (BN / 128) + i;
+                        tma_load_2d_mc(smB + stage * B_BYTES + h * (64 * BK * 2), &mapB, &full[stage],
+                                       g.b_y0 + tn * BN + h * 64, g.b_x0 + ka * BK, 0x3);
+                    }
+                } else if (kPair) {
+                    tma_load_2d_mc(smB + stage * B_BYTES + rank * (B_BYTES / 2), &mapB, &full[stage],
+                                   g.b_x0 + ka * BK, g.b_y0 + tn * BN + (int)rank * (BN / 2), 0x3);
+                } else if (kBmn) {
 #pragma unroll
                     for (int h = 0; h < BN / 64; ++h)
                         tma_load_2d(smB + stage * B_BYTES + h * (64 * BK * 2), &mapB, &full[stage],
@@ -235,6 +291,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tma_load_2d(smB + stage * B_BYTES, &mapB, &full[stage], g.b_x0 + ka * BK, g.b_y0 + tn * BN);
                 }
                 issued = issued < STAGES ? issued + 1 : STAGES;
+                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+            }
+        }
+        if (kPair && !*abort_flag) {
+            // the peer's MMA commits land on these empty barriers: wait (bounded) for the last
+            // STAGES of them so none arrives after this CTA has exited
+            for (int i = 0; i < STAGES; ++i) {
+                if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, g.err, kErrWaitEmpty, wns)) break;
                 if (++stage == STAGES) { stage = 0; phase ^= 1u; }
             }
         }
@@ -272,7 +336,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int k = 0; k < BK / 16; ++k)   // advance the start address by one K = 16 step
                     mma_bf16(d, ad + kStepA * k, bd + kStepB * k, idesc, (kb | k) != 0);
-                mma_commit(&empty[stage]);
+                if (kPair)
+                    mma_commit_mc(&empty[stage], 0x3);
+                else
+                    mma_commit(&empty[stage]);
                 if (++stage == STAGES) { stage = 0; phase ^= 1u; }
             }
             if (!ok) break;
@@ -294,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!mbar_wait(&acc_full[acc], acc_phase, abort_flag, g.err, kErrWaitAccFull, wns)) break;
             tc_fence_after();
             int tm, tn;
-            tile_coords(g, tile, tm, tn);
+            tile_coords<kPair>(g, tile, tm, tn);
             const int row = tm * BM + sub * 32 + lane;
             const uint32_t t0 = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(sub * 32) << 16);
             uint8_t* stage = epi_smem + sub * EPI_WARP_BYTES;
@@ -326,6 +393,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         tmem_dealloc(tmem_base, TMEM_COLS);
     }
+    if (kPair) cluster_sync_all();   // neither CTA leaves while the other may still write to it
 }
 
 }  // namespace tc
