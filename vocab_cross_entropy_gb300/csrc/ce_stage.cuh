@@ -92,8 +92,10 @@ __device__ __forceinline__ void fwd_stage_any(const uint4* buf, int nvec, int re
 // under label smoothing (kShift), then the thread holding the target overwrites that entry with
 // gt (its own later store to the same address).  Without kShift the entries are the plain
 // product (an FMA with a zero addend rounds the same, but measured 1.2% slower in the one-pass
-// kernel).  kPacked: the exponent arguments two at a time (ffma2, same rounding); measured 1.1%
-// faster in the one-pass kernel and no faster in the backward alone.
+// kernel).  kPacked: the exponent arguments and the products two at a time (fma/mul .f32x2, the
+// same rounding as the scalar forms); measured 1.1% + 1.0% faster in the one-pass kernel, and no
+// faster in the backward alone.  Packed sums in the forward (even and odd columns summed apart)
+// measured 0.3% slower in the one-pass kernel than the scalar tree.
 template <typename S, typename O, int NT, int U, bool kFull, bool kShift = false, bool kPacked = false>
 __device__ __forceinline__ void bwd_stage(const uint4* buf, int nvec, O* gcol, int rel0, int tid, float coef,
                                           float bias, float gt, float shift) {
@@ -120,8 +122,14 @@ __device__ __forceinline__ void bwd_stage(const uint4* buf, int nvec, O* gcol, i
                     a1 = fmaf(v[k + 1], kLog2e, -bias);
                 }
                 const float e0 = ex2(a0), e1 = ex2(a1);
-                v[k] = kShift ? fmaf(coef, e0, -shift) : coef * e0;
-                v[k + 1] = kShift ? fmaf(coef, e1, -shift) : coef * e1;
+                if (kPacked && kShift) {
+                    ffma2(e0, e1, coef, -shift, v[k], v[k + 1]);
+                } else if (kPacked) {
+                    fmul2(e0, e1, coef, v[k], v[k + 1]);
+                } else {
+                    v[k] = kShift ? fmaf(coef, e0, -shift) : coef * e0;
+                    v[k + 1] = kShift ? fmaf(coef, e1, -shift) : coef * e1;
+                }
             }
             GroupStore<O, G>::run(gcol + vi * G, v);
         }

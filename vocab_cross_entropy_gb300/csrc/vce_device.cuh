@@ -159,6 +159,16 @@ __device__ __forceinline__ void ffma2(float a0, float a1, float b, float c, floa
         : "f"(a0), "f"(a1), "f"(b), "f"(c));
 }
 
+// (d0, d1) = (a0 * b, a1 * b), two products in one packed fp32 instruction; each rounds as the
+// scalar product a * b does.
+__device__ __forceinline__ void fmul2(float a0, float a1, float b, float& d0, float& d1) {
+    asm("{\n\t.reg .b64 pa, pb, pd;\n\t"
+        "mov.b64 pa, {%2, %3};\n\tmov.b64 pb, {%4, %4};\n\t"
+        "mul.rn.f32x2 pd, pa, pb;\n\tmov.b64 {%0, %1}, pd;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b));
+}
+
 // ---- (max, sum-exp) pairs ------------------------------------------------------------------
 //
 // A pair (m, s) stands for the multiset sum  s * e^m = sum_k e^{v_k}, with m one of the v_k
