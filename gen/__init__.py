@@ -16,6 +16,9 @@ Workloads (sizes and value distributions of the pages' problems):
   chunked  the pages' matrix cut into 8 column chunks of 16032
   linear   E [8192, 4096] ~N(0,1), W [128256, 4096] ~N(0, 0.02^2), 2% ignored;
            small case T=8191, D=128, V=32 (the Cut Cross-Entropy issue #14 toy)
+  linear_peaked  the linear shapes with hidden states aligned to their targets
+           (E_i = 0.5 N(0,1) + a W_{t_i}, target logit ~24 above the rest), standing in
+           for a trained model's concentrated softmax
 """
 from __future__ import annotations
 
@@ -65,6 +68,7 @@ def _load():
             for name in ("vce_gen_normal_rows_f32", "vce_gen_normal_rows_bf16"):
                 getattr(lib, name).argtypes = [u64, u64, i64, i64, i64, i64, f64, f64, p, p, p]
             lib.vce_gen_copy_cols.argtypes = [p, i64, i64, i64, i64, i64, p, i64]
+            lib.vce_gen_aligned_rows_bf16.argtypes = [u64, u64, i64, i64, i64, f64, p, p, p]
             _lib = lib
     return _lib
 
@@ -232,7 +236,13 @@ def custom(T, V, dtype="bf16", seed=7, std=2.0, n_margin=0, margin=(17.0, 50.0),
 
 @dataclass
 class LinearProblem:
-    """Fused linear-CE workload: E [T, D] ~N(0,1), W [V, D] ~N(0, 0.02^2), bf16, labels in [0, V)."""
+    """Fused linear-CE workload: E [T, D] ~N(0,1), W [V, D] ~N(0, 0.02^2), bf16, labels in [0, V).
+
+    peak > 0 draws hidden states aligned with their targets, a stand-in for a trained model
+    whose softmax is concentrated on the label: E_i = e_std * N(0, 1) + a * W_{t_i} with
+    a = peak / (D * w_std^2), so the target logit sits about `peak` above the others
+    (ignored rows get the noise alone).
+    """
     name: str
     T: int
     D: int
@@ -241,6 +251,7 @@ class LinearProblem:
     n_ignore: int
     e_std: float = 1.0
     w_std: float = 0.02
+    peak: float = 0.0
     ignore_index: int = IGNORE_INDEX
     labels: np.ndarray = field(init=False)
     ignore_rows: np.ndarray = field(init=False)
@@ -252,11 +263,25 @@ class LinearProblem:
         labels[self.ignore_rows] = self.ignore_index
         self.labels = labels
 
+    def _aligned(self, r0, n, out, W=None):
+        """Rows r0..r0+n-1 of the target-aligned E (peak > 0), W the full classifier or None."""
+        t = self.labels[r0: r0 + n]
+        ok = (t >= 0) & (t < self.V)
+        tt = np.where(ok, t, 0)
+        add = np.ascontiguousarray(W[tt]) if W is not None else self.W_rows(tt)
+        a = np.where(ok, self.peak / (self.D * self.w_std ** 2), 0.0).astype(np.float64)
+        _load().vce_gen_aligned_rows_bf16(self.seed, S_E, r0, n, self.D, self.e_std, _ptr(add), _ptr(a),
+                                          _ptr(out))
+        return out
+
     def E_rows(self, idx):
         idx = np.atleast_1d(np.asarray(idx, np.int64))
         out = np.empty((len(idx), self.D), np.uint16)
         for k, r in enumerate(idx):
-            normal_rows(self.seed, S_E, int(r), 1, self.D, 0.0, self.e_std, "bf16", out=out[k: k + 1])
+            if self.peak > 0:
+                self._aligned(int(r), 1, out[k: k + 1])
+            else:
+                normal_rows(self.seed, S_E, int(r), 1, self.D, 0.0, self.e_std, "bf16", out=out[k: k + 1])
         return out
 
     def W_rows(self, idx):
@@ -266,8 +291,13 @@ class LinearProblem:
             normal_rows(self.seed, S_W, int(r), 1, self.D, 0.0, self.w_std, "bf16", out=out[k: k + 1])
         return out
 
-    def E(self, out=None, threads=None):
+    def E(self, out=None, threads=None, W=None):
+        """All of E; with peak > 0 the classifier W (bf16 bits) is drawn first unless given."""
         out = np.empty((self.T, self.D), np.uint16) if out is None else out
+        if self.peak > 0:
+            W = self.W(threads=threads) if W is None else W
+            _parallel_rows(self.T, lambda r0, n: self._aligned(r0, n, out[r0: r0 + n], W), threads)
+            return out
         _parallel_rows(self.T, lambda r0, n: normal_rows(self.seed, S_E, r0, n, self.D, 0.0, self.e_std,
                                                          "bf16", out=out[r0: r0 + n]), threads)
         return out
@@ -289,5 +319,12 @@ def linear_small(seed=1005):
     return LinearProblem("linear_small", T, 128, 32, seed, round(0.02 * T))
 
 
-def linear_custom(T, D, V, seed=11, n_ignore=0, e_std=1.0, w_std=0.02):
-    return LinearProblem("linear_custom", T, D, V, seed, n_ignore, e_std, w_std)
+def linear_custom(T, D, V, seed=11, n_ignore=0, e_std=1.0, w_std=0.02, peak=0.0):
+    return LinearProblem("linear_custom", T, D, V, seed, n_ignore, e_std, w_std, peak)
+
+
+def linear_peaked(seed=1006):
+    """The linear workload's shapes with target-aligned hidden states (noise std 0.5, the
+    target logit ~24 above the rest): a concentrated softmax for gradient filtering."""
+    T = 8192
+    return LinearProblem("linear_peaked", T, 4096, 128256, seed, round(0.02 * T), 0.5, 0.02, 24.0)

@@ -144,6 +144,28 @@ void vce_gen_normal_rows_bf16(uint64_t seed, uint64_t stream, int64_t r0, int64_
     }
 }
 
+/*
+ * Rows r0 .. r0+nrows-1 of a [*, ncols] matrix whose element (r, j) is
+ *     std * (normal number r*ncols + j of the stream) + a[r - r0] * bf16(add[(r - r0), j]),
+ * computed in double, rounded to fp32 and then to bf16 (ties to even).  `add` holds nrows
+ * rows of ncols bf16 values (stride ncols).  With add = the classifier rows of the rows'
+ * labels this draws hidden states aligned with their targets.
+ */
+void vce_gen_aligned_rows_bf16(uint64_t seed, uint64_t stream, int64_t r0, int64_t nrows, int64_t ncols,
+                               double std, const uint16_t* add, const double* a, uint16_t* out) {
+    uint64_t key = stream_key(seed, stream);
+    for (int64_t r = 0; r < nrows; ++r) {
+        uint16_t* row = out + r * ncols;
+        const uint16_t* ar = add + r * ncols;
+        uint64_t base = (uint64_t)(r0 + r) * (uint64_t)ncols;
+        for (int64_t j = 0; j < ncols; ++j) {
+            double v = std * normal_at(key, base + (uint64_t)j);
+            if (a[r] != 0.0) v += a[r] * (double)bf16_bits_to_f32(ar[j]);
+            row[j] = f32_to_bf16_bits((float)v);
+        }
+    }
+}
+
 /* Copy columns [c0, c0+w) of nrows rows (strides ld_in / ld_out, elements of `esize` bytes). */
 void vce_gen_copy_cols(const void* in, int64_t ld_in, int64_t nrows, int64_t c0, int64_t w,
                        int64_t esize, void* out, int64_t ld_out) {

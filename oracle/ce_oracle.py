@@ -36,6 +36,8 @@ the merge rescales the sums to the global maximum.
 The fused linear-CE follows the Cut Cross-Entropy issue #14 page
 (linear_cross_entropy(e, c, targets), no bias; impl="cce_exact": no gradient
 filtering): logits z = E W^T, then the CE above, then dE = G W and dW = G^T E.
+The same page names gradient filtering as what "cce_exact" turns off and gives no rule for
+it; linear_ce_filtered states the block rule this library takes (see there).
 """
 from __future__ import annotations
 
@@ -361,3 +363,53 @@ def linear_ce_grad_columns(E, W, labels, fwd, c, cols, ignore_index=IGNORE_INDEX
         hit = np.nonzero(valid & (labels == j))[0]
         G[hit, k] = -np.asarray(c)[hit] * p_nt[hit]
     return G
+
+
+# ----------------------------------------------------------------------------------------
+# gradient filtering of the fused linear-CE (Cut Cross-Entropy issue #14: impl="cce_exact"
+# is the variant that disables it; the page states no rule)
+#
+# Reading taken: G is cut into blocks of `block` rows by `block` vocabulary columns, aligned
+# at row 0 and column 0 (block = 128 in the library).  A block is dropped -- its entries count
+# as 0 in dE = G W and dW = G^T E -- when no valid row of it has its target among the block's
+# columns and every non-target probability p_ij of its valid rows is below eps.  Kept blocks
+# keep their exact entries.  The loss and the statistics are not filtered.
+
+def filter_blocks(z, labels, eps, block=128, ignore_index=IGNORE_INDEX):
+    """keep[rb, cb] for the blocks of G, with the blocks' largest non-target probability
+    (0 where a block has no valid row) and whether a block holds a valid row's target."""
+    z = np.asarray(z, np.float64)
+    T, V = z.shape
+    fwd = ce_rows(z, labels, ignore_index)
+    valid = fwd["valid"]
+    labels = np.asarray(labels, np.int64)
+    nr, nc = -(-T // block), -(-V // block)
+    pmax = np.zeros((nr, nc))
+    has_t = np.zeros((nr, nc), bool)
+    starts = np.arange(0, V, block)
+    pnt = sigmoid(fwd["x"])
+    for i in np.nonzero(valid)[0]:
+        p = np.zeros(V)
+        if np.isfinite(fwd["lse_nt"][i]):
+            p = np.exp(z[i] - fwd["lse_nt"][i]) * pnt[i]   # p_j, j != t (collapse-safe form)
+        p[labels[i]] = 0.0
+        rb = i // block
+        pmax[rb] = np.maximum(pmax[rb], np.maximum.reduceat(p, starts))
+        has_t[rb, labels[i] // block] = True
+    return has_t | (pmax >= eps), pmax, has_t
+
+
+def linear_ce_filtered(E, W, labels, eps, reduction="mean", grad_output=1.0, ignore_index=IGNORE_INDEX,
+                       block=128):
+    """linear_ce with gradient filtering: dE and dW from G with its dropped blocks zeroed."""
+    E = np.asarray(E, np.float64)
+    W = np.asarray(W, np.float64)
+    r = linear_ce(E, W, labels, reduction, grad_output, ignore_index)
+    keep, pmax, has_t = filter_blocks(r["z"], labels, eps, block, ignore_index)
+    T, V = r["z"].shape
+    mask = np.repeat(np.repeat(keep, block, axis=0), block, axis=1)[:T, :V]
+    Gf = np.where(mask, r["grad"], 0.0)
+    r["dE"] = Gf @ W
+    r["dW"] = Gf.T @ E
+    r["keep"], r["block_pmax"], r["block_target"] = keep, pmax, has_t
+    return r
