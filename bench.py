@@ -1,7 +1,7 @@
 """Throughput of the collapse-safe CE forward+backward on one GB300 (or N replicas).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload pages|chunked|mid|linear]
+                    [--workload pages|chunked|mid|linear|linear_peaked]
 
 One step = ce_forward + ce_backward over one batch of the workload (default: the pages'
 shape, T=16384 rows x V=128256 bf16 logits, mean over non-ignored rows, 10% of rows with
@@ -366,17 +366,21 @@ class ChunkedWorkload(CEWorkload):
 
 
 class LinearWorkload:
-    """Fused linear-CE: E [8192, 4096], W [128256, 4096] bf16; one linear_ce_fwd_bwd call per step."""
+    """Fused linear-CE: E [8192, 4096], W [128256, 4096] bf16; one linear_ce_fwd_bwd call per step
+    (linear_ce_fwd_bwd_filtered when filter_eps > 0)."""
 
-    def __init__(self, problem, device):
+    def __init__(self, problem, device, filter_eps=0.0):
         import vocab_cross_entropy_gb300 as vce
         self.vce = vce
         self.p = problem
+        self.filter_eps = float(filter_eps)
         T, D, V = problem.T, problem.D, problem.V
-        self.E_host = torch.empty((T, D), dtype=torch.int16, pin_memory=True)
-        problem.E(out=self.E_host.numpy().view(np.uint16))
         self.W_host = torch.empty((V, D), dtype=torch.int16, pin_memory=True)
         problem.W(out=self.W_host.numpy().view(np.uint16))
+        self.E_host = torch.empty((T, D), dtype=torch.int16, pin_memory=True)
+        problem.E(out=self.E_host.numpy().view(np.uint16), W=self.W_host.numpy().view(np.uint16))
+        self.kept = torch.zeros(1, dtype=torch.int64, device=device)
+        self.blocks = (-(-T // 128)) * (-(-V // 128))
         self.E = self.E_host.view(torch.bfloat16).to(device)
         self.W = self.W_host.view(torch.bfloat16).to(device)
         self.labels_host = torch.from_numpy(problem.labels).pin_memory()
@@ -393,6 +397,12 @@ class LinearWorkload:
         self.launches_per_step = 3 + 3 * nchunks     # statistics GEMM + merge + reduce, 3 GEMMs per chunk
 
     def step(self, stream):
+        if self.filter_eps > 0:
+            self.vce.linear_ce_fwd_bwd_filtered(self.E, self.W, self.labels, self.filter_eps, grad_output=self.go,
+                                                dE=self.dE, dW=self.dW, loss_rows=self.loss_rows,
+                                                loss_out=self.loss_out, workspace=self.ws, kept_blocks=self.kept,
+                                                status=self.status, stream=stream)
+            return
         self.vce.linear_ce_fwd_bwd(self.E, self.W, self.labels, grad_output=self.go, dE=self.dE, dW=self.dW,
                                    loss_rows=self.loss_rows, loss_out=self.loss_out, workspace=self.ws,
                                    status=self.status, stream=stream)
@@ -414,16 +424,38 @@ class LinearWorkload:
     def tokens(self):
         return self.p.T
 
+    def kept_blocks(self):
+        return int(self.kept.item()) if self.filter_eps > 0 else self.blocks
+
     def flops(self):
+        """Algorithmic: z twice (statistics, then recomputed for G) over all of [T, V], and dE, dW
+        over the kept 128 x 128 blocks of G (all of them without filtering)."""
         p = self.p
-        return 8.0 * p.T * p.V * p.D
+        if self.filter_eps <= 0:
+            return 8.0 * p.T * p.V * p.D
+        return 4.0 * p.T * p.V * p.D + 4.0 * self.kept_blocks() * 128 * 128 * p.D
+
+    def executed_flops(self):
+        """What the tensor cores run: G enters dE and dW as two bf16 halves (hi + lo)."""
+        p = self.p
+        if self.filter_eps <= 0:
+            return 12.0 * p.T * p.V * p.D
+        return 4.0 * p.T * p.V * p.D + 8.0 * self.kept_blocks() * 128 * 128 * p.D
 
     def describe(self):
         p = self.p
-        return {"workload": f"{p.name}: fused linear-CE fwd+bwd, E [{p.T}, {p.D}] x W [{p.V}, {p.D}] bf16, mean over "
-                            f"non-ignored rows ({len(p.ignore_rows)} ignored), dE and dW bf16",
-                "T": p.T, "D": p.D, "V": p.V, "operands": "bf16", "accumulate": "f32",
-                "l2": "no flush: W (%.2f GB) larger than the 129 MB L2" % (p.V * p.D * 2 / 1e9)}
+        d = {"workload": f"{p.name}: fused linear-CE fwd+bwd, E [{p.T}, {p.D}] x W [{p.V}, {p.D}] bf16, mean over "
+                         f"non-ignored rows ({len(p.ignore_rows)} ignored), dE and dW bf16",
+             "T": p.T, "D": p.D, "V": p.V, "operands": "bf16", "accumulate": "f32",
+             "l2": "no flush: W (%.2f GB) larger than the 129 MB L2" % (p.V * p.D * 2 / 1e9)}
+        if p.peak > 0:
+            d["hidden_states"] = (f"aligned with their targets: E_i = {p.e_std} N(0,1) + a W_(t_i), target logit "
+                                  f"~{p.peak} above the rest (a stand-in for a trained model's concentrated softmax)")
+        if self.filter_eps > 0:
+            k = self.kept_blocks()
+            d.update(filter_eps=self.filter_eps, kept_blocks=k, blocks=self.blocks,
+                     kept_fraction=round(k / self.blocks, 5))
+        return d
 
 
 # ------------------------------------------------------------------------------- timing
@@ -486,11 +518,13 @@ def cpu_oracle_baseline(problem, budget_s=12.0, max_rows=4096):
 # ------------------------------------------------------------------------------- main
 
 def run_linear(args, rank, local_rank, world, device):
-    problem = gen.linear(seed=1005 + rank)
+    peaked = args.workload == "linear_peaked"
+    problem = gen.linear_peaked(seed=1006 + rank) if peaked else gen.linear(seed=1005 + rank)
     if args.vocab:
-        problem = gen.LinearProblem(f"linear[V={args.vocab}]", problem.T, problem.D, args.vocab, problem.seed,
-                                    problem.n_ignore)
-    w = LinearWorkload(problem, device)
+        problem = gen.LinearProblem(f"{problem.name}[V={args.vocab}]", problem.T, problem.D, args.vocab,
+                                    problem.seed, problem.n_ignore, problem.e_std, problem.w_std, problem.peak)
+    eps = args.filter_eps if args.filter_eps is not None else (2.0 ** -12 if peaked else 0.0)
+    w = LinearWorkload(problem, device, eps)
     stream = torch.cuda.current_stream(device)
     for _ in range(args.warmup):
         w.step(stream)
@@ -508,17 +542,20 @@ def run_linear(args, rank, local_rank, world, device):
     ms_step = ms / args.steps
     peaks = measured_peaks()
     achieved = w.flops() / (ms_step / 1e3) / 1e12
+    call = "linear_ce_fwd_bwd_filtered" if eps > 0 else "linear_ce_fwd_bwd"
     out = {
-        "metric": "fused linear-CE fwd+bwd tokens/s at T=8192, D=4096, V=128256 bf16; TFLOP/s vs bf16 peak",
+        "metric": ("fused linear-CE fwd+bwd tokens/s at T=8192, D=4096, V=128256 bf16"
+                   + (f", gradient filtering at eps={eps:.3g}" if eps > 0 else "") + "; TFLOP/s vs bf16 peak"),
         "value": round(tokens_all / (ms_step / 1e3), 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": dict(w.describe(), parallelism=f"replicas{world}"),
-        "roofline": {"bound": "tensor", "kernel": "linear_ce_fwd_bwd (all launches of one call)",
+        "roofline": {"bound": "tensor", "kernel": f"{call} (all launches of one call)",
                      "achieved": round(achieved, 1), "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
                      "frac": round(achieved / peaks["bf16_tflops_sustained"], 4),
                      "frac_of_burst": round(achieved / peaks["bf16_tflops"], 4), "peak_source": peaks["source"],
-                     "algorithmic_flop_per_call": w.flops(), "executed_flop_per_call": 1.5 * w.flops(),
+                     "algorithmic_flop_per_call": w.flops(), "executed_flop_per_call": w.executed_flops(),
+                     "executed_tflops": round(w.executed_flops() / (ms_step / 1e3) / 1e12, 1),
                      "traffic": None},
         "e2e": {"value": round(tokens_all / (e2e_ms / e2e_steps / 1e3), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": w.h2d_bytes, "d2h_bytes_per_step": w.d2h_bytes, "steps": e2e_steps},
@@ -533,7 +570,7 @@ def run_ours(args, rank, local_rank, world):
     device = torch.device("cuda", local_rank)
     torch.cuda.set_device(device)
     init_dist(world, "nccl")
-    if args.workload == "linear":
+    if args.workload in ("linear", "linear_peaked"):
         return run_linear(args, rank, local_rank, world, device)
     problem = {"pages": gen.pages, "chunked": gen.pages, "fused": gen.pages, "mid": gen.mid}[args.workload](
         seed=(1002 if args.workload == "mid" else 1003) + rank)
@@ -688,7 +725,10 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["pages", "fused", "chunked", "mid", "linear"], default="pages")
+    ap.add_argument("--workload", choices=["pages", "fused", "chunked", "mid", "linear", "linear_peaked"],
+                    default="pages")
+    ap.add_argument("--filter-eps", type=float, default=None,
+                    help="linear workloads: gradient-filter threshold (default 2^-12 for linear_peaked, 0 for linear)")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--logits-dtype", choices=["bf16", "f32"], default="bf16",
                     help="storage type of the logits (and gradient) for the CE workloads")

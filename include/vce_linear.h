@@ -25,7 +25,8 @@ extern "C" {
  * Bytes of workspace linear_ce_fwd_bwd needs for these sizes; 0 if the sizes are
  * invalid (T, V >= 1; D >= 8 and a multiple of 8).  For T=8192, D=4096, V=128256 it is
  * about 0.87 GB (per-tile statistics, one 16384-column vocabulary chunk of the gradient as
- * two bf16 halves, and the compensated dE accumulator pair).
+ * two bf16 halves, the compensated dE accumulator pair, and the gradient-filter bit tables
+ * of one chunk).
  */
 size_t linear_ce_workspace_bytes(int64_t T, int64_t D, int64_t V);
 
@@ -59,6 +60,32 @@ int linear_ce_fwd_bwd(const void* E, const void* W, int64_t T, int64_t D, int64_
                       const float* grad_output, float* loss_rows, float* loss_out,
                       void* dE, void* dW, vce_dtype grad_dt,
                       void* workspace, size_t workspace_bytes, int32_t* status, vce_stream_t s);
+
+/*
+ * linear_ce_fwd_bwd_filtered -- linear_ce_fwd_bwd with gradient filtering (Cut Cross-Entropy
+ * issue #14: the filtering that impl="cce_exact" turns off; the page states no rule, this is
+ * the rule taken here).
+ *   G is cut into blocks of 128 rows by 128 vocabulary columns (aligned at 0).  A block is
+ *   dropped -- its entries count as 0 in dE = G W and dW = G^T E -- when none of its valid
+ *   rows has its target among the block's columns and every non-target probability p_ij of
+ *   its valid rows is below filter_eps.  The dW and dE GEMMs skip the dropped blocks'
+ *   K blocks (128 rows, resp. columns, is a whole number of their K blocks), so kept blocks
+ *   keep exactly the unfiltered arithmetic and the work falls with the dropped fraction.
+ *   The loss and row statistics are never filtered.
+ *
+ *   filter_eps   threshold on p_ij, finite and >= 0; 0 is exactly linear_ce_fwd_bwd (no
+ *                block is dropped).  NaN, negative or infinite: VCE_ERR_ARG, nothing enqueued.
+ *   kept_blocks  optional device uint64 (8-byte aligned, may be NULL): set to the number of
+ *                (row block, column block) pairs kept, over all vocabulary chunks; 0 when
+ *                filter_eps = 0 (the filter does not run)
+ *   Every other argument as linear_ce_fwd_bwd; the workspace size is the same.
+ */
+int linear_ce_fwd_bwd_filtered(const void* E, const void* W, int64_t T, int64_t D, int64_t V,
+                               const int64_t* labels, int64_t ignore_index, vce_reduction red,
+                               const float* grad_output, float* loss_rows, float* loss_out,
+                               void* dE, void* dW, vce_dtype grad_dt, float filter_eps,
+                               unsigned long long* kept_blocks, void* workspace, size_t workspace_bytes,
+                               int32_t* status, vce_stream_t s);
 
 /*
  * vce_gemm_bf16 -- the tensor-core GEMM the linear-CE is built on, with a plain fp32 output:

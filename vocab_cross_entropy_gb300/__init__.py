@@ -16,7 +16,7 @@ import torch
 __all__ = ["VceError", "lib", "library_path", "ce_forward", "ce_backward", "ce_forward_ls", "ce_backward_ls",
            "ce_forward_backward", "ce_forward_backward_ls", "ce_merge_chunks", "ce_merge_chunks_ls",
            "ce_merge_chunks_noalloc",
-           "linear_ce_workspace_bytes", "linear_ce_fwd_bwd", "vce_get_status", "vce_status_string",
+           "linear_ce_workspace_bytes", "linear_ce_fwd_bwd", "linear_ce_fwd_bwd_filtered", "vce_get_status", "vce_status_string",
            "vce_abi_version", "cross_entropy", "IGNORE_INDEX", "F32", "BF16", "RED"]
 
 IGNORE_INDEX = -100
@@ -62,6 +62,9 @@ def _load():
         L.linear_ce_workspace_bytes.argtypes = [i64, i64, i64]
         L.linear_ce_workspace_bytes.restype = sz
         L.linear_ce_fwd_bwd.argtypes = [p, p, i64, i64, i64, p, i64, i32, p, p, p, p, p, i32, p, sz, p, p]
+        if hasattr(L, "linear_ce_fwd_bwd_filtered"):
+            L.linear_ce_fwd_bwd_filtered.argtypes = [p, p, i64, i64, i64, p, i64, i32, p, p, p, p, p, i32, f32, p,
+                                                     p, sz, p, p]
         L.vce_gemm_bf16.argtypes = [p, i32, p, i32, i64, i64, i64, p, i64, p]
         L.vce_gemm_bf16.restype = i32
         L.vce_test_gemm_stall.argtypes = [p, p, i64, i64, i64, p, ctypes.c_uint64, p, p]
@@ -71,7 +74,7 @@ def _load():
     for name in ("ce_forward", "ce_backward", "ce_forward_ls", "ce_backward_ls", "ce_forward_backward",
                  "ce_forward_backward_ls", "ce_merge_chunks_ls",
                  "ce_merge_chunks", "ce_merge_chunks_noalloc",
-                 "linear_ce_fwd_bwd",
+                 "linear_ce_fwd_bwd", "linear_ce_fwd_bwd_filtered",
                  "vce_get_status"):
         if hasattr(L, name):
             getattr(L, name).restype = i32
@@ -360,6 +363,27 @@ def linear_ce_fwd_bwd(E, W, labels, ignore_index=IGNORE_INDEX, reduction="mean",
 
     Returns (loss_out, loss_rows, dE, dW, status).
     """
+    return _linear_ce(E, W, labels, ignore_index, reduction, grad_output, grad_dtype, dE, dW, loss_rows, loss_out,
+                      workspace, status, stream, None, None)
+
+
+def linear_ce_fwd_bwd_filtered(E, W, labels, filter_eps, ignore_index=IGNORE_INDEX, reduction="mean", *,
+                               grad_output=None, grad_dtype=None, dE=None, dW=None, loss_rows=None, loss_out=None,
+                               workspace=None, kept_blocks=None, status=None, stream=None):
+    """linear_ce_fwd_bwd with gradient filtering at threshold filter_eps (128 x 128 blocks of G).
+
+    Returns (loss_out, loss_rows, dE, dW, status, kept_blocks), kept_blocks a device int64 [1]
+    with the number of blocks kept.
+    """
+    if kept_blocks is None:
+        kept_blocks = torch.empty(1, dtype=torch.int64, device=E.device)
+    out = _linear_ce(E, W, labels, ignore_index, reduction, grad_output, grad_dtype, dE, dW, loss_rows, loss_out,
+                     workspace, status, stream, float(filter_eps), kept_blocks)
+    return out + (kept_blocks,)
+
+
+def _linear_ce(E, W, labels, ignore_index, reduction, grad_output, grad_dtype, dE, dW, loss_rows, loss_out,
+               workspace, status, stream, filter_eps, kept_blocks):
     T, D = E.shape
     V = W.shape[0]
     dev = E.device
@@ -375,10 +399,16 @@ def linear_ce_fwd_bwd(E, W, labels, ignore_index=IGNORE_INDEX, reduction="mean",
     need = linear_ce_workspace_bytes(T, D, V)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
-    _check("linear_ce_fwd_bwd", _get().linear_ce_fwd_bwd(
-        _ptr(E), _ptr(W), T, D, V, _ptr(labels), int(ignore_index), RED[reduction], _ptr(grad_output),
-        _ptr(loss_rows), _ptr(loss_out), _ptr(dE), _ptr(dW), _dtype(dE), _ptr(workspace), workspace.numel(),
-        _ptr(status), _stream(stream)))
+    if filter_eps is None:
+        _check("linear_ce_fwd_bwd", _get().linear_ce_fwd_bwd(
+            _ptr(E), _ptr(W), T, D, V, _ptr(labels), int(ignore_index), RED[reduction], _ptr(grad_output),
+            _ptr(loss_rows), _ptr(loss_out), _ptr(dE), _ptr(dW), _dtype(dE), _ptr(workspace), workspace.numel(),
+            _ptr(status), _stream(stream)))
+    else:
+        _check("linear_ce_fwd_bwd_filtered", _get().linear_ce_fwd_bwd_filtered(
+            _ptr(E), _ptr(W), T, D, V, _ptr(labels), int(ignore_index), RED[reduction], _ptr(grad_output),
+            _ptr(loss_rows), _ptr(loss_out), _ptr(dE), _ptr(dW), _dtype(dE), filter_eps, _ptr(kept_blocks),
+            _ptr(workspace), workspace.numel(), _ptr(status), _stream(stream)))
     return loss_out, loss_rows, dE, dW, status
 
 

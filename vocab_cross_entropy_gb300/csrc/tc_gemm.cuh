@@ -175,7 +175,58 @@ struct GemmArgs {
     uint32_t tx_extra;      // bytes announced per stage beyond the copies (0; > 0 only to test the
                             // give-up path: the stage never completes and the waits must time out)
     uint64_t wait_ns;       // limit of every wait (0: kWaitNs)
+    // Optional K-block skipping (gradient filtering): row tm of skip holds one bit per 128
+    // K columns (two K blocks) of M tile tm, skip_ld 32-bit words per row; a clear bit means
+    // A is all zero there for this tile.  Applies to both halves (A0 and A1) alike.  Null:
+    // every K block runs.
+    const uint32_t* skip;
+    int skip_ld;
 };
+
+// Calls f(kb, ka, mine) for the K blocks of M tile tm in order -- kb the block index (A0
+// blocks, then A1 blocks), ka its index within its half -- and stops when f returns false.
+// Without skip bits that is every K block (mine = true).  With them (gradient filtering) it is
+// the K blocks of the 128-column blocks whose bit is set for this tile or, for a CTA pair, for
+// its partner (both CTAs then load the same stages; mine says whether this tile multiplies).
+// The bits are scanned 32 blocks at a time with find-first-set, the next word loaded while the
+// current one is walked, so skipped blocks cost nothing.  nk is nk_a0 or 2 nk_a0.
+template <class F>
+__device__ __forceinline__ void for_each_kblock(const GemmArgs& g, int tm, bool pair, F&& f) {
+    if (!g.skip) {
+        for (int kb = 0; kb < g.nk; ++kb)
+            if (!f(kb, kb >= g.nk_a0 ? kb - g.nk_a0 : kb, true)) return;
+        return;
+    }
+    const uint32_t* own = g.skip + (size_t)tm * g.skip_ld;
+    const uint32_t* peer = pair ? g.skip + (size_t)(tm ^ 1) * g.skip_ld : own;
+    for (int half = 0; half * g.nk_a0 < g.nk; ++half) {
+        uint32_t on = own[0], pn = peer[0];
+        for (int w = 0; w < g.skip_ld; ++w) {
+            const uint32_t o = on;
+            uint32_t m = on | pn;
+            if (w + 1 < g.skip_ld) {
+                on = own[w + 1];
+                pn = peer[w + 1];
+            }
+            while (m) {
+                const int bit = __ffs(m) - 1;
+                m &= m - 1u;
+                const bool mine = (o >> bit) & 1u;
+                const int ka0 = 2 * (w * 32 + bit);   // 128 columns = two K blocks
+                for (int ka = ka0; ka < ka0 + 2 && ka < g.nk_a0; ++ka)
+                    if (!f(half * g.nk_a0 + ka, ka, mine)) return;
+            }
+        }
+    }
+}
+
+// Whether M tile tm reads any kept K block.
+__device__ __forceinline__ bool tile_has_blocks(const GemmArgs& g, int tm) {
+    if (!g.skip) return true;
+    uint32_t m = 0;
+    for (int w = 0; w < g.skip_ld; ++w) m |= g.skip[(size_t)tm * g.skip_ld + w];
+    return m != 0u;
+}
 
 // kPair: the grid runs as clusters of two CTAs (blockIdx 2c and 2c + 1) that take tiles 2q and
 // 2q + 1, which are (2p, n) and (2p + 1, n): the two share their B tile.  tiles_m is even.
@@ -258,11 +309,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int tile = blockIdx.x; tile < ntiles && !*abort_flag; tile += gridDim.x) {
             int tm, tn;
             tile_coords<kPair>(g, tile, tm, tn);
-            for (int kb = 0; kb < g.nk; ++kb) {
-                if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, g.err, kErrWaitEmpty, wns)) break;
+            for_each_kblock(g, tm, kPair, [&](int kb, int ka, bool) {
+                if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, g.err, kErrWaitEmpty, wns)) return false;
                 mbar_arrive_expect_tx(&full[stage], STAGE_BYTES + g.tx_extra);
                 const bool second = kb >= g.nk_a0;
-                const int ka = second ? kb - g.nk_a0 : kb;
                 const CUtensorMap* ma = second ? &mapA1 : &mapA0;
                 if (kAmn) {
 #pragma unroll
@@ -292,7 +342,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 issued = issued < STAGES ? issued + 1 : STAGES;
                 if (++stage == STAGES) { stage = 0; phase ^= 1u; }
-            }
+                return true;
+            });
         }
         if (kPair && !*abort_flag) {
             // the peer's MMA commits land on these empty barriers: wait (bounded) for the last
@@ -327,21 +378,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!mbar_wait(&acc_free[acc], acc_phase ^ 1u, abort_flag, g.err, kErrWaitAccFree, wns)) break;
             tc_fence_after();
             const uint32_t d = tmem_base + (uint32_t)(acc * BN);
-            bool ok = true;
-            for (int kb = 0; kb < g.nk; ++kb) {
-                if (!mbar_wait(&full[stage], phase, abort_flag, g.err, kErrWaitFull, wns)) { ok = false; break; }
+            int tm, tn;
+            tile_coords<kPair>(g, tile, tm, tn);
+            bool ok = true, issued = false;
+            for_each_kblock(g, tm, kPair, [&](int, int, bool mine) {
+                if (!mbar_wait(&full[stage], phase, abort_flag, g.err, kErrWaitFull, wns)) {
+                    ok = false;
+                    return false;
+                }
                 tc_fence_after();
                 const uint64_t ad = kAmn ? desc_mnmajor_sw128(a0 + stage * A_BYTES) : desc_kmajor_sw128(a0 + stage * A_BYTES);
                 const uint64_t bd = kBmn ? desc_mnmajor_sw128(b0 + stage * B_BYTES) : desc_kmajor_sw128(b0 + stage * B_BYTES);
+                if (mine) {   // else loaded for the partner only: released without MMAs
 #pragma unroll
-                for (int k = 0; k < BK / 16; ++k)   // advance the start address by one K = 16 step
-                    mma_bf16(d, ad + kStepA * k, bd + kStepB * k, idesc, (kb | k) != 0);
+                    for (int k = 0; k < BK / 16; ++k)   // advance the start address by one K = 16 step
+                        mma_bf16(d, ad + kStepA * k, bd + kStepB * k, idesc, (issued || k != 0) ? 1u : 0u);
+                    issued = true;
+                }
                 if (kPair)
                     mma_commit_mc(&empty[stage], 0x3);
                 else
                     mma_commit(&empty[stage]);
                 if (++stage == STAGES) { stage = 0; phase ^= 1u; }
-            }
+                return true;
+            });
             if (!ok) break;
             mma_commit(&acc_full[acc]);
             acc ^= 1;
@@ -368,17 +428,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             // Two register buffers: the next 32 columns load from TMEM while these are consumed.
             static_assert((BN / 32) % 2 == 0, "column pieces go in pairs");
             uint32_t ra[32], rb[32];
-            tmem_ld32(t0, ra);
             typename Epi::Row st;
-            Epi::begin(ep, st, row, tn);   // its global loads overlap the first TMEM load
+            if (!tile_has_blocks(g, tm)) {   // every K block skipped: no MMA wrote the accumulator
+#pragma unroll
+                for (int k = 0; k < 32; ++k) ra[k] = 0u;
+                Epi::begin(ep, st, row, tn);
 #pragma unroll 1
-            for (int c = 0; c < BN / 32; c += 2) {
-                tmem_wait_ld(ra);
-                tmem_ld32(t0 + (uint32_t)((c + 1) * 32), rb);
-                Epi::consume(ep, st, row, tn * BN + c * 32, ra, stage);
-                tmem_wait_ld(rb);
-                if (c + 2 < BN / 32) tmem_ld32(t0 + (uint32_t)((c + 2) * 32), ra);
-                Epi::consume(ep, st, row, tn * BN + (c + 1) * 32, rb, stage);
+                for (int c = 0; c < BN / 32; ++c) Epi::consume(ep, st, row, tn * BN + c * 32, ra, stage);
+            } else {
+                tmem_ld32(t0, ra);
+                Epi::begin(ep, st, row, tn);   // its global loads overlap the first TMEM load
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; c += 2) {
+                    tmem_wait_ld(ra);
+                    tmem_ld32(t0 + (uint32_t)((c + 1) * 32), rb);
+                    Epi::consume(ep, st, row, tn * BN + c * 32, ra, stage);
+                    tmem_wait_ld(rb);
+                    if (c + 2 < BN / 32) tmem_ld32(t0 + (uint32_t)((c + 2) * 32), ra);
+                    Epi::consume(ep, st, row, tn * BN + (c + 1) * 32, rb, stage);
+                }
             }
             Epi::end(ep, st, row, tn);
             tc_fence_before();
