@@ -413,3 +413,23 @@ def linear_ce_filtered(E, W, labels, eps, reduction="mean", grad_output=1.0, ign
     r["dW"] = Gf.T @ E
     r["keep"], r["block_pmax"], r["block_target"] = keep, pmax, has_t
     return r
+
+
+def filter_blocks_columns(E, W, labels, fwd, cols, eps, block=128, ignore_index=IGNORE_INDEX):
+    """The filter's keep decision for one column block -- `cols`, the columns of that block --
+    in every row block, from the row forward `fwd` of the whole matrix (linear_ce_row_forward):
+    the column-sampled form of filter_blocks, for matrices too large to form z."""
+    E = np.asarray(E, np.float64)
+    z = E @ np.asarray(W, np.float64)[cols].T                      # [T, len(cols)]
+    labels = np.asarray(labels, np.int64)
+    valid = fwd["valid"]
+    L = fwd["lse_nt"]
+    live = valid & np.isfinite(L)
+    p = np.zeros_like(z)
+    p[live] = np.exp(z[live] - L[live, None]) * sigmoid(fwd["x"][live])[:, None]
+    tgt = (labels[:, None] == np.asarray(cols)[None, :]) & valid[:, None]
+    p[tgt] = 0.0
+    starts = np.arange(0, z.shape[0], block)
+    pmax = np.maximum.reduceat(p.max(axis=1), starts)
+    has_t = np.logical_or.reduceat(tgt.any(axis=1), starts)
+    return has_t | (pmax >= eps), pmax, has_t

@@ -10,6 +10,10 @@
   bf16 gradient  the device bits equal RNE_bf16(o), o rounded once from fp64, or one of
                  its two bf16 neighbours
   reduced loss   relative 1e-4
+  linear-CE loss the same, plus a per-row slack where the logits are fp32 sums of D bf16
+                 products formed on the tensor cores (tests/test_lce_gpu.z_sum_slack): a
+                 row's loss moves by sigma(x) |dx|, and with a large target margin the loss
+                 is ~e^x, so its relative error is the absolute error of x itself
 """
 import numpy as np
 
@@ -19,13 +23,15 @@ LOSS_RTOL = 1e-4
 G32_ATOL, G32_RTOL = 1e-6, 1e-4
 
 
-def check_loss_rows(got, want, valid, what="loss"):
+def check_loss_rows(got, want, valid, what="loss", slack=None):
     got = np.asarray(got, np.float64)
     want = np.asarray(want, np.float64)
     valid = np.asarray(valid, bool)
     assert np.all(got[~valid] == 0.0) and not np.any(np.signbit(got[~valid])), f"{what}: ignored rows not +0"
     g, w = got[valid], want[valid]
     exempt = (np.abs(w) < 1e-30) & ((g == 0) | (np.abs(g) < np.finfo(np.float32).tiny))
+    if slack is not None:
+        exempt |= np.abs(g - w) <= LOSS_RTOL * np.abs(w) + np.asarray(slack, np.float64)[valid]
     rel = np.abs(g - w) / np.maximum(np.abs(w), 1e-300)
     bad = (~exempt) & ~(rel <= LOSS_RTOL) & ~((g == w) & np.isinf(w))
     assert not bad.any(), (f"{what}: {bad.sum()} rows beyond rel {LOSS_RTOL}; worst rel "
@@ -63,8 +69,8 @@ def bf16_tensor_bits(t):
     return t.detach().view(torch.int16).cpu().numpy().view(np.uint16)
 
 
-def check_reduced(got, want, what="reduced loss"):
+def check_reduced(got, want, what="reduced loss", slack=0.0):
     if np.isnan(want):
         assert np.isnan(got), f"{what}: expected NaN, got {got}"
         return
-    assert abs(got - want) <= LOSS_RTOL * abs(want), f"{what}: {got} vs {want}"
+    assert abs(got - want) <= LOSS_RTOL * abs(want) + slack, f"{what}: {got} vs {want}"

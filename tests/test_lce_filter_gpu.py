@@ -15,7 +15,7 @@ import gen
 from oracle import ce_oracle as O
 from tests import _grading as G
 from tests.test_ce_gpu import vce  # noqa: F401  (fixture)
-from tests.test_lce_gpu import dev_bf16, grade_sum, host
+from tests.test_lce_gpu import dev_bf16, grade_sum, host, z_sum_slack
 from tests.test_oracle_filter import _eps_in_a_gap
 
 pytestmark = pytest.mark.gpu
@@ -110,3 +110,53 @@ def test_invalid_eps_is_refused(vce, eps):
     labels = torch.from_numpy(p.labels).cuda()
     with pytest.raises(vce.VceError):
         vce.linear_ce_fwd_bwd_filtered(dev_bf16(Eb), dev_bf16(Wb), labels, eps)
+
+
+def test_full_size_peaked_sampled(vce):
+    """E [8192, 4096] aligned with the targets, W [128256, 4096], eps = 2^-12, the launch the
+    bench times: every loss row; dE rows of two whole 128-row blocks and dW rows of two
+    128-column blocks against the filtered oracle, keep decisions from z in fp64 (none of
+    them within a factor 2 of eps)."""
+    p = gen.linear_peaked()
+    Wb = p.W()
+    Eb = p.E(W=Wb)
+    eps = 2.0 ** -12
+    labels = torch.from_numpy(p.labels).cuda()
+    lo, lr, dE, dW, st, kept = vce.linear_ce_fwd_bwd_filtered(dev_bf16(Eb), dev_bf16(Wb), labels, eps)
+    torch.cuda.synchronize()
+    assert vce.vce_get_status(st) == 0
+    E, W = O.widen(Eb, "bf16"), O.widen(Wb, "bf16")
+    fwd = O.linear_ce_row_forward(E, W, p.labels, block=512)
+    # losses ~e^-21: their relative error is the absolute error of x, which the fp32 sums of
+    # 4096 products forming z carry (z_t ~ 24); z_sum_slack bounds it
+    slack = z_sum_slack(E, W, p.labels, fwd)
+    G.check_loss_rows(lr.cpu().numpy(), fwd["loss"], fwd["valid"], "full-size loss rows", slack=slack)
+    N = int(fwd["valid"].sum())
+    G.check_reduced(lo.item(), float(fwd["loss"][fwd["valid"]].sum()) / N, slack=float(slack.sum()) / N)
+    c = O.row_scale(fwd["valid"], "mean", 1.0)
+    rng = np.random.default_rng(9)
+    aW = np.abs(W)
+    kept_rows = []
+    for rb in (3, 41):   # dE: whole row blocks, so the keep decisions are those of the full matrix
+        rows = np.arange(128 * rb, 128 * rb + 128)
+        z = E[rows] @ W.T
+        keep, pmax, _ = O.filter_blocks(z, p.labels[rows], eps, 128)
+        assert np.all((pmax < eps / 2) | (pmax > 2 * eps))
+        kept_rows.append(int(keep.sum()))
+        sub = {k: v[rows] for k, v in fwd.items()}
+        Gr = O.ce_grad_rows(z, p.labels[rows], sub, c[rows])
+        Gf = np.where(np.repeat(keep[0], 128)[None, :p.V], Gr, 0.0)
+        pick = np.sort(rng.choice(128, 24, replace=False))
+        grade_sum(host(dE[torch.from_numpy(rows[pick]).cuda()]), Gf[pick] @ W, np.abs(Gf[pick]) @ aW,
+                  f"full-size dE rows of block {rb}")
+    assert 0 < min(kept_rows) and max(kept_rows) < -(-p.V // 128)
+    for cb in (int(p.labels[p.labels >= 0][0]) // 128, 7):   # a block holding a target, and block 7
+        cols = np.arange(128 * cb, min(128 * cb + 128, p.V))
+        keep, pmax, _ = O.filter_blocks_columns(E, W, p.labels, fwd, cols, eps, 128)
+        assert np.all((pmax < eps / 2) | (pmax > 2 * eps))
+        Gc = O.linear_ce_grad_columns(E, W, p.labels, fwd, c, cols)
+        Gf = np.where(np.repeat(keep, 128)[:p.T, None], Gc, 0.0)
+        pick = np.sort(rng.choice(len(cols), 16, replace=False))
+        grade_sum(host(dW[torch.from_numpy(cols[pick]).cuda()]), Gf[:, pick].T @ E, np.abs(Gf[:, pick]).T @ np.abs(E),
+                  f"full-size dW rows of column block {cb}")
+    assert 0 < int(kept.item()) < -(-p.T // 128) * -(-p.V // 128)

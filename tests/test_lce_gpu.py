@@ -45,6 +45,17 @@ def grade_sum(got, want, abs_terms, what):
     return info
 
 
+def z_sum_slack(E, W, labels, fwd):
+    """Per-row loss slack for logits formed as fp32 sums of D products: x = L' - z_t moves by
+    at most 2^-14 (sum_d |E_id W_td| + ||E_i|| max_j ||W_j||) (the first term bounds z_t's sum,
+    the second, by Cauchy-Schwarz, every z_j's and so L'), and the loss by sigma(x) times that."""
+    valid = fwd["valid"]
+    t = np.where(valid, np.asarray(labels), 0)
+    a_t = np.einsum("ij,ij->i", np.abs(E), np.abs(W[t]))
+    a_nt = np.linalg.norm(E, axis=1) * np.linalg.norm(W, axis=1).max()
+    return np.where(valid, SUM_ATOL_REL * O.sigmoid(fwd["x"]) * (a_t + a_nt), 0.0)
+
+
 def run_lce(vce, p, reduction="mean", grad_output=1.0, grad_dtype=torch.bfloat16):
     Eb, Wb = p.E(), p.W()
     E, W = dev_bf16(Eb), dev_bf16(Wb)

@@ -123,6 +123,23 @@ def test_dropped_entries_bound_the_change():
     assert np.abs(f["dW"] - r["dW"]).max() > 0   # filtering did change something
 
 
+def test_column_sampled_decisions_match_the_full_ones():
+    """filter_blocks_columns (one column block at a time, from the row forward) gives the
+    column of filter_blocks' keep table for every column block, ragged last block included."""
+    p, E, W = _problem(100, 12, 70, 25, n_ignore=4, peak=4.0, w_std=0.5)
+    fwd = O.linear_ce_row_forward(E, W, p.labels, block=32)
+    z = E @ W.T
+    probe, pm, _ = O.filter_blocks(z, p.labels, 2.0, block=16)
+    eps = _eps_in_a_gap(pm, 0.5)
+    keep, pmax, has_t = O.filter_blocks(z, p.labels, eps, block=16)
+    assert 0 < keep.sum() < keep.size
+    for cb in range(keep.shape[1]):
+        cols = np.arange(16 * cb, min(16 * cb + 16, 70))
+        k, m, h = O.filter_blocks_columns(E, W, p.labels, fwd, cols, eps, block=16)
+        assert np.array_equal(k, keep[:, cb]) and np.array_equal(h, has_t[:, cb])
+        np.testing.assert_allclose(m, pmax[:, cb], rtol=1e-12, atol=0)
+
+
 # ---------------------------------------------------------------- planted mistakes
 
 def _must_fail(*checks):
