@@ -271,36 +271,49 @@ struct EpiKahan {
         if (row >= p.rows || col0 >= p.cols) return;
         const int64_t base = (int64_t)row * p.cols + col0;
         if (p.cols - col0 >= 32) {   // full 32-column piece: 16-byte accesses
+            // four groups' loads are issued before their stores: the stores go to the same
+            // arrays, so loads interleaved with them would each wait out a memory latency
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                float s[4], c[4];
-                const float x[4] = {__uint_as_float(acc[4 * q]), __uint_as_float(acc[4 * q + 1]),
-                                    __uint_as_float(acc[4 * q + 2]), __uint_as_float(acc[4 * q + 3])};
-                if (p.first) {
+            for (int q0 = 0; q0 < 8; q0 += 4) {
+                float4 ld_a[4], ld_k[4];
+                if (!p.first) {
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) { s[e] = x[e]; c[e] = 0.f; }
-                } else {
-                    const float4 a = *reinterpret_cast<const float4*>(p.sum + base + 4 * q);
-                    const float4 k = *reinterpret_cast<const float4*>(p.comp + base + 4 * q);
-                    const float av[4] = {a.x, a.y, a.z, a.w}, kv[4] = {k.x, k.y, k.z, k.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        float err;
-                        two_sum(av[e], x[e], s[e], err);
-                        c[e] = kv[e] + err;
+                    for (int q = 0; q < 4; ++q) {
+                        ld_a[q] = *reinterpret_cast<const float4*>(p.sum + base + 4 * (q0 + q));
+                        ld_k[q] = *reinterpret_cast<const float4*>(p.comp + base + 4 * (q0 + q));
                     }
                 }
-                if (p.last) {
-                    if (p.bf16) {
-                        uint2 w = make_uint2(pack_bf16x2(s[0] + c[0], s[1] + c[1]), pack_bf16x2(s[2] + c[2], s[3] + c[3]));
-                        *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(p.out) + base + 4 * q) = w;
+#pragma unroll
+                for (int q = q0; q < q0 + 4; ++q) {
+                    float s[4], c[4];
+                    const float x[4] = {__uint_as_float(acc[4 * q]), __uint_as_float(acc[4 * q + 1]),
+                                        __uint_as_float(acc[4 * q + 2]), __uint_as_float(acc[4 * q + 3])};
+                    if (p.first) {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) { s[e] = x[e]; c[e] = 0.f; }
                     } else {
-                        *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + base + 4 * q) =
-                            make_float4(s[0] + c[0], s[1] + c[1], s[2] + c[2], s[3] + c[3]);
+                        const float av[4] = {ld_a[q - q0].x, ld_a[q - q0].y, ld_a[q - q0].z, ld_a[q - q0].w};
+                        const float kv[4] = {ld_k[q - q0].x, ld_k[q - q0].y, ld_k[q - q0].z, ld_k[q - q0].w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            float err;
+                            two_sum(av[e], x[e], s[e], err);
+                            c[e] = kv[e] + err;
+                        }
                     }
-                } else {
-                    *reinterpret_cast<float4*>(p.sum + base + 4 * q) = make_float4(s[0], s[1], s[2], s[3]);
-                    *reinterpret_cast<float4*>(p.comp + base + 4 * q) = make_float4(c[0], c[1], c[2], c[3]);
+                    if (p.last) {
+                        if (p.bf16) {
+                            uint2 w = make_uint2(pack_bf16x2(s[0] + c[0], s[1] + c[1]),
+                                                 pack_bf16x2(s[2] + c[2], s[3] + c[3]));
+                            *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(p.out) + base + 4 * q) = w;
+                        } else {
+                            *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + base + 4 * q) =
+                                make_float4(s[0] + c[0], s[1] + c[1], s[2] + c[2], s[3] + c[3]);
+                        }
+                    } else {
+                        *reinterpret_cast<float4*>(p.sum + base + 4 * q) = make_float4(s[0], s[1], s[2], s[3]);
+                        *reinterpret_cast<float4*>(p.comp + base + 4 * q) = make_float4(c[0], c[1], c[2], c[3]);
+                    }
                 }
             }
             return;
