@@ -167,13 +167,15 @@ struct EpiGrad {
         // A target column in the piece keeps its block anyway (begin), so including its
         // value in emax changes nothing.
         if (p.keep_w && !r.zero && emax >= r.thr) r.bits |= 1u << ((col0 % BN) >> 7);
-        // row-major [T_pad][ldg]: 64 contiguous bytes per thread
+        // row-major [T_pad][ldg]: 64 contiguous bytes per thread.  Evict-first stores: the
+        // chunk's G (512 MB at T = 8192) is read back from DRAM by the next two GEMMs anyway,
+        // and should not push E and W out of L2 meanwhile (measured 0.4% faster per call).
         uint4* dh = reinterpret_cast<uint4*>(p.g_hi + (int64_t)row * p.ldg + col0);
         uint4* dl = reinterpret_cast<uint4*>(p.g_lo + (int64_t)row * p.ldg + col0);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            dh[q] = make_uint4(hi[4 * q], hi[4 * q + 1], hi[4 * q + 2], hi[4 * q + 3]);
-            dl[q] = make_uint4(lo[4 * q], lo[4 * q + 1], lo[4 * q + 2], lo[4 * q + 3]);
+            st_stream16(dh + q, make_uint4(hi[4 * q], hi[4 * q + 1], hi[4 * q + 2], hi[4 * q + 3]));
+            st_stream16(dl + q, make_uint4(lo[4 * q], lo[4 * q + 1], lo[4 * q + 2], lo[4 * q + 3]));
         }
     }
     __device__ __forceinline__ static void end(const Params& p, Row& r, int row, int tn) {
@@ -193,7 +195,8 @@ struct EpiGrad {
     }
 };
 
-// Step 2b: dW rows of the chunk, stored once (bf16 round-to-nearest-even or fp32).
+// Step 2b: dW rows of the chunk, stored once (bf16 round-to-nearest-even or fp32), evict-first:
+// nothing in the call reads them back.
 struct EpiStore {
     struct Params {
         void* out;
@@ -214,7 +217,7 @@ struct EpiStore {
                 for (int k = 0; k < 16; ++k) w[k] = pack_bf16x2(__uint_as_float(acc[2 * k]), __uint_as_float(acc[2 * k + 1]));
                 uint4* d = reinterpret_cast<uint4*>(o);
 #pragma unroll
-                for (int q = 0; q < 4; ++q) d[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+                for (int q = 0; q < 4; ++q) st_stream16(d + q, make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]));
             } else {
 #pragma unroll
                 for (int k = 0; k < 32; ++k)
@@ -225,7 +228,8 @@ struct EpiStore {
             if (n == 32) {
                 uint4* d = reinterpret_cast<uint4*>(o);
 #pragma unroll
-                for (int q = 0; q < 8; ++q) d[q] = make_uint4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
+                for (int q = 0; q < 8; ++q)
+                    st_stream16(d + q, make_uint4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]));
             } else {
 #pragma unroll
                 for (int k = 0; k < 32; ++k)
