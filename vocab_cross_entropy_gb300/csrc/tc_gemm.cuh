@@ -16,6 +16,9 @@
 // tile i+1.  Shared-memory tiles use the 128-byte swizzle that TMA writes and the MMA
 // descriptors read.  Every wait is bounded: a wait that exceeds kWaitNs sets an error
 // code, every role stops, in-flight copies are drained (bounded) and TMEM is released.
+// Two options: a launch as 2-CTA clusters whose CTAs share each B tile through TMA multicast
+// (kPair), and K-block skipping from a per-tile bit table (GemmArgs::skip, gradient
+// filtering), which visits only the K blocks whose bits are set.
 #pragma once
 
 #include <cuda.h>
