@@ -293,9 +293,16 @@ BWD_RING_FILES = ["vocab_cross_entropy_gb300/csrc/ce_bwd_ring.cu", "vocab_cross_
                   "vocab_cross_entropy_gb300/csrc/vce_device.cuh", "vocab_cross_entropy_gb300/csrc/vce_async.cuh"]
 
 
-def forward_kernel(V):
-    """The kernel ce_forward runs for contiguous, 16-byte aligned [T, V] logits."""
-    return "k_ce_fwd_ring" if V % 8 == 0 else "k_ce_fwd"
+def forward_kernel(V, T=None, es=2):
+    """The kernel ce_forward runs for contiguous, 16-byte aligned [T, V] logits: the ring, except
+    for rows of 32-64 KB with fewer than 64 per SM (and layouts the ring does not take)."""
+    if V % 8:
+        return "k_ce_fwd"
+    if T is not None and 32768 < V * es <= 65536:
+        sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+        if T < 64 * sms:
+            return "k_ce_fwd"
+    return "k_ce_fwd_ring"
 
 
 FWD_RING_FILES = ["vocab_cross_entropy_gb300/csrc/ce_fwd_ring.cu", "vocab_cross_entropy_gb300/csrc/ce_stage.cuh",
@@ -669,7 +676,7 @@ def run_ours(args, rank, local_rank, world):
                                "traffic": (profiled_traffic("k_ce_fused_ring_pages", RING_FILES)
                                            if captured_shape(w) and one_pass_kernel(w.p.V) == "k_ce_fused_ring"
                                            else None)}
-        fkern = forward_kernel(w.p.V)
+        fkern = forward_kernel(w.p.V, w.p.T, w.es)
         out["roofline_fwd"] = {"bound": "hbm", "kernel": fkern + " + k_ce_reduce (the ce_forward call)",
                                "achieved": round(w.bytes_fwd() / (fwd_ms / 1e3) / 1e9, 1), "peak": peaks["hbm_gbs"],
                                "unit": "GB/s",

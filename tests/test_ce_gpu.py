@@ -421,3 +421,27 @@ def test_backward_ring_padded_gradient(vce, dtype, gdt):
     ign = torch.from_numpy(p.labels == p.ignore_index).cuda()
     g = gbuf[:, :5000][ign].float()
     assert torch.all(g == 0) and not torch.any(torch.signbit(g))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_empty_batch(vce, dtype):
+    """T = 0 rows through every CE entry point: the calls succeed, MEAN is 0/0 = NaN, SUM is 0,
+    the status word is 0 (reading: mean over N = 0 rows, as torch)."""
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    logits = torch.empty(0, 1000, dtype=tdt, device="cuda")
+    labels = torch.empty(0, dtype=torch.int64, device="cuda")
+    for red, want in (("mean", None), ("sum", 0.0)):
+        loss_out, loss_rows, stats, status = vce.ce_forward(logits, labels, -100, red)
+        go = torch.ones(1, device="cuda")
+        grad = vce.ce_backward(logits, labels, stats, go, -100, red)
+        lo2, lr2, st2, g2, s2 = vce.ce_forward_backward(logits, labels, -100, red, grad_output=go)
+        chunks = [torch.empty(0, 300, dtype=tdt, device="cuda"), torch.empty(0, 700, dtype=tdt, device="cuda")]
+        lo3, lr3, st3, g3, cs3, s3 = vce.ce_merge_chunks(chunks, labels, -100, red, grad_output=go)
+        torch.cuda.synchronize()
+        for lo, s in ((loss_out, status), (lo2, s2), (lo3, s3)):
+            assert vce.vce_get_status(s) == 0
+            if want is None:
+                assert np.isnan(lo.item())
+            else:
+                assert lo.item() == want
+        assert grad.shape == (0, 1000) and g2.shape == (0, 1000) and [g.shape for g in g3] == [(0, 300), (0, 700)]

@@ -296,10 +296,16 @@ extern "C" int ce_forward_ls(const void* logits, vce_dtype dt, int64_t T, int64_
     if (cudaMemsetAsync(status, 0, sizeof(int32_t), s) != cudaSuccess) return VCE_ERR_CUDA;
     if (T > 0) {
         // Rows streamed through shared memory where the layout allows it, else one block per
-        // row with loads from global memory.
+        // row with loads from global memory.  Rows of 32-64 KB with fewer than 64 per SM also
+        // take the per-block kernel: the ring's ramp and tail then weigh more than its
+        // streaming gains (measured at 4096 x 32000 bf16: 0.0631 against 0.0713 ms; at
+        // 15624 x 32000 the two are equal, and longer rows favour the ring).
         bool launched = false;
-        cudaError_t e = launch_fwd_ring(dt, logits, T, V, ld, labels, ignore_index, label_smoothing, loss_rows,
-                                        row_stats, status, s, &launched);
+        const int64_t row_bytes = V * (int64_t)es;
+        const bool few_short_rows = row_bytes > 32768 && row_bytes <= 65536 && T < 64 * (int64_t)device_sm_count();
+        cudaError_t e = few_short_rows ? cudaSuccess
+                                       : launch_fwd_ring(dt, logits, T, V, ld, labels, ignore_index, label_smoothing,
+                                                         loss_rows, row_stats, status, s, &launched);
         if (e == cudaSuccess && !launched) {
             const int nt = pick_threads(V * (int64_t)es);
             e = dt == VCE_BF16 ? dispatch_fwd<uint16_t>(nt, logits, T, V, ld, labels, ignore_index, label_smoothing,
