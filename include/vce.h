@@ -117,8 +117,9 @@ int vce_get_status(const int32_t* status, vce_stream_t s, int32_t* host_out);
  *   status     [1] int32, set to 0 by this call, VCE_ERR_LABEL on a bad label, or
  *              105 / 106 / 108 / 110 when a bounded device-side wait gave up after 2 s
  *              (rows of 16-byte multiples stream through a shared-memory stage ring:
- *              free stage, loaded stage, warp partials, free statistics slots); the
- *              outputs are then undefined
+ *              free stage, loaded stage, warp partials, free statistics slots; rows of
+ *              32-64 KB with fewer than 64 rows per SM take a per-block kernel instead,
+ *              which has no such waits); the outputs are then undefined
  */
 int ce_forward(const void* logits, vce_dtype dt, int64_t T, int64_t V, int64_t ld,
                const int64_t* labels, int64_t ignore_index, vce_reduction red,
