@@ -19,6 +19,7 @@
 #include <mutex>
 
 #include "vce.h"
+#include "vce_host.h"
 
 namespace {
 
@@ -26,14 +27,13 @@ namespace {
 constexpr long long kScratchEntries = VCE_NOALLOC_MAX_CHUNK_ROWS;
 static __device__ __align__(256) float4 g_chunk_stats_scratch[kScratchEntries];
 
-constexpr int kMaxDevices = 64;
-float* g_scratch_addr[kMaxDevices];   // device address of the array on each device, once known
+float* g_scratch_addr[vce::kMaxDevices];   // device address of the array on each device, once known
 std::mutex g_scratch_mu;
 
 // The array's device address on the current device; the first call for a device looks it up.
 int scratch_address(float** out) {
     int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return VCE_ERR_CUDA;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= vce::kMaxDevices) return VCE_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_scratch_mu);
     if (!g_scratch_addr[dev]) {
         void* p = nullptr;

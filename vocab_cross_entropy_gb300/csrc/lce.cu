@@ -369,7 +369,6 @@ bool make_map(CUtensorMap* m, const void* base, int64_t inner, int64_t outer, in
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-constexpr int kMaxDevices = 64;
 
 // Clusters of two CTAs that fit on the device at once, queried once per device and kernel
 // (0: none fit, the caller then launches single CTAs).

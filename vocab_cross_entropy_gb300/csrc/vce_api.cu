@@ -10,7 +10,6 @@
 namespace vce {
 
 namespace {
-constexpr int kMaxDevices = 64;
 std::atomic<int> g_sms[kMaxDevices];
 std::atomic<int> g_arch[kMaxDevices];   // 0 unknown, 1 ok, -1 not sm_100-family
 

@@ -18,6 +18,10 @@ inline bool fits_bytes(int64_t rows, int64_t ld, size_t esize) {
     return ld <= lim / rows;
 }
 
+// Per-device caches hold this many devices; calls on a device beyond it report an error
+// (or skip the cached fast path where one exists).
+constexpr int kMaxDevices = 64;
+
 int device_sm_count();     // SMs of the current device (cached per device)
 int require_sm100();       // VCE_OK when the current device is an sm_100-family GPU
 
