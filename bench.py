@@ -309,6 +309,12 @@ FWD_RING_FILES = ["vocab_cross_entropy_gb300/csrc/ce_fwd_ring.cu", "vocab_cross_
                   "vocab_cross_entropy_gb300/csrc/vce_device.cuh", "vocab_cross_entropy_gb300/csrc/vce_async.cuh"]
 
 
+CHUNK_FILES = ["vocab_cross_entropy_gb300/csrc/ce_fwd.cu", "vocab_cross_entropy_gb300/csrc/ce_rows.cuh",
+               "vocab_cross_entropy_gb300/csrc/ce_bwd_ring.cu", "vocab_cross_entropy_gb300/csrc/ce_stage.cuh",
+               "vocab_cross_entropy_gb300/csrc/ce_segments.h", "vocab_cross_entropy_gb300/csrc/vce_device.cuh",
+               "vocab_cross_entropy_gb300/csrc/vce_async.cuh"]
+
+
 def one_pass_kernel(V):
     """The kernel ce_forward_backward runs for contiguous, 16-byte aligned [T, V] buffers."""
     return "k_ce_fused_ring" if V % 8 == 0 else "k_ce_fused"
@@ -638,7 +644,9 @@ def run_ours(args, rank, local_rank, world):
                                           + ("k_ce_bwd_ring" if ring else "k_ce_bwd") + ")",
                 "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": round(achieved / peaks["hbm_gbs"], 4), "peak_source": peaks["source"],
-                "algorithmic_bytes_per_launch": call_bytes, "traffic": None}
+                "algorithmic_bytes_per_launch": call_bytes,
+                "traffic": (profiled_traffic("ce_merge_chunks_pages", CHUNK_FILES)
+                            if args.workload == "chunked" and ring and captured_shape(w) else None)}
     else:
         achieved = bwd_bytes / (bwd_ms / 1e3) / 1e9
         bkern = backward_kernel(w.p.V)
