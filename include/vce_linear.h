@@ -110,6 +110,20 @@ int vce_gemm_bf16(const void* A, int a_mn, const void* B, int b_mn, int64_t M, i
 int vce_test_gemm_stall(const void* A, const void* B, int64_t M, int64_t N, int64_t K, float* C,
                         uint64_t wait_ns, int32_t* status, vce_stream_t s);
 
+/*
+ * vce_test_gemm_skip -- test hook for the GEMM's K-block skipping (no page counterpart; the
+ * machinery gradient filtering uses).  As vce_gemm_bf16 with A [M, K], B [N, K] K-major, C
+ * [M, N] fp32, except that M tile i (128 rows) adds only the 128-column K blocks b whose bit
+ * b % 32 of skip[i * skip_ld + b / 32] is set:
+ *     C[m][n] = sum over set blocks b of sum_{k in block b} A[m][k] B[n][k]
+ * (0 where a tile has no set bit).  skip: device uint32 [ceil(M/128)][skip_ld], skip_ld >=
+ * ceil(ceil(K/128) / 32).  pair = 1 runs the tiles as 2-CTA clusters sharing B (both CTAs
+ * load the union of their blocks, each multiplies its own); it needs an even number of M
+ * tiles.  Bad pair or skip_ld: VCE_ERR_ARG.
+ */
+int vce_test_gemm_skip(const void* A, const void* B, int64_t M, int64_t N, int64_t K, const uint32_t* skip,
+                       int64_t skip_ld, int pair, float* C, vce_stream_t s);
+
 #ifdef __cplusplus
 }
 #endif

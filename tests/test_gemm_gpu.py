@@ -52,3 +52,43 @@ def test_stalled_pipeline_gives_up_and_the_context_survives(vce):
     want = A64 @ B64.T
     bound = 2.0 ** -20 * (np.abs(A64) @ np.abs(B64).T) + 1e-30
     assert np.all(np.abs(C.cpu().numpy().astype(np.float64) - want) <= bound)
+
+
+@pytest.mark.parametrize("pair", [False, True])
+@pytest.mark.parametrize("M,N,K", [(512, 512, 1000), (1024, 256, 4160)])
+def test_k_block_skipping(vce, pair, M, N, K):
+    """The K-block skipping gradient filtering rides on, against float64: each 128-row M tile
+    adds only the 128-column K blocks whose bit is set (a ragged last block included); one tile
+    keeps none (its accumulator is never written: zeros), one keeps all.  pair: the same on
+    2-CTA clusters, where both CTAs load the union of their blocks and each multiplies its own."""
+    rng = np.random.default_rng(M + K + pair)
+    A, A64 = _bf16(rng, (M, K))
+    B, B64 = _bf16(rng, (N, K), 0.05)
+    tiles, nblk = -(-M // 128), -(-K // 128)
+    words = -(-nblk // 32) + 1   # one spare word: rows may be longer than needed
+    keep = rng.random((tiles, nblk)) < 0.4
+    keep[1] = False
+    keep[2] = True
+    bits = np.zeros((tiles, words), np.uint32)
+    for t in range(tiles):
+        for b in np.nonzero(keep[t])[0]:
+            bits[t, b // 32] |= np.uint32(1) << np.uint32(b % 32)
+    C = vce.vce_test_gemm_skip(A.cuda(), B.cuda(), torch.from_numpy(bits.view(np.int32)).cuda(), pair)
+    torch.cuda.synchronize()
+    kmask = np.repeat(keep, 128, axis=1)[:, :K]                    # [tiles, K]
+    Am = A64 * np.repeat(kmask, 128, axis=0)[:M]                   # dropped blocks of each tile zeroed
+    want = Am @ B64.T
+    bound = 2.0 ** -20 * (np.abs(Am) @ np.abs(B64).T) + 1e-30
+    got = C.cpu().numpy().astype(np.float64)
+    assert np.all(got[128:256] == 0.0), "a tile with no kept block must be zero"
+    assert np.all(np.abs(got - want) <= bound), f"max err/bound {np.max(np.abs(got - want) / bound):.3g}"
+
+
+def test_k_block_skipping_refuses_bad_arguments(vce):
+    A = torch.zeros(384, 128, dtype=torch.bfloat16, device="cuda")   # 3 M tiles: no pairs
+    B = torch.zeros(256, 128, dtype=torch.bfloat16, device="cuda")
+    bits = torch.zeros(3, 1, dtype=torch.int32, device="cuda")
+    with pytest.raises(vce.VceError):
+        vce.vce_test_gemm_skip(A, B, bits, True)
+    with pytest.raises(vce.VceError):
+        vce.vce_test_gemm_skip(A, B, torch.zeros(3, 0, dtype=torch.int32, device="cuda"), False)

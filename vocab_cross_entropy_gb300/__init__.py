@@ -69,6 +69,9 @@ def _load():
         L.vce_gemm_bf16.restype = i32
         L.vce_test_gemm_stall.argtypes = [p, p, i64, i64, i64, p, ctypes.c_uint64, p, p]
         L.vce_test_gemm_stall.restype = i32
+        if hasattr(L, "vce_test_gemm_skip"):
+            L.vce_test_gemm_skip.argtypes = [p, p, i64, i64, i64, p, i64, i32, p, p]
+            L.vce_test_gemm_skip.restype = i32
         L.vce_test_ce_fused_stall.argtypes = [p, i64, i64, p, p, p, p, p, ctypes.c_uint64, p, p]
         L.vce_test_ce_fused_stall.restype = i32
     for name in ("ce_forward", "ce_backward", "ce_forward_ls", "ce_backward_ls", "ce_forward_backward",
@@ -334,6 +337,17 @@ def vce_test_gemm_stall(A, B, wait_ns=50_000_000, *, stream=None):
     _check("vce_test_gemm_stall", _get().vce_test_gemm_stall(_ptr(A), _ptr(B), M, N, K, _ptr(C), int(wait_ns),
                                                           _ptr(status), _stream(stream)))
     return vce_get_status(status, stream)
+
+
+def vce_test_gemm_skip(A, B, skip_bits, pair=False, *, stream=None):
+    """C = A B^T over the 128-column K blocks whose bit is set for each 128-row M tile;
+    skip_bits an int32 device tensor [ceil(M/128), words]; pair runs 2-CTA clusters."""
+    M, K = A.shape
+    N = B.shape[0]
+    C = torch.empty(M, N, dtype=torch.float32, device=A.device)
+    _check("vce_test_gemm_skip", _get().vce_test_gemm_skip(_ptr(A), _ptr(B), M, N, K, _ptr(skip_bits),
+                                                        skip_bits.shape[1], int(pair), _ptr(C), _stream(stream)))
+    return C
 
 
 def vce_test_ce_fused_stall(logits, labels, wait_ns=50_000_000, *, stream=None):

@@ -405,11 +405,13 @@ int pair_clusters(K kern) {
 // skip K blocks (gradient filtering) also run one CTA per SM: a pair loads the union of both
 // tiles' K blocks, and with sparse tiles that costs more than the shared B tile saves
 // (measured 22.77 against 21.98 ms for a filtered call keeping 12% of the blocks).
+// pair_mode: -1 the rule above, 0 never pairs, 1 pairs whenever tiles_m is even (skip or not;
+// the test hook uses it to run the pair path with skip bits).
 template <class Epi, bool kAmn = false, bool kBmn = false>
 cudaError_t run_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b, const CUtensorMap& b_half,
-                     const tc::GemmArgs& g, const typename Epi::Params& ep, cudaStream_t s) {
+                     const tc::GemmArgs& g, const typename Epi::Params& ep, cudaStream_t s, int pair_mode = -1) {
     const int64_t tiles = (int64_t)g.tiles_m * g.tiles_n;
-    if (g.tiles_m % 2 == 0 && !g.skip) {
+    if (g.tiles_m % 2 == 0 && (pair_mode == 1 || (pair_mode < 0 && !g.skip))) {
         auto kern = tc::k_tc_gemm<Epi, kAmn, kBmn, true>;
         static bool attr_set = false;   // per process; the attribute is per function, not per device
         if (!attr_set) {
@@ -644,3 +646,26 @@ extern "C" int linear_ce_fwd_bwd(const void* E, const void* W, int64_t T, int64_
     return linear_ce_fwd_bwd_filtered(E, W, T, D, V, labels, ignore_index, red, grad_output, loss_rows, loss_out, dE,
                                       dW, grad_dt, 0.f, nullptr, workspace, workspace_bytes, status, s);
 }
+
+extern "C" int vce_test_gemm_skip(const void* A, const void* B, int64_t M, int64_t N, int64_t K, const uint32_t* skip,
+                                  int64_t skip_ld, int pair, float* C, vce_stream_t s) {
+    if (!A || !B || !C || !skip) return VCE_ERR_NULL;
+    if (M < 1 || N < 1 || K < 1 || (M % 8) || (N % 8) || (K % 8) || M > (1 << 20) || N > (1 << 20) || K > (1 << 20))
+        return VCE_ERR_SHAPE;
+    const int64_t tiles_m = cdiv(M, BM);
+    if (skip_ld < cdiv(cdiv(K, 128), 32) || skip_ld > (1 << 20)) return VCE_ERR_ARG;
+    if (pair != 0 && (pair != 1 || tiles_m % 2)) return VCE_ERR_ARG;
+    if (!aligned(A, 16) || !aligned(B, 16) || !aligned(C, 16) || !aligned(skip, 4)) return VCE_ERR_ALIGN;
+    int rc = require_sm100();
+    if (rc) return rc;
+    CUtensorMap ma, mb, mb2;
+    if (!make_map(&ma, A, K, M, K, BM) || !make_map(&mb, B, K, N, K, BN) || !make_map(&mb2, B, K, N, K, BN / 2))
+        return VCE_ERR_CUDA;
+    const int nk = (int)cdiv(K, BK);
+    tc::GemmArgs g{(int)tiles_m, (int)cdiv(N, BN), nk, nk, 0, 0, 0, 0, nullptr};
+    g.skip = skip;
+    g.skip_ld = (int)skip_ld;
+    EpiStore::Params ep{C, N, M, N, 0, 0};
+    return run_gemm<EpiStore>(ma, ma, mb, mb2, g, ep, s, pair) == cudaSuccess ? VCE_OK : VCE_ERR_CUDA;
+}
+
