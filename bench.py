@@ -406,7 +406,7 @@ class LinearWorkload:
         self.status = torch.empty(1, dtype=torch.int32, device=device)
         self.go = torch.ones(1, dtype=torch.float32, device=device)
         self.loss_host = torch.empty(1, dtype=torch.float32, pin_memory=True)
-        nchunks = -(-V // 16384)
+        nchunks = -(-V // 32768)
         self.launches_per_step = 3 + 3 * nchunks     # statistics GEMM + merge + reduce, 3 GEMMs per chunk
 
     def step(self, stream):

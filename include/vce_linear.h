@@ -24,7 +24,7 @@ extern "C" {
 /*
  * Bytes of workspace linear_ce_fwd_bwd needs for these sizes; 0 if the sizes are
  * invalid (T, V >= 1; D >= 8 and a multiple of 8).  For T=8192, D=4096, V=128256 it is
- * about 0.87 GB (per-tile statistics, one 16384-column vocabulary chunk of the gradient as
+ * about 1.41 GB (per-tile statistics, one 32768-column vocabulary chunk of the gradient as
  * two bf16 halves, the compensated dE accumulator pair, and the gradient-filter bit tables
  * of one chunk).
  */

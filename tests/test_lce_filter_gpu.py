@@ -37,12 +37,12 @@ def _run(vce, Eb, Wb, p, eps, reduction="mean", grad_dtype=torch.bfloat16):
     return lo, lr, dE, dW, int(kept.item())
 
 
-# T=300: odd row tiles (dE on single CTAs), ragged T and V, most rows ignored so that blocks
-# without a target exist; V=20000: two vocabulary chunks, dE on CTA pairs; V=16768: a second
-# chunk of 384 columns
+# T=300: odd row tiles, ragged T and V, most rows ignored so that blocks without a target
+# exist; V=40000: two vocabulary chunks of the 32768-column chunking; V=33152: a second chunk
+# of 384 columns
 @pytest.mark.parametrize("T,D,V,peak,reduction,n_ignore", [(300, 192, 1000, 8.0, "mean", 280),
-                                                           (512, 128, 20000, 9.0, "sum", 5),
-                                                           (256, 64, 16768, 7.0, "mean", 5)])
+                                                           (384, 128, 40000, 9.0, "sum", 5),
+                                                           (256, 64, 33152, 7.0, "mean", 5)])
 def test_filtered_matches_the_filtered_oracle(vce, T, D, V, peak, reduction, n_ignore):
     p = gen.linear_custom(T, D, V, seed=T + V, n_ignore=n_ignore, e_std=0.5, w_std=0.05, peak=peak)
     Eb, Wb = _inputs(p)

@@ -39,7 +39,7 @@ using tc::BM;
 using tc::BN;
 using tc::BK;
 
-constexpr int64_t kChunkCols = 16384;   // vocabulary columns per gradient chunk (a multiple of BN)
+constexpr int64_t kChunkCols = 32768;   // vocabulary columns per gradient chunk (a multiple of BN)
 
 inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 inline int64_t round_up(int64_t a, int64_t b) { return cdiv(a, b) * b; }
