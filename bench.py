@@ -697,11 +697,61 @@ def run_ours(args, rank, local_rank, world):
         print(json.dumps(out), flush=True)
 
 
+def run_reference_linear(args, world):
+    """The linear-CE oracle (fp64, CPU) on sampled rows: z, loss and G for each row over the whole
+    vocabulary, and its dE row.  W is widened once, outside the timed steps; dW needs every
+    row and is not sampled.  The filtered workload's rows are timed unfiltered (the filter's
+    block decisions need 128 rows of z per sampled row)."""
+    from oracle import ce_oracle as O
+    peaked = args.workload == "linear_peaked"
+    p = gen.linear_peaked() if peaked else gen.linear()
+    if args.vocab:
+        p = gen.LinearProblem(f"{p.name}[V={args.vocab}]", p.T, p.D, args.vocab, p.seed, p.n_ignore, p.e_std,
+                              p.w_std, p.peak)
+    W = O.widen(p.W(), "bf16")
+    N = int(np.sum(p.labels != p.ignore_index))
+    rows_per_step = 2
+    rng = np.random.default_rng(7)
+
+    def one_step():
+        rows = np.sort(rng.choice(p.T, rows_per_step, replace=False))
+        E = O.widen(p.E_rows(rows), "bf16")
+        z = E @ W.T
+        fwd = O.ce_rows(z, p.labels[rows])
+        G = O.ce_grad_rows(z, p.labels[rows], fwd, O.row_scale(fwd["valid"], "sum", 1.0 / N))
+        return G @ W
+
+    for _ in range(args.warmup):
+        one_step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        one_step()
+    dt = time.perf_counter() - t0
+    value = rows_per_step * args.steps / dt
+    eps = args.filter_eps if args.filter_eps is not None else (2.0 ** -12 if peaked else 0.0)
+    metric = ("fused linear-CE fwd+bwd tokens/s at T=8192, D=4096, V=128256 bf16"
+              + (f", gradient filtering at eps={eps:.3g}" if eps > 0 else "") + "; TFLOP/s vs bf16 peak")
+    sample = (f"{rows_per_step} random rows per step: z over all {p.V} columns, loss, G and the dE row, "
+              f"fp64 numpy" + (", unfiltered" if eps > 0 else ""))
+    print(json.dumps({
+        "impl": "reference", "metric": metric, "value": round(value, 3), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{p.name}: fused linear-CE T={p.T} D={p.D} V={p.V}, {rows_per_step} sampled rows "
+                               "per step", "T": p.T, "D": p.D, "V": p.V},
+        "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
 def run_reference(args, rank, world):
     """The oracle (fp64, CPU) as the reference arm: rank 0 alone, bounded samples per step."""
     if rank != 0:
         return
-    problem = {"pages": gen.pages, "mid": gen.mid}[args.workload]()
+    if args.workload in ("linear", "linear_peaked"):
+        return run_reference_linear(args, world)
+    # the one-pass and chunked workloads hold the pages' matrix
+    problem = {"pages": gen.pages, "fused": gen.pages, "chunked": gen.pages, "mid": gen.mid}[args.workload]()
     from oracle import ce_oracle as O
     N = int(np.sum(problem.labels != problem.ignore_index))
     rows_per_step = 64
