@@ -60,3 +60,20 @@ def test_reference_arm_under_two_ranks_prints_once():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["cpu_baseline"]["kind"] == "oracle"
+
+
+@pytest.mark.parametrize("workload", ["linear", "linear_peaked"])
+def test_reference_arm_linear_workloads(workload):
+    """The reference arm on the linear workloads (a small vocabulary): one JSON line with the
+    arm's metric, the oracle as the timed program and a stated sample."""
+    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload", workload,
+           "--vocab", "256", "--steps", "1", "--warmup", "3"]
+    out = subprocess.run(cmd, capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [l for l in out.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["metric"].startswith("fused linear-CE") and d["value"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and "sampled rows" in d["config"]["workload"]
+    assert ("gradient filtering" in d["metric"]) == (workload == "linear_peaked")
+    assert d["e2e"] == {"value": d["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
