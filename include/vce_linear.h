@@ -117,7 +117,8 @@ int vce_test_gemm_stall(const void* A, const void* B, int64_t M, int64_t N, int6
  * b % 32 of skip[i * skip_ld + b / 32] is set:
  *     C[m][n] = sum over set blocks b of sum_{k in block b} A[m][k] B[n][k]
  * (0 where a tile has no set bit).  skip: device uint32 [ceil(M/128)][skip_ld], skip_ld >=
- * ceil(ceil(K/128) / 32).  pair = 1 runs the tiles as 2-CTA clusters sharing B (both CTAs
+ * ceil(ceil(K/128) / 32); bits of blocks at or past ceil(K/128) must be clear (C is undefined
+ * for a tile that sets only such bits).  pair = 1 runs the tiles as 2-CTA clusters sharing B (both CTAs
  * load the union of their blocks, each multiplies its own); it needs an even number of M
  * tiles.  Bad pair or skip_ld: VCE_ERR_ARG.
  */
