@@ -61,3 +61,24 @@ def test_argument_errors_need_no_gpu(lib):
     m = lib.ce_merge_chunks
     assert m(0, None, None, None, 1, 4, None, -100, 2, None, None, None, None, None, None, 1, None, None,
              None) == -8
+
+
+def test_linear_and_gemm_hook_argument_errors_need_no_gpu(lib):
+    """linear_ce_fwd_bwd_filtered refuses a NaN, negative or infinite eps, and vce_test_gemm_skip
+    refuses null pointers, bad shapes, short bit rows and pairs on an odd tile count, all before
+    any CUDA call."""
+    P, i64, i32, f32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    x = P(0x1000)
+    f = lib.linear_ce_fwd_bwd_filtered
+    f.argtypes = [P, P, i64, i64, i64, P, i64, i32, P, P, P, P, P, i32, f32, P, P, sz, P, P]
+    args = lambda eps: (x, x, 16, 64, 100, x, -100, 2, x, x, x, x, x, 1, eps, None, x, 1 << 30, x, None)
+    for eps in (float("nan"), -1e-3, float("inf")):
+        assert f(*args(eps)) == -8, eps
+    assert lib.linear_ce_workspace_bytes(i64(16), i64(60), i64(100)) == 0      # D not a multiple of 8
+    g = lib.vce_test_gemm_skip
+    g.argtypes = [P, P, i64, i64, i64, P, i64, i32, P, P]
+    assert g(None, x, 256, 256, 128, x, 1, 0, x, None) == -1                     # null A
+    assert g(x, x, 256, 256, 100, x, 1, 0, x, None) == -3                        # K not a multiple of 8
+    assert g(x, x, 256, 256, 8192, x, 1, 0, x, None) == -8                       # 64 blocks need 2 words
+    assert g(x, x, 384, 256, 128, x, 1, 1, x, None) == -8                        # 3 M tiles cannot pair
+    assert g(x, x, 256, 256, 128, x, 1, 2, x, None) == -8                        # pair is 0 or 1
