@@ -160,3 +160,19 @@ def test_full_size_peaked_sampled(vce):
         grade_sum(host(dW[torch.from_numpy(cols[pick]).cuda()]), Gf[:, pick].T @ E, np.abs(Gf[:, pick]).T @ np.abs(E),
                   f"full-size dW rows of column block {cb}")
     assert 0 < int(kept.item()) < -(-p.T // 128) * -(-p.V // 128)
+
+
+@pytest.mark.parametrize("eps", [0.0, 2.0 ** -12])
+def test_all_rows_ignored(vce, eps):
+    """Every label ignored: the mean is 0/0 = NaN, every loss row 0, dE = dW = 0.  Filtered, no
+    block is kept, so every dW and dE tile takes the zero-accumulator epilogue, and the dE merge
+    adds zero partials across both vocabulary chunks."""
+    p = gen.linear_custom(256, 64, 40000, seed=36, w_std=0.05)
+    Eb, Wb = _inputs(p)
+    labels = torch.full((p.T,), -100, dtype=torch.int64, device="cuda")
+    lo, lr, dE, dW, st, kept = vce.linear_ce_fwd_bwd_filtered(dev_bf16(Eb), dev_bf16(Wb), labels, eps)
+    torch.cuda.synchronize()
+    assert vce.vce_get_status(st) == 0
+    assert np.isnan(lo.item()) and torch.all(lr == 0)
+    assert torch.all(dE == 0) and torch.all(dW == 0)
+    assert int(kept.item()) == 0
