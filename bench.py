@@ -528,6 +528,31 @@ def cpu_oracle_baseline(problem, budget_s=12.0, max_rows=4096):
                       f"included), fp64 numpy forward+backward, single thread, {dt:.1f} s"}
 
 
+def cpu_oracle_baseline_linear(problem, budget_s=12.0, max_rows=256):
+    """The fp64 linear-CE oracle as it stands on a row sample (host cores): z over the whole
+    vocabulary, the loss, G and the dE row of each sampled row; W widened once, untimed."""
+    from oracle import ce_oracle as O
+    W = O.widen(problem.W(), "bf16")
+    N = int(np.sum(problem.labels != problem.ignore_index))
+    order = np.random.default_rng(123).permutation(problem.T)
+    done, block = 0, 2
+    t0 = time.perf_counter()
+    while done < max_rows and time.perf_counter() - t0 < budget_s:
+        rows = np.sort(order[done: done + block])
+        E = O.widen(problem.E_rows(rows), "bf16")
+        z = E @ W.T
+        fwd = O.ce_rows(z, problem.labels[rows])
+        G = O.ce_grad_rows(z, problem.labels[rows], fwd, O.row_scale(fwd["valid"], "sum", 1.0 / N))
+        G @ W
+        done += len(rows)
+    dt = time.perf_counter() - t0
+    cores = int(os.environ.get("OPENBLAS_NUM_THREADS") or os.environ.get("OMP_NUM_THREADS") or os.cpu_count() or 1)
+    return {"value": done / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{done} random rows of the same T={problem.T}, D={problem.D}, V={problem.V} problem: z over "
+                      f"all columns, loss, G and the dE row, fp64 numpy (matrix products on up to {cores} BLAS "
+                      f"threads), {dt:.1f} s; W widened once, untimed"}
+
+
 # ------------------------------------------------------------------------------- main
 
 def run_linear(args, rank, local_rank, world, device):
@@ -575,6 +600,8 @@ def run_linear(args, rank, local_rank, world, device):
         "gpu_launches": w.launches_per_step * args.steps,
         "clocks": clocks,
     }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_oracle_baseline_linear(problem)
     if rank == 0:
         print(json.dumps(out), flush=True)
 

@@ -77,3 +77,14 @@ def test_reference_arm_linear_workloads(workload):
     assert d["cpu_baseline"]["kind"] == "oracle" and "sampled rows" in d["config"]["workload"]
     assert ("gradient filtering" in d["metric"]) == (workload == "linear_peaked")
     assert d["e2e"] == {"value": d["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_linear_cpu_baseline_host_logic():
+    """The linear line's cpu_baseline: the oracle on a bounded row sample, rows / seconds."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import gen
+    p = gen.linear_custom(64, 32, 300, seed=41, n_ignore=3)
+    b = bench.cpu_oracle_baseline_linear(p, budget_s=2.0, max_rows=8)
+    assert b["kind"] == "oracle" and b["value"] > 0 and b["cores"] >= 1
+    assert b["sample"].startswith("8 random rows")
