@@ -11,6 +11,10 @@ from HBM with no flush needed.  `value` is whole-job tokens/s (all ranks); `e2e`
 metric with the step's inputs copied from pinned host memory and the loss read back inside
 the timed region.  `--impl reference` times the fp64 CPU oracle on a bounded row sample.
 
+The default line also carries `linear`: the fused linear-CE (E [8192, 4096], W [128256, 4096]
+bf16, linear_ce_fwd_bwd) timed the same way in its own region, with its tensor-core rate
+against the measured bf16 peaks, the CUDA-event time of each of its GEMMs and its own clocks.
+
 Under torchrun (--gpus N > 1) each rank runs an independent replica on its own batch
 (rows are independent: no data-path collective); the timed region is bracketed by a
 barrier and the max over ranks is taken.  Rank 0 prints one JSON line.
@@ -420,6 +424,31 @@ class LinearWorkload:
                                    loss_rows=self.loss_rows, loss_out=self.loss_out, workspace=self.ws,
                                    status=self.status, stream=stream)
 
+    def timed_step(self, stream):
+        """One call through linear_ce_fwd_bwd_timed: {GEMM kind: (milliseconds, launches)}."""
+        _, split = self.vce.linear_ce_fwd_bwd_timed(self.E, self.W, self.labels, self.filter_eps,
+                                                    grad_output=self.go, dE=self.dE, dW=self.dW,
+                                                    loss_rows=self.loss_rows, loss_out=self.loss_out,
+                                                    workspace=self.ws, kept_blocks=self.kept, status=self.status,
+                                                    stream=stream)
+        return split
+
+    def full_size(self):
+        """The shapes the committed GEMM captures were scaled to."""
+        p = self.p
+        return (p.T, p.D, p.V, self.filter_eps) == (8192, 4096, 128256, 0.0)
+
+    def gemm_flops(self, kind):
+        """(algorithmic, executed) flop of one call's GEMMs of a kind: z over all of [T, V] for
+        the statistics and gradient-tile GEMMs; dW and dE over the kept 128 x 128 blocks of G
+        (all of them without filtering), executed twice (G's hi and lo halves)."""
+        p = self.p
+        if kind in ("statistics", "gradient_tiles"):
+            f = 2.0 * p.T * p.V * p.D
+            return f, f
+        f = 2.0 * p.T * p.V * p.D if self.filter_eps <= 0 else 2.0 * self.kept_blocks() * 128 * 128 * p.D
+        return f, 2.0 * f
+
     def e2e_step(self, stream):
         self.E.copy_(self.E_host.view(torch.bfloat16), non_blocking=True)
         self.W.copy_(self.W_host.view(torch.bfloat16), non_blocking=True)
@@ -507,25 +536,42 @@ def time_kernel(workload, steps, stream):
     return statistics.mean(f), statistics.mean(g)
 
 
-def cpu_oracle_baseline(problem, budget_s=12.0, max_rows=4096):
-    """The fp64 oracle as it stands, on a row sample of the same workload (host cores)."""
-    from oracle import ce_oracle as O
-    N = int(np.sum(problem.labels != problem.ignore_index))
-    rng = np.random.default_rng(123)
-    order = rng.permutation(problem.T)
-    done = 0
-    t0 = time.perf_counter()
-    block = 64
-    while done < max_rows and time.perf_counter() - t0 < budget_s:
-        rows = np.sort(order[done: done + block])
-        z = O.widen(problem.rows(rows), problem.dtype)
-        fwd = O.ce_rows(z, problem.labels[rows])
-        O.ce_grad_rows(z, problem.labels[rows], fwd, O.row_scale(fwd["valid"], "sum", 1.0 / N))
-        done += len(rows)
-    dt = time.perf_counter() - t0
-    return {"value": done / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-            "sample": f"{done} random rows of the same T={problem.T}, V={problem.V} matrix (input generation "
-                      f"included), fp64 numpy forward+backward, single thread, {dt:.1f} s"}
+def cpu_oracle_baseline(problem, budget_s=8.0):
+    """The fp64 oracle as it stands, on a row sample of the same workload (host cores): once on
+    one core, then on every core at once (one fresh worker process per core, each on its own
+    share of the sample; started with subprocess, never forked from this CUDA process)."""
+    from oracle import cpu_timing
+    one = cpu_timing.time_rows(problem, 0, 1, budget_s)
+    single = one["rows"] / (one["stop"] - one["start"])
+    cores = os.cpu_count() or 1
+    spec = json.dumps({k: getattr(problem, k) for k in ("name", "T", "V", "dtype", "seed", "std", "n_margin",
+                                                       "margin_lo", "margin_hi", "n_ignore")})
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               PYTHONPATH=ROOT + os.pathsep + os.environ.get("PYTHONPATH", ""))
+    procs = [subprocess.Popen([sys.executable, "-m", "oracle.cpu_timing", spec, str(i), str(cores), str(budget_s)],
+                              cwd=ROOT, env=env, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+             for i in range(cores)]
+    parts = []
+    for pr in procs:
+        out, _ = pr.communicate(timeout=budget_s + 120)
+        if pr.returncode == 0 and out.strip():
+            parts.append(json.loads(out.strip().splitlines()[-1]))
+    rec = {"value": single, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+           "sample": f"{one['rows']} random rows of the same T={problem.T}, V={problem.V} matrix (input generation "
+                     f"included), fp64 numpy forward+backward on one core, {one['stop'] - one['start']:.1f} s",
+           "host_cores": cores}
+    if len(parts) == cores:
+        rows = sum(p_["rows"] for p_ in parts)
+        wall = max(p_["stop"] for p_ in parts) - min(p_["start"] for p_ in parts)
+        rec.update(value=rows / wall, cores=cores,
+                   sample=f"{rows} random rows of the same T={problem.T}, V={problem.V} matrix (input generation "
+                          f"included), fp64 numpy forward+backward, {cores} worker processes (one per host core, "
+                          f"one thread each) for {wall:.1f} s",
+                   single_core={"value": single, "cores": 1, "rows": one["rows"],
+                                "seconds": round(one["stop"] - one["start"], 2)})
+    else:
+        rec["all_cores"] = f"unavailable: {len(parts)} of {cores} worker processes reported"
+    return rec
 
 
 def cpu_oracle_baseline_linear(problem, budget_s=12.0, max_rows=256):
@@ -555,50 +601,114 @@ def cpu_oracle_baseline_linear(problem, budget_s=12.0, max_rows=256):
 
 # ------------------------------------------------------------------------------- main
 
-def run_linear(args, rank, local_rank, world, device):
-    peaked = args.workload == "linear_peaked"
+def linear_problem(args, rank, peaked):
     problem = gen.linear_peaked(seed=1006 + rank) if peaked else gen.linear(seed=1005 + rank)
     if args.vocab:
         problem = gen.LinearProblem(f"{problem.name}[V={args.vocab}]", problem.T, problem.D, args.vocab,
                                     problem.seed, problem.n_ignore, problem.e_std, problem.w_std, problem.peak)
-    eps = args.filter_eps if args.filter_eps is not None else (2.0 ** -12 if peaked else 0.0)
-    w = LinearWorkload(problem, device, eps)
+    return problem
+
+
+LINEAR_GEMMS = {
+    "statistics": "k_tc_gemm<EpiStats> (z = E W^T, per-tile row statistics)",
+    "gradient_tiles": "k_tc_gemm<EpiGrad> (z recomputed, G = c (p - onehot) as bf16 hi + lo)",
+    "dW": "k_tc_gemm<EpiStore> (dW = G^T E, compensated)",
+    "dE": "k_tc_gemm<EpiKahan> (dE += G W, compensated, two-sum across chunks)",
+}
+
+
+def measure_linear(w, steps, warmup, e2e_steps, world, device, local_rank):
+    """Times linear-CE calls (CUDA events on the launching stream), the per-GEMM split of one
+    call (events around each GEMM launch), and the end-to-end call with host copies."""
     stream = torch.cuda.current_stream(device)
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         w.step(stream)
     torch.cuda.synchronize(device)
     with ClockSampler(local_rank) as clk:
-        ms = time_steps(w.step, args.steps, stream, world, device)
+        ms = time_steps(w.step, steps, stream, world, device)
     clocks = clk.summary()
-    e2e_steps = max(3, min(args.e2e_steps, args.steps))
+    # per-GEMM split: a few timed calls (blocking), averaged
+    reps = max(3, min(steps, 10))
+    tot = {k: [0.0, 0] for k in LINEAR_GEMMS}
+    for _ in range(reps):
+        split = w.timed_step(stream)
+        for k, (m, n) in split.items():
+            tot[k][0] += m / reps
+            tot[k][1] = n
+    e2e_steps = max(3, min(e2e_steps, steps))
     w.e2e_step(stream)
     e2e_ms = time_steps(w.e2e_step, e2e_steps, stream, world, device)
     status = w.vce.vce_get_status(w.status)
     if status != 0:
         raise RuntimeError(f"device status {status}")
-    tokens_all = sum_over_ranks(w.tokens(), world, device)
-    ms_step = ms / args.steps
+    return {"ms_step": ms / steps, "e2e_ms": e2e_ms / e2e_steps, "e2e_steps": e2e_steps, "clocks": clocks,
+            "gemms": tot, "tokens_all": sum_over_ranks(w.tokens(), world, device)}
+
+
+def linear_record(w, m, peaks, world):
+    """The linear-CE measurement as a JSON object: throughput, tensor-core rate against the
+    measured bf16 peaks (burst as `frac`, sustained beside it), the per-GEMM split with the
+    dominant GEMM's roofline, clocks and the end-to-end figure."""
+    ms = m["ms_step"]
+    alg = w.flops() / (ms / 1e3) / 1e12
+    exe = w.executed_flops() / (ms / 1e3) / 1e12
+    gemms = {}
+    for k, (gms, n) in m["gemms"].items():
+        fa, fe = w.gemm_flops(k)
+        gemms[k] = {"kernel": LINEAR_GEMMS[k], "launches": n, "ms_per_call": round(gms, 4),
+                    "ms_per_launch": round(gms / max(n, 1), 4),
+                    "algorithmic_tflops": round(fa / (gms / 1e3) / 1e12, 1) if gms > 0 else None,
+                    "executed_tflops": round(fe / (gms / 1e3) / 1e12, 1) if gms > 0 else None}
+    dom = max(gemms, key=lambda k: gemms[k]["ms_per_call"])
+    d = gemms[dom]
+    return {
+        "value": round(m["tokens_all"] / (ms / 1e3), 1), "unit": "tokens/s", "ms_per_call": round(ms, 4),
+        "algorithmic_tflops": round(alg, 1), "executed_tflops": round(exe, 1),
+        "frac": round(alg / peaks["bf16_tflops"], 4), "peak": peaks["bf16_tflops"],
+        "frac_of_sustained": round(alg / peaks["bf16_tflops_sustained"], 4),
+        "peak_sustained": peaks["bf16_tflops_sustained"], "peak_source": peaks["source"],
+        "algorithmic_flop_per_call": w.flops(), "executed_flop_per_call": w.executed_flops(),
+        "gemms": gemms,
+        "roofline": {"bound": "tensor", "kernel": d["kernel"], "achieved": d["algorithmic_tflops"],
+                     "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": round(d["algorithmic_tflops"] / peaks["bf16_tflops"], 4),
+                     "executed": d["executed_tflops"], "ms_per_launch": d["ms_per_launch"],
+                     "traffic": profiled_traffic(f"linear_{dom}_gemm", LINEAR_FILES) if w.full_size() else None},
+        "e2e": {"value": round(m["tokens_all"] / (m["e2e_ms"] / 1e3), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": w.h2d_bytes, "d2h_bytes_per_step": w.d2h_bytes, "steps": m["e2e_steps"]},
+        "gpu_launches_per_call": w.launches_per_step,
+        "clocks": m["clocks"],
+    }
+
+
+LINEAR_FILES = ["vocab_cross_entropy_gb300/csrc/lce.cu", "vocab_cross_entropy_gb300/csrc/tc_gemm.cuh",
+                "vocab_cross_entropy_gb300/csrc/tc_launch.cuh", "vocab_cross_entropy_gb300/csrc/vce_async.cuh",
+                "vocab_cross_entropy_gb300/csrc/vce_device.cuh"]
+
+
+def run_linear(args, rank, local_rank, world, device):
+    peaked = args.workload == "linear_peaked"
+    problem = linear_problem(args, rank, peaked)
+    eps = args.filter_eps if args.filter_eps is not None else (2.0 ** -12 if peaked else 0.0)
+    w = LinearWorkload(problem, device, eps)
+    m = measure_linear(w, args.steps, args.warmup, args.e2e_steps, world, device, local_rank)
     peaks = measured_peaks()
-    achieved = w.flops() / (ms_step / 1e3) / 1e12
+    rec = linear_record(w, m, peaks, world)
     call = "linear_ce_fwd_bwd_filtered" if eps > 0 else "linear_ce_fwd_bwd"
     out = {
         "metric": ("fused linear-CE fwd+bwd tokens/s at T=8192, D=4096, V=128256 bf16"
                    + (f", gradient filtering at eps={eps:.3g}" if eps > 0 else "") + "; TFLOP/s vs bf16 peak"),
-        "value": round(tokens_all / (ms_step / 1e3), 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
+        "value": rec["value"], "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": rec["ms_per_call"], "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": dict(w.describe(), parallelism=f"replicas{world}"),
-        "roofline": {"bound": "tensor", "kernel": f"{call} (all launches of one call)",
-                     "achieved": round(achieved, 1), "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
-                     "frac": round(achieved / peaks["bf16_tflops_sustained"], 4),
-                     "frac_of_burst": round(achieved / peaks["bf16_tflops"], 4), "peak_source": peaks["source"],
-                     "algorithmic_flop_per_call": w.flops(), "executed_flop_per_call": w.executed_flops(),
-                     "executed_tflops": round(w.executed_flops() / (ms_step / 1e3) / 1e12, 1),
-                     "traffic": None},
-        "e2e": {"value": round(tokens_all / (e2e_ms / e2e_steps / 1e3), 1), "unit": "tokens/s",
-                "h2d_bytes_per_step": w.h2d_bytes, "d2h_bytes_per_step": w.d2h_bytes, "steps": e2e_steps},
+        "config": dict(w.describe(), parallelism=f"replicas{world}", call=call),
+        "roofline": rec["roofline"],
+        "call_tflops": {k: rec[k] for k in ("algorithmic_tflops", "executed_tflops", "frac", "peak",
+                                            "frac_of_sustained", "peak_sustained", "peak_source")},
+        "gemms": rec["gemms"],
+        "e2e": rec["e2e"],
         "gpu_launches": w.launches_per_step * args.steps,
-        "clocks": clocks,
+        "clocks": rec["clocks"],
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_oracle_baseline_linear(problem)
@@ -718,6 +828,18 @@ def run_ours(args, rank, local_rank, world):
                                "frac": round(w.bytes_fwd() / (fwd_ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
                                "traffic": (profiled_traffic("k_ce_fwd_ring_pages", FWD_RING_FILES)
                                            if captured_shape(w) and fkern == "k_ce_fwd_ring" else None)}
+    if args.workload == "pages" and not args.no_linear and not args.rows and args.logits_dtype == "bf16" \
+            and args.reduction == "mean" and not args.label_smoothing:
+        # the fused linear-CE of the same run (E [8192, 4096], W [128256, 4096] bf16) beside the CE line
+        del w
+        torch.cuda.empty_cache()
+        lw = LinearWorkload(linear_problem(args, rank, False), device, 0.0)
+        lm = measure_linear(lw, min(args.steps, 30), args.warmup, args.e2e_steps, world, device, local_rank)
+        lsteps = min(args.steps, 30)
+        out["linear"] = dict(linear_record(lw, lm, peaks, world), call="linear_ce_fwd_bwd",
+                             workload=lw.describe()["workload"], steps=lsteps,
+                             gpu_launches=lw.launches_per_step * lsteps)
+        del lw
     if rank == 0 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_oracle_baseline(problem)
     if rank == 0:
@@ -831,6 +953,8 @@ def main(argv=None):
     ap.add_argument("--label-smoothing", type=float, default=0.0,
                     help="pages workload through ce_forward_ls / ce_backward_ls with this eps")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-linear", action="store_true",
+                    help="pages workload: leave out the fused linear-CE record of the default line")
     ap.add_argument("--rows", type=int, default=None,
                     help="profiling only: draw the first ROWS rows of the workload instead of all T")
     ap.add_argument("--vocab", type=int, default=None,

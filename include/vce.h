@@ -94,6 +94,25 @@ size_t vce_row_stats_floats(void);
 int vce_get_status(const int32_t* status, vce_stream_t s, int32_t* host_out);
 
 /*
+ * vce_debug_checks -- 1 if this library was built with device-side index checks
+ * (python -m vocab_cross_entropy_gb300.build --debug-checks, which makes libvce_debug.so),
+ * else 0.  No page counterpart: a debugging aid.
+ */
+int vce_debug_checks(void);
+
+/*
+ * vce_debug_status -- in a build with device-side index checks: waits for the device
+ * (cudaDeviceSynchronize), then writes to *host_out the code of the first index check that
+ * failed since the last call (121 a row outside [0, T); 122 a column range outside its row
+ * or chunk; 123 a chunk or segment index outside its table; 124 a stage or ring slot
+ * outside the ring; 125 a GEMM output tile outside the output), or 0, and clears the record.
+ * A kernel whose check fails skips that access (it never traps), so its outputs are then
+ * incomplete.  In the release build it writes 0 and waits for nothing.  Returns VCE_OK,
+ * VCE_ERR_NULL or VCE_ERR_CUDA.  No page counterpart: a debugging aid.
+ */
+int vce_debug_status(int32_t* host_out);
+
+/*
  * ce_forward -- per-row NLL and the statistics its gradient needs.  [TT, Numerics;
  * Memory/perf, compiled forward]  For row i with label t:
  *     L'_i = log sum_{j != t} exp(z_ij)          (target left out by a column test)
@@ -287,7 +306,10 @@ int ce_merge_chunks_ls(int k, const void* const* chunk_logits, const int64_t* ch
  *     VCE_ERR_SCRATCH_LIMIT and enqueue nothing.
  *   - The first call on each device looks up the array's device address on that device
  *     (cudaGetSymbolAddress, with that device current); make that first call before
- *     capturing any stream.  A failed lookup returns VCE_ERR_CUDA.
+ *     capturing any stream.  A failed lookup returns VCE_ERR_CUDA.  The address is kept
+ *     with the unique id of the device's context: after a device reset (a new context,
+ *     in which the library's module and its array are loaded anew) the next call looks it
+ *     up again, and that call, too, belongs before any stream capture.
  *   - Every call on a device uses the same array and leaves its contents behind.  Calls
  *     whose work can overlap on the GPU (different streams without ordering, or different
  *     host threads) race on it and give undefined results; order them on one stream.

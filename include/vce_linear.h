@@ -39,8 +39,10 @@ size_t linear_ce_workspace_bytes(int64_t T, int64_t D, int64_t V);
  *   branch, ignored rows 0):
  *       dE = G W   [T, D],       dW = G^T E   [V, D].
  *   G enters the two gradient GEMMs as an exact-to-16-bits pair of bf16 terms
- *   (G = G_hi + G_lo), every product sum is accumulated in fp32, and the partial dE of
- *   successive vocabulary chunks is merged with a two-sum compensated fp32 pair.
+ *   (G = G_hi + G_lo).  Both gradient GEMMs accumulate compensated: each run of 1024
+ *   consecutive products of a sum (along T for dW, along the vocabulary for dE) is summed in
+ *   fp32 on the tensor cores, and the runs are added into a (sum, compensation) fp32 pair
+ *   with a two-sum; dE's pair is carried across vocabulary chunks the same way.
  *
  *   E            [T, D] bf16 row-major, 16-byte aligned
  *   W            [V, D] bf16 row-major, 16-byte aligned
@@ -52,8 +54,9 @@ size_t linear_ce_workspace_bytes(int64_t T, int64_t D, int64_t V);
  *                aligned, written (bf16 rounded to nearest even from fp32)
  *   workspace    >= linear_ce_workspace_bytes(T, D, V) bytes, 256-byte aligned,
  *                scratch owned by the caller, contents undefined on return
- *   status       [1] int32: 0, VCE_ERR_LABEL, or 101..104 when a device-side wait of
- *                the GEMM pipeline gave up (the outputs are then undefined)
+ *   status       [1] int32: 0, VCE_ERR_LABEL, or 100..104 when the GEMM pipeline gave up
+ *                (100: the two CTAs of a pair got different tensor-memory columns; 101..104: a
+ *                device-side wait ran out), the outputs then being undefined
  */
 int linear_ce_fwd_bwd(const void* E, const void* W, int64_t T, int64_t D, int64_t V,
                       const int64_t* labels, int64_t ignore_index, vce_reduction red,
@@ -71,7 +74,9 @@ int linear_ce_fwd_bwd(const void* E, const void* W, int64_t T, int64_t D, int64_
  *   its valid rows is below filter_eps.  The dW and dE GEMMs skip the dropped blocks'
  *   K blocks (128 rows, resp. columns, is a whole number of their K blocks), so kept blocks
  *   keep exactly the unfiltered arithmetic and the work falls with the dropped fraction.
- *   The loss and row statistics are never filtered.
+ *   The loss and row statistics are never filtered.  The filtered gradient GEMMs run on
+ *   single CTAs and accumulate each tile's kept blocks in one fp32 sum (no compensation
+ *   within a chunk; dE's chunks are still merged with the two-sum pair).
  *
  *   filter_eps   threshold on p_ij, finite and >= 0; 0 is exactly linear_ce_fwd_bwd (no
  *                block is dropped).  NaN, negative or infinite: VCE_ERR_ARG, nothing enqueued.
@@ -88,24 +93,59 @@ int linear_ce_fwd_bwd_filtered(const void* E, const void* W, int64_t T, int64_t 
                                int32_t* status, vce_stream_t s);
 
 /*
+ * linear_ce_fwd_bwd_timed -- linear_ce_fwd_bwd_filtered with a CUDA event recorded on `s`
+ * before and after each of its tensor-core GEMM launches (no page counterpart: it measures
+ * the call for the benchmark).  The outputs are those of linear_ce_fwd_bwd_filtered (which
+ * filter_eps = 0 makes linear_ce_fwd_bwd).  It waits for the stream, then writes to host
+ * memory, per GEMM kind k (0 statistics GEMM, 1 gradient-tile GEMMs, 2 dW GEMMs, 3 dE
+ * GEMMs), gemm_ms[k] = the summed milliseconds of its launches and gemm_launches[k] = their
+ * number.  Blocking; the events are created and destroyed by the call.  NULL gemm_ms or
+ * gemm_launches: VCE_ERR_NULL.
+ */
+int linear_ce_fwd_bwd_timed(const void* E, const void* W, int64_t T, int64_t D, int64_t V,
+                            const int64_t* labels, int64_t ignore_index, vce_reduction red,
+                            const float* grad_output, float* loss_rows, float* loss_out,
+                            void* dE, void* dW, vce_dtype grad_dt, float filter_eps,
+                            unsigned long long* kept_blocks, void* workspace, size_t workspace_bytes,
+                            int32_t* status, vce_stream_t s, float* gemm_ms, int* gemm_launches);
+
+/*
  * vce_gemm_bf16 -- the tensor-core GEMM the linear-CE is built on, with a plain fp32 output:
  *     C[m][n] = sum_k A(m, k) B(n, k)
  * A is [M, K] row-major (a_mn = 0, K-major) or [K, M] row-major (a_mn = 1, MN-major); B is
- * [N, K] (b_mn = 0) or [K, N] (b_mn = 1).  bf16 operands, fp32 accumulation, 128 x 256
- * tiles.  M, N, K multiples of 8; A, B, C 16-byte aligned; C [M, ldc] fp32, ldc >= N and a
- * multiple of 4.  No page counterpart: it exposes the building block for testing.
+ * [N, K] (b_mn = 0) or [K, N] (b_mn = 1).  bf16 operands, fp32 accumulation, tiles 256
+ * columns wide, run on CTA pairs (256-row tiles) when ceil(M / 128) is even, else on single
+ * CTAs (128-row tiles).  M, N, K multiples of 8; A, B, C 16-byte aligned; C [M, ldc] fp32,
+ * ldc >= N and a multiple of 4.  No page counterpart: it exposes the building block for
+ * testing.
  */
 int vce_gemm_bf16(const void* A, int a_mn, const void* B, int b_mn, int64_t M, int64_t N, int64_t K,
                   float* C, int64_t ldc, vce_stream_t s);
 
 /*
+ * vce_gemm_bf16_variant -- vce_gemm_bf16 in a chosen launch form (no page counterpart; for
+ * testing and timing the forms the linear-CE uses):
+ *   pair    0: single CTAs, 128-row tiles; 1: CTA pairs issuing cta_group::2 MMAs, 256-row tiles
+ *           (needs ceil(M / 128) even)
+ *   bn      tile width, 128 or 256 columns
+ *   seg_kb  0: one fp32 accumulation over all of K; > 0 (bn = 128 only): compensated
+ *           accumulation, each run of seg_kb * 64 consecutive K products summed afresh and the
+ *           runs added into a (sum, compensation) pair with a two-sum; C = sum + compensation
+ * Any other pair, bn or seg_kb: VCE_ERR_ARG, nothing enqueued.  Other arguments as
+ * vce_gemm_bf16.
+ */
+int vce_gemm_bf16_variant(const void* A, int a_mn, const void* B, int b_mn, int64_t M, int64_t N, int64_t K,
+                          float* C, int64_t ldc, int pair, int bn, int seg_kb, vce_stream_t s);
+
+/*
  * vce_test_gemm_stall -- test hook for the GEMM's give-up path (no page counterpart).
- * Runs vce_gemm_bf16's pipeline (A [M,K], B [N,K] K-major) with its producer announcing 16
- * more bytes per stage than its copies deliver, so no stage ever completes.  Every wait of
- * the kernel is bounded by wait_ns (1 ms .. 2 s): the waiting role gives up, writes its code
- * to *status (101 empty-slot, 102 full-slot, 103 accumulator-free, 104 accumulator-full
- * wait), the other roles stop, copies in flight are drained, tensor memory is released and
- * the kernel returns; the context stays usable.  C's contents are undefined afterwards.
+ * Runs vce_gemm_bf16's pipeline (A [M,K], B [N,K] K-major; CTA pairs when ceil(M / 128) is
+ * even, else single CTAs) with its producer announcing 16 more bytes per stage than its
+ * copies deliver, so no stage ever completes.  Every wait of the kernel is bounded by wait_ns
+ * (1 ms .. 2 s): the waiting role gives up, writes its code to *status (101 empty-slot, 102
+ * full-slot, 103 accumulator-free, 104 accumulator-full wait), the other roles (of both CTAs
+ * of a pair) stop, copies in flight are drained, tensor memory is released and the kernel
+ * returns; the context stays usable.  C's contents are undefined afterwards.
  */
 int vce_test_gemm_stall(const void* A, const void* B, int64_t M, int64_t N, int64_t K, float* C,
                         uint64_t wait_ns, int32_t* status, vce_stream_t s);
@@ -118,12 +158,11 @@ int vce_test_gemm_stall(const void* A, const void* B, int64_t M, int64_t N, int6
  *     C[m][n] = sum over set blocks b of sum_{k in block b} A[m][k] B[n][k]
  * (0 where a tile has no set bit).  skip: device uint32 [ceil(M/128)][skip_ld], skip_ld >=
  * ceil(ceil(K/128) / 32); bits of blocks at or past ceil(K/128) must be clear (C is undefined
- * for a tile that sets only such bits).  pair = 1 runs the tiles as 2-CTA clusters sharing B (both CTAs
- * load the union of their blocks, each multiplies its own); it needs an even number of M
- * tiles.  Bad pair or skip_ld: VCE_ERR_ARG.
+ * for a tile that sets only such bits).  It runs on single CTAs, as the filtered linear-CE's
+ * gradient GEMMs do.  Bad skip_ld: VCE_ERR_ARG.
  */
 int vce_test_gemm_skip(const void* A, const void* B, int64_t M, int64_t N, int64_t K, const uint32_t* skip,
-                       int64_t skip_ld, int pair, float* C, vce_stream_t s);
+                       int64_t skip_ld, float* C, vce_stream_t s);
 
 #ifdef __cplusplus
 }

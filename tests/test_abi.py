@@ -64,9 +64,10 @@ def test_argument_errors_need_no_gpu(lib):
 
 
 def test_linear_and_gemm_hook_argument_errors_need_no_gpu(lib):
-    """linear_ce_fwd_bwd_filtered refuses a NaN, negative or infinite eps, and vce_test_gemm_skip
-    refuses null pointers, bad shapes, short bit rows and pairs on an odd tile count, all before
-    any CUDA call."""
+    """linear_ce_fwd_bwd_filtered refuses a NaN, negative or infinite eps, vce_test_gemm_skip
+    refuses null pointers, bad shapes and short bit rows, and vce_gemm_bf16_variant refuses pairs
+    on an odd tile count, unknown tile widths and compensation on 256-wide tiles, all before any
+    CUDA call."""
     P, i64, i32, f32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
     x = P(0x1000)
     f = lib.linear_ce_fwd_bwd_filtered
@@ -76,9 +77,15 @@ def test_linear_and_gemm_hook_argument_errors_need_no_gpu(lib):
         assert f(*args(eps)) == -8, eps
     assert lib.linear_ce_workspace_bytes(i64(16), i64(60), i64(100)) == 0      # D not a multiple of 8
     g = lib.vce_test_gemm_skip
-    g.argtypes = [P, P, i64, i64, i64, P, i64, i32, P, P]
-    assert g(None, x, 256, 256, 128, x, 1, 0, x, None) == -1                     # null A
-    assert g(x, x, 256, 256, 100, x, 1, 0, x, None) == -3                        # K not a multiple of 8
-    assert g(x, x, 256, 256, 8192, x, 1, 0, x, None) == -8                       # 64 blocks need 2 words
-    assert g(x, x, 384, 256, 128, x, 1, 1, x, None) == -8                        # 3 M tiles cannot pair
-    assert g(x, x, 256, 256, 128, x, 1, 2, x, None) == -8                        # pair is 0 or 1
+    g.argtypes = [P, P, i64, i64, i64, P, i64, P, P]
+    assert g(None, x, 256, 256, 128, x, 1, x, None) == -1                        # null A
+    assert g(x, x, 256, 256, 100, x, 1, x, None) == -3                           # K not a multiple of 8
+    assert g(x, x, 256, 256, 8192, x, 1, x, None) == -8                          # 64 blocks need 2 words
+    v = lib.vce_gemm_bf16_variant
+    v.argtypes = [P, i32, P, i32, i64, i64, i64, P, i64, i32, i32, i32, P]
+    assert v(x, 0, x, 0, 384, 256, 128, x, 256, 1, 256, 0, None) == -8          # 3 M tiles cannot pair
+    assert v(x, 0, x, 0, 256, 256, 128, x, 256, 2, 256, 0, None) == -8          # pair is 0 or 1
+    assert v(x, 0, x, 0, 256, 256, 128, x, 256, 1, 64, 0, None) == -8           # tile width 128 or 256
+    assert v(x, 0, x, 0, 256, 256, 128, x, 256, 1, 256, 4, None) == -8          # compensation needs 128
+    assert v(x, 0, x, 0, 256, 256, 128, x, 256, 1, 128, -1, None) == -8         # segment length >= 0
+    assert v(x, 0, x, 0, 256, 256, 128, x, 200, 1, 128, 0, None) == -4          # ldc < N

@@ -34,12 +34,63 @@ def test_gemm_layouts(vce, a_mn, b_mn, M, N, K):
     assert np.all(err <= bound), f"max err/bound {np.max(err / bound):.3g}"
 
 
-def test_stalled_pipeline_gives_up_and_the_context_survives(vce):
+@pytest.mark.parametrize("pair,bn,seg_kb", [(0, 256, 0), (1, 256, 0), (0, 128, 0), (1, 128, 0), (0, 128, 2),
+                                          (1, 128, 3), (1, 128, 1)])
+@pytest.mark.parametrize("a_mn,b_mn", [(False, False), (True, True), (False, True)])
+@pytest.mark.parametrize("M,N,K", [(256, 256, 64), (512, 384, 1000), (2560, 640, 1536)])
+def test_gemm_variants(vce, pair, bn, seg_kb, a_mn, b_mn, M, N, K):
+    """Every launch form of the GEMM -- single CTAs or CTA pairs (cta_group::2), 128- or
+    256-column tiles, compensated accumulation over segments of seg_kb K blocks -- against a
+    float64 product of the same bf16 values."""
+    rng = np.random.default_rng(M + 3 * N + K + 5 * pair + bn + seg_kb + 7 * a_mn + 11 * b_mn)
+    A, A64 = _bf16(rng, (K, M) if a_mn else (M, K))
+    B, B64 = _bf16(rng, (K, N) if b_mn else (N, K), 0.05)
+    C = vce.vce_gemm_bf16_variant(A.cuda(), B.cuda(), a_mn, b_mn, pair=pair, bn=bn, seg_kb=seg_kb)
+    torch.cuda.synchronize()
+    Am = A64.T if a_mn else A64
+    Bm = B64.T if b_mn else B64
+    want = Am @ Bm.T
+    bound = 2.0 ** -20 * (np.abs(Am) @ np.abs(Bm).T) + 1e-30
+    err = np.abs(C.cpu().numpy().astype(np.float64) - want)
+    assert np.all(err <= bound), f"max err/bound {np.max(err / bound):.3g}"
+
+
+@pytest.mark.parametrize("pair", [0, 1])
+def test_compensated_accumulation_keeps_what_fp32_drops(vce, pair):
+    """K = 16384: 8192 products of 1 followed by 8192 products of 2^-16 (times a per-column
+    power of two).  A single fp32 accumulator holding 8192 has an ulp of 2^-10, and each
+    MMA step adds 16 * 2^-16 = 2^-12 < half an ulp: plain accumulation can lose all of the
+    second half.  Compensated accumulation sums 1024 products per segment exactly and adds
+    the segments with a two-sum, so C = 8192.125 * scale exactly."""
+    M, N, K = 256, 128, 16384
+    A = torch.ones(M, K, dtype=torch.bfloat16)
+    scale = 2.0 ** (np.arange(N) % 4)
+    b = np.empty((N, K), np.float32)
+    b[:, : K // 2] = 1.0
+    b[:, K // 2:] = 2.0 ** -16
+    b *= scale[:, None].astype(np.float32)
+    B = torch.from_numpy(b).to(torch.bfloat16)
+    C = vce.vce_gemm_bf16_variant(A.cuda(), B.cuda(), pair=pair, bn=128, seg_kb=16)
+    torch.cuda.synchronize()
+    want = (8192.0 + 8192 * 2.0 ** -16) * scale
+    assert np.array_equal(C.cpu().numpy().astype(np.float64), np.broadcast_to(want, (M, N)))
+
+
+def test_gemm_variant_refuses_bad_arguments(vce):
+    A = torch.zeros(384, 128, dtype=torch.bfloat16, device="cuda")   # 3 M tiles: no pairs
+    B = torch.zeros(256, 128, dtype=torch.bfloat16, device="cuda")
+    for kw in (dict(pair=1), dict(bn=64), dict(bn=256, seg_kb=4), dict(seg_kb=-1), dict(pair=2)):
+        with pytest.raises(vce.VceError):
+            vce.vce_gemm_bf16_variant(A, B, **kw)
+
+
+@pytest.mark.parametrize("M", [128, 256])   # single CTAs; a CTA pair
+def test_stalled_pipeline_gives_up_and_the_context_survives(vce, M):
     """A stage that never completes: the bounded waits give up with a status code, the kernel
-    returns, and the next GEMM on the same context is correct."""
+    returns (both CTAs of a pair), and the next GEMM on the same context is correct."""
     import time
     rng = np.random.default_rng(5)
-    A, A64 = _bf16(rng, (256, 128))
+    A, A64 = _bf16(rng, (M, 128))
     B, B64 = _bf16(rng, (512, 128), 0.05)
     Ad, Bd = A.cuda(), B.cuda()
     t0 = time.time()
@@ -54,14 +105,12 @@ def test_stalled_pipeline_gives_up_and_the_context_survives(vce):
     assert np.all(np.abs(C.cpu().numpy().astype(np.float64) - want) <= bound)
 
 
-@pytest.mark.parametrize("pair", [False, True])
-@pytest.mark.parametrize("M,N,K", [(512, 512, 1000), (1024, 256, 4160)])
-def test_k_block_skipping(vce, pair, M, N, K):
+@pytest.mark.parametrize("M,N,K", [(512, 512, 1000), (1024, 256, 4160), (384, 512, 256)])
+def test_k_block_skipping(vce, M, N, K):
     """The K-block skipping gradient filtering rides on, against float64: each 128-row M tile
     adds only the 128-column K blocks whose bit is set (a ragged last block included); one tile
-    keeps none (its accumulator is never written: zeros), one keeps all.  pair: the same on
-    2-CTA clusters, where both CTAs load the union of their blocks and each multiplies its own."""
-    rng = np.random.default_rng(M + K + pair)
+    keeps none (its accumulator is never written: zeros), one keeps all."""
+    rng = np.random.default_rng(M + K)
     A, A64 = _bf16(rng, (M, K))
     B, B64 = _bf16(rng, (N, K), 0.05)
     tiles, nblk = -(-M // 128), -(-K // 128)
@@ -73,7 +122,7 @@ def test_k_block_skipping(vce, pair, M, N, K):
     for t in range(tiles):
         for b in np.nonzero(keep[t])[0]:
             bits[t, b // 32] |= np.uint32(1) << np.uint32(b % 32)
-    C = vce.vce_test_gemm_skip(A.cuda(), B.cuda(), torch.from_numpy(bits.view(np.int32)).cuda(), pair)
+    C = vce.vce_test_gemm_skip(A.cuda(), B.cuda(), torch.from_numpy(bits.view(np.int32)).cuda())
     torch.cuda.synchronize()
     kmask = np.repeat(keep, 128, axis=1)[:, :K]                    # [tiles, K]
     Am = A64 * np.repeat(kmask, 128, axis=0)[:M]                   # dropped blocks of each tile zeroed
@@ -85,10 +134,7 @@ def test_k_block_skipping(vce, pair, M, N, K):
 
 
 def test_k_block_skipping_refuses_bad_arguments(vce):
-    A = torch.zeros(384, 128, dtype=torch.bfloat16, device="cuda")   # 3 M tiles: no pairs
+    A = torch.zeros(384, 128, dtype=torch.bfloat16, device="cuda")
     B = torch.zeros(256, 128, dtype=torch.bfloat16, device="cuda")
-    bits = torch.zeros(3, 1, dtype=torch.int32, device="cuda")
     with pytest.raises(vce.VceError):
-        vce.vce_test_gemm_skip(A, B, bits, True)
-    with pytest.raises(vce.VceError):
-        vce.vce_test_gemm_skip(A, B, torch.zeros(3, 0, dtype=torch.int32, device="cuda"), False)
+        vce.vce_test_gemm_skip(A, B, torch.zeros(3, 0, dtype=torch.int32, device="cuda"))

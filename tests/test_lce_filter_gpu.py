@@ -16,6 +16,17 @@ from oracle import ce_oracle as O
 from tests import _grading as G
 from tests.test_ce_gpu import vce  # noqa: F401  (fixture)
 from tests.test_lce_gpu import dev_bf16, grade_sum, host, z_sum_slack
+
+CHUNK = 32768   # vocabulary columns per gradient chunk
+
+
+def filtered_steps(T, V):
+    """Accumulation steps of the filtered gradient GEMMs, which sum a whole chunk's K in one fp32
+    accumulator (16 products per step, G's hi and lo halves both): dW over 2 T, dE over twice
+    the chunk width."""
+    t_pad = -(-T // 128) * 128
+    v_pad = -(-V // 256) * 256
+    return {"dW": 2 * t_pad // 16, "dE": 2 * min(v_pad, CHUNK) // 16}
 from tests.test_oracle_filter import _eps_in_a_gap
 
 pytestmark = pytest.mark.gpu
@@ -58,8 +69,9 @@ def test_filtered_matches_the_filtered_oracle(vce, T, D, V, peak, reduction, n_i
     G.check_reduced(lo.item(), ref["loss_out"])
     mask = np.repeat(np.repeat(keep, 128, 0), 128, 1)[:T, :V]
     aG = np.abs(np.where(mask, ref["grad"], 0.0))
-    grade_sum(host(dE), ref["dE"], aG @ np.abs(W), "dE")
-    grade_sum(host(dW), ref["dW"], aG.T @ np.abs(E), "dW")
+    st = filtered_steps(p.T, p.V)
+    grade_sum(host(dE), ref["dE"], aG @ np.abs(W), "dE", steps=st["dE"])
+    grade_sum(host(dW), ref["dW"], aG.T @ np.abs(E), "dW", steps=st["dW"])
 
 
 def test_fp32_gradients_and_per_row_grad_output(vce):
@@ -79,8 +91,9 @@ def test_fp32_gradients_and_per_row_grad_output(vce):
     assert int(kept.item()) == int(ref["keep"].sum())
     mask = np.repeat(np.repeat(ref["keep"], 128, 0), 128, 1)[:p.T, :p.V]
     aG = np.abs(np.where(mask, ref["grad"], 0.0))
-    grade_sum(host(dE), ref["dE"], aG @ np.abs(W), "dE")
-    grade_sum(host(dW), ref["dW"], aG.T @ np.abs(E), "dW")
+    st = filtered_steps(p.T, p.V)
+    grade_sum(host(dE), ref["dE"], aG @ np.abs(W), "dE", steps=st["dE"])
+    grade_sum(host(dW), ref["dW"], aG.T @ np.abs(E), "dW", steps=st["dW"])
 
 
 def test_large_eps_keeps_only_target_blocks(vce):
@@ -148,7 +161,7 @@ def test_full_size_peaked_sampled(vce):
         Gf = np.where(np.repeat(keep[0], 128)[None, :p.V], Gr, 0.0)
         pick = np.sort(rng.choice(128, 24, replace=False))
         grade_sum(host(dE[torch.from_numpy(rows[pick]).cuda()]), Gf[pick] @ W, np.abs(Gf[pick]) @ aW,
-                  f"full-size dE rows of block {rb}")
+                  f"full-size dE rows of block {rb}", steps=filtered_steps(p.T, p.V)["dE"])
     assert 0 < min(kept_rows) and max(kept_rows) < -(-p.V // 128)
     for cb in (int(p.labels[p.labels >= 0][0]) // 128, 7):   # a block holding a target, and block 7
         cols = np.arange(128 * cb, min(128 * cb + 128, p.V))
@@ -158,7 +171,7 @@ def test_full_size_peaked_sampled(vce):
         Gf = np.where(np.repeat(keep, 128)[:p.T, None], Gc, 0.0)
         pick = np.sort(rng.choice(len(cols), 16, replace=False))
         grade_sum(host(dW[torch.from_numpy(cols[pick]).cuda()]), Gf[:, pick].T @ E, np.abs(Gf[:, pick]).T @ np.abs(E),
-                  f"full-size dW rows of column block {cb}")
+                  f"full-size dW rows of column block {cb}", steps=filtered_steps(p.T, p.V)["dW"])
     assert 0 < int(kept.item()) < -(-p.T // 128) * -(-p.V // 128)
 
 

@@ -91,6 +91,20 @@ def test_noalloc_matches_the_workspace_entry_point_on_two_calls_in_a_row():
     _compare_one_call(vce, p2, w2, "sum", 0.5)
 
 
+def test_noalloc_after_a_larger_call_with_another_chunk_count():
+    """A large call, then a smaller one with a different k and T: the array still holds the
+    large call's statistics in the entries past the small call's k * T, and in the same
+    entries under the other [k][T] layout, so a read at a wrong stride or with a stale k or T
+    would pick up values that are not this call's."""
+    vce = _vce()
+    w1 = [200, 200, 200, 200, 416]
+    p1 = gen.custom(50000, sum(w1), "bf16", seed=503, std=2.0, n_margin=5000, margin=(17.0, 50.0), n_ignore=500)
+    _compare_one_call(vce, p1, w1, "mean", 1.0)
+    w2 = [300, 129, 700]
+    p2 = gen.custom(3001, sum(w2), "bf16", seed=504, std=2.5, n_margin=300, margin=(20.0, 45.0), n_ignore=30)
+    _compare_one_call(vce, p2, w2, "none", 0.75)
+
+
 def test_noalloc_refuses_sizes_beyond_its_array():
     vce = _vce()
     lib = vce.lib

@@ -16,7 +16,9 @@ import torch
 __all__ = ["VceError", "lib", "library_path", "ce_forward", "ce_backward", "ce_forward_ls", "ce_backward_ls",
            "ce_forward_backward", "ce_forward_backward_ls", "ce_merge_chunks", "ce_merge_chunks_ls",
            "ce_merge_chunks_noalloc",
-           "linear_ce_workspace_bytes", "linear_ce_fwd_bwd", "linear_ce_fwd_bwd_filtered", "vce_get_status", "vce_status_string",
+           "linear_ce_workspace_bytes", "linear_ce_fwd_bwd", "linear_ce_fwd_bwd_filtered", "linear_ce_fwd_bwd_timed",
+           "vce_get_status", "vce_status_string", "vce_debug_checks", "vce_debug_status", "use_library",
+           "restore_library",
            "vce_abi_version", "cross_entropy", "IGNORE_INDEX", "F32", "BF16", "RED"]
 
 IGNORE_INDEX = -100
@@ -27,6 +29,8 @@ CHUNK_STATS = 4
 _DT = {torch.float32: F32, torch.bfloat16: BF16}
 
 library_path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libvce.so")
+# the same library built with device-side index checks (build --debug-checks)
+debug_library_path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libvce_debug.so")
 
 
 class VceError(RuntimeError):
@@ -35,17 +39,21 @@ class VceError(RuntimeError):
         super().__init__(f"{fn} failed: {code} ({vce_status_string(code)})")
 
 
-def _load():
-    if not os.path.exists(library_path):
-        raise ImportError(f"{library_path} is not built: run `python -m vocab_cross_entropy_gb300.build` "
+def _load(path=None):
+    path = path or library_path
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is not built: run `python -m vocab_cross_entropy_gb300.build` "
                           "(or __graft_entry__.build()) first; this library has no fallback path")
-    L = ctypes.CDLL(library_path)
+    L = ctypes.CDLL(path)
     p, i64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
     L.vce_abi_version.restype = i32
     L.vce_status_string.argtypes = [i32]
     L.vce_status_string.restype = ctypes.c_char_p
     L.vce_row_stats_floats.restype = sz
     L.vce_get_status.argtypes = [p, p, p]
+    L.vce_debug_checks.restype = i32
+    L.vce_debug_status.argtypes = [p]
+    L.vce_debug_status.restype = i32
     L.ce_forward.argtypes = [p, i32, i64, i64, i64, p, i64, i32, p, p, p, p, p]
     L.ce_backward.argtypes = [p, i32, i64, i64, i64, p, i64, i32, p, p, p, i32, i64, p]
     L.ce_forward_backward.argtypes = [p, i32, i64, i64, i64, p, i64, i32, p, p, p, p, p, i32, i64, p, p]
@@ -65,19 +73,23 @@ def _load():
         if hasattr(L, "linear_ce_fwd_bwd_filtered"):
             L.linear_ce_fwd_bwd_filtered.argtypes = [p, p, i64, i64, i64, p, i64, i32, p, p, p, p, p, i32, f32, p,
                                                      p, sz, p, p]
+        L.linear_ce_fwd_bwd_timed.argtypes = [p, p, i64, i64, i64, p, i64, i32, p, p, p, p, p, i32, f32, p, p, sz,
+                                              p, p, p, p]
         L.vce_gemm_bf16.argtypes = [p, i32, p, i32, i64, i64, i64, p, i64, p]
         L.vce_gemm_bf16.restype = i32
+        L.vce_gemm_bf16_variant.argtypes = [p, i32, p, i32, i64, i64, i64, p, i64, i32, i32, i32, p]
+        L.vce_gemm_bf16_variant.restype = i32
         L.vce_test_gemm_stall.argtypes = [p, p, i64, i64, i64, p, ctypes.c_uint64, p, p]
         L.vce_test_gemm_stall.restype = i32
         if hasattr(L, "vce_test_gemm_skip"):
-            L.vce_test_gemm_skip.argtypes = [p, p, i64, i64, i64, p, i64, i32, p, p]
+            L.vce_test_gemm_skip.argtypes = [p, p, i64, i64, i64, p, i64, p, p]
             L.vce_test_gemm_skip.restype = i32
         L.vce_test_ce_fused_stall.argtypes = [p, i64, i64, p, p, p, p, p, ctypes.c_uint64, p, p]
         L.vce_test_ce_fused_stall.restype = i32
     for name in ("ce_forward", "ce_backward", "ce_forward_ls", "ce_backward_ls", "ce_forward_backward",
                  "ce_forward_backward_ls", "ce_merge_chunks_ls",
                  "ce_merge_chunks", "ce_merge_chunks_noalloc",
-                 "linear_ce_fwd_bwd", "linear_ce_fwd_bwd_filtered",
+                 "linear_ce_fwd_bwd", "linear_ce_fwd_bwd_filtered", "linear_ce_fwd_bwd_timed",
                  "vce_get_status"):
         if hasattr(L, name):
             getattr(L, name).restype = i32
@@ -92,6 +104,34 @@ def _get():
     if _lib is None:
         _lib = _load()
     return _lib
+
+
+def use_library(path):
+    """Route every call of this module to the library at `path` (e.g. debug_library_path, the
+    build with device-side index checks); returns the previous library (None if none was
+    loaded yet).  No fallback: the library must exist."""
+    global _lib
+    prev = _lib
+    _lib = _load(path)
+    return prev
+
+
+def restore_library(prev):
+    """Undo use_library: route calls back to `prev` (None: the default library, loaded on use)."""
+    global _lib
+    _lib = prev
+
+
+def vce_debug_checks() -> bool:
+    """Whether the library in use was built with device-side index checks."""
+    return bool(_get().vce_debug_checks())
+
+
+def vce_debug_status() -> int:
+    """Waits for the device; the first failed index check's code since the last call, or 0."""
+    out = ctypes.c_int32(0)
+    _check("vce_debug_status", _get().vce_debug_status(ctypes.byref(out)))
+    return int(out.value)
 
 
 def __getattr__(name):   # `lib` is loaded on first use, so the build module imports without it
@@ -328,6 +368,20 @@ def vce_gemm_bf16(A, B, a_mn=False, b_mn=False, *, C=None, stream=None):
     return C
 
 
+def vce_gemm_bf16_variant(A, B, a_mn=False, b_mn=False, *, pair=False, bn=256, seg_kb=0, C=None, stream=None):
+    """vce_gemm_bf16 in a chosen launch form: CTA pairs or single CTAs, 128- or 256-column
+    tiles, compensated accumulation over runs of seg_kb * 64 products (bn = 128)."""
+    M = A.shape[1] if a_mn else A.shape[0]
+    K = A.shape[0] if a_mn else A.shape[1]
+    N = B.shape[1] if b_mn else B.shape[0]
+    if C is None:
+        C = torch.empty(M, N, dtype=torch.float32, device=A.device)
+    _check("vce_gemm_bf16_variant", _get().vce_gemm_bf16_variant(
+        _ptr(A), int(a_mn), _ptr(B), int(b_mn), M, N, K, _ptr(C), C.stride(0), int(pair), int(bn), int(seg_kb),
+        _stream(stream)))
+    return C
+
+
 def vce_test_gemm_stall(A, B, wait_ns=50_000_000, *, stream=None):
     """Run the GEMM pipeline with a stage that never completes; returns the device status word."""
     M, K = A.shape
@@ -339,14 +393,14 @@ def vce_test_gemm_stall(A, B, wait_ns=50_000_000, *, stream=None):
     return vce_get_status(status, stream)
 
 
-def vce_test_gemm_skip(A, B, skip_bits, pair=False, *, stream=None):
+def vce_test_gemm_skip(A, B, skip_bits, *, stream=None):
     """C = A B^T over the 128-column K blocks whose bit is set for each 128-row M tile;
-    skip_bits an int32 device tensor [ceil(M/128), words]; pair runs 2-CTA clusters."""
+    skip_bits an int32 device tensor [ceil(M/128), words]."""
     M, K = A.shape
     N = B.shape[0]
     C = torch.empty(M, N, dtype=torch.float32, device=A.device)
     _check("vce_test_gemm_skip", _get().vce_test_gemm_skip(_ptr(A), _ptr(B), M, N, K, _ptr(skip_bits),
-                                                        skip_bits.shape[1], int(pair), _ptr(C), _stream(stream)))
+                                                        skip_bits.shape[1], _ptr(C), _stream(stream)))
     return C
 
 
@@ -396,8 +450,26 @@ def linear_ce_fwd_bwd_filtered(E, W, labels, filter_eps, ignore_index=IGNORE_IND
     return out + (kept_blocks,)
 
 
+GEMM_KINDS = ("statistics", "gradient_tiles", "dW", "dE")
+
+
+def linear_ce_fwd_bwd_timed(E, W, labels, filter_eps=0.0, ignore_index=IGNORE_INDEX, reduction="mean", *,
+                            grad_output=None, grad_dtype=None, dE=None, dW=None, loss_rows=None, loss_out=None,
+                            workspace=None, kept_blocks=None, status=None, stream=None):
+    """linear_ce_fwd_bwd(_filtered) with CUDA events around each GEMM launch (blocking).
+
+    Returns ((loss_out, loss_rows, dE, dW, status), {kind: (milliseconds, launches)}) for the
+    GEMM kinds in GEMM_KINDS.
+    """
+    ms = (ctypes.c_float * 4)()
+    n = (ctypes.c_int * 4)()
+    out = _linear_ce(E, W, labels, ignore_index, reduction, grad_output, grad_dtype, dE, dW, loss_rows, loss_out,
+                     workspace, status, stream, float(filter_eps), kept_blocks, timed=(ms, n))
+    return out, {k: (float(ms[i]), int(n[i])) for i, k in enumerate(GEMM_KINDS)}
+
+
 def _linear_ce(E, W, labels, ignore_index, reduction, grad_output, grad_dtype, dE, dW, loss_rows, loss_out,
-               workspace, status, stream, filter_eps, kept_blocks):
+               workspace, status, stream, filter_eps, kept_blocks, timed=None):
     T, D = E.shape
     V = W.shape[0]
     dev = E.device
@@ -413,7 +485,12 @@ def _linear_ce(E, W, labels, ignore_index, reduction, grad_output, grad_dtype, d
     need = linear_ce_workspace_bytes(T, D, V)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
-    if filter_eps is None:
+    if timed is not None:
+        _check("linear_ce_fwd_bwd_timed", _get().linear_ce_fwd_bwd_timed(
+            _ptr(E), _ptr(W), T, D, V, _ptr(labels), int(ignore_index), RED[reduction], _ptr(grad_output),
+            _ptr(loss_rows), _ptr(loss_out), _ptr(dE), _ptr(dW), _dtype(dE), filter_eps, _ptr(kept_blocks),
+            _ptr(workspace), workspace.numel(), _ptr(status), _stream(stream), timed[0], timed[1]))
+    elif filter_eps is None:
         _check("linear_ce_fwd_bwd", _get().linear_ce_fwd_bwd(
             _ptr(E), _ptr(W), T, D, V, _ptr(labels), int(ignore_index), RED[reduction], _ptr(grad_output),
             _ptr(loss_rows), _ptr(loss_out), _ptr(dE), _ptr(dW), _dtype(dE), _ptr(workspace), workspace.numel(),

@@ -1,7 +1,10 @@
 """Build libvce.so in-tree from csrc/*.cu for sm_103a (nvcc, one translation unit per file,
 compiled in parallel, then linked with the static CUDA runtime).
 
-    python -m vocab_cross_entropy_gb300.build [--force] [--verbose]
+    python -m vocab_cross_entropy_gb300.build [--force] [--verbose] [--debug-checks]
+
+--debug-checks builds libvce_debug.so instead: the same library with device-side index
+checks (csrc/vce_check.cuh) compiled in.
 """
 from __future__ import annotations
 
@@ -17,6 +20,9 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libvce.so")
+# the debug build: the same sources with device-side index checks (csrc/vce_check.cuh)
+BUILD_DEBUG = os.path.join(PKG, "_build_debug")
+LIB_DEBUG = os.path.join(PKG, "libvce_debug.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "-I", INCLUDE, "-I", CSRC,
@@ -42,18 +48,21 @@ def _stale(target, sources):
     return any(os.path.getmtime(s) > t for s in sources)
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, debug_checks: bool = False) -> str:
+    """Compile libvce.so (or, with debug_checks, libvce_debug.so with -DVCE_DEBUG_CHECKS)."""
+    build_dir, lib = (BUILD_DEBUG, LIB_DEBUG) if debug_checks else (BUILD, LIB)
+    flags = NVCC_FLAGS + (["-DVCE_DEBUG_CHECKS"] if debug_checks else [])
+    os.makedirs(build_dir, exist_ok=True)
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     deps = _deps()
     nvcc = _nvcc()
     objs = []
     jobs = []
     for s in srcs:
-        o = os.path.join(BUILD, os.path.basename(s)[:-3] + ".o")
+        o = os.path.join(build_dir, os.path.basename(s)[:-3] + ".o")
         objs.append(o)
         if force or _stale(o, [s] + deps):
-            jobs.append([nvcc, *ARCH, *NVCC_FLAGS, "-c", s, "-o", o] + (["-Xptxas", "-v"] if verbose else []))
+            jobs.append([nvcc, *ARCH, *flags, "-c", s, "-o", o] + (["-Xptxas", "-v"] if verbose else []))
 
     def run(cmd):
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -65,12 +74,13 @@ def build(force: bool = False, verbose: bool = False) -> str:
     if jobs:
         with ThreadPoolExecutor(max(1, min(len(jobs), os.cpu_count() or 1))) as ex:
             list(ex.map(run, jobs))
-    if force or jobs or _stale(LIB, objs):
-        tmp = LIB + f".tmp{os.getpid()}"
+    if force or jobs or _stale(lib, objs):
+        tmp = lib + f".tmp{os.getpid()}"
         run([nvcc, *ARCH, "-shared", "-o", tmp, *objs])
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="--verbose" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose="--verbose" in sys.argv,
+                debug_checks="--debug-checks" in sys.argv))

@@ -19,6 +19,7 @@
 #include "ce_segments.h"
 #include "vce.h"
 #include "vce_device.cuh"
+#include "vce_check.cuh"
 #include "vce_host.h"
 
 namespace vce {
@@ -34,6 +35,9 @@ __global__ void __launch_bounds__(NT) k_ce_bwd(const __grid_constant__ SegTable 
     for (int64_t it = blockIdx.x; it < items; it += gridDim.x) {
         const int64_t row = it / tab.k;
         const int c = (int)(it - row * tab.k);
+        if (!dbg::ok(c >= 0 && c < tab.k && row < tab.T, dbg::kChunk) ||
+            !dbg::ok(tab.width[c] <= tab.ld_in[c] && tab.width[c] <= tab.ld_out[c], dbg::kCols))
+            continue;   // block-uniform
         const float4 st = row_stats[row];
         const bool zero = (st.w == 0.f);   // ignored row or bad label: +0.0 by selection
         const float cg = zero ? 0.f : grad_output[go_per_row ? row : 0] * st.w;
@@ -66,6 +70,8 @@ cudaError_t dispatch_bwd2(int nt, const SegTable& tab, const int64_t* labels, co
 }
 
 }  // namespace
+
+VCE_DEBUG_READER(debug_word_ce_bwd)
 
 cudaError_t launch_ce_bwd(vce_dtype dt, vce_dtype gdt, int nt, const SegTable& tab, const int64_t* labels,
                          const float* rs, const float* go, int per_row, cudaStream_t s, float eov) {

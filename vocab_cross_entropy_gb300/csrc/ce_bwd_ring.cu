@@ -31,6 +31,7 @@
 #include "vce.h"
 #include "vce_async.cuh"
 #include "vce_device.cuh"
+#include "vce_check.cuh"
 #include "vce_host.h"
 
 namespace vce {
@@ -139,6 +140,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_bwd_ring(const __grid_consta
                             break;
                         }
                         const uint32_t nb = (uint32_t)std::min<int64_t>(kChunk, bytes - (int64_t)j * kChunk);
+                        if (!dbg::ok(row < tab.T && c < tab.k && (int64_t)j * kChunk + nb <= bytes &&
+                                         w <= tab.ld_in[c],
+                                     dbg::kCols)) {
+                            *abort_flag = 1;   // no copy: the other roles stop at their next wait
+                            stop = true;
+                            break;
+                        }
                         tc::mbar_arrive_expect_tx(&ctl.full[st], nb);
                         tc::bulk_load(smem + st * kChunk, src + (int64_t)j * kChunk, nb, &ctl.full[st]);
                         ++q;
@@ -166,6 +174,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_bwd_ring(const __grid_consta
                 const int64_t it = base + (int64_t)b * stride;
                 const int64_t row = it / tab.k;
                 const int c = (int)(it - row * tab.k);
+                if (!dbg::ok(row < tab.T && c < tab.k && tab.width[c] <= tab.ld_out[c], dbg::kCols)) continue;
                 O* grow = static_cast<O*>(tab.out[c]) + row * tab.ld_out[c];
                 const float zero[G] = {};
                 for (int64_t vi = lane; vi < tab.width[c] / G; vi += 32) GroupStore<O, G>::run(grow + vi * G, zero);
@@ -198,7 +207,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_bwd_ring(const __grid_consta
                     const int nvec = (int)(std::min<int64_t>(kChunk, bytes - (int64_t)j * kChunk) / 16);
                     const int col0 = j * (kChunk / (int)sizeof(S));
                     const int rel0 = ri.tl - (col0 + tid * G);
-                    if (nvec == kVecPerThread * kConsumers)
+                    if (!dbg::ok((int64_t)col0 + (int64_t)nvec * G <= bytes / es && nvec <= kChunk / 16, dbg::kCols))
+                        ;   // the stage's columns would leave the item's row: no store
+                    else if (nvec == kVecPerThread * kConsumers)
                         stage::bwd_stage<S, O, kConsumers, kVecPerThread, true, kShift>(
                             buf, nvec, grow + col0, rel0, tid, ri.coef, ri.bias, ri.gt, ri.shift);
                     else
@@ -224,6 +235,8 @@ cudaError_t launch(const Args& args, const SegTable& tab, cudaStream_t s) {
 }
 
 }  // namespace bring
+
+VCE_DEBUG_READER(debug_word_ce_bwd_ring)
 
 cudaError_t launch_bwd_ring(vce_dtype dt, vce_dtype gdt, const SegTable& tab, const int64_t* labels,
                             const float* row_stats, const float* grad_output, int go_per_row, float eps_over_v,

@@ -25,6 +25,7 @@
 #include "ce_segments.h"
 #include "vce.h"
 #include "vce_device.cuh"
+#include "vce_check.cuh"
 #include "vce_host.h"
 
 namespace vce {
@@ -65,6 +66,7 @@ __global__ void __launch_bounds__(NT, 1024 / NT)
     const float w_valid = (red == VCE_RED_MEAN) ? *inv_n : 1.f;
     for (int64_t row = blockIdx.x; row < T; row += gridDim.x) {
         const int64_t t = labels[row];
+        if (!dbg::ok(row >= 0 && row < T && V <= ld && V <= ld_g, dbg::kRow)) continue;   // block-uniform
         const S* in = logits + row * ld;
         O* out = grad + row * ld_g;
         const bool ignored = (t == ignore_index);
@@ -133,6 +135,9 @@ cudaError_t dispatch_fused2(int nt, const void* logits, int64_t T, int64_t V, in
 }
 
 }  // namespace
+
+VCE_DEBUG_READER(debug_word_ce_fused)
+
 }  // namespace vce
 
 using namespace vce;

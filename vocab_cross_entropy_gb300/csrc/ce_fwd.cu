@@ -27,6 +27,7 @@
 
 #include "vce.h"
 #include "vce_device.cuh"
+#include "vce_check.cuh"
 #include "vce_host.h"
 #include "ce_rows.cuh"
 #include "ce_segments.h"
@@ -58,6 +59,7 @@ __global__ void __launch_bounds__(NT, (kSmooth ? 1024 : 1536) / NT) k_ce_fwd(con
             }
             continue;
         }
+        if (!dbg::ok(row >= 0 && row < T && V <= ld, dbg::kRow)) continue;   // block-uniform
         float m = -kInf, s = 0.f, mb = 0.f, sz = 0.f;
         fwd_segment<S, NT, true, kLoadStream, kSmooth>(logits + row * ld, V, t, m, s, mb, &sm_zt, threadIdx.x, &sz);
         if (kSmooth) {   // block sum of the logits (the barrier below publishes the warp sums)
@@ -154,6 +156,9 @@ __global__ void __launch_bounds__(kChunkThreads, 2) k_ce_chunk_fwd(const __grid_
     for (int64_t it = (int64_t)blockIdx.x * (kChunkThreads / 32) + (threadIdx.x >> 5); it < items; it += warps) {
         const int64_t row = it / tab.k;
         const int c = (int)(it - row * tab.k);
+        if (!dbg::ok(c >= 0 && c < tab.k && row < tab.T, dbg::kChunk) ||
+            !dbg::ok(tab.width[c] <= tab.ld_in[c], dbg::kCols))
+            continue;   // warp-uniform
         const int64_t t = labels[row];
         const int64_t w = tab.width[c];
         const int64_t tl = (t == ignore_index) ? -1 : t - tab.off[c];
@@ -255,6 +260,8 @@ int check_common(vce_dtype dt, vce_reduction red, int64_t T) {
 }
 
 }  // namespace
+
+VCE_DEBUG_READER(debug_word_ce_fwd)
 
 cudaError_t launch_stats_merge(const float* part, int k, int64_t T, int64_t V, const int64_t* labels,
                                int64_t ignore_index, float* loss_rows, float* row_stats, int32_t* status,

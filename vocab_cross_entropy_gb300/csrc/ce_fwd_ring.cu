@@ -32,6 +32,7 @@
 #include "vce.h"
 #include "vce_async.cuh"
 #include "vce_device.cuh"
+#include "vce_check.cuh"
 #include "vce_host.h"
 
 namespace vce {
@@ -149,6 +150,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_fwd_ring(const __grid_consta
                             break;
                         }
                         const uint32_t nb = (uint32_t)std::min<int64_t>(kChunk, bytes - (int64_t)j * kChunk);
+                        if (!dbg::ok(row < a.T && (int64_t)j * kChunk + nb <= bytes && a.V <= a.ld, dbg::kCols)) {
+                            *abort_flag = 1;   // no copy: the other roles stop at their next wait
+                            stop = true;
+                            break;
+                        }
                         tc::mbar_arrive_expect_tx(&ctl.full[st], nb);
                         tc::bulk_load(smem + st * kChunk, src + (int64_t)j * kChunk, nb, &ctl.full[st]);
                         ++q;
@@ -272,6 +278,8 @@ cudaError_t launch(const Args& args, int sms, cudaStream_t s) {
 }
 
 }  // namespace fring
+
+VCE_DEBUG_READER(debug_word_ce_fwd_ring)
 
 cudaError_t launch_fwd_ring(vce_dtype dt, const void* logits, int64_t T, int64_t V, int64_t ld, const int64_t* labels,
                             int64_t ignore_index, float eps, float* loss_rows, float* row_stats, int32_t* status,

@@ -13,7 +13,10 @@
 // loaded holds its 4 MiB until the process exits.  Host code cannot use the array's name as
 // a device address (in host code it names a host-side stand-in), so the device address is
 // looked up once per device with cudaGetSymbolAddress, with that device current, and passed
-// to the kernels.
+// to the kernels.  The lookup is remembered together with the unique id of the device's
+// current context: after a device reset the context, the loaded module and the array are new,
+// and the next call looks the address up again.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -27,20 +30,57 @@ namespace {
 constexpr long long kScratchEntries = VCE_NOALLOC_MAX_CHUNK_ROWS;
 static __device__ __align__(256) float4 g_chunk_stats_scratch[kScratchEntries];
 
-float* g_scratch_addr[vce::kMaxDevices];   // device address of the array on each device, once known
+struct ScratchEntry {
+    unsigned long long ctx_id;   // unique id of the context the address belongs to (0: none yet)
+    float* addr;
+};
+ScratchEntry g_scratch[vce::kMaxDevices];
 std::mutex g_scratch_mu;
 
-// The array's device address on the current device; the first call for a device looks it up.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+// The unique id of the calling thread's current context (process-wide unique, never reused),
+// through the driver entry points the runtime hands out; false if it cannot be read.
+bool current_context_id(unsigned long long* id) {
+    static CtxGetCurrentFn get_current = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    if (!get_current || !get_id) {
+        void* a = nullptr;
+        void* b = nullptr;
+        cudaDriverEntryPointQueryResult qa, qb;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &a, 12000, cudaEnableDefault, &qa) != cudaSuccess ||
+            qa != cudaDriverEntryPointSuccess ||
+            cudaGetDriverEntryPointByVersion("cuCtxGetId", &b, 12000, cudaEnableDefault, &qb) != cudaSuccess ||
+            qb != cudaDriverEntryPointSuccess)
+            return false;
+        get_current = reinterpret_cast<CtxGetCurrentFn>(a);
+        get_id = reinterpret_cast<CtxGetIdFn>(b);
+    }
+    CUcontext ctx = nullptr;
+    if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return false;
+    return get_id(ctx, id) == CUDA_SUCCESS && *id != 0;
+}
+
+// The array's device address on the current device; the first call for a device (and the
+// first after a reset of it) looks it up.
 int scratch_address(float** out) {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= vce::kMaxDevices) return VCE_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (!g_scratch_addr[dev]) {
+    ScratchEntry& e = g_scratch[dev];
+    unsigned long long id = 0;
+    const bool have_ctx = current_context_id(&id);
+    if (!have_ctx || e.ctx_id != id || !e.addr) {
+        // (with no context current on this thread yet, the lookup makes the device's primary
+        // context current)
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_chunk_stats_scratch) != cudaSuccess || p == nullptr) return VCE_ERR_CUDA;
-        g_scratch_addr[dev] = static_cast<float*>(p);
+        if (!have_ctx && !current_context_id(&id)) return VCE_ERR_CUDA;
+        e.addr = static_cast<float*>(p);
+        e.ctx_id = id;
     }
-    *out = g_scratch_addr[dev];
+    *out = e.addr;
     return VCE_OK;
 }
 

@@ -48,6 +48,7 @@
 #include "ce_stage.cuh"
 #include "vce_async.cuh"
 #include "vce_device.cuh"
+#include "vce_check.cuh"
 #include "vce_host.h"
 
 namespace vce {
@@ -242,6 +243,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_fused_ring(const __grid_cons
                                        a.wait_ns, kSuspendRole))
                         break;
                     const uint32_t nb = (uint32_t)min(kChunk, bytes - j * kChunk);
+                    if (!dbg::ok(row < a.T && c0 + w <= a.V && a.V <= a.ld && j * kChunk + (int)nb <= bytes,
+                                 dbg::kCols)) {
+                        *abort_flag = 1;   // no copy: the other roles stop at their next wait
+                        break;
+                    }
                     tc::mbar_arrive_expect_tx(&ctl.full[st], nb + a.tx_extra);
                     tc::bulk_load(smem + st * kChunk, src + (int64_t)j * kChunk, nb, &ctl.full[st]);
                     ++q;
@@ -331,6 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_fused_ring(const __grid_cons
                     a.row_stats[row] = make_float4(0.f, 0.f, 0.f, 0.f);
                     if (t != a.ignore_index) atomicCAS(a.status, 0, (int32_t)VCE_ERR_LABEL);
                 }
+                if (!dbg::ok(c0 + w <= a.ld_g, dbg::kCols)) continue;
                 O* grow = static_cast<O*>(a.grad) + row * a.ld_g + c0;
                 const float zero[G] = {};
                 for (int vi = lane; vi < w / G; vi += 32) GroupStore<O, G>::run(grow + vi * G, zero);
@@ -398,7 +405,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_fused_ring(const __grid_cons
                     const int nvec = min(kChunk, bytes - j * kChunk) / 16;
                     const int col0 = j * (kChunk / (int)sizeof(S));
                     const int rel0 = ri.tl - (col0 + tid * G);
-                    if (nvec == kFullVec)
+                    if (!dbg::ok(col0 + nvec * G <= w && c0 + w <= a.ld_g, dbg::kCols))
+                        ;   // the stage's columns would leave the CTA's slice: no store
+                    else if (nvec == kFullVec)
                         stage::bwd_stage<S, O, kConsumers, kVecPerThread, true, kSmooth, true>(
                             buf, nvec, grow + col0, rel0, tid, cf.x, cf.y, cf.z, cf.w);
                     else
@@ -476,6 +485,8 @@ cudaError_t launch_cs(int C, const Args& args, int sms, cudaStream_t s, bool* la
 }
 
 }  // namespace ring
+
+VCE_DEBUG_READER(debug_word_ce_ring)
 
 cudaError_t launch_fused_ring(vce_dtype dt, vce_dtype gdt, const void* logits, int64_t T, int64_t V, int64_t ld,
                               const int64_t* labels, int64_t ignore_index, int red, const float* grad_output,

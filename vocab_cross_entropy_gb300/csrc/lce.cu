@@ -8,27 +8,30 @@
 //
 // Steps, all on the tensor cores through tc_gemm.cuh (bf16 operands, fp32 accumulators); every
 // operand is read in its natural row-major layout (K-major or MN-major tiles):
-//   1. z = E W^T tile by tile (128 rows x 256 vocabulary columns, K = D); the epilogue keeps
-//      per-row (max, sum-exp) over the tile's non-target columns and the target logit, one
-//      partial per (row, vocabulary tile); a merge gives L', x, the loss and row_stats.
+//   1. z = E W^T tile by tile (256 rows on a CTA pair x 256 vocabulary columns, K = D); the
+//      epilogue keeps per-row (max, sum-exp) over the tile's non-target columns and the target
+//      logit, one partial per (row, vocabulary tile); a merge gives L', x, the loss and row_stats.
 //   2. per vocabulary chunk of Vc columns:
 //        G = c (softmax - onehot) of the recomputed z tile, split G = G_hi + G_lo in bf16
 //            (a 16-bit significand in total), written once as [T, Vc];
-//        dW[chunk] = G^T E      (A = G MN-major, B = E MN-major, K = 2T: G_hi^T E + G_lo^T E;
-//                                one complete reduction)
-//        dE      += G W[chunk]  (A = G K-major, B = W MN-major, K = 2Vc), merged across chunks
-//                               with a two-sum compensated fp32 accumulator pair.
+//        dW[chunk] = G^T E      (A = G MN-major, B = E MN-major, K = 2T: G_hi^T E + G_lo^T E)
+//        dE      += G W[chunk]  (A = G K-major, B = W MN-major, K = 2Vc)
+//      Both gradient GEMMs accumulate compensated: every 1024 products of the K loop are summed
+//      afresh in tensor memory and added into a (sum, compensation) pair with a two-sum; dE's
+//      pair is carried across chunks in global memory, merged the same way.
 #include <cuda.h>
 #include <cuda_runtime.h>
-#include <cudaTypedefs.h>
 #include <stdint.h>
 
 #include <algorithm>
 #include <atomic>
+#include <vector>
 
 #include "tc_gemm.cuh"
+#include "tc_launch.cuh"
 #include "vce.h"
 #include "vce_device.cuh"
+#include "vce_check.cuh"
 #include "vce_host.h"
 #include "vce_linear.h"
 
@@ -36,8 +39,12 @@ namespace vce {
 namespace {
 
 using tc::BM;
-using tc::BN;
 using tc::BK;
+using tc::Mat;
+using tc::Variant;
+
+constexpr int BN = 256;                 // vocabulary columns of a z tile (statistics, gradient tiles)
+constexpr int kSegKb = 16;              // K blocks (of 64) per compensated accumulation segment
 
 constexpr int64_t kChunkCols = 32768;   // vocabulary columns per gradient chunk (a multiple of BN)
 
@@ -49,6 +56,7 @@ inline int64_t round_up(int64_t a, int64_t b) { return cdiv(a, b) * b; }
 
 // Step 1: per (row, vocabulary tile): (max, sum-exp) over non-target columns < V, target logit.
 struct EpiStats {
+    static constexpr bool kCompensated = false;
     struct Params {
         const int64_t* labels;
         int64_t ignore_index, T, V;
@@ -68,7 +76,7 @@ struct EpiStats {
         r.t = row < p.T ? p.labels[row] : p.ignore_index;
         if (r.t == p.ignore_index) r.t = -1;
     }
-    __device__ __forceinline__ static void consume(const Params& p, Row& r, int, int col0, const uint32_t (&acc)[32], uint8_t*) {
+    __device__ __forceinline__ static void consume(const Params& p, Row& r, int, int col0, const uint32_t (&acc)[32]) {
         float v[32];
 #pragma unroll
         for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(acc[k]);
@@ -100,6 +108,7 @@ struct EpiStats {
 // ORs its 32 rows' marks; the first warp to set a block's bit also sets it in the transposed
 // table and counts the block.
 struct EpiGrad {
+    static constexpr bool kCompensated = false;
     struct Params {
         const int64_t* labels;
         int64_t T, width, col_off;   // rows, chunk width, chunk's first global column
@@ -143,7 +152,7 @@ struct EpiGrad {
         }
     }
     __device__ __forceinline__ static void consume(const Params& p, Row& r, int row, int col0,
-                                                   const uint32_t (&acc)[32], uint8_t*) {
+                                                   const uint32_t (&acc)[32]) {
         uint32_t hi[16], lo[16];
         float emax = 0.f;   // largest 2^(z log2e - bias) over the piece's columns < width
 #pragma unroll
@@ -170,6 +179,8 @@ struct EpiGrad {
         // row-major [T_pad][ldg]: 64 contiguous bytes per thread.  Evict-first stores: the
         // chunk's G (512 MB at T = 8192) is read back from DRAM by the next two GEMMs anyway,
         // and should not push E and W out of L2 meanwhile (measured 0.4% faster per call).
+        // G is [round_up(T, 128)][ldg]
+        if (!dbg::ok(row < (p.T + 127) / 128 * 128 && col0 + 32 <= p.ldg, dbg::kTile)) return;
         uint4* dh = reinterpret_cast<uint4*>(p.g_hi + (int64_t)row * p.ldg + col0);
         uint4* dl = reinterpret_cast<uint4*>(p.g_lo + (int64_t)row * p.ldg + col0);
 #pragma unroll
@@ -195,54 +206,13 @@ struct EpiGrad {
     }
 };
 
-// Step 2b: dW rows of the chunk, stored once (bf16 round-to-nearest-even or fp32), evict-first:
-// nothing in the call reads them back.
-struct EpiStore {
-    struct Params {
-        void* out;
-        int64_t ld, rows, cols, row_off;
-        int bf16;
-    };
-    struct Row {};
-    __device__ __forceinline__ static void begin(const Params&, Row&, int, int) {}
-    __device__ __forceinline__ static void consume(const Params& p, Row&, int row, int col0, const uint32_t (&acc)[32], uint8_t*) {
-        if (row >= p.rows || col0 >= p.cols) return;
-        const int64_t base = (p.row_off + row) * p.ld + col0;
-        const int n = (p.cols - col0) < 32 ? (int)(p.cols - col0) : 32;
-        if (p.bf16) {
-            uint16_t* o = reinterpret_cast<uint16_t*>(p.out) + base;
-            if (n == 32) {
-                uint32_t w[16];
-#pragma unroll
-                for (int k = 0; k < 16; ++k) w[k] = pack_bf16x2(__uint_as_float(acc[2 * k]), __uint_as_float(acc[2 * k + 1]));
-                uint4* d = reinterpret_cast<uint4*>(o);
-#pragma unroll
-                for (int q = 0; q < 4; ++q) st_stream16(d + q, make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]));
-            } else {
-#pragma unroll
-                for (int k = 0; k < 32; ++k)
-                    if (k < n) o[k] = to_bf16(__uint_as_float(acc[k]));
-            }
-        } else {
-            float* o = reinterpret_cast<float*>(p.out) + base;
-            if (n == 32) {
-                uint4* d = reinterpret_cast<uint4*>(o);
-#pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    st_stream16(d + q, make_uint4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]));
-            } else {
-#pragma unroll
-                for (int k = 0; k < 32; ++k)
-                    if (k < n) o[k] = __uint_as_float(acc[k]);
-            }
-        }
-    }
-    __device__ __forceinline__ static void end(const Params&, Row&, int, int) {}
-};
+// Step 2b, dW rows of the chunk: tc::EpiStore (stored once as sum + compensation).
 
-// Step 2c: dE partial of one chunk added into (sum, compensation) with a two-sum; the first
-// chunk initialises the pair, the last writes sum + compensation to the output.
+// Step 2c: the dE partial of one chunk, a (sum, compensation) pair of fp32 tiles, merged into
+// the pair carried in global memory with a two-sum; the first chunk initialises it, the last
+// writes sum + compensation to the output.
 struct EpiKahan {
+    static constexpr bool kCompensated = true;
     struct Params {
         float *sum, *comp;   // [rows][cols]
         int64_t rows, cols;
@@ -252,26 +222,14 @@ struct EpiKahan {
     };
     struct Row {};
     __device__ __forceinline__ static void begin(const Params&, Row&, int, int) {}
-    // a + x = t + e exactly (Knuth's two-sum); the compensation accumulates e
-    __device__ __forceinline__ static void two_sum(float a, float x, float& t, float& e) {
-        t = a + x;
-        const float bp = t - a;
-        e = (a - (t - bp)) + (x - bp);
+    // (a, ka) + (x, kx) -> (s, c): s + c = a + x exactly up to the compensations' own sum
+    __device__ __forceinline__ static void merge(float a, float ka, float x, float kx, float& s, float& c) {
+        float e;
+        tc::two_sum(a, x, s, e);
+        c = (ka + kx) + e;
     }
-    __device__ __forceinline__ static void put(const Params& p, int64_t i, float s, float c) {
-        if (p.last) {
-            const float v = s + c;
-            if (p.bf16)
-                reinterpret_cast<uint16_t*>(p.out)[i] = to_bf16(v);
-            else
-                reinterpret_cast<float*>(p.out)[i] = v;
-        } else {
-            p.sum[i] = s;
-            p.comp[i] = c;
-        }
-    }
-    __device__ __forceinline__ static void consume(const Params& p, Row&, int row, int col0, const uint32_t (&acc)[32],
-                                                   uint8_t*) {
+    __device__ __forceinline__ static void consume2(const Params& p, Row&, int row, int col0, const float (&x)[32],
+                                                    const float (&kx)[32]) {
         if (row >= p.rows || col0 >= p.cols) return;
         const int64_t base = (int64_t)row * p.cols + col0;
         if (p.cols - col0 >= 32) {   // full 32-column piece: 16-byte accesses
@@ -290,20 +248,14 @@ struct EpiKahan {
 #pragma unroll
                 for (int q = q0; q < q0 + 4; ++q) {
                     float s[4], c[4];
-                    const float x[4] = {__uint_as_float(acc[4 * q]), __uint_as_float(acc[4 * q + 1]),
-                                        __uint_as_float(acc[4 * q + 2]), __uint_as_float(acc[4 * q + 3])};
                     if (p.first) {
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) { s[e] = x[e]; c[e] = 0.f; }
+                        for (int e = 0; e < 4; ++e) { s[e] = x[4 * q + e]; c[e] = kx[4 * q + e]; }
                     } else {
                         const float av[4] = {ld_a[q - q0].x, ld_a[q - q0].y, ld_a[q - q0].z, ld_a[q - q0].w};
                         const float kv[4] = {ld_k[q - q0].x, ld_k[q - q0].y, ld_k[q - q0].z, ld_k[q - q0].w};
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            float err;
-                            two_sum(av[e], x[e], s[e], err);
-                            c[e] = kv[e] + err;
-                        }
+                        for (int e = 0; e < 4; ++e) merge(av[e], kv[e], x[4 * q + e], kx[4 * q + e], s[e], c[e]);
                     }
                     if (p.last) {
                         if (p.bf16) {
@@ -326,15 +278,28 @@ struct EpiKahan {
 #pragma unroll
         for (int k = 0; k < 32; ++k) {
             if (k >= n) break;
-            const float x = __uint_as_float(acc[k]);
-            float sv = x, cv = 0.f;
-            if (!p.first) {
-                float err;
-                two_sum(p.sum[base + k], x, sv, err);
-                cv = p.comp[base + k] + err;
+            float sv = x[k], cv = kx[k];
+            if (!p.first) merge(p.sum[base + k], p.comp[base + k], x[k], kx[k], sv, cv);
+            if (p.last) {
+                if (p.bf16)
+                    reinterpret_cast<uint16_t*>(p.out)[base + k] = to_bf16(sv + cv);
+                else
+                    reinterpret_cast<float*>(p.out)[base + k] = sv + cv;
+            } else {
+                p.sum[base + k] = sv;
+                p.comp[base + k] = cv;
             }
-            put(p, base + k, sv, cv);
         }
+    }
+    // an uncompensated accumulator tile (filtered GEMMs): the pair (acc, 0)
+    __device__ __forceinline__ static void consume(const Params& p, Row& r, int row, int col0, const uint32_t (&acc)[32]) {
+        float x[32], z[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+            x[k] = __uint_as_float(acc[k]);
+            z[k] = 0.f;
+        }
+        consume2(p, r, row, col0, x, z);
     }
     __device__ __forceinline__ static void end(const Params&, Row&, int, int) {}
 };
@@ -342,111 +307,26 @@ struct EpiKahan {
 // ------------------------------------------------------------------------------------------
 // host side
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+// CUDA events around each GEMM launch of one call, on the call's stream (measurement only).
+struct GemmTimer {
+    enum { kStats = 0, kGrad = 1, kDW = 2, kDE = 3, kKinds = 4 };
+    std::vector<cudaEvent_t> ev;   // begin and end of each launch, in launch order
+    std::vector<int> kind;         // the kind of each launch
+    bool mark(cudaStream_t s) {
+        cudaEvent_t e;
+        if (cudaEventCreate(&e) != cudaSuccess) return false;
+        ev.push_back(e);
+        return cudaEventRecord(e, s) == cudaSuccess;
     }
-    return fn;
-}
-
-// 2-D bf16 map over a row-major [outer, inner] matrix with row pitch ld elements; box
-// box_rows x 64 elements (128 B, the swizzle span).  Loads past the extents read zeros.
-bool make_map(CUtensorMap* m, const void* base, int64_t inner, int64_t outer, int64_t ld, int box_rows) {
-    auto fn = encode_fn();
-    if (!fn) return false;
-    cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
-    cuuint64_t strides[1] = {(cuuint64_t)(ld * 2)};
-    cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
-    cuuint32_t es[2] = {1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-
-// Clusters of two CTAs that fit on the device at once, queried once per device and kernel
-// (0: none fit, the caller then launches single CTAs).
-template <class K>
-int pair_clusters(K kern) {
-    static std::atomic<int> fit[kMaxDevices];
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
-    int clusters = fit[dev].load() - 1;
-    if (clusters < 0) {
-        cudaLaunchConfig_t cfg = {};
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.gridDim = dim3(2 * (device_sm_count() / 2));
-        cfg.blockDim = dim3(tc::kThreads);
-        cfg.dynamicSmemBytes = tc::SMEM_BYTES;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess) {
-            (void)cudaGetLastError();
-            clusters = 0;
-        }
-        fit[dev].store(clusters + 1);
+    bool begin(cudaStream_t s) { return mark(s); }
+    bool end(cudaStream_t s, int k) {
+        kind.push_back(k);
+        return mark(s);
     }
-    return clusters;
-}
-
-// Runs one GEMM.  With an even tiles_m the grid runs as 2-CTA clusters that share each B tile
-// (k_tc_gemm's kPair); a K-major B is then read through b_half, the same matrix with boxes of
-// BN/2 rows.  Otherwise, or when no 2-CTA cluster fits, one CTA per SM through b.  GEMMs that
-// skip K blocks (gradient filtering) also run one CTA per SM: a pair loads the union of both
-// tiles' K blocks, and with sparse tiles that costs more than the shared B tile saves
-// (measured 22.77 against 21.98 ms for a filtered call keeping 12% of the blocks).
-// pair_mode: -1 the rule above, 0 never pairs, 1 pairs whenever tiles_m is even (skip or not;
-// the test hook uses it to run the pair path with skip bits).
-template <class Epi, bool kAmn = false, bool kBmn = false>
-cudaError_t run_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b, const CUtensorMap& b_half,
-                     const tc::GemmArgs& g, const typename Epi::Params& ep, cudaStream_t s, int pair_mode = -1) {
-    const int64_t tiles = (int64_t)g.tiles_m * g.tiles_n;
-    if (g.tiles_m % 2 == 0 && (pair_mode == 1 || (pair_mode < 0 && !g.skip))) {
-        auto kern = tc::k_tc_gemm<Epi, kAmn, kBmn, true>;
-        static bool attr_set = false;   // per process; the attribute is per function, not per device
-        if (!attr_set) {
-            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::SMEM_BYTES);
-            if (e != cudaSuccess) return e;
-            attr_set = true;
-        }
-        const int fit = pair_clusters(kern);
-        if (fit > 0) {
-            cudaLaunchConfig_t cfg = {};
-            cudaLaunchAttribute attr[1];
-            attr[0].id = cudaLaunchAttributeClusterDimension;
-            attr[0].val.clusterDim.x = 2;
-            attr[0].val.clusterDim.y = 1;
-            attr[0].val.clusterDim.z = 1;
-            cfg.gridDim = dim3((unsigned)(2 * std::min<int64_t>(tiles / 2, fit)));
-            cfg.blockDim = dim3(tc::kThreads);
-            cfg.dynamicSmemBytes = tc::SMEM_BYTES;
-            cfg.stream = s;
-            cfg.attrs = attr;
-            cfg.numAttrs = 1;
-            return cudaLaunchKernelEx(&cfg, kern, a0, a1, kBmn ? b : b_half, g, ep);
-        }
+    ~GemmTimer() {
+        for (cudaEvent_t e : ev) cudaEventDestroy(e);
     }
-    auto kern = tc::k_tc_gemm<Epi, kAmn, kBmn, false>;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
-    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(tiles, device_sm_count()));
-    kern<<<grid, tc::kThreads, tc::SMEM_BYTES, s>>>(a0, a1, b, g, ep);
-    return cudaGetLastError();
-}
+};
 
 struct Layout {
     int64_t T, D, V, T_pad, V_pad, Vc, tiles_v;
@@ -496,12 +376,18 @@ extern "C" size_t linear_ce_workspace_bytes(int64_t T, int64_t D, int64_t V) {
     return layout(T, D, V, &L) ? L.total : 0;
 }
 
-extern "C" int linear_ce_fwd_bwd_filtered(const void* E, const void* W, int64_t T, int64_t D, int64_t V,
-                                          const int64_t* labels, int64_t ignore_index, vce_reduction red,
-                                          const float* grad_output, float* loss_rows, float* loss_out, void* dE,
-                                          void* dW, vce_dtype grad_dt, float filter_eps,
-                                          unsigned long long* kept_blocks, void* workspace, size_t workspace_bytes,
-                                          int32_t* status, vce_stream_t s) {
+namespace vce {
+
+VCE_DEBUG_READER(debug_word_lce)
+
+namespace {
+
+// The whole call; with a timer, events are recorded around every GEMM launch.
+int linear_ce_run(const void* E, const void* W, int64_t T, int64_t D, int64_t V, const int64_t* labels,
+                  int64_t ignore_index, vce_reduction red, const float* grad_output, float* loss_rows,
+                  float* loss_out, void* dE, void* dW, vce_dtype grad_dt, float filter_eps,
+                  unsigned long long* kept_blocks, void* workspace, size_t workspace_bytes, int32_t* status,
+                  cudaStream_t s, GemmTimer* timer) {
     if (!(filter_eps >= 0.f) || filter_eps == kInf) return VCE_ERR_ARG;   // NaN, negative or infinite
     if (red != VCE_RED_NONE && red != VCE_RED_SUM && red != VCE_RED_MEAN) return VCE_ERR_DTYPE;
     if (grad_dt != VCE_BF16 && grad_dt != VCE_F32) return VCE_ERR_DTYPE;
@@ -510,12 +396,10 @@ extern "C" int linear_ce_fwd_bwd_filtered(const void* E, const void* W, int64_t 
     if (!E || !W || !labels || !grad_output || !loss_rows || !dE || !dW || !status) return VCE_ERR_NULL;
     if (red != VCE_RED_NONE && !loss_out) return VCE_ERR_NULL;
     if (!workspace || workspace_bytes < L.total) return VCE_ERR_WORKSPACE;
-    const size_t gs = grad_dt == VCE_BF16 ? 2 : 4;
     if (!aligned(E, 16) || !aligned(W, 16) || !aligned(workspace, 256) || !aligned(labels, 8) ||
         !aligned(loss_rows, 4) || !aligned(grad_output, 4) || !aligned(dE, 16) || !aligned(dW, 16) ||
         (loss_out && !aligned(loss_out, 4)) || (kept_blocks && !aligned(kept_blocks, 8)))
         return VCE_ERR_ALIGN;
-    (void)gs;
     int rc = require_sm100();
     if (rc) return rc;
 
@@ -534,23 +418,21 @@ extern "C" int linear_ce_fwd_bwd_filtered(const void* E, const void* W, int64_t 
     if (kept_blocks && cudaMemsetAsync(kept_blocks, 0, sizeof(unsigned long long), s) != cudaSuccess)
         return VCE_ERR_CUDA;
 
-    // K-major maps (box 64 K x rows) and MN-major maps (box 64 MN x 64 K) over row-major matrices
-    CUtensorMap mE, mW, mW2, mEmn, mWmn, mGhi, mGlo, mGhi_mn, mGlo_mn;
-    if (!make_map(&mE, E, D, T, D, BM) || !make_map(&mW, W, D, V, D, BN) || !make_map(&mW2, W, D, V, D, BN / 2) ||
-        !make_map(&mEmn, E, D, T, D, BK) ||
-        !make_map(&mWmn, W, D, V, D, BK) || !make_map(&mGhi, ghi, L.Vc, L.T_pad, L.Vc, BM) ||
-        !make_map(&mGlo, glo, L.Vc, L.T_pad, L.Vc, BM) || !make_map(&mGhi_mn, ghi, L.Vc, L.T_pad, L.Vc, BK) ||
-        !make_map(&mGlo_mn, glo, L.Vc, L.T_pad, L.Vc, BK))
-        return VCE_ERR_CUDA;
-
+    // operands, row-major: E [T, D], W [V, D], the gradient chunk halves [T_pad, Vc]
+    const Mat mE{E, D, T, D}, mW{W, D, V, D}, mGhi{ghi, L.Vc, L.T_pad, L.Vc}, mGlo{glo, L.Vc, L.T_pad, L.Vc};
     const int nkD = (int)cdiv(D, BK);
     const int tiles_t = (int)(L.T_pad / BM);
+    // 256-row tiles on CTA pairs where the rows split evenly, else single CTAs
+    const bool pairs_t = tiles_t % 2 == 0;
+    const Variant vz{pairs_t, BN};
 
     // 1. forward statistics over the whole vocabulary
     {
         tc::GemmArgs g{tiles_t, (int)L.tiles_v, nkD, nkD, 0, 0, 0, 0, status};
         EpiStats::Params ep{labels, ignore_index, T, V, reinterpret_cast<float4*>(part)};
-        if (run_gemm<EpiStats>(mE, mE, mW, mW2, g, ep, s) != cudaSuccess) return VCE_ERR_CUDA;
+        if (timer && !timer->begin(s)) return VCE_ERR_CUDA;
+        if (tc::launch_gemm<EpiStats, false, false>(mE, mE, mW, g, ep, vz, s) != cudaSuccess) return VCE_ERR_CUDA;
+        if (timer && !timer->end(s, GemmTimer::kStats)) return VCE_ERR_CUDA;
         if (launch_stats_merge(part, (int)L.tiles_v, T, V, labels, ignore_index, loss_rows, stats, status, s) !=
             cudaSuccess)
             return VCE_ERR_CUDA;
@@ -559,7 +441,11 @@ extern "C" int linear_ce_fwd_bwd_filtered(const void* E, const void* W, int64_t 
             return VCE_ERR_CUDA;
     }
 
-    // 2. gradients, one vocabulary chunk at a time
+    // 2. gradients, one vocabulary chunk at a time.  Exact: compensated accumulation on 128-wide
+    // tiles (CTA pairs where the rows split evenly).  Filtered: single CTAs skipping the dropped
+    // K blocks, one fp32 accumulation per tile.
+    const int gbn = filter ? 256 : 128;
+    const int seg = filter ? 0 : kSegKb;
     const int64_t nchunks = cdiv(L.V_pad, L.Vc);
     for (int64_t ci = 0; ci < nchunks; ++ci) {
         const int64_t off = ci * L.Vc;
@@ -571,72 +457,78 @@ extern "C" int linear_ce_fwd_bwd_filtered(const void* E, const void* W, int64_t 
             EpiGrad::Params ep{labels, T,      width,  off,    reinterpret_cast<const float4*>(stats), grad_output,
                                red == VCE_RED_NONE, ghi, glo, L.Vc, filter_eps, keep_w, L.ldw, keep_e, L.lde,
                                filter ? kept_blocks : nullptr};
-            if (run_gemm<EpiGrad>(mE, mE, mW, mW2, g, ep, s) != cudaSuccess) return VCE_ERR_CUDA;
+            if (timer && !timer->begin(s)) return VCE_ERR_CUDA;
+            if (tc::launch_gemm<EpiGrad, false, false>(mE, mE, mW, g, ep, vz, s) != cudaSuccess) return VCE_ERR_CUDA;
+            if (timer && !timer->end(s, GemmTimer::kGrad)) return VCE_ERR_CUDA;
         }
         {   // dW[off : off + width] = G^T E: A = G (MN-major), B = E (MN-major), K = 2 T_pad (hi then lo);
-            // M tile = 128 vocabulary columns = one row of keep_w, K block = 64 rows of T
+            // M tile = 128 vocabulary columns = one row of keep_w, K block = 64 rows of T.  width_pad
+            // is a multiple of 256, so the M tiles always pair.
             const int nkT = (int)(L.T_pad / BK);
-            tc::GemmArgs g{(int)(width_pad / BM), (int)cdiv(D, BN), 2 * nkT, nkT, 0, 0, 0, 1, status};
+            tc::GemmArgs g{(int)(width_pad / BM), (int)cdiv(D, gbn), 2 * nkT, nkT, 0, 0, 0, 1, status};
             g.skip = keep_w;
             g.skip_ld = L.ldw;
-            EpiStore::Params ep{dW, D, width, D, off, grad_dt == VCE_BF16};
-            if (run_gemm<EpiStore, true, true>(mGhi_mn, mGlo_mn, mEmn, mEmn, g, ep, s) != cudaSuccess) return VCE_ERR_CUDA;
+            g.seg_kb = seg;
+            tc::EpiStore::Params ep{dW, D, width, D, off, grad_dt == VCE_BF16};
+            if (timer && !timer->begin(s)) return VCE_ERR_CUDA;
+            if (tc::launch_gemm<tc::EpiStore, true, true>(mGhi, mGlo, mE, g, ep, Variant{!filter, gbn}, s) !=
+                cudaSuccess)
+                return VCE_ERR_CUDA;
+            if (timer && !timer->end(s, GemmTimer::kDW)) return VCE_ERR_CUDA;
         }
         {   // dE += G W[off : off + width]: A = G (K-major), B = W rows (MN-major), K = 2 width (hi then lo);
             // M tile = 128 rows of T = one row of keep_e, K block = 64 vocabulary columns
             const int nkc = (int)cdiv(width, BK);
-            tc::GemmArgs g{tiles_t, (int)cdiv(D, BN), 2 * nkc, nkc, (int)off, 0, 0, 1, status};
+            tc::GemmArgs g{tiles_t, (int)cdiv(D, gbn), 2 * nkc, nkc, (int)off, 0, 0, 1, status};
             g.skip = keep_e;
             g.skip_ld = L.lde;
+            g.seg_kb = seg;
             EpiKahan::Params ep{dsum, dcomp, T, D, ci == 0, ci == nchunks - 1, dE, grad_dt == VCE_BF16};
-            if (run_gemm<EpiKahan, false, true>(mGhi, mGlo, mWmn, mWmn, g, ep, s) != cudaSuccess) return VCE_ERR_CUDA;
+            if (timer && !timer->begin(s)) return VCE_ERR_CUDA;
+            if (tc::launch_gemm<EpiKahan, false, true>(mGhi, mGlo, mW, g, ep, Variant{!filter && pairs_t, gbn}, s) !=
+                cudaSuccess)
+                return VCE_ERR_CUDA;
+            if (timer && !timer->end(s, GemmTimer::kDE)) return VCE_ERR_CUDA;
         }
     }
     return VCE_OK;
 }
 
-extern "C" int vce_gemm_bf16(const void* A, int a_mn, const void* B, int b_mn, int64_t M, int64_t N, int64_t K,
-                             float* C, int64_t ldc, vce_stream_t s) {
-    if (!A || !B || !C) return VCE_ERR_NULL;
-    if (M < 1 || N < 1 || K < 1 || (M % 8) || (N % 8) || (K % 8) || M > (1 << 30) || N > (1 << 30) || K > (1 << 30))
-        return VCE_ERR_SHAPE;
-    if (ldc < N) return VCE_ERR_LD;
-    if (!aligned(A, 16) || !aligned(B, 16) || !aligned(C, 16) || (ldc % 4)) return VCE_ERR_ALIGN;
-    int rc = require_sm100();
-    if (rc) return rc;
-    CUtensorMap ma, mb, mb2;
-    const bool ok_a = a_mn ? make_map(&ma, A, M, K, M, BK) : make_map(&ma, A, K, M, K, BM);
-    const bool ok_b = b_mn ? make_map(&mb, B, N, K, N, BK) && make_map(&mb2, B, N, K, N, BK)
-                           : make_map(&mb, B, K, N, K, BN) && make_map(&mb2, B, K, N, K, BN / 2);
-    if (!ok_a || !ok_b) return VCE_ERR_CUDA;
-    const int nk = (int)cdiv(K, BK);
-    tc::GemmArgs g{(int)cdiv(M, BM), (int)cdiv(N, BN), nk, nk, 0, 0, 0, 0, nullptr};
-    EpiStore::Params ep{C, ldc, M, N, 0, 0};
-    cudaError_t e;
-    if (a_mn && b_mn) e = run_gemm<EpiStore, true, true>(ma, ma, mb, mb2, g, ep, s);
-    else if (a_mn) e = run_gemm<EpiStore, true, false>(ma, ma, mb, mb2, g, ep, s);
-    else if (b_mn) e = run_gemm<EpiStore, false, true>(ma, ma, mb, mb2, g, ep, s);
-    else e = run_gemm<EpiStore, false, false>(ma, ma, mb, mb2, g, ep, s);
-    return e == cudaSuccess ? VCE_OK : VCE_ERR_CUDA;
+}  // namespace
+}  // namespace vce
+
+extern "C" int linear_ce_fwd_bwd_filtered(const void* E, const void* W, int64_t T, int64_t D, int64_t V,
+                                          const int64_t* labels, int64_t ignore_index, vce_reduction red,
+                                          const float* grad_output, float* loss_rows, float* loss_out, void* dE,
+                                          void* dW, vce_dtype grad_dt, float filter_eps,
+                                          unsigned long long* kept_blocks, void* workspace, size_t workspace_bytes,
+                                          int32_t* status, vce_stream_t s) {
+    return linear_ce_run(E, W, T, D, V, labels, ignore_index, red, grad_output, loss_rows, loss_out, dE, dW, grad_dt,
+                         filter_eps, kept_blocks, workspace, workspace_bytes, status, s, nullptr);
 }
 
-extern "C" int vce_test_gemm_stall(const void* A, const void* B, int64_t M, int64_t N, int64_t K, float* C,
-                                   uint64_t wait_ns, int32_t* status, vce_stream_t s) {
-    if (!A || !B || !C || !status) return VCE_ERR_NULL;
-    if (M < 1 || N < 1 || K < 1 || (M % 8) || (N % 8) || (K % 8) || M > (1 << 20) || N > (1 << 20) || K > (1 << 20))
-        return VCE_ERR_SHAPE;
-    if (wait_ns < 1000000ull || wait_ns > 2000000000ull) return VCE_ERR_ARG;   // 1 ms .. 2 s
-    if (!aligned(A, 16) || !aligned(B, 16) || !aligned(C, 16)) return VCE_ERR_ALIGN;
-    int rc = require_sm100();
-    if (rc) return rc;
-    CUtensorMap ma, mb, mb2;
-    if (!make_map(&ma, A, K, M, K, BM) || !make_map(&mb, B, K, N, K, BN) || !make_map(&mb2, B, K, N, K, BN / 2))
-        return VCE_ERR_CUDA;
-    if (cudaMemsetAsync(status, 0, sizeof(int32_t), s) != cudaSuccess) return VCE_ERR_CUDA;
-    const int nk = (int)cdiv(K, BK);
-    tc::GemmArgs g{(int)cdiv(M, BM), (int)cdiv(N, BN), nk, nk, 0, 0, 0, 0, status, 16u, wait_ns};
-    EpiStore::Params ep{C, N, M, N, 0, 0};
-    return run_gemm<EpiStore>(ma, ma, mb, mb2, g, ep, s) == cudaSuccess ? VCE_OK : VCE_ERR_CUDA;
+extern "C" int linear_ce_fwd_bwd_timed(const void* E, const void* W, int64_t T, int64_t D, int64_t V,
+                                       const int64_t* labels, int64_t ignore_index, vce_reduction red,
+                                       const float* grad_output, float* loss_rows, float* loss_out, void* dE,
+                                       void* dW, vce_dtype grad_dt, float filter_eps, unsigned long long* kept_blocks,
+                                       void* workspace, size_t workspace_bytes, int32_t* status, vce_stream_t s,
+                                       float* gemm_ms, int* gemm_launches) {
+    if (!gemm_ms || !gemm_launches) return VCE_ERR_NULL;
+    GemmTimer timer;
+    int rc = linear_ce_run(E, W, T, D, V, labels, ignore_index, red, grad_output, loss_rows, loss_out, dE, dW,
+                           grad_dt, filter_eps, kept_blocks, workspace, workspace_bytes, status, s, &timer);
+    for (int k = 0; k < GemmTimer::kKinds; ++k) {
+        gemm_ms[k] = 0.f;
+        gemm_launches[k] = 0;
+    }
+    if (rc == VCE_OK && cudaStreamSynchronize(s) != cudaSuccess) rc = VCE_ERR_CUDA;
+    for (size_t i = 0; rc == VCE_OK && i < timer.kind.size(); ++i) {
+        float ms = 0.f;
+        if (cudaEventElapsedTime(&ms, timer.ev[2 * i], timer.ev[2 * i + 1]) != cudaSuccess) rc = VCE_ERR_CUDA;
+        gemm_ms[timer.kind[i]] += ms;
+        gemm_launches[timer.kind[i]] += 1;
+    }
+    return rc;
 }
 
 extern "C" int linear_ce_fwd_bwd(const void* E, const void* W, int64_t T, int64_t D, int64_t V, const int64_t* labels,
@@ -646,26 +538,3 @@ extern "C" int linear_ce_fwd_bwd(const void* E, const void* W, int64_t T, int64_
     return linear_ce_fwd_bwd_filtered(E, W, T, D, V, labels, ignore_index, red, grad_output, loss_rows, loss_out, dE,
                                       dW, grad_dt, 0.f, nullptr, workspace, workspace_bytes, status, s);
 }
-
-extern "C" int vce_test_gemm_skip(const void* A, const void* B, int64_t M, int64_t N, int64_t K, const uint32_t* skip,
-                                  int64_t skip_ld, int pair, float* C, vce_stream_t s) {
-    if (!A || !B || !C || !skip) return VCE_ERR_NULL;
-    if (M < 1 || N < 1 || K < 1 || (M % 8) || (N % 8) || (K % 8) || M > (1 << 20) || N > (1 << 20) || K > (1 << 20))
-        return VCE_ERR_SHAPE;
-    const int64_t tiles_m = cdiv(M, BM);
-    if (skip_ld < cdiv(cdiv(K, 128), 32) || skip_ld > (1 << 20)) return VCE_ERR_ARG;
-    if (pair != 0 && (pair != 1 || tiles_m % 2)) return VCE_ERR_ARG;
-    if (!aligned(A, 16) || !aligned(B, 16) || !aligned(C, 16) || !aligned(skip, 4)) return VCE_ERR_ALIGN;
-    int rc = require_sm100();
-    if (rc) return rc;
-    CUtensorMap ma, mb, mb2;
-    if (!make_map(&ma, A, K, M, K, BM) || !make_map(&mb, B, K, N, K, BN) || !make_map(&mb2, B, K, N, K, BN / 2))
-        return VCE_ERR_CUDA;
-    const int nk = (int)cdiv(K, BK);
-    tc::GemmArgs g{(int)tiles_m, (int)cdiv(N, BN), nk, nk, 0, 0, 0, 0, nullptr};
-    g.skip = skip;
-    g.skip_ld = (int)skip_ld;
-    EpiStore::Params ep{C, N, M, N, 0, 0};
-    return run_gemm<EpiStore>(ma, ma, mb, mb2, g, ep, s, pair) == cudaSuccess ? VCE_OK : VCE_ERR_CUDA;
-}
-

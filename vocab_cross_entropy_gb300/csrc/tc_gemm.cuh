@@ -1,24 +1,35 @@
 // A persistent, warp-specialised bf16 GEMM on the sm_100-family tensor cores:
-//     acc[m, n] = sum_k A[m, k] * B[n, k]      (fp32 accumulators)
+//     acc[m, n] = sum_k A[m, k] * B[n, k]      (fp32 accumulators in tensor memory)
 // Each operand is K-major (global rows run along K) or MN-major (global rows run along M,
-// resp. N), chosen at compile time.
-// with a caller-supplied epilogue that consumes each 128 x 256 accumulator tile from
-// tensor memory.  Hand-written PTX for the TMA loads (cp.async.bulk.tensor), the
-// mbarrier pipeline and the tcgen05 MMA / TMEM instructions.
+// resp. N), chosen at compile time, with a caller-supplied epilogue that consumes each
+// accumulator tile from tensor memory.  Hand-written PTX for the TMA loads
+// (cp.async.bulk.tensor), the mbarrier pipeline and the tcgen05 MMA / TMEM instructions.
 //
-//   warp 0 (one lane)  TMA producer: A tile 128 x 64 and B tile 256 x 64 per stage (K-major:
-//                      one box of 64 K x rows; MN-major: boxes of 64 MN x 64 K)
-//   warp 1 (one lane)  MMA issuer:   4 x tcgen05.mma (M=128, N=256, K=16) per stage
-//   warp 2             TMEM allocation / release (512 columns = two accumulators)
+//   warp 0 (one lane)  TMA producer: this CTA's A tile (128 x 64) and B rows (x 64) per stage
+//   warp 1 (one lane)  MMA issuer:   4 x tcgen05.mma (K = 16) per stage
+//   warp 2             TMEM allocation / release (all 512 columns)
 //   warps 4..7         epilogue: tcgen05.ld 32 lanes x 32 columns at a time, one
 //                      accumulator row per thread
-// The accumulator is double buffered so the epilogue of tile i overlaps the MMAs of
-// tile i+1.  Shared-memory tiles use the 128-byte swizzle that TMA writes and the MMA
-// descriptors read.  Every wait is bounded: a wait that exceeds kWaitNs sets an error
-// code, every role stops, in-flight copies are drained (bounded) and TMEM is released.
-// Two options: a launch as 2-CTA clusters whose CTAs share each B tile through TMA multicast
-// (kPair), and K-block skipping from a per-tile bit table (GemmArgs::skip, gradient
-// filtering), which visits only the K blocks whose bits are set.
+// The accumulator is double buffered so the epilogue of tile i overlaps the MMAs of tile
+// i+1.  Shared-memory tiles use the 128-byte swizzle that TMA writes and the MMA descriptors
+// read.  Every wait is bounded: a wait that exceeds its limit sets an error code, every role
+// stops, in-flight copies are drained (bounded) and TMEM is released.
+//
+// Two launch forms (template kCta2):
+//   single CTAs      tile 128 x kBN; the CTA loads A (128 rows) and all kBN rows of B.
+//   CTA pairs        a 2-CTA cluster computes a 256 x kBN tile with tcgen05.mma.cta_group::2:
+//                    each CTA loads its own 128 rows of A and its own kBN/2 rows of B into its
+//                    own shared memory (plain TMA loads, no multicast), the even CTA issues the
+//                    MMAs, which read both CTAs' operands and write each CTA's 128 accumulator
+//                    rows into that CTA's tensor memory.  Both CTAs' copies complete on the even
+//                    CTA's stage barrier; the MMA commits arrive on both CTAs' barriers.  Per
+//                    CTA a stage holds A plus half of B, so B crosses from L2 once per pair and
+//                    more stages fit.
+// Two options: K-block skipping from a per-tile bit table (GemmArgs::skip, gradient filtering,
+// single CTAs only), and compensated accumulation (GemmArgs::seg_kb, kBN = 128): the K loop is
+// cut into segments of seg_kb blocks, each accumulated afresh in tensor memory, and the
+// epilogue adds each segment into a (sum, compensation) pair kept in the other half of tensor
+// memory with a two-sum, so the fp32 rounding of the accumulation spans one segment only.
 #pragma once
 
 #include <cuda.h>
@@ -26,69 +37,34 @@
 #include <stdint.h>
 
 #include "vce_async.cuh"
+#include "vce_check.cuh"
 
 namespace vce {
 namespace tc {
 
-constexpr int BM = 128, BN = 256, BK = 64;
-constexpr int STAGES = 4;
+constexpr int BM = 128, BK = 64;       // A rows per CTA, K per stage
 constexpr int A_BYTES = BM * BK * 2;   // 16 KB
-constexpr int B_BYTES = BN * BK * 2;   // 32 KB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int TMEM_COLS = 2 * BN;      // two fp32 accumulators of 128 lanes x 256 columns
 constexpr int kThreads = 256;
-constexpr int EPI_WARP_BYTES = 5120;   // per epilogue warp: staging space an epilogue may use
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 4 * EPI_WARP_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+constexpr int TMEM_COLS = 512;         // two accumulators (kBN = 256), or two + a pair (kBN = 128)
+constexpr int kMaxSmem = 232448;       // opt-in dynamic shared memory per block (227 KB)
 
-// error codes written to the kernel's error word when a wait gives up
-enum { kErrWaitEmpty = 101, kErrWaitFull = 102, kErrWaitAccFree = 103, kErrWaitAccFull = 104 };
+template <bool kCta2, int kBN>
+struct Cfg {
+    static_assert(kBN == 128 || kBN == 256, "tile width");
+    static constexpr int kBRows = kCta2 ? kBN / 2 : kBN;   // rows of the B tile this CTA loads
+    static constexpr int kBBytes = kBRows * BK * 2;
+    static constexpr int kStageBytes = A_BYTES + kBBytes;
+    static constexpr int kReserve = 1024 /*alignment*/ + 256 /*barriers*/;
+    static constexpr int kStagesFit = (kMaxSmem - kReserve) / kStageBytes;
+    static constexpr int kStages = kStagesFit > 9 ? 9 : kStagesFit;
+    static constexpr int kSmem = kStages * kStageBytes + kReserve;
+};
 
-// ---- tcgen05 ------------------------------------------------------------------------------
+// error codes written to the kernel's error word when a wait gives up (100: the two CTAs of a
+// pair were given different tensor-memory columns)
+enum { kErrTmemPair = 100, kErrWaitEmpty = 101, kErrWaitFull = 102, kErrWaitAccFree = 103, kErrWaitAccFull = 104 };
 
-__device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)), "r"(ncols)
-                 : "memory");
-}
-__device__ __forceinline__ void tmem_relinquish() {
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
-}
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-// D[tmem] (+)= A[smem] * B[smem]^T, bf16 inputs, fp32 accumulate, one thread issues.
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                         uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// As mma_commit, arriving on the mbarrier at the same shared-memory offset in every CTA of the
-// cluster that `mask` names.
-__device__ __forceinline__ void mma_commit_mc(uint64_t* bar, uint16_t mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-            smem_u32(bar)),
-        "h"(mask)
-        : "memory");
-}
-
-// TMA tile load into the same shared-memory offset of every CTA of the cluster that `mask`
-// names, each completing bytes on its own mbarrier at `bar`'s offset.
-__device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y,
-                                               uint16_t mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster "
-        "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
-        "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"(mask)
-        : "memory");
-}
+// ---- cluster helpers ----------------------------------------------------------------------
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;
@@ -98,11 +74,132 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
 __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
 }
+// The shared::cluster address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t cluster_addr(const void* p, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+// Arrive on an mbarrier given by its shared::cluster address (this CTA's or a peer's).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
 
-// Arrive on `bar` once every tcgen05.mma issued so far by this thread has completed.
-__device__ __forceinline__ void mma_commit(uint64_t* bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
-                 : "memory");
+// Bounded wait (as mbar_wait); kCluster: with cluster-scope acquire, for barriers that the
+// other CTA of a pair arrives on.
+template <bool kCluster>
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int32_t* err,
+                                         int code, uint64_t wait_ns) {
+    if (!kCluster) return mbar_wait(bar, parity, abort_flag, err, code, wait_ns);
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    while (true) {
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer() - t0 > wait_ns) {
+            *abort_flag = 1;
+            if (err) atomicCAS(err, 0, code);
+            return false;
+        }
+    }
+}
+
+// TMA tile load into this CTA's shared memory, completing its bytes on the mbarrier at the
+// shared::cluster address `bar` -- this CTA's or, for a CTA pair, the even CTA's.
+template <bool kCta2>
+__device__ __forceinline__ void tma_load(void* dst, const CUtensorMap* map, uint32_t bar, int x, int y) {
+    if constexpr (kCta2) {
+        asm volatile(
+            "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes "
+            "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+            "l"(map), "r"(x), "r"(y), "r"(bar)
+            : "memory");
+    } else {
+        asm volatile(
+            "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+            "[%4];" ::"r"(smem_u32(dst)),
+            "l"(map), "r"(x), "r"(y), "r"(bar)
+            : "memory");
+    }
+}
+
+// ---- tcgen05 ------------------------------------------------------------------------------
+
+template <bool kCta2>
+__device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
+    if constexpr (kCta2)
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)),
+                     "r"(ncols)
+                     : "memory");
+    else
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)),
+                     "r"(ncols)
+                     : "memory");
+}
+template <bool kCta2>
+__device__ __forceinline__ void tmem_relinquish() {
+    if constexpr (kCta2)
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    else
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+template <bool kCta2>
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    if constexpr (kCta2)
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+    else
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// D[tmem] (+)= A[smem] * B[smem]^T, bf16 inputs, fp32 accumulate, one thread issues (for a
+// pair: a thread of the even CTA, and A, B, D span both CTAs).
+template <bool kCta2>
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
+    if constexpr (kCta2)
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+            "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+            : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+            "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+            : "memory");
+}
+
+// Arrive on the mbarrier at shared::cluster address `bar` once every tcgen05.mma issued so far
+// by this thread has completed.
+template <bool kCta2>
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    if constexpr (kCta2)
+        asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                     : "memory");
+    else
+        asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                     : "memory");
 }
 
 // 32 consecutive fp32 columns of this thread's TMEM lane (lane = 32 * (warp % 4) + lane id).
@@ -117,6 +214,18 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
           "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
         : "r"(taddr));
 }
+// Store 32 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]),
+        "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]),
+        "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
 // Wait until this thread's tcgen05.ld have landed.  r, the destination of the last load, is
 // tied to the wait, so no use of it can be scheduled before the wait.
 __device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[32]) {
@@ -129,6 +238,7 @@ __device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[32]) {
                  :
                  : "memory");
 }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // Shared-memory matrix descriptor: K-major operand, rows of 64 bf16 (128 B) written by TMA
 // with the 128-byte swizzle; 8-row groups 1024 B apart (stride byte offset).  The leading
@@ -164,10 +274,17 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn = 
            ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// a + x = t + e exactly (Knuth's two-sum).
+__device__ __forceinline__ void two_sum(float a, float x, float& t, float& e) {
+    t = a + x;
+    const float bp = t - a;
+    e = (a - (t - bp)) + (x - bp);
+}
+
 // ---- the kernel ---------------------------------------------------------------------------
 
 struct GemmArgs {
-    int tiles_m, tiles_n;   // output tiles (BM x BN)
+    int tiles_m, tiles_n;   // output tiles of 128 rows x kBN columns (tiles_m even for CTA pairs)
     int nk;                 // K blocks (of BK) per tile
     int nk_a0;              // the first nk_a0 blocks read A0, the rest A1 (K restarts at 0 for A1)
     int b_x0;               // B's K coordinate of block kb is b_x0 + (kb mod nk_a0) * BK
@@ -178,46 +295,42 @@ struct GemmArgs {
     uint32_t tx_extra;      // bytes announced per stage beyond the copies (0; > 0 only to test the
                             // give-up path: the stage never completes and the waits must time out)
     uint64_t wait_ns;       // limit of every wait (0: kWaitNs)
-    // Optional K-block skipping (gradient filtering): row tm of skip holds one bit per 128
-    // K columns (two K blocks) of M tile tm, skip_ld 32-bit words per row; a clear bit means
-    // A is all zero there for this tile.  Applies to both halves (A0 and A1) alike.  Null:
-    // every K block runs.
+    // Optional K-block skipping (gradient filtering, single CTAs): row tm of skip holds one bit
+    // per 128 K columns (two K blocks) of M tile tm, skip_ld 32-bit words per row; a clear bit
+    // means A is all zero there for this tile.  Applies to both halves (A0 and A1) alike.
+    // Null: every K block runs.
     const uint32_t* skip;
     int skip_ld;
+    // Compensated accumulation (kBN = 128, no skip; the epilogue must take (sum, compensation)
+    // pairs): K blocks per accumulation segment; 0 = the whole K loop in one accumulator.
+    int seg_kb;
 };
 
-// Calls f(kb, ka, mine) for the K blocks of M tile tm in order -- kb the block index (A0
-// blocks, then A1 blocks), ka its index within its half -- and stops when f returns false.
-// Without skip bits that is every K block (mine = true).  With them (gradient filtering) it is
-// the K blocks of the 128-column blocks whose bit is set for this tile or, for a CTA pair, for
-// its partner (both CTAs then load the same stages; mine says whether this tile multiplies).
-// The bits are scanned 32 blocks at a time with find-first-set, the next word loaded while the
-// current one is walked, so skipped blocks cost nothing.  nk is nk_a0 or 2 nk_a0.
+// Calls f(kb, ka) for the K blocks of M tile tm in order -- kb the block index (A0 blocks,
+// then A1 blocks), ka its index within its half -- and stops when f returns false.  Without
+// skip bits that is every K block.  With them (gradient filtering) it is the K blocks of the
+// 128-column blocks whose bit is set for this tile.  The bits are scanned 32 blocks at a time
+// with find-first-set, the next word loaded while the current one is walked, so skipped
+// blocks cost nothing.  nk is nk_a0 or 2 nk_a0.
 template <class F>
-__device__ __forceinline__ void for_each_kblock(const GemmArgs& g, int tm, bool pair, F&& f) {
+__device__ __forceinline__ void for_each_kblock(const GemmArgs& g, int tm, F&& f) {
     if (!g.skip) {
         for (int kb = 0; kb < g.nk; ++kb)
-            if (!f(kb, kb >= g.nk_a0 ? kb - g.nk_a0 : kb, true)) return;
+            if (!f(kb, kb >= g.nk_a0 ? kb - g.nk_a0 : kb)) return;
         return;
     }
     const uint32_t* own = g.skip + (size_t)tm * g.skip_ld;
-    const uint32_t* peer = pair ? g.skip + (size_t)(tm ^ 1) * g.skip_ld : own;
     for (int half = 0; half * g.nk_a0 < g.nk; ++half) {
-        uint32_t on = own[0], pn = peer[0];
+        uint32_t on = own[0];
         for (int w = 0; w < g.skip_ld; ++w) {
-            const uint32_t o = on;
-            uint32_t m = on | pn;
-            if (w + 1 < g.skip_ld) {
-                on = own[w + 1];
-                pn = peer[w + 1];
-            }
+            uint32_t m = on;
+            if (w + 1 < g.skip_ld) on = own[w + 1];
             while (m) {
                 const int bit = __ffs(m) - 1;
                 m &= m - 1u;
-                const bool mine = (o >> bit) & 1u;
                 const int ka0 = 2 * (w * 32 + bit);   // 128 columns = two K blocks
                 for (int ka = ka0; ka < ka0 + 2 && ka < g.nk_a0; ++ka)
-                    if (!f(half * g.nk_a0 + ka, ka, mine)) return;
+                    if (!f(half * g.nk_a0 + ka, ka)) return;
             }
         }
     }
@@ -231,56 +344,60 @@ __device__ __forceinline__ bool tile_has_blocks(const GemmArgs& g, int tm) {
     return m != 0u;
 }
 
-// kPair: the grid runs as clusters of two CTAs (blockIdx 2c and 2c + 1) that take tiles 2q and
-// 2q + 1, which are (2p, n) and (2p + 1, n): the two share their B tile.  tiles_m is even.
-template <bool kPair>
-__device__ __forceinline__ void tile_coords(const GemmArgs& g, int tile, int& tm, int& tn) {
-    if (kPair && g.n_fastest) {
-        const int q = tile >> 1;
-        tn = q % g.tiles_n;
-        tm = 2 * (q / g.tiles_n) + (tile & 1);
-    } else if (g.n_fastest) {
+// Tile `tile` of the launch: M tile tm (128 rows) and N tile tn.  A CTA pair walks tiles of
+// 256 rows; CTA `rank` of the pair takes the M tile 2 mm + rank.
+template <bool kCta2>
+__device__ __forceinline__ void tile_coords(const GemmArgs& g, int tile, uint32_t rank, int& tm, int& tn) {
+    const int tiles_mm = kCta2 ? g.tiles_m / 2 : g.tiles_m;
+    int mm;
+    if (g.n_fastest) {
         tn = tile % g.tiles_n;
-        tm = tile / g.tiles_n;
+        mm = tile / g.tiles_n;
     } else {
-        tm = tile % g.tiles_m;
-        tn = tile / g.tiles_m;
+        mm = tile % tiles_mm;
+        tn = tile / tiles_mm;
     }
+    tm = kCta2 ? 2 * mm + (int)rank : mm;
 }
 
+// The epilogue interface (Epi):
+//   struct Params; struct Row;
+//   begin(p, row_state, row, tn)                        before a tile's columns
+//   consume(p, row_state, row, col0, acc[32])           32 accumulator columns, in order
+//   end(p, row_state, row, tn)                          after them (all lanes of the warp)
+//   kCompensated, consume2(p, row_state, row, col0, sum[32], comp[32]): the final columns of a
+//     compensated (seg_kb > 0) tile as (sum, compensation) pairs.
 // kAmn / kBmn: the operand is MN-major; its tensor map then has 64 x 64 boxes over a global
-// [K, M] (resp. [K, N]) matrix, and the tile is loaded as BM/64 (resp. BN/64) boxes.
-// kPair: launched as clusters of two CTAs that compute the two M-neighbours of one B tile
-// (tile_coords).  Each CTA loads its own A tile and one half of the shared B tile, multicast
-// into the same stage of both CTAs (a K-major B map then has boxes of BN/2 rows), so B crosses
-// from L2 once per pair.  A stage is free again once both CTAs' MMAs have read it: every MMA
-// commit arrives on the stage's empty barrier in both CTAs, and empty counts two arrivals.
-template <class Epi, bool kAmn = false, bool kBmn = false, bool kPair = false>
+// [K, M] (resp. [K, N]) matrix, and the tile is loaded as 2 (resp. kBRows / 64) boxes.  A
+// K-major B map has boxes of kBRows rows.
+template <class Epi, bool kAmn, bool kBmn, bool kCta2, int kBN>
 __global__ void __launch_bounds__(kThreads, 1)
     k_tc_gemm(const __grid_constant__ CUtensorMap mapA0, const __grid_constant__ CUtensorMap mapA1,
               const __grid_constant__ CUtensorMap mapB, const GemmArgs g, const typename Epi::Params ep) {
+    using C = Cfg<kCta2, kBN>;
+    constexpr int S = C::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* smA = smem;
-    uint8_t* smB = smem + STAGES * A_BYTES;
-    uint8_t* epi_smem = smem + STAGES * STAGE_BYTES;
-    uint64_t* full = reinterpret_cast<uint64_t*>(epi_smem + 4 * EPI_WARP_BYTES);
-    uint64_t* empty = full + STAGES;
-    uint64_t* acc_full = empty + STAGES;
+    uint8_t* smB = smem + S * A_BYTES;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * C::kStageBytes);
+    uint64_t* empty = full + S;
+    uint64_t* acc_full = empty + S;
     uint64_t* acc_free = acc_full + 2;
     uint64_t* drain = acc_free + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = kCta2 ? cluster_ctarank() : 0u;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
+        for (int s = 0; s < S; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kPair ? 2 : 1);
+            mbar_init(&empty[s], 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&acc_full[a], 1);
-            mbar_init(&acc_free[a], 4 * 32);
+            mbar_init(&acc_free[a], kCta2 ? 8 : 4);   // one arrival per epilogue warp (of both CTAs)
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -290,85 +407,87 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_map(&mapB);
     }
     if (warp == 2) {
-        tmem_alloc(tmem_slot, TMEM_COLS);
-        tmem_relinquish();
+        tmem_alloc<kCta2>(tmem_slot, TMEM_COLS);
+        tmem_relinquish<kCta2>();
     }
     tc_fence_before();
-    if (kPair)
-        cluster_sync_all();   // the peer's copies and commits reach these barriers only once they exist
+    if (kCta2)
+        cluster_sync_all();   // the peer's copies, commits and arrivals reach these barriers only once they exist
     else
         __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    const uint32_t rank = kPair ? cluster_ctarank() : 0u;
-    const int ntiles = g.tiles_m * g.tiles_n;
+    if (kCta2 && threadIdx.x == 0 && rank == 1 && ld_cluster_u32(cluster_addr(tmem_slot, 0)) != tmem_base) {
+        *abort_flag = 1;   // the pair's MMAs address both CTAs' tensor memory at the even CTA's columns
+        if (g.err) atomicCAS(g.err, 0, (int)kErrTmemPair);
+    }
+    if (kCta2) __syncthreads();   // the check above before any role of this CTA starts
+    const int ntiles = (kCta2 ? g.tiles_m / 2 : g.tiles_m) * g.tiles_n;
+    const int tile0 = kCta2 ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+    const int tstep = kCta2 ? (int)(gridDim.x >> 1) : (int)gridDim.x;
     const uint64_t wns = g.wait_ns ? g.wait_ns : kWaitNs;
+    // accumulation segments per tile (compensated accumulation needs the free half of TMEM)
+    const int seg_kb = (kBN == 128 && !g.skip && Epi::kCompensated) ? g.seg_kb : 0;
+    const int nseg = seg_kb > 0 ? (g.nk + seg_kb - 1) / seg_kb : 1;
 
     if (warp == 0 && lane == 0) {
         // ---------------- TMA producer
         int stage = 0;
         uint32_t phase = 0;
         int issued = 0;   // stages whose copies were issued and not yet known complete
-        for (int tile = blockIdx.x; tile < ntiles && !*abort_flag; tile += gridDim.x) {
+        for (int tile = tile0; tile < ntiles && !*abort_flag; tile += tstep) {
             int tm, tn;
-            tile_coords<kPair>(g, tile, tm, tn);
-            for_each_kblock(g, tm, kPair, [&](int kb, int ka, bool) {
-                if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, g.err, kErrWaitEmpty, wns)) return false;
-                mbar_arrive_expect_tx(&full[stage], STAGE_BYTES + g.tx_extra);
-                const bool second = kb >= g.nk_a0;
-                const CUtensorMap* ma = second ? &mapA1 : &mapA0;
+            tile_coords<kCta2>(g, tile, rank, tm, tn);
+            for_each_kblock(g, tm, [&](int kb, int ka) {
+                if (!wait_bar<kCta2>(&empty[stage], phase ^ 1u, abort_flag, g.err, kErrWaitEmpty, wns)) return false;
+                // the barrier that counts this stage's bytes: the even CTA's for a pair
+                const uint32_t fb = kCta2 ? cluster_addr(&full[stage], 0) : smem_u32(&full[stage]);
+                if (!kCta2 || rank == 0)
+                    mbar_arrive_expect_tx(&full[stage], (kCta2 ? 2 : 1) * C::kStageBytes + g.tx_extra);
+                const CUtensorMap* ma = kb >= g.nk_a0 ? &mapA1 : &mapA0;
+                uint8_t* sa = smA + stage * A_BYTES;
+                uint8_t* sb = smB + stage * C::kBBytes;
                 if (kAmn) {
 #pragma unroll
                     for (int h = 0; h < BM / 64; ++h)
-                        tma_load_2d(smA + stage * A_BYTES + h * (64 * BK * 2), ma, &full[stage],
-                                    g.a_y0 + tm * BM + h * 64, ka * BK);
+                        tma_load<kCta2>(sa + h * (64 * BK * 2), ma, fb, g.a_y0 + tm * BM + h * 64, ka * BK);
                 } else {
-                    tma_load_2d(smA + stage * A_BYTES, ma, &full[stage], ka * BK, g.a_y0 + tm * BM);
+                    tma_load<kCta2>(sa, ma, fb, ka * BK, g.a_y0 + tm * BM);
                 }
-                if (kPair && kBmn) {
+                const int n0 = g.b_y0 + tn * kBN + (int)rank * C::kBRows;
+                if (kBmn) {
 #pragma unroll
-                    for (int i = 0; i < BN / 128; ++i) {
-                        const int h = (int)rank * (BN / 128) + i;
-                        tma_load_2d_mc(smB + stage * B_BYTES + h * (64 * BK * 2), &mapB, &full[stage],
-                                       g.b_y0 + tn * BN + h * 64, g.b_x0 + ka * BK, 0x3);
-                    }
-                } else if (kPair) {
-                    tma_load_2d_mc(smB + stage * B_BYTES + rank * (B_BYTES / 2), &mapB, &full[stage],
-                                   g.b_x0 + ka * BK, g.b_y0 + tn * BN + (int)rank * (BN / 2), 0x3);
-                } else if (kBmn) {
-#pragma unroll
-                    for (int h = 0; h < BN / 64; ++h)
-                        tma_load_2d(smB + stage * B_BYTES + h * (64 * BK * 2), &mapB, &full[stage],
-                                    g.b_y0 + tn * BN + h * 64, g.b_x0 + ka * BK);
+                    for (int h = 0; h < C::kBRows / 64; ++h)
+                        tma_load<kCta2>(sb + h * (64 * BK * 2), &mapB, fb, n0 + h * 64, g.b_x0 + ka * BK);
                 } else {
-                    tma_load_2d(smB + stage * B_BYTES, &mapB, &full[stage], g.b_x0 + ka * BK, g.b_y0 + tn * BN);
+                    tma_load<kCta2>(sb, &mapB, fb, g.b_x0 + ka * BK, n0);
                 }
-                issued = issued < STAGES ? issued + 1 : STAGES;
-                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                issued = issued < S ? issued + 1 : S;
+                if (++stage == S) { stage = 0; phase ^= 1u; }
                 return true;
             });
         }
-        if (kPair && !*abort_flag) {
-            // the peer's MMA commits land on these empty barriers: wait (bounded) for the last
-            // STAGES of them so none arrives after this CTA has exited
-            for (int i = 0; i < STAGES; ++i) {
-                if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, g.err, kErrWaitEmpty, wns)) break;
-                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
-            }
-        }
         if (*abort_flag) {
-            // drain: wait (bounded) for the copies of the last `issued` stages so no TMA write
-            // lands in shared memory after the block has exited
-            for (int i = 0; i < issued; ++i) {
-                if (--stage < 0) { stage = STAGES - 1; phase ^= 1u; }
+            if (!kCta2 || rank == 0) {
+                // drain: wait (bounded) for the copies of the last `issued` stages (a pair's
+                // stage completes once both CTAs' copies landed) so no TMA write lands in
+                // shared memory after the block has exited
+                for (int i = 0; i < issued; ++i) {
+                    if (--stage < 0) { stage = S - 1; phase ^= 1u; }
+                    const uint64_t t0 = globaltimer();
+                    while (!mbar_try_wait(&full[stage], phase) && globaltimer() - t0 < wns) {
+                    }
+                }
+            } else {
+                // the odd CTA's copies complete on the even CTA's barriers: give them time to land
                 const uint64_t t0 = globaltimer();
-                while (!mbar_try_wait(&full[stage], phase) && globaltimer() - t0 < wns) {
+                while (globaltimer() - t0 < 1000000ull) {
                 }
             }
         }
-    } else if (warp == 1 && lane == 0) {
+    } else if (warp == 1 && lane == 0 && (!kCta2 || rank == 0)) {
         // ---------------- MMA issuer
-        constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, kAmn, kBmn);
+        constexpr uint32_t idesc = idesc_bf16_f32(kCta2 ? 2 * BM : BM, kBN, kAmn, kBmn);
         // one MMA consumes K = 16: 32 B along a K-major row, or 16 K-rows (2 KB) of an MN-major tile
         constexpr uint32_t kStepA = kAmn ? (2048 >> 4) : (32 >> 4);
         constexpr uint32_t kStepB = kBmn ? (2048 >> 4) : (32 >> 4);
@@ -377,41 +496,56 @@ __global__ void __launch_bounds__(kThreads, 1)
         int acc = 0;
         uint32_t acc_phase = 0;
         const uint32_t a0 = smem_u32(smA), b0 = smem_u32(smB);
-        for (int tile = blockIdx.x; tile < ntiles && !*abort_flag; tile += gridDim.x) {
-            if (!mbar_wait(&acc_free[acc], acc_phase ^ 1u, abort_flag, g.err, kErrWaitAccFree, wns)) break;
+        // commits arrive on this CTA's barrier and, for a pair, on the odd CTA's too
+        auto commit = [&](uint64_t* bar) {
+            mma_commit<kCta2>(smem_u32(bar));
+            if (kCta2) mma_commit<kCta2>(cluster_addr(bar, 1));
+        };
+        for (int tile = tile0; tile < ntiles && !*abort_flag; tile += tstep) {
+            if (!wait_bar<kCta2>(&acc_free[acc], acc_phase ^ 1u, abort_flag, g.err, kErrWaitAccFree, wns)) break;
             tc_fence_after();
-            const uint32_t d = tmem_base + (uint32_t)(acc * BN);
+            uint32_t d = tmem_base + (uint32_t)(acc * kBN);
             int tm, tn;
-            tile_coords<kPair>(g, tile, tm, tn);
+            tile_coords<kCta2>(g, tile, rank, tm, tn);
             bool ok = true, issued = false;
-            for_each_kblock(g, tm, kPair, [&](int, int, bool mine) {
-                if (!mbar_wait(&full[stage], phase, abort_flag, g.err, kErrWaitFull, wns)) {
+            int kvis = 0;
+            for_each_kblock(g, tm, [&](int, int) {
+                if (!wait_bar<false>(&full[stage], phase, abort_flag, g.err, kErrWaitFull, wns)) {
                     ok = false;
                     return false;
                 }
                 tc_fence_after();
                 const uint64_t ad = kAmn ? desc_mnmajor_sw128(a0 + stage * A_BYTES) : desc_kmajor_sw128(a0 + stage * A_BYTES);
-                const uint64_t bd = kBmn ? desc_mnmajor_sw128(b0 + stage * B_BYTES) : desc_kmajor_sw128(b0 + stage * B_BYTES);
-                if (mine) {   // else loaded for the partner only: released without MMAs
+                const uint64_t bd =
+                    kBmn ? desc_mnmajor_sw128(b0 + stage * C::kBBytes) : desc_kmajor_sw128(b0 + stage * C::kBBytes);
 #pragma unroll
-                    for (int k = 0; k < BK / 16; ++k)   // advance the start address by one K = 16 step
-                        mma_bf16(d, ad + kStepA * k, bd + kStepB * k, idesc, (issued || k != 0) ? 1u : 0u);
-                    issued = true;
+                for (int k = 0; k < BK / 16; ++k)   // advance the start address by one K = 16 step
+                    mma_bf16<kCta2>(d, ad + kStepA * k, bd + kStepB * k, idesc, (issued || k != 0) ? 1u : 0u);
+                issued = true;
+                commit(&empty[stage]);
+                if (++stage == S) { stage = 0; phase ^= 1u; }
+                if (seg_kb > 0 && ++kvis % seg_kb == 0 && kvis < g.nk) {
+                    // segment done: hand this accumulator to the epilogue, continue in the other
+                    commit(&acc_full[acc]);
+                    acc ^= 1;
+                    if (acc == 0) acc_phase ^= 1u;
+                    if (!wait_bar<kCta2>(&acc_free[acc], acc_phase ^ 1u, abort_flag, g.err, kErrWaitAccFree, wns)) {
+                        ok = false;
+                        return false;
+                    }
+                    tc_fence_after();
+                    d = tmem_base + (uint32_t)(acc * kBN);
+                    issued = false;
                 }
-                if (kPair)
-                    mma_commit_mc(&empty[stage], 0x3);
-                else
-                    mma_commit(&empty[stage]);
-                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 return true;
             });
             if (!ok) break;
-            mma_commit(&acc_full[acc]);
+            commit(&acc_full[acc]);
             acc ^= 1;
             if (acc == 0) acc_phase ^= 1u;
         }
         // every MMA this thread issued has finished before TMEM can be released
-        mma_commit(drain);
+        mma_commit<kCta2>(smem_u32(drain));
         const uint64_t t0 = globaltimer();
         while (!mbar_try_wait(drain, 0) && globaltimer() - t0 < wns) {
         }
@@ -420,51 +554,120 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int sub = warp & 3;
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
-            if (!mbar_wait(&acc_full[acc], acc_phase, abort_flag, g.err, kErrWaitAccFull, wns)) break;
-            tc_fence_after();
-            int tm, tn;
-            tile_coords<kPair>(g, tile, tm, tn);
-            const int row = tm * BM + sub * 32 + lane;
-            const uint32_t t0 = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(sub * 32) << 16);
-            uint8_t* stage = epi_smem + sub * EPI_WARP_BYTES;
-            // Two register buffers: the next 32 columns load from TMEM while these are consumed.
-            static_assert((BN / 32) % 2 == 0, "column pieces go in pairs");
-            uint32_t ra[32], rb[32];
-            typename Epi::Row st;
-            if (!tile_has_blocks(g, tm)) {   // every K block skipped: no MMA wrote the accumulator
-#pragma unroll
-                for (int k = 0; k < 32; ++k) ra[k] = 0u;
-                Epi::begin(ep, st, row, tn);
-#pragma unroll 1
-                for (int c = 0; c < BN / 32; ++c) Epi::consume(ep, st, row, tn * BN + c * 32, ra, stage);
-            } else {
-                tmem_ld32(t0, ra);
-                Epi::begin(ep, st, row, tn);   // its global loads overlap the first TMEM load
-#pragma unroll 1
-                for (int c = 0; c < BN / 32; c += 2) {
-                    tmem_wait_ld(ra);
-                    tmem_ld32(t0 + (uint32_t)((c + 1) * 32), rb);
-                    Epi::consume(ep, st, row, tn * BN + c * 32, ra, stage);
-                    tmem_wait_ld(rb);
-                    if (c + 2 < BN / 32) tmem_ld32(t0 + (uint32_t)((c + 2) * 32), ra);
-                    Epi::consume(ep, st, row, tn * BN + (c + 1) * 32, rb, stage);
-                }
-            }
-            Epi::end(ep, st, row, tn);
+        const uint32_t lane_off = (uint32_t)(sub * 32) << 16;
+        auto release = [&]() {   // this warp is done with accumulator `acc`
             tc_fence_before();
-            mbar_arrive(&acc_free[acc]);
+            __syncwarp();
+            if (lane == 0) {
+                if (kCta2)
+                    mbar_arrive_cluster(cluster_addr(&acc_free[acc], 0));
+                else
+                    mbar_arrive(&acc_free[acc]);
+            }
             acc ^= 1;
             if (acc == 0) acc_phase ^= 1u;
+        };
+        bool live = true;
+        for (int tile = tile0; tile < ntiles && live; tile += tstep) {
+            int tm, tn;
+            tile_coords<kCta2>(g, tile, rank, tm, tn);
+            const int row = tm * BM + sub * 32 + lane;
+            typename Epi::Row st;
+            for (int seg = 0; seg < nseg; ++seg) {
+                // the warp decides together: tcgen05.ld is a warp-wide instruction
+                const bool ok = wait_bar<kCta2>(&acc_full[acc], acc_phase, abort_flag, g.err, kErrWaitAccFull, wns);
+                if (!__all_sync(0xffffffffu, ok)) {
+                    live = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t t0 = tmem_base + (uint32_t)(acc * kBN) + lane_off;
+                // warp-uniform: a tile outside the output is not written (its accumulator is released)
+                if (!dbg::ok(tm >= 0 && tm < g.tiles_m && tn >= 0 && tn < g.tiles_n, dbg::kTile)) {
+                } else if (nseg == 1) {
+                    // Two register buffers: the next 32 columns load from TMEM while these are consumed.
+                    static_assert((kBN / 32) % 2 == 0, "column pieces go in pairs");
+                    uint32_t ra[32], rb[32];
+                    if (!tile_has_blocks(g, tm)) {   // every K block skipped: no MMA wrote the accumulator
+#pragma unroll
+                        for (int k = 0; k < 32; ++k) ra[k] = 0u;
+                        Epi::begin(ep, st, row, tn);
+#pragma unroll 1
+                        for (int c = 0; c < kBN / 32; ++c) Epi::consume(ep, st, row, tn * kBN + c * 32, ra);
+                    } else {
+                        tmem_ld32(t0, ra);
+                        Epi::begin(ep, st, row, tn);   // its global loads overlap the first TMEM load
+#pragma unroll 1
+                        for (int c = 0; c < kBN / 32; c += 2) {
+                            tmem_wait_ld(ra);
+                            tmem_ld32(t0 + (uint32_t)((c + 1) * 32), rb);
+                            Epi::consume(ep, st, row, tn * kBN + c * 32, ra);
+                            tmem_wait_ld(rb);
+                            if (c + 2 < kBN / 32) tmem_ld32(t0 + (uint32_t)((c + 2) * 32), ra);
+                            Epi::consume(ep, st, row, tn * kBN + (c + 1) * 32, rb);
+                        }
+                    }
+                    Epi::end(ep, st, row, tn);
+                } else if constexpr (Epi::kCompensated && kBN == 128) {
+                    // the (sum, compensation) pair of this tile lives in columns 256..383 and 384..511
+                    const uint32_t ps = tmem_base + 256u + lane_off, pc = tmem_base + 384u + lane_off;
+                    const bool last = seg == nseg - 1;
+                    if (last) Epi::begin(ep, st, row, tn);
+#pragma unroll 1
+                    for (int c = 0; c < kBN / 32; ++c) {
+                        uint32_t x[32], s[32], e[32];
+                        tmem_ld32(t0 + (uint32_t)(c * 32), x);
+                        if (seg > 0) {
+                            tmem_ld32(ps + (uint32_t)(c * 32), s);
+                            tmem_ld32(pc + (uint32_t)(c * 32), e);
+                        }
+                        tmem_wait_ld(x);
+                        if (seg == 0) {   // the pair starts as (segment 0, 0)
+#pragma unroll
+                            for (int k = 0; k < 32; ++k) {
+                                s[k] = x[k];
+                                e[k] = 0u;
+                            }
+                        } else {
+#pragma unroll
+                            for (int k = 0; k < 32; ++k) {
+                                float t, r;
+                                two_sum(__uint_as_float(s[k]), __uint_as_float(x[k]), t, r);
+                                s[k] = __float_as_uint(t);
+                                e[k] = __float_as_uint(__uint_as_float(e[k]) + r);
+                            }
+                        }
+                        if (last) {
+                            float fs[32], fe[32];
+#pragma unroll
+                            for (int k = 0; k < 32; ++k) {
+                                fs[k] = __uint_as_float(s[k]);
+                                fe[k] = __uint_as_float(e[k]);
+                            }
+                            Epi::consume2(ep, st, row, tn * kBN + c * 32, fs, fe);
+                        } else {
+                            tmem_st32(ps + (uint32_t)(c * 32), s);
+                            tmem_st32(pc + (uint32_t)(c * 32), e);
+                        }
+                    }
+                    if (last)
+                        Epi::end(ep, st, row, tn);
+                    else
+                        tmem_wait_st();   // the pair is complete before the next segment reads it
+                }
+                release();
+            }
         }
     }
     tc_fence_before();
     __syncthreads();
+    // a pair: no CTA releases its tensor memory or leaves while the other's MMAs, copies or
+    // arrivals may still reach it
+    if (kCta2) cluster_sync_all();
     if (warp == 2) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, TMEM_COLS);
+        tmem_dealloc<kCta2>(tmem_base, TMEM_COLS);
     }
-    if (kPair) cluster_sync_all();   // neither CTA leaves while the other may still write to it
 }
 
 }  // namespace tc

@@ -5,6 +5,7 @@
 #include <atomic>
 
 #include "vce.h"
+#include "vce_check.cuh"
 #include "vce_host.h"
 
 namespace vce {
@@ -63,6 +64,7 @@ extern "C" const char* vce_status_string(int status) {
         case VCE_ERR_ARG: return "invalid argument";
         case VCE_ERR_DEVICE: return "the current device is not an sm_100-family GPU";
         case VCE_ERR_SCRATCH_LIMIT: return "k * T exceeds the built-in scratch of ce_merge_chunks_noalloc";
+        case 100: return "the two CTAs of a GEMM pair were given different tensor-memory columns";
         case 101: return "a GEMM pipeline wait for a free shared-memory stage gave up";
         case 102: return "a GEMM pipeline wait for a loaded shared-memory stage gave up";
         case 103: return "a GEMM pipeline wait for a free accumulator gave up";
@@ -73,6 +75,11 @@ extern "C" const char* vce_status_string(int status) {
         case 108: return "a one-pass CE wait for the warps' partial row statistics gave up";
         case 109: return "a one-pass CE wait for a row's gradient coefficients gave up";
         case 110: return "a CE forward wait for free statistics slots gave up";
+        case 121: return "debug check: a row index outside [0, T)";
+        case 122: return "debug check: a column range outside its row or chunk";
+        case 123: return "debug check: a chunk or segment index outside its table";
+        case 124: return "debug check: a stage or ring slot outside the ring";
+        case 125: return "debug check: a GEMM output tile outside the output";
         default: return "unknown status";
     }
 }
@@ -82,5 +89,23 @@ extern "C" int vce_get_status(const int32_t* status, vce_stream_t s, int32_t* ho
     if (cudaMemcpyAsync(host_out, status, sizeof(int32_t), cudaMemcpyDeviceToHost, s) != cudaSuccess)
         return VCE_ERR_CUDA;
     if (cudaStreamSynchronize(s) != cudaSuccess) return VCE_ERR_CUDA;
+    return VCE_OK;
+}
+
+extern "C" int vce_debug_checks(void) { return vce::dbg::kEnabled ? 1 : 0; }
+
+extern "C" int vce_debug_status(int32_t* host_out) {
+    if (!host_out) return VCE_ERR_NULL;
+    *host_out = 0;
+    if (!vce::dbg::kEnabled) return VCE_OK;
+    if (cudaDeviceSynchronize() != cudaSuccess) return VCE_ERR_CUDA;
+    int (*const readers[])(int32_t*) = {vce::debug_word_ce_fwd,   vce::debug_word_ce_bwd, vce::debug_word_ce_fwd_ring,
+                                        vce::debug_word_ce_bwd_ring, vce::debug_word_ce_ring, vce::debug_word_ce_fused,
+                                        vce::debug_word_lce,      vce::debug_word_gemm_hooks};
+    for (auto rd : readers) {
+        int32_t w = 0;
+        if (rd(&w) != 0) return VCE_ERR_CUDA;
+        if (*host_out == 0) *host_out = w;   // the first code found; every word is cleared
+    }
     return VCE_OK;
 }

@@ -33,4 +33,15 @@ cudaError_t launch_stats_merge(const float* part, int k, int64_t T, int64_t V, c
 cudaError_t launch_loss_reduce(const float* loss_rows, const int64_t* labels, int64_t T, int64_t V,
                                int64_t ignore_index, int red, float* loss_out, float* row_stats, cudaStream_t s);
 
+// Debug-build index checks (vce_check.cuh): each translation unit with checks reads and clears
+// its own debug word (0 in the release build).
+int debug_word_ce_fwd(int32_t* out);
+int debug_word_ce_bwd(int32_t* out);
+int debug_word_ce_fwd_ring(int32_t* out);
+int debug_word_ce_bwd_ring(int32_t* out);
+int debug_word_ce_ring(int32_t* out);
+int debug_word_ce_fused(int32_t* out);
+int debug_word_lce(int32_t* out);
+int debug_word_gemm_hooks(int32_t* out);
+
 }  // namespace vce
