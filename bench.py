@@ -683,7 +683,7 @@ def linear_record(w, m, peaks, world):
 
 LINEAR_FILES = ["vocab_cross_entropy_gb300/csrc/lce.cu", "vocab_cross_entropy_gb300/csrc/tc_gemm.cuh",
                 "vocab_cross_entropy_gb300/csrc/tc_launch.cuh", "vocab_cross_entropy_gb300/csrc/vce_async.cuh",
-                "vocab_cross_entropy_gb300/csrc/vce_device.cuh"]
+                "vocab_cross_entropy_gb300/csrc/vce_device.cuh", "vocab_cross_entropy_gb300/csrc/vce_check.cuh"]
 
 
 def run_linear(args, rank, local_rank, world, device):

@@ -60,6 +60,13 @@ typedef struct CUstream_st* vce_stream_t; /* the same handle as cudaStream_t; NU
 #define VCE_MAX_CHUNKS 64   /* most column chunks ce_merge_chunks accepts */
 #define VCE_NOALLOC_MAX_CHUNK_ROWS 262144   /* most k * T for ce_merge_chunks_noalloc (4 MiB) */
 
+/* Exported entry points (the library is built with hidden symbol visibility otherwise). */
+#if defined(__GNUC__)
+#define VCE_API __attribute__((visibility("default")))
+#else
+#define VCE_API
+#endif
+
 typedef enum { VCE_F32 = 0, VCE_BF16 = 1 } vce_dtype;
 typedef enum { VCE_RED_NONE = 0, VCE_RED_SUM = 1, VCE_RED_MEAN = 2 } vce_reduction;
 
@@ -79,26 +86,34 @@ enum {
 };
 
 /* Library ABI version (VCE_ABI_VERSION of the build). */
-int vce_abi_version(void);
+VCE_API int vce_abi_version(void);
 
 /* Static text for a status code; never NULL. */
-const char* vce_status_string(int status);
+VCE_API const char* vce_status_string(int status);
 
 /* Floats per row of the row_stats buffer (= VCE_ROW_STATS). */
-size_t vce_row_stats_floats(void);
+VCE_API size_t vce_row_stats_floats(void);
 
 /*
  * Waits for stream `s`, then copies the device status word to *host_out.
  * Returns VCE_OK or VCE_ERR_CUDA / VCE_ERR_NULL.
  */
-int vce_get_status(const int32_t* status, vce_stream_t s, int32_t* host_out);
+VCE_API int vce_get_status(const int32_t* status, vce_stream_t s, int32_t* host_out);
+
+/*
+ * vce_last_cuda_error -- the cudaError_t behind the most recent VCE_ERR_CUDA an entry point
+ * returned on the calling host thread (0 if none), then cleared; vce_cuda_error_name gives
+ * its name.  No page counterpart: a diagnostic.
+ */
+VCE_API int vce_last_cuda_error(void);
+VCE_API const char* vce_cuda_error_name(int code);
 
 /*
  * vce_debug_checks -- 1 if this library was built with device-side index checks
  * (python -m vocab_cross_entropy_gb300.build --debug-checks, which makes libvce_debug.so),
  * else 0.  No page counterpart: a debugging aid.
  */
-int vce_debug_checks(void);
+VCE_API int vce_debug_checks(void);
 
 /*
  * vce_debug_status -- in a build with device-side index checks: waits for the device
@@ -110,7 +125,7 @@ int vce_debug_checks(void);
  * incomplete.  In the release build it writes 0 and waits for nothing.  Returns VCE_OK,
  * VCE_ERR_NULL or VCE_ERR_CUDA.  No page counterpart: a debugging aid.
  */
-int vce_debug_status(int32_t* host_out);
+VCE_API int vce_debug_status(int32_t* host_out);
 
 /*
  * ce_forward -- per-row NLL and the statistics its gradient needs.  [TT, Numerics;
@@ -140,7 +155,7 @@ int vce_debug_status(int32_t* host_out);
  *              32-64 KB with fewer than 64 rows per SM take a per-block kernel instead,
  *              which has no such waits); the outputs are then undefined
  */
-int ce_forward(const void* logits, vce_dtype dt, int64_t T, int64_t V, int64_t ld,
+VCE_API int ce_forward(const void* logits, vce_dtype dt, int64_t T, int64_t V, int64_t ld,
                const int64_t* labels, int64_t ignore_index, vce_reduction red,
                float* loss_rows, float* loss_out, float* row_stats, int32_t* status,
                vce_stream_t s);
@@ -160,7 +175,7 @@ int ce_forward(const void* logits, vce_dtype dt, int64_t T, int64_t V, int64_t l
  *   grad_logits  [T, ld_grad] of dtype grad_dt (VCE_F32 or VCE_BF16), written;
  *                it must not overlap the logits
  */
-int ce_backward(const void* logits, vce_dtype dt, int64_t T, int64_t V, int64_t ld,
+VCE_API int ce_backward(const void* logits, vce_dtype dt, int64_t T, int64_t V, int64_t ld,
                 const int64_t* labels, int64_t ignore_index, vce_reduction red,
                 const float* row_stats, const float* grad_output,
                 void* grad_logits, vce_dtype grad_dt, int64_t ld_grad, vce_stream_t s);
@@ -177,12 +192,12 @@ int ce_backward(const void* logits, vce_dtype dt, int64_t T, int64_t V, int64_t 
  * returns VCE_ERR_ARG.  eps = 0 is exactly ce_forward / ce_backward.  Pass the same eps to
  * both calls.  Other arguments as ce_forward / ce_backward.
  */
-int ce_forward_ls(const void* logits, vce_dtype dt, int64_t T, int64_t V, int64_t ld,
+VCE_API int ce_forward_ls(const void* logits, vce_dtype dt, int64_t T, int64_t V, int64_t ld,
                   const int64_t* labels, int64_t ignore_index, float label_smoothing,
                   vce_reduction red, float* loss_rows, float* loss_out, float* row_stats,
                   int32_t* status, vce_stream_t s);
 
-int ce_backward_ls(const void* logits, vce_dtype dt, int64_t T, int64_t V, int64_t ld,
+VCE_API int ce_backward_ls(const void* logits, vce_dtype dt, int64_t T, int64_t V, int64_t ld,
                    const int64_t* labels, int64_t ignore_index, float label_smoothing,
                    vce_reduction red, const float* row_stats, const float* grad_output,
                    void* grad_logits, vce_dtype grad_dt, int64_t ld_grad, vce_stream_t s);
@@ -209,7 +224,7 @@ int ce_backward_ls(const void* logits, vce_dtype dt, int64_t T, int64_t V, int64
  *                coefficients); the outputs are then undefined
  *   grad_logits  [T, ld_grad] of dtype grad_dt, written; must not overlap the logits
  */
-int ce_forward_backward(const void* logits, vce_dtype dt, int64_t T, int64_t V, int64_t ld,
+VCE_API int ce_forward_backward(const void* logits, vce_dtype dt, int64_t T, int64_t V, int64_t ld,
                         const int64_t* labels, int64_t ignore_index, vce_reduction red,
                         const float* grad_output, float* loss_rows, float* loss_out,
                         float* row_stats, void* grad_logits, vce_dtype grad_dt, int64_t ld_grad,
@@ -222,7 +237,7 @@ int ce_forward_backward(const void* logits, vce_dtype dt, int64_t T, int64_t V, 
  * returns VCE_ERR_ARG; eps = 0 is exactly ce_forward_backward.  Other arguments as
  * ce_forward_backward.
  */
-int ce_forward_backward_ls(const void* logits, vce_dtype dt, int64_t T, int64_t V, int64_t ld,
+VCE_API int ce_forward_backward_ls(const void* logits, vce_dtype dt, int64_t T, int64_t V, int64_t ld,
                            const int64_t* labels, int64_t ignore_index, float label_smoothing,
                            vce_reduction red, const float* grad_output, float* loss_rows,
                            float* loss_out, float* row_stats, void* grad_logits, vce_dtype grad_dt,
@@ -239,7 +254,7 @@ int ce_forward_backward_ls(const void* logits, vce_dtype dt, int64_t T, int64_t 
  * afterwards.  Returns VCE_ERR_ARG, enqueuing nothing but the status reset, when [T, V] does
  * not take the shared-memory kernel (V not a multiple of 8, pointers not 16-byte aligned).
  */
-int vce_test_ce_fused_stall(const void* logits, int64_t T, int64_t V, const int64_t* labels,
+VCE_API int vce_test_ce_fused_stall(const void* logits, int64_t T, int64_t V, const int64_t* labels,
                             const float* grad_output, float* loss_rows, float* row_stats,
                             void* grad_logits, uint64_t wait_ns, int32_t* status, vce_stream_t s);
 
@@ -266,7 +281,7 @@ int vce_test_ce_fused_stall(const void* logits, int64_t T, int64_t V, const int6
  *   chunk_stats_ws           [k * T * VCE_CHUNK_STATS] fp32, 16-byte aligned, scratch
  *   other arguments          as ce_forward / ce_backward
  */
-int ce_merge_chunks(int k, const void* const* chunk_logits, const int64_t* chunk_width,
+VCE_API int ce_merge_chunks(int k, const void* const* chunk_logits, const int64_t* chunk_width,
                     const int64_t* chunk_ld, vce_dtype dt, int64_t T,
                     const int64_t* labels, int64_t ignore_index, vce_reduction red,
                     float* loss_rows, float* loss_out, float* row_stats,
@@ -282,7 +297,7 @@ int ce_merge_chunks(int k, const void* const* chunk_logits, const int64_t* chunk
  * [0, 1) (or NaN) returns VCE_ERR_ARG; 0 is exactly ce_merge_chunks.  Other arguments as
  * ce_merge_chunks.
  */
-int ce_merge_chunks_ls(int k, const void* const* chunk_logits, const int64_t* chunk_width,
+VCE_API int ce_merge_chunks_ls(int k, const void* const* chunk_logits, const int64_t* chunk_width,
                        const int64_t* chunk_ld, vce_dtype dt, int64_t T,
                        const int64_t* labels, int64_t ignore_index, float label_smoothing,
                        vce_reduction red, float* loss_rows, float* loss_out, float* row_stats,
@@ -314,7 +329,7 @@ int ce_merge_chunks_ls(int k, const void* const* chunk_logits, const int64_t* ch
  *     whose work can overlap on the GPU (different streams without ordering, or different
  *     host threads) race on it and give undefined results; order them on one stream.
  */
-int ce_merge_chunks_noalloc(int k, const void* const* chunk_logits, const int64_t* chunk_width,
+VCE_API int ce_merge_chunks_noalloc(int k, const void* const* chunk_logits, const int64_t* chunk_width,
                             const int64_t* chunk_ld, vce_dtype dt, int64_t T,
                             const int64_t* labels, int64_t ignore_index, vce_reduction red,
                             float* loss_rows, float* loss_out, float* row_stats,

@@ -24,11 +24,11 @@ extern "C" {
 /*
  * Bytes of workspace linear_ce_fwd_bwd needs for these sizes; 0 if the sizes are
  * invalid (T, V >= 1; D >= 8 and a multiple of 8).  For T=8192, D=4096, V=128256 it is
- * about 1.41 GB (per-tile statistics, one 32768-column vocabulary chunk of the gradient as
- * two bf16 halves, the compensated dE accumulator pair, and the gradient-filter bit tables
- * of one chunk).
+ * about 1.95 GB (per-tile statistics, one 32768-column vocabulary chunk of the gradient as
+ * two bf16 halves, the compensated dE accumulator pair, the fp32 dW partial of one chunk,
+ * and the gradient-filter bit tables of one chunk).
  */
-size_t linear_ce_workspace_bytes(int64_t T, int64_t D, int64_t V);
+VCE_API size_t linear_ce_workspace_bytes(int64_t T, int64_t D, int64_t V);
 
 /*
  * linear_ce_fwd_bwd -- loss and gradients of CE(softmax(E W^T), labels) in one call.
@@ -39,10 +39,9 @@ size_t linear_ce_workspace_bytes(int64_t T, int64_t D, int64_t V);
  *   branch, ignored rows 0):
  *       dE = G W   [T, D],       dW = G^T E   [V, D].
  *   G enters the two gradient GEMMs as an exact-to-16-bits pair of bf16 terms
- *   (G = G_hi + G_lo).  Both gradient GEMMs accumulate compensated: each run of 1024
- *   consecutive products of a sum (along T for dW, along the vocabulary for dE) is summed in
- *   fp32 on the tensor cores, and the runs are added into a (sum, compensation) fp32 pair
- *   with a two-sum; dE's pair is carried across vocabulary chunks the same way.
+ *   (G = G_hi + G_lo).  Each GEMM accumulates in fp32 on the tensor cores; dW is formed as
+ *   two partial products over the halves of T and dE as one partial product per 32768-column
+ *   vocabulary chunk, and the partials are merged with a two-sum compensated fp32 pair.
  *
  *   E            [T, D] bf16 row-major, 16-byte aligned
  *   W            [V, D] bf16 row-major, 16-byte aligned
@@ -58,7 +57,7 @@ size_t linear_ce_workspace_bytes(int64_t T, int64_t D, int64_t V);
  *                (100: the two CTAs of a pair got different tensor-memory columns; 101..104: a
  *                device-side wait ran out), the outputs then being undefined
  */
-int linear_ce_fwd_bwd(const void* E, const void* W, int64_t T, int64_t D, int64_t V,
+VCE_API int linear_ce_fwd_bwd(const void* E, const void* W, int64_t T, int64_t D, int64_t V,
                       const int64_t* labels, int64_t ignore_index, vce_reduction red,
                       const float* grad_output, float* loss_rows, float* loss_out,
                       void* dE, void* dW, vce_dtype grad_dt,
@@ -75,8 +74,8 @@ int linear_ce_fwd_bwd(const void* E, const void* W, int64_t T, int64_t D, int64_
  *   K blocks (128 rows, resp. columns, is a whole number of their K blocks), so kept blocks
  *   keep exactly the unfiltered arithmetic and the work falls with the dropped fraction.
  *   The loss and row statistics are never filtered.  The filtered gradient GEMMs run on
- *   single CTAs and accumulate each tile's kept blocks in one fp32 sum (no compensation
- *   within a chunk; dE's chunks are still merged with the two-sum pair).
+ *   single CTAs; dW is one product over all of T (dE's chunks are still merged with the
+ *   two-sum pair).
  *
  *   filter_eps   threshold on p_ij, finite and >= 0; 0 is exactly linear_ce_fwd_bwd (no
  *                block is dropped).  NaN, negative or infinite: VCE_ERR_ARG, nothing enqueued.
@@ -85,7 +84,7 @@ int linear_ce_fwd_bwd(const void* E, const void* W, int64_t T, int64_t D, int64_
  *                filter_eps = 0 (the filter does not run)
  *   Every other argument as linear_ce_fwd_bwd; the workspace size is the same.
  */
-int linear_ce_fwd_bwd_filtered(const void* E, const void* W, int64_t T, int64_t D, int64_t V,
+VCE_API int linear_ce_fwd_bwd_filtered(const void* E, const void* W, int64_t T, int64_t D, int64_t V,
                                const int64_t* labels, int64_t ignore_index, vce_reduction red,
                                const float* grad_output, float* loss_rows, float* loss_out,
                                void* dE, void* dW, vce_dtype grad_dt, float filter_eps,
@@ -102,7 +101,7 @@ int linear_ce_fwd_bwd_filtered(const void* E, const void* W, int64_t T, int64_t 
  * number.  Blocking; the events are created and destroyed by the call.  NULL gemm_ms or
  * gemm_launches: VCE_ERR_NULL.
  */
-int linear_ce_fwd_bwd_timed(const void* E, const void* W, int64_t T, int64_t D, int64_t V,
+VCE_API int linear_ce_fwd_bwd_timed(const void* E, const void* W, int64_t T, int64_t D, int64_t V,
                             const int64_t* labels, int64_t ignore_index, vce_reduction red,
                             const float* grad_output, float* loss_rows, float* loss_out,
                             void* dE, void* dW, vce_dtype grad_dt, float filter_eps,
@@ -119,23 +118,17 @@ int linear_ce_fwd_bwd_timed(const void* E, const void* W, int64_t T, int64_t D, 
  * ldc >= N and a multiple of 4.  No page counterpart: it exposes the building block for
  * testing.
  */
-int vce_gemm_bf16(const void* A, int a_mn, const void* B, int b_mn, int64_t M, int64_t N, int64_t K,
+VCE_API int vce_gemm_bf16(const void* A, int a_mn, const void* B, int b_mn, int64_t M, int64_t N, int64_t K,
                   float* C, int64_t ldc, vce_stream_t s);
 
 /*
  * vce_gemm_bf16_variant -- vce_gemm_bf16 in a chosen launch form (no page counterpart; for
- * testing and timing the forms the linear-CE uses):
- *   pair    0: single CTAs, 128-row tiles; 1: CTA pairs issuing cta_group::2 MMAs, 256-row tiles
- *           (needs ceil(M / 128) even)
- *   bn      tile width, 128 or 256 columns
- *   seg_kb  0: one fp32 accumulation over all of K; > 0 (bn = 128 only): compensated
- *           accumulation, each run of seg_kb * 64 consecutive K products summed afresh and the
- *           runs added into a (sum, compensation) pair with a two-sum; C = sum + compensation
- * Any other pair, bn or seg_kb: VCE_ERR_ARG, nothing enqueued.  Other arguments as
- * vce_gemm_bf16.
+ * testing and timing the forms the linear-CE uses): pair = 0 single CTAs, 128-row tiles;
+ * pair = 1 CTA pairs issuing cta_group::2 MMAs, 256-row tiles (needs ceil(M / 128) even).
+ * Any other pair: VCE_ERR_ARG, nothing enqueued.  Other arguments as vce_gemm_bf16.
  */
-int vce_gemm_bf16_variant(const void* A, int a_mn, const void* B, int b_mn, int64_t M, int64_t N, int64_t K,
-                          float* C, int64_t ldc, int pair, int bn, int seg_kb, vce_stream_t s);
+VCE_API int vce_gemm_bf16_variant(const void* A, int a_mn, const void* B, int b_mn, int64_t M, int64_t N, int64_t K,
+                          float* C, int64_t ldc, int pair, vce_stream_t s);
 
 /*
  * vce_test_gemm_stall -- test hook for the GEMM's give-up path (no page counterpart).
@@ -147,7 +140,7 @@ int vce_gemm_bf16_variant(const void* A, int a_mn, const void* B, int b_mn, int6
  * of a pair) stop, copies in flight are drained, tensor memory is released and the kernel
  * returns; the context stays usable.  C's contents are undefined afterwards.
  */
-int vce_test_gemm_stall(const void* A, const void* B, int64_t M, int64_t N, int64_t K, float* C,
+VCE_API int vce_test_gemm_stall(const void* A, const void* B, int64_t M, int64_t N, int64_t K, float* C,
                         uint64_t wait_ns, int32_t* status, vce_stream_t s);
 
 /*
@@ -161,7 +154,7 @@ int vce_test_gemm_stall(const void* A, const void* B, int64_t M, int64_t N, int6
  * for a tile that sets only such bits).  It runs on single CTAs, as the filtered linear-CE's
  * gradient GEMMs do.  Bad skip_ld: VCE_ERR_ARG.
  */
-int vce_test_gemm_skip(const void* A, const void* B, int64_t M, int64_t N, int64_t K, const uint32_t* skip,
+VCE_API int vce_test_gemm_skip(const void* A, const void* B, int64_t M, int64_t N, int64_t K, const uint32_t* skip,
                        int64_t skip_ld, float* C, vce_stream_t s);
 
 #ifdef __cplusplus

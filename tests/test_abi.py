@@ -66,8 +66,7 @@ def test_argument_errors_need_no_gpu(lib):
 def test_linear_and_gemm_hook_argument_errors_need_no_gpu(lib):
     """linear_ce_fwd_bwd_filtered refuses a NaN, negative or infinite eps, vce_test_gemm_skip
     refuses null pointers, bad shapes and short bit rows, and vce_gemm_bf16_variant refuses pairs
-    on an odd tile count, unknown tile widths and compensation on 256-wide tiles, all before any
-    CUDA call."""
+    on an odd tile count, all before any CUDA call."""
     P, i64, i32, f32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
     x = P(0x1000)
     f = lib.linear_ce_fwd_bwd_filtered
@@ -82,10 +81,7 @@ def test_linear_and_gemm_hook_argument_errors_need_no_gpu(lib):
     assert g(x, x, 256, 256, 100, x, 1, x, None) == -3                           # K not a multiple of 8
     assert g(x, x, 256, 256, 8192, x, 1, x, None) == -8                          # 64 blocks need 2 words
     v = lib.vce_gemm_bf16_variant
-    v.argtypes = [P, i32, P, i32, i64, i64, i64, P, i64, i32, i32, i32, P]
-    assert v(x, 0, x, 0, 384, 256, 128, x, 256, 1, 256, 0, None) == -8          # 3 M tiles cannot pair
-    assert v(x, 0, x, 0, 256, 256, 128, x, 256, 2, 256, 0, None) == -8          # pair is 0 or 1
-    assert v(x, 0, x, 0, 256, 256, 128, x, 256, 1, 64, 0, None) == -8           # tile width 128 or 256
-    assert v(x, 0, x, 0, 256, 256, 128, x, 256, 1, 256, 4, None) == -8          # compensation needs 128
-    assert v(x, 0, x, 0, 256, 256, 128, x, 256, 1, 128, -1, None) == -8         # segment length >= 0
-    assert v(x, 0, x, 0, 256, 256, 128, x, 200, 1, 128, 0, None) == -4          # ldc < N
+    v.argtypes = [P, i32, P, i32, i64, i64, i64, P, i64, i32, P]
+    assert v(x, 0, x, 0, 384, 256, 128, x, 256, 1, None) == -8          # 3 M tiles cannot pair
+    assert v(x, 0, x, 0, 256, 256, 128, x, 256, 2, None) == -8          # pair is 0 or 1
+    assert v(x, 0, x, 0, 256, 256, 128, x, 200, 1, None) == -4          # ldc < N

@@ -15,19 +15,14 @@ import gen
 from oracle import ce_oracle as O
 from tests import _grading as G
 from tests.test_ce_gpu import vce  # noqa: F401  (fixture)
-from tests.test_lce_gpu import dev_bf16, grade_sum, host, z_sum_slack
-
-CHUNK = 32768   # vocabulary columns per gradient chunk
+from tests.test_lce_gpu import dev_bf16, grade_sum, host, lce_steps, z_sum_slack
+from tests.test_oracle_filter import _eps_in_a_gap
 
 
 def filtered_steps(T, V):
-    """Accumulation steps of the filtered gradient GEMMs, which sum a whole chunk's K in one fp32
-    accumulator (16 products per step, G's hi and lo halves both): dW over 2 T, dE over twice
-    the chunk width."""
-    t_pad = -(-T // 128) * 128
-    v_pad = -(-V // 256) * 256
-    return {"dW": 2 * t_pad // 16, "dE": 2 * min(v_pad, CHUNK) // 16}
-from tests.test_oracle_filter import _eps_in_a_gap
+    """Accumulation steps of the filtered gradient GEMMs (dW over all of T in one launch)."""
+    return lce_steps(T, V, filtered=True)
+
 
 pytestmark = pytest.mark.gpu
 

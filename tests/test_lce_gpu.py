@@ -7,15 +7,16 @@ the tensor-core path can carry, beta * sum_k |t_k| plus half a bf16 ulp of its o
 
   accumulation   each fp32 accumulator adds `steps` MMA partial sums (16 products each), one
                  rounding per addition, counted as a whole fp32 ulp (2^-23) so that a
-                 truncating adder is covered: steps * 2^-23.  The exact call accumulates
-                 compensated: 1024 products (64 steps) per segment, the segments (and dE's
-                 vocabulary chunks) merged by two-sum, so steps = 64 whatever the sum's
-                 length.  The filtered call accumulates a whole chunk's K in one sum:
-                 steps = K / 16.
+                 truncating adder is covered: steps * 2^-23.  The partials of separate
+                 launches are merged with a two-sum, so `steps` is that of one launch: dW is
+                 two launches over the halves of T (steps = 2 (T / 2) / 16, G's hi and lo
+                 halves both), dE one launch per 32768-column vocabulary chunk (steps =
+                 2 chunk / 16); the filtered call's dW is one launch over all of T.
   G split        G enters as G_hi + G_lo, the lo half rounded to bf16: 2^-18 per term.
   G evaluation   each G entry is an fp32 product of c, sigma(x) and a hardware exp2: 2^-20.
 
-Each grading prints how many entries needed the clause and their condition numbers.
+Each grading prints how many entries needed the clause, their condition numbers, and the
+largest share of the bound any of them used.
 """
 import numpy as np
 import pytest
@@ -32,8 +33,15 @@ pytestmark = pytest.mark.gpu
 ACC_ULP = 2.0 ** -23       # one fp32 ulp per accumulation step
 G_SPLIT = 2.0 ** -18       # the bf16 rounding of G's lo half
 G_EVAL = 2.0 ** -20        # fp32 evaluation of a G entry
-SEG_STEPS = 64             # compensated accumulation: 1024 products per segment
+CHUNK = 32768              # vocabulary columns per gradient chunk
 Z_SLACK_REL = 2.0 ** -14   # fp32 tensor-core logits: 2 x (D / 16) x 2^-23 at D = 4096
+
+
+def lce_steps(T, V, filtered=False):
+    """Accumulation steps of one launch of each gradient GEMM (see the module docstring)."""
+    t_pad = -(-T // 128) * 128
+    v_pad = -(-V // 256) * 256
+    return {"dW": (2 if filtered else 1) * t_pad // 16, "dE": 2 * min(v_pad, CHUNK) // 16}
 
 
 def sum_bound(steps):
@@ -58,10 +66,11 @@ def _bf16_half_ulp(v):
     return 0.5 * np.ldexp(1.0, np.maximum(e - 8, -133))
 
 
-def grade_sum(got, want, abs_terms, what, steps=SEG_STEPS):
+def grade_sum(got, want, abs_terms, what, steps):
     """bf16 bits (or fp32 values) of a GEMM output vs the fp64 oracle and its sum of |terms|.
     Returns the report line: entries beyond one ulp (bf16) or the plain fp32 tolerance, how
-    many of them only the cancellation clause passes, and their condition numbers."""
+    many of them only the cancellation clause passes, their condition numbers, and the largest
+    share of the clause's bound they used."""
     beta = sum_bound(steps)
     want = np.asarray(want, np.float64)
     abs_terms = np.asarray(abs_terms, np.float64)
@@ -69,23 +78,25 @@ def grade_sum(got, want, abs_terms, what, steps=SEG_STEPS):
         d = R.bf16_ulp_distance(got, want)
         val = O.widen(got, "bf16")
         plain = d <= 1
-        within = np.abs(val - want) <= beta * abs_terms + _bf16_half_ulp(val)
+        slack = beta * abs_terms + _bf16_half_ulp(val)
     else:
         val = got.astype(np.float64)
-        err = np.abs(val - want)
-        plain = err <= 1e-6 + 1e-4 * np.abs(want)
-        within = err <= beta * abs_terms
+        plain = np.abs(val - want) <= 1e-6 + 1e-4 * np.abs(want)
+        slack = beta * abs_terms
+    err = np.abs(val - want)
+    within = err <= slack
     ok = plain | within
     clause = ~plain & within
     cond = abs_terms / np.maximum(np.abs(want), 1e-300)
     info = (f"{what}: {np.sum(~plain)} of {plain.size} beyond the plain bar, {np.sum(clause)} passed by the "
-            f"cancellation clause (beta = {beta:.3g})")
+            f"cancellation clause (beta = {beta:.3g}, {steps} accumulation steps)")
     if clause.any():
         c = cond[clause]
-        info += f", condition numbers {c.min():.3g} .. {c.max():.3g} (median {np.median(c):.3g})"
+        info += (f", condition numbers {c.min():.3g} .. {c.max():.3g} (median {np.median(c):.3g}), "
+                 f"at most {np.max(err[clause] / slack[clause]):.2f} of the bound used")
         info += f"; plain-bar entries: median condition {np.median(cond[plain]):.3g}"
     if (~ok).any():
-        info += (f"; {np.sum(~ok)} FAIL, worst |err| / sum|t| {np.max((np.abs(val - want) / abs_terms)[~ok]):.3g}"
+        info += (f"; {np.sum(~ok)} FAIL, worst |err| / sum|t| {np.max((err / abs_terms)[~ok]):.3g}"
                  f" at condition {cond[~ok][:5]}")
     print(info)
     assert ok.all(), info
@@ -126,8 +137,9 @@ def full_check(vce, p, reduction="mean", grad_output=1.0, grad_dtype=torch.bfloa
     if reduction != "none":
         G.check_reduced(loss_out.item(), ref["loss_out"])
     aG = np.abs(ref["grad"])
-    grade_sum(host(dE), ref["dE"], aG @ np.abs(W), "dE")
-    grade_sum(host(dW), ref["dW"], aG.T @ np.abs(E), "dW")
+    st = lce_steps(p.T, p.V)
+    grade_sum(host(dE), ref["dE"], aG @ np.abs(W), "dE", st["dE"])
+    grade_sum(host(dW), ref["dW"], aG.T @ np.abs(E), "dW", st["dW"])
 
 
 def test_pages_toy_shape(vce):
@@ -191,9 +203,11 @@ def test_full_size_sampled(vce):
     z = E[rows] @ W.T
     sub = {k: v[rows] for k, v in fwd.items()}
     Gr = O.ce_grad_rows(z, p.labels[rows], sub, c[rows])
-    grade_sum(host(dE[torch.from_numpy(rows).cuda()]), Gr @ W, np.abs(Gr) @ aW, "full-size dE rows")
+    st = lce_steps(p.T, p.V)
+    grade_sum(host(dE[torch.from_numpy(rows).cuda()]), Gr @ W, np.abs(Gr) @ aW, "full-size dE rows", st["dE"])
     # dW rows: one vocabulary column of G over all T rows, times E
     targets = np.unique(p.labels[fwd["valid"]])
     cols = np.unique(np.concatenate([rng.choice(p.V, 112, replace=False), rng.choice(targets, 16, replace=False)]))
     Gc = O.linear_ce_grad_columns(E, W, p.labels, fwd, c, cols)
-    grade_sum(host(dW[torch.from_numpy(cols).cuda()]), Gc.T @ E, np.abs(Gc).T @ np.abs(E), "full-size dW rows")
+    grade_sum(host(dW[torch.from_numpy(cols).cuda()]), Gc.T @ E, np.abs(Gc).T @ np.abs(E), "full-size dW rows",
+              st["dW"])

@@ -36,7 +36,11 @@ debug_library_path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "l
 class VceError(RuntimeError):
     def __init__(self, fn, code):
         self.code = code
-        super().__init__(f"{fn} failed: {code} ({vce_status_string(code)})")
+        msg = f"{fn} failed: {code} ({vce_status_string(code)})"
+        if code == -7:   # VCE_ERR_CUDA: name the CUDA runtime result behind it
+            e = _get().vce_last_cuda_error()
+            msg += f"; CUDA: {e} {_get().vce_cuda_error_name(e).decode()}"
+        super().__init__(msg)
 
 
 def _load(path=None):
@@ -51,6 +55,9 @@ def _load(path=None):
     L.vce_status_string.restype = ctypes.c_char_p
     L.vce_row_stats_floats.restype = sz
     L.vce_get_status.argtypes = [p, p, p]
+    L.vce_last_cuda_error.restype = i32
+    L.vce_cuda_error_name.argtypes = [i32]
+    L.vce_cuda_error_name.restype = ctypes.c_char_p
     L.vce_debug_checks.restype = i32
     L.vce_debug_status.argtypes = [p]
     L.vce_debug_status.restype = i32
@@ -77,7 +84,7 @@ def _load(path=None):
                                               p, p, p, p]
         L.vce_gemm_bf16.argtypes = [p, i32, p, i32, i64, i64, i64, p, i64, p]
         L.vce_gemm_bf16.restype = i32
-        L.vce_gemm_bf16_variant.argtypes = [p, i32, p, i32, i64, i64, i64, p, i64, i32, i32, i32, p]
+        L.vce_gemm_bf16_variant.argtypes = [p, i32, p, i32, i64, i64, i64, p, i64, i32, p]
         L.vce_gemm_bf16_variant.restype = i32
         L.vce_test_gemm_stall.argtypes = [p, p, i64, i64, i64, p, ctypes.c_uint64, p, p]
         L.vce_test_gemm_stall.restype = i32
@@ -368,17 +375,15 @@ def vce_gemm_bf16(A, B, a_mn=False, b_mn=False, *, C=None, stream=None):
     return C
 
 
-def vce_gemm_bf16_variant(A, B, a_mn=False, b_mn=False, *, pair=False, bn=256, seg_kb=0, C=None, stream=None):
-    """vce_gemm_bf16 in a chosen launch form: CTA pairs or single CTAs, 128- or 256-column
-    tiles, compensated accumulation over runs of seg_kb * 64 products (bn = 128)."""
+def vce_gemm_bf16_variant(A, B, a_mn=False, b_mn=False, *, pair=False, C=None, stream=None):
+    """vce_gemm_bf16 in a chosen launch form: CTA pairs (256-row tiles) or single CTAs."""
     M = A.shape[1] if a_mn else A.shape[0]
     K = A.shape[0] if a_mn else A.shape[1]
     N = B.shape[1] if b_mn else B.shape[0]
     if C is None:
         C = torch.empty(M, N, dtype=torch.float32, device=A.device)
     _check("vce_gemm_bf16_variant", _get().vce_gemm_bf16_variant(
-        _ptr(A), int(a_mn), _ptr(B), int(b_mn), M, N, K, _ptr(C), C.stride(0), int(pair), int(bn), int(seg_kb),
-        _stream(stream)))
+        _ptr(A), int(a_mn), _ptr(B), int(b_mn), M, N, K, _ptr(C), C.stride(0), int(pair), _stream(stream)))
     return C
 
 

@@ -25,8 +25,10 @@ BUILD_DEBUG = os.path.join(PKG, "_build_debug")
 LIB_DEBUG = os.path.join(PKG, "libvce_debug.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "-I", INCLUDE, "-I", CSRC,
-              "--expt-relaxed-constexpr"]
+# Hidden symbol visibility: only the C ABI (VCE_API in include/*.h) is exported, so two builds
+# loaded in one process (the release and the debug-check library) share no internal symbol.
+NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2,-fvisibility=hidden", "-I", INCLUDE,
+              "-I", CSRC, "--expt-relaxed-constexpr"]
 
 
 def _nvcc():

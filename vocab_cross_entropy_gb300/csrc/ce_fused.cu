@@ -31,14 +31,21 @@
 namespace vce {
 namespace {
 
+// The weight 1/N of the mean (N = the number of valid labels) into *inv_n, and the status word
+// cleared for the kernels that follow on the stream.  Eight labels per thread are in flight
+// before any is used.
 template <int NT>
 __global__ void __launch_bounds__(NT) k_ce_count_valid(const int64_t* __restrict__ labels, int64_t T, int64_t V,
-                                                       int64_t ignore_index, float* inv_n) {
+                                                       int64_t ignore_index, float* inv_n, int32_t* status) {
+    constexpr int U = 8;
     __shared__ long long sm_n[NT / 32];
     long long n = 0;
-    for (int64_t i = threadIdx.x; i < T; i += NT) {
-        const int64_t t = labels[i];
-        n += (t != ignore_index && t >= 0 && t < V) ? 1 : 0;
+    for (int64_t i0 = threadIdx.x; i0 < T; i0 += (int64_t)NT * U) {
+        int64_t t[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) t[u] = i0 + (int64_t)u * NT < T ? labels[i0 + (int64_t)u * NT] : ignore_index;
+#pragma unroll
+        for (int u = 0; u < U; ++u) n += (t[u] != ignore_index && t[u] >= 0 && t[u] < V) ? 1 : 0;
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) n += __shfl_xor_sync(0xFFFFFFFFu, n, off);
@@ -49,6 +56,7 @@ __global__ void __launch_bounds__(NT) k_ce_count_valid(const int64_t* __restrict
         long long tot = 0;
         for (int w = 0; w < NT / 32; ++w) tot += sm_n[w];
         *inv_n = tot > 0 ? (float)(1.0 / (double)tot) : 0.f;   // the value k_ce_reduce computes
+        *status = 0;
     }
 }
 
@@ -165,12 +173,14 @@ extern "C" int ce_forward_backward_ls(const void* logits, vce_dtype dt, int64_t 
     if (red != VCE_RED_NONE && !aligned(loss_out, 4)) return VCE_ERR_ALIGN;
     int rc = require_sm100();
     if (rc) return rc;
-    if (cudaMemsetAsync(status, 0, sizeof(int32_t), s) != cudaSuccess) return VCE_ERR_CUDA;
+    // the mean's weight first (it also clears the status word); otherwise clear it here
+    if (T > 0 && red == VCE_RED_MEAN) {
+        k_ce_count_valid<1024><<<1, 1024, 0, s>>>(labels, T, V, ignore_index, loss_out, status);
+        if (cudaGetLastError() != cudaSuccess) return VCE_ERR_CUDA;
+    } else if (cudaMemsetAsync(status, 0, sizeof(int32_t), s) != cudaSuccess) {
+        return VCE_ERR_CUDA;
+    }
     if (T > 0) {
-        if (red == VCE_RED_MEAN) {
-            k_ce_count_valid<1024><<<1, 1024, 0, s>>>(labels, T, V, ignore_index, loss_out);
-            if (cudaGetLastError() != cudaSuccess) return VCE_ERR_CUDA;
-        }
         const float eps = label_smoothing;
         // The row held in shared memory where the layout allows it, else the L2 re-read.
         bool launched = false;

@@ -40,9 +40,11 @@ namespace {
 // Three blocks of 512 threads per SM (registers capped at 42): the row stream is issue- and
 // latency-bound, and 48 resident warps per SM measured 10% faster than 32 at T=16384, V=128256 bf16.
 // kSmooth: label smoothing eps > 0 (the row's sum of all logits is reduced alongside; two
-// blocks per SM, since the extra sum does not fit in 42 registers).
-template <typename S, int NT, bool kSmooth>
-__global__ void __launch_bounds__(NT, (kSmooth ? 1024 : 1536) / NT) k_ce_fwd(const S* __restrict__ logits, int64_t T, int64_t V, int64_t ld,
+// blocks per SM, since the extra sum does not fit in 42 registers).  kU: 16-byte loads in
+// flight per thread; 8 (two blocks per SM) covers a 64 KB row in one round of loads.
+template <typename S, int NT, bool kSmooth, int kU = kUnroll>
+__global__ void __launch_bounds__(NT, (kSmooth || kU > kUnroll ? 1024 : 1536) / NT)
+    k_ce_fwd(const S* __restrict__ logits, int64_t T, int64_t V, int64_t ld,
                                                const int64_t* __restrict__ labels, int64_t ignore_index,
                                                float eps, float* __restrict__ loss_rows,
                                                float4* __restrict__ row_stats, int32_t* status) {
@@ -61,7 +63,8 @@ __global__ void __launch_bounds__(NT, (kSmooth ? 1024 : 1536) / NT) k_ce_fwd(con
         }
         if (!dbg::ok(row >= 0 && row < T && V <= ld, dbg::kRow)) continue;   // block-uniform
         float m = -kInf, s = 0.f, mb = 0.f, sz = 0.f;
-        fwd_segment<S, NT, true, kLoadStream, kSmooth>(logits + row * ld, V, t, m, s, mb, &sm_zt, threadIdx.x, &sz);
+        fwd_segment<S, NT, true, kLoadStream, kSmooth, kU>(logits + row * ld, V, t, m, s, mb, &sm_zt, threadIdx.x,
+                                                            &sz);
         if (kSmooth) {   // block sum of the logits (the barrier below publishes the warp sums)
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) sz += __shfl_xor_sync(0xFFFFFFFFu, sz, off);
@@ -83,22 +86,85 @@ __global__ void __launch_bounds__(NT, (kSmooth ? 1024 : 1536) / NT) k_ce_fwd(con
     }
 }
 
+// One warp per row, for rows of at most 64 KB: each lane streams its share of the row with
+// eight 16-byte loads in flight (six with label smoothing, whose row sum needs registers) and
+// the warp reduces with shuffles only, so no block barrier sits between rows and every
+// resident warp keeps its loads in flight.  24 warps per SM (80 registers).
+constexpr int kWarpRowThreads = 256;
+
+template <typename S, bool kSmooth>
+__global__ void __launch_bounds__(kWarpRowThreads, 3)
+    k_ce_fwd_warp(const S* __restrict__ logits, int64_t T, int64_t V, int64_t ld, const int64_t* __restrict__ labels,
+                  int64_t ignore_index, float eps, float* __restrict__ loss_rows, float4* __restrict__ row_stats,
+                  int32_t* status) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = (int64_t)gridDim.x * (kWarpRowThreads / 32);
+    for (int64_t row = (int64_t)blockIdx.x * (kWarpRowThreads / 32) + (threadIdx.x >> 5); row < T; row += warps) {
+        const int64_t t = labels[row];
+        const bool ignored = (t == ignore_index);
+        if (ignored || t < 0 || t >= V) {   // no read of the row: loss 0 (ignored) or NaN (bad label)
+            if (lane == 0) {
+                loss_rows[row] = ignored ? 0.f : __int_as_float(0x7FC00000);
+                row_stats[row] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (!ignored) flag_label_error(status);
+            }
+            continue;
+        }
+        if (!dbg::ok(row >= 0 && row < T && V <= ld, dbg::kRow)) continue;   // warp-uniform
+        float m = -kInf, s = 0.f, mb = 0.f, sz = 0.f;
+        float zt_found = kInf;   // stays +inf except in the lane that meets the target
+        fwd_segment<S, 32, true, kLoadStream, kSmooth, kSmooth ? 6 : 8>(logits + row * ld, V, t, m, s, mb, &zt_found,
+                                                                        lane, &sz);
+        ms_warp_reduce(m, s);
+        if (kSmooth) {
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) sz += __shfl_xor_sync(0xFFFFFFFFu, sz, off);
+        }
+        const unsigned hit = __ballot_sync(0xFFFFFFFFu, zt_found != kInf);
+        const float zt = hit ? __shfl_sync(0xFFFFFFFFu, zt_found, __ffs(hit) - 1) : 0.f;
+        if (lane == 0) {
+            float loss;
+            row_stats[row] = kSmooth ? ce_row_finish_smoothed(m, s, zt, sz, V, eps, &loss) : ce_row_finish(m, s, zt, &loss);
+            loss_rows[row] = loss;
+        }
+    }
+}
+
 // Fixed-order reduction of the per-row losses (one block).  Rows with a bad label add NaN.
-// MEAN also writes each valid row's weight 1/N into its statistics.
+// MEAN also writes each valid row's weight 1/N into its statistics.  Thread tid takes rows
+// tid + NT (8 j + u), u < 8: eight rows' label and loss loads are in flight before any is
+// used, and the validity of up to 64 rows stays in a register mask for the weight pass (longer
+// inputs reread their labels there).  The partition is fixed, so the sum is bitwise
+// reproducible.
 template <int NT>
 __global__ void __launch_bounds__(NT) k_ce_reduce(const float* __restrict__ loss_rows, const int64_t* __restrict__ labels,
                                                   int64_t T, int64_t V, int64_t ignore_index, int red,
                                                   float* loss_out, float4* row_stats) {
+    constexpr int U = 8;
     __shared__ double sm_a[NT / 32];
     __shared__ long long sm_n[NT / 32];
     __shared__ float sm_inv;
     double acc = 0.0;
     long long n = 0;
-    for (int64_t i = threadIdx.x; i < T; i += NT) {
-        const int64_t t = labels[i];
-        if (t != ignore_index) {
-            acc += (double)loss_rows[i];
-            n += (t >= 0 && t < V) ? 1 : 0;
+    uint64_t valid_mask = 0;   // bit j * U + u: row tid + NT (U j + u) is valid (j < 8)
+    int j = 0;
+    for (int64_t i0 = threadIdx.x; i0 < T; i0 += (int64_t)NT * U, ++j) {
+        int64_t t[U];
+        float l[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t i = i0 + (int64_t)u * NT;
+            t[u] = i < T ? labels[i] : ignore_index;
+            l[u] = i < T ? loss_rows[i] : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            if (t[u] != ignore_index) {
+                acc += (double)l[u];
+                const bool ok = t[u] >= 0 && t[u] < V;
+                n += ok ? 1 : 0;
+                if (ok && j < 8) valid_mask |= 1ull << (j * U + u);
+            }
         }
     }
 #pragma unroll
@@ -129,9 +195,21 @@ __global__ void __launch_bounds__(NT) k_ce_reduce(const float* __restrict__ loss
     if (red != VCE_RED_MEAN) return;
     __syncthreads();
     const float inv = sm_inv;
-    for (int64_t i = threadIdx.x; i < T; i += NT) {
-        const int64_t t = labels[i];
-        if (t != ignore_index && t >= 0 && t < V) row_stats[i].w = inv;
+    j = 0;
+    for (int64_t i0 = threadIdx.x; i0 < T; i0 += (int64_t)NT * U, ++j) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t i = i0 + (int64_t)u * NT;
+            if (i >= T) break;
+            bool ok;
+            if (j < 8) {
+                ok = (valid_mask >> (j * U + u)) & 1ull;
+            } else {
+                const int64_t t = labels[i];
+                ok = t != ignore_index && t >= 0 && t < V;
+            }
+            if (ok) row_stats[i].w = inv;
+        }
     }
 }
 
@@ -217,12 +295,24 @@ __global__ void k_ce_merge(const float4* __restrict__ chunk_stats, int k, int64_
 // ------------------------------------------------------------------------------------------
 // host side
 
-template <typename S, int NT>
+template <typename S, int NT, int kU = kUnroll>
 cudaError_t launch_fwd(const void* logits, int64_t T, int64_t V, int64_t ld, const int64_t* labels, int64_t ig,
                        float eps, float* loss_rows, float* row_stats, int32_t* status, cudaStream_t s) {
-    auto kern = eps > 0.f ? k_ce_fwd<S, NT, true> : k_ce_fwd<S, NT, false>;
+    // label smoothing keeps four loads in flight: its row sum needs the registers
+    auto kern = eps > 0.f ? k_ce_fwd<S, NT, true, kUnroll> : k_ce_fwd<S, NT, false, kU>;
     kern<<<grid_for(kern, NT, T), NT, 0, s>>>(reinterpret_cast<const S*>(logits), T, V, ld, labels, ig, eps,
                                               loss_rows, reinterpret_cast<float4*>(row_stats), status);
+    return cudaGetLastError();
+}
+
+template <typename S>
+cudaError_t launch_fwd_warp(const void* logits, int64_t T, int64_t V, int64_t ld, const int64_t* labels, int64_t ig,
+                            float eps, float* loss_rows, float* row_stats, int32_t* status, cudaStream_t s) {
+    auto kern = eps > 0.f ? k_ce_fwd_warp<S, true> : k_ce_fwd_warp<S, false>;
+    const int64_t blocks = (T + kWarpRowThreads / 32 - 1) / (kWarpRowThreads / 32);
+    kern<<<grid_for(kern, kWarpRowThreads, blocks), kWarpRowThreads, 0, s>>>(
+        reinterpret_cast<const S*>(logits), T, V, ld, labels, ig, eps, loss_rows, reinterpret_cast<float4*>(row_stats),
+        status);
     return cudaGetLastError();
 }
 
@@ -239,6 +329,7 @@ cudaError_t launch_chunk_fwd(const SegTable& tab, const int64_t* labels, int64_t
 template <typename S>
 cudaError_t dispatch_fwd(int nt, const void* logits, int64_t T, int64_t V, int64_t ld, const int64_t* labels,
                          int64_t ig, float eps, float* lr, float* rs, int32_t* st, cudaStream_t s) {
+    if (nt == -512) return launch_fwd<S, 512, 8>(logits, T, V, ld, labels, ig, eps, lr, rs, st, s);
     if (nt == 128) return launch_fwd<S, 128>(logits, T, V, ld, labels, ig, eps, lr, rs, st, s);
     if (nt == 256) return launch_fwd<S, 256>(logits, T, V, ld, labels, ig, eps, lr, rs, st, s);
     return launch_fwd<S, 512>(logits, T, V, ld, labels, ig, eps, lr, rs, st, s);
@@ -302,19 +393,30 @@ extern "C" int ce_forward_ls(const void* logits, vce_dtype dt, int64_t T, int64_
     if ((rc = require_sm100())) return rc;
     if (cudaMemsetAsync(status, 0, sizeof(int32_t), s) != cudaSuccess) return VCE_ERR_CUDA;
     if (T > 0) {
-        // Rows streamed through shared memory where the layout allows it, else one block per
-        // row with loads from global memory.  Rows of 32-64 KB with fewer than 64 per SM also
-        // take the per-block kernel: the ring's ramp and tail then weigh more than its
-        // streaming gains (measured at 4096 x 32000 bf16: 0.0631 against 0.0713 ms; at
-        // 15624 x 32000 the two are equal, and longer rows favour the ring).
+        // Rows of at most 32 KB: one warp per row (k_ce_fwd_warp; 8192 x 16000 bf16: 0.0695
+        // against 0.0815 ms on the ring).  Rows of 32-64 KB with fewer than 64 per SM: one block
+        // per row with the whole row's loads in flight at once (the ring's ramp and tail weigh
+        // more than its streaming gains there; a warp per row streams them latency-bound).
+        // Longer rows stream through shared memory where the layout allows it, else one block
+        // per row with loads from global memory.
         bool launched = false;
         const int64_t row_bytes = V * (int64_t)es;
         const bool few_short_rows = row_bytes > 32768 && row_bytes <= 65536 && T < 64 * (int64_t)device_sm_count();
-        cudaError_t e = few_short_rows ? cudaSuccess
-                                       : launch_fwd_ring(dt, logits, T, V, ld, labels, ignore_index, label_smoothing,
-                                                         loss_rows, row_stats, status, s, &launched);
+        cudaError_t e = cudaSuccess;
+        int nt = pick_threads(row_bytes);
+        if (row_bytes <= 32768) {
+            e = dt == VCE_BF16 ? launch_fwd_warp<uint16_t>(logits, T, V, ld, labels, ignore_index, label_smoothing,
+                                                           loss_rows, row_stats, status, s)
+                               : launch_fwd_warp<float>(logits, T, V, ld, labels, ignore_index, label_smoothing,
+                                                        loss_rows, row_stats, status, s);
+            launched = true;
+        } else if (few_short_rows) {
+            nt = -512;   // 512 threads, eight loads in flight each
+        } else {
+            e = launch_fwd_ring(dt, logits, T, V, ld, labels, ignore_index, label_smoothing, loss_rows, row_stats,
+                                status, s, &launched);
+        }
         if (e == cudaSuccess && !launched) {
-            const int nt = pick_threads(V * (int64_t)es);
             e = dt == VCE_BF16 ? dispatch_fwd<uint16_t>(nt, logits, T, V, ld, labels, ignore_index, label_smoothing,
                                                         loss_rows, row_stats, status, s)
                                : dispatch_fwd<float>(nt, logits, T, V, ld, labels, ignore_index, label_smoothing,

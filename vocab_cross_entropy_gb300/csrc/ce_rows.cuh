@@ -21,7 +21,8 @@ constexpr int kUnroll = 4;
 // kLazy: sum against a lazily updated reference (ms_push_lazy); otherwise m ends as the exact
 // maximum of the non-target values (ms_push), as the chunk statistics report it.
 // kSumZ: also add every value of the segment (target included) into sz.
-template <typename S, int NT, bool kLazy, int kLoad = kLoadStream, bool kSumZ = false>
+// kU: 16-byte loads in flight per thread before any is used.
+template <typename S, int NT, bool kLazy, int kLoad = kLoadStream, bool kSumZ = false, int kU = kUnroll>
 __device__ __forceinline__ void fwd_segment(const S* __restrict__ row, int64_t w, int64_t tl, float& m,
                                             float& s, float& mb, float* zt_out, const int tid,
                                             float* sz = nullptr) {
@@ -48,15 +49,15 @@ __device__ __forceinline__ void fwd_segment(const S* __restrict__ row, int64_t w
 
     const uint4* vp = reinterpret_cast<const uint4*>(row + h);
     const uint64_t pol = l2_policy<kLoad>();
-    for (int64_t v0 = tid; v0 < nvec; v0 += (int64_t)NT * kUnroll) {
-        uint4 r[kUnroll];
+    for (int64_t v0 = tid; v0 < nvec; v0 += (int64_t)NT * kU) {
+        uint4 r[kU];
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
+        for (int u = 0; u < kU; ++u) {
             const int64_t vi = v0 + (int64_t)u * NT;
             if (vi < nvec) r[u] = ld16<kLoad>(vp + vi, pol);
         }
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
+        for (int u = 0; u < kU; ++u) {
             const int64_t vi = v0 + (int64_t)u * NT;
             if (vi < nvec) {
                 float v[G];

@@ -1,6 +1,6 @@
-// The tensor-core GEMM as a plain fp32-output product, and its test hooks: the variants the
-// linear-CE runs (single CTAs or CTA pairs, 128- or 256-column tiles, compensated
-// accumulation), the give-up path of the pipeline's bounded waits, and K-block skipping.
+// The tensor-core GEMM as a plain fp32-output product, and its test hooks: the two launch
+// forms the linear-CE runs (single CTAs or CTA pairs), the give-up path of the pipeline's
+// bounded waits, and K-block skipping.
 // No page counterpart: they expose the building block of the linear-CE for testing.
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -16,8 +16,8 @@ namespace {
 
 using tc::BK;
 using tc::BM;
+using tc::BN;
 using tc::Mat;
-using tc::Variant;
 
 inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
@@ -25,24 +25,23 @@ bool sizes_ok(int64_t M, int64_t N, int64_t K, int64_t lim) {
     return M >= 1 && N >= 1 && K >= 1 && M % 8 == 0 && N % 8 == 0 && K % 8 == 0 && M <= lim && N <= lim && K <= lim;
 }
 
-// C[M, ldc] = op(A) op(B)^T with the given layouts and variant.
+// C[M, ldc] = op(A) op(B)^T with the given layouts, on CTA pairs or single CTAs.
 int gemm(const void* A, int a_mn, const void* B, int b_mn, int64_t M, int64_t N, int64_t K, float* C, int64_t ldc,
-         Variant v, int seg_kb, cudaStream_t s) {
+         bool pair, cudaStream_t s) {
     const Mat ma = a_mn ? Mat{A, M, K, M} : Mat{A, K, M, K};
     const Mat mb = b_mn ? Mat{B, N, K, N} : Mat{B, K, N, K};
     const int nk = (int)cdiv(K, BK);
-    tc::GemmArgs g{(int)cdiv(M, BM), (int)cdiv(N, v.bn), nk, nk, 0, 0, 0, 0, nullptr};
-    g.seg_kb = seg_kb;
+    tc::GemmArgs g{(int)cdiv(M, BM), (int)cdiv(N, BN), nk, nk, 0, 0, 0, 0, nullptr};
     tc::EpiStore::Params ep{C, ldc, M, N, 0, 0};
     cudaError_t e;
     if (a_mn && b_mn)
-        e = tc::launch_gemm<tc::EpiStore, true, true>(ma, ma, mb, g, ep, v, s);
+        e = tc::launch_gemm<tc::EpiStore, true, true>(ma, ma, mb, g, ep, pair, s);
     else if (a_mn)
-        e = tc::launch_gemm<tc::EpiStore, true, false>(ma, ma, mb, g, ep, v, s);
+        e = tc::launch_gemm<tc::EpiStore, true, false>(ma, ma, mb, g, ep, pair, s);
     else if (b_mn)
-        e = tc::launch_gemm<tc::EpiStore, false, true>(ma, ma, mb, g, ep, v, s);
+        e = tc::launch_gemm<tc::EpiStore, false, true>(ma, ma, mb, g, ep, pair, s);
     else
-        e = tc::launch_gemm<tc::EpiStore, false, false>(ma, ma, mb, g, ep, v, s);
+        e = tc::launch_gemm<tc::EpiStore, false, false>(ma, ma, mb, g, ep, pair, s);
     return e == cudaSuccess ? VCE_OK : VCE_ERR_CUDA;
 }
 
@@ -62,21 +61,19 @@ extern "C" int vce_gemm_bf16(const void* A, int a_mn, const void* B, int b_mn, i
     if (!aligned(A, 16) || !aligned(B, 16) || !aligned(C, 16) || (ldc % 4)) return VCE_ERR_ALIGN;
     int rc = require_sm100();
     if (rc) return rc;
-    return gemm(A, a_mn, B, b_mn, M, N, K, C, ldc, Variant{cdiv(M, BM) % 2 == 0, 256}, 0, s);
+    return gemm(A, a_mn, B, b_mn, M, N, K, C, ldc, cdiv(M, BM) % 2 == 0, s);
 }
 
 extern "C" int vce_gemm_bf16_variant(const void* A, int a_mn, const void* B, int b_mn, int64_t M, int64_t N, int64_t K,
-                                     float* C, int64_t ldc, int pair, int bn, int seg_kb, vce_stream_t s) {
+                                     float* C, int64_t ldc, int pair, vce_stream_t s) {
     if (!A || !B || !C) return VCE_ERR_NULL;
     if (!sizes_ok(M, N, K, 1 << 30)) return VCE_ERR_SHAPE;
     if (ldc < N) return VCE_ERR_LD;
-    if ((pair != 0 && pair != 1) || (bn != 128 && bn != 256) || seg_kb < 0 || (seg_kb > 0 && bn != 128) ||
-        (pair && cdiv(M, BM) % 2))
-        return VCE_ERR_ARG;
+    if ((pair != 0 && pair != 1) || (pair && cdiv(M, BM) % 2)) return VCE_ERR_ARG;
     if (!aligned(A, 16) || !aligned(B, 16) || !aligned(C, 16) || (ldc % 4)) return VCE_ERR_ALIGN;
     int rc = require_sm100();
     if (rc) return rc;
-    return gemm(A, a_mn, B, b_mn, M, N, K, C, ldc, Variant{pair != 0, bn}, seg_kb, s);
+    return gemm(A, a_mn, B, b_mn, M, N, K, C, ldc, pair != 0, s);
 }
 
 extern "C" int vce_test_gemm_stall(const void* A, const void* B, int64_t M, int64_t N, int64_t K, float* C,
@@ -89,12 +86,12 @@ extern "C" int vce_test_gemm_stall(const void* A, const void* B, int64_t M, int6
     if (rc) return rc;
     if (cudaMemsetAsync(status, 0, sizeof(int32_t), s) != cudaSuccess) return VCE_ERR_CUDA;
     const int nk = (int)cdiv(K, BK);
-    const Variant v{cdiv(M, BM) % 2 == 0, 256};
-    tc::GemmArgs g{(int)cdiv(M, BM), (int)cdiv(N, v.bn), nk, nk, 0, 0, 0, 0, status, 16u, wait_ns};
+    tc::GemmArgs g{(int)cdiv(M, BM), (int)cdiv(N, BN), nk, nk, 0, 0, 0, 0, status, 16u, wait_ns};
     tc::EpiStore::Params ep{C, N, M, N, 0, 0};
     const Mat ma{A, K, M, K}, mb{B, K, N, K};
-    return tc::launch_gemm<tc::EpiStore, false, false>(ma, ma, mb, g, ep, v, s) == cudaSuccess ? VCE_OK
-                                                                                                : VCE_ERR_CUDA;
+    return tc::launch_gemm<tc::EpiStore, false, false>(ma, ma, mb, g, ep, cdiv(M, BM) % 2 == 0, s) == cudaSuccess
+               ? VCE_OK
+               : VCE_ERR_CUDA;
 }
 
 extern "C" int vce_test_gemm_skip(const void* A, const void* B, int64_t M, int64_t N, int64_t K, const uint32_t* skip,
@@ -106,12 +103,12 @@ extern "C" int vce_test_gemm_skip(const void* A, const void* B, int64_t M, int64
     int rc = require_sm100();
     if (rc) return rc;
     const int nk = (int)cdiv(K, BK);
-    tc::GemmArgs g{(int)cdiv(M, BM), (int)cdiv(N, 256), nk, nk, 0, 0, 0, 0, nullptr};
+    tc::GemmArgs g{(int)cdiv(M, BM), (int)cdiv(N, BN), nk, nk, 0, 0, 0, 0, nullptr};
     g.skip = skip;
     g.skip_ld = (int)skip_ld;
     tc::EpiStore::Params ep{C, N, M, N, 0, 0};
     const Mat ma{A, K, M, K}, mb{B, K, N, K};
-    return tc::launch_gemm<tc::EpiStore, false, false>(ma, ma, mb, g, ep, Variant{false, 256}, s) == cudaSuccess
+    return tc::launch_gemm<tc::EpiStore, false, false>(ma, ma, mb, g, ep, false, s) == cudaSuccess
                ? VCE_OK
                : VCE_ERR_CUDA;
 }

@@ -39,12 +39,9 @@ namespace vce {
 namespace {
 
 using tc::BM;
+using tc::BN;
 using tc::BK;
 using tc::Mat;
-using tc::Variant;
-
-constexpr int BN = 256;                 // vocabulary columns of a z tile (statistics, gradient tiles)
-constexpr int kSegKb = 16;              // K blocks (of 64) per compensated accumulation segment
 
 constexpr int64_t kChunkCols = 32768;   // vocabulary columns per gradient chunk (a multiple of BN)
 
@@ -56,7 +53,6 @@ inline int64_t round_up(int64_t a, int64_t b) { return cdiv(a, b) * b; }
 
 // Step 1: per (row, vocabulary tile): (max, sum-exp) over non-target columns < V, target logit.
 struct EpiStats {
-    static constexpr bool kCompensated = false;
     struct Params {
         const int64_t* labels;
         int64_t ignore_index, T, V;
@@ -108,7 +104,6 @@ struct EpiStats {
 // ORs its 32 rows' marks; the first warp to set a block's bit also sets it in the transposed
 // table and counts the block.
 struct EpiGrad {
-    static constexpr bool kCompensated = false;
     struct Params {
         const int64_t* labels;
         int64_t T, width, col_off;   // rows, chunk width, chunk's first global column
@@ -126,13 +121,16 @@ struct EpiGrad {
     };
     struct Row {
         float coef, bias, gt, thr;   // thr: p_ij >= eps  <=>  2^(z log2e - bias) >= thr
+        float bias_c;                // bias - log2 |coef|: |coef| 2^(z log2e - bias) = 2^(z log2e - bias_c)
+        uint32_t sign;               // 0x80008000 when coef < 0 (flips both halves of a packed bf16 pair)
         int64_t tl;
         bool zero;
         uint32_t bits;               // kept marks of this row's two 128-column halves of the tile
     };
     __device__ __forceinline__ static void begin(const Params& p, Row& r, int row, int tn) {
         r.zero = true;
-        r.coef = r.bias = r.gt = 0.f;
+        r.coef = r.bias = r.gt = r.bias_c = 0.f;
+        r.sign = 0u;
         r.thr = kInf;
         r.tl = -1;
         r.bits = 0u;
@@ -143,6 +141,8 @@ struct EpiGrad {
                 r.zero = false;
                 r.coef = c * st.y;
                 r.bias = (st.x == -kInf) ? 0.f : st.x * kLog2e;
+                r.bias_c = r.bias - log2f(fabsf(r.coef));   // +inf for coef = 0: every entry 2^-inf = 0
+                r.sign = r.coef < 0.f ? 0x80008000u : 0u;
                 r.gt = c * st.z;
                 r.tl = p.labels[row] - p.col_off;
                 if (st.y > 0.f) r.thr = p.eps / st.y;   // p_ij = sigma(x) 2^(z log2e - bias)
@@ -154,6 +154,23 @@ struct EpiGrad {
     __device__ __forceinline__ static void consume(const Params& p, Row& r, int row, int col0,
                                                    const uint32_t (&acc)[32]) {
         uint32_t hi[16], lo[16];
+        // The common piece -- a weighted row, no filtering, neither its target column nor the
+        // vocabulary's end among its 32 columns -- takes the coefficient into the exponent:
+        // g = 2^(z log2e - bias_c), one FFMA and one exp2 per entry.  An entry below 2^-126
+        // flushes to zero there; G only feeds the dW and dE sums, where such a term is far
+        // below the fp32 rounding of any nonzero sum.
+        if (!r.zero && !p.keep_w && (uint64_t)(r.tl - col0) >= 32u && (int64_t)col0 + 32 <= p.width) {
+#pragma unroll
+            for (int k = 0; k < 32; k += 2) {
+                const float g0 = ex2(fmaf(__uint_as_float(acc[k]), kLog2e, -r.bias_c));
+                const float g1 = ex2(fmaf(__uint_as_float(acc[k + 1]), kLog2e, -r.bias_c));
+                const uint32_t h = pack_bf16x2(g0, g1);
+                hi[k / 2] = h ^ r.sign;
+                lo[k / 2] = pack_bf16x2(g0 - bf16_lo(h), g1 - bf16_hi(h)) ^ r.sign;
+            }
+            store(p, row, col0, hi, lo);
+            return;
+        }
         float emax = 0.f;   // largest 2^(z log2e - bias) over the piece's columns < width
 #pragma unroll
         for (int k = 0; k < 32; k += 2) {
@@ -176,9 +193,13 @@ struct EpiGrad {
         // A target column in the piece keeps its block anyway (begin), so including its
         // value in emax changes nothing.
         if (p.keep_w && !r.zero && emax >= r.thr) r.bits |= 1u << ((col0 % BN) >> 7);
-        // row-major [T_pad][ldg]: 64 contiguous bytes per thread.  Evict-first stores: the
-        // chunk's G (512 MB at T = 8192) is read back from DRAM by the next two GEMMs anyway,
-        // and should not push E and W out of L2 meanwhile (measured 0.4% faster per call).
+        store(p, row, col0, hi, lo);
+    }
+    // row-major [T_pad][ldg]: 64 contiguous bytes per thread.  Evict-first stores: the chunk's G
+    // (512 MB at T = 8192) is read back from DRAM by the next two GEMMs anyway, and should not
+    // push E and W out of L2 meanwhile (measured 0.4% faster per call).
+    __device__ __forceinline__ static void store(const Params& p, int row, int col0, const uint32_t (&hi)[16],
+                                                 const uint32_t (&lo)[16]) {
         // G is [round_up(T, 128)][ldg]
         if (!dbg::ok(row < (p.T + 127) / 128 * 128 && col0 + 32 <= p.ldg, dbg::kTile)) return;
         uint4* dh = reinterpret_cast<uint4*>(p.g_hi + (int64_t)row * p.ldg + col0);
@@ -206,32 +227,39 @@ struct EpiGrad {
     }
 };
 
-// Step 2b, dW rows of the chunk: tc::EpiStore (stored once as sum + compensation).
-
-// Step 2c: the dE partial of one chunk, a (sum, compensation) pair of fp32 tiles, merged into
-// the pair carried in global memory with a two-sum; the first chunk initialises it, the last
-// writes sum + compensation to the output.
+// Step 2b/2c: a partial product merged into a (sum, compensation) pair of fp32 arrays in
+// global memory with a two-sum: the first part initialises the pair, the last writes
+// sum + compensation to the output (bf16 or fp32) at row out_row_off + row.  dE: one part per
+// vocabulary chunk, the pair [T, D] with its compensation array.  dW: one part per half of the
+// rows of T (two parts), the pair the chunk's [width, D] sums alone (comp = null: with two
+// parts the compensation would only ever hold the last merge's error, which is rounded away
+// with it).
 struct EpiKahan {
-    static constexpr bool kCompensated = true;
     struct Params {
-        float *sum, *comp;   // [rows][cols]
+        float *sum, *comp;   // [rows][cols]; comp may be null (the pair's compensation is then 0)
         int64_t rows, cols;
         int first, last;
         void* out;
         int bf16;
+        int64_t out_row_off;
     };
     struct Row {};
     __device__ __forceinline__ static void begin(const Params&, Row&, int, int) {}
     // (a, ka) + (x, kx) -> (s, c): s + c = a + x exactly up to the compensations' own sum
     __device__ __forceinline__ static void merge(float a, float ka, float x, float kx, float& s, float& c) {
-        float e;
-        tc::two_sum(a, x, s, e);
+        s = a + x;   // a + x = s + e exactly (Knuth's two-sum); the compensation accumulates e
+        const float bp = s - a;
+        const float e = (a - (s - bp)) + (x - bp);
         c = (ka + kx) + e;
     }
-    __device__ __forceinline__ static void consume2(const Params& p, Row&, int row, int col0, const float (&x)[32],
-                                                    const float (&kx)[32]) {
+    __device__ __forceinline__ static void consume(const Params& p, Row&, int row, int col0, const uint32_t (&acc)[32]) {
         if (row >= p.rows || col0 >= p.cols) return;
+        float x[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) x[k] = __uint_as_float(acc[k]);
         const int64_t base = (int64_t)row * p.cols + col0;
+        const int64_t obase = (p.out_row_off + row) * p.cols + col0;
+        const bool has_comp = p.comp != nullptr;
         if (p.cols - col0 >= 32) {   // full 32-column piece: 16-byte accesses
             // four groups' loads are issued before their stores: the stores go to the same
             // arrays, so loads interleaved with them would each wait out a memory latency
@@ -242,7 +270,8 @@ struct EpiKahan {
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         ld_a[q] = *reinterpret_cast<const float4*>(p.sum + base + 4 * (q0 + q));
-                        ld_k[q] = *reinterpret_cast<const float4*>(p.comp + base + 4 * (q0 + q));
+                        ld_k[q] = has_comp ? *reinterpret_cast<const float4*>(p.comp + base + 4 * (q0 + q))
+                                           : make_float4(0.f, 0.f, 0.f, 0.f);
                     }
                 }
 #pragma unroll
@@ -250,25 +279,26 @@ struct EpiKahan {
                     float s[4], c[4];
                     if (p.first) {
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) { s[e] = x[4 * q + e]; c[e] = kx[4 * q + e]; }
+                        for (int e = 0; e < 4; ++e) { s[e] = x[4 * q + e]; c[e] = 0.f; }
                     } else {
                         const float av[4] = {ld_a[q - q0].x, ld_a[q - q0].y, ld_a[q - q0].z, ld_a[q - q0].w};
                         const float kv[4] = {ld_k[q - q0].x, ld_k[q - q0].y, ld_k[q - q0].z, ld_k[q - q0].w};
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) merge(av[e], kv[e], x[4 * q + e], kx[4 * q + e], s[e], c[e]);
+                        for (int e = 0; e < 4; ++e) merge(av[e], kv[e], x[4 * q + e], 0.f, s[e], c[e]);
                     }
                     if (p.last) {
                         if (p.bf16) {
                             uint2 w = make_uint2(pack_bf16x2(s[0] + c[0], s[1] + c[1]),
                                                  pack_bf16x2(s[2] + c[2], s[3] + c[3]));
-                            *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(p.out) + base + 4 * q) = w;
+                            *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(p.out) + obase + 4 * q) = w;
                         } else {
-                            *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + base + 4 * q) =
+                            *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + obase + 4 * q) =
                                 make_float4(s[0] + c[0], s[1] + c[1], s[2] + c[2], s[3] + c[3]);
                         }
                     } else {
                         *reinterpret_cast<float4*>(p.sum + base + 4 * q) = make_float4(s[0], s[1], s[2], s[3]);
-                        *reinterpret_cast<float4*>(p.comp + base + 4 * q) = make_float4(c[0], c[1], c[2], c[3]);
+                        if (has_comp)
+                            *reinterpret_cast<float4*>(p.comp + base + 4 * q) = make_float4(c[0], c[1], c[2], c[3]);
                     }
                 }
             }
@@ -278,28 +308,18 @@ struct EpiKahan {
 #pragma unroll
         for (int k = 0; k < 32; ++k) {
             if (k >= n) break;
-            float sv = x[k], cv = kx[k];
-            if (!p.first) merge(p.sum[base + k], p.comp[base + k], x[k], kx[k], sv, cv);
+            float sv = x[k], cv = 0.f;
+            if (!p.first) merge(p.sum[base + k], has_comp ? p.comp[base + k] : 0.f, x[k], 0.f, sv, cv);
             if (p.last) {
                 if (p.bf16)
-                    reinterpret_cast<uint16_t*>(p.out)[base + k] = to_bf16(sv + cv);
+                    reinterpret_cast<uint16_t*>(p.out)[obase + k] = to_bf16(sv + cv);
                 else
-                    reinterpret_cast<float*>(p.out)[base + k] = sv + cv;
+                    reinterpret_cast<float*>(p.out)[obase + k] = sv + cv;
             } else {
                 p.sum[base + k] = sv;
-                p.comp[base + k] = cv;
+                if (has_comp) p.comp[base + k] = cv;
             }
         }
-    }
-    // an uncompensated accumulator tile (filtered GEMMs): the pair (acc, 0)
-    __device__ __forceinline__ static void consume(const Params& p, Row& r, int row, int col0, const uint32_t (&acc)[32]) {
-        float x[32], z[32];
-#pragma unroll
-        for (int k = 0; k < 32; ++k) {
-            x[k] = __uint_as_float(acc[k]);
-            z[k] = 0.f;
-        }
-        consume2(p, r, row, col0, x, z);
     }
     __device__ __forceinline__ static void end(const Params&, Row&, int, int) {}
 };
@@ -331,7 +351,7 @@ struct GemmTimer {
 struct Layout {
     int64_t T, D, V, T_pad, V_pad, Vc, tiles_v;
     int ldw, lde;   // words per row of the two filter tables
-    size_t off_part, off_stats, off_ghi, off_glo, off_sum, off_comp, off_keep_w, off_keep_e, keep_bytes, total;
+    size_t off_part, off_stats, off_ghi, off_glo, off_sum, off_comp, off_wsum, off_keep_w, off_keep_e, keep_bytes, total;
 };
 
 bool layout(int64_t T, int64_t D, int64_t V, Layout* L) {
@@ -356,6 +376,7 @@ bool layout(int64_t T, int64_t D, int64_t V, Layout* L) {
     L->off_glo = take((size_t)L->T_pad * L->Vc * 2);
     L->off_sum = take((size_t)T * D * 4);
     L->off_comp = take((size_t)T * D * 4);
+    L->off_wsum = take((size_t)L->Vc * D * 4);   // dW partial of one chunk's first half of T
     // gradient-filter tables of one chunk: [Vc/128][ldw] and [T_pad/128][lde] bits
     L->ldw = (int)cdiv(L->T_pad / 128, 32);
     L->lde = (int)cdiv(L->Vc / 128, 32);
@@ -410,6 +431,7 @@ int linear_ce_run(const void* E, const void* W, int64_t T, int64_t D, int64_t V,
     uint16_t* glo = reinterpret_cast<uint16_t*>(ws + L.off_glo);
     float* dsum = reinterpret_cast<float*>(ws + L.off_sum);
     float* dcomp = reinterpret_cast<float*>(ws + L.off_comp);
+    float* wsum = reinterpret_cast<float*>(ws + L.off_wsum);
     const bool filter = filter_eps > 0.f;
     uint32_t* keep_w = filter ? reinterpret_cast<uint32_t*>(ws + L.off_keep_w) : nullptr;
     uint32_t* keep_e = filter ? reinterpret_cast<uint32_t*>(ws + L.off_keep_e) : nullptr;
@@ -424,14 +446,13 @@ int linear_ce_run(const void* E, const void* W, int64_t T, int64_t D, int64_t V,
     const int tiles_t = (int)(L.T_pad / BM);
     // 256-row tiles on CTA pairs where the rows split evenly, else single CTAs
     const bool pairs_t = tiles_t % 2 == 0;
-    const Variant vz{pairs_t, BN};
 
     // 1. forward statistics over the whole vocabulary
     {
         tc::GemmArgs g{tiles_t, (int)L.tiles_v, nkD, nkD, 0, 0, 0, 0, status};
         EpiStats::Params ep{labels, ignore_index, T, V, reinterpret_cast<float4*>(part)};
         if (timer && !timer->begin(s)) return VCE_ERR_CUDA;
-        if (tc::launch_gemm<EpiStats, false, false>(mE, mE, mW, g, ep, vz, s) != cudaSuccess) return VCE_ERR_CUDA;
+        if (tc::launch_gemm<EpiStats, false, false>(mE, mE, mW, g, ep, pairs_t, s) != cudaSuccess) return VCE_ERR_CUDA;
         if (timer && !timer->end(s, GemmTimer::kStats)) return VCE_ERR_CUDA;
         if (launch_stats_merge(part, (int)L.tiles_v, T, V, labels, ignore_index, loss_rows, stats, status, s) !=
             cudaSuccess)
@@ -441,11 +462,9 @@ int linear_ce_run(const void* E, const void* W, int64_t T, int64_t D, int64_t V,
             return VCE_ERR_CUDA;
     }
 
-    // 2. gradients, one vocabulary chunk at a time.  Exact: compensated accumulation on 128-wide
-    // tiles (CTA pairs where the rows split evenly).  Filtered: single CTAs skipping the dropped
-    // K blocks, one fp32 accumulation per tile.
-    const int gbn = filter ? 256 : 128;
-    const int seg = filter ? 0 : kSegKb;
+    // 2. gradients, one vocabulary chunk at a time.  Exact: CTA pairs; dW as two partial products
+    // over the halves of T merged with a two-sum, dE's chunk partials merged the same way.
+    // Filtered: single CTAs skipping the dropped K blocks, dW in one product.
     const int64_t nchunks = cdiv(L.V_pad, L.Vc);
     for (int64_t ci = 0; ci < nchunks; ++ci) {
         const int64_t off = ci * L.Vc;
@@ -458,35 +477,45 @@ int linear_ce_run(const void* E, const void* W, int64_t T, int64_t D, int64_t V,
                                red == VCE_RED_NONE, ghi, glo, L.Vc, filter_eps, keep_w, L.ldw, keep_e, L.lde,
                                filter ? kept_blocks : nullptr};
             if (timer && !timer->begin(s)) return VCE_ERR_CUDA;
-            if (tc::launch_gemm<EpiGrad, false, false>(mE, mE, mW, g, ep, vz, s) != cudaSuccess) return VCE_ERR_CUDA;
+            if (tc::launch_gemm<EpiGrad, false, false>(mE, mE, mW, g, ep, pairs_t, s) != cudaSuccess) return VCE_ERR_CUDA;
             if (timer && !timer->end(s, GemmTimer::kGrad)) return VCE_ERR_CUDA;
         }
         {   // dW[off : off + width] = G^T E: A = G (MN-major), B = E (MN-major), K = 2 T_pad (hi then lo);
             // M tile = 128 vocabulary columns = one row of keep_w, K block = 64 rows of T.  width_pad
             // is a multiple of 256, so the M tiles always pair.
             const int nkT = (int)(L.T_pad / BK);
-            tc::GemmArgs g{(int)(width_pad / BM), (int)cdiv(D, gbn), 2 * nkT, nkT, 0, 0, 0, 1, status};
-            g.skip = keep_w;
-            g.skip_ld = L.ldw;
-            g.seg_kb = seg;
-            tc::EpiStore::Params ep{dW, D, width, D, off, grad_dt == VCE_BF16};
-            if (timer && !timer->begin(s)) return VCE_ERR_CUDA;
-            if (tc::launch_gemm<tc::EpiStore, true, true>(mGhi, mGlo, mE, g, ep, Variant{!filter, gbn}, s) !=
-                cudaSuccess)
-                return VCE_ERR_CUDA;
-            if (timer && !timer->end(s, GemmTimer::kDW)) return VCE_ERR_CUDA;
+            if (filter) {
+                tc::GemmArgs g{(int)(width_pad / BM), (int)cdiv(D, BN), 2 * nkT, nkT, 0, 0, 0, 1, status};
+                g.skip = keep_w;
+                g.skip_ld = L.ldw;
+                tc::EpiStore::Params ep{dW, D, width, D, off, grad_dt == VCE_BF16};
+                if (timer && !timer->begin(s)) return VCE_ERR_CUDA;
+                if (tc::launch_gemm<tc::EpiStore, true, true>(mGhi, mGlo, mE, g, ep, false, s) != cudaSuccess)
+                    return VCE_ERR_CUDA;
+                if (timer && !timer->end(s, GemmTimer::kDW)) return VCE_ERR_CUDA;
+            } else {
+                // nkT is even (T_pad is a multiple of 128): part h takes K blocks [h nkT/2, (h+1) nkT/2)
+                // of both halves of G and of E's rows
+                for (int h = 0; h < 2; ++h) {
+                    tc::GemmArgs g{(int)(width_pad / BM), (int)cdiv(D, BN), nkT, nkT / 2, 0, 0, 0, 1, status};
+                    g.ka0 = h * (nkT / 2);
+                    EpiKahan::Params ep{wsum, nullptr, width, D, h == 0, h == 1, dW, grad_dt == VCE_BF16, off};
+                    if (timer && !timer->begin(s)) return VCE_ERR_CUDA;
+                    if (tc::launch_gemm<EpiKahan, true, true>(mGhi, mGlo, mE, g, ep, true, s) != cudaSuccess)
+                        return VCE_ERR_CUDA;
+                    if (timer && !timer->end(s, GemmTimer::kDW)) return VCE_ERR_CUDA;
+                }
+            }
         }
         {   // dE += G W[off : off + width]: A = G (K-major), B = W rows (MN-major), K = 2 width (hi then lo);
             // M tile = 128 rows of T = one row of keep_e, K block = 64 vocabulary columns
             const int nkc = (int)cdiv(width, BK);
-            tc::GemmArgs g{tiles_t, (int)cdiv(D, gbn), 2 * nkc, nkc, (int)off, 0, 0, 1, status};
+            tc::GemmArgs g{tiles_t, (int)cdiv(D, BN), 2 * nkc, nkc, (int)off, 0, 0, 1, status};
             g.skip = keep_e;
             g.skip_ld = L.lde;
-            g.seg_kb = seg;
-            EpiKahan::Params ep{dsum, dcomp, T, D, ci == 0, ci == nchunks - 1, dE, grad_dt == VCE_BF16};
+            EpiKahan::Params ep{dsum, dcomp, T, D, ci == 0, ci == nchunks - 1, dE, grad_dt == VCE_BF16, 0};
             if (timer && !timer->begin(s)) return VCE_ERR_CUDA;
-            if (tc::launch_gemm<EpiKahan, false, true>(mGhi, mGlo, mW, g, ep, Variant{!filter && pairs_t, gbn}, s) !=
-                cudaSuccess)
+            if (tc::launch_gemm<EpiKahan, false, true>(mGhi, mGlo, mW, g, ep, !filter && pairs_t, s) != cudaSuccess)
                 return VCE_ERR_CUDA;
             if (timer && !timer->end(s, GemmTimer::kDE)) return VCE_ERR_CUDA;
         }

@@ -16,20 +16,18 @@
 // stops, in-flight copies are drained (bounded) and TMEM is released.
 //
 // Two launch forms (template kCta2):
-//   single CTAs      tile 128 x kBN; the CTA loads A (128 rows) and all kBN rows of B.
-//   CTA pairs        a 2-CTA cluster computes a 256 x kBN tile with tcgen05.mma.cta_group::2:
-//                    each CTA loads its own 128 rows of A and its own kBN/2 rows of B into its
+//   single CTAs      tile 128 x 256; the CTA loads A (128 rows) and all 256 rows of B.
+//   CTA pairs        a 2-CTA cluster computes a 256 x 256 tile with tcgen05.mma.cta_group::2:
+//                    each CTA loads its own 128 rows of A and its own 128 rows of B into its
 //                    own shared memory (plain TMA loads, no multicast), the even CTA issues the
 //                    MMAs, which read both CTAs' operands and write each CTA's 128 accumulator
 //                    rows into that CTA's tensor memory.  Both CTAs' copies complete on the even
 //                    CTA's stage barrier; the MMA commits arrive on both CTAs' barriers.  Per
-//                    CTA a stage holds A plus half of B, so B crosses from L2 once per pair and
-//                    more stages fit.
-// Two options: K-block skipping from a per-tile bit table (GemmArgs::skip, gradient filtering,
-// single CTAs only), and compensated accumulation (GemmArgs::seg_kb, kBN = 128): the K loop is
-// cut into segments of seg_kb blocks, each accumulated afresh in tensor memory, and the
-// epilogue adds each segment into a (sum, compensation) pair kept in the other half of tensor
-// memory with a two-sum, so the fp32 rounding of the accumulation spans one segment only.
+//                    CTA a stage holds A plus half of B, so B crosses from L2 once per pair,
+//                    shared memory reads per MMA fall by a third and seven stages fit.
+// Options: K-block skipping from a per-tile bit table (GemmArgs::skip, gradient filtering,
+// single CTAs only), and a K offset (GemmArgs::ka0) so that one product can be split along K
+// into launches whose partial sums the caller merges.
 #pragma once
 
 #include <cuda.h>
@@ -42,21 +40,19 @@
 namespace vce {
 namespace tc {
 
-constexpr int BM = 128, BK = 64;       // A rows per CTA, K per stage
-constexpr int A_BYTES = BM * BK * 2;   // 16 KB
+constexpr int BM = 128, BN = 256, BK = 64;   // A rows per CTA, tile columns, K per stage
+constexpr int A_BYTES = BM * BK * 2;          // 16 KB
 constexpr int kThreads = 256;
-constexpr int TMEM_COLS = 512;         // two accumulators (kBN = 256), or two + a pair (kBN = 128)
-constexpr int kMaxSmem = 232448;       // opt-in dynamic shared memory per block (227 KB)
+constexpr int TMEM_COLS = 2 * BN;             // two fp32 accumulators of 128 lanes x 256 columns
+constexpr int kMaxSmem = 232448;              // opt-in dynamic shared memory per block (227 KB)
 
-template <bool kCta2, int kBN>
+template <bool kCta2>
 struct Cfg {
-    static_assert(kBN == 128 || kBN == 256, "tile width");
-    static constexpr int kBRows = kCta2 ? kBN / 2 : kBN;   // rows of the B tile this CTA loads
+    static constexpr int kBRows = kCta2 ? BN / 2 : BN;   // rows of the B tile this CTA loads
     static constexpr int kBBytes = kBRows * BK * 2;
     static constexpr int kStageBytes = A_BYTES + kBBytes;
     static constexpr int kReserve = 1024 /*alignment*/ + 256 /*barriers*/;
-    static constexpr int kStagesFit = (kMaxSmem - kReserve) / kStageBytes;
-    static constexpr int kStages = kStagesFit > 9 ? 9 : kStagesFit;
+    static constexpr int kStages = (kMaxSmem - kReserve) / kStageBytes;   // 4 single, 7 paired
     static constexpr int kSmem = kStages * kStageBytes + kReserve;
 };
 
@@ -214,18 +210,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
           "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
         : "r"(taddr));
 }
-// Store 32 consecutive fp32 columns of this thread's TMEM lane.
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
-        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
-        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
-        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]),
-        "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]),
-        "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
-        : "memory");
-}
 // Wait until this thread's tcgen05.ld have landed.  r, the destination of the last load, is
 // tied to the wait, so no use of it can be scheduled before the wait.
 __device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[32]) {
@@ -238,7 +222,6 @@ __device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[32]) {
                  :
                  : "memory");
 }
-__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // Shared-memory matrix descriptor: K-major operand, rows of 64 bf16 (128 B) written by TMA
 // with the 128-byte swizzle; 8-row groups 1024 B apart (stride byte offset).  The leading
@@ -274,20 +257,13 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn = 
            ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-// a + x = t + e exactly (Knuth's two-sum).
-__device__ __forceinline__ void two_sum(float a, float x, float& t, float& e) {
-    t = a + x;
-    const float bp = t - a;
-    e = (a - (t - bp)) + (x - bp);
-}
-
 // ---- the kernel ---------------------------------------------------------------------------
 
 struct GemmArgs {
-    int tiles_m, tiles_n;   // output tiles of 128 rows x kBN columns (tiles_m even for CTA pairs)
+    int tiles_m, tiles_n;   // output tiles of 128 rows x 256 columns (tiles_m even for CTA pairs)
     int nk;                 // K blocks (of BK) per tile
     int nk_a0;              // the first nk_a0 blocks read A0, the rest A1 (K restarts at 0 for A1)
-    int b_x0;               // B's K coordinate of block kb is b_x0 + (kb mod nk_a0) * BK
+    int b_x0;               // B's K coordinate of block kb is b_x0 + (ka0 + kb mod nk_a0) * BK
     int a_y0, b_y0;         // row offsets of the A and B tiles
     int n_fastest;          // tile order: 0 = m fastest (blocks in flight share B tiles),
                             //             1 = n fastest (blocks in flight share A tiles)
@@ -301,9 +277,9 @@ struct GemmArgs {
     // Null: every K block runs.
     const uint32_t* skip;
     int skip_ld;
-    // Compensated accumulation (kBN = 128, no skip; the epilogue must take (sum, compensation)
-    // pairs): K blocks per accumulation segment; 0 = the whole K loop in one accumulator.
-    int seg_kb;
+    // K offset: block ka of a half reads K block ka0 + ka of A (and of B, after b_x0), so a
+    // product split along K runs as launches over [ka0, ka0 + nk_a0).
+    int ka0;
 };
 
 // Calls f(kb, ka) for the K blocks of M tile tm in order -- kb the block index (A0 blocks,
@@ -365,16 +341,14 @@ __device__ __forceinline__ void tile_coords(const GemmArgs& g, int tile, uint32_
 //   begin(p, row_state, row, tn)                        before a tile's columns
 //   consume(p, row_state, row, col0, acc[32])           32 accumulator columns, in order
 //   end(p, row_state, row, tn)                          after them (all lanes of the warp)
-//   kCompensated, consume2(p, row_state, row, col0, sum[32], comp[32]): the final columns of a
-//     compensated (seg_kb > 0) tile as (sum, compensation) pairs.
 // kAmn / kBmn: the operand is MN-major; its tensor map then has 64 x 64 boxes over a global
 // [K, M] (resp. [K, N]) matrix, and the tile is loaded as 2 (resp. kBRows / 64) boxes.  A
 // K-major B map has boxes of kBRows rows.
-template <class Epi, bool kAmn, bool kBmn, bool kCta2, int kBN>
+template <class Epi, bool kAmn, bool kBmn, bool kCta2>
 __global__ void __launch_bounds__(kThreads, 1)
     k_tc_gemm(const __grid_constant__ CUtensorMap mapA0, const __grid_constant__ CUtensorMap mapA1,
               const __grid_constant__ CUtensorMap mapB, const GemmArgs g, const typename Epi::Params ep) {
-    using C = Cfg<kCta2, kBN>;
+    using C = Cfg<kCta2>;
     constexpr int S = C::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -426,9 +400,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tile0 = kCta2 ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
     const int tstep = kCta2 ? (int)(gridDim.x >> 1) : (int)gridDim.x;
     const uint64_t wns = g.wait_ns ? g.wait_ns : kWaitNs;
-    // accumulation segments per tile (compensated accumulation needs the free half of TMEM)
-    const int seg_kb = (kBN == 128 && !g.skip && Epi::kCompensated) ? g.seg_kb : 0;
-    const int nseg = seg_kb > 0 ? (g.nk + seg_kb - 1) / seg_kb : 1;
 
     if (warp == 0 && lane == 0) {
         // ---------------- TMA producer
@@ -447,20 +418,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const CUtensorMap* ma = kb >= g.nk_a0 ? &mapA1 : &mapA0;
                 uint8_t* sa = smA + stage * A_BYTES;
                 uint8_t* sb = smB + stage * C::kBBytes;
+                const int k = (g.ka0 + ka) * BK;
                 if (kAmn) {
 #pragma unroll
                     for (int h = 0; h < BM / 64; ++h)
-                        tma_load<kCta2>(sa + h * (64 * BK * 2), ma, fb, g.a_y0 + tm * BM + h * 64, ka * BK);
+                        tma_load<kCta2>(sa + h * (64 * BK * 2), ma, fb, g.a_y0 + tm * BM + h * 64, k);
                 } else {
-                    tma_load<kCta2>(sa, ma, fb, ka * BK, g.a_y0 + tm * BM);
+                    tma_load<kCta2>(sa, ma, fb, k, g.a_y0 + tm * BM);
                 }
-                const int n0 = g.b_y0 + tn * kBN + (int)rank * C::kBRows;
+                const int n0 = g.b_y0 + tn * BN + (int)rank * C::kBRows;
                 if (kBmn) {
 #pragma unroll
                     for (int h = 0; h < C::kBRows / 64; ++h)
-                        tma_load<kCta2>(sb + h * (64 * BK * 2), &mapB, fb, n0 + h * 64, g.b_x0 + ka * BK);
+                        tma_load<kCta2>(sb + h * (64 * BK * 2), &mapB, fb, n0 + h * 64, g.b_x0 + k);
                 } else {
-                    tma_load<kCta2>(sb, &mapB, fb, g.b_x0 + ka * BK, n0);
+                    tma_load<kCta2>(sb, &mapB, fb, g.b_x0 + k, n0);
                 }
                 issued = issued < S ? issued + 1 : S;
                 if (++stage == S) { stage = 0; phase ^= 1u; }
@@ -487,7 +459,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1 && lane == 0 && (!kCta2 || rank == 0)) {
         // ---------------- MMA issuer
-        constexpr uint32_t idesc = idesc_bf16_f32(kCta2 ? 2 * BM : BM, kBN, kAmn, kBmn);
+        constexpr uint32_t idesc = idesc_bf16_f32(kCta2 ? 2 * BM : BM, BN, kAmn, kBmn);
         // one MMA consumes K = 16: 32 B along a K-major row, or 16 K-rows (2 KB) of an MN-major tile
         constexpr uint32_t kStepA = kAmn ? (2048 >> 4) : (32 >> 4);
         constexpr uint32_t kStepB = kBmn ? (2048 >> 4) : (32 >> 4);
@@ -504,11 +476,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int tile = tile0; tile < ntiles && !*abort_flag; tile += tstep) {
             if (!wait_bar<kCta2>(&acc_free[acc], acc_phase ^ 1u, abort_flag, g.err, kErrWaitAccFree, wns)) break;
             tc_fence_after();
-            uint32_t d = tmem_base + (uint32_t)(acc * kBN);
+            const uint32_t d = tmem_base + (uint32_t)(acc * BN);
             int tm, tn;
             tile_coords<kCta2>(g, tile, rank, tm, tn);
             bool ok = true, issued = false;
-            int kvis = 0;
             for_each_kblock(g, tm, [&](int, int) {
                 if (!wait_bar<false>(&full[stage], phase, abort_flag, g.err, kErrWaitFull, wns)) {
                     ok = false;
@@ -524,19 +495,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 issued = true;
                 commit(&empty[stage]);
                 if (++stage == S) { stage = 0; phase ^= 1u; }
-                if (seg_kb > 0 && ++kvis % seg_kb == 0 && kvis < g.nk) {
-                    // segment done: hand this accumulator to the epilogue, continue in the other
-                    commit(&acc_full[acc]);
-                    acc ^= 1;
-                    if (acc == 0) acc_phase ^= 1u;
-                    if (!wait_bar<kCta2>(&acc_free[acc], acc_phase ^ 1u, abort_flag, g.err, kErrWaitAccFree, wns)) {
-                        ok = false;
-                        return false;
-                    }
-                    tc_fence_after();
-                    d = tmem_base + (uint32_t)(acc * kBN);
-                    issued = false;
-                }
                 return true;
             });
             if (!ok) break;
@@ -567,96 +525,43 @@ __global__ void __launch_bounds__(kThreads, 1)
             acc ^= 1;
             if (acc == 0) acc_phase ^= 1u;
         };
-        bool live = true;
-        for (int tile = tile0; tile < ntiles && live; tile += tstep) {
+        for (int tile = tile0; tile < ntiles; tile += tstep) {
+            // the warp decides together: tcgen05.ld is a warp-wide instruction
+            const bool ok = wait_bar<kCta2>(&acc_full[acc], acc_phase, abort_flag, g.err, kErrWaitAccFull, wns);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            tc_fence_after();
             int tm, tn;
             tile_coords<kCta2>(g, tile, rank, tm, tn);
             const int row = tm * BM + sub * 32 + lane;
+            const uint32_t t0 = tmem_base + (uint32_t)(acc * BN) + lane_off;
             typename Epi::Row st;
-            for (int seg = 0; seg < nseg; ++seg) {
-                // the warp decides together: tcgen05.ld is a warp-wide instruction
-                const bool ok = wait_bar<kCta2>(&acc_full[acc], acc_phase, abort_flag, g.err, kErrWaitAccFull, wns);
-                if (!__all_sync(0xffffffffu, ok)) {
-                    live = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t t0 = tmem_base + (uint32_t)(acc * kBN) + lane_off;
+            // Two register buffers: the next 32 columns load from TMEM while these are consumed.
+            static_assert((BN / 32) % 2 == 0, "column pieces go in pairs");
+            uint32_t ra[32], rb[32];
+            if (!dbg::ok(tm >= 0 && tm < g.tiles_m && tn >= 0 && tn < g.tiles_n, dbg::kTile)) {
                 // warp-uniform: a tile outside the output is not written (its accumulator is released)
-                if (!dbg::ok(tm >= 0 && tm < g.tiles_m && tn >= 0 && tn < g.tiles_n, dbg::kTile)) {
-                } else if (nseg == 1) {
-                    // Two register buffers: the next 32 columns load from TMEM while these are consumed.
-                    static_assert((kBN / 32) % 2 == 0, "column pieces go in pairs");
-                    uint32_t ra[32], rb[32];
-                    if (!tile_has_blocks(g, tm)) {   // every K block skipped: no MMA wrote the accumulator
+            } else if (!tile_has_blocks(g, tm)) {   // every K block skipped: no MMA wrote the accumulator
 #pragma unroll
-                        for (int k = 0; k < 32; ++k) ra[k] = 0u;
-                        Epi::begin(ep, st, row, tn);
+                for (int k = 0; k < 32; ++k) ra[k] = 0u;
+                Epi::begin(ep, st, row, tn);
 #pragma unroll 1
-                        for (int c = 0; c < kBN / 32; ++c) Epi::consume(ep, st, row, tn * kBN + c * 32, ra);
-                    } else {
-                        tmem_ld32(t0, ra);
-                        Epi::begin(ep, st, row, tn);   // its global loads overlap the first TMEM load
+                for (int c = 0; c < BN / 32; ++c) Epi::consume(ep, st, row, tn * BN + c * 32, ra);
+                Epi::end(ep, st, row, tn);
+            } else {
+                tmem_ld32(t0, ra);
+                Epi::begin(ep, st, row, tn);   // its global loads overlap the first TMEM load
 #pragma unroll 1
-                        for (int c = 0; c < kBN / 32; c += 2) {
-                            tmem_wait_ld(ra);
-                            tmem_ld32(t0 + (uint32_t)((c + 1) * 32), rb);
-                            Epi::consume(ep, st, row, tn * kBN + c * 32, ra);
-                            tmem_wait_ld(rb);
-                            if (c + 2 < kBN / 32) tmem_ld32(t0 + (uint32_t)((c + 2) * 32), ra);
-                            Epi::consume(ep, st, row, tn * kBN + (c + 1) * 32, rb);
-                        }
-                    }
-                    Epi::end(ep, st, row, tn);
-                } else if constexpr (Epi::kCompensated && kBN == 128) {
-                    // the (sum, compensation) pair of this tile lives in columns 256..383 and 384..511
-                    const uint32_t ps = tmem_base + 256u + lane_off, pc = tmem_base + 384u + lane_off;
-                    const bool last = seg == nseg - 1;
-                    if (last) Epi::begin(ep, st, row, tn);
-#pragma unroll 1
-                    for (int c = 0; c < kBN / 32; ++c) {
-                        uint32_t x[32], s[32], e[32];
-                        tmem_ld32(t0 + (uint32_t)(c * 32), x);
-                        if (seg > 0) {
-                            tmem_ld32(ps + (uint32_t)(c * 32), s);
-                            tmem_ld32(pc + (uint32_t)(c * 32), e);
-                        }
-                        tmem_wait_ld(x);
-                        if (seg == 0) {   // the pair starts as (segment 0, 0)
-#pragma unroll
-                            for (int k = 0; k < 32; ++k) {
-                                s[k] = x[k];
-                                e[k] = 0u;
-                            }
-                        } else {
-#pragma unroll
-                            for (int k = 0; k < 32; ++k) {
-                                float t, r;
-                                two_sum(__uint_as_float(s[k]), __uint_as_float(x[k]), t, r);
-                                s[k] = __float_as_uint(t);
-                                e[k] = __float_as_uint(__uint_as_float(e[k]) + r);
-                            }
-                        }
-                        if (last) {
-                            float fs[32], fe[32];
-#pragma unroll
-                            for (int k = 0; k < 32; ++k) {
-                                fs[k] = __uint_as_float(s[k]);
-                                fe[k] = __uint_as_float(e[k]);
-                            }
-                            Epi::consume2(ep, st, row, tn * kBN + c * 32, fs, fe);
-                        } else {
-                            tmem_st32(ps + (uint32_t)(c * 32), s);
-                            tmem_st32(pc + (uint32_t)(c * 32), e);
-                        }
-                    }
-                    if (last)
-                        Epi::end(ep, st, row, tn);
-                    else
-                        tmem_wait_st();   // the pair is complete before the next segment reads it
+                for (int c = 0; c < BN / 32; c += 2) {
+                    tmem_wait_ld(ra);
+                    tmem_ld32(t0 + (uint32_t)((c + 1) * 32), rb);
+                    Epi::consume(ep, st, row, tn * BN + c * 32, ra);
+                    tmem_wait_ld(rb);
+                    if (c + 2 < BN / 32) tmem_ld32(t0 + (uint32_t)((c + 2) * 32), ra);
+                    Epi::consume(ep, st, row, tn * BN + (c + 1) * 32, rb);
                 }
-                release();
+                Epi::end(ep, st, row, tn);
             }
+            release();
         }
     }
     tc_fence_before();

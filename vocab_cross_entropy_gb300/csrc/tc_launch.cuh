@@ -1,6 +1,6 @@
 // Host side of the tensor-core GEMM (tc_gemm.cuh): TMA maps over row-major bf16 matrices, the
 // launch of one GEMM as single CTAs or as CTA pairs, and the plain store epilogue (fp32 or
-// bf16 output, with or without compensated accumulation).
+// bf16 output).
 #pragma once
 
 #include <cuda.h>
@@ -54,13 +54,6 @@ inline bool make_map(CUtensorMap* map, const Mat& m, int box_rows) {
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// How a GEMM runs: as CTA pairs (cta_group::2, tiles of 256 rows; tiles_m must be even) or as
-// single CTAs, with tiles kBN = 128 or 256 columns wide.
-struct Variant {
-    bool pair;
-    int bn;
-};
-
 // The kernel's shared-memory opt-in, set once per device (the attribute belongs to the
 // function in the current device's context), and the number of 2-CTA clusters that fit on the
 // device at once (0: none).  ready: the caller's per-kernel cache, per device 0 (unknown) or
@@ -100,21 +93,21 @@ cudaError_t prepare_kernel(K kern, int smem, bool pair, std::atomic<int> (&ready
     return cudaSuccess;
 }
 
-template <class Epi, bool kAmn, bool kBmn, bool kCta2, int kBN>
+template <class Epi, bool kAmn, bool kBmn, bool kCta2>
 cudaError_t launch_gemm_as(const Mat& a0, const Mat& a1, const Mat& b, const GemmArgs& g,
                            const typename Epi::Params& ep, cudaStream_t s) {
-    using C = Cfg<kCta2, kBN>;
+    using C = Cfg<kCta2>;
     CUtensorMap ma0, ma1, mb;
     if (!make_map(&ma0, a0, kAmn ? 64 : BM) || !make_map(&ma1, a1, kAmn ? 64 : BM) ||
         !make_map(&mb, b, kBmn ? 64 : C::kBRows))
-        return cudaErrorInvalidValue;
-    auto kern = k_tc_gemm<Epi, kAmn, kBmn, kCta2, kBN>;
+        return record_cuda(cudaErrorInvalidValue);
+    auto kern = k_tc_gemm<Epi, kAmn, kBmn, kCta2>;
     static std::atomic<int> ready[kMaxDevices];   // one cache per kernel instantiation
     int clusters = 0;
     cudaError_t e = prepare_kernel(kern, C::kSmem, kCta2, ready, &clusters);
-    if (e != cudaSuccess) return e;
+    if (e != cudaSuccess) return record_cuda(e);
     if (kCta2) {
-        if (clusters < 1 || g.tiles_m % 2) return cudaErrorInvalidConfiguration;
+        if (clusters < 1 || g.tiles_m % 2) return record_cuda(cudaErrorInvalidConfiguration);
         const int64_t tiles = (int64_t)(g.tiles_m / 2) * g.tiles_n;
         cudaLaunchConfig_t cfg = {};
         cudaLaunchAttribute attr[1];
@@ -128,35 +121,27 @@ cudaError_t launch_gemm_as(const Mat& a0, const Mat& a1, const Mat& b, const Gem
         cfg.stream = s;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        return cudaLaunchKernelEx(&cfg, kern, ma0, ma1, mb, g, ep);
+        return record_cuda(cudaLaunchKernelEx(&cfg, kern, ma0, ma1, mb, g, ep));
     }
     const int64_t tiles = (int64_t)g.tiles_m * g.tiles_n;
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(tiles, device_sm_count()));
     kern<<<grid, kThreads, C::kSmem, s>>>(ma0, ma1, mb, g, ep);
-    return cudaGetLastError();
+    return record_cuda(cudaGetLastError());
 }
 
-// One GEMM in the given variant.  Pairs need an even tiles_m and no skip bits; compensated
-// accumulation (seg_kb > 0) needs kBN = 128.
+// One GEMM, as CTA pairs (pair: tiles_m must be even and there must be no skip bits) or as
+// single CTAs.
 template <class Epi, bool kAmn, bool kBmn>
 cudaError_t launch_gemm(const Mat& a0, const Mat& a1, const Mat& b, const GemmArgs& g,
-                        const typename Epi::Params& ep, Variant v, cudaStream_t s) {
-    if (v.pair && (g.tiles_m % 2 || g.skip)) return cudaErrorInvalidConfiguration;
-    if (g.seg_kb > 0 && v.bn != 128) return cudaErrorInvalidConfiguration;
-    if (v.bn == 128)
-        return v.pair ? launch_gemm_as<Epi, kAmn, kBmn, true, 128>(a0, a1, b, g, ep, s)
-                      : launch_gemm_as<Epi, kAmn, kBmn, false, 128>(a0, a1, b, g, ep, s);
-    if (v.bn == 256)
-        return v.pair ? launch_gemm_as<Epi, kAmn, kBmn, true, 256>(a0, a1, b, g, ep, s)
-                      : launch_gemm_as<Epi, kAmn, kBmn, false, 256>(a0, a1, b, g, ep, s);
-    return cudaErrorInvalidValue;
+                        const typename Epi::Params& ep, bool pair, cudaStream_t s) {
+    if (pair && (g.tiles_m % 2 || g.skip)) return record_cuda(cudaErrorInvalidConfiguration);
+    return pair ? launch_gemm_as<Epi, kAmn, kBmn, true>(a0, a1, b, g, ep, s)
+                : launch_gemm_as<Epi, kAmn, kBmn, false>(a0, a1, b, g, ep, s);
 }
 
 // Output tile rows into [rows, cols] at row offset row_off with row pitch ld (bf16 rounded to
-// nearest even from fp32, or fp32), evict-first: nothing in a call reads them back.  With
-// compensated accumulation the stored value is sum + compensation.
+// nearest even from fp32, or fp32), evict-first: nothing in a call reads them back.
 struct EpiStore {
-    static constexpr bool kCompensated = true;
     struct Params {
         void* out;
         int64_t ld, rows, cols, row_off;
@@ -164,7 +149,7 @@ struct EpiStore {
     };
     struct Row {};
     __device__ __forceinline__ static void begin(const Params&, Row&, int, int) {}
-    __device__ __forceinline__ static void store(const Params& p, int row, int col0, const float (&v)[32]) {
+    __device__ __forceinline__ static void consume(const Params& p, Row&, int row, int col0, const uint32_t (&acc)[32]) {
         if (row >= p.rows || col0 >= p.cols) return;
         const int64_t base = (p.row_off + row) * p.ld + col0;
         const int n = (p.cols - col0) < 32 ? (int)(p.cols - col0) : 32;
@@ -173,14 +158,14 @@ struct EpiStore {
             if (n == 32) {
                 uint32_t w[16];
 #pragma unroll
-                for (int k = 0; k < 16; ++k) w[k] = pack_bf16x2(v[2 * k], v[2 * k + 1]);
+                for (int k = 0; k < 16; ++k) w[k] = pack_bf16x2(__uint_as_float(acc[2 * k]), __uint_as_float(acc[2 * k + 1]));
                 uint4* d = reinterpret_cast<uint4*>(o);
 #pragma unroll
                 for (int q = 0; q < 4; ++q) st_stream16(d + q, make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]));
             } else {
 #pragma unroll
                 for (int k = 0; k < 32; ++k)
-                    if (k < n) o[k] = to_bf16(v[k]);
+                    if (k < n) o[k] = to_bf16(__uint_as_float(acc[k]));
             }
         } else {
             float* o = reinterpret_cast<float*>(p.out) + base;
@@ -188,27 +173,13 @@ struct EpiStore {
                 uint4* d = reinterpret_cast<uint4*>(o);
 #pragma unroll
                 for (int q = 0; q < 8; ++q)
-                    st_stream16(d + q, make_uint4(__float_as_uint(v[4 * q]), __float_as_uint(v[4 * q + 1]),
-                                                  __float_as_uint(v[4 * q + 2]), __float_as_uint(v[4 * q + 3])));
+                    st_stream16(d + q, make_uint4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]));
             } else {
 #pragma unroll
                 for (int k = 0; k < 32; ++k)
-                    if (k < n) o[k] = v[k];
+                    if (k < n) o[k] = __uint_as_float(acc[k]);
             }
         }
-    }
-    __device__ __forceinline__ static void consume(const Params& p, Row&, int row, int col0, const uint32_t (&acc)[32]) {
-        float v[32];
-#pragma unroll
-        for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(acc[k]);
-        store(p, row, col0, v);
-    }
-    __device__ __forceinline__ static void consume2(const Params& p, Row&, int row, int col0, const float (&s)[32],
-                                                    const float (&c)[32]) {
-        float v[32];
-#pragma unroll
-        for (int k = 0; k < 32; ++k) v[k] = s[k] + c[k];
-        store(p, row, col0, v);
     }
     __device__ __forceinline__ static void end(const Params&, Row&, int, int) {}
 };

@@ -12,6 +12,7 @@ namespace vce {
 
 namespace {
 std::atomic<int> g_sms[kMaxDevices];
+thread_local int g_last_cuda = 0;   // the last failed CUDA result an entry point saw on this thread
 std::atomic<int> g_arch[kMaxDevices];   // 0 unknown, 1 ok, -1 not sm_100-family
 
 int current_device() {
@@ -20,6 +21,11 @@ int current_device() {
     return d;
 }
 }  // namespace
+
+cudaError_t record_cuda(cudaError_t e) {
+    if (e != cudaSuccess) g_last_cuda = (int)e;
+    return e;
+}
 
 int device_sm_count() {
     const int d = current_device();
@@ -109,3 +115,12 @@ extern "C" int vce_debug_status(int32_t* host_out) {
     }
     return VCE_OK;
 }
+
+extern "C" int vce_last_cuda_error(void) {
+    int e = vce::g_last_cuda;
+    vce::g_last_cuda = 0;
+    const cudaError_t rt = cudaGetLastError();   // also clears the runtime's own record
+    return e ? e : (int)rt;
+}
+
+extern "C" const char* vce_cuda_error_name(int code) { return cudaGetErrorName((cudaError_t)code); }

@@ -23,6 +23,9 @@ inline bool fits_bytes(int64_t rows, int64_t ld, size_t esize) {
 constexpr int kMaxDevices = 64;
 
 int device_sm_count();     // SMs of the current device (cached per device)
+
+// Remembers a failed CUDA runtime result for vce_last_cuda_error (per host thread); returns e.
+cudaError_t record_cuda(cudaError_t e);
 int require_sm100();       // VCE_OK when the current device is an sm_100-family GPU
 
 // Per-row merge of k partial (max, sum-exp, target, owner) statistics laid out [k][T] as
