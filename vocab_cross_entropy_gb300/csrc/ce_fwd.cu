@@ -40,10 +40,9 @@ namespace {
 // Three blocks of 512 threads per SM (registers capped at 42): the row stream is issue- and
 // latency-bound, and 48 resident warps per SM measured 10% faster than 32 at T=16384, V=128256 bf16.
 // kSmooth: label smoothing eps > 0 (the row's sum of all logits is reduced alongside; two
-// blocks per SM, since the extra sum does not fit in 42 registers).  kU: 16-byte loads in
-// flight per thread; 8 (two blocks per SM) covers a 64 KB row in one round of loads.
-template <typename S, int NT, bool kSmooth, int kU = kUnroll>
-__global__ void __launch_bounds__(NT, (kSmooth || kU > kUnroll ? 1024 : 1536) / NT)
+// blocks per SM, since the extra sum does not fit in 42 registers).
+template <typename S, int NT, bool kSmooth>
+__global__ void __launch_bounds__(NT, (kSmooth ? 1024 : 1536) / NT)
     k_ce_fwd(const S* __restrict__ logits, int64_t T, int64_t V, int64_t ld,
                                                const int64_t* __restrict__ labels, int64_t ignore_index,
                                                float eps, float* __restrict__ loss_rows,
@@ -63,8 +62,7 @@ __global__ void __launch_bounds__(NT, (kSmooth || kU > kUnroll ? 1024 : 1536) / 
         }
         if (!dbg::ok(row >= 0 && row < T && V <= ld, dbg::kRow)) continue;   // block-uniform
         float m = -kInf, s = 0.f, mb = 0.f, sz = 0.f;
-        fwd_segment<S, NT, true, kLoadStream, kSmooth, kU>(logits + row * ld, V, t, m, s, mb, &sm_zt, threadIdx.x,
-                                                            &sz);
+        fwd_segment<S, NT, true, kLoadStream, kSmooth>(logits + row * ld, V, t, m, s, mb, &sm_zt, threadIdx.x, &sz);
         if (kSmooth) {   // block sum of the logits (the barrier below publishes the warp sums)
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) sz += __shfl_xor_sync(0xFFFFFFFFu, sz, off);
@@ -295,11 +293,10 @@ __global__ void k_ce_merge(const float4* __restrict__ chunk_stats, int k, int64_
 // ------------------------------------------------------------------------------------------
 // host side
 
-template <typename S, int NT, int kU = kUnroll>
+template <typename S, int NT>
 cudaError_t launch_fwd(const void* logits, int64_t T, int64_t V, int64_t ld, const int64_t* labels, int64_t ig,
                        float eps, float* loss_rows, float* row_stats, int32_t* status, cudaStream_t s) {
-    // label smoothing keeps four loads in flight: its row sum needs the registers
-    auto kern = eps > 0.f ? k_ce_fwd<S, NT, true, kUnroll> : k_ce_fwd<S, NT, false, kU>;
+    auto kern = eps > 0.f ? k_ce_fwd<S, NT, true> : k_ce_fwd<S, NT, false>;
     kern<<<grid_for(kern, NT, T), NT, 0, s>>>(reinterpret_cast<const S*>(logits), T, V, ld, labels, ig, eps,
                                               loss_rows, reinterpret_cast<float4*>(row_stats), status);
     return cudaGetLastError();
@@ -329,7 +326,6 @@ cudaError_t launch_chunk_fwd(const SegTable& tab, const int64_t* labels, int64_t
 template <typename S>
 cudaError_t dispatch_fwd(int nt, const void* logits, int64_t T, int64_t V, int64_t ld, const int64_t* labels,
                          int64_t ig, float eps, float* lr, float* rs, int32_t* st, cudaStream_t s) {
-    if (nt == -512) return launch_fwd<S, 512, 8>(logits, T, V, ld, labels, ig, eps, lr, rs, st, s);
     if (nt == 128) return launch_fwd<S, 128>(logits, T, V, ld, labels, ig, eps, lr, rs, st, s);
     if (nt == 256) return launch_fwd<S, 256>(logits, T, V, ld, labels, ig, eps, lr, rs, st, s);
     return launch_fwd<S, 512>(logits, T, V, ld, labels, ig, eps, lr, rs, st, s);
@@ -394,25 +390,23 @@ extern "C" int ce_forward_ls(const void* logits, vce_dtype dt, int64_t T, int64_
     if (cudaMemsetAsync(status, 0, sizeof(int32_t), s) != cudaSuccess) return VCE_ERR_CUDA;
     if (T > 0) {
         // Rows of at most 32 KB: one warp per row (k_ce_fwd_warp; 8192 x 16000 bf16: 0.0695
-        // against 0.0815 ms on the ring).  Rows of 32-64 KB with fewer than 64 per SM: one block
-        // per row with the whole row's loads in flight at once (the ring's ramp and tail weigh
-        // more than its streaming gains there; a warp per row streams them latency-bound).
-        // Longer rows stream through shared memory where the layout allows it, else one block
-        // per row with loads from global memory.
+        // against 0.0815 ms on the ring).  Rows of 32-64 KB with fewer than 64 per SM: one
+        // 256-thread block per row, six per SM (4096 x 32000 bf16: 0.0613 ms; the ring 0.0713, a
+        // warp per row 0.0798, 512-thread blocks with a row's eight loads per thread in flight at
+        // once 0.0797).  Longer rows stream through shared memory where the layout allows it,
+        // else one block per row with loads from global memory.
         bool launched = false;
         const int64_t row_bytes = V * (int64_t)es;
         const bool few_short_rows = row_bytes > 32768 && row_bytes <= 65536 && T < 64 * (int64_t)device_sm_count();
         cudaError_t e = cudaSuccess;
-        int nt = pick_threads(row_bytes);
+        const int nt = pick_threads(row_bytes);
         if (row_bytes <= 32768) {
             e = dt == VCE_BF16 ? launch_fwd_warp<uint16_t>(logits, T, V, ld, labels, ignore_index, label_smoothing,
                                                            loss_rows, row_stats, status, s)
                                : launch_fwd_warp<float>(logits, T, V, ld, labels, ignore_index, label_smoothing,
                                                         loss_rows, row_stats, status, s);
             launched = true;
-        } else if (few_short_rows) {
-            nt = -512;   // 512 threads, eight loads in flight each
-        } else {
+        } else if (!few_short_rows) {
             e = launch_fwd_ring(dt, logits, T, V, ld, labels, ignore_index, label_smoothing, loss_rows, row_stats,
                                 status, s, &launched);
         }
