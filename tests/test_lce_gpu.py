@@ -12,7 +12,8 @@ the tensor-core path can carry, beta * sum_k |t_k| plus half a bf16 ulp of its o
                  two launches over the halves of T (steps = 2 (T / 2) / 16, G's hi and lo
                  halves both), dE one launch per 32768-column vocabulary chunk (steps =
                  2 chunk / 16); the filtered call's dW is one launch over all of T.
-  G split        G enters as G_hi + G_lo, the lo half rounded to bf16: 2^-18 per term.
+  G split        G enters as G_hi + G_lo, each a rounding to 8 significant bits (bf16, unit
+                 roundoff 2^-8): |g - G_hi - G_lo| <= 2^-16 |g| per term.
   G evaluation   each G entry is an fp32 product of c, sigma(x) and a hardware exp2: 2^-20.
 
 Each grading prints how many entries needed the clause, their condition numbers, and the
@@ -31,7 +32,7 @@ from tests.test_ce_gpu import vce  # noqa: F401  (fixture)
 pytestmark = pytest.mark.gpu
 
 ACC_ULP = 2.0 ** -23       # one fp32 ulp per accumulation step
-G_SPLIT = 2.0 ** -18       # the bf16 rounding of G's lo half
+G_SPLIT = 2.0 ** -16       # G = G_hi + G_lo: two roundings to bf16 (2^-8 each, compounded)
 G_EVAL = 2.0 ** -20        # fp32 evaluation of a G entry
 CHUNK = 32768              # vocabulary columns per gradient chunk
 Z_SLACK_REL = 2.0 ** -14   # fp32 tensor-core logits: 2 x (D / 16) x 2^-23 at D = 4096

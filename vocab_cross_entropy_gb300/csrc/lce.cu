@@ -495,13 +495,14 @@ int linear_ce_run(const void* E, const void* W, int64_t T, int64_t D, int64_t V,
                 if (timer && !timer->end(s, GemmTimer::kDW)) return VCE_ERR_CUDA;
             } else {
                 // nkT is even (T_pad is a multiple of 128): part h takes K blocks [h nkT/2, (h+1) nkT/2)
-                // of both halves of G and of E's rows
+                // of E's rows and of both halves of G, G_hi's and G_lo's tiles of a block in one
+                // stage beside E's
                 for (int h = 0; h < 2; ++h) {
-                    tc::GemmArgs g{(int)(width_pad / BM), (int)cdiv(D, BN), nkT, nkT / 2, 0, 0, 0, 1, status};
+                    tc::GemmArgs g{(int)(width_pad / BM), (int)cdiv(D, BN), nkT / 2, nkT / 2, 0, 0, 0, 1, status};
                     g.ka0 = h * (nkT / 2);
                     EpiKahan::Params ep{wsum, nullptr, width, D, h == 0, h == 1, dW, grad_dt == VCE_BF16, off};
                     if (timer && !timer->begin(s)) return VCE_ERR_CUDA;
-                    if (tc::launch_gemm<EpiKahan, true, true>(mGhi, mGlo, mE, g, ep, true, s) != cudaSuccess)
+                    if (tc::launch_gemm<EpiKahan, true, true, true>(mGhi, mGlo, mE, g, ep, true, s) != cudaSuccess)
                         return VCE_ERR_CUDA;
                     if (timer && !timer->end(s, GemmTimer::kDW)) return VCE_ERR_CUDA;
                 }
@@ -510,13 +511,19 @@ int linear_ce_run(const void* E, const void* W, int64_t T, int64_t D, int64_t V,
         {   // dE += G W[off : off + width]: A = G (K-major), B = W rows (MN-major), K = 2 width (hi then lo);
             // M tile = 128 rows of T = one row of keep_e, K block = 64 vocabulary columns
             const int nkc = (int)cdiv(width, BK);
-            tc::GemmArgs g{tiles_t, (int)cdiv(D, BN), 2 * nkc, nkc, (int)off, 0, 0, 1, status};
-            g.skip = keep_e;
-            g.skip_ld = L.lde;
             EpiKahan::Params ep{dsum, dcomp, T, D, ci == 0, ci == nchunks - 1, dE, grad_dt == VCE_BF16, 0};
             if (timer && !timer->begin(s)) return VCE_ERR_CUDA;
-            if (tc::launch_gemm<EpiKahan, false, true>(mGhi, mGlo, mW, g, ep, !filter && pairs_t, s) != cudaSuccess)
-                return VCE_ERR_CUDA;
+            if (filter) {
+                tc::GemmArgs g{tiles_t, (int)cdiv(D, BN), 2 * nkc, nkc, (int)off, 0, 0, 1, status};
+                g.skip = keep_e;
+                g.skip_ld = L.lde;
+                if (tc::launch_gemm<EpiKahan, false, true>(mGhi, mGlo, mW, g, ep, false, s) != cudaSuccess)
+                    return VCE_ERR_CUDA;
+            } else {   // G_hi's and G_lo's tiles of a K block in one stage beside W's
+                tc::GemmArgs g{tiles_t, (int)cdiv(D, BN), nkc, nkc, (int)off, 0, 0, 1, status};
+                if (tc::launch_gemm<EpiKahan, false, true, true>(mGhi, mGlo, mW, g, ep, pairs_t, s) != cudaSuccess)
+                    return VCE_ERR_CUDA;
+            }
             if (timer && !timer->end(s, GemmTimer::kDE)) return VCE_ERR_CUDA;
         }
     }

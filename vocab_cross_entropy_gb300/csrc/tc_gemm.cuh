@@ -26,8 +26,10 @@
 //                    CTA a stage holds A plus half of B, so B crosses from L2 once per pair,
 //                    shared memory reads per MMA fall by a third and seven stages fit.
 // Options: K-block skipping from a per-tile bit table (GemmArgs::skip, gradient filtering,
-// single CTAs only), and a K offset (GemmArgs::ka0) so that one product can be split along K
-// into launches whose partial sums the caller merges.
+// single CTAs only); a K offset (GemmArgs::ka0) so that one product can be split along K into
+// launches whose partial sums the caller merges; and dual A operands (template kDualA):
+// acc = (A0 + A1) B^T with A0's and A1's tiles of one K block held in the same stage beside a
+// single B tile, so B is loaded once for both (the linear-CE's G_hi and G_lo).
 #pragma once
 
 #include <cuda.h>
@@ -46,13 +48,15 @@ constexpr int kThreads = 256;
 constexpr int TMEM_COLS = 2 * BN;             // two fp32 accumulators of 128 lanes x 256 columns
 constexpr int kMaxSmem = 232448;              // opt-in dynamic shared memory per block (227 KB)
 
-template <bool kCta2>
+template <bool kCta2, bool kDualA = false>
 struct Cfg {
     static constexpr int kBRows = kCta2 ? BN / 2 : BN;   // rows of the B tile this CTA loads
     static constexpr int kBBytes = kBRows * BK * 2;
-    static constexpr int kStageBytes = A_BYTES + kBBytes;
+    static constexpr int kABytes = (kDualA ? 2 : 1) * A_BYTES;
+    static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr int kReserve = 1024 /*alignment*/ + 256 /*barriers*/;
-    static constexpr int kStages = (kMaxSmem - kReserve) / kStageBytes;   // 4 single, 7 paired
+    // single: 4 stages (3 with dual A); pair: 7 stages (4 with dual A)
+    static constexpr int kStages = (kMaxSmem - kReserve) / kStageBytes;
     static constexpr int kSmem = kStages * kStageBytes + kReserve;
 };
 
@@ -262,7 +266,8 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn = 
 struct GemmArgs {
     int tiles_m, tiles_n;   // output tiles of 128 rows x 256 columns (tiles_m even for CTA pairs)
     int nk;                 // K blocks (of BK) per tile
-    int nk_a0;              // the first nk_a0 blocks read A0, the rest A1 (K restarts at 0 for A1)
+    int nk_a0;              // the first nk_a0 blocks read A0, the rest A1 (K restarts at 0 for A1);
+                            // with dual A operands each of the nk_a0 blocks reads both
     int b_x0;               // B's K coordinate of block kb is b_x0 + (ka0 + kb mod nk_a0) * BK
     int a_y0, b_y0;         // row offsets of the A and B tiles
     int n_fastest;          // tile order: 0 = m fastest (blocks in flight share B tiles),
@@ -344,16 +349,16 @@ __device__ __forceinline__ void tile_coords(const GemmArgs& g, int tile, uint32_
 // kAmn / kBmn: the operand is MN-major; its tensor map then has 64 x 64 boxes over a global
 // [K, M] (resp. [K, N]) matrix, and the tile is loaded as 2 (resp. kBRows / 64) boxes.  A
 // K-major B map has boxes of kBRows rows.
-template <class Epi, bool kAmn, bool kBmn, bool kCta2>
+template <class Epi, bool kAmn, bool kBmn, bool kCta2, bool kDualA = false>
 __global__ void __launch_bounds__(kThreads, 1)
     k_tc_gemm(const __grid_constant__ CUtensorMap mapA0, const __grid_constant__ CUtensorMap mapA1,
               const __grid_constant__ CUtensorMap mapB, const GemmArgs g, const typename Epi::Params ep) {
-    using C = Cfg<kCta2>;
+    using C = Cfg<kCta2, kDualA>;
     constexpr int S = C::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* smA = smem;
-    uint8_t* smB = smem + S * A_BYTES;
+    uint8_t* smA = smem;   // per stage: A0 (and A1) tiles
+    uint8_t* smB = smem + S * C::kABytes;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * C::kStageBytes);
     uint64_t* empty = full + S;
     uint64_t* acc_full = empty + S;
@@ -409,22 +414,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int tile = tile0; tile < ntiles && !*abort_flag; tile += tstep) {
             int tm, tn;
             tile_coords<kCta2>(g, tile, rank, tm, tn);
-            for_each_kblock(g, tm, [&](int kb, int ka) {
+            auto each = [&](auto&& f) {   // the stages of this tile: K blocks, or (A0, A1) block pairs
+                if (kDualA) {
+                    for (int ka = 0; ka < g.nk_a0; ++ka)
+                        if (!f(0, ka)) return;
+                } else {
+                    for_each_kblock(g, tm, f);
+                }
+            };
+            each([&](int kb, int ka) {
                 if (!wait_bar<kCta2>(&empty[stage], phase ^ 1u, abort_flag, g.err, kErrWaitEmpty, wns)) return false;
                 // the barrier that counts this stage's bytes: the even CTA's for a pair
                 const uint32_t fb = kCta2 ? cluster_addr(&full[stage], 0) : smem_u32(&full[stage]);
                 if (!kCta2 || rank == 0)
                     mbar_arrive_expect_tx(&full[stage], (kCta2 ? 2 : 1) * C::kStageBytes + g.tx_extra);
-                const CUtensorMap* ma = kb >= g.nk_a0 ? &mapA1 : &mapA0;
-                uint8_t* sa = smA + stage * A_BYTES;
+                uint8_t* sa = smA + stage * C::kABytes;
                 uint8_t* sb = smB + stage * C::kBBytes;
                 const int k = (g.ka0 + ka) * BK;
-                if (kAmn) {
+                auto load_a = [&](const CUtensorMap* ma, uint8_t* dst) {
+                    if (kAmn) {
 #pragma unroll
-                    for (int h = 0; h < BM / 64; ++h)
-                        tma_load<kCta2>(sa + h * (64 * BK * 2), ma, fb, g.a_y0 + tm * BM + h * 64, k);
+                        for (int h = 0; h < BM / 64; ++h)
+                            tma_load<kCta2>(dst + h * (64 * BK * 2), ma, fb, g.a_y0 + tm * BM + h * 64, k);
+                    } else {
+                        tma_load<kCta2>(dst, ma, fb, k, g.a_y0 + tm * BM);
+                    }
+                };
+                if (kDualA) {
+                    load_a(&mapA0, sa);
+                    load_a(&mapA1, sa + A_BYTES);
                 } else {
-                    tma_load<kCta2>(sa, ma, fb, k, g.a_y0 + tm * BM);
+                    load_a(kb >= g.nk_a0 ? &mapA1 : &mapA0, sa);
                 }
                 const int n0 = g.b_y0 + tn * BN + (int)rank * C::kBRows;
                 if (kBmn) {
@@ -480,23 +500,35 @@ __global__ void __launch_bounds__(kThreads, 1)
             int tm, tn;
             tile_coords<kCta2>(g, tile, rank, tm, tn);
             bool ok = true, issued = false;
-            for_each_kblock(g, tm, [&](int, int) {
+            auto stage_mmas = [&](int, int) {
                 if (!wait_bar<false>(&full[stage], phase, abort_flag, g.err, kErrWaitFull, wns)) {
                     ok = false;
                     return false;
                 }
                 tc_fence_after();
-                const uint64_t ad = kAmn ? desc_mnmajor_sw128(a0 + stage * A_BYTES) : desc_kmajor_sw128(a0 + stage * A_BYTES);
+                const uint32_t sa = a0 + stage * C::kABytes;
                 const uint64_t bd =
                     kBmn ? desc_mnmajor_sw128(b0 + stage * C::kBBytes) : desc_kmajor_sw128(b0 + stage * C::kBBytes);
 #pragma unroll
-                for (int k = 0; k < BK / 16; ++k)   // advance the start address by one K = 16 step
-                    mma_bf16<kCta2>(d, ad + kStepA * k, bd + kStepB * k, idesc, (issued || k != 0) ? 1u : 0u);
+                for (int h = 0; h < (kDualA ? 2 : 1); ++h) {   // A0, then A1 against the same B tile
+                    const uint32_t at = sa + h * A_BYTES;
+                    const uint64_t ad = kAmn ? desc_mnmajor_sw128(at) : desc_kmajor_sw128(at);
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k)   // advance the start address by one K = 16 step
+                        mma_bf16<kCta2>(d, ad + kStepA * k, bd + kStepB * k, idesc,
+                                        (issued || h != 0 || k != 0) ? 1u : 0u);
+                }
                 issued = true;
                 commit(&empty[stage]);
                 if (++stage == S) { stage = 0; phase ^= 1u; }
                 return true;
-            });
+            };
+            if (kDualA) {
+                for (int ka = 0; ka < g.nk_a0; ++ka)
+                    if (!stage_mmas(0, ka)) break;
+            } else {
+                for_each_kblock(g, tm, stage_mmas);
+            }
             if (!ok) break;
             commit(&acc_full[acc]);
             acc ^= 1;

@@ -93,15 +93,15 @@ cudaError_t prepare_kernel(K kern, int smem, bool pair, std::atomic<int> (&ready
     return cudaSuccess;
 }
 
-template <class Epi, bool kAmn, bool kBmn, bool kCta2>
+template <class Epi, bool kAmn, bool kBmn, bool kCta2, bool kDualA>
 cudaError_t launch_gemm_as(const Mat& a0, const Mat& a1, const Mat& b, const GemmArgs& g,
                            const typename Epi::Params& ep, cudaStream_t s) {
-    using C = Cfg<kCta2>;
+    using C = Cfg<kCta2, kDualA>;
     CUtensorMap ma0, ma1, mb;
     if (!make_map(&ma0, a0, kAmn ? 64 : BM) || !make_map(&ma1, a1, kAmn ? 64 : BM) ||
         !make_map(&mb, b, kBmn ? 64 : C::kBRows))
         return record_cuda(cudaErrorInvalidValue);
-    auto kern = k_tc_gemm<Epi, kAmn, kBmn, kCta2>;
+    auto kern = k_tc_gemm<Epi, kAmn, kBmn, kCta2, kDualA>;
     static std::atomic<int> ready[kMaxDevices];   // one cache per kernel instantiation
     int clusters = 0;
     cudaError_t e = prepare_kernel(kern, C::kSmem, kCta2, ready, &clusters);
@@ -130,13 +130,15 @@ cudaError_t launch_gemm_as(const Mat& a0, const Mat& a1, const Mat& b, const Gem
 }
 
 // One GEMM, as CTA pairs (pair: tiles_m must be even and there must be no skip bits) or as
-// single CTAs.
-template <class Epi, bool kAmn, bool kBmn>
+// single CTAs.  kDualA: acc = (A0 + A1) B^T over nk_a0 K blocks, both A tiles of a block in one
+// stage (no skip bits).
+template <class Epi, bool kAmn, bool kBmn, bool kDualA = false>
 cudaError_t launch_gemm(const Mat& a0, const Mat& a1, const Mat& b, const GemmArgs& g,
                         const typename Epi::Params& ep, bool pair, cudaStream_t s) {
     if (pair && (g.tiles_m % 2 || g.skip)) return record_cuda(cudaErrorInvalidConfiguration);
-    return pair ? launch_gemm_as<Epi, kAmn, kBmn, true>(a0, a1, b, g, ep, s)
-                : launch_gemm_as<Epi, kAmn, kBmn, false>(a0, a1, b, g, ep, s);
+    if (kDualA && g.skip) return record_cuda(cudaErrorInvalidConfiguration);
+    return pair ? launch_gemm_as<Epi, kAmn, kBmn, true, kDualA>(a0, a1, b, g, ep, s)
+                : launch_gemm_as<Epi, kAmn, kBmn, false, kDualA>(a0, a1, b, g, ep, s);
 }
 
 // Output tile rows into [rows, cols] at row offset row_off with row pitch ld (bf16 rounded to
