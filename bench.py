@@ -612,8 +612,8 @@ def linear_problem(args, rank, peaked):
 LINEAR_GEMMS = {
     "statistics": "k_tc_gemm<EpiStats> (z = E W^T, per-tile row statistics)",
     "gradient_tiles": "k_tc_gemm<EpiGrad> (z recomputed, G = c (p - onehot) as bf16 hi + lo)",
-    "dW": "k_tc_gemm<EpiStore> (dW = G^T E, compensated)",
-    "dE": "k_tc_gemm<EpiKahan> (dE += G W, compensated, two-sum across chunks)",
+    "dW": "k_tc_gemm<EpiKahan> (dW = G^T E over the halves of T, two-sum merge; G_hi and G_lo tiles beside one E tile)",
+    "dE": "k_tc_gemm<EpiKahan> (dE += G W, two-sum across chunks; G_hi and G_lo tiles beside one W tile)",
 }
 
 
