@@ -353,14 +353,19 @@ def test_non_target_spikes_take_the_rescale_path(vce, dtype):
     grade_grad(grad, ref["grad"])
 
 
-# ---- ce_forward's shared-memory stage ring (rows of whole 16-byte vectors) ------------------
+# ---- ce_forward's row kernels: one warp per row (rows of at most 32 KB), the shared-memory --
+# ---- stage ring (longer rows of whole 16-byte vectors; rows of two stages in two consumer groups)
 
 @pytest.mark.parametrize("T,V,dtype,reduction", [
-    (40, 8, "bf16", "mean"),          # one partial stage per row, many rows per CTA
-    (300, 4096, "f32", "none"),       # one whole stage per row
-    (200, 70000, "bf16", "sum"),      # 4.3 stages per row: partial last stage
-    (24, 128256, "f32", "mean"),      # 15.7 stages per row: the ring wraps within a row
-    (700, 16384, "bf16", "mean"),     # exactly one whole stage; 4-5 rows per CTA
+    (40, 8, "bf16", "mean"),          # warp per row, 16-byte rows
+    (300, 4096, "f32", "none"),       # warp per row, 16 KB rows
+    (200, 70000, "bf16", "sum"),      # ring: 4.3 stages per row, partial last stage
+    (24, 128256, "f32", "mean"),      # ring: 15.7 stages per row, the ring wraps within a row
+    (700, 16384, "bf16", "mean"),     # warp per row, exactly 32 KB
+    (4000, 2000, "bf16", "mean"),     # warp per row, 26-27 rows per warp's stride
+    (2000, 12000, "f32", "none"),     # ring, two groups: 1.46 stages per row, 13-14 rows per CTA
+    (1300, 32768, "bf16", "sum"),     # ring, two groups: two whole stages, 8-9 rows per CTA
+    (1300, 16392, "bf16", "mean"),    # ring, two groups: one whole stage and 16 bytes
 ])
 def test_forward_ring_shapes(vce, T, V, dtype, reduction):
     p = gen.custom(T, V, dtype, seed=T + V, std=2.0, n_margin=max(1, T // 10), margin=(17.0, 50.0),

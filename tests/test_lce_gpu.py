@@ -176,14 +176,17 @@ def test_raised_targets_do_not_collapse(vce):
     full_check(vce, p, "sum")
 
 
-def test_invalid_label(vce):
-    p = gen.linear_custom(64, 64, 100, seed=2)
+@pytest.mark.parametrize("V", [100, 9000])   # one statistics tile per row; 36 (merged in ranges)
+def test_invalid_label(vce, V):
+    p = gen.linear_custom(64, 64, V, seed=2)
     p.labels = p.labels.copy()
-    p.labels[5] = 100
+    p.labels[5] = V
+    p.labels[7] = -100
     E, W = dev_bf16(p.E()), dev_bf16(p.W())
     out = vce.linear_ce_fwd_bwd(E, W, torch.from_numpy(p.labels).cuda())
     assert vce.vce_get_status(out[4]) == 1
     assert np.isnan(out[1][5].item())
+    assert out[1][7].item() == 0.0
 
 
 def test_full_size_sampled(vce):

@@ -59,6 +59,23 @@ def test_smoothing_parity(vce, eps, dtype, reduction, V):
         assert torch.equal(rows, r2) and torch.equal(stats, s2) and torch.equal(grad, g2)
 
 
+@pytest.mark.parametrize("T,V,dtype", [(2000, 3008, "bf16"), (1300, 24576, "bf16"), (600, 10000, "f32")])
+def test_smoothing_forward_ring_groups(vce, T, V, dtype):
+    """Many rows per CTA with the row sums of label smoothing: one warp per row (6 KB rows), the
+    forward ring's two consumer groups (48 KB and 40 KB rows)."""
+    eps = 0.1
+    p = gen.custom(T, V, dtype, seed=T + 7, std=2.0, n_margin=T // 10, margin=(17.0, 50.0), n_ignore=T // 20)
+    storage = p.full()
+    logits = to_device(storage, dtype)
+    labels = torch.from_numpy(p.labels).cuda()
+    out, rows, stats, status = vce.ce_forward_ls(logits, labels, eps, reduction="mean")
+    torch.cuda.synchronize()
+    assert vce.vce_get_status(status) == 0
+    ref = O.ce_smoothed(O.widen(storage, dtype), p.labels, eps, "mean", 1.0)
+    G.check_loss_rows(rows.cpu().numpy(), ref["loss_rows"], ref["valid"])
+    G.check_reduced(out.item(), ref["loss_out"])
+
+
 def test_smoothing_rejects_bad_eps(vce):
     x = torch.zeros(2, 4, device="cuda")
     lab = torch.zeros(2, dtype=torch.int64, device="cuda")

@@ -16,7 +16,7 @@
 // each row, scalar accesses on an unaligned head and tail):
 //   k_ce_fwd        one row per block iteration: (max, sum-exp) over j != t, z_t,
 //                   then loss and row statistics
-//   k_ce_reduce     one block: fixed-order fp64 sum of the losses, N, and 1/N weights
+//   k_ce_reduce     one block: fixed-order compensated fp32 sum of the losses, N, and 1/N weights
 //   k_ce_bwd        (ce_bwd.cu) one (chunk, row) segment per block iteration: the gradient
 //   k_ce_chunk_fwd  one (chunk, row) segment per warp: chunk statistics
 //   k_ce_merge      one row per thread: merge the chunk statistics, then as k_ce_fwd
@@ -49,6 +49,7 @@ __global__ void __launch_bounds__(NT, (kSmooth ? 1024 : 1536) / NT)
                                                float4* __restrict__ row_stats, int32_t* status) {
     __shared__ float sm_m[NT / 32], sm_s[NT / 32], sm_sz[NT / 32];
     __shared__ float sm_zt;
+    asm volatile("griddepcontrol.launch_dependents;");   // the loss reduction may be scheduled now
     for (int64_t row = blockIdx.x; row < T; row += gridDim.x) {
         const int64_t t = labels[row];
         const bool ignored = (t == ignore_index);
@@ -97,6 +98,7 @@ __global__ void __launch_bounds__(kWarpRowThreads, 3)
                   int32_t* status) {
     const int lane = threadIdx.x & 31;
     const int64_t warps = (int64_t)gridDim.x * (kWarpRowThreads / 32);
+    asm volatile("griddepcontrol.launch_dependents;");   // the loss reduction may be scheduled now
     for (int64_t row = (int64_t)blockIdx.x * (kWarpRowThreads / 32) + (threadIdx.x >> 5); row < T; row += warps) {
         const int64_t t = labels[row];
         const bool ignored = (t == ignore_index);
@@ -134,15 +136,37 @@ __global__ void __launch_bounds__(kWarpRowThreads, 3)
 // used, and the validity of up to 64 rows stays in a register mask for the weight pass (longer
 // inputs reread their labels there).  The partition is fixed, so the sum is bitwise
 // reproducible.
+//
+// The sum is an fp32 pair (s, c) carried with error-free two-sum steps (Knuth's TwoSum: s + x
+// = t + e exactly), so s + c holds the exact sum of the terms up to rounding of the
+// compensation itself, far below the fp32 rounding of the result; the pairs merge the same
+// way across lanes and warps.  (This device runs fp64 arithmetic at a small fraction of its
+// fp32 rate: fp64 partials made this one-block kernel take 17 us at T = 16384.)  Only the
+// final division is done in fp64.  A non-finite sum (an inf loss row, or NaN) is s alone.
+//
+// Launched as a programmatic dependent of the row kernel before it: griddepcontrol.wait makes
+// the row kernel's results visible before any read here.
+__device__ __forceinline__ void two_sum_add(float& s, float& c, float x) {
+    const float t = s + x;
+    const float bp = t - s;
+    c += (s - (t - bp)) + (x - bp);
+    s = t;
+}
+__device__ __forceinline__ void two_sum_merge(float& s, float& c, float s2, float c2) {
+    two_sum_add(s, c, s2);
+    c += c2;
+}
+
 template <int NT>
 __global__ void __launch_bounds__(NT) k_ce_reduce(const float* __restrict__ loss_rows, const int64_t* __restrict__ labels,
                                                   int64_t T, int64_t V, int64_t ignore_index, int red,
                                                   float* loss_out, float4* row_stats) {
     constexpr int U = 8;
-    __shared__ double sm_a[NT / 32];
+    __shared__ float sm_s[NT / 32], sm_c[NT / 32];
     __shared__ long long sm_n[NT / 32];
     __shared__ float sm_inv;
-    double acc = 0.0;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    float acc = 0.f, comp = 0.f;
     long long n = 0;
     uint64_t valid_mask = 0;   // bit j * U + u: row tid + NT (U j + u) is valid (j < 8)
     int j = 0;
@@ -158,7 +182,7 @@ __global__ void __launch_bounds__(NT) k_ce_reduce(const float* __restrict__ loss
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             if (t[u] != ignore_index) {
-                acc += (double)l[u];
+                two_sum_add(acc, comp, l[u]);
                 const bool ok = t[u] >= 0 && t[u] < V;
                 n += ok ? 1 : 0;
                 if (ok && j < 8) valid_mask |= 1ull << (j * U + u);
@@ -167,26 +191,32 @@ __global__ void __launch_bounds__(NT) k_ce_reduce(const float* __restrict__ loss
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
-        acc += __shfl_xor_sync(0xFFFFFFFFu, acc, off);
+        const float s2 = __shfl_xor_sync(0xFFFFFFFFu, acc, off);
+        const float c2 = __shfl_xor_sync(0xFFFFFFFFu, comp, off);
+        two_sum_merge(acc, comp, s2, c2);
         n += __shfl_xor_sync(0xFFFFFFFFu, n, off);
     }
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    if (lane == 0) { sm_a[wid] = acc; sm_n[wid] = n; }
+    if (lane == 0) { sm_s[wid] = acc; sm_c[wid] = comp; sm_n[wid] = n; }
     __syncthreads();
     if (wid == 0) {
-        acc = lane < NT / 32 ? sm_a[lane] : 0.0;
+        acc = lane < NT / 32 ? sm_s[lane] : 0.f;
+        comp = lane < NT / 32 ? sm_c[lane] : 0.f;
         n = lane < NT / 32 ? sm_n[lane] : 0;
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) {
-            acc += __shfl_xor_sync(0xFFFFFFFFu, acc, off);
+            const float s2 = __shfl_xor_sync(0xFFFFFFFFu, acc, off);
+            const float c2 = __shfl_xor_sync(0xFFFFFFFFu, comp, off);
+            two_sum_merge(acc, comp, s2, c2);
             n += __shfl_xor_sync(0xFFFFFFFFu, n, off);
         }
         if (lane == 0) {
+            const double sum = isfinite(acc) ? (double)acc + (double)comp : (double)acc;
             if (red == VCE_RED_MEAN) {
-                *loss_out = (float)(acc / (double)n);   // 0/0 = NaN when every row is ignored
+                *loss_out = (float)(sum / (double)n);   // 0/0 = NaN when every row is ignored
                 sm_inv = n > 0 ? (float)(1.0 / (double)n) : 0.f;
             } else {
-                *loss_out = (float)acc;
+                *loss_out = (float)sum;
             }
         }
     }
@@ -290,6 +320,69 @@ __global__ void k_ce_merge(const float4* __restrict__ chunk_stats, int k, int64_
     }
 }
 
+// The merge for many partials per row (the linear-CE's per-tile statistics, 501 tiles at V =
+// 128256): one thread per row merges its k partials one after another, and 8192 rows keep only
+// 32 SMs busy (0.146 ms per call).  Here a block takes 32 consecutive rows (one per lane) and
+// its kSeg warps split the partials into contiguous ranges, so each load instruction reads
+// 32 consecutive rows' partials of one tile; warp 0 then merges the kSeg ranges in order and
+// finishes the row.  The partition is fixed, so the result is reproducible.
+constexpr int kMergeSeg = 8;
+
+__global__ void __launch_bounds__(32 * kMergeSeg) k_ce_merge_seg(const float4* __restrict__ chunk_stats, int k,
+                                                                int64_t T, int64_t V,
+                                                                const int64_t* __restrict__ labels,
+                                                                int64_t ignore_index, float* __restrict__ loss_rows,
+                                                                float4* __restrict__ row_stats, int32_t* status) {
+    __shared__ float4 part[kMergeSeg][32];   // (m, s, z_t, owner) of each range, per row
+    const int lane = threadIdx.x & 31, seg = threadIdx.x >> 5;
+    const int c0 = (int)((int64_t)k * seg / kMergeSeg), c1 = (int)((int64_t)k * (seg + 1) / kMergeSeg);
+    for (int64_t base = (int64_t)blockIdx.x * 32; base < T; base += (int64_t)gridDim.x * 32) {
+        const int64_t row = base + lane;
+        const int64_t t = row < T ? labels[row] : ignore_index;
+        const bool valid = row < T && t != ignore_index && t >= 0 && t < V;
+        float M = -kInf, S = 0.f, zt = 0.f, own = 0.f;
+        if (valid) {
+            int c = c0;
+            for (; c + 4 <= c1; c += 4) {   // four partials in flight before any is merged
+                float4 cs[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) cs[u] = chunk_stats[(int64_t)(c + u) * T + row];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    ms_merge(M, S, cs[u].x, cs[u].y);
+                    if (cs[u].w != 0.f) { zt = cs[u].z; own = 1.f; }
+                }
+            }
+            for (; c < c1; ++c) {
+                const float4 cs = chunk_stats[(int64_t)c * T + row];
+                ms_merge(M, S, cs.x, cs.y);
+                if (cs.w != 0.f) { zt = cs.z; own = 1.f; }
+            }
+        }
+        part[seg][lane] = make_float4(M, S, zt, own);
+        __syncthreads();
+        if (seg == 0 && row < T) {
+            if (!valid) {
+                loss_rows[row] = (t == ignore_index) ? 0.f : __int_as_float(0x7FC00000);
+                row_stats[row] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (t != ignore_index) flag_label_error(status);
+            } else {
+                float Mr = -kInf, Sr = 0.f, ztr = 0.f;
+#pragma unroll
+                for (int g = 0; g < kMergeSeg; ++g) {
+                    const float4 pg = part[g][lane];
+                    ms_merge(Mr, Sr, pg.x, pg.y);
+                    if (pg.w != 0.f) ztr = pg.z;
+                }
+                float loss;
+                row_stats[row] = ce_row_finish(Mr, Sr, ztr, &loss);
+                loss_rows[row] = loss;
+            }
+        }
+        __syncthreads();
+    }
+}
+
 // ------------------------------------------------------------------------------------------
 // host side
 
@@ -332,11 +425,21 @@ cudaError_t dispatch_fwd(int nt, const void* logits, int64_t T, int64_t V, int64
 }
 
 
+// A programmatic dependent launch: the block may be scheduled while the row kernel before it
+// drains, and waits in griddepcontrol.wait until that kernel's writes are visible.
 cudaError_t launch_reduce(const float* loss_rows, const int64_t* labels, int64_t T, int64_t V, int64_t ig, int red,
                           float* loss_out, float* row_stats, cudaStream_t s) {
-    k_ce_reduce<1024><<<1, 1024, 0, s>>>(loss_rows, labels, T, V, ig, red, loss_out,
-                                         reinterpret_cast<float4*>(row_stats));
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(1);
+    cfg.blockDim = dim3(1024);
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k_ce_reduce<1024>, loss_rows, labels, T, V, ig, red, loss_out,
+                              reinterpret_cast<float4*>(row_stats));
 }
 
 int check_common(vce_dtype dt, vce_reduction red, int64_t T) {
@@ -353,6 +456,14 @@ VCE_DEBUG_READER(debug_word_ce_fwd)
 cudaError_t launch_stats_merge(const float* part, int k, int64_t T, int64_t V, const int64_t* labels,
                                int64_t ignore_index, float* loss_rows, float* row_stats, int32_t* status,
                                cudaStream_t s) {
+    if (k >= 4 * kMergeSeg) {   // many partials per row: ranges of them per warp
+        const int64_t blocks = (T + 31) / 32;
+        const int mg = (int)std::max<int64_t>(1, std::min<int64_t>(blocks, (int64_t)device_sm_count() * 8));
+        k_ce_merge_seg<<<mg, 32 * kMergeSeg, 0, s>>>(reinterpret_cast<const float4*>(part), k, T, V, labels,
+                                                      ignore_index, loss_rows, reinterpret_cast<float4*>(row_stats),
+                                                      status);
+        return cudaGetLastError();
+    }
     const int mt = 256;
     const int mg = (int)std::max<int64_t>(1, std::min<int64_t>((T + mt - 1) / mt, (int64_t)device_sm_count() * 8));
     k_ce_merge<<<mg, mt, 0, s>>>(reinterpret_cast<const float4*>(part), k, T, V, labels, ignore_index, loss_rows,
@@ -389,28 +500,26 @@ extern "C" int ce_forward_ls(const void* logits, vce_dtype dt, int64_t T, int64_
     if ((rc = require_sm100())) return rc;
     if (cudaMemsetAsync(status, 0, sizeof(int32_t), s) != cudaSuccess) return VCE_ERR_CUDA;
     if (T > 0) {
-        // Rows of at most 32 KB: one warp per row (k_ce_fwd_warp; 8192 x 16000 bf16: 0.0695
-        // against 0.0815 ms on the ring).  Rows of 32-64 KB with fewer than 64 per SM: one
-        // 256-thread block per row, six per SM (4096 x 32000 bf16: 0.0613 ms; the ring 0.0713, a
-        // warp per row 0.0798, 512-thread blocks with a row's eight loads per thread in flight at
-        // once 0.0797).  Longer rows stream through shared memory where the layout allows it,
-        // else one block per row with loads from global memory.
+        // Rows of at most 32 KB: one warp per row (k_ce_fwd_warp; 8192 x 16000 bf16: 0.070 ms,
+        // against 0.080 on the stage ring and 0.102 on the ring's four consumer groups).  Longer
+        // rows of whole 16-byte vectors stream through the shared-memory stage ring (rows of
+        // two stages with its consumers in two groups: 4096 x 32000 bf16, 0.0592 ms, against
+        // 0.0613 on one block per row), other layouts one block per row with global loads.
         bool launched = false;
         const int64_t row_bytes = V * (int64_t)es;
-        const bool few_short_rows = row_bytes > 32768 && row_bytes <= 65536 && T < 64 * (int64_t)device_sm_count();
         cudaError_t e = cudaSuccess;
-        const int nt = pick_threads(row_bytes);
         if (row_bytes <= 32768) {
             e = dt == VCE_BF16 ? launch_fwd_warp<uint16_t>(logits, T, V, ld, labels, ignore_index, label_smoothing,
                                                            loss_rows, row_stats, status, s)
                                : launch_fwd_warp<float>(logits, T, V, ld, labels, ignore_index, label_smoothing,
                                                         loss_rows, row_stats, status, s);
             launched = true;
-        } else if (!few_short_rows) {
+        } else {
             e = launch_fwd_ring(dt, logits, T, V, ld, labels, ignore_index, label_smoothing, loss_rows, row_stats,
                                 status, s, &launched);
         }
         if (e == cudaSuccess && !launched) {
+            const int nt = pick_threads(row_bytes);
             e = dt == VCE_BF16 ? dispatch_fwd<uint16_t>(nt, logits, T, V, ld, labels, ignore_index, label_smoothing,
                                                         loss_rows, row_stats, status, s)
                                : dispatch_fwd<float>(nt, logits, T, V, ld, labels, ignore_index, label_smoothing,

@@ -8,9 +8,10 @@
 //   producer warp   one lane streams each row into a ring of seven 32 KB stages with bulk
 //                   asynchronous copies (cp.async.bulk), completion counted on per-stage
 //                   mbarriers, and publishes each row's index and target column
-//   consumer warps  per stage, a thread's 4 x 16-byte vectors summed at once into its
-//                   (max, sum-exp) pair (stage::fwd_stage); the stage goes back to the producer
-//                   right away; at the end of a row each warp publishes its pair
+//   consumer warps  in kGroups groups (1 or 2), group g taking the CTA's rows g, g + kGroups, ...; per
+//                   stage, a thread's 16-byte vectors summed four at a time into its (max,
+//                   sum-exp) pair (stage::fwd_stage); the stage goes back to the producer right
+//                   away; at the end of a row each warp of the group publishes its pair
 //   stats warp      merges the warps' pairs, finishes the row (loss, row statistics) and frees
 //                   the row's slots; it also writes the outputs of ignored and invalid rows
 // Row hand-offs go through kSlots mbarrier-guarded slots, by the row's index in the CTA's
@@ -19,9 +20,18 @@
 // four 16-byte loads in flight and sums them one vector at a time); here the copies need no
 // registers and the sum takes fewer instructions per element.
 //
+// Groups: a row costs each warp that touches it a fixed amount of work (its stage waits and
+// releases, the shuffle merge of its lanes, the hand-off), so rows of two stages run with the
+// consumers in 2 groups: each thread then takes twice the columns of a row for the same
+// per-row work.  Each group holds one stage at a time, so 2 stages are being summed and 5 are
+// loading ahead.  (4096 x 32000 bf16: 0.0592 ms for the call, against 0.0654 without groups
+// and 0.0613 on one block per row.  Rows of one stage in 4 groups lost to one warp per row:
+// 8192 x 16000, 0.102 against 0.070 ms.)
+//
 // Every wait is bounded (2 s); a wait that gives up writes its code to the status word (105
 // free stage, 106 loaded stage, 108 warp partials, 110 free slots) and sets the CTA's abort
-// flag, after which every role keeps its arrivals but skips the work and later waits.
+// flag, after which every role keeps its arrivals but skips the work and later waits.  111:
+// consumer groups asked for rows too long for them (the kernel returns before any wait).
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -44,13 +54,13 @@ constexpr int kConsumerWarps = 16;
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kProducerWarp = kConsumerWarps, kStatsWarp = kConsumerWarps + 1;
 constexpr int kThreads = kConsumers + 64;
-constexpr int kVecPerThread = kChunk / 16 / kConsumers;
+constexpr int kVecPerThread = kChunk / 16 / kConsumers;   // per 4-vector batch of a stage
 constexpr uint32_t kSuspendNs = 0;       // plain polls (a suspend hint measured no faster here)
 constexpr int kSlots = 4;                // hand-off slots: consumers run up to kSlots rows ahead of the stats warp
 constexpr int kInfoSlots = 16;           // > the rows the producer can run ahead of the stats warp (kStages + kSlots)
 static_assert(kVecPerThread * kConsumers * 16 == kChunk, "every consumer takes the same whole vectors of a stage");
 static_assert((kConsumerWarps & (kConsumerWarps - 1)) == 0 && kConsumerWarps <= 32, "warp pairs merge in one warp");
-enum { kErrEmpty = 105, kErrFull = 106, kErrPartials = 108, kErrSlots = 110 };
+enum { kErrEmpty = 105, kErrFull = 106, kErrPartials = 108, kErrSlots = 110, kErrGroups = 111 };
 
 struct RowInfo {
     int64_t row;
@@ -87,9 +97,23 @@ __device__ __forceinline__ bool label_valid(const Args& a, int64_t t) {
 }
 
 // kSmooth: label smoothing eps > 0; each row's sum of all logits is reduced alongside the pair.
-template <typename S, bool kSmooth>
+// kGroups: consumer groups (1 or 2), each summing whole rows (see the file comment).
+template <typename S, bool kSmooth, int kGroups>
 __global__ void __launch_bounds__(kThreads, 1) k_ce_fwd_ring(const __grid_constant__ Args a) {
     constexpr int G = Elt<S>::kGroup;
+    constexpr int kGW = kConsumerWarps / kGroups;   // warps of a group
+    constexpr int kGT = kGW * 32;                   // threads of a group
+    static_assert(kGroups == 1 || kGroups == 2, "consumer groups");
+    // Hand-off slots in use.  With groups, a group waits on a stage's fill of ring position p
+    // while other groups may still hold earlier positions; the parity wait is only sound once
+    // the stage's previous fill (p - kStages) has landed.  A group starts row e after the stats
+    // warp read row e - kUse, so every row up to e - kUse has been summed; with kUse * nchunk <=
+    // kStages that covers p - kStages for every chunk of row e.  kUse >= kGroups keeps the
+    // slot barriers within one phase of their waiters.
+    constexpr int kUse = kGroups == 2 ? 3 : kSlots;
+    static_assert(kUse <= kSlots && kUse >= kGroups, "slot count");
+    // the loss reduction after this kernel may be scheduled now (it waits for this grid's writes)
+    asm volatile("griddepcontrol.launch_dependents;");
     extern __shared__ __align__(128) uint8_t smem[];
     Ctl& ctl = *reinterpret_cast<Ctl*>(smem + kStages * kChunk);
     volatile int* abort_flag = &ctl.abort;
@@ -97,14 +121,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_fwd_ring(const __grid_consta
     const int64_t stride = gridDim.x;
     const int64_t bytes = a.V * (int64_t)sizeof(S);
     const int nchunk = (int)((bytes + kChunk - 1) / kChunk);
+    if (kGroups > 1 && nchunk * kUse > kStages) {   // rows too long for groups (the host never asks)
+        if (threadIdx.x == 0) atomicCAS(a.status, 0, (int32_t)kErrGroups);
+        return;
+    }
 
     if (threadIdx.x == 0) {
         for (int st = 0; st < kStages; ++st) {
             tc::mbar_init(&ctl.full[st], 1);
-            tc::mbar_init(&ctl.empty[st], kConsumerWarps);
+            tc::mbar_init(&ctl.empty[st], kGW);
         }
-        for (int p = 0; p < kSlots; ++p) {
-            tc::mbar_init(&ctl.rbar[p], kConsumerWarps);
+        for (int p = 0; p < kUse; ++p) {
+            tc::mbar_init(&ctl.rbar[p], kGW);
             tc::mbar_init(&ctl.fbar[p], 1);
         }
         for (int i = 0; i < kInfoSlots; ++i) ctl.info[i] = RowInfo{-1, -1, 0};
@@ -195,20 +223,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_fwd_ring(const __grid_consta
         __syncwarp();
         const int nv = count_valid();
         for (int e = 0; e < nv; ++e) {
-            const int par = e % kSlots;
-            tc::mbar_wait(&ctl.rbar[par], (e / kSlots) & 1, abort_flag, a.status, kErrPartials, a.wait_ns,
+            const int par = e % kUse;
+            tc::mbar_wait(&ctl.rbar[par], (e / kUse) & 1, abort_flag, a.status, kErrPartials, a.wait_ns,
                           kSuspendNs);
-            float m = lane < kConsumerWarps ? ctl.red_m[par][lane] : -kInf;
-            float s = lane < kConsumerWarps ? ctl.red_s[par][lane] : 0.f;
+            float m = lane < kGW ? ctl.red_m[par][lane] : -kInf;
+            float s = lane < kGW ? ctl.red_s[par][lane] : 0.f;
 #pragma unroll
-            for (int off = kConsumerWarps / 2; off > 0; off >>= 1) {
+            for (int off = kGW / 2; off > 0; off >>= 1) {
                 const float m2 = __shfl_xor_sync(0xFFFFFFFFu, m, off);
                 const float s2 = __shfl_xor_sync(0xFFFFFFFFu, s, off);
                 ms_merge(m, s, m2, s2);
             }
             float tot = 0.f;   // the row's sum of logits, warps added in a fixed order
             if (kSmooth && lane == 0)
-                for (int w = 0; w < kConsumerWarps; ++w) tot += ctl.red_z[par][w];
+                for (int w = 0; w < kGW; ++w) tot += ctl.red_z[par][w];
             if (lane == 0) {
                 const RowInfo ri = ctl.info[e % kInfoSlots];
                 const float zt = ctl.zt[par];
@@ -224,14 +252,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_fwd_ring(const __grid_consta
         }
     } else {
         // ---------------- consumers ----------------
-        const int tid = threadIdx.x;
+        const int grp = warp / kGW, gw = warp % kGW;
+        const int gtid = threadIdx.x - grp * kGT;   // thread index within the group
         const int nv = count_valid();
-        uint32_t q = 0;   // ring chunk of the current row's first chunk
-        for (int e = 0; e < nv; ++e, q += nchunk) {
-            const int par = e % kSlots;
-            // the slot was read for row e - kSlots
-            if (e >= kSlots)
-                tc::mbar_wait(&ctl.fbar[par], ((e / kSlots) & 1) ^ 1, abort_flag, a.status, kErrSlots, a.wait_ns,
+        for (int e = grp; e < nv; e += kGroups) {
+            const int par = e % kUse;
+            const uint32_t q = (uint32_t)e * (uint32_t)nchunk;   // ring chunk of the row's first chunk
+            // the slot was read for row e - kUse
+            if (e >= kUse)
+                tc::mbar_wait(&ctl.fbar[par], ((e / kUse) & 1) ^ 1, abort_flag, a.status, kErrSlots, a.wait_ns,
                               kSuspendNs);
             float m = -kInf, s = 0.f, mb = 0.f, sz = 0.f;
             int tl = -1;
@@ -244,9 +273,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_fwd_ring(const __grid_consta
                 if (ok) {
                     const uint4* buf = reinterpret_cast<const uint4*>(smem + st * kChunk);
                     const int nvec = (int)(std::min<int64_t>(kChunk, bytes - (int64_t)j * kChunk) / 16);
-                    const int rel0 = tl - (j * (kChunk / (int)sizeof(S)) + tid * G);
-                    stage::fwd_stage_any<S, kConsumers, kVecPerThread, kSmooth>(buf, nvec, rel0, tid, m, s, mb,
-                                                                                &ctl.zt[par], &sz);
+#pragma unroll
+                    for (int b = 0; b < kGroups; ++b) {   // batches of kVecPerThread vectors per thread
+                        const int v0 = b * kVecPerThread * kGT;
+                        if (v0 >= nvec) break;
+                        const int rel0 = tl - (j * (kChunk / (int)sizeof(S)) + (v0 + gtid) * G);
+                        stage::fwd_stage_any<S, kGT, kVecPerThread, kSmooth>(buf + v0, nvec - v0, rel0, gtid, m, s,
+                                                                             mb, &ctl.zt[par], &sz);
+                    }
                 }
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(&ctl.empty[st]);
@@ -257,9 +291,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_fwd_ring(const __grid_consta
                 for (int off = 16; off > 0; off >>= 1) sz += __shfl_xor_sync(0xFFFFFFFFu, sz, off);
             }
             if (lane == 0) {
-                ctl.red_m[par][warp] = m;
-                ctl.red_s[par][warp] = s;
-                if (kSmooth) ctl.red_z[par][warp] = sz;
+                ctl.red_m[par][gw] = m;
+                ctl.red_s[par][gw] = s;
+                if (kSmooth) ctl.red_z[par][gw] = sz;
             }
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&ctl.rbar[par]);
@@ -267,14 +301,23 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_fwd_ring(const __grid_consta
     }
 }
 
-template <typename S>
-cudaError_t launch(const Args& args, int sms, cudaStream_t s) {
-    auto kern = args.eps > 0.f ? k_ce_fwd_ring<S, true> : k_ce_fwd_ring<S, false>;
+// Rows of two stages run in 2 groups (kUse * nchunk <= kStages), other rows in 1 (every
+// consumer warp on every stage).
+template <typename S, int kGroups>
+cudaError_t launch_groups(const Args& args, int sms, cudaStream_t s) {
+    auto kern = args.eps > 0.f ? k_ce_fwd_ring<S, true, kGroups> : k_ce_fwd_ring<S, false, kGroups>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     const int grid = (int)std::min<int64_t>(sms, args.T);
     kern<<<grid, kThreads, kSmemBytes, s>>>(args);
     return cudaGetLastError();
+}
+
+template <typename S>
+cudaError_t launch(const Args& args, int sms, cudaStream_t s) {
+    const int64_t nchunk = (args.V * (int64_t)sizeof(S) + kChunk - 1) / kChunk;
+    if (nchunk == 2) return launch_groups<S, 2>(args, sms, s);
+    return launch_groups<S, 1>(args, sms, s);
 }
 
 }  // namespace fring

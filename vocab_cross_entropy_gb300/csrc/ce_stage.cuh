@@ -33,20 +33,27 @@ __device__ __forceinline__ bool holds_target(int rel0) {
     return rel0 >= 0 && rel0 < U * Span && (rel0 % Span) < G;
 }
 
-// Forward over one loaded stage: the thread's (max, sum-exp) pair takes its U * G values at
-// once (one reference check, one overflow check).  kTarget: this thread holds the target,
-// whose value goes to *zt and is left out of the sum.  kSumZ: the stage's values (target
-// included) are also added to *sz.
-template <typename S, int NT, int U, bool kFull, bool kTarget, bool kSumZ = false>
-__device__ __forceinline__ void fwd_stage(const uint4* buf, int nvec, int rel0, int tid, float& m, float& s,
-                                          float& mb, float* zt, float* sz = nullptr) {
-    constexpr int G = Elt<S>::kGroup;
-    float v[U][G];
+// The thread's U vectors of a loaded stage (vectors past a partial stage's end read as -inf).
+template <typename S, int NT, int U, bool kFull>
+__device__ __forceinline__ void load_stage(const uint4* buf, int nvec, int tid, uint4 (&r)[U]) {
 #pragma unroll
     for (int u = 0; u < U; ++u) {
         const int vi = tid + u * NT;
-        Elt<S>::unpack((kFull || vi < nvec) ? tc::lds16(buf + vi) : neg_inf16<S>(), v[u]);
+        r[u] = (kFull || vi < nvec) ? tc::lds16(buf + vi) : neg_inf16<S>();
     }
+}
+
+// Forward over the thread's U vectors of a stage: the (max, sum-exp) pair takes its U * G
+// values at once (one reference check, one overflow check).  kTarget: this thread holds the
+// target, whose value goes to *zt and is left out of the sum.  kSumZ: the stage's values
+// (target included) are also added to *sz.
+template <typename S, int NT, int U, bool kFull, bool kTarget, bool kSumZ = false>
+__device__ __forceinline__ void fwd_vectors(const uint4 (&r)[U], int nvec, int rel0, int tid, float& m, float& s,
+                                            float& mb, float* zt, float* sz = nullptr) {
+    constexpr int G = Elt<S>::kGroup;
+    float v[U][G];
+#pragma unroll
+    for (int u = 0; u < U; ++u) Elt<S>::unpack(r[u], v[u]);
     if (kSumZ) {
 #pragma unroll
         for (int u = 0; u < U; ++u) {
@@ -74,21 +81,39 @@ __device__ __forceinline__ void fwd_stage(const uint4* buf, int nvec, int rel0, 
     ms_push_lazy_batch<U, G>(v, m, s, mb);
 }
 
-// The forward of a stage, choosing the instantiation for this thread and stage.
+// Forward over one loaded stage (load_stage, then fwd_vectors); r keeps the loaded vectors.
+template <typename S, int NT, int U, bool kFull, bool kTarget, bool kSumZ = false>
+__device__ __forceinline__ void fwd_stage(const uint4* buf, int nvec, int rel0, int tid, float& m, float& s,
+                                          float& mb, float* zt, float* sz, uint4 (&r)[U]) {
+    load_stage<S, NT, U, kFull>(buf, nvec, tid, r);
+    fwd_vectors<S, NT, U, kFull, kTarget, kSumZ>(r, nvec, rel0, tid, m, s, mb, zt, sz);
+}
+
+// The forward of a stage, choosing the instantiation for this thread and stage.  nvec may
+// exceed U * NT (a later batch of the same stage follows); only the first U * NT are summed.
+// r: the thread's loaded vectors (for a caller that keeps them).
+template <typename S, int NT, int U, bool kSumZ = false>
+__device__ __forceinline__ void fwd_stage_any(const uint4* buf, int nvec, int rel0, int tid, float& m, float& s,
+                                              float& mb, float* zt, float* sz, uint4 (&r)[U]) {
+    const bool full = nvec >= U * NT;
+    if (holds_target<S, NT, U>(rel0)) {
+        if (full) fwd_stage<S, NT, U, true, true, kSumZ>(buf, nvec, rel0, tid, m, s, mb, zt, sz, r);
+        else fwd_stage<S, NT, U, false, true, kSumZ>(buf, nvec, rel0, tid, m, s, mb, zt, sz, r);
+    } else {
+        if (full) fwd_stage<S, NT, U, true, false, kSumZ>(buf, nvec, rel0, tid, m, s, mb, zt, sz, r);
+        else fwd_stage<S, NT, U, false, false, kSumZ>(buf, nvec, rel0, tid, m, s, mb, zt, sz, r);
+    }
+}
 template <typename S, int NT, int U, bool kSumZ = false>
 __device__ __forceinline__ void fwd_stage_any(const uint4* buf, int nvec, int rel0, int tid, float& m, float& s,
                                               float& mb, float* zt, float* sz = nullptr) {
-    const bool full = nvec == U * NT;
-    if (holds_target<S, NT, U>(rel0)) {
-        if (full) fwd_stage<S, NT, U, true, true, kSumZ>(buf, nvec, rel0, tid, m, s, mb, zt, sz);
-        else fwd_stage<S, NT, U, false, true, kSumZ>(buf, nvec, rel0, tid, m, s, mb, zt, sz);
-    } else {
-        if (full) fwd_stage<S, NT, U, true, false, kSumZ>(buf, nvec, rel0, tid, m, s, mb, zt, sz);
-        else fwd_stage<S, NT, U, false, false, kSumZ>(buf, nvec, rel0, tid, m, s, mb, zt, sz);
-    }
+    uint4 r[U];
+    fwd_stage_any<S, NT, U, kSumZ>(buf, nvec, rel0, tid, m, s, mb, zt, sz, r);
 }
 
-// Gradient of one held stage: coef * 2^(z log2 e - bias) for every column, less shift = c eps / V
+// Gradient of the thread's U vectors of a held stage (bwd_vectors: from registers the caller
+// loaded; bwd_stage: read from the shared-memory stage): coef * 2^(z log2 e - bias) for every
+// column, less shift = c eps / V
 // under label smoothing (kShift), then the thread holding the target overwrites that entry with
 // gt (its own later store to the same address).  Without kShift the entries are the plain
 // product (an FMA with a zero addend rounds the same, but measured 1.2% slower in the one-pass
@@ -97,15 +122,9 @@ __device__ __forceinline__ void fwd_stage_any(const uint4* buf, int nvec, int re
 // faster in the backward alone.  Packed sums in the forward (even and odd columns summed apart)
 // measured 0.3% slower in the one-pass kernel than the scalar tree.
 template <typename S, typename O, int NT, int U, bool kFull, bool kShift = false, bool kPacked = false>
-__device__ __forceinline__ void bwd_stage(const uint4* buf, int nvec, O* gcol, int rel0, int tid, float coef,
-                                          float bias, float gt, float shift) {
+__device__ __forceinline__ void bwd_vectors(const uint4 (&r)[U], int nvec, O* gcol, int rel0, int tid, float coef,
+                                            float bias, float gt, float shift) {
     constexpr int G = Elt<S>::kGroup;
-    uint4 r[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-        const int vi = tid + u * NT;
-        if (kFull || vi < nvec) r[u] = tc::lds16(buf + vi);
-    }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
         const int vi = tid + u * NT;
@@ -135,6 +154,18 @@ __device__ __forceinline__ void bwd_stage(const uint4* buf, int nvec, O* gcol, i
         }
     }
     if (holds_target<S, NT, U>(rel0)) Elt<O>::store1(gcol + tid * G + rel0, gt);
+}
+
+template <typename S, typename O, int NT, int U, bool kFull, bool kShift = false, bool kPacked = false>
+__device__ __forceinline__ void bwd_stage(const uint4* buf, int nvec, O* gcol, int rel0, int tid, float coef,
+                                          float bias, float gt, float shift) {
+    uint4 r[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const int vi = tid + u * NT;
+        if (kFull || vi < nvec) r[u] = tc::lds16(buf + vi);
+    }
+    bwd_vectors<S, O, NT, U, kFull, kShift, kPacked>(r, nvec, gcol, rel0, tid, coef, bias, gt, shift);
 }
 
 }  // namespace stage
