@@ -150,10 +150,12 @@ VCE_API int vce_debug_status(int32_t* host_out);
  *              NONE) or 0 (ignored / invalid row).  Consumed by ce_backward.
  *   status     [1] int32, set to 0 by this call, VCE_ERR_LABEL on a bad label, or
  *              105 / 106 / 108 / 110 when a bounded device-side wait gave up after 2 s
- *              (rows of 16-byte multiples stream through a shared-memory stage ring:
- *              free stage, loaded stage, warp partials, free statistics slots; rows of
- *              32-64 KB with fewer than 64 rows per SM take a per-block kernel instead,
- *              which has no such waits); the outputs are then undefined
+ *              (rows longer than 32 KB made of 16-byte vectors stream through a
+ *              shared-memory stage ring: free stage, loaded stage, warp partials, free
+ *              statistics slots; shorter rows take one warp per row and other layouts
+ *              one block per row, which have no such waits), or 111 if the ring's
+ *              consumer groups were given rows longer than two stages (not reachable
+ *              from this call); the outputs are then undefined
  */
 VCE_API int ce_forward(const void* logits, vce_dtype dt, int64_t T, int64_t V, int64_t ld,
                const int64_t* labels, int64_t ignore_index, vce_reduction red,

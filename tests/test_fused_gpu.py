@@ -88,6 +88,22 @@ def test_fused_ring_wraps_over_many_rows(vce):
     check_against_oracle(p, storage, out, rows, grad, "none", np.linspace(0.5, 1.5, 600))
 
 
+@pytest.mark.parametrize("T,V,dtype,reduction", [
+    (2000, 5000, "bf16", "mean"),       # one CTA per row, one stage: 13-14 rows per CTA
+    (600, 65536, "bf16", "none"),       # one CTA per row, four whole stages: three of the next row's beside them
+    (1500, 70000, "bf16", "sum"),       # 2-CTA clusters, about 20 rows per cluster
+    (300, 128256, "f32", "mean"),       # 4-CTA clusters
+    (160, 400000, "bf16", "mean"),      # 8-CTA clusters, about 8 rows per cluster
+])
+def test_fused_many_rows_per_cta(vce, T, V, dtype, reduction):
+    """Many rows per CTA or cluster, for every cluster size: the stage ring wraps many times
+    and the hand-off slots, double-buffered by row parity, are rewritten many times."""
+    p = gen.custom(T, V, dtype, seed=T + V, std=2.0, n_margin=T // 10, margin=(17.0, 50.0), n_ignore=T // 20)
+    go = np.linspace(0.5, 1.5, T) if reduction == "none" else 1.0
+    storage, out, rows, grad = fused(vce, p, reduction, go)
+    check_against_oracle(p, storage, out, rows, grad, reduction, go)
+
+
 def test_fused_padded_leading_dimensions(vce):
     """ld = V + 8 and ld_grad = V + 16 (shared-memory path): the padding is neither read into
     the statistics nor written."""
