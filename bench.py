@@ -218,7 +218,8 @@ class CEWorkload:
         self.grad = torch.empty((T, V), dtype=tdt, device=device)
         self.loss_host = torch.empty(T if reduction == "none" else 1, dtype=torch.float32, pin_memory=True)
         self.n_valid = int(np.sum(problem.labels != problem.ignore_index))
-        self.launches_per_step = 2 if reduction == "none" else 3   # forward kernel, (k_ce_reduce,) backward kernel
+        # forward kernel, k_ce_reduce (SUM / MEAN, unless the forward ring reduces in-kernel), backward kernel
+        self.launches_per_step = 2 if (reduction == "none" or forward_reduces_in_kernel(V, T, self.es, reduction)) else 3
 
     def fwd(self, stream):
         if self.eps:
@@ -298,15 +299,29 @@ BWD_RING_FILES = ["vocab_cross_entropy_gb300/csrc/ce_bwd_ring.cu", "vocab_cross_
 
 
 def forward_kernel(V, T=None, es=2):
-    """The kernel ce_forward runs for contiguous, 16-byte aligned [T, V] logits: the ring, except
-    for rows of 32-64 KB with fewer than 64 per SM (and layouts the ring does not take)."""
+    """The kernel ce_forward runs for contiguous, 16-byte aligned [T, V] logits: one warp per row
+    for rows of at most 32 KB, the stage ring for longer rows (and one block per row for layouts
+    neither takes)."""
+    if V * es <= 32768:
+        return "k_ce_fwd_warp"
     if V % 8:
         return "k_ce_fwd"
-    if T is not None and 32768 < V * es <= 65536:
-        sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
-        if T < 64 * sms:
-            return "k_ce_fwd"
     return "k_ce_fwd_ring"
+
+
+def forward_reduces_in_kernel(V, T, es, reduction):
+    """Whether the ce_forward call's row kernel reduces the losses itself (the stage ring, SUM or
+    MEAN, at most 65536 rows) instead of a k_ce_reduce launch after it."""
+    return forward_kernel(V, T, es) == "k_ce_fwd_ring" and reduction != "none" and T <= 65536
+
+
+def forward_call_kernels(V, T, es, reduction):
+    """The ce_forward call's kernels, as the bench line names them."""
+    k = forward_kernel(V, T, es)
+    if reduction == "none":
+        return k
+    return k + (" (the loss reduction folded in)" if forward_reduces_in_kernel(V, T, es, reduction)
+                else " + k_ce_reduce")
 
 
 FWD_RING_FILES = ["vocab_cross_entropy_gb300/csrc/ce_fwd_ring.cu", "vocab_cross_entropy_gb300/csrc/ce_stage.cuh",
@@ -411,7 +426,9 @@ class LinearWorkload:
         self.go = torch.ones(1, dtype=torch.float32, device=device)
         self.loss_host = torch.empty(1, dtype=torch.float32, pin_memory=True)
         nchunks = -(-V // 32768)
-        self.launches_per_step = 3 + 3 * nchunks     # statistics GEMM + merge + reduce, 3 GEMMs per chunk
+        # statistics GEMM + merge + reduce; per chunk the gradient-tile GEMM, dW (two launches over the
+        # halves of T, or one over the kept blocks when filtering) and dE
+        self.launches_per_step = 3 + (3 if filter_eps > 0 else 4) * nchunks
 
     def step(self, stream):
         if self.filter_eps > 0:
@@ -822,7 +839,7 @@ def run_ours(args, rank, local_rank, world):
                                            if captured_shape(w) and one_pass_kernel(w.p.V) == "k_ce_fused_ring"
                                            else None)}
         fkern = forward_kernel(w.p.V, w.p.T, w.es)
-        out["roofline_fwd"] = {"bound": "hbm", "kernel": fkern + " + k_ce_reduce (the ce_forward call)",
+        out["roofline_fwd"] = {"bound": "hbm", "kernel": forward_call_kernels(w.p.V, w.p.T, w.es, w.red) + " (the ce_forward call)",
                                "achieved": round(w.bytes_fwd() / (fwd_ms / 1e3) / 1e9, 1), "peak": peaks["hbm_gbs"],
                                "unit": "GB/s",
                                "frac": round(w.bytes_fwd() / (fwd_ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4),

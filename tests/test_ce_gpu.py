@@ -411,6 +411,45 @@ def test_forward_ring_non_finite_and_bad_labels(vce):
             assert abs(lr[r] - ref["loss_rows"][r]) <= 1e-4 * ref["loss_rows"][r]
 
 
+@pytest.mark.parametrize("reduction", ["mean", "sum", "none"])
+def test_forward_ring_bad_labels_and_reduction(vce, reduction):
+    """Rows of 40 KB (the stage ring, two consumer groups; for SUM and MEAN it also reduces the
+    losses itself): ignored rows, labels below 0 and at V.  The status is VCE_ERR_LABEL, bad rows'
+    losses and a reduced loss are NaN, and the valid rows match the oracle, weights included."""
+    T, V = 700, 20000
+    p = gen.custom(T, V, "bf16", seed=31, std=2.0, n_margin=20, margin=(17.0, 50.0), n_ignore=35)
+    labels = p.labels.copy()
+    bad = np.array([3, 150, 699])
+    labels[bad] = [-7, V, V + 123]
+    storage = p.full()
+    logits = to_device(storage, "bf16")
+    lab = torch.from_numpy(labels).cuda()
+    loss_out, loss_rows, stats, status = vce.ce_forward(logits, lab, -100, reduction)
+    torch.cuda.synchronize()
+    assert vce.vce_get_status(status) == 1
+    lr = loss_rows.cpu().numpy()
+    assert np.all(np.isnan(lr[bad]))
+    ok = labels.copy()
+    ok[bad] = -100
+    ref = O.ce(O.widen(storage, "bf16"), ok, "none")
+    valid = ref["valid"]
+    G.check_loss_rows(np.where(np.isin(np.arange(T), bad), 0.0, lr), ref["loss_rows"], valid)
+    if reduction != "none":
+        assert np.isnan(loss_out.item())
+    st = stats.cpu().numpy()
+    n_valid = int(valid.sum())
+    want_w = 1.0 / n_valid if reduction == "mean" else 1.0
+    assert np.all(st[valid, 3] == np.float32(want_w))
+    assert np.all(st[~valid, 3] == 0)
+    # the same batch without the bad labels reduces to the oracle's value, status 0
+    lab2 = torch.from_numpy(ok).cuda()
+    loss_out2, rows2, stats2, status2 = vce.ce_forward(logits, lab2, -100, reduction)
+    torch.cuda.synchronize()
+    assert vce.vce_get_status(status2) == 0
+    if reduction != "none":
+        G.check_reduced(loss_out2.item(), O.ce(O.widen(storage, "bf16"), ok, reduction)["loss_out"])
+
+
 @pytest.mark.parametrize("dtype,gdt", [("bf16", torch.float32), ("f32", torch.bfloat16), ("bf16", torch.bfloat16)])
 def test_backward_ring_padded_gradient(vce, dtype, gdt):
     """ce_backward on the stage ring into a wider gradient buffer (ld_grad = V + 8): every entry

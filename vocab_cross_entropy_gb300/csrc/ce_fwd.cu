@@ -499,6 +499,7 @@ extern "C" int ce_forward_ls(const void* logits, vce_dtype dt, int64_t T, int64_
     if (red != VCE_RED_NONE && !aligned(loss_out, 4)) return VCE_ERR_ALIGN;
     if ((rc = require_sm100())) return rc;
     if (cudaMemsetAsync(status, 0, sizeof(int32_t), s) != cudaSuccess) return VCE_ERR_CUDA;
+    bool reduced = false;   // the ring kernel reduced the losses itself
     if (T > 0) {
         // Rows of at most 32 KB: one warp per row (k_ce_fwd_warp; 8192 x 16000 bf16: 0.070 ms,
         // against 0.080 on the stage ring and 0.102 on the ring's four consumer groups).  Longer
@@ -515,8 +516,8 @@ extern "C" int ce_forward_ls(const void* logits, vce_dtype dt, int64_t T, int64_
                                                         loss_rows, row_stats, status, s);
             launched = true;
         } else {
-            e = launch_fwd_ring(dt, logits, T, V, ld, labels, ignore_index, label_smoothing, loss_rows, row_stats,
-                                status, s, &launched);
+            e = launch_fwd_ring(dt, logits, T, V, ld, labels, ignore_index, label_smoothing, red, loss_rows, loss_out,
+                                row_stats, status, s, &launched, &reduced);
         }
         if (e == cudaSuccess && !launched) {
             const int nt = pick_threads(row_bytes);
@@ -527,7 +528,7 @@ extern "C" int ce_forward_ls(const void* logits, vce_dtype dt, int64_t T, int64_
         }
         if (e != cudaSuccess) return VCE_ERR_CUDA;
     }
-    if (red != VCE_RED_NONE &&
+    if (red != VCE_RED_NONE && !reduced &&
         launch_reduce(loss_rows, labels, T, V, ignore_index, red, loss_out, row_stats, s) != cudaSuccess)
         return VCE_ERR_CUDA;
     return VCE_OK;

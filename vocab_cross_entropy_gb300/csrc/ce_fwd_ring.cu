@@ -28,6 +28,15 @@
 // and 0.0613 on one block per row.  Rows of one stage in 4 groups lost to one warp per row:
 // 8192 x 16000, 0.102 against 0.070 ms.)
 //
+// The loss reduction folded in (Args::fold, for SUM / MEAN with at most kFoldMaxRows rows): the
+// consumer warps count every valid label of the batch at the start, while the first copies are
+// in flight, so the stats warp writes each row's weight 1/N itself; at the end each CTA adds one
+// to a counter in the high 16 bits of the status word (which the caller cleared), and the CTA
+// that finds itself last sums every row's loss in a fixed order (fp32 two-sum pairs, as
+// k_ce_reduce) and writes the reduced loss.  Error codes stay in the low 16 bits: within the
+// kernel they go to a word in shared memory and are merged into the status word at the end,
+// first code wins; the last CTA clears the counter bits.  No separate reduction launch.
+//
 // Every wait is bounded (2 s); a wait that gives up writes its code to the status word (105
 // free stage, 106 loaded stage, 108 warp partials, 110 free slots) and sets the CTA's abort
 // flag, after which every role keeps its arrivals but skips the work and later waits.  111:
@@ -58,9 +67,10 @@ constexpr int kVecPerThread = kChunk / 16 / kConsumers;   // per 4-vector batch 
 constexpr uint32_t kSuspendNs = 0;       // plain polls (a suspend hint measured no faster here)
 constexpr int kSlots = 4;                // hand-off slots: consumers run up to kSlots rows ahead of the stats warp
 constexpr int kInfoSlots = 16;           // > the rows the producer can run ahead of the stats warp (kStages + kSlots)
+constexpr int64_t kFoldMaxRows = 65536;  // the folded reduction: every CTA counts every label (at most 512 KB)
 static_assert(kVecPerThread * kConsumers * 16 == kChunk, "every consumer takes the same whole vectors of a stage");
 static_assert((kConsumerWarps & (kConsumerWarps - 1)) == 0 && kConsumerWarps <= 32, "warp pairs merge in one warp");
-enum { kErrEmpty = 105, kErrFull = 106, kErrPartials = 108, kErrSlots = 110, kErrGroups = 111 };
+enum { kErrEmpty = 105, kErrFull = 106, kErrPartials = 108, kErrSlots = 110, kErrGroups = 111, kErrCount = 112 };
 
 struct RowInfo {
     int64_t row;
@@ -76,6 +86,12 @@ struct alignas(16) Ctl {
     uint64_t empty[kStages];           // stage released (one arrival per consumer warp)
     uint64_t rbar[kSlots];             // warp pairs published (one arrival per consumer warp)
     uint64_t fbar[kSlots];             // the slot read by the stats warp
+    uint64_t nbar;                     // the consumer warps' label counts published (folded reduction)
+    int nwarp[kConsumerWarps];         // each consumer warp's count of the batch's valid labels
+    long long n_all;                   // the batch's valid labels (stats warp)
+    float red_sum[kThreads / 32], red_comp[kThreads / 32];   // the last CTA's loss sum, per warp
+    int err;                           // first error code of the CTA (folded reduction)
+    int last;                          // this CTA finished last (folded reduction)
     int abort;
 };
 constexpr int kSmemBytes = kStages * kChunk + (int)sizeof(Ctl);
@@ -90,7 +106,30 @@ struct Args {
     int32_t* status;
     float eps;                         // label smoothing (k_ce_fwd_ring<S, true> only)
     uint64_t wait_ns;
+    int fold;                          // reduce the losses in this kernel (SUM / MEAN)
+    int red;                           // vce_reduction
+    float* loss_out;                   // the reduced loss (fold)
 };
+
+// Merge an error code into the low 16 bits of the status word, whose high bits may count
+// finished CTAs: the first code wins.  Each retry follows another thread's change of the word
+// (a CTA's count or a code), so the loop ends.
+__device__ __forceinline__ void status_merge(int32_t* status, int32_t code) {
+    int32_t old = *reinterpret_cast<volatile int32_t*>(status);
+    while ((old & 0xFFFF) == 0) {
+        const int32_t prev = atomicCAS(status, old, old | code);
+        if (prev == old) break;
+        old = prev;
+    }
+}
+
+// Fixed-order two-sum accumulation (the same steps as k_ce_reduce).
+__device__ __forceinline__ void fold_add(float& s, float& c, float x) {
+    const float t = s + x;
+    const float bp = t - s;
+    c += (s - (t - bp)) + (x - bp);
+    s = t;
+}
 
 __device__ __forceinline__ bool label_valid(const Args& a, int64_t t) {
     return t != a.ignore_index && t >= 0 && t < a.V;
@@ -135,11 +174,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_fwd_ring(const __grid_consta
             tc::mbar_init(&ctl.rbar[p], kGW);
             tc::mbar_init(&ctl.fbar[p], 1);
         }
+        tc::mbar_init(&ctl.nbar, kConsumerWarps);
         for (int i = 0; i < kInfoSlots; ++i) ctl.info[i] = RowInfo{-1, -1, 0};
         ctl.abort = 0;
+        ctl.err = 0;
+        ctl.n_all = 0;
         tc::fence_mbar_init();
     }
     __syncthreads();
+    // error codes: the status word itself, or (folded reduction) the CTA's word, merged at the end
+    int32_t* errp = a.fold ? &ctl.err : a.status;
 
     // The number of valid rows of this CTA (each warp counts for itself).
     auto count_valid = [&]() {
@@ -172,7 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_fwd_ring(const __grid_consta
                     const char* src = static_cast<const char*>(a.logits) + row * a.ld * (int64_t)sizeof(S);
                     for (int j = 0; j < nchunk; ++j) {
                         const int st = (int)(q % kStages);
-                        if (!tc::mbar_wait(&ctl.empty[st], ((q / kStages) & 1) ^ 1, abort_flag, a.status, kErrEmpty,
+                        if (!tc::mbar_wait(&ctl.empty[st], ((q / kStages) & 1) ^ 1, abort_flag, errp, kErrEmpty,
                                            a.wait_ns, kSuspendNs)) {
                             stop = true;
                             break;
@@ -217,14 +261,25 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_fwd_ring(const __grid_consta
                 if (row >= a.T || label_valid(a, t)) continue;
                 a.loss_rows[row] = (t == a.ignore_index) ? 0.f : __int_as_float(0x7FC00000);
                 a.row_stats[row] = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (t != a.ignore_index) atomicCAS(a.status, 0, (int32_t)VCE_ERR_LABEL);
+                if (t != a.ignore_index) atomicCAS(errp, 0, (int32_t)VCE_ERR_LABEL);
             }
         }
         __syncwarp();
         const int nv = count_valid();
+        // folded reduction: the batch's valid labels, counted by the consumer warps (MEAN weight)
+        float w_valid = 1.f;
+        if (a.fold) {
+            tc::mbar_wait(&ctl.nbar, 0, abort_flag, errp, kErrCount, a.wait_ns, kSuspendNs);
+            if (lane == 0) {
+                long long n = 0;
+                for (int w = 0; w < kConsumerWarps; ++w) n += ctl.nwarp[w];
+                ctl.n_all = n;
+                if (a.red == VCE_RED_MEAN) w_valid = n > 0 ? (float)(1.0 / (double)n) : 0.f;
+            }
+        }
         for (int e = 0; e < nv; ++e) {
             const int par = e % kUse;
-            tc::mbar_wait(&ctl.rbar[par], (e / kUse) & 1, abort_flag, a.status, kErrPartials, a.wait_ns,
+            tc::mbar_wait(&ctl.rbar[par], (e / kUse) & 1, abort_flag, errp, kErrPartials, a.wait_ns,
                           kSuspendNs);
             float m = lane < kGW ? ctl.red_m[par][lane] : -kInf;
             float s = lane < kGW ? ctl.red_s[par][lane] : 0.f;
@@ -243,8 +298,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_fwd_ring(const __grid_consta
                 tc::mbar_arrive(&ctl.fbar[par]);   // the slot may be rewritten
                 if (ri.row >= 0 && ri.row < a.T) {  // false only after an abort
                     float loss;
-                    a.row_stats[ri.row] = kSmooth ? ce_row_finish_smoothed(m, s, zt, tot, a.V, a.eps, &loss)
-                                                  : ce_row_finish(m, s, zt, &loss);
+                    float4 st4 = kSmooth ? ce_row_finish_smoothed(m, s, zt, tot, a.V, a.eps, &loss)
+                                         : ce_row_finish(m, s, zt, &loss);
+                    st4.w = w_valid;   // 1, or 1/N for a folded MEAN (else k_ce_reduce writes it)
+                    a.row_stats[ri.row] = st4;
                     a.loss_rows[ri.row] = loss;
                 }
             }
@@ -254,20 +311,31 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_fwd_ring(const __grid_consta
         // ---------------- consumers ----------------
         const int grp = warp / kGW, gw = warp % kGW;
         const int gtid = threadIdx.x - grp * kGT;   // thread index within the group
+        if (a.fold) {   // the batch's valid labels, consumer thread c taking rows c, c + kConsumers, ...
+            int n = 0;
+#pragma unroll 8
+            for (int64_t row = threadIdx.x; row < a.T; row += kConsumers) n += label_valid(a, a.labels[row]);
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) n += __shfl_xor_sync(0xFFFFFFFFu, n, off);
+            if (lane == 0) {
+                ctl.nwarp[warp] = n;
+                tc::mbar_arrive(&ctl.nbar);
+            }
+        }
         const int nv = count_valid();
         for (int e = grp; e < nv; e += kGroups) {
             const int par = e % kUse;
             const uint32_t q = (uint32_t)e * (uint32_t)nchunk;   // ring chunk of the row's first chunk
             // the slot was read for row e - kUse
             if (e >= kUse)
-                tc::mbar_wait(&ctl.fbar[par], ((e / kUse) & 1) ^ 1, abort_flag, a.status, kErrSlots, a.wait_ns,
+                tc::mbar_wait(&ctl.fbar[par], ((e / kUse) & 1) ^ 1, abort_flag, errp, kErrSlots, a.wait_ns,
                               kSuspendNs);
             float m = -kInf, s = 0.f, mb = 0.f, sz = 0.f;
             int tl = -1;
             for (int j = 0; j < nchunk; ++j) {
                 const uint32_t p = q + j;
                 const int st = (int)(p % kStages);
-                const bool ok = tc::mbar_wait(&ctl.full[st], (p / kStages) & 1, abort_flag, a.status, kErrFull,
+                const bool ok = tc::mbar_wait(&ctl.full[st], (p / kStages) & 1, abort_flag, errp, kErrFull,
                                               a.wait_ns, kSuspendNs);
                 if (j == 0) tl = ctl.info[e % kInfoSlots].tl;
                 if (ok) {
@@ -299,6 +367,46 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_fwd_ring(const __grid_consta
             if (lane == 0) tc::mbar_arrive(&ctl.rbar[par]);
         }
     }
+    if (!a.fold) return;
+
+    // ---------------- folded reduction ----------------
+    __syncthreads();   // every role is done: this CTA's rows are written
+    if (threadIdx.x == 0) {
+        if (ctl.err) status_merge(a.status, ctl.err);
+        __threadfence();
+        const int32_t prev = atomicAdd(a.status, 1 << 16);
+        ctl.last = ((prev >> 16) & 0xFFFF) == (int32_t)gridDim.x - 1;
+    }
+    __syncthreads();
+    if (!ctl.last) return;
+    __threadfence();
+    // Every row's loss (0 for an ignored row, NaN for a bad label), thread i taking rows i,
+    // i + kThreads, ...; pairs merged across lanes, then warps, in a fixed order.
+    float sum = 0.f, comp = 0.f;
+    for (int64_t i = threadIdx.x; i < a.T; i += kThreads) fold_add(sum, comp, __ldcg(a.loss_rows + i));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const float s2 = __shfl_xor_sync(0xFFFFFFFFu, sum, off);
+        const float c2 = __shfl_xor_sync(0xFFFFFFFFu, comp, off);
+        fold_add(sum, comp, s2);
+        comp += c2;
+    }
+    if (lane == 0) {
+        ctl.red_sum[warp] = sum;
+        ctl.red_comp[warp] = comp;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float s = 0.f, c = 0.f;
+        for (int w = 0; w < kThreads / 32; ++w) {
+            fold_add(s, c, ctl.red_sum[w]);
+            c += ctl.red_comp[w];
+        }
+        const double tot = isfinite(s) ? (double)s + (double)c : (double)s;
+        const long long n = ctl.n_all;
+        *a.loss_out = a.red == VCE_RED_MEAN ? (float)(tot / (double)n) : (float)tot;   // 0/0: NaN
+        atomicAnd(a.status, 0xFFFF);   // the counter bits go; the first error code stays
+    }
 }
 
 // Rows of two stages run in 2 groups (kUse * nchunk <= kStages), other rows in 1 (every
@@ -325,17 +433,22 @@ cudaError_t launch(const Args& args, int sms, cudaStream_t s) {
 VCE_DEBUG_READER(debug_word_ce_fwd_ring)
 
 cudaError_t launch_fwd_ring(vce_dtype dt, const void* logits, int64_t T, int64_t V, int64_t ld, const int64_t* labels,
-                            int64_t ignore_index, float eps, float* loss_rows, float* row_stats, int32_t* status,
-                            cudaStream_t s, bool* launched) {
+                            int64_t ignore_index, float eps, int red, float* loss_rows, float* loss_out,
+                            float* row_stats, int32_t* status, cudaStream_t s, bool* launched, bool* reduced) {
     using namespace fring;
     *launched = false;
+    *reduced = false;
     // 16-byte rows: every row starts on a 16-byte boundary and is whole 16-byte vectors.
     if (T < 1 || V % 8 || ld % 8 || !aligned(logits, 16) || V > (int64_t)1 << 30) return cudaSuccess;
+    const bool fold = red != VCE_RED_NONE && T <= kFoldMaxRows;
     Args args{logits, T, V, ld, labels, ignore_index, loss_rows, reinterpret_cast<float4*>(row_stats), status,
-              eps, tc::kWaitNs};
+              eps, tc::kWaitNs, fold ? 1 : 0, red, loss_out};
     const int sms = device_sm_count();
     const cudaError_t e = dt == VCE_BF16 ? launch<uint16_t>(args, sms, s) : launch<float>(args, sms, s);
-    if (e == cudaSuccess) *launched = true;
+    if (e == cudaSuccess) {
+        *launched = true;
+        *reduced = fold;
+    }
     return e;
 }
 

@@ -70,9 +70,12 @@ cudaError_t launch_bwd_ring(vce_dtype dt, vce_dtype gdt, const SegTable& tab, co
 // CE forward with each row streamed through a shared-memory stage ring (ce_fwd_ring.cu); eps:
 // label smoothing (0: none).  Sets *launched when it enqueued the kernel; leaves it false,
 // enqueuing nothing, when the layout does not fit (rows or leading dimension not multiples of
-// 8 elements, logits not 16-byte aligned).
+// 8 elements, logits not 16-byte aligned).  For red SUM / MEAN and at most 65536 rows the
+// kernel also reduces the losses into *loss_out and writes the rows' weights, and sets
+// *reduced; the status word must then be 0 when the kernel starts (its high bits count the
+// finished CTAs).
 cudaError_t launch_fwd_ring(vce_dtype dt, const void* logits, int64_t T, int64_t V, int64_t ld, const int64_t* labels,
-                            int64_t ignore_index, float eps, float* loss_rows, float* row_stats, int32_t* status,
-                            cudaStream_t s, bool* launched);
+                            int64_t ignore_index, float eps, int red, float* loss_rows, float* loss_out,
+                            float* row_stats, int32_t* status, cudaStream_t s, bool* launched, bool* reduced);
 
 }  // namespace vce
