@@ -411,6 +411,31 @@ def test_forward_ring_non_finite_and_bad_labels(vce):
             assert abs(lr[r] - ref["loss_rows"][r]) <= 1e-4 * ref["loss_rows"][r]
 
 
+@pytest.mark.parametrize("T,V", [(24, 20000), (152, 17000), (300, 40000)])
+def test_folded_reduction_repeats_exactly(vce, T, V):
+    """Rows of the forward ring reduced in-kernel by the CTA that finishes last, with every CTA
+    finishing within microseconds of the others: 40 calls into buffers refilled with NaN each
+    time give the same reduced loss, bit for bit, and the oracle's value."""
+    p = gen.custom(T, V, "bf16", seed=T + 1, std=2.0, n_ignore=2)
+    storage = p.full()
+    logits = to_device(storage, "bf16")
+    labels = torch.from_numpy(p.labels).cuda()
+    want = O.ce(O.widen(storage, "bf16"), p.labels, "mean")["loss_out"]
+    rows = torch.empty(T, dtype=torch.float32, device="cuda")
+    out = torch.empty(1, dtype=torch.float32, device="cuda")
+    stats = torch.empty(T, 4, dtype=torch.float32, device="cuda")
+    status = torch.empty(1, dtype=torch.int32, device="cuda")
+    got = []
+    for _ in range(40):
+        rows.fill_(float("nan"))
+        out.fill_(float("nan"))
+        vce.ce_forward(logits, labels, reduction="mean", loss_rows=rows, loss_out=out, row_stats=stats, status=status)
+        got.append(out.item())
+        assert vce.vce_get_status(status) == 0
+    assert all(g == got[0] for g in got), got
+    G.check_reduced(got[0], want)
+
+
 @pytest.mark.parametrize("reduction", ["mean", "sum", "none"])
 def test_forward_ring_bad_labels_and_reduction(vce, reduction):
     """Rows of 40 KB (the stage ring, two consumer groups; for SUM and MEAN it also reduces the

@@ -1,0 +1,111 @@
+// The loss reduction folded into the end of a ring kernel (ce_fwd_ring.cu: ce_forward;
+// ce_ring.cu: ce_forward_backward), for SUM and MEAN over at most kMaxRows rows.
+//
+// Method: torchtitan PR #5723 "[loss] fix softmax collapse with improved ce perf" -- the loss is
+// the sum of the rows' NLL, over the N rows with a valid label for MEAN (ignored rows weigh 0).
+//
+// Protocol.  The caller clears the status word before the kernel.  Every CTA counts the
+// batch's valid labels itself (count_valid_strided, while its first copies are in flight), so
+// each row's weight 1/N is known where the row is finished.  Within the kernel, error codes
+// collect in a word of the CTA's shared memory.  At the end each CTA merges its code into the
+// low 16 bits of the status word (the first code wins) and adds one to a count of finished CTAs
+// in the high 16 bits; the CTA that finds itself last sums every row's loss in a fixed order
+// (thread i takes rows i, i + NT, ...; lanes, then warps, merged in order) as an fp32 (sum,
+// compensation) pair with two-sum steps, as k_ce_reduce does, writes the reduced loss and
+// clears the count.  The sum of an ignored row's +0 loss adds nothing; a bad label's NaN
+// makes the reduced loss NaN.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "vce.h"
+
+namespace vce {
+namespace fold {
+
+constexpr int64_t kMaxRows = 65536;   // every CTA reads every label: at most 512 KB of them
+
+// Merge an error code into the low 16 bits of the status word, whose high bits may count
+// finished CTAs: the first code wins.  Each retry follows another thread's change of the word
+// (a CTA's count or a code), so the loop ends.
+__device__ __forceinline__ void status_merge(int32_t* status, int32_t code) {
+    int32_t old = *reinterpret_cast<volatile int32_t*>(status);
+    while ((old & 0xFFFF) == 0) {
+        const int32_t prev = atomicCAS(status, old, old | code);
+        if (prev == old) break;
+        old = prev;
+    }
+}
+
+// s + x = t + e exactly (Knuth's TwoSum); e goes into the compensation c.
+__device__ __forceinline__ void add(float& s, float& c, float x) {
+    const float t = s + x;
+    const float bp = t - s;
+    c += (s - (t - bp)) + (x - bp);
+    s = t;
+}
+
+// This thread's count of valid labels among rows first, first + step, ... (eight loads in
+// flight).
+__device__ __forceinline__ int count_valid_strided(const int64_t* labels, int64_t T, int64_t V,
+                                                   int64_t ignore_index, int64_t first, int64_t step) {
+    int n = 0;
+#pragma unroll 8
+    for (int64_t row = first; row < T; row += step) {
+        const int64_t t = labels[row];
+        n += (t != ignore_index && t >= 0 && t < V) ? 1 : 0;
+    }
+    return n;
+}
+
+// Called by all NT threads of the block once every output of its rows is written (and, in a
+// cluster, after the closing cluster barrier).  err: the CTA's error word in shared memory;
+// n_all: the batch's valid labels; sm_sum, sm_comp: NT / 32 floats of shared memory; sm_last:
+// one int of shared memory.
+template <int NT>
+__device__ __forceinline__ void finish(int32_t* status, const int* err, const float* loss_rows, int64_t T,
+                                       long long n_all, int red, float* loss_out, float* sm_sum, float* sm_comp,
+                                       int* sm_last) {
+    // Every thread's own stores (the rows' losses, weights, gradients) are made visible device-
+    // wide before the count moves: a fence orders only the fencing thread's writes, and the block
+    // barrier does not wait for other warps' global stores to be performed.
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        if (*err) status_merge(status, *err);
+        const int32_t prev = atomicAdd(status, 1 << 16);
+        *sm_last = ((prev >> 16) & 0xFFFF) == (int32_t)gridDim.x - 1;
+    }
+    __syncthreads();
+    if (!*sm_last) return;
+    __threadfence();
+    float sum = 0.f, comp = 0.f;
+    for (int64_t i = threadIdx.x; i < T; i += NT) add(sum, comp, __ldcg(loss_rows + i));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const float s2 = __shfl_xor_sync(0xFFFFFFFFu, sum, off);
+        const float c2 = __shfl_xor_sync(0xFFFFFFFFu, comp, off);
+        add(sum, comp, s2);
+        comp += c2;
+    }
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (lane == 0) {
+        sm_sum[warp] = sum;
+        sm_comp[warp] = comp;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float s = 0.f, c = 0.f;
+        for (int w = 0; w < NT / 32; ++w) {
+            add(s, c, sm_sum[w]);
+            c += sm_comp[w];
+        }
+        const double tot = isfinite(s) ? (double)s + (double)c : (double)s;
+        *loss_out = red == VCE_RED_MEAN ? (float)(tot / (double)n_all) : (float)tot;   // 0/0: NaN
+        atomicAnd(status, 0xFFFF);   // the count goes; the first error code stays
+    }
+}
+
+}  // namespace fold
+}  // namespace vce

@@ -14,7 +14,8 @@
 // in and V*e_g out per row, instead of 2*V*e in and V*e_g out for the two separate calls.
 //
 //   k_ce_count_valid  one block: 1/N for the mean, parked in loss_out[0] until k_ce_reduce
-//                     replaces it by the mean loss
+//                     replaces it by the mean loss (unless the ring kernel counts N and reduces
+//                     the losses itself: SUM / MEAN over at most 65536 rows)
 //   k_ce_fused        one row per block iteration: forward stream, statistics, backward stream
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -173,20 +174,31 @@ extern "C" int ce_forward_backward_ls(const void* logits, vce_dtype dt, int64_t 
     if (red != VCE_RED_NONE && !aligned(loss_out, 4)) return VCE_ERR_ALIGN;
     int rc = require_sm100();
     if (rc) return rc;
-    // the mean's weight first (it also clears the status word); otherwise clear it here
-    if (T > 0 && red == VCE_RED_MEAN) {
+    // The ring kernel counts N and reduces the losses itself where it can (SUM / MEAN, at most
+    // 65536 rows): the status word is cleared for it.  Otherwise the mean's weight 1/N comes
+    // first (k_ce_count_valid, which also clears the status word) and k_ce_reduce last.
+    const bool ring_reduces = T > 0 && fused_ring_reduces(red, T) &&
+                              fused_ring_layout_ok(dt, T, V, ld, ld_grad, logits, grad_logits);
+    auto count_first = [&]() {
         k_ce_count_valid<1024><<<1, 1024, 0, s>>>(labels, T, V, ignore_index, loss_out, status);
-        if (cudaGetLastError() != cudaSuccess) return VCE_ERR_CUDA;
+        return cudaGetLastError() == cudaSuccess;
+    };
+    if (T > 0 && red == VCE_RED_MEAN && !ring_reduces) {
+        if (!count_first()) return VCE_ERR_CUDA;
     } else if (cudaMemsetAsync(status, 0, sizeof(int32_t), s) != cudaSuccess) {
         return VCE_ERR_CUDA;
     }
+    bool reduced = false;
     if (T > 0) {
         const float eps = label_smoothing;
         // The row held in shared memory where the layout allows it, else the L2 re-read.
         bool launched = false;
         cudaError_t e = launch_fused_ring(dt, grad_dt, logits, T, V, ld, labels, ignore_index, red, grad_output,
                                           loss_out, loss_rows, row_stats, grad_logits, ld_grad, status, s, &launched,
-                                          eps);
+                                          eps, 2000000000ull, 0, ring_reduces ? &reduced : nullptr, loss_out);
+        // no cluster fitted after all: the fallback needs the mean's weight first
+        if (e == cudaSuccess && !launched && ring_reduces && red == VCE_RED_MEAN && !count_first())
+            return VCE_ERR_CUDA;
         if (e == cudaSuccess && !launched) {
             const int nt = pick_threads(V * (int64_t)es);
             if (dt == VCE_BF16 && grad_dt == VCE_BF16)
@@ -207,7 +219,7 @@ extern "C" int ce_forward_backward_ls(const void* logits, vce_dtype dt, int64_t 
         }
         if (e != cudaSuccess) return VCE_ERR_CUDA;
     }
-    if (red != VCE_RED_NONE &&
+    if (red != VCE_RED_NONE && !reduced &&
         launch_loss_reduce(loss_rows, labels, T, V, ignore_index, red, loss_out, row_stats, s) != cudaSuccess)
         return VCE_ERR_CUDA;
     return VCE_OK;

@@ -28,14 +28,10 @@
 // and 0.0613 on one block per row.  Rows of one stage in 4 groups lost to one warp per row:
 // 8192 x 16000, 0.102 against 0.070 ms.)
 //
-// The loss reduction folded in (Args::fold, for SUM / MEAN with at most kFoldMaxRows rows): the
-// consumer warps count every valid label of the batch at the start, while the first copies are
-// in flight, so the stats warp writes each row's weight 1/N itself; at the end each CTA adds one
-// to a counter in the high 16 bits of the status word (which the caller cleared), and the CTA
-// that finds itself last sums every row's loss in a fixed order (fp32 two-sum pairs, as
-// k_ce_reduce) and writes the reduced loss.  Error codes stay in the low 16 bits: within the
-// kernel they go to a word in shared memory and are merged into the status word at the end,
-// first code wins; the last CTA clears the counter bits.  No separate reduction launch.
+// The loss reduction folded in (Args::fold, for SUM / MEAN with at most fold::kMaxRows rows;
+// ce_fold.cuh): the consumer warps count every valid label of the batch at the start, while the
+// first copies are in flight, so the stats warp writes each row's weight 1/N itself, and the
+// CTA that finishes last sums the rows' losses.  No separate reduction launch.
 //
 // Every wait is bounded (2 s); a wait that gives up writes its code to the status word (105
 // free stage, 106 loaded stage, 108 warp partials, 110 free slots) and sets the CTA's abort
@@ -47,6 +43,7 @@
 #include <algorithm>
 
 #include "ce_segments.h"
+#include "ce_fold.cuh"
 #include "ce_stage.cuh"
 #include "vce.h"
 #include "vce_async.cuh"
@@ -67,7 +64,6 @@ constexpr int kVecPerThread = kChunk / 16 / kConsumers;   // per 4-vector batch 
 constexpr uint32_t kSuspendNs = 0;       // plain polls (a suspend hint measured no faster here)
 constexpr int kSlots = 4;                // hand-off slots: consumers run up to kSlots rows ahead of the stats warp
 constexpr int kInfoSlots = 16;           // > the rows the producer can run ahead of the stats warp (kStages + kSlots)
-constexpr int64_t kFoldMaxRows = 65536;  // the folded reduction: every CTA counts every label (at most 512 KB)
 static_assert(kVecPerThread * kConsumers * 16 == kChunk, "every consumer takes the same whole vectors of a stage");
 static_assert((kConsumerWarps & (kConsumerWarps - 1)) == 0 && kConsumerWarps <= 32, "warp pairs merge in one warp");
 enum { kErrEmpty = 105, kErrFull = 106, kErrPartials = 108, kErrSlots = 110, kErrGroups = 111, kErrCount = 112 };
@@ -110,26 +106,6 @@ struct Args {
     int red;                           // vce_reduction
     float* loss_out;                   // the reduced loss (fold)
 };
-
-// Merge an error code into the low 16 bits of the status word, whose high bits may count
-// finished CTAs: the first code wins.  Each retry follows another thread's change of the word
-// (a CTA's count or a code), so the loop ends.
-__device__ __forceinline__ void status_merge(int32_t* status, int32_t code) {
-    int32_t old = *reinterpret_cast<volatile int32_t*>(status);
-    while ((old & 0xFFFF) == 0) {
-        const int32_t prev = atomicCAS(status, old, old | code);
-        if (prev == old) break;
-        old = prev;
-    }
-}
-
-// Fixed-order two-sum accumulation (the same steps as k_ce_reduce).
-__device__ __forceinline__ void fold_add(float& s, float& c, float x) {
-    const float t = s + x;
-    const float bp = t - s;
-    c += (s - (t - bp)) + (x - bp);
-    s = t;
-}
 
 __device__ __forceinline__ bool label_valid(const Args& a, int64_t t) {
     return t != a.ignore_index && t >= 0 && t < a.V;
@@ -312,9 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_fwd_ring(const __grid_consta
         const int grp = warp / kGW, gw = warp % kGW;
         const int gtid = threadIdx.x - grp * kGT;   // thread index within the group
         if (a.fold) {   // the batch's valid labels, consumer thread c taking rows c, c + kConsumers, ...
-            int n = 0;
-#pragma unroll 8
-            for (int64_t row = threadIdx.x; row < a.T; row += kConsumers) n += label_valid(a, a.labels[row]);
+            int n = fold::count_valid_strided(a.labels, a.T, a.V, a.ignore_index, threadIdx.x, kConsumers);
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) n += __shfl_xor_sync(0xFFFFFFFFu, n, off);
             if (lane == 0) {
@@ -370,47 +344,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_fwd_ring(const __grid_consta
     if (!a.fold) return;
 
     // ---------------- folded reduction ----------------
-    __syncthreads();   // every role is done: this CTA's rows are written
-    if (threadIdx.x == 0) {
-        if (ctl.err) status_merge(a.status, ctl.err);
-        __threadfence();
-        const int32_t prev = atomicAdd(a.status, 1 << 16);
-        ctl.last = ((prev >> 16) & 0xFFFF) == (int32_t)gridDim.x - 1;
-    }
-    __syncthreads();
-    if (!ctl.last) return;
-    __threadfence();
-    // Every row's loss (0 for an ignored row, NaN for a bad label), thread i taking rows i,
-    // i + kThreads, ...; pairs merged across lanes, then warps, in a fixed order.
-    float sum = 0.f, comp = 0.f;
-    for (int64_t i = threadIdx.x; i < a.T; i += kThreads) fold_add(sum, comp, __ldcg(a.loss_rows + i));
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-        const float s2 = __shfl_xor_sync(0xFFFFFFFFu, sum, off);
-        const float c2 = __shfl_xor_sync(0xFFFFFFFFu, comp, off);
-        fold_add(sum, comp, s2);
-        comp += c2;
-    }
-    if (lane == 0) {
-        ctl.red_sum[warp] = sum;
-        ctl.red_comp[warp] = comp;
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        float s = 0.f, c = 0.f;
-        for (int w = 0; w < kThreads / 32; ++w) {
-            fold_add(s, c, ctl.red_sum[w]);
-            c += ctl.red_comp[w];
-        }
-        const double tot = isfinite(s) ? (double)s + (double)c : (double)s;
-        const long long n = ctl.n_all;
-        *a.loss_out = a.red == VCE_RED_MEAN ? (float)(tot / (double)n) : (float)tot;   // 0/0: NaN
-        atomicAnd(a.status, 0xFFFF);   // the counter bits go; the first error code stays
-    }
+    fold::finish<kThreads>(a.status, &ctl.err, a.loss_rows, a.T, ctl.n_all, a.red, a.loss_out, ctl.red_sum,
+                           ctl.red_comp, &ctl.last);
 }
 
-// Rows of two stages run in 2 groups (kUse * nchunk <= kStages), other rows in 1 (every
-// consumer warp on every stage).
 template <typename S, int kGroups>
 cudaError_t launch_groups(const Args& args, int sms, cudaStream_t s) {
     auto kern = args.eps > 0.f ? k_ce_fwd_ring<S, true, kGroups> : k_ce_fwd_ring<S, false, kGroups>;
@@ -440,14 +377,14 @@ cudaError_t launch_fwd_ring(vce_dtype dt, const void* logits, int64_t T, int64_t
     *reduced = false;
     // 16-byte rows: every row starts on a 16-byte boundary and is whole 16-byte vectors.
     if (T < 1 || V % 8 || ld % 8 || !aligned(logits, 16) || V > (int64_t)1 << 30) return cudaSuccess;
-    const bool fold = red != VCE_RED_NONE && T <= kFoldMaxRows;
+    const bool in_kernel = red != VCE_RED_NONE && T <= fold::kMaxRows;
     Args args{logits, T, V, ld, labels, ignore_index, loss_rows, reinterpret_cast<float4*>(row_stats), status,
-              eps, tc::kWaitNs, fold ? 1 : 0, red, loss_out};
+              eps, tc::kWaitNs, in_kernel ? 1 : 0, red, loss_out};
     const int sms = device_sm_count();
     const cudaError_t e = dt == VCE_BF16 ? launch<uint16_t>(args, sms, s) : launch<float>(args, sms, s);
     if (e == cudaSuccess) {
         *launched = true;
-        *reduced = fold;
+        *reduced = in_kernel;
     }
     return e;
 }

@@ -31,6 +31,12 @@
 // the CTA's sequence: a slot of one parity is rewritten two rows later, after every reader of
 // it has arrived on a barrier the writer waits for.
 //
+// The loss reduction folded in (Args::fold, for SUM / MEAN over at most fold::kMaxRows rows;
+// ce_fold.cuh): the consumer warps count the batch's valid labels before their first row, so the
+// stats warp has 1/N for the row weights and gradient coefficients without a counting kernel
+// before this one, and the CTA that finishes last sums the rows' losses; no reduction kernel
+// after it either.
+//
 // Every wait is bounded (2 s).  A wait that gives up writes its code to the status word
 // (105 free stage, 106 loaded stage, 107 cluster exchange, 108 warp partials, 109 row
 // coefficients) and sets the CTA's abort flag; the CTA then keeps every arrival (stage
@@ -45,6 +51,7 @@
 
 #include "ce_segments.h"
 #include "vce.h"
+#include "ce_fold.cuh"
 #include "ce_stage.cuh"
 #include "vce_async.cuh"
 #include "vce_device.cuh"
@@ -92,6 +99,12 @@ struct alignas(16) Ctl {
     uint64_t xbar[2];                  // cluster pairs stored (one arrival per CTA)
     uint64_t rbar[2];                  // warp pairs published (one arrival per consumer warp)
     uint64_t cbar[2];                  // coefficients published (the stats warp)
+    uint64_t nbar;                     // the consumer warps' label counts published (folded reduction)
+    int nwarp[kConsumerWarps];         // each consumer warp's count of the batch's valid labels
+    long long n_all;                   // the batch's valid labels (stats warp)
+    float red_sum[kThreads / 32], red_comp[kThreads / 32];   // the last CTA's loss sum, per warp
+    int err;                           // first error code of the CTA (folded reduction)
+    int last;                          // this CTA finished last (folded reduction)
     int abort;
 };
 constexpr int kSmemBytes = kStages * kChunk + (int)sizeof(Ctl);
@@ -113,6 +126,8 @@ struct Args {
     uint64_t wait_ns;                  // bound of every wait
     uint32_t tx_extra;                 // 0; > 0 only in the give-up test (a stage never completes)
     float eps;                         // label smoothing (k_ce_fused_ring<S, O, C, true> only)
+    int fold;                          // reduce the losses in this kernel (SUM / MEAN; inv_n unused)
+    float* loss_out;                   // the reduced loss (fold)
 };
 
 // ---- cluster and bulk-copy primitives (inline PTX) -----------------------------------------
@@ -212,12 +227,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_fused_ring(const __grid_cons
             tc::mbar_init(&ctl.rbar[p], kConsumerWarps);
             tc::mbar_init(&ctl.cbar[p], 1);
         }
+        tc::mbar_init(&ctl.nbar, kConsumerWarps);
         for (int i = 0; i < kInfoSlots; ++i) ctl.info[i] = RowInfo{-1, -1, 0};
         ctl.abort = 0;
+        ctl.err = 0;
+        ctl.n_all = 0;
         tc::fence_mbar_init();
     }
     if (C > 1) cluster_sync();   // peers arrive on these barriers from now on
     else __syncthreads();
+    // error codes: the status word itself, or (folded reduction) the CTA's word, merged at the end
+    int32_t* errp = a.fold ? &ctl.err : a.status;
 
     // The number of valid rows of this cluster (each warp counts for itself).
     auto count_valid = [&]() {
@@ -241,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_fused_ring(const __grid_cons
                 const char* src = static_cast<const char*>(a.logits) + (row * a.ld + c0) * (int64_t)sizeof(S);
                 for (int j = 0; j < nchunk; ++j) {
                     const int st = (int)(q % kStages);
-                    if (!tc::mbar_wait(&ctl.empty[st], ((q / kStages) & 1) ^ 1, abort_flag, a.status, kErrEmpty,
+                    if (!tc::mbar_wait(&ctl.empty[st], ((q / kStages) & 1) ^ 1, abort_flag, errp, kErrEmpty,
                                        a.wait_ns, kSuspendRole))
                         break;
                     const uint32_t nb = (uint32_t)min(kChunk, bytes - j * kChunk);
@@ -263,12 +283,21 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_fused_ring(const __grid_cons
         __syncwarp();
     } else if (warp == kStatsWarp) {
         // ---------------- row statistics ----------------
-        const float w_valid = (a.red == VCE_RED_MEAN) ? *a.inv_n : 1.f;
+        float w_valid = 1.f;   // the row weight: 1/N for MEAN
+        if (a.fold) {   // N from the consumer warps' counts
+            tc::mbar_wait(&ctl.nbar, 0, abort_flag, errp, kErrPartials, a.wait_ns, kSuspendRole);
+            long long n = 0;
+            for (int k = 0; k < kConsumerWarps; ++k) n += ctl.nwarp[k];
+            if (lane == 0) ctl.n_all = n;
+            if (a.red == VCE_RED_MEAN) w_valid = n > 0 ? (float)(1.0 / (double)n) : 0.f;   // as k_ce_reduce
+        } else if (a.red == VCE_RED_MEAN) {
+            w_valid = *a.inv_n;
+        }
         const int nv = count_valid();
         for (int e = 0; e < nv; ++e) {
             const int par = e & 1;
             const uint32_t ph = (e >> 1) & 1;
-            tc::mbar_wait(&ctl.rbar[par], ph, abort_flag, a.status, kErrPartials, a.wait_ns, kSuspendRole);
+            tc::mbar_wait(&ctl.rbar[par], ph, abort_flag, errp, kErrPartials, a.wait_ns, kSuspendRole);
             float m = lane < kConsumerWarps ? ctl.red_m[par][lane] : -kInf;
             float s = lane < kConsumerWarps ? ctl.red_s[par][lane] : 0.f;
 #pragma unroll
@@ -291,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_fused_ring(const __grid_cons
                         if (kSmooth) st_peer1(peer_addr(&ctl.slot_z[par][rank], r), sz);
                     }
                     for (uint32_t r = 0; r < (uint32_t)C; ++r) arrive_peer(peer_addr(&ctl.xbar[par], r));
-                    wait_exchange(&ctl.xbar[par], ph, abort_flag, a.status, a.wait_ns);
+                    wait_exchange(&ctl.xbar[par], ph, abort_flag, errp, a.wait_ns);
                     M = -kInf;
                     Ssum = 0.f;
                     tot = 0.f;
@@ -321,6 +350,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_fused_ring(const __grid_cons
     } else {
         // ---------------- consumers ----------------
         const int tid = threadIdx.x;
+        if (a.fold) {   // the batch's valid labels, consumer thread c taking rows c, c + kConsumers, ...
+            int n = fold::count_valid_strided(a.labels, a.T, a.V, a.ignore_index, tid, kConsumers);
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) n += __shfl_xor_sync(0xFFFFFFFFu, n, off);
+            if (lane == 0) {
+                ctl.nwarp[warp] = n;
+                tc::mbar_arrive(&ctl.nbar);
+            }
+        }
 
         // Rows whose label is ignore_index or invalid: gradient +0.0 by selection, logits unread.
         // Each warp reads the labels of 32 of the cluster's rows at once and zero-fills the
@@ -337,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_fused_ring(const __grid_cons
                 if (rank == 0 && lane == 0) {
                     a.loss_rows[row] = (t == a.ignore_index) ? 0.f : __int_as_float(0x7FC00000);
                     a.row_stats[row] = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (t != a.ignore_index) atomicCAS(a.status, 0, (int32_t)VCE_ERR_LABEL);
+                    if (t != a.ignore_index) atomicCAS(errp, 0, (int32_t)VCE_ERR_LABEL);
                 }
                 if (!dbg::ok(c0 + w <= a.ld_g, dbg::kCols)) continue;
                 O* grow = static_cast<O*>(a.grad) + row * a.ld_g + c0;
@@ -353,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_fused_ring(const __grid_cons
             for (int j = j0; j < j1; ++j) {
                 const uint32_t p = q0 + j;
                 const int st = (int)(p % kStages);
-                const bool ok = tc::mbar_wait(&ctl.full[st], (p / kStages) & 1, abort_flag, a.status, kErrFull,
+                const bool ok = tc::mbar_wait(&ctl.full[st], (p / kStages) & 1, abort_flag, errp, kErrFull,
                                               a.wait_ns, kSuspendConsumer);
                 if (j == 0) ri = ctl.info[e % kInfoSlots];
                 if (!ok) continue;
@@ -396,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_fused_ring(const __grid_cons
             if (more) forward(q + nchunk, 0, pre, e + 1, ri2, m2, s2, mb2, sz2);
 
             // the row's gradient, each stage released once this warp is done with it
-            tc::mbar_wait(&ctl.cbar[par], (e >> 1) & 1, abort_flag, a.status, kErrCoefs, a.wait_ns, kSuspendConsumer);
+            tc::mbar_wait(&ctl.cbar[par], (e >> 1) & 1, abort_flag, errp, kErrCoefs, a.wait_ns, kSuspendConsumer);
             const float4 cf = ctl.coefs[par];
             const bool in_range = ri.row >= 0 && ri.row < a.T;   // false only after an abort
             O* grow = static_cast<O*>(a.grad) + (in_range ? ri.row : 0) * a.ld_g + c0;
@@ -429,6 +467,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_fused_ring(const __grid_cons
         }
     }
     if (C > 1) cluster_sync();   // no CTA leaves while a peer may still write into its shared memory
+    if (a.fold)
+        fold::finish<kThreads>(a.status, &ctl.err, a.loss_rows, a.T, ctl.n_all, a.red, a.loss_out, ctl.red_sum,
+                               ctl.red_comp, &ctl.last);
 }
 
 template <typename S, typename O, int C, bool kSmooth>
@@ -490,31 +531,59 @@ cudaError_t launch_cs(int C, const Args& args, int sms, cudaStream_t s, bool* la
 
 VCE_DEBUG_READER(debug_word_ce_ring)
 
-cudaError_t launch_fused_ring(vce_dtype dt, vce_dtype gdt, const void* logits, int64_t T, int64_t V, int64_t ld,
-                              const int64_t* labels, int64_t ignore_index, int red, const float* grad_output,
-                              const float* inv_n, float* loss_rows, float* row_stats, void* grad, int64_t ld_g,
-                              int32_t* status, cudaStream_t s, bool* launched, float eps, uint64_t wait_ns,
-                              uint32_t tx_extra) {
+namespace {
+// The cluster size and slice (columns per CTA, a multiple of 8) for rows of V entries of es
+// bytes: the smallest cluster whose slices fit kSliceStages stages; C > kMaxCluster if none.
+void cluster_shape(int64_t V, int64_t es, int* C_out, int64_t* slice_out) {
     using namespace ring;
-    *launched = false;
-    // 16-byte rows and slices: every row and slice starts on a 16-byte boundary, and each slice
-    // is whole 16-byte vectors of input and output.
-    if (T < 1 || V % 8 || ld % 8 || ld_g % 8 || !aligned(logits, 16) || !aligned(grad, 16)) return cudaSuccess;
-    const int64_t es = dt == VCE_BF16 ? 2 : 4;
     int C = 1;
     int64_t slice = V;
     for (; C <= kMaxCluster; C *= 2) {
         slice = ((V + C - 1) / C + 7) / 8 * 8;
         if (slice * es <= (int64_t)kSliceStages * kChunk) break;
     }
-    if (C > kMaxCluster) return cudaSuccess;   // rows too long for an 8-CTA cluster
+    *C_out = C;
+    *slice_out = slice;
+}
+}  // namespace
+
+bool fused_ring_layout_ok(vce_dtype dt, int64_t T, int64_t V, int64_t ld, int64_t ld_g, const void* logits,
+                          const void* grad) {
+    // 16-byte rows and slices: every row and slice starts on a 16-byte boundary, and each slice
+    // is whole 16-byte vectors of input and output.
+    if (T < 1 || V % 8 || ld % 8 || ld_g % 8 || !aligned(logits, 16) || !aligned(grad, 16)) return false;
+    int C;
+    int64_t slice;
+    cluster_shape(V, dt == VCE_BF16 ? 2 : 4, &C, &slice);
+    return C <= ring::kMaxCluster;
+}
+
+bool fused_ring_reduces(int red, int64_t T) { return red != VCE_RED_NONE && T >= 1 && T <= fold::kMaxRows; }
+
+cudaError_t launch_fused_ring(vce_dtype dt, vce_dtype gdt, const void* logits, int64_t T, int64_t V, int64_t ld,
+                              const int64_t* labels, int64_t ignore_index, int red, const float* grad_output,
+                              const float* inv_n, float* loss_rows, float* row_stats, void* grad, int64_t ld_g,
+                              int32_t* status, cudaStream_t s, bool* launched, float eps, uint64_t wait_ns,
+                              uint32_t tx_extra, bool* reduced, float* loss_out) {
+    using namespace ring;
+    *launched = false;
+    if (reduced) *reduced = false;
+    if (!fused_ring_layout_ok(dt, T, V, ld, ld_g, logits, grad)) return cudaSuccess;
+    int C;
+    int64_t slice;
+    cluster_shape(V, dt == VCE_BF16 ? 2 : 4, &C, &slice);
+    const bool in_kernel = reduced && loss_out && fused_ring_reduces(red, T);
     Args args{logits, T,   V,    ld,   labels, ignore_index, red,   grad_output, inv_n,
-              loss_rows, reinterpret_cast<float4*>(row_stats), grad, ld_g, status, slice, wait_ns, tx_extra, eps};
+              loss_rows, reinterpret_cast<float4*>(row_stats), grad, ld_g, status, slice, wait_ns, tx_extra, eps,
+              in_kernel ? 1 : 0, loss_out};
     const int sms = device_sm_count();
-    if (dt == VCE_BF16 && gdt == VCE_BF16) return launch_cs<uint16_t, uint16_t>(C, args, sms, s, launched);
-    if (dt == VCE_BF16) return launch_cs<uint16_t, float>(C, args, sms, s, launched);
-    if (gdt == VCE_BF16) return launch_cs<float, uint16_t>(C, args, sms, s, launched);
-    return launch_cs<float, float>(C, args, sms, s, launched);
+    cudaError_t e;
+    if (dt == VCE_BF16 && gdt == VCE_BF16) e = launch_cs<uint16_t, uint16_t>(C, args, sms, s, launched);
+    else if (dt == VCE_BF16) e = launch_cs<uint16_t, float>(C, args, sms, s, launched);
+    else if (gdt == VCE_BF16) e = launch_cs<float, uint16_t>(C, args, sms, s, launched);
+    else e = launch_cs<float, float>(C, args, sms, s, launched);
+    if (e == cudaSuccess && *launched && reduced) *reduced = in_kernel;
+    return e;
 }
 
 }  // namespace vce

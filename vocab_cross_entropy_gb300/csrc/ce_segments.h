@@ -48,16 +48,25 @@ cudaError_t launch_ce_bwd(vce_dtype dt, vce_dtype gdt, int nt, const SegTable& t
 
 // One-pass forward+backward with each row held in shared memory between its two passes
 // (ce_ring.cu).  Sets *launched when it enqueued the kernel; leaves it false, enqueuing
-// nothing, when the shape or layout does not fit (rows or leading dimensions not multiples of
-// 8 elements, pointers not 16-byte aligned, rows too long for an 8-CTA cluster).  eps: label
-// smoothing (0: none).  wait_ns
-// bounds every wait of the kernel; tx_extra > 0 (tests only) announces that many bytes more
-// per stage than each copy delivers, so no stage completes and the waits give up.
+// nothing, when the shape or layout does not fit (fused_ring_layout_ok false, or no cluster
+// fits).  eps: label smoothing (0: none).  wait_ns bounds every wait of the kernel; tx_extra > 0
+// (tests only) announces that many bytes more per stage than each copy delivers, so no stage
+// completes and the waits give up.  reduced != null asks the kernel to reduce the losses into
+// *loss_out itself (SUM / MEAN over at most 65536 rows; inv_n is then unused and the status word
+// must be 0 when the kernel starts) and reports whether it does.
 cudaError_t launch_fused_ring(vce_dtype dt, vce_dtype gdt, const void* logits, int64_t T, int64_t V, int64_t ld,
                               const int64_t* labels, int64_t ignore_index, int red, const float* grad_output,
                               const float* inv_n, float* loss_rows, float* row_stats, void* grad, int64_t ld_g,
                               int32_t* status, cudaStream_t s, bool* launched, float eps = 0.f,
-                              uint64_t wait_ns = 2000000000ull, uint32_t tx_extra = 0);
+                              uint64_t wait_ns = 2000000000ull, uint32_t tx_extra = 0, bool* reduced = nullptr,
+                              float* loss_out = nullptr);
+
+// Whether launch_fused_ring takes this layout: rows and leading dimensions of whole 16-byte
+// vectors, both buffers 16-byte aligned, rows short enough for an 8-CTA cluster; and whether
+// it reduces the losses itself for `red` over T rows.
+bool fused_ring_layout_ok(vce_dtype dt, int64_t T, int64_t V, int64_t ld, int64_t ld_g, const void* logits,
+                          const void* grad);
+bool fused_ring_reduces(int red, int64_t T);
 
 // The gradient of every (chunk, row) segment of `tab` with each segment streamed through a
 // shared-memory stage ring (ce_bwd_ring.cu): the same entries as launch_ce_bwd.  Leaves
