@@ -436,6 +436,32 @@ def test_folded_reduction_repeats_exactly(vce, T, V):
     G.check_reduced(got[0], want)
 
 
+def test_forward_ring_beyond_the_folded_reduction(vce):
+    """65540 rows of 32 KB + 16 B: more rows than the ring reduces in-kernel, so k_ce_reduce runs
+    after it.  The MEAN call's loss is the fp64 mean of the same kernel's per-row losses (its
+    NONE call), its weights 1/N, and a bad label still sets the status."""
+    T, V = 65540, 16392
+    p = gen.custom(T, V, "bf16", seed=77, std=2.0, n_ignore=650)
+    logits = to_device(p.full(), "bf16")
+    labels = torch.from_numpy(p.labels).cuda()
+    _, rows_none, _, st_none = vce.ce_forward(logits, labels, -100, "none")
+    out, rows, stats, status = vce.ce_forward(logits, labels, -100, "mean")
+    torch.cuda.synchronize()
+    assert vce.vce_get_status(status) == 0 and vce.vce_get_status(st_none) == 0
+    assert torch.equal(rows, rows_none)
+    valid = p.labels != -100
+    n = int(valid.sum())
+    want = float(np.sum(rows_none.cpu().numpy().astype(np.float64)[valid])) / n
+    assert abs(out.item() - want) <= 1e-6 * abs(want)
+    w = stats.cpu().numpy()[:, 3]
+    assert np.all(w[valid] == np.float32(1.0 / n)) and np.all(w[~valid] == 0)
+    bad = p.labels.copy()
+    bad[T - 1] = V
+    out2, _, _, status2 = vce.ce_forward(logits, torch.from_numpy(bad).cuda(), -100, "sum")
+    torch.cuda.synchronize()
+    assert vce.vce_get_status(status2) == 1 and np.isnan(out2.item())
+
+
 @pytest.mark.parametrize("reduction", ["mean", "sum", "none"])
 def test_forward_ring_bad_labels_and_reduction(vce, reduction):
     """Rows of 40 KB (the stage ring, two consumer groups; for SUM and MEAN it also reduces the

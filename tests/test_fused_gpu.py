@@ -132,6 +132,15 @@ def test_folded_reduction_repeats_exactly(vce, T, V):
     G.check_reduced(got[0], want)
 
 
+@pytest.mark.parametrize("reduction", ["mean", "sum"])
+def test_fused_beyond_the_folded_reduction(vce, reduction):
+    """70000 rows of 16 bytes: more rows than the ring reduces in-kernel, so k_ce_count_valid runs
+    before it (MEAN) and k_ce_reduce after it; checked in full against the oracle."""
+    p = gen.custom(70000, 8, "bf16", seed=5, std=2.0, n_margin=700, margin=(17.0, 50.0), n_ignore=700)
+    storage, out, rows, grad = fused(vce, p, reduction, 1.0)
+    check_against_oracle(p, storage, out, rows, grad, reduction, 1.0)
+
+
 def test_fused_padded_leading_dimensions(vce):
     """ld = V + 8 and ld_grad = V + 16 (shared-memory path): the padding is neither read into
     the statistics nor written."""
