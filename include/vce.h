@@ -153,9 +153,11 @@ VCE_API int vce_debug_status(int32_t* host_out);
  *              (rows longer than 32 KB made of 16-byte vectors stream through a
  *              shared-memory stage ring: free stage, loaded stage, warp partials, free
  *              statistics slots; shorter rows take one warp per row and other layouts
- *              one block per row, which have no such waits), or 111 if the ring's
- *              consumer groups were given rows longer than two stages (not reachable
- *              from this call); the outputs are then undefined
+ *              one block per row, which have no such waits), 112 when the ring's wait
+ *              for the batch's label count gave up (SUM / MEAN, at most 65536 rows: the
+ *              ring then reduces the losses itself), or 111 if the ring's consumer
+ *              groups were given rows longer than two stages (not reachable from this
+ *              call); the outputs are then undefined
  */
 VCE_API int ce_forward(const void* logits, vce_dtype dt, int64_t T, int64_t V, int64_t ld,
                const int64_t* labels, int64_t ignore_index, vce_reduction red,
@@ -214,8 +216,10 @@ VCE_API int ce_backward_ls(const void* logits, vce_dtype dt, int64_t T, int64_t 
  * and logits and grad_logits are 16-byte aligned, a cluster of up to 8 CTAs holds the row in
  * shared memory between its two passes [MC, VocabParallelCrossEntropy: the vocabulary split
  * with a (max, sum-exp, target) exchange]; otherwise the gradient pass re-reads the row from
- * L2.  HBM moves V*e in and V*e_g out per row.  For reduction MEAN, *loss_out holds 1/N
- * while the call's work runs and the mean loss when it is done.
+ * L2.  HBM moves V*e in and V*e_g out per row.  On the shared-memory path with SUM or MEAN
+ * and at most 65536 rows, the kernel counts N and reduces the losses itself (the CTA that
+ * finishes last sums them in a fixed order); otherwise, for MEAN, *loss_out holds 1/N while
+ * the call's work runs and the mean loss when it is done.
  *
  *   logits, dt, T, V, ld, labels, ignore_index, red: as ce_forward
  *   grad_output  fp32 [1] (SUM, MEAN) or [T] (NONE), read on the device

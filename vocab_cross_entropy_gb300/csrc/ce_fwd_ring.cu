@@ -36,7 +36,8 @@
 // Every wait is bounded (2 s); a wait that gives up writes its code to the status word (105
 // free stage, 106 loaded stage, 108 warp partials, 110 free slots) and sets the CTA's abort
 // flag, after which every role keeps its arrivals but skips the work and later waits.  111:
-// consumer groups asked for rows too long for them (the kernel returns before any wait).
+// consumer groups asked for rows too long for them (the kernel returns before any wait).  112:
+// the stats warp's wait for the consumer warps' label counts (folded reduction) gave up.
 #include <cuda_runtime.h>
 #include <stdint.h>
 

@@ -82,6 +82,7 @@ extern "C" const char* vce_status_string(int status) {
         case 109: return "a one-pass CE wait for a row's gradient coefficients gave up";
         case 110: return "a CE forward wait for free statistics slots gave up";
         case 111: return "a CE forward ring was launched with consumer groups for rows too long for them";
+        case 112: return "a CE forward wait for the batch's label count gave up";
         case 121: return "debug check: a row index outside [0, T)";
         case 122: return "debug check: a column range outside its row or chunk";
         case 123: return "debug check: a chunk or segment index outside its table";
