@@ -6,7 +6,7 @@
 // (cp.async.bulk.tensor), the mbarrier pipeline and the tcgen05 MMA / TMEM instructions.
 //
 //   warp 0 (one lane)  TMA producer: this CTA's A tile (128 x 64) and B rows (x 64) per stage
-//   warp 1 (one lane)  MMA issuer:   4 x tcgen05.mma (K = 16) per stage
+//   warp 1 (one lane)  MMA issuer:   4 x tcgen05.mma (K = 16) per stage, 8 with dual A operands
 //   warp 2             TMEM allocation / release (all 512 columns)
 //   warps 4..7         epilogue: tcgen05.ld 32 lanes x 32 columns at a time, one
 //                      accumulator row per thread
