@@ -49,7 +49,6 @@ __global__ void __launch_bounds__(NT, (kSmooth ? 1024 : 1536) / NT)
                                                float4* __restrict__ row_stats, int32_t* status) {
     __shared__ float sm_m[NT / 32], sm_s[NT / 32], sm_sz[NT / 32];
     __shared__ float sm_zt;
-    asm volatile("griddepcontrol.launch_dependents;");   // the loss reduction may be scheduled now
     for (int64_t row = blockIdx.x; row < T; row += gridDim.x) {
         const int64_t t = labels[row];
         const bool ignored = (t == ignore_index);
@@ -98,7 +97,6 @@ __global__ void __launch_bounds__(kWarpRowThreads, 3)
                   int32_t* status) {
     const int lane = threadIdx.x & 31;
     const int64_t warps = (int64_t)gridDim.x * (kWarpRowThreads / 32);
-    asm volatile("griddepcontrol.launch_dependents;");   // the loss reduction may be scheduled now
     for (int64_t row = (int64_t)blockIdx.x * (kWarpRowThreads / 32) + (threadIdx.x >> 5); row < T; row += warps) {
         const int64_t t = labels[row];
         const bool ignored = (t == ignore_index);
@@ -143,9 +141,7 @@ __global__ void __launch_bounds__(kWarpRowThreads, 3)
 // way across lanes and warps.  (This device runs fp64 arithmetic at a small fraction of its
 // fp32 rate: fp64 partials made this one-block kernel take 17 us at T = 16384.)  Only the
 // final division is done in fp64.  A non-finite sum (an inf loss row, or NaN) is s alone.
-//
-// Launched as a programmatic dependent of the row kernel before it: griddepcontrol.wait makes
-// the row kernel's results visible before any read here.
+
 __device__ __forceinline__ void two_sum_add(float& s, float& c, float x) {
     const float t = s + x;
     const float bp = t - s;
@@ -165,7 +161,6 @@ __global__ void __launch_bounds__(NT) k_ce_reduce(const float* __restrict__ loss
     __shared__ float sm_s[NT / 32], sm_c[NT / 32];
     __shared__ long long sm_n[NT / 32];
     __shared__ float sm_inv;
-    asm volatile("griddepcontrol.wait;" ::: "memory");
     float acc = 0.f, comp = 0.f;
     long long n = 0;
     uint64_t valid_mask = 0;   // bit j * U + u: row tid + NT (U j + u) is valid (j < 8)
@@ -425,21 +420,11 @@ cudaError_t dispatch_fwd(int nt, const void* logits, int64_t T, int64_t V, int64
 }
 
 
-// A programmatic dependent launch: the block may be scheduled while the row kernel before it
-// drains, and waits in griddepcontrol.wait until that kernel's writes are visible.
 cudaError_t launch_reduce(const float* loss_rows, const int64_t* labels, int64_t T, int64_t V, int64_t ig, int red,
                           float* loss_out, float* row_stats, cudaStream_t s) {
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.gridDim = dim3(1);
-    cfg.blockDim = dim3(1024);
-    cfg.stream = s;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k_ce_reduce<1024>, loss_rows, labels, T, V, ig, red, loss_out,
-                              reinterpret_cast<float4*>(row_stats));
+    k_ce_reduce<1024><<<1, 1024, 0, s>>>(loss_rows, labels, T, V, ig, red, loss_out,
+                                         reinterpret_cast<float4*>(row_stats));
+    return cudaGetLastError();
 }
 
 int check_common(vce_dtype dt, vce_reduction red, int64_t T) {

@@ -128,8 +128,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_fwd_ring(const __grid_consta
     // slot barriers within one phase of their waiters.
     constexpr int kUse = kGroups == 2 ? 3 : kSlots;
     static_assert(kUse <= kSlots && kUse >= kGroups, "slot count");
-    // the loss reduction after this kernel may be scheduled now (it waits for this grid's writes)
-    asm volatile("griddepcontrol.launch_dependents;");
     extern __shared__ __align__(128) uint8_t smem[];
     Ctl& ctl = *reinterpret_cast<Ctl*>(smem + kStages * kChunk);
     volatile int* abort_flag = &ctl.abort;

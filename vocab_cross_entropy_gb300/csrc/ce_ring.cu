@@ -203,8 +203,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_fused_ring(const __grid_cons
     constexpr int G = Elt<S>::kGroup;
     constexpr int kFullVec = kChunk / 16;
     extern __shared__ __align__(128) uint8_t smem[];
-    // the loss reduction after this kernel may be scheduled now (it waits for this grid's writes)
-    asm volatile("griddepcontrol.launch_dependents;");
     Ctl& ctl = *reinterpret_cast<Ctl*>(smem + kStages * kChunk);
     volatile int* abort_flag = &ctl.abort;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
