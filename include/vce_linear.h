@@ -124,8 +124,10 @@ VCE_API int vce_gemm_bf16(const void* A, int a_mn, const void* B, int b_mn, int6
 /*
  * vce_gemm_bf16_variant -- vce_gemm_bf16 in a chosen launch form (no page counterpart; for
  * testing and timing the forms the linear-CE uses): pair = 0 single CTAs, 128-row tiles;
- * pair = 1 CTA pairs issuing cta_group::2 MMAs, 256-row tiles (needs ceil(M / 128) even).
- * Any other pair: VCE_ERR_ARG, nothing enqueued.  Other arguments as vce_gemm_bf16.
+ * pair = 1 CTA pairs issuing cta_group::2 MMAs, 256-row tiles (needs ceil(M / 128) even);
+ * pair = 2 CTA pairs with two 64-column K blocks per pipeline stage (also needs
+ * ceil(K / 64) even).  Any other pair, or a form the shape does not allow: VCE_ERR_ARG,
+ * nothing enqueued.  Other arguments as vce_gemm_bf16.
  */
 VCE_API int vce_gemm_bf16_variant(const void* A, int a_mn, const void* B, int b_mn, int64_t M, int64_t N, int64_t K,
                           float* C, int64_t ldc, int pair, vce_stream_t s);

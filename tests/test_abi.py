@@ -83,5 +83,6 @@ def test_linear_and_gemm_hook_argument_errors_need_no_gpu(lib):
     v = lib.vce_gemm_bf16_variant
     v.argtypes = [P, i32, P, i32, i64, i64, i64, P, i64, i32, P]
     assert v(x, 0, x, 0, 384, 256, 128, x, 256, 1, None) == -8          # 3 M tiles cannot pair
-    assert v(x, 0, x, 0, 256, 256, 128, x, 256, 2, None) == -8          # pair is 0 or 1
+    assert v(x, 0, x, 0, 256, 256, 128, x, 256, 3, None) == -8          # pair is 0, 1 or 2
+    assert v(x, 0, x, 0, 256, 256, 192, x, 256, 2, None) == -8          # 3 K blocks cannot pair up
     assert v(x, 0, x, 0, 256, 256, 128, x, 200, 1, None) == -4          # ldc < N

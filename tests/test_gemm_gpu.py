@@ -34,15 +34,20 @@ def test_gemm_layouts(vce, a_mn, b_mn, M, N, K):
     assert np.all(err <= bound), f"max err/bound {np.max(err / bound):.3g}"
 
 
-@pytest.mark.parametrize("pair", [0, 1])
+@pytest.mark.parametrize("pair", [0, 1, 2])
 @pytest.mark.parametrize("a_mn,b_mn", [(False, False), (True, True), (False, True), (True, False)])
-@pytest.mark.parametrize("M,N,K", [(256, 256, 64), (512, 384, 1000), (2560, 640, 1536)])
+@pytest.mark.parametrize("M,N,K", [(256, 256, 64), (256, 256, 128), (512, 384, 1000), (2560, 640, 1536)])
 def test_gemm_variants(vce, pair, a_mn, b_mn, M, N, K):
-    """Both launch forms of the GEMM -- single CTAs and CTA pairs issuing cta_group::2 MMAs --
-    against a float64 product of the same bf16 values."""
+    """The three launch forms of the GEMM -- single CTAs, CTA pairs issuing cta_group::2 MMAs,
+    and pairs taking two K blocks per stage -- against a float64 product of the same bf16
+    values.  The last form refuses an odd count of 64-column K blocks."""
     rng = np.random.default_rng(M + 3 * N + K + 5 * pair + 7 * a_mn + 11 * b_mn)
     A, A64 = _bf16(rng, (K, M) if a_mn else (M, K))
     B, B64 = _bf16(rng, (K, N) if b_mn else (N, K), 0.05)
+    if pair == 2 and (K + 63) // 64 % 2:
+        with pytest.raises(vce.VceError):
+            vce.vce_gemm_bf16_variant(A.cuda(), B.cuda(), a_mn, b_mn, pair=pair)
+        return
     C = vce.vce_gemm_bf16_variant(A.cuda(), B.cuda(), a_mn, b_mn, pair=pair)
     torch.cuda.synchronize()
     Am = A64.T if a_mn else A64
@@ -54,14 +59,16 @@ def test_gemm_variants(vce, pair, a_mn, b_mn, M, N, K):
 
 
 def test_pairs_and_single_ctas_agree_bitwise(vce):
-    """The two launch forms accumulate each tile's K blocks in the same order: equal bits."""
+    """The three launch forms accumulate each tile's K blocks in the same order: equal bits."""
     rng = np.random.default_rng(17)
     A, _ = _bf16(rng, (1024, 2048))
     B, _ = _bf16(rng, (768, 2048), 0.05)
     C1 = vce.vce_gemm_bf16_variant(A.cuda(), B.cuda(), pair=0)
     C2 = vce.vce_gemm_bf16_variant(A.cuda(), B.cuda(), pair=1)
+    C3 = vce.vce_gemm_bf16_variant(A.cuda(), B.cuda(), pair=2)
     torch.cuda.synchronize()
     assert torch.equal(C1, C2)
+    assert torch.equal(C1, C3)
 
 
 def test_gemm_variant_refuses_bad_arguments(vce):

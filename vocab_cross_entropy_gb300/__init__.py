@@ -375,8 +375,9 @@ def vce_gemm_bf16(A, B, a_mn=False, b_mn=False, *, C=None, stream=None):
     return C
 
 
-def vce_gemm_bf16_variant(A, B, a_mn=False, b_mn=False, *, pair=False, C=None, stream=None):
-    """vce_gemm_bf16 in a chosen launch form: CTA pairs (256-row tiles) or single CTAs."""
+def vce_gemm_bf16_variant(A, B, a_mn=False, b_mn=False, *, pair=0, C=None, stream=None):
+    """vce_gemm_bf16 in a chosen launch form: pair 0 single CTAs, 1 CTA pairs (256-row tiles),
+    2 CTA pairs with two K blocks per pipeline stage."""
     M = A.shape[1] if a_mn else A.shape[0]
     K = A.shape[0] if a_mn else A.shape[1]
     N = B.shape[1] if b_mn else B.shape[0]

@@ -26,22 +26,25 @@ bool sizes_ok(int64_t M, int64_t N, int64_t K, int64_t lim) {
 }
 
 // C[M, ldc] = op(A) op(B)^T with the given layouts, on CTA pairs or single CTAs.
+// k2: two K blocks per stage (needs an even number of K blocks).
+template <bool kK2>
+cudaError_t gemm_as(const Mat& ma, const Mat& mb, int a_mn, int b_mn, const tc::GemmArgs& g,
+                    const tc::EpiStore::Params& ep, bool pair, cudaStream_t s) {
+    if (a_mn && b_mn) return tc::launch_gemm<tc::EpiStore, true, true, false, kK2>(ma, ma, mb, g, ep, pair, s);
+    if (a_mn) return tc::launch_gemm<tc::EpiStore, true, false, false, kK2>(ma, ma, mb, g, ep, pair, s);
+    if (b_mn) return tc::launch_gemm<tc::EpiStore, false, true, false, kK2>(ma, ma, mb, g, ep, pair, s);
+    return tc::launch_gemm<tc::EpiStore, false, false, false, kK2>(ma, ma, mb, g, ep, pair, s);
+}
+
 int gemm(const void* A, int a_mn, const void* B, int b_mn, int64_t M, int64_t N, int64_t K, float* C, int64_t ldc,
-         bool pair, cudaStream_t s) {
+         bool pair, bool k2, cudaStream_t s) {
     const Mat ma = a_mn ? Mat{A, M, K, M} : Mat{A, K, M, K};
     const Mat mb = b_mn ? Mat{B, N, K, N} : Mat{B, K, N, K};
     const int nk = (int)cdiv(K, BK);
     tc::GemmArgs g{(int)cdiv(M, BM), (int)cdiv(N, BN), nk, nk, 0, 0, 0, 0, nullptr};
     tc::EpiStore::Params ep{C, ldc, M, N, 0, 0};
-    cudaError_t e;
-    if (a_mn && b_mn)
-        e = tc::launch_gemm<tc::EpiStore, true, true>(ma, ma, mb, g, ep, pair, s);
-    else if (a_mn)
-        e = tc::launch_gemm<tc::EpiStore, true, false>(ma, ma, mb, g, ep, pair, s);
-    else if (b_mn)
-        e = tc::launch_gemm<tc::EpiStore, false, true>(ma, ma, mb, g, ep, pair, s);
-    else
-        e = tc::launch_gemm<tc::EpiStore, false, false>(ma, ma, mb, g, ep, pair, s);
+    const cudaError_t e = k2 ? gemm_as<true>(ma, mb, a_mn, b_mn, g, ep, pair, s)
+                             : gemm_as<false>(ma, mb, a_mn, b_mn, g, ep, pair, s);
     return e == cudaSuccess ? VCE_OK : VCE_ERR_CUDA;
 }
 
@@ -61,7 +64,7 @@ extern "C" int vce_gemm_bf16(const void* A, int a_mn, const void* B, int b_mn, i
     if (!aligned(A, 16) || !aligned(B, 16) || !aligned(C, 16) || (ldc % 4)) return VCE_ERR_ALIGN;
     int rc = require_sm100();
     if (rc) return rc;
-    return gemm(A, a_mn, B, b_mn, M, N, K, C, ldc, cdiv(M, BM) % 2 == 0, s);
+    return gemm(A, a_mn, B, b_mn, M, N, K, C, ldc, cdiv(M, BM) % 2 == 0, false, s);
 }
 
 extern "C" int vce_gemm_bf16_variant(const void* A, int a_mn, const void* B, int b_mn, int64_t M, int64_t N, int64_t K,
@@ -69,11 +72,11 @@ extern "C" int vce_gemm_bf16_variant(const void* A, int a_mn, const void* B, int
     if (!A || !B || !C) return VCE_ERR_NULL;
     if (!sizes_ok(M, N, K, 1 << 30)) return VCE_ERR_SHAPE;
     if (ldc < N) return VCE_ERR_LD;
-    if ((pair != 0 && pair != 1) || (pair && cdiv(M, BM) % 2)) return VCE_ERR_ARG;
+    if (pair < 0 || pair > 2 || (pair && cdiv(M, BM) % 2) || (pair == 2 && cdiv(K, BK) % 2)) return VCE_ERR_ARG;
     if (!aligned(A, 16) || !aligned(B, 16) || !aligned(C, 16) || (ldc % 4)) return VCE_ERR_ALIGN;
     int rc = require_sm100();
     if (rc) return rc;
-    return gemm(A, a_mn, B, b_mn, M, N, K, C, ldc, pair != 0, s);
+    return gemm(A, a_mn, B, b_mn, M, N, K, C, ldc, pair != 0, pair == 2, s);
 }
 
 extern "C" int vce_test_gemm_stall(const void* A, const void* B, int64_t M, int64_t N, int64_t K, float* C,

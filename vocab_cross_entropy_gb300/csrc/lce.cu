@@ -452,7 +452,10 @@ int linear_ce_run(const void* E, const void* W, int64_t T, int64_t D, int64_t V,
         tc::GemmArgs g{tiles_t, (int)L.tiles_v, nkD, nkD, 0, 0, 0, 0, status};
         EpiStats::Params ep{labels, ignore_index, T, V, reinterpret_cast<float4*>(part)};
         if (timer && !timer->begin(s)) return VCE_ERR_CUDA;
-        if (tc::launch_gemm<EpiStats, false, false>(mE, mE, mW, g, ep, pairs_t, s) != cudaSuccess) return VCE_ERR_CUDA;
+        // two K blocks per stage where D gives an even number of them (eight MMAs per stage)
+        const cudaError_t e = nkD % 2 == 0 ? tc::launch_gemm<EpiStats, false, false, false, true>(mE, mE, mW, g, ep, pairs_t, s)
+                                           : tc::launch_gemm<EpiStats, false, false>(mE, mE, mW, g, ep, pairs_t, s);
+        if (e != cudaSuccess) return VCE_ERR_CUDA;
         if (timer && !timer->end(s, GemmTimer::kStats)) return VCE_ERR_CUDA;
         if (launch_stats_merge(part, (int)L.tiles_v, T, V, labels, ignore_index, loss_rows, stats, status, s) !=
             cudaSuccess)
@@ -477,7 +480,10 @@ int linear_ce_run(const void* E, const void* W, int64_t T, int64_t D, int64_t V,
                                red == VCE_RED_NONE, ghi, glo, L.Vc, filter_eps, keep_w, L.ldw, keep_e, L.lde,
                                filter ? kept_blocks : nullptr};
             if (timer && !timer->begin(s)) return VCE_ERR_CUDA;
-            if (tc::launch_gemm<EpiGrad, false, false>(mE, mE, mW, g, ep, pairs_t, s) != cudaSuccess) return VCE_ERR_CUDA;
+            const cudaError_t e =
+                nkD % 2 == 0 ? tc::launch_gemm<EpiGrad, false, false, false, true>(mE, mE, mW, g, ep, pairs_t, s)
+                             : tc::launch_gemm<EpiGrad, false, false>(mE, mE, mW, g, ep, pairs_t, s);
+            if (e != cudaSuccess) return VCE_ERR_CUDA;
             if (timer && !timer->end(s, GemmTimer::kGrad)) return VCE_ERR_CUDA;
         }
         {   // dW[off : off + width] = G^T E: A = G (MN-major), B = E (MN-major), K = 2 T_pad (hi then lo);

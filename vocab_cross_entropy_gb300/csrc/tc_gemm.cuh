@@ -7,6 +7,7 @@
 //
 //   warp 0 (one lane)  TMA producer: this CTA's A tile (128 x 64) and B rows (x 64) per stage
 //   warp 1 (one lane)  MMA issuer:   4 x tcgen05.mma (K = 16) per stage, 8 with dual A operands
+//                                    or two K blocks per stage
 //   warp 2             TMEM allocation / release (all 512 columns)
 //   warps 4..7         epilogue: tcgen05.ld 32 lanes x 32 columns at a time, one
 //                      accumulator row per thread
@@ -27,9 +28,11 @@
 //                    shared memory reads per MMA fall by a third and seven stages fit.
 // Options: K-block skipping from a per-tile bit table (GemmArgs::skip, gradient filtering,
 // single CTAs only); a K offset (GemmArgs::ka0) so that one product can be split along K into
-// launches whose partial sums the caller merges; and dual A operands (template kDualA):
+// launches whose partial sums the caller merges; dual A operands (template kDualA):
 // acc = (A0 + A1) B^T with A0's and A1's tiles of one K block held in the same stage beside a
-// single B tile, so B is loaded once for both (the linear-CE's G_hi and G_lo).
+// single B tile, so B is loaded once for both (the linear-CE's G_hi and G_lo); and two K blocks
+// per stage (template kK2: A's and B's tiles of blocks k and k + 1 in one stage, eight MMAs per
+// stage, the same accumulation order; one A operand, no skip bits, an even number of blocks).
 #pragma once
 
 #include <cuda.h>
@@ -48,14 +51,19 @@ constexpr int kThreads = 256;
 constexpr int TMEM_COLS = 2 * BN;             // two fp32 accumulators of 128 lanes x 256 columns
 constexpr int kMaxSmem = 232448;              // opt-in dynamic shared memory per block (227 KB)
 
-template <bool kCta2, bool kDualA = false>
+// kK2: a stage holds two consecutive K blocks of A and of B (eight MMAs per stage).
+template <bool kCta2, bool kDualA = false, bool kK2 = false>
 struct Cfg {
+    static_assert(!(kDualA && kK2), "dual A operands take one K block per stage");
+    static constexpr int kKPer = kK2 ? 2 : 1;              // K blocks per stage
     static constexpr int kBRows = kCta2 ? BN / 2 : BN;   // rows of the B tile this CTA loads
-    static constexpr int kBBytes = kBRows * BK * 2;
-    static constexpr int kABytes = (kDualA ? 2 : 1) * A_BYTES;
+    static constexpr int kBBlock = kBRows * BK * 2;       // B bytes of one K block
+    static constexpr int kBBytes = kKPer * kBBlock;
+    static constexpr int kABytes = (kDualA ? 2 : kKPer) * A_BYTES;
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr int kReserve = 1024 /*alignment*/ + 256 /*barriers*/;
-    // single: 4 stages (3 with dual A); pair: 7 stages (4 with dual A)
+    // single: 4 stages (3 with dual A, 2 with two K blocks); pair: 7 stages (4 with dual A, 3
+    // with two K blocks)
     static constexpr int kStages = (kMaxSmem - kReserve) / kStageBytes;
     static constexpr int kSmem = kStages * kStageBytes + kReserve;
 };
@@ -349,11 +357,11 @@ __device__ __forceinline__ void tile_coords(const GemmArgs& g, int tile, uint32_
 // kAmn / kBmn: the operand is MN-major; its tensor map then has 64 x 64 boxes over a global
 // [K, M] (resp. [K, N]) matrix, and the tile is loaded as 2 (resp. kBRows / 64) boxes.  A
 // K-major B map has boxes of kBRows rows.
-template <class Epi, bool kAmn, bool kBmn, bool kCta2, bool kDualA = false>
+template <class Epi, bool kAmn, bool kBmn, bool kCta2, bool kDualA = false, bool kK2 = false>
 __global__ void __launch_bounds__(kThreads, 1)
     k_tc_gemm(const __grid_constant__ CUtensorMap mapA0, const __grid_constant__ CUtensorMap mapA1,
               const __grid_constant__ CUtensorMap mapB, const GemmArgs g, const typename Epi::Params ep) {
-    using C = Cfg<kCta2, kDualA>;
+    using C = Cfg<kCta2, kDualA, kK2>;
     constexpr int S = C::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -414,10 +422,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int tile = tile0; tile < ntiles && !*abort_flag; tile += tstep) {
             int tm, tn;
             tile_coords<kCta2>(g, tile, rank, tm, tn);
-            auto each = [&](auto&& f) {   // the stages of this tile: K blocks, or (A0, A1) block pairs
-                if (kDualA) {
+            auto each = [&](auto&& f) {   // the stages of this tile: K blocks, (A0, A1) block pairs
+                if (kDualA) {             // or pairs of consecutive K blocks
                     for (int ka = 0; ka < g.nk_a0; ++ka)
                         if (!f(0, ka)) return;
+                } else if (kK2) {
+                    for (int ka = 0; ka < g.nk; ka += 2)
+                        if (!f(ka, ka)) return;
                 } else {
                     for_each_kblock(g, tm, f);
                 }
@@ -430,8 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_arrive_expect_tx(&full[stage], (kCta2 ? 2 : 1) * C::kStageBytes + g.tx_extra);
                 uint8_t* sa = smA + stage * C::kABytes;
                 uint8_t* sb = smB + stage * C::kBBytes;
-                const int k = (g.ka0 + ka) * BK;
-                auto load_a = [&](const CUtensorMap* ma, uint8_t* dst) {
+                auto load_a = [&](const CUtensorMap* ma, uint8_t* dst, int k) {
                     if (kAmn) {
 #pragma unroll
                         for (int h = 0; h < BM / 64; ++h)
@@ -440,19 +450,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tma_load<kCta2>(dst, ma, fb, k, g.a_y0 + tm * BM);
                     }
                 };
-                if (kDualA) {
-                    load_a(&mapA0, sa);
-                    load_a(&mapA1, sa + A_BYTES);
-                } else {
-                    load_a(kb >= g.nk_a0 ? &mapA1 : &mapA0, sa);
-                }
                 const int n0 = g.b_y0 + tn * BN + (int)rank * C::kBRows;
-                if (kBmn) {
+                auto load_b = [&](uint8_t* dst, int k) {
+                    if (kBmn) {
 #pragma unroll
-                    for (int h = 0; h < C::kBRows / 64; ++h)
-                        tma_load<kCta2>(sb + h * (64 * BK * 2), &mapB, fb, n0 + h * 64, g.b_x0 + k);
+                        for (int h = 0; h < C::kBRows / 64; ++h)
+                            tma_load<kCta2>(dst + h * (64 * BK * 2), &mapB, fb, n0 + h * 64, g.b_x0 + k);
+                    } else {
+                        tma_load<kCta2>(dst, &mapB, fb, g.b_x0 + k, n0);
+                    }
+                };
+                if (kDualA) {
+                    const int k = (g.ka0 + ka) * BK;
+                    load_a(&mapA0, sa, k);
+                    load_a(&mapA1, sa + A_BYTES, k);
+                    load_b(sb, k);
                 } else {
-                    tma_load<kCta2>(sb, &mapB, fb, g.b_x0 + k, n0);
+#pragma unroll
+                    for (int h = 0; h < C::kKPer; ++h) {   // K blocks kb (and kb + 1) of the stage
+                        const int k = (g.ka0 + ka + h) * BK;
+                        load_a(kb + h >= g.nk_a0 ? &mapA1 : &mapA0, sa + h * A_BYTES, k);
+                        load_b(sb + h * C::kBBlock, k);
+                    }
                 }
                 issued = issued < S ? issued + 1 : S;
                 if (++stage == S) { stage = 0; phase ^= 1u; }
@@ -507,12 +526,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_after();
                 const uint32_t sa = a0 + stage * C::kABytes;
-                const uint64_t bd =
-                    kBmn ? desc_mnmajor_sw128(b0 + stage * C::kBBytes) : desc_kmajor_sw128(b0 + stage * C::kBBytes);
 #pragma unroll
-                for (int h = 0; h < (kDualA ? 2 : 1); ++h) {   // A0, then A1 against the same B tile
-                    const uint32_t at = sa + h * A_BYTES;
+                for (int h = 0; h < (kDualA ? 2 : C::kKPer); ++h) {   // A0, then A1 against the same B
+                    const uint32_t at = sa + h * A_BYTES;             // tile; or K blocks kb, kb + 1
+                    const uint32_t bt = b0 + stage * C::kBBytes + (kK2 ? h * C::kBBlock : 0);
                     const uint64_t ad = kAmn ? desc_mnmajor_sw128(at) : desc_kmajor_sw128(at);
+                    const uint64_t bd = kBmn ? desc_mnmajor_sw128(bt) : desc_kmajor_sw128(bt);
 #pragma unroll
                     for (int k = 0; k < BK / 16; ++k)   // advance the start address by one K = 16 step
                         mma_bf16<kCta2>(d, ad + kStepA * k, bd + kStepB * k, idesc,
@@ -526,6 +545,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (kDualA) {
                 for (int ka = 0; ka < g.nk_a0; ++ka)
                     if (!stage_mmas(0, ka)) break;
+            } else if (kK2) {
+                for (int ka = 0; ka < g.nk; ka += 2)
+                    if (!stage_mmas(ka, ka)) break;
             } else {
                 for_each_kblock(g, tm, stage_mmas);
             }

@@ -93,15 +93,15 @@ cudaError_t prepare_kernel(K kern, int smem, bool pair, std::atomic<int> (&ready
     return cudaSuccess;
 }
 
-template <class Epi, bool kAmn, bool kBmn, bool kCta2, bool kDualA>
+template <class Epi, bool kAmn, bool kBmn, bool kCta2, bool kDualA, bool kK2 = false>
 cudaError_t launch_gemm_as(const Mat& a0, const Mat& a1, const Mat& b, const GemmArgs& g,
                            const typename Epi::Params& ep, cudaStream_t s) {
-    using C = Cfg<kCta2, kDualA>;
+    using C = Cfg<kCta2, kDualA, kK2>;
     CUtensorMap ma0, ma1, mb;
     if (!make_map(&ma0, a0, kAmn ? 64 : BM) || !make_map(&ma1, a1, kAmn ? 64 : BM) ||
         !make_map(&mb, b, kBmn ? 64 : C::kBRows))
         return record_cuda(cudaErrorInvalidValue);
-    auto kern = k_tc_gemm<Epi, kAmn, kBmn, kCta2, kDualA>;
+    auto kern = k_tc_gemm<Epi, kAmn, kBmn, kCta2, kDualA, kK2>;
     static std::atomic<int> ready[kMaxDevices];   // one cache per kernel instantiation
     int clusters = 0;
     cudaError_t e = prepare_kernel(kern, C::kSmem, kCta2, ready, &clusters);
@@ -131,14 +131,16 @@ cudaError_t launch_gemm_as(const Mat& a0, const Mat& a1, const Mat& b, const Gem
 
 // One GEMM, as CTA pairs (pair: tiles_m must be even and there must be no skip bits) or as
 // single CTAs.  kDualA: acc = (A0 + A1) B^T over nk_a0 K blocks, both A tiles of a block in one
-// stage (no skip bits).
-template <class Epi, bool kAmn, bool kBmn, bool kDualA = false>
+// stage (no skip bits).  kK2: two consecutive K blocks per stage (one A operand: nk == nk_a0, an
+// even nk, no skip bits; the same accumulation order as one block per stage).
+template <class Epi, bool kAmn, bool kBmn, bool kDualA = false, bool kK2 = false>
 cudaError_t launch_gemm(const Mat& a0, const Mat& a1, const Mat& b, const GemmArgs& g,
                         const typename Epi::Params& ep, bool pair, cudaStream_t s) {
     if (pair && (g.tiles_m % 2 || g.skip)) return record_cuda(cudaErrorInvalidConfiguration);
     if (kDualA && g.skip) return record_cuda(cudaErrorInvalidConfiguration);
-    return pair ? launch_gemm_as<Epi, kAmn, kBmn, true, kDualA>(a0, a1, b, g, ep, s)
-                : launch_gemm_as<Epi, kAmn, kBmn, false, kDualA>(a0, a1, b, g, ep, s);
+    if (kK2 && (g.skip || g.nk % 2 || g.nk != g.nk_a0)) return record_cuda(cudaErrorInvalidConfiguration);
+    return pair ? launch_gemm_as<Epi, kAmn, kBmn, true, kDualA, kK2>(a0, a1, b, g, ep, s)
+                : launch_gemm_as<Epi, kAmn, kBmn, false, kDualA, kK2>(a0, a1, b, g, ep, s);
 }
 
 // Output tile rows into [rows, cols] at row offset row_off with row pitch ld (bf16 rounded to
