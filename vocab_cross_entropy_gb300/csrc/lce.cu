@@ -53,6 +53,7 @@ inline int64_t round_up(int64_t a, int64_t b) { return cdiv(a, b) * b; }
 
 // Step 1: per (row, vocabulary tile): (max, sum-exp) over non-target columns < V, target logit.
 struct EpiStats {
+    static constexpr int kScratch = 0;
     struct Params {
         const int64_t* labels;
         int64_t ignore_index, T, V;
@@ -104,6 +105,8 @@ struct EpiStats {
 // ORs its 32 rows' marks; the first warp to set a block's bit also sets it in the transposed
 // table and counts the block.
 struct EpiGrad {
+    // per epilogue warp: G_hi and G_lo of its 32 rows x 64 columns, 4 KB each (see put/flush)
+    static constexpr int kScratch = 4 * 8192;
     struct Params {
         const int64_t* labels;
         int64_t T, width, col_off;   // rows, chunk width, chunk's first global column
@@ -126,6 +129,7 @@ struct EpiGrad {
         int64_t tl;
         bool zero;
         uint32_t bits;               // kept marks of this row's two 128-column halves of the tile
+        uint8_t* scratch;            // this warp's 8 KB of shared memory
     };
     __device__ __forceinline__ static void begin(const Params& p, Row& r, int row, int tn) {
         r.zero = true;
@@ -168,47 +172,72 @@ struct EpiGrad {
                 hi[k / 2] = h ^ r.sign;
                 lo[k / 2] = pack_bf16x2(g0 - bf16_lo(h), g1 - bf16_hi(h)) ^ r.sign;
             }
-            store(p, row, col0, hi, lo);
-            return;
-        }
-        float emax = 0.f;   // largest 2^(z log2e - bias) over the piece's columns < width
+        } else {
+            float emax = 0.f;   // largest 2^(z log2e - bias) over the piece's columns < width
 #pragma unroll
-        for (int k = 0; k < 32; k += 2) {
-            float g[2];
+            for (int k = 0; k < 32; k += 2) {
+                float g[2];
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int col = col0 + k + e;
-                const float ev = ex2(fmaf(__uint_as_float(acc[k + e]), kLog2e, -r.bias));
-                float x = r.coef * ev;
-                if (p.keep_w && col < p.width) emax = fmaxf(emax, ev);
-                if (col == r.tl) x = r.gt;
-                if (r.zero || col >= p.width) x = 0.f;
-                g[e] = x;
+                for (int e = 0; e < 2; ++e) {
+                    const int col = col0 + k + e;
+                    const float ev = ex2(fmaf(__uint_as_float(acc[k + e]), kLog2e, -r.bias));
+                    float x = r.coef * ev;
+                    if (p.keep_w && col < p.width) emax = fmaxf(emax, ev);
+                    if (col == r.tl) x = r.gt;
+                    if (r.zero || col >= p.width) x = 0.f;
+                    g[e] = x;
+                }
+                const uint32_t h = pack_bf16x2(g[0], g[1]);
+                const float r0 = g[0] - bf16_lo(h), r1 = g[1] - bf16_hi(h);
+                hi[k / 2] = h;
+                lo[k / 2] = pack_bf16x2(r0, r1);
             }
-            const uint32_t h = pack_bf16x2(g[0], g[1]);
-            const float r0 = g[0] - bf16_lo(h), r1 = g[1] - bf16_hi(h);
-            hi[k / 2] = h;
-            lo[k / 2] = pack_bf16x2(r0, r1);
+            // A target column in the piece keeps its block anyway (begin), so including its
+            // value in emax changes nothing.
+            if (p.keep_w && !r.zero && emax >= r.thr) r.bits |= 1u << ((col0 % BN) >> 7);
         }
-        // A target column in the piece keeps its block anyway (begin), so including its
-        // value in emax changes nothing.
-        if (p.keep_w && !r.zero && emax >= r.thr) r.bits |= 1u << ((col0 % BN) >> 7);
-        store(p, row, col0, hi, lo);
+        put(r, col0, hi, lo);
+        if ((col0 >> 5) & 1) flush(p, r, row, col0 - 32);   // the second 32 columns of a 64-column pair
     }
-    // row-major [T_pad][ldg]: 64 contiguous bytes per thread.  Evict-first stores: the chunk's G
-    // (512 MB at T = 8192) is read back from DRAM by the next two GEMMs anyway, and should not
-    // push E and W out of L2 meanwhile (measured 0.4% faster per call).
-    __device__ __forceinline__ static void store(const Params& p, int row, int col0, const uint32_t (&hi)[16],
-                                                 const uint32_t (&lo)[16]) {
-        // G is [round_up(T, 128)][ldg]
-        if (!dbg::ok(row < (p.T + 127) / 128 * 128 && col0 + 32 <= p.ldg, dbg::kTile)) return;
-        uint4* dh = reinterpret_cast<uint4*>(p.g_hi + (int64_t)row * p.ldg + col0);
-        uint4* dl = reinterpret_cast<uint4*>(p.g_lo + (int64_t)row * p.ldg + col0);
+    // G goes out through shared memory so that every store writes whole 128-byte lines: a
+    // thread holds 64 B of its own row per piece, and storing that directly writes half
+    // sectors of 32 different rows per instruction.  A row of the scratch is 128 B (64
+    // columns); its 16-byte chunk c sits in slot c ^ (row & 7), so that the eight lanes of a
+    // quarter warp hit eight different bank groups both when each writes its own row (put)
+    // and when they read the eight chunks of one row (flush).
+    __device__ __forceinline__ static void put(const Row& r, int col0, const uint32_t (&hi)[16],
+                                               const uint32_t (&lo)[16]) {
+        const int lane = threadIdx.x & 31;
+        const int c0 = ((col0 >> 5) & 1) * 4;   // first chunk of this piece within the 128-byte row
+        uint8_t* row_h = r.scratch + lane * 128;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            st_stream16(dh + q, make_uint4(hi[4 * q], hi[4 * q + 1], hi[4 * q + 2], hi[4 * q + 3]));
-            st_stream16(dl + q, make_uint4(lo[4 * q], lo[4 * q + 1], lo[4 * q + 2], lo[4 * q + 3]));
+            const int slot = (c0 + q) ^ (lane & 7);
+            tc::sts16(row_h + slot * 16, make_uint4(hi[4 * q], hi[4 * q + 1], hi[4 * q + 2], hi[4 * q + 3]));
+            tc::sts16(row_h + 4096 + slot * 16, make_uint4(lo[4 * q], lo[4 * q + 1], lo[4 * q + 2], lo[4 * q + 3]));
         }
+    }
+    // The warp's 32 rows x 64 columns from col0 to row-major [T_pad][ldg], four rows of 128 B per
+    // store.  Evict-first stores: the chunk's G (512 MB at T = 8192) is read back from DRAM by
+    // the next two GEMMs anyway, and should not push E and W out of L2 meanwhile.
+    __device__ __forceinline__ static void flush(const Params& p, const Row& r, int row, int col0) {
+        __syncwarp();
+        const int lane = threadIdx.x & 31;
+        const int row0 = row - lane;   // the warp's first row
+        const int c = lane & 7;
+        const int64_t t_pad = (p.T + 127) / 128 * 128;   // G is [round_up(T, 128)][ldg]
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int rr = 4 * i + (lane >> 3);
+            const int off = rr * 128 + ((c ^ (rr & 7)) * 16);
+            const uint4 h = tc::lds16(r.scratch + off);
+            const uint4 l = tc::lds16(r.scratch + 4096 + off);
+            if (!dbg::ok(row0 + rr < t_pad && col0 + 64 <= p.ldg, dbg::kTile)) continue;
+            const int64_t at = (int64_t)(row0 + rr) * p.ldg + col0 + c * 8;
+            st_stream16(p.g_hi + at, h);
+            st_stream16(p.g_lo + at, l);
+        }
+        __syncwarp();   // the reads above before the next pair's writes
     }
     __device__ __forceinline__ static void end(const Params& p, Row& r, int row, int tn) {
         if (!p.keep_w) return;
@@ -235,6 +264,7 @@ struct EpiGrad {
 // parts the compensation would only ever hold the last merge's error, which is rounded away
 // with it).
 struct EpiKahan {
+    static constexpr int kScratch = 0;
     struct Params {
         float *sum, *comp;   // [rows][cols]; comp may be null (the pair's compensation is then 0)
         int64_t rows, cols;

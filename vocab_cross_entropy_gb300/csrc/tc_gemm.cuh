@@ -52,7 +52,9 @@ constexpr int TMEM_COLS = 2 * BN;             // two fp32 accumulators of 128 la
 constexpr int kMaxSmem = 232448;              // opt-in dynamic shared memory per block (227 KB)
 
 // kK2: a stage holds two consecutive K blocks of A and of B (eight MMAs per stage).
-template <bool kCta2, bool kDualA = false, bool kK2 = false>
+// kScratch: shared memory the epilogue asks for beside the stage ring (Epi::kScratch bytes,
+// a quarter per epilogue warp), placed after the barriers.
+template <bool kCta2, bool kDualA = false, bool kK2 = false, int kScratch = 0>
 struct Cfg {
     static_assert(!(kDualA && kK2), "dual A operands take one K block per stage");
     static constexpr int kKPer = kK2 ? 2 : 1;              // K blocks per stage
@@ -61,7 +63,7 @@ struct Cfg {
     static constexpr int kBBytes = kKPer * kBBlock;
     static constexpr int kABytes = (kDualA ? 2 : kKPer) * A_BYTES;
     static constexpr int kStageBytes = kABytes + kBBytes;
-    static constexpr int kReserve = 1024 /*alignment*/ + 256 /*barriers*/;
+    static constexpr int kReserve = 1024 /*alignment*/ + 256 /*barriers*/ + kScratch;
     // single: 4 stages (3 with dual A, 2 with two K blocks); pair: 7 stages (4 with dual A, 3
     // with two K blocks)
     static constexpr int kStages = (kMaxSmem - kReserve) / kStageBytes;
@@ -361,7 +363,7 @@ template <class Epi, bool kAmn, bool kBmn, bool kCta2, bool kDualA = false, bool
 __global__ void __launch_bounds__(kThreads, 1)
     k_tc_gemm(const __grid_constant__ CUtensorMap mapA0, const __grid_constant__ CUtensorMap mapA1,
               const __grid_constant__ CUtensorMap mapB, const GemmArgs g, const typename Epi::Params ep) {
-    using C = Cfg<kCta2, kDualA, kK2>;
+    using C = Cfg<kCta2, kDualA, kK2, Epi::kScratch>;
     constexpr int S = C::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -589,6 +591,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int row = tm * BM + sub * 32 + lane;
             const uint32_t t0 = tmem_base + (uint32_t)(acc * BN) + lane_off;
             typename Epi::Row st;
+            if constexpr (Epi::kScratch > 0)   // this warp's quarter of the scratch after the barriers
+                st.scratch = smem + S * C::kStageBytes + 256 + sub * (Epi::kScratch / 4);
             // Two register buffers: the next 32 columns load from TMEM while these are consumed.
             static_assert((BN / 32) % 2 == 0, "column pieces go in pairs");
             uint32_t ra[32], rb[32];

@@ -96,7 +96,7 @@ cudaError_t prepare_kernel(K kern, int smem, bool pair, std::atomic<int> (&ready
 template <class Epi, bool kAmn, bool kBmn, bool kCta2, bool kDualA, bool kK2 = false>
 cudaError_t launch_gemm_as(const Mat& a0, const Mat& a1, const Mat& b, const GemmArgs& g,
                            const typename Epi::Params& ep, cudaStream_t s) {
-    using C = Cfg<kCta2, kDualA, kK2>;
+    using C = Cfg<kCta2, kDualA, kK2, Epi::kScratch>;
     CUtensorMap ma0, ma1, mb;
     if (!make_map(&ma0, a0, kAmn ? 64 : BM) || !make_map(&ma1, a1, kAmn ? 64 : BM) ||
         !make_map(&mb, b, kBmn ? 64 : C::kBRows))
@@ -146,6 +146,7 @@ cudaError_t launch_gemm(const Mat& a0, const Mat& a1, const Mat& b, const GemmAr
 // Output tile rows into [rows, cols] at row offset row_off with row pitch ld (bf16 rounded to
 // nearest even from fp32, or fp32), evict-first: nothing in a call reads them back.
 struct EpiStore {
+    static constexpr int kScratch = 0;
     struct Params {
         void* out;
         int64_t ld, rows, cols, row_off;
