@@ -439,6 +439,53 @@ def test_folded_reduction_repeats_exactly(vce, T, V):
     G.check_reduced(got[0], want)
 
 
+@pytest.mark.parametrize("reduction", ["mean", "none"])
+def test_forward_ring_launch_slots(vce, reduction):
+    """The stage ring claims rows from a per-launch slot of device words that its last CTA puts
+    back to zero, and writes the status word itself.  1100 calls (more than the 1024 slots, so
+    every slot is used and reused) into a status word filled with garbage and outputs filled
+    with NaN each time: every call's status is 0 and its outputs equal the first call's, bit for
+    bit.  A call with a bad label in the middle sets VCE_ERR_LABEL, and the next calls, which
+    reuse slots after it, are clean again."""
+    T, V = 400, 20000
+    p = gen.custom(T, V, "bf16", seed=91, std=2.0, n_margin=10, n_ignore=40)
+    logits = to_device(p.full(), "bf16")
+    labels = torch.from_numpy(p.labels).cuda()
+    bad_np = p.labels.copy()
+    bad_np[17] = V
+    bad = torch.from_numpy(bad_np).cuda()
+    rows = torch.empty(T, dtype=torch.float32, device="cuda")
+    out = torch.empty(1, dtype=torch.float32, device="cuda")
+    stats = torch.empty(T, 4, dtype=torch.float32, device="cuda")
+    status = torch.empty(1, dtype=torch.int32, device="cuda")
+    first = None
+    for i in range(1100):
+        status.fill_(0x7FFF1234)
+        rows.fill_(float("nan"))
+        out.fill_(float("nan"))
+        lab = bad if i == 500 else labels
+        vce.ce_forward(logits, lab, reduction=reduction, loss_rows=rows, loss_out=out, row_stats=stats,
+                       status=status)
+        if i == 500:
+            assert vce.vce_get_status(status) == 1
+            assert np.isnan(rows[17].item())
+            continue
+        if i % 50 and i != 501:   # the status and outputs of every 50th call, and the one after the error
+            continue
+        assert vce.vce_get_status(status) == 0, i
+        got = (rows.clone(), stats.clone(), out.clone())
+        if first is None:
+            first = got
+            ref = O.ce(O.widen(p.full(), "bf16"), p.labels, "none")
+            G.check_loss_rows(got[0].cpu().numpy(), ref["loss_rows"], ref["valid"])
+        else:
+            assert torch.equal(got[0], first[0]) and torch.equal(got[1], first[1]), i
+            if reduction != "none":
+                assert torch.equal(got[2], first[2]), i
+    torch.cuda.synchronize()
+    assert vce.vce_get_status(status) == 0
+
+
 def test_forward_ring_beyond_the_folded_reduction(vce):
     """65540 rows of 32 KB + 16 B: more rows than the ring reduces in-kernel, so k_ce_reduce runs
     after it.  The MEAN call's loss is the fp64 mean of the same kernel's per-row losses (its

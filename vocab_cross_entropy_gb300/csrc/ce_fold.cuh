@@ -19,6 +19,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "ce_slots.cuh"
 #include "vce.h"
 
 namespace vce {
@@ -59,29 +60,23 @@ __device__ __forceinline__ int count_valid_strided(const int64_t* labels, int64_
     return n;
 }
 
-// Called by all NT threads of the block once every output of its rows is written (and, in a
-// cluster, after the closing cluster barrier).  err: the CTA's error word in shared memory;
-// n_all: the batch's valid labels; sm_sum, sm_comp: NT / 32 floats of shared memory; sm_last:
-// one int of shared memory.
+// The last CTA's reduction: every row's loss summed in a fixed order (thread i takes rows i,
+// i + NT, ...; lanes, then warps, merged in order) as an fp32 (sum, compensation) pair;
+// thread 0 writes the reduced loss.  All NT threads call it.
 template <int NT>
-__device__ __forceinline__ void finish(int32_t* status, const int* err, const float* loss_rows, int64_t T,
-                                       long long n_all, int red, float* loss_out, float* sm_sum, float* sm_comp,
-                                       int* sm_last) {
-    // Every thread's own stores (the rows' losses, weights, gradients) are made visible device-
-    // wide before the count moves: a fence orders only the fencing thread's writes, and the block
-    // barrier does not wait for other warps' global stores to be performed.
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        if (*err) status_merge(status, *err);
-        const int32_t prev = atomicAdd(status, 1 << 16);
-        *sm_last = ((prev >> 16) & 0xFFFF) == (int32_t)gridDim.x - 1;
-    }
-    __syncthreads();
-    if (!*sm_last) return;
-    __threadfence();
+__device__ __forceinline__ void sum_losses(const float* loss_rows, int64_t T, long long n_all, int red,
+                                           float* loss_out, float* sm_sum, float* sm_comp) {
     float sum = 0.f, comp = 0.f;
-    for (int64_t i = threadIdx.x; i < T; i += NT) add(sum, comp, __ldcg(loss_rows + i));
+    // up to eight loads in flight ahead of the (serial) additions, which take the rows in the
+    // same order as one at a time
+    for (int64_t i = threadIdx.x; i < T; i += 8 * NT) {
+        float v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) v[u] = i + u * NT < T ? __ldcg(loss_rows + i + u * NT) : 0.f;
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            if (i + u * NT < T) add(sum, comp, v[u]);
+    }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
         const float s2 = __shfl_xor_sync(0xFFFFFFFFu, sum, off);
@@ -103,7 +98,57 @@ __device__ __forceinline__ void finish(int32_t* status, const int* err, const fl
         }
         const double tot = isfinite(s) ? (double)s + (double)c : (double)s;
         *loss_out = red == VCE_RED_MEAN ? (float)(tot / (double)n_all) : (float)tot;   // 0/0: NaN
-        atomicAnd(status, 0xFFFF);   // the count goes; the first error code stays
+    }
+}
+
+// Called by all NT threads of the block once every output of its rows is written (and, in a
+// cluster, after the closing cluster barrier).  err: the CTA's error word in shared memory;
+// n_all: the batch's valid labels; sm_sum, sm_comp: NT / 32 floats of shared memory; sm_last:
+// one int of shared memory.  The count of finished CTAs sits in the status word's high bits.
+template <int NT>
+__device__ __forceinline__ void finish(int32_t* status, const int* err, const float* loss_rows, int64_t T,
+                                       long long n_all, int red, float* loss_out, float* sm_sum, float* sm_comp,
+                                       int* sm_last) {
+    // Every thread's own stores (the rows' losses, weights, gradients) are made visible device-
+    // wide before the count moves: a fence orders only the fencing thread's writes, and the block
+    // barrier does not wait for other warps' global stores to be performed.
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        if (*err) status_merge(status, *err);
+        const int32_t prev = atomicAdd(status, 1 << 16);
+        *sm_last = ((prev >> 16) & 0xFFFF) == (int32_t)gridDim.x - 1;
+    }
+    __syncthreads();
+    if (!*sm_last) return;
+    __threadfence();
+    sum_losses<NT>(loss_rows, T, n_all, red, loss_out, sm_sum, sm_comp);
+    if (threadIdx.x == 0) atomicAnd(status, 0xFFFF);   // the count goes; the first error code stays
+}
+
+// The same end for a kernel that holds a launch slot (ce_slots.cuh): the count and the first
+// error code sit in the slot; the last CTA reduces the losses if `reduce`, writes the status
+// word (the first code, or 0) and puts the slot back to zero.  Every claim on the slot's row
+// counter was made before its CTA got here.
+template <int NT>
+__device__ __forceinline__ void finish_slot(slots::LaunchSlot& slot, int32_t* status, const int* err, bool reduce,
+                                            const float* loss_rows, int64_t T, long long n_all, int red,
+                                            float* loss_out, float* sm_sum, float* sm_comp, int* sm_last) {
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        if (*err) atomicCAS(&slot.err, 0, *err);
+        const int prev = atomicAdd(&slot.done, 1);
+        *sm_last = prev == (int)gridDim.x - 1;
+    }
+    __syncthreads();
+    if (!*sm_last) return;
+    __threadfence();
+    if (reduce) sum_losses<NT>(loss_rows, T, n_all, red, loss_out, sm_sum, sm_comp);
+    if (threadIdx.x == 0) {
+        *status = atomicExch(&slot.err, 0);
+        atomicExch(&slot.done, 0);
+        atomicExch(&slot.rows, 0u);
     }
 }
 

@@ -483,8 +483,11 @@ extern "C" int ce_forward_ls(const void* logits, vce_dtype dt, int64_t T, int64_
     }
     if (red != VCE_RED_NONE && !aligned(loss_out, 4)) return VCE_ERR_ALIGN;
     if ((rc = require_sm100())) return rc;
-    if (cudaMemsetAsync(status, 0, sizeof(int32_t), s) != cudaSuccess) return VCE_ERR_CUDA;
     bool reduced = false;   // the ring kernel reduced the losses itself
+    // The ring kernel writes the status word itself (its launch slot carries the error code);
+    // every other path clears it first and merges codes into it.
+    auto clear_status = [&]() { return cudaMemsetAsync(status, 0, sizeof(int32_t), s) == cudaSuccess; };
+    if (T == 0 && !clear_status()) return VCE_ERR_CUDA;
     if (T > 0) {
         // Rows of at most 32 KB: one warp per row (k_ce_fwd_warp; 8192 x 16000 bf16: 0.070 ms,
         // against 0.080 on the stage ring and 0.102 on the ring's four consumer groups).  Longer
@@ -495,6 +498,7 @@ extern "C" int ce_forward_ls(const void* logits, vce_dtype dt, int64_t T, int64_
         const int64_t row_bytes = V * (int64_t)es;
         cudaError_t e = cudaSuccess;
         if (row_bytes <= 32768) {
+            if (!clear_status()) return VCE_ERR_CUDA;
             e = dt == VCE_BF16 ? launch_fwd_warp<uint16_t>(logits, T, V, ld, labels, ignore_index, label_smoothing,
                                                            loss_rows, row_stats, status, s)
                                : launch_fwd_warp<float>(logits, T, V, ld, labels, ignore_index, label_smoothing,
@@ -505,6 +509,7 @@ extern "C" int ce_forward_ls(const void* logits, vce_dtype dt, int64_t T, int64_
                                 row_stats, status, s, &launched, &reduced);
         }
         if (e == cudaSuccess && !launched) {
+            if (!clear_status()) return VCE_ERR_CUDA;
             const int nt = pick_threads(row_bytes);
             e = dt == VCE_BF16 ? dispatch_fwd<uint16_t>(nt, logits, T, V, ld, labels, ignore_index, label_smoothing,
                                                         loss_rows, row_stats, status, s)

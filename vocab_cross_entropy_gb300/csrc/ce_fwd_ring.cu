@@ -4,16 +4,21 @@
 // Method: torchtitan PR #5723 "[loss] fix softmax collapse with improved ce perf" (Numerics:
 // target-excluded log-sum-exp, softplus NLL) — the same per-row statistics as k_ce_fwd.
 //
-// One CTA per SM walks the valid rows blockIdx.x, blockIdx.x + gridDim.x, ... with three roles:
-//   producer warp   one lane streams each row into a ring of seven 32 KB stages with bulk
-//                   asynchronous copies (cp.async.bulk), completion counted on per-stage
-//                   mbarriers, and publishes each row's index and target column
+// One CTA per SM.  A CTA starts on row blockIdx.x and then claims rows one at a time from its
+// launch slot's counter (ce_slots.cuh): at 4096 x 32000 bf16 a fixed share of rows b, b +
+// gridDim.x, ... had the CTAs end their rows between 33.8 and 42.7 us (5% of the rows are
+// ignored and unevenly spread, and SMs do not all stream equally fast).  Three roles:
+//   producer warp   one lane claims the rows and streams each valid one into a ring of seven
+//                   32 KB stages with bulk asynchronous copies (cp.async.bulk), completion
+//                   counted on per-stage mbarriers, and publishes each row's index and target
+//                   column; after the last row, an end marker per consumer group
 //   consumer warps  in kGroups groups (1 or 2), group g taking the CTA's rows g, g + kGroups, ...; per
 //                   stage, a thread's 16-byte vectors summed four at a time into its (max,
 //                   sum-exp) pair (stage::fwd_stage); the stage goes back to the producer right
 //                   away; at the end of a row each warp of the group publishes its pair
 //   stats warp      merges the warps' pairs, finishes the row (loss, row statistics) and frees
-//                   the row's slots; it also writes the outputs of ignored and invalid rows
+//                   the row's slots; it also writes the outputs of the ignored and invalid rows
+//                   among blockIdx.x, blockIdx.x + gridDim.x, ...
 // Row hand-offs go through kSlots mbarrier-guarded slots, by the row's index in the CTA's
 // sequence mod kSlots; consumers wait for the stats warp to free a slot before writing it
 // again, kSlots rows later.  The bf16 row stream of k_ce_fwd is issue-bound (a thread keeps
@@ -28,16 +33,18 @@
 // and 0.0613 on one block per row.  Rows of one stage in 4 groups lost to one warp per row:
 // 8192 x 16000, 0.102 against 0.070 ms.)
 //
+// The CTA that finishes last writes the status word (the launch's first error code, or 0) and
+// puts the launch slot back to zero, so the caller's status word needs no clearing beforehand.
 // The loss reduction folded in (Args::fold, for SUM / MEAN with at most fold::kMaxRows rows;
 // ce_fold.cuh): the consumer warps count every valid label of the batch at the start, while the
 // first copies are in flight, so the stats warp writes each row's weight 1/N itself, and the
-// CTA that finishes last sums the rows' losses.  No separate reduction launch.
+// last CTA also sums the rows' losses.  No separate reduction launch.
 //
-// Every wait is bounded (2 s); a wait that gives up writes its code to the status word (105
-// free stage, 106 loaded stage, 108 warp partials, 110 free slots) and sets the CTA's abort
-// flag, after which every role keeps its arrivals but skips the work and later waits.  111:
-// consumer groups asked for rows too long for them (the kernel returns before any wait).  112:
-// the stats warp's wait for the consumer warps' label counts (folded reduction) gave up.
+// Every wait is bounded (2 s); a wait that gives up records its code (105 free stage, 106
+// loaded stage, 108 warp partials, 110 free slots) and sets the CTA's abort flag, after which
+// every role stops at its next wait.  111: consumer groups asked for rows too long for them
+// (the kernel writes the status word and returns before any wait).  112: the stats warp's wait
+// for the consumer warps' label counts (folded reduction) gave up.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -65,6 +72,7 @@ constexpr int kVecPerThread = kChunk / 16 / kConsumers;   // per 4-vector batch 
 constexpr uint32_t kSuspendNs = 0;       // plain polls (a suspend hint measured no faster here)
 constexpr int kSlots = 4;                // hand-off slots: consumers run up to kSlots rows ahead of the stats warp
 constexpr int kInfoSlots = 16;           // > the rows the producer can run ahead of the stats warp (kStages + kSlots)
+constexpr int kPre = 4;                  // fixed rows per CTA before the claimed ones
 static_assert(kVecPerThread * kConsumers * 16 == kChunk, "every consumer takes the same whole vectors of a stage");
 static_assert((kConsumerWarps & (kConsumerWarps - 1)) == 0 && kConsumerWarps <= 32, "warp pairs merge in one warp");
 enum { kErrEmpty = 105, kErrFull = 106, kErrPartials = 108, kErrSlots = 110, kErrGroups = 111, kErrCount = 112 };
@@ -106,6 +114,7 @@ struct Args {
     int fold;                          // reduce the losses in this kernel (SUM / MEAN)
     int red;                           // vce_reduction
     float* loss_out;                   // the reduced loss (fold)
+    int slot;                          // this launch's slot (ce_slots.cuh)
 };
 
 __device__ __forceinline__ bool label_valid(const Args& a, int64_t t) {
@@ -136,9 +145,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_fwd_ring(const __grid_consta
     const int64_t bytes = a.V * (int64_t)sizeof(S);
     const int nchunk = (int)((bytes + kChunk - 1) / kChunk);
     if (kGroups > 1 && nchunk * kUse > kStages) {   // rows too long for groups (the host never asks)
-        if (threadIdx.x == 0) atomicCAS(a.status, 0, (int32_t)kErrGroups);
+        if (threadIdx.x == 0 && blockIdx.x == 0) *a.status = kErrGroups;   // the slot stays untouched
         return;
     }
+    slots::LaunchSlot& slot = slots::g_launch_slots[a.slot];
 
     if (threadIdx.x == 0) {
         for (int st = 0; st < kStages; ++st) {
@@ -157,65 +167,91 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_fwd_ring(const __grid_consta
         tc::fence_mbar_init();
     }
     __syncthreads();
-    // error codes: the status word itself, or (folded reduction) the CTA's word, merged at the end
-    int32_t* errp = a.fold ? &ctl.err : a.status;
-
-    // The number of valid rows of this CTA (each warp counts for itself).
-    auto count_valid = [&]() {
-        int n = 0;
-#pragma unroll 4
-        for (int64_t row = blockIdx.x + (int64_t)lane * stride; row < a.T; row += 32 * stride)
-            n += label_valid(a, a.labels[row]);
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) n += __shfl_xor_sync(0xFFFFFFFFu, n, off);
-        return n;
-    };
+    // error codes: the CTA's word, merged into the launch slot at the end
+    int32_t* errp = &ctl.err;
 
     if (warp == kProducerWarp) {
         // ---------------- producer ----------------
-        // The warp reads the labels of 32 rows at a time (one per lane) and lane 0 issues the
-        // valid ones in order, so no copy waits on a label load of its own.
-        uint32_t q = 0, e = 0;
+        // A CTA's first kPre rows are fixed (blockIdx.x + k gridDim.x, k < kPre): the warp loads
+        // their labels at once and lane 0 issues the valid ones back to back, which fills the
+        // ring without waiting on anything.  Every later row is claimed one at a time, as
+        // kPre gridDim.x + the launch slot's count of earlier claims, so a CTA that streams
+        // faster takes more rows and all end within about a row of each other.  The first two
+        // claims go out before the fixed rows; after that, the claim of the row after next and
+        // the label of the next row are in flight while this row's copies wait for free stages.
+        // Rows whose label is not valid are skipped (the stats warp writes their outputs).
+        // After the last row, kGroups end markers (row -1) complete the first stage of the next
+        // kGroups rows without data.
+        uint32_t q = 0, e = 0, q_copies = 0;   // ring positions used; of them, by copies (lane 0)
         bool stop = false;
-        for (int64_t base = blockIdx.x; base < a.T && !stop; base += 32 * stride) {
-            const int64_t my = base + (int64_t)lane * stride;
-            const int64_t t_my = my < a.T ? a.labels[my] : 0;
-            uint32_t todo = __ballot_sync(0xFFFFFFFFu, my < a.T && label_valid(a, t_my));
-            while (todo && !stop) {
-                const int b = __ffs(todo) - 1;
-                todo &= todo - 1;
-                const int64_t t = __shfl_sync(0xFFFFFFFFu, t_my, b);
-                if (lane == 0) {
-                    const int64_t row = base + (int64_t)b * stride;
-                    ctl.info[e % kInfoSlots] = RowInfo{row, (int)t, 0};   // published with the first stage
-                    const char* src = static_cast<const char*>(a.logits) + row * a.ld * (int64_t)sizeof(S);
-                    for (int j = 0; j < nchunk; ++j) {
-                        const int st = (int)(q % kStages);
-                        if (!tc::mbar_wait(&ctl.empty[st], ((q / kStages) & 1) ^ 1, abort_flag, errp, kErrEmpty,
-                                           a.wait_ns, kSuspendNs)) {
-                            stop = true;
-                            break;
-                        }
-                        const uint32_t nb = (uint32_t)std::min<int64_t>(kChunk, bytes - (int64_t)j * kChunk);
-                        if (!dbg::ok(row < a.T && (int64_t)j * kChunk + nb <= bytes && a.V <= a.ld, dbg::kCols)) {
-                            *abort_flag = 1;   // no copy: the other roles stop at their next wait
-                            stop = true;
-                            break;
-                        }
-                        tc::mbar_arrive_expect_tx(&ctl.full[st], nb);
-                        tc::bulk_load(smem + st * kChunk, src + (int64_t)j * kChunk, nb, &ctl.full[st]);
-                        ++q;
-                    }
-                    ++e;
-                    stop = stop || *abort_flag;
+        auto issue = [&](int64_t row, int64_t t) {   // lane 0: the copies of a valid row
+            ctl.info[e % kInfoSlots] = RowInfo{row, (int)t, 0};   // published with the first stage
+            const char* src = static_cast<const char*>(a.logits) + row * a.ld * (int64_t)sizeof(S);
+            for (int j = 0; j < nchunk; ++j) {
+                const int st = (int)(q % kStages);
+                if (!tc::mbar_wait(&ctl.empty[st], ((q / kStages) & 1) ^ 1, abort_flag, errp, kErrEmpty, a.wait_ns,
+                                   kSuspendNs)) {
+                    stop = true;
+                    return;
                 }
-                stop = __shfl_sync(0xFFFFFFFFu, stop, 0);
+                const uint32_t nb = (uint32_t)std::min<int64_t>(kChunk, bytes - (int64_t)j * kChunk);
+                if (!dbg::ok(row < a.T && (int64_t)j * kChunk + nb <= bytes && a.V <= a.ld, dbg::kCols)) {
+                    *abort_flag = 1;   // no copy: the other roles stop at their next wait
+                    stop = true;
+                    return;
+                }
+                tc::mbar_arrive_expect_tx(&ctl.full[st], nb);
+                tc::bulk_load(smem + st * kChunk, src + (int64_t)j * kChunk, nb, &ctl.full[st]);
+                q_copies = ++q;
             }
+            ++e;
+            stop = stop || *abort_flag;
+        };
+        unsigned int c1 = 0, c2 = 0;
+        if (lane == 0) {
+            c1 = atomicAdd(&slot.rows, 1u);
+            c2 = atomicAdd(&slot.rows, 1u);
         }
-        if (lane == 0) {   // copies still in flight (only after an abort) land before the CTA may exit
-            int never = 0;
-            for (uint32_t p = q > (uint32_t)kStages ? q - kStages : 0; p < q; ++p)
-                tc::mbar_wait(&ctl.full[p % kStages], (p / kStages) & 1, &never, nullptr, 0, a.wait_ns);
+        const int64_t my = blockIdx.x + (int64_t)lane * stride;
+        const int64_t t_my = lane < kPre && my < a.T ? a.labels[my] : 0;
+        const uint32_t pre = __ballot_sync(0xFFFFFFFFu, lane < kPre && my < a.T && label_valid(a, t_my));
+#pragma unroll
+        for (int k = 0; k < kPre; ++k) {
+            const int64_t t = __shfl_sync(0xFFFFFFFFu, t_my, k);
+            if (lane == 0 && ((pre >> k) & 1u) && !stop) issue(blockIdx.x + (int64_t)k * stride, t);
+        }
+        if (lane == 0) {
+            const int64_t base = (int64_t)kPre * stride;
+            int64_t r0 = base + c1, r1 = base + c2;
+            int64_t t0 = r0 < a.T ? a.labels[r0] : 0;
+            while (r0 < a.T && !stop) {
+                const int64_t r2 = base + atomicAdd(&slot.rows, 1u);
+                const int64_t t1 = r1 < a.T ? a.labels[r1] : 0;
+                if (label_valid(a, t0)) issue(r0, t0);
+                r0 = r1;
+                t0 = t1;
+                r1 = r2;
+            }
+            for (int g = 0; g < kGroups && !stop; ++g) {   // end markers, one per consumer group
+                const int st = (int)(q % kStages);
+                if (!tc::mbar_wait(&ctl.empty[st], ((q / kStages) & 1) ^ 1, abort_flag, errp, kErrEmpty, a.wait_ns,
+                                   kSuspendNs))
+                    break;
+                ctl.info[e % kInfoSlots] = RowInfo{-1, -1, 0};
+                tc::mbar_arrive(&ctl.full[st]);
+                q += (uint32_t)nchunk;   // the marker stands for a whole row's positions
+                ++e;
+            }
+            // After an abort, copies still in flight land before the CTA may exit.  Only the last
+            // kStages positions can hold one, and only those no later marker refilled (a refill
+            // waited for the consumers to release the stage, so its copy had landed).
+            if (*abort_flag) {
+                int never = 0;
+                const uint32_t lo = q > (uint32_t)kStages ? q - kStages : 0;
+                for (uint32_t p = q_copies > (uint32_t)kStages ? q_copies - kStages : 0; p < q_copies; ++p)
+                    if (p >= lo)
+                        tc::mbar_wait(&ctl.full[p % kStages], (p / kStages) & 1, &never, nullptr, 0, a.wait_ns);
+            }
         }
         __syncwarp();
     } else if (warp == kStatsWarp) {
@@ -240,7 +276,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_fwd_ring(const __grid_consta
             }
         }
         __syncwarp();
-        const int nv = count_valid();
         // folded reduction: the batch's valid labels, counted by the consumer warps (MEAN weight)
         float w_valid = 1.f;
         if (a.fold) {
@@ -252,10 +287,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_fwd_ring(const __grid_consta
                 if (a.red == VCE_RED_MEAN) w_valid = n > 0 ? (float)(1.0 / (double)n) : 0.f;
             }
         }
-        for (int e = 0; e < nv; ++e) {
+        for (int e = 0;; ++e) {   // until the end marker
             const int par = e % kUse;
-            tc::mbar_wait(&ctl.rbar[par], (e / kUse) & 1, abort_flag, errp, kErrPartials, a.wait_ns,
-                          kSuspendNs);
+            const bool ok = tc::mbar_wait(&ctl.rbar[par], (e / kUse) & 1, abort_flag, errp, kErrPartials, a.wait_ns,
+                                          kSuspendNs);
+            if (!__all_sync(0xFFFFFFFFu, ok)) break;
+            const RowInfo ri = ctl.info[e % kInfoSlots];
+            if (ri.row < 0) break;
             float m = lane < kGW ? ctl.red_m[par][lane] : -kInf;
             float s = lane < kGW ? ctl.red_s[par][lane] : 0.f;
 #pragma unroll
@@ -268,10 +306,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_fwd_ring(const __grid_consta
             if (kSmooth && lane == 0)
                 for (int w = 0; w < kGW; ++w) tot += ctl.red_z[par][w];
             if (lane == 0) {
-                const RowInfo ri = ctl.info[e % kInfoSlots];
                 const float zt = ctl.zt[par];
                 tc::mbar_arrive(&ctl.fbar[par]);   // the slot may be rewritten
-                if (ri.row >= 0 && ri.row < a.T) {  // false only after an abort
+                if (ri.row < a.T) {
                     float loss;
                     float4 st4 = kSmooth ? ce_row_finish_smoothed(m, s, zt, tot, a.V, a.eps, &loss)
                                          : ce_row_finish(m, s, zt, &loss);
@@ -295,22 +332,33 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_fwd_ring(const __grid_consta
                 tc::mbar_arrive(&ctl.nbar);
             }
         }
-        const int nv = count_valid();
-        for (int e = grp; e < nv; e += kGroups) {
+        for (int e = grp;; e += kGroups) {   // until this group's end marker
             const int par = e % kUse;
             const uint32_t q = (uint32_t)e * (uint32_t)nchunk;   // ring chunk of the row's first chunk
             // the slot was read for row e - kUse
-            if (e >= kUse)
-                tc::mbar_wait(&ctl.fbar[par], ((e / kUse) & 1) ^ 1, abort_flag, errp, kErrSlots, a.wait_ns,
-                              kSuspendNs);
+            if (e >= kUse) {
+                const bool ok = tc::mbar_wait(&ctl.fbar[par], ((e / kUse) & 1) ^ 1, abort_flag, errp, kErrSlots,
+                                              a.wait_ns, kSuspendNs);
+                if (!__all_sync(0xFFFFFFFFu, ok)) break;
+            }
+            // the row's first stage, or its end marker
+            const bool ok0 = tc::mbar_wait(&ctl.full[q % kStages], (q / kStages) & 1, abort_flag, errp, kErrFull,
+                                           a.wait_ns, kSuspendNs);
+            if (!__all_sync(0xFFFFFFFFu, ok0)) break;
+            const RowInfo ri = ctl.info[e % kInfoSlots];
+            if (ri.row < 0) {   // no more rows: the stats warp learns it from the same slot
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&ctl.rbar[par]);
+                break;
+            }
+            const int tl = ri.tl;
             float m = -kInf, s = 0.f, mb = 0.f, sz = 0.f;
-            int tl = -1;
             for (int j = 0; j < nchunk; ++j) {
                 const uint32_t p = q + j;
                 const int st = (int)(p % kStages);
-                const bool ok = tc::mbar_wait(&ctl.full[st], (p / kStages) & 1, abort_flag, errp, kErrFull,
-                                              a.wait_ns, kSuspendNs);
-                if (j == 0) tl = ctl.info[e % kInfoSlots].tl;
+                const bool ok = j == 0 || __all_sync(0xFFFFFFFFu, tc::mbar_wait(&ctl.full[st], (p / kStages) & 1,
+                                                                                abort_flag, errp, kErrFull,
+                                                                                a.wait_ns, kSuspendNs));
                 if (ok) {
                     const uint4* buf = reinterpret_cast<const uint4*>(smem + st * kChunk);
                     const int nvec = (int)(std::min<int64_t>(kChunk, bytes - (int64_t)j * kChunk) / 16);
@@ -340,11 +388,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_fwd_ring(const __grid_consta
             if (lane == 0) tc::mbar_arrive(&ctl.rbar[par]);
         }
     }
-    if (!a.fold) return;
 
-    // ---------------- folded reduction ----------------
-    fold::finish<kThreads>(a.status, &ctl.err, a.loss_rows, a.T, ctl.n_all, a.red, a.loss_out, ctl.red_sum,
-                           ctl.red_comp, &ctl.last);
+    // ---------------- the launch's end: status word, folded reduction ----------------
+    fold::finish_slot<kThreads>(slot, a.status, &ctl.err, a.fold != 0, a.loss_rows, a.T, ctl.n_all, a.red,
+                                a.loss_out, ctl.red_sum, ctl.red_comp, &ctl.last);
 }
 
 template <typename S, int kGroups>
@@ -377,8 +424,9 @@ cudaError_t launch_fwd_ring(vce_dtype dt, const void* logits, int64_t T, int64_t
     // 16-byte rows: every row starts on a 16-byte boundary and is whole 16-byte vectors.
     if (T < 1 || V % 8 || ld % 8 || !aligned(logits, 16) || V > (int64_t)1 << 30) return cudaSuccess;
     const bool in_kernel = red != VCE_RED_NONE && T <= fold::kMaxRows;
-    Args args{logits, T, V, ld, labels, ignore_index, loss_rows, reinterpret_cast<float4*>(row_stats), status,
-              eps, tc::kWaitNs, in_kernel ? 1 : 0, red, loss_out};
+    Args args{logits,    T,   V,          ld,          labels,          ignore_index, loss_rows,
+              reinterpret_cast<float4*>(row_stats), status, eps, tc::kWaitNs, in_kernel ? 1 : 0, red, loss_out,
+              slots::next_slot()};
     const int sms = device_sm_count();
     const cudaError_t e = dt == VCE_BF16 ? launch<uint16_t>(args, sms, s) : launch<float>(args, sms, s);
     if (e == cudaSuccess) {
