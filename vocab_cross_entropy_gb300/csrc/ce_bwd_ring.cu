@@ -7,17 +7,20 @@
 // per-element arithmetic as k_ce_bwd (grad = coef * 2^(z log2 e - bias), the target entry gt).
 //
 // Items are (row, chunk) pairs of a segment table, row-major over its k chunks (k = 1 for a
-// [T, V] matrix).  One CTA per SM walks the items blockIdx.x, blockIdx.x + gridDim.x, ... with
-// three roles:
-//   producer warp   reads the row statistics of 32 items at a time (one per lane); lane 0
-//                   publishes each weighted item's row, chunk, coefficients (coef, bias, target
-//                   gradient, smoothing shift) and target column, and streams the item into a
-//                   ring of seven 32 KB stages with bulk asynchronous copies (cp.async.bulk)
+// [T, V] matrix).  One CTA per SM.  A CTA takes the items blockIdx.x + i gridDim.x, i < kPre,
+// and then claims items one at a time from its launch slot's counter (ce_slots.cuh), so the
+// CTAs end within about an item of each other instead of each owning a fixed share whose
+// weighted items vary.  Three roles:
+//   producer warp   lane 0 publishes each weighted item's row, chunk, coefficients (coef, bias,
+//                   target gradient, smoothing shift) and target column, and streams the item
+//                   into a ring of seven 32 KB stages with bulk asynchronous copies
+//                   (cp.async.bulk); after the last item, an end marker
 //   consumer warps  per stage, a thread's 4 x 16-byte vectors to gradient entries stored with
 //                   16-byte streaming stores (stage::bwd_stage); the stage goes back to the
 //                   producer right away
-//   zero warp       writes +0.0 over the gradient of items of weight 0 (ignored or invalid
-//                   labels), whose logits are not read
+//   zero warp       writes +0.0 over the gradient of the items of weight 0 (ignored or invalid
+//                   labels) among blockIdx.x, blockIdx.x + gridDim.x, ..., whose logits are not
+//                   read
 // Every wait is bounded (2 s).  A wait that gives up sets the CTA's abort flag; every role then
 // keeps its arrivals but skips the work and later waits.  ce_backward has no status word, so
 // the gradient is then undefined without a report.
@@ -27,6 +30,7 @@
 #include <algorithm>
 
 #include "ce_segments.h"
+#include "ce_slots.cuh"
 #include "ce_stage.cuh"
 #include "vce.h"
 #include "vce_async.cuh"
@@ -45,6 +49,7 @@ constexpr int kProducerWarp = kConsumerWarps, kZeroWarp = kConsumerWarps + 1;
 constexpr int kThreads = kConsumers + 64;
 constexpr int kVecPerThread = kChunk / 16 / kConsumers;
 constexpr int kInfoSlots = 16;         // > the rows the producer can run ahead (kStages, at one stage a row)
+constexpr int kPre = 4;                // fixed items per CTA before the claimed ones
 static_assert(kVecPerThread * kConsumers * 16 == kChunk, "every consumer takes the same whole vectors of a stage");
 
 // A weighted item of the CTA's sequence: where its gradient goes and how it is formed.
@@ -60,6 +65,7 @@ struct alignas(16) Ctl {
     uint64_t full[kStages];            // stage loaded
     uint64_t empty[kStages];           // stage released (one arrival per consumer warp)
     int abort;
+    int64_t last_claim;                // the producer's last claim, stored once its reply is in
 };
 constexpr int kSmemBytes = kStages * kChunk + (int)sizeof(Ctl);
 
@@ -70,6 +76,7 @@ struct Args {
     int go_per_row;
     float eps_over_v;                  // label smoothing eps / V (0: none)
     uint64_t wait_ns;
+    int slot;                          // this launch's slot (ce_slots.cuh)
 };
 
 template <typename S, typename O, bool kShift>
@@ -95,72 +102,100 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_bwd_ring(const __grid_consta
     }
     __syncthreads();
 
-    // The number of items of this CTA with a nonzero weight (each warp counts for itself).
-    auto count_valid = [&]() {
-        int n = 0;
-#pragma unroll 4
-        for (int64_t it = blockIdx.x + (int64_t)lane * stride; it < items; it += 32 * stride)
-            n += a.row_stats[it / tab.k].w != 0.f;
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) n += __shfl_xor_sync(0xFFFFFFFFu, n, off);
-        return n;
-    };
+    slots::LaunchSlot& slot = slots::g_launch_slots[a.slot];
 
     if (warp == kProducerWarp) {
         // ---------------- producer ----------------
-        uint32_t q = 0, e = 0;
+        // The fixed items' statistics and labels are loaded by the warp at once, so lane 0
+        // issues them back to back and the ring fills without waiting on anything.  Then the
+        // claim of the item after next and the statistics and label of the next item are in
+        // flight while this item's copies wait for free stages.
+        uint32_t q = 0, e = 0, q_copies = 0;   // ring positions used; of them, by copies (lane 0)
         bool stop = false;
-        for (int64_t base = blockIdx.x; base < items && !stop; base += 32 * stride) {
-            const int64_t my = base + (int64_t)lane * stride;
-            const float4 st_my = my < items ? a.row_stats[my / tab.k] : make_float4(0.f, 0.f, 0.f, 0.f);
-            uint32_t todo = __ballot_sync(0xFFFFFFFFu, st_my.w != 0.f);
-            while (todo && !stop) {
-                const int b = __ffs(todo) - 1;
-                todo &= todo - 1;
-                const float sx = __shfl_sync(0xFFFFFFFFu, st_my.x, b), sy = __shfl_sync(0xFFFFFFFFu, st_my.y, b);
-                const float sz = __shfl_sync(0xFFFFFFFFu, st_my.z, b), sw = __shfl_sync(0xFFFFFFFFu, st_my.w, b);
-                if (lane == 0) {
-                    const int64_t it = base + (int64_t)b * stride;
-                    const int64_t row = it / tab.k;
-                    const int c = (int)(it - row * tab.k);
-                    const int64_t t = a.labels[row], off = tab.off[c], w = tab.width[c];
-                    const float cg = a.grad_output[a.go_per_row ? row : 0] * sw;
-                    // the item's coefficients, published with its first stage
-                    ctl.info[e % kInfoSlots] = RowInfo{row, (t >= off && t < off + w) ? (int)(t - off) : -1, c,
-                                                       cg * sy, (sx == -kInf) ? 0.f : sx * kLog2e, cg * sz,
-                                                       cg * a.eps_over_v};
-                    const char* src = static_cast<const char*>(tab.in[c]) + row * tab.ld_in[c] * es;
-                    const int64_t bytes = w * es;
-                    const int nchunk = stages_of(c);
-                    for (int j = 0; j < nchunk; ++j) {
-                        const int st = (int)(q % kStages);
-                        if (!tc::mbar_wait(&ctl.empty[st], ((q / kStages) & 1) ^ 1, abort_flag, nullptr, 0,
-                                           a.wait_ns)) {
-                            stop = true;
-                            break;
-                        }
-                        const uint32_t nb = (uint32_t)std::min<int64_t>(kChunk, bytes - (int64_t)j * kChunk);
-                        if (!dbg::ok(row < tab.T && c < tab.k && (int64_t)j * kChunk + nb <= bytes &&
-                                         w <= tab.ld_in[c],
-                                     dbg::kCols)) {
-                            *abort_flag = 1;   // no copy: the other roles stop at their next wait
-                            stop = true;
-                            break;
-                        }
-                        tc::mbar_arrive_expect_tx(&ctl.full[st], nb);
-                        tc::bulk_load(smem + st * kChunk, src + (int64_t)j * kChunk, nb, &ctl.full[st]);
-                        ++q;
-                    }
-                    ++e;
-                    stop = stop || *abort_flag;
+        auto issue = [&](int64_t it, float4 st, int64_t t) {   // lane 0: a weighted item
+            const int64_t row = it / tab.k;
+            const int c = (int)(it - row * tab.k);
+            const int64_t off = tab.off[c], w = tab.width[c];
+            const float cg = a.grad_output[a.go_per_row ? row : 0] * st.w;
+            // the item's coefficients, published with its first stage
+            ctl.info[e % kInfoSlots] = RowInfo{row, (t >= off && t < off + w) ? (int)(t - off) : -1, c, cg * st.y,
+                                               (st.x == -kInf) ? 0.f : st.x * kLog2e, cg * st.z, cg * a.eps_over_v};
+            const char* src = static_cast<const char*>(tab.in[c]) + row * tab.ld_in[c] * es;
+            const int64_t bytes = w * es;
+            const int nchunk = stages_of(c);
+            for (int j = 0; j < nchunk; ++j) {
+                const int st_i = (int)(q % kStages);
+                if (!tc::mbar_wait(&ctl.empty[st_i], ((q / kStages) & 1) ^ 1, abort_flag, nullptr, 0, a.wait_ns)) {
+                    stop = true;
+                    return;
                 }
-                stop = __shfl_sync(0xFFFFFFFFu, stop, 0);
+                const uint32_t nb = (uint32_t)std::min<int64_t>(kChunk, bytes - (int64_t)j * kChunk);
+                if (!dbg::ok(row < tab.T && c < tab.k && (int64_t)j * kChunk + nb <= bytes && w <= tab.ld_in[c],
+                             dbg::kCols)) {
+                    *abort_flag = 1;   // no copy: the other roles stop at their next wait
+                    stop = true;
+                    return;
+                }
+                tc::mbar_arrive_expect_tx(&ctl.full[st_i], nb);
+                tc::bulk_load(smem + st_i * kChunk, src + (int64_t)j * kChunk, nb, &ctl.full[st_i]);
+                q_copies = ++q;
             }
+            ++e;
+            stop = stop || *abort_flag;
+        };
+        unsigned int c1 = 0, c2 = 0;
+        if (lane == 0) {
+            c1 = atomicAdd(&slot.rows, 1u);
+            c2 = atomicAdd(&slot.rows, 1u);
         }
-        if (lane == 0) {   // copies still in flight (only after an abort) land before the CTA may exit
-            int never = 0;
-            for (uint32_t p = q > (uint32_t)kStages ? q - kStages : 0; p < q; ++p)
-                tc::mbar_wait(&ctl.full[p % kStages], (p / kStages) & 1, &never, nullptr, 0, a.wait_ns);
+        const int64_t my = blockIdx.x + (int64_t)lane * stride;
+        const bool mine = lane < kPre && my < items;
+        const float4 st_my = mine ? a.row_stats[my / tab.k] : make_float4(0.f, 0.f, 0.f, 0.f);
+        const int64_t t_my = mine ? a.labels[my / tab.k] : 0;
+        const uint32_t pre = __ballot_sync(0xFFFFFFFFu, mine && st_my.w != 0.f);
+#pragma unroll
+        for (int k = 0; k < kPre; ++k) {
+            const float4 st = make_float4(__shfl_sync(0xFFFFFFFFu, st_my.x, k), __shfl_sync(0xFFFFFFFFu, st_my.y, k),
+                                          __shfl_sync(0xFFFFFFFFu, st_my.z, k), __shfl_sync(0xFFFFFFFFu, st_my.w, k));
+            const int64_t t = __shfl_sync(0xFFFFFFFFu, t_my, k);
+            if (lane == 0 && ((pre >> k) & 1u) && !stop) issue(blockIdx.x + (int64_t)k * stride, st, t);
+        }
+        if (lane == 0) {
+            const int64_t base = (int64_t)kPre * stride;
+            const float4 none = make_float4(0.f, 0.f, 0.f, 0.f);
+            int64_t i0 = base + c1, i1 = base + c2;
+            float4 s0 = i0 < items ? a.row_stats[i0 / tab.k] : none;
+            int64_t t0 = i0 < items ? a.labels[i0 / tab.k] : 0;
+            while (i0 < items && !stop) {
+                const int64_t i2 = base + atomicAdd(&slot.rows, 1u);
+                const float4 s1 = i1 < items ? a.row_stats[i1 / tab.k] : none;
+                const int64_t t1 = i1 < items ? a.labels[i1 / tab.k] : 0;
+                if (s0.w != 0.f) issue(i0, s0, t0);
+                i0 = i1;
+                s0 = s1;
+                t0 = t1;
+                i1 = i2;
+            }
+            // Wait for the last claim's reply: every claim on the slot's counter has landed before
+            // this CTA counts itself finished, so the last CTA's reset of it comes after them all.
+            *reinterpret_cast<volatile int64_t*>(&ctl.last_claim) = i1;
+            if (!stop) {   // the end marker: the next item's first stage completes without data
+                const int st_i = (int)(q % kStages);
+                if (tc::mbar_wait(&ctl.empty[st_i], ((q / kStages) & 1) ^ 1, abort_flag, nullptr, 0, a.wait_ns)) {
+                    ctl.info[e % kInfoSlots] = RowInfo{-1, -1, 0, 0.f, 0.f, 0.f, 0.f};
+                    tc::mbar_arrive(&ctl.full[st_i]);
+                    ++q;
+                }
+            }
+            // After an abort, copies still in flight land before the CTA may exit.  Only the last
+            // kStages positions can hold one, and only those the marker did not refill.
+            if (*abort_flag) {
+                int never = 0;
+                const uint32_t lo = q > (uint32_t)kStages ? q - kStages : 0;
+                for (uint32_t p = q_copies > (uint32_t)kStages ? q_copies - kStages : 0; p < q_copies; ++p)
+                    if (p >= lo)
+                        tc::mbar_wait(&ctl.full[p % kStages], (p / kStages) & 1, &never, nullptr, 0, a.wait_ns);
+            }
         }
         __syncwarp();
     } else if (warp == kZeroWarp) {
@@ -183,25 +218,24 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_bwd_ring(const __grid_consta
     } else {
         // ---------------- consumers ----------------
         const int tid = threadIdx.x;
-        const int nv = count_valid();
         uint32_t q = 0;   // ring chunk of the current item's first stage
-        for (int e = 0; e < nv; ++e) {
-            RowInfo ri{-1, -1, 0, 0.f, 0.f, 0.f, 0.f};
-            O* grow = nullptr;
-            int nchunk = 1;
-            int64_t bytes = 0;
+        for (int e = 0;; ++e) {   // until the end marker
+            // the item is known once its first stage (or the end marker) has landed
+            const bool ok0 = tc::mbar_wait(&ctl.full[q % kStages], (q / kStages) & 1, abort_flag, nullptr, 0,
+                                           a.wait_ns);
+            if (!__all_sync(0xFFFFFFFFu, ok0)) break;
+            const RowInfo ri = ctl.info[e % kInfoSlots];
+            if (ri.row < 0) break;
+            const bool in_range = ri.row < tab.T && ri.c >= 0 && ri.c < tab.k;
+            const int c = in_range ? ri.c : 0;
+            O* grow = in_range ? static_cast<O*>(tab.out[c]) + ri.row * tab.ld_out[c] : nullptr;
+            const int64_t bytes = tab.width[c] * es;
+            const int nchunk = stages_of(c);
             for (int j = 0; j < nchunk; ++j) {
                 const uint32_t p = q + j;
                 const int st = (int)(p % kStages);
-                const bool ok = tc::mbar_wait(&ctl.full[st], (p / kStages) & 1, abort_flag, nullptr, 0, a.wait_ns);
-                if (j == 0) {   // the item is known once its first stage has landed
-                    ri = ctl.info[e % kInfoSlots];
-                    const bool in_range = ri.row >= 0 && ri.row < tab.T && ri.c >= 0 && ri.c < tab.k;   // else: aborted
-                    const int c = in_range ? ri.c : 0;
-                    grow = in_range ? static_cast<O*>(tab.out[c]) + ri.row * tab.ld_out[c] : nullptr;
-                    bytes = tab.width[c] * es;
-                    nchunk = stages_of(c);
-                }
+                const bool ok = j == 0 || tc::mbar_wait(&ctl.full[st], (p / kStages) & 1, abort_flag, nullptr, 0,
+                                                        a.wait_ns);
                 if (ok && grow && !*abort_flag) {
                     const uint4* buf = reinterpret_cast<const uint4*>(smem + st * kChunk);
                     const int nvec = (int)(std::min<int64_t>(kChunk, bytes - (int64_t)j * kChunk) / 16);
@@ -220,6 +254,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_bwd_ring(const __grid_consta
                 if (lane == 0) tc::mbar_arrive(&ctl.empty[st]);
             }
             q += nchunk;
+        }
+    }
+
+    // ---------------- the launch's end: the launch slot goes back to zero ----------------
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        if (atomicAdd(&slot.done, 1) == (int)gridDim.x - 1) {
+            __threadfence();
+            atomicExch(&slot.rows, 0u);
+            atomicExch(&slot.done, 0);
         }
     }
 }
@@ -251,7 +296,7 @@ cudaError_t launch_bwd_ring(vce_dtype dt, vce_dtype gdt, const SegTable& tab, co
             !aligned(tab.out[c], 16) || tab.width[c] > ((int64_t)1 << 30) / std::max(es, gs))
             return cudaSuccess;
     const Args args{labels, reinterpret_cast<const float4*>(row_stats), grad_output, go_per_row, eps_over_v,
-                    tc::kWaitNs};
+                    tc::kWaitNs, slots::next_slot()};
     cudaError_t e;
     if (dt == VCE_BF16 && gdt == VCE_BF16) e = launch<uint16_t, uint16_t>(args, tab, s);
     else if (dt == VCE_BF16) e = launch<uint16_t, float>(args, tab, s);

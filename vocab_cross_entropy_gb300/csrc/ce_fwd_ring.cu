@@ -98,6 +98,7 @@ struct alignas(16) Ctl {
     int err;                           // first error code of the CTA (folded reduction)
     int last;                          // this CTA finished last (folded reduction)
     int abort;
+    int64_t last_claim;                // the producer's last claim, stored once its reply is in
 };
 constexpr int kSmemBytes = kStages * kChunk + (int)sizeof(Ctl);
 
@@ -232,6 +233,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_fwd_ring(const __grid_consta
                 t0 = t1;
                 r1 = r2;
             }
+            // Wait for the last claim's reply: every claim on the slot's counter has landed before
+            // this CTA counts itself finished, so the last CTA's reset of it comes after them all.
+            *reinterpret_cast<volatile int64_t*>(&ctl.last_claim) = r1;
             for (int g = 0; g < kGroups && !stop; ++g) {   // end markers, one per consumer group
                 const int st = (int)(q % kStages);
                 if (!tc::mbar_wait(&ctl.empty[st], ((q / kStages) & 1) ^ 1, abort_flag, errp, kErrEmpty, a.wait_ns,
