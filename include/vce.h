@@ -40,7 +40,15 @@
  *   - Per-row losses and reduced losses are fp32 whatever the logits dtype.
  *   - Return value: VCE_OK, or a negative host-detected error (nothing was
  *     enqueued in that case).  Device-detected errors go to *status; read it after
- *     the stream has run (vce_get_status does that).
+ *     the stream has run (vce_get_status does that).  *status need not be cleared
+ *     before a call: every call writes it.
+ *   - The stage-ring kernels of ce_forward, ce_backward and ce_forward_backward
+ *     share a launch slot of device words across their CTAs (dynamic row claims,
+ *     the count of finished CTAs, the first error code), taken round-robin from
+ *     1024 slots per kernel file and left zero by the launch's last CTA.  At most
+ *     1024 launches of one of these kernels may therefore be in flight at once,
+ *     across all streams and host threads of a process (a graph replays the slot
+ *     it was captured with: do not run one graph's replays concurrently).
  */
 #ifndef VCE_H
 #define VCE_H

@@ -486,6 +486,36 @@ def test_forward_ring_launch_slots(vce, reduction):
     assert vce.vce_get_status(status) == 0
 
 
+@pytest.mark.parametrize("V", [20000, 70000])
+def test_backward_ring_launch_slots(vce, V):
+    """The backward ring claims items from a per-launch slot that its last CTA puts back to zero:
+    1100 calls (more than the 1024 slots) into a gradient filled with NaN every 50 calls give the
+    same gradient, bit for bit, and the first one matches the oracle."""
+    T = 300
+    p = gen.custom(T, V, "bf16", seed=V + 3, std=2.0, n_margin=8, n_ignore=30)
+    storage = p.full()
+    logits = to_device(storage, "bf16")
+    labels = torch.from_numpy(p.labels).cuda()
+    _, _, stats, status = vce.ce_forward(logits, labels, reduction="mean")
+    assert vce.vce_get_status(status) == 0
+    go = torch.ones(1, device="cuda")
+    grad = torch.empty_like(logits)
+    first = None
+    for i in range(1100):
+        if i % 50 == 0:
+            grad.fill_(float("nan"))
+        vce.ce_backward(logits, labels, stats, go, grad_logits=grad)
+        if i % 50:
+            continue
+        if first is None:
+            first = grad.clone()
+            ref = O.ce(O.widen(storage, "bf16"), p.labels, "mean")
+            grade_grad(first, ref["grad"], p.margin_rows, p.labels)
+        else:
+            assert torch.equal(grad, first), i
+    torch.cuda.synchronize()
+
+
 def test_forward_ring_beyond_the_folded_reduction(vce):
     """65540 rows of 32 KB + 16 B: more rows than the ring reduces in-kernel, so k_ce_reduce runs
     after it.  The MEAN call's loss is the fp64 mean of the same kernel's per-row losses (its

@@ -204,6 +204,58 @@ def test_fused_pages_shape(vce):
     G.check_grad_bf16(G.bf16_tensor_bits(grad[torch.from_numpy(rr).cuda()]), want)
 
 
+@pytest.mark.parametrize("V,reduction", [(70000, "mean"), (70000, "none"), (20000, "sum")])
+def test_one_pass_launch_slots(vce, V, reduction):
+    """The one-pass ring claims rows from a per-launch slot of device words that its last CTA
+    puts back to zero (2-CTA clusters at V = 70000: the cluster's first CTA hands each claim to
+    its peer), and writes the status word itself.  1100 calls (more than the 1024 slots) into a
+    status word filled with garbage and outputs filled with NaN each time: every checked call's
+    status is 0 and its outputs equal the first call's, bit for bit; a call with a bad label in
+    the middle sets VCE_ERR_LABEL and the calls after it are clean."""
+    T = 300
+    p = gen.custom(T, V, "bf16", seed=V + 5, std=2.0, n_margin=8, n_ignore=30)
+    storage = p.full()
+    logits = to_device(storage, "bf16")
+    labels = torch.from_numpy(p.labels).cuda()
+    bad_np = p.labels.copy()
+    bad_np[41] = -9
+    bad = torch.from_numpy(bad_np).cuda()
+    go = torch.ones(T if reduction == "none" else 1, device="cuda")
+    rows = torch.empty(T, dtype=torch.float32, device="cuda")
+    out = torch.empty(1, dtype=torch.float32, device="cuda")
+    stats = torch.empty(T, 4, dtype=torch.float32, device="cuda")
+    grad = torch.empty_like(logits)
+    status = torch.empty(1, dtype=torch.int32, device="cuda")
+    first = None
+    for i in range(1100):
+        status.fill_(0x7FFF1234)
+        if i % 50 == 0 or i in (500, 501):
+            rows.fill_(float("nan"))
+            out.fill_(float("nan"))
+            grad.fill_(float("nan"))
+        lab = bad if i == 500 else labels
+        vce.ce_forward_backward(logits, lab, reduction=reduction, grad_output=go, grad_logits=grad, loss_rows=rows,
+                                loss_out=out, row_stats=stats, status=status)
+        if i == 500:
+            assert vce.vce_get_status(status) == 1
+            assert np.isnan(rows[41].item())
+            continue
+        if i % 50 and i != 501:
+            continue
+        assert vce.vce_get_status(status) == 0, i
+        got = (rows.clone(), stats.clone(), grad.clone(), out.clone())
+        if first is None:
+            first = got
+            check_against_oracle(p, storage, got[3], got[0], got[2], reduction)
+        else:
+            for x, y in zip(got[:3], first[:3]):
+                assert torch.equal(x, y), i
+            if reduction != "none":
+                assert torch.equal(got[3], first[3]), i
+    torch.cuda.synchronize()
+    assert vce.vce_get_status(status) == 0
+
+
 def test_stalled_ring_gives_up_and_the_context_survives(vce):
     """Stages that never complete (2-CTA clusters): the bounded waits give up with a status code,
     the kernel returns within seconds, and the next one-pass call on the same context is correct."""

@@ -174,19 +174,24 @@ extern "C" int ce_forward_backward_ls(const void* logits, vce_dtype dt, int64_t 
     if (red != VCE_RED_NONE && !aligned(loss_out, 4)) return VCE_ERR_ALIGN;
     int rc = require_sm100();
     if (rc) return rc;
-    // The ring kernel counts N and reduces the losses itself where it can (SUM / MEAN, at most
-    // 65536 rows): the status word is cleared for it.  Otherwise the mean's weight 1/N comes
-    // first (k_ce_count_valid, which also clears the status word) and k_ce_reduce last.
-    const bool ring_reduces = T > 0 && fused_ring_reduces(red, T) &&
-                              fused_ring_layout_ok(dt, T, V, ld, ld_grad, logits, grad_logits);
+    // The ring kernel writes the status word itself (its launch slot carries the error code), and
+    // it counts N and reduces the losses itself where it can (SUM / MEAN, at most 65536 rows).
+    // Otherwise the mean's weight 1/N comes first (k_ce_count_valid, which also clears the
+    // status word) and k_ce_reduce last; the L2 re-read kernel needs the status word cleared.
+    const bool ring_ok = T > 0 && fused_ring_layout_ok(dt, T, V, ld, ld_grad, logits, grad_logits);
+    const bool ring_reduces = ring_ok && fused_ring_reduces(red, T);
     auto count_first = [&]() {
         k_ce_count_valid<1024><<<1, 1024, 0, s>>>(labels, T, V, ignore_index, loss_out, status);
         return cudaGetLastError() == cudaSuccess;
     };
+    auto clear_status = [&]() { return cudaMemsetAsync(status, 0, sizeof(int32_t), s) == cudaSuccess; };
+    bool cleared = false;
     if (T > 0 && red == VCE_RED_MEAN && !ring_reduces) {
         if (!count_first()) return VCE_ERR_CUDA;
-    } else if (cudaMemsetAsync(status, 0, sizeof(int32_t), s) != cudaSuccess) {
-        return VCE_ERR_CUDA;
+        cleared = true;
+    } else if (!ring_ok) {
+        if (!clear_status()) return VCE_ERR_CUDA;
+        cleared = true;
     }
     bool reduced = false;
     if (T > 0) {
@@ -196,9 +201,13 @@ extern "C" int ce_forward_backward_ls(const void* logits, vce_dtype dt, int64_t 
         cudaError_t e = launch_fused_ring(dt, grad_dt, logits, T, V, ld, labels, ignore_index, red, grad_output,
                                           loss_out, loss_rows, row_stats, grad_logits, ld_grad, status, s, &launched,
                                           eps, 2000000000ull, 0, ring_reduces ? &reduced : nullptr, loss_out);
-        // no cluster fitted after all: the fallback needs the mean's weight first
-        if (e == cudaSuccess && !launched && ring_reduces && red == VCE_RED_MEAN && !count_first())
-            return VCE_ERR_CUDA;
+        // no cluster fitted after all: the fallback needs the mean's weight first, and a cleared
+        // status word
+        if (e == cudaSuccess && !launched && ring_reduces && red == VCE_RED_MEAN) {
+            if (!count_first()) return VCE_ERR_CUDA;
+            cleared = true;
+        }
+        if (e == cudaSuccess && !launched && !cleared && !clear_status()) return VCE_ERR_CUDA;
         if (e == cudaSuccess && !launched) {
             const int nt = pick_threads(V * (int64_t)es);
             if (dt == VCE_BF16 && grad_dt == VCE_BF16)

@@ -12,10 +12,14 @@
 // A row of a 128256-entry vocabulary in bf16 (250.5 KB) does not fit one SM's shared memory,
 // so a cluster of C CTAs on C SMs takes it, each CTA a column slice of at most 128 KB of its
 // stage ring (224 KB: seven 32 KB stages, or fourteen 16 KB stages for bf16 rows in a cluster).
-// Each CTA (one per SM) walks the valid rows of its cluster in order, with three roles:
+// A cluster walks the rows cid, cid + ncl, ... (cid: the cluster's index, ncl: the clusters);
+// a single CTA, for rows of at most 128 KB, takes four such rows and then claims rows one at a
+// time from its launch slot (ce_slots.cuh), so the CTAs end within about a row of each other.
+// Each CTA (one per SM) skips the rows whose label is not valid and has three roles:
 //   producer warp   one lane streams each row's slice into the shared-memory stage ring
 //                   with bulk asynchronous copies (cp.async.bulk; completion counted
-//                   on a per-stage mbarrier), running ahead into later rows as stages free up
+//                   on a per-stage mbarrier), running ahead into later rows as stages free up;
+//                   after the last row, an end marker that the other roles stop at
 //   consumer warps  forward of a row over its held stages (per-thread (max, sum-exp) pairs,
 //                   the target masked out by its column), each warp's pair published to shared
 //                   memory; then, while the row's statistics are being finished, the forward
@@ -32,18 +36,19 @@
 // the CTA's sequence: a slot of one parity is rewritten two rows later, after every reader of
 // it has arrived on a barrier the writer waits for.
 //
-// The loss reduction folded in (Args::fold, for SUM / MEAN over at most fold::kMaxRows rows;
+// The CTA that finishes last writes the status word (the launch's first error code, or 0) and
+// puts the launch slot back to zero, so the caller's status word needs no clearing first.  The
+// loss reduction folded in (Args::fold, for SUM / MEAN over at most fold::kMaxRows rows;
 // ce_fold.cuh): the consumer warps count the batch's valid labels before their first row, so the
 // stats warp has 1/N for the row weights and gradient coefficients without a counting kernel
-// before this one, and the CTA that finishes last sums the rows' losses; no reduction kernel
-// after it either.
+// before this one, and the last CTA also sums the rows' losses; no reduction kernel after it
+// either.
 //
-// Every wait is bounded (2 s).  A wait that gives up writes its code to the status word
-// (105 free stage, 106 loaded stage, 107 cluster exchange, 108 warp partials, 109 row
-// coefficients) and sets the CTA's abort flag; the CTA then keeps every arrival (stage
-// releases, exchange, hand-offs) but skips the work and later waits, so no peer or warp is
-// left waiting on it, and the producer waits, again bounded, for its copies in flight before
-// the CTA reaches the closing cluster barrier.
+// Every wait is bounded (2 s).  A wait that gives up records its code (105 free stage, 106
+// loaded stage, 107 cluster exchange, 108 warp partials, 109 row coefficients) and sets the
+// CTA's abort flag; its roles then stop at their next wait (a peer waiting on this CTA's
+// exchange gives up in turn, bounded), and the producer waits, again bounded, for its copies
+// in flight before the CTA reaches the closing cluster barrier.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -101,6 +106,7 @@ struct RowInfo {
 };
 constexpr int kInfoSlots = 16;         // > the rows the producer can run ahead (kStages at one chunk a row; a
                                        // cluster's slices are more than four 16 KB stages)
+constexpr int kPre = 4;                // a single CTA's fixed rows before the claimed ones
 
 struct alignas(16) Ctl {
     RowInfo info[kInfoSlots];          // by the row's index in the sequence, mod kInfoSlots
@@ -118,9 +124,10 @@ struct alignas(16) Ctl {
     int nwarp[kConsumerWarps];         // each consumer warp's count of the batch's valid labels
     long long n_all;                   // the batch's valid labels (stats warp)
     float red_sum[kThreads / 32], red_comp[kThreads / 32];   // the last CTA's loss sum, per warp
-    int err;                           // first error code of the CTA (folded reduction)
-    int last;                          // this CTA finished last (folded reduction)
+    int err;                           // first error code of the CTA
+    int last;                          // this CTA finished last
     int abort;
+    int64_t last_claim;                // a single CTA's last claim, stored once its reply is in
 };
 constexpr int kSmemBytes = kRingBytes + (int)sizeof(Ctl);
 
@@ -143,6 +150,7 @@ struct Args {
     float eps;                         // label smoothing (k_ce_fused_ring<S, O, C, true> only)
     int fold;                          // reduce the losses in this kernel (SUM / MEAN; inv_n unused)
     float* loss_out;                   // the reduced loss (fold)
+    int slot;                          // this launch's slot (ce_slots.cuh)
 };
 
 // ---- cluster and bulk-copy primitives (inline PTX) -----------------------------------------
@@ -251,49 +259,108 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_fused_ring(const __grid_cons
     }
     if (C > 1) cluster_sync();   // peers arrive on these barriers from now on
     else __syncthreads();
-    // error codes: the status word itself, or (folded reduction) the CTA's word, merged at the end
-    int32_t* errp = a.fold ? &ctl.err : a.status;
-
-    // The number of valid rows of this cluster (each warp counts for itself).
-    auto count_valid = [&]() {
-        int n = 0;
-#pragma unroll 4
-        for (int64_t row = cid + (int64_t)lane * ncl; row < a.T; row += 32 * ncl) n += label_valid(a, a.labels[row]);
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) n += __shfl_xor_sync(0xFFFFFFFFu, n, off);
-        return n;
-    };
+    // error codes: the CTA's word, merged into the launch slot at the end
+    int32_t* errp = &ctl.err;
+    slots::LaunchSlot& slot = slots::g_launch_slots[a.slot];
 
     if (warp == kProducerWarp) {
         // ---------------- producer ----------------
+        // A single CTA takes its first kPre rows fixed (blockIdx.x + k gridDim.x, k < kPre) and
+        // then claims rows one at a time from the launch slot's counter (kPre gridDim.x + the
+        // count of earlier claims), so a CTA that streams faster takes more rows.  The claims of
+        // the next three rows and the label of the next row are in flight while this row's
+        // copies wait for free stages.  A cluster walks the fixed rows cid, cid + ncl, ...: a
+        // claim would have to reach every CTA of the cluster, and handing each one on through
+        // the peers' shared memory cost more (pages' shape, 2-CTA clusters: 1.37-1.46 ms against
+        // 1.33-1.34 ms) than the balance gained.  Rows whose label is not valid are skipped (the
+        // consumer warps zero-fill their gradients).  After the last row, an end marker (row -1)
+        // completes the next row's first stage without data.
         if (lane == 0) {
-            uint32_t q = 0, e = 0;
-            for (int64_t row = next_valid(a, cid, ncl); row < a.T && !*abort_flag;
-                 row = next_valid(a, row + ncl, ncl), ++e) {
+            uint32_t q = 0, e = 0, q_copies = 0;   // ring positions used; of them, by copies
+            bool stop = false;
+            auto issue = [&](int64_t row, int64_t t) {   // the copies of a valid row
                 // the row's index and target column, for the other roles (published by the first
                 // chunk's barrier arrival)
-                ctl.info[e % kInfoSlots] = RowInfo{row, (int)(a.labels[row] - c0), 0};
+                ctl.info[e % kInfoSlots] = RowInfo{row, (int)(t - c0), 0};
                 const char* src = static_cast<const char*>(a.logits) + (row * a.ld + c0) * (int64_t)sizeof(S);
                 for (int j = 0; j < nchunk; ++j) {
                     const int st = (int)(q % kStages);
                     if (!tc::mbar_wait(&ctl.empty[st], ((q / kStages) & 1) ^ 1, abort_flag, errp, kErrEmpty,
-                                       a.wait_ns, kSuspendRole))
-                        break;
+                                       a.wait_ns, kSuspendRole)) {
+                        stop = true;
+                        return;
+                    }
                     const uint32_t nb = (uint32_t)min(kChunk, bytes - j * kChunk);
                     if (!dbg::ok(row < a.T && c0 + w <= a.V && a.V <= a.ld && j * kChunk + (int)nb <= bytes,
                                  dbg::kCols)) {
                         *abort_flag = 1;   // no copy: the other roles stop at their next wait
-                        break;
+                        stop = true;
+                        return;
                     }
                     tc::mbar_arrive_expect_tx(&ctl.full[st], nb + a.tx_extra);
                     tc::bulk_load(smem + st * kChunk, src + (int64_t)j * kChunk, nb, &ctl.full[st]);
+                    q_copies = ++q;
+                }
+                ++e;
+                stop = stop || *abort_flag;
+            };
+            const int64_t base = (int64_t)kPre * ncl;
+            unsigned int c1 = 0, c2 = 0, c3 = 0;
+            if (C == 1) {   // the first three claims go out before the fixed rows
+                c1 = atomicAdd(&slot.rows, 1u);
+                c2 = atomicAdd(&slot.rows, 1u);
+                c3 = atomicAdd(&slot.rows, 1u);
+            }
+            int64_t tp[kPre];
+#pragma unroll
+            for (int k = 0; k < kPre; ++k) {
+                const int64_t row = cid + (int64_t)k * ncl;
+                tp[k] = row < a.T ? a.labels[row] : 0;
+            }
+#pragma unroll
+            for (int k = 0; k < kPre; ++k) {
+                const int64_t row = cid + (int64_t)k * ncl;
+                if (row < a.T && label_valid(a, tp[k]) && !stop) issue(row, tp[k]);
+            }
+            // Rows r0, r1, r2: the next three of the sequence (the claims' replies are taken even
+            // after an abort: see below).
+            auto fixed = [&](uint32_t k) { return base + (int64_t)k * ncl + cid; };
+            int64_t r0 = C == 1 ? base + c1 : fixed(0);
+            int64_t r1 = C == 1 ? base + c2 : fixed(1);
+            int64_t r2 = C == 1 ? base + c3 : fixed(2);
+            uint32_t k_next = 3;
+            int64_t t0 = r0 < a.T ? a.labels[r0] : 0;
+            while (r0 < a.T && !stop) {
+                const int64_t r3 = C == 1 ? base + atomicAdd(&slot.rows, 1u) : fixed(k_next);
+                const int64_t t1 = r1 < a.T ? a.labels[r1] : 0;
+                if (label_valid(a, t0)) issue(r0, t0);
+                ++k_next;
+                r0 = r1;
+                t0 = t1;
+                r1 = r2;
+                r2 = r3;
+            }
+            // Every claim's reply is in before this CTA counts itself finished (r0, r1 and r2 hold
+            // the last ones), so the last CTA's reset of the counter comes after them all.
+            *reinterpret_cast<volatile int64_t*>(&ctl.last_claim) = r0 + r1 + r2;
+            if (!stop) {   // the end marker: the next row's first stage completes without data
+                const int st = (int)(q % kStages);
+                if (tc::mbar_wait(&ctl.empty[st], ((q / kStages) & 1) ^ 1, abort_flag, errp, kErrEmpty, a.wait_ns,
+                                  kSuspendRole)) {
+                    ctl.info[e % kInfoSlots] = RowInfo{-1, -1, 0};
+                    tc::mbar_arrive(&ctl.full[st]);
                     ++q;
                 }
             }
-            // Copies still in flight (only after an abort) land before the CTA may exit.
-            int never = 0;
-            for (uint32_t p = q > (uint32_t)kStages ? q - kStages : 0; p < q; ++p)
-                tc::mbar_wait(&ctl.full[p % kStages], (p / kStages) & 1, &never, nullptr, 0, a.wait_ns);
+            // After an abort, copies still in flight land before the CTA may exit.  Only the last
+            // kStages positions can hold one, and only those the marker did not refill.
+            if (*abort_flag) {
+                int never = 0;
+                const uint32_t lo = q > (uint32_t)kStages ? q - kStages : 0;
+                for (uint32_t p = q_copies > (uint32_t)kStages ? q_copies - kStages : 0; p < q_copies; ++p)
+                    if (p >= lo)
+                        tc::mbar_wait(&ctl.full[p % kStages], (p / kStages) & 1, &never, nullptr, 0, a.wait_ns);
+            }
         }
         __syncwarp();
     } else if (warp == kStatsWarp) {
@@ -308,11 +375,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_fused_ring(const __grid_cons
         } else if (a.red == VCE_RED_MEAN) {
             w_valid = *a.inv_n;
         }
-        const int nv = count_valid();
-        for (int e = 0; e < nv; ++e) {
+        for (int e = 0;; ++e) {   // until the end marker
             const int par = e & 1;
             const uint32_t ph = (e >> 1) & 1;
-            tc::mbar_wait(&ctl.rbar[par], ph, abort_flag, errp, kErrPartials, a.wait_ns, kSuspendRole);
+            const bool ok = tc::mbar_wait(&ctl.rbar[par], ph, abort_flag, errp, kErrPartials, a.wait_ns, kSuspendRole);
+            // (after an abort the consumers may have ended early: their slot is then not a row's)
+            if (!__all_sync(0xFFFFFFFFu, ok) || __any_sync(0xFFFFFFFFu, *abort_flag != 0)) break;
+            const RowInfo ri = ctl.info[e % kInfoSlots];
+            if (ri.row < 0) break;
             float m = lane < kConsumerWarps ? ctl.red_m[par][lane] : -kInf;
             float s = lane < kConsumerWarps ? ctl.red_s[par][lane] : 0.f;
 #pragma unroll
@@ -322,7 +392,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_fused_ring(const __grid_cons
                 ms_merge(m, s, m2, s2);
             }
             if (lane == 0) {
-                const RowInfo ri = ctl.info[e % kInfoSlots];
                 const bool own = (uint32_t)ri.tl < (uint32_t)w;
                 float sz = 0.f;   // the slice's sum of logits, warps added in a fixed order
                 if (kSmooth)
@@ -346,7 +415,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_fused_ring(const __grid_cons
                         if (kSmooth) tot += ctl.slot_z[par][r];
                     }
                 }
-                const bool in_range = ri.row >= 0 && ri.row < a.T;   // false only after an abort
+                const bool in_range = ri.row < a.T;   // false only after an abort
                 float loss;
                 float4 st4 = kSmooth ? ce_row_finish_smoothed(M, Ssum, zt, tot, a.V, a.eps, &loss)
                                      : ce_row_finish(M, Ssum, zt, &loss);
@@ -400,15 +469,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_fused_ring(const __grid_cons
         }
 
         // Forward over chunks [j0, j1) of valid row e, whose first chunk is ring chunk q0.  The
-        // row's index and target column are read once its first chunk has landed.
+        // row's index and target column are read once its first chunk has landed; false if that
+        // was the end marker (or the wait gave up).
         auto forward = [&](uint32_t q0, int j0, int j1, int e, RowInfo& ri, float& m, float& s, float& mb,
                            float& sz) {
             for (int j = j0; j < j1; ++j) {
                 const uint32_t p = q0 + j;
                 const int st = (int)(p % kStages);
-                const bool ok = tc::mbar_wait(&ctl.full[st], (p / kStages) & 1, abort_flag, errp, kErrFull,
-                                              a.wait_ns, kSuspendConsumer);
-                if (j == 0) ri = ctl.info[e % kInfoSlots];
+                bool ok = tc::mbar_wait(&ctl.full[st], (p / kStages) & 1, abort_flag, errp, kErrFull, a.wait_ns,
+                                        kSuspendConsumer);
+                if (j == 0) {
+                    if (!__all_sync(0xFFFFFFFFu, ok)) return false;
+                    ri = ctl.info[e % kInfoSlots];
+                    if (ri.row < 0) return false;
+                }
                 if (!ok) continue;
                 const uint4* buf = reinterpret_cast<const uint4*>(smem + st * kChunk);
                 const int nvec = min(kChunk, bytes - j * kChunk) / 16;
@@ -416,6 +490,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_fused_ring(const __grid_cons
                 stage::fwd_stage_any<S, kConsumers, kVecPerThread, kSmooth>(buf, nvec, rel0, tid, m, s, mb,
                                                                             &ctl.zt[e & 1], &sz);
             }
+            return true;
         };
         // This warp's pair of the row, for the stats warp.
         auto publish = [&](int par, float m, float s, float sz) {
@@ -433,20 +508,26 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_fused_ring(const __grid_cons
             if (lane == 0) tc::mbar_arrive(&ctl.rbar[par]);
         };
 
-        const int nv = count_valid();
+        // The stats warp learns of the end from the end marker's slot: the warps arrive on its
+        // partials barrier without partials.
+        auto publish_end = [&](int par) {
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&ctl.rbar[par]);
+        };
         uint32_t q = 0;   // ring chunk of the current row's first chunk
         RowInfo ri{-1, -1, 0};
-        if (nv > 0) {
+        bool have;
+        {
             float m = -kInf, s = 0.f, mb = 0.f, sz = 0.f;
-            forward(q, 0, nchunk, 0, ri, m, s, mb, sz);
-            publish(0, m, s, sz);
+            have = forward(q, 0, nchunk, 0, ri, m, s, mb, sz);
+            if (have) publish(0, m, s, sz);
+            else publish_end(0);
         }
-        for (int e = 0; e < nv; ++e) {
+        for (int e = 0; have; ++e) {
             const int par = e & 1;
-            const bool more = e + 1 < nv;
             RowInfo ri2{-1, -1, 0};
             float m2 = -kInf, s2 = 0.f, mb2 = 0.f, sz2 = 0.f;
-            if (more) forward(q + nchunk, 0, pre, e + 1, ri2, m2, s2, mb2, sz2);
+            const bool more = forward(q + nchunk, 0, pre, e + 1, ri2, m2, s2, mb2, sz2);
 
             // the row's gradient, each stage released once this warp is done with it
             tc::mbar_wait(&ctl.cbar[par], (e >> 1) & 1, abort_flag, errp, kErrCoefs, a.wait_ns, kSuspendConsumer);
@@ -477,14 +558,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_fused_ring(const __grid_cons
             if (more) {
                 forward(q, pre, nchunk, e + 1, ri2, m2, s2, mb2, sz2);
                 publish(par ^ 1, m2, s2, sz2);
+            } else {
+                publish_end(par ^ 1);
             }
             ri = ri2;
+            have = more;
         }
     }
     if (C > 1) cluster_sync();   // no CTA leaves while a peer may still write into its shared memory
-    if (a.fold)
-        fold::finish<kThreads>(a.status, &ctl.err, a.loss_rows, a.T, ctl.n_all, a.red, a.loss_out, ctl.red_sum,
-                               ctl.red_comp, &ctl.last);
+    fold::finish_slot<kThreads>(slot, a.status, &ctl.err, a.fold != 0, a.loss_rows, a.T, ctl.n_all, a.red,
+                                a.loss_out, ctl.red_sum, ctl.red_comp, &ctl.last);
 }
 
 template <typename S, typename O, int C, bool kSmooth>
@@ -590,7 +673,7 @@ cudaError_t launch_fused_ring(vce_dtype dt, vce_dtype gdt, const void* logits, i
     const bool in_kernel = reduced && loss_out && fused_ring_reduces(red, T);
     Args args{logits, T,   V,    ld,   labels, ignore_index, red,   grad_output, inv_n,
               loss_rows, reinterpret_cast<float4*>(row_stats), grad, ld_g, status, slice, wait_ns, tx_extra, eps,
-              in_kernel ? 1 : 0, loss_out};
+              in_kernel ? 1 : 0, loss_out, slots::next_slot()};
     const int sms = device_sm_count();
     cudaError_t e;
     if (dt == VCE_BF16 && gdt == VCE_BF16) e = launch_cs<uint16_t, uint16_t>(C, args, sms, s, launched);
