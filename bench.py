@@ -165,8 +165,8 @@ def kernel_source_hash(files):
 
 
 RING_FILES = ["vocab_cross_entropy_gb300/csrc/ce_ring.cu", "vocab_cross_entropy_gb300/csrc/ce_stage.cuh",
-              "vocab_cross_entropy_gb300/csrc/ce_fold.cuh", "vocab_cross_entropy_gb300/csrc/vce_device.cuh",
-              "vocab_cross_entropy_gb300/csrc/vce_async.cuh"]
+              "vocab_cross_entropy_gb300/csrc/ce_fold.cuh", "vocab_cross_entropy_gb300/csrc/ce_slots.cuh",
+              "vocab_cross_entropy_gb300/csrc/vce_device.cuh", "vocab_cross_entropy_gb300/csrc/vce_async.cuh"]
 
 
 def captured_shape(w):
@@ -296,7 +296,8 @@ def backward_kernel(V):
 
 
 BWD_RING_FILES = ["vocab_cross_entropy_gb300/csrc/ce_bwd_ring.cu", "vocab_cross_entropy_gb300/csrc/ce_stage.cuh",
-                  "vocab_cross_entropy_gb300/csrc/vce_device.cuh", "vocab_cross_entropy_gb300/csrc/vce_async.cuh"]
+                  "vocab_cross_entropy_gb300/csrc/ce_slots.cuh", "vocab_cross_entropy_gb300/csrc/vce_device.cuh",
+                  "vocab_cross_entropy_gb300/csrc/vce_async.cuh"]
 
 
 def forward_kernel(V, T=None, es=2):
@@ -318,8 +319,8 @@ def forward_reduces_in_kernel(V, T, es, reduction):
 
 def forward_call_kernels(V, T, es, reduction):
     """The ce_forward call's kernels in launch order: the row kernel, and k_ce_reduce unless the
-    row kernel reduces the losses itself (or reduction is none).  The status word's clear is a
-    memset, not a kernel of this library."""
+    row kernel reduces the losses itself (or reduction is none).  The stage ring writes the status
+    word itself; before the other row kernels a memset clears it (not a kernel of this library)."""
     k = forward_kernel(V, T, es)
     if reduction == "none":
         return [k]
@@ -329,14 +330,14 @@ def forward_call_kernels(V, T, es, reduction):
 
 
 FWD_RING_FILES = ["vocab_cross_entropy_gb300/csrc/ce_fwd_ring.cu", "vocab_cross_entropy_gb300/csrc/ce_stage.cuh",
-                  "vocab_cross_entropy_gb300/csrc/ce_fold.cuh", "vocab_cross_entropy_gb300/csrc/vce_device.cuh",
-                  "vocab_cross_entropy_gb300/csrc/vce_async.cuh"]
+                  "vocab_cross_entropy_gb300/csrc/ce_fold.cuh", "vocab_cross_entropy_gb300/csrc/ce_slots.cuh",
+                  "vocab_cross_entropy_gb300/csrc/vce_device.cuh", "vocab_cross_entropy_gb300/csrc/vce_async.cuh"]
 
 
 CHUNK_FILES = ["vocab_cross_entropy_gb300/csrc/ce_fwd.cu", "vocab_cross_entropy_gb300/csrc/ce_rows.cuh",
                "vocab_cross_entropy_gb300/csrc/ce_bwd_ring.cu", "vocab_cross_entropy_gb300/csrc/ce_stage.cuh",
-               "vocab_cross_entropy_gb300/csrc/ce_segments.h", "vocab_cross_entropy_gb300/csrc/vce_device.cuh",
-               "vocab_cross_entropy_gb300/csrc/vce_async.cuh"]
+               "vocab_cross_entropy_gb300/csrc/ce_slots.cuh", "vocab_cross_entropy_gb300/csrc/ce_segments.h",
+               "vocab_cross_entropy_gb300/csrc/vce_device.cuh", "vocab_cross_entropy_gb300/csrc/vce_async.cuh"]
 
 
 def one_pass_kernel(V):
