@@ -516,6 +516,46 @@ def test_backward_ring_launch_slots(vce, V):
     torch.cuda.synchronize()
 
 
+def test_ring_launches_on_two_streams(vce):
+    """Ring launches on two streams that nothing orders against each other hold different launch
+    slots: 200 forward + backward pairs alternating between the streams, each on its own batch,
+    give every checked result equal, bit for bit, to the batch's first, and the first matches
+    the oracle."""
+    T, V = 300, 20000
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    batches = []
+    for seed in (5, 6):
+        p = gen.custom(T, V, "bf16", seed=seed, std=2.0, n_margin=6, n_ignore=20)
+        storage = p.full()
+        batches.append(dict(p=p, storage=storage, logits=to_device(storage, "bf16"),
+                            labels=torch.from_numpy(p.labels).cuda(),
+                            rows=torch.empty(T, device="cuda"), out=torch.empty(1, device="cuda"),
+                            stats=torch.empty(T, 4, device="cuda"),
+                            status=torch.empty(1, dtype=torch.int32, device="cuda"),
+                            go=torch.ones(1, device="cuda"),
+                            grad=torch.empty(T, V, dtype=torch.bfloat16, device="cuda"), snaps=[]))
+    torch.cuda.synchronize()
+    for i in range(200):
+        for b, s in zip(batches, streams):
+            with torch.cuda.stream(s):
+                vce.ce_forward(b["logits"], b["labels"], reduction="mean", loss_rows=b["rows"],
+                               loss_out=b["out"], row_stats=b["stats"], status=b["status"], stream=s)
+                vce.ce_backward(b["logits"], b["labels"], b["stats"], b["go"], grad_logits=b["grad"], stream=s)
+                if i % 40 == 0:
+                    b["snaps"].append((b["rows"].clone(), b["out"].clone(), b["grad"].clone(), b["status"].clone()))
+    torch.cuda.synchronize()
+    for b in batches:
+        rows0, out0, grad0, st0 = b["snaps"][0]
+        assert int(st0.item()) == 0
+        ref = O.ce(O.widen(b["storage"], "bf16"), b["p"].labels, "mean")
+        G.check_loss_rows(rows0.cpu().numpy(), ref["loss_rows"], ref["valid"])
+        G.check_reduced(out0.item(), ref["loss_out"])
+        grade_grad(grad0, ref["grad"], b["p"].margin_rows, b["p"].labels)
+        for rows, out, grad, st in b["snaps"][1:]:
+            assert int(st.item()) == 0
+            assert torch.equal(rows, rows0) and torch.equal(out, out0) and torch.equal(grad, grad0)
+
+
 def test_forward_ring_beyond_the_folded_reduction(vce):
     """65540 rows of 32 KB + 16 B: more rows than the ring reduces in-kernel, so k_ce_reduce runs
     after it.  The MEAN call's loss is the fp64 mean of the same kernel's per-row losses (its

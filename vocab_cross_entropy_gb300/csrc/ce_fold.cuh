@@ -144,9 +144,13 @@ __device__ __forceinline__ void finish_slot(slots::LaunchSlot& slot, int32_t* st
     __syncthreads();
     if (!*sm_last) return;
     __threadfence();
+    // every CTA merged its code before it counted itself: the slot's word is final, and its
+    // read overlaps the sum's loads
+    int code = 0;
+    if (threadIdx.x == 0) code = atomicExch(&slot.err, 0);
     if (reduce) sum_losses<NT>(loss_rows, T, n_all, red, loss_out, sm_sum, sm_comp);
     if (threadIdx.x == 0) {
-        *status = atomicExch(&slot.err, 0);
+        *status = code;
         atomicExch(&slot.done, 0);
         atomicExch(&slot.rows, 0u);
     }
