@@ -4,16 +4,15 @@
 // Method: torchtitan PR #5723 "[loss] fix softmax collapse with improved ce perf" -- the loss is
 // the sum of the rows' NLL, over the N rows with a valid label for MEAN (ignored rows weigh 0).
 //
-// Protocol.  The caller clears the status word before the kernel.  Every CTA counts the
-// batch's valid labels itself (count_valid_strided, while its first copies are in flight), so
-// each row's weight 1/N is known where the row is finished.  Within the kernel, error codes
-// collect in a word of the CTA's shared memory.  At the end each CTA merges its code into the
-// low 16 bits of the status word (the first code wins) and adds one to a count of finished CTAs
-// in the high 16 bits; the CTA that finds itself last sums every row's loss in a fixed order
-// (thread i takes rows i, i + NT, ...; lanes, then warps, merged in order) as an fp32 (sum,
-// compensation) pair with two-sum steps, as k_ce_reduce does, writes the reduced loss and
-// clears the count.  The sum of an ignored row's +0 loss adds nothing; a bad label's NaN
-// makes the reduced loss NaN.
+// Protocol.  Every CTA counts the batch's valid labels itself (count_valid_strided, while its
+// first copies are in flight), so each row's weight 1/N is known where the row is finished.
+// Within the kernel, error codes collect in a word of the CTA's shared memory.  At the end each
+// CTA merges its code into its launch slot (ce_slots.cuh; the first code wins) and adds one to
+// the slot's count of finished CTAs; the CTA that finds itself last sums every row's loss in a
+// fixed order (thread i takes rows i, i + NT, ...; lanes, then warps, merged in order) as an
+// fp32 (sum, compensation) pair with two-sum steps, as k_ce_reduce does, writes the reduced
+// loss and the status word, and puts the slot back to zero.  The sum of an ignored row's +0
+// loss adds nothing; a bad label's NaN makes the reduced loss NaN.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -26,18 +25,6 @@ namespace vce {
 namespace fold {
 
 constexpr int64_t kMaxRows = 65536;   // every CTA reads every label: at most 512 KB of them
-
-// Merge an error code into the low 16 bits of the status word, whose high bits may count
-// finished CTAs: the first code wins.  Each retry follows another thread's change of the word
-// (a CTA's count or a code), so the loop ends.
-__device__ __forceinline__ void status_merge(int32_t* status, int32_t code) {
-    int32_t old = *reinterpret_cast<volatile int32_t*>(status);
-    while ((old & 0xFFFF) == 0) {
-        const int32_t prev = atomicCAS(status, old, old | code);
-        if (prev == old) break;
-        old = prev;
-    }
-}
 
 // s + x = t + e exactly (Knuth's TwoSum); e goes into the compensation c.
 __device__ __forceinline__ void add(float& s, float& c, float x) {
@@ -101,35 +88,12 @@ __device__ __forceinline__ void sum_losses(const float* loss_rows, int64_t T, lo
     }
 }
 
-// Called by all NT threads of the block once every output of its rows is written (and, in a
-// cluster, after the closing cluster barrier).  err: the CTA's error word in shared memory;
-// n_all: the batch's valid labels; sm_sum, sm_comp: NT / 32 floats of shared memory; sm_last:
-// one int of shared memory.  The count of finished CTAs sits in the status word's high bits.
-template <int NT>
-__device__ __forceinline__ void finish(int32_t* status, const int* err, const float* loss_rows, int64_t T,
-                                       long long n_all, int red, float* loss_out, float* sm_sum, float* sm_comp,
-                                       int* sm_last) {
-    // Every thread's own stores (the rows' losses, weights, gradients) are made visible device-
-    // wide before the count moves: a fence orders only the fencing thread's writes, and the block
-    // barrier does not wait for other warps' global stores to be performed.
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        if (*err) status_merge(status, *err);
-        const int32_t prev = atomicAdd(status, 1 << 16);
-        *sm_last = ((prev >> 16) & 0xFFFF) == (int32_t)gridDim.x - 1;
-    }
-    __syncthreads();
-    if (!*sm_last) return;
-    __threadfence();
-    sum_losses<NT>(loss_rows, T, n_all, red, loss_out, sm_sum, sm_comp);
-    if (threadIdx.x == 0) atomicAnd(status, 0xFFFF);   // the count goes; the first error code stays
-}
-
-// The same end for a kernel that holds a launch slot (ce_slots.cuh): the count and the first
-// error code sit in the slot; the last CTA reduces the losses if `reduce`, writes the status
-// word (the first code, or 0) and puts the slot back to zero.  Every claim on the slot's row
-// counter was made before its CTA got here.
+// The end of a ring kernel, called by all NT threads of the block once every output of its rows
+// is written (and, in a cluster, after the closing cluster barrier).  err: the CTA's error word
+// in shared memory; n_all: the batch's valid labels; sm_sum, sm_comp: NT / 32 floats of shared
+// memory; sm_last: one int of shared memory.  The last CTA reduces the losses if `reduce`,
+// writes the status word (the first code, or 0) and puts the slot back to zero.  Every claim on
+// the slot's row counter was made before its CTA got here.
 template <int NT>
 __device__ __forceinline__ void finish_slot(slots::LaunchSlot& slot, int32_t* status, const int* err, bool reduce,
                                             const float* loss_rows, int64_t T, long long n_all, int red,

@@ -492,8 +492,8 @@ extern "C" int ce_forward_ls(const void* logits, vce_dtype dt, int64_t T, int64_
         // Rows of at most 32 KB: one warp per row (k_ce_fwd_warp; 8192 x 16000 bf16: 0.070 ms,
         // against 0.080 on the stage ring and 0.102 on the ring's four consumer groups).  Longer
         // rows of whole 16-byte vectors stream through the shared-memory stage ring (rows of
-        // two stages with its consumers in two groups: 4096 x 32000 bf16, 0.0592 ms, against
-        // 0.0613 on one block per row), other layouts one block per row with global loads.
+        // two stages with its consumers in two groups: 4096 x 32000 bf16, 0.052 ms back to back,
+        // against 0.0613 on one block per row), other layouts one block per row with global loads.
         bool launched = false;
         const int64_t row_bytes = V * (int64_t)es;
         cudaError_t e = cudaSuccess;
