@@ -262,15 +262,32 @@ VCE_API int ce_forward_backward_ls(const void* logits, vce_dtype dt, int64_t T, 
  * shared-memory kernel (no page counterpart).  Runs that kernel on bf16 logits [T, V]
  * (ld = V), ignore_index -100, reduction SUM, with its producer announcing 16 more bytes per
  * stage than its copies deliver, so no stage ever completes.  Every wait is bounded by wait_ns
- * (1 ms .. 2 s): the waiting warps give up and write their code to *status (105..109, see
- * ce_forward_backward).  The CTA keeps its barrier arrivals, lets its copies land (bounded)
- * and returns; the context stays usable.  loss_rows, row_stats and grad_logits are undefined
- * afterwards.  Returns VCE_ERR_ARG, enqueuing nothing but the status reset, when [T, V] does
- * not take the shared-memory kernel (V not a multiple of 8, pointers not 16-byte aligned).
+ * (1 ms .. 2 s): the waiting warps give up and record their code, which the last CTA writes
+ * to *status (105..109, see ce_forward_backward).  Each role stops at its next wait, the
+ * producer lets its copies land (bounded) and the kernel returns; the context stays usable and
+ * the launch slot is left zero.  loss_rows, row_stats and grad_logits are undefined afterwards.
+ * Returns VCE_ERR_ARG, enqueuing nothing but the status reset, when [T, V] does not take the
+ * shared-memory kernel (V not a multiple of 8, pointers not 16-byte aligned).
  */
 VCE_API int vce_test_ce_fused_stall(const void* logits, int64_t T, int64_t V, const int64_t* labels,
                             const float* grad_output, float* loss_rows, float* row_stats,
                             void* grad_logits, uint64_t wait_ns, int32_t* status, vce_stream_t s);
+
+/*
+ * vce_test_ce_fwd_stall -- test hook for the give-up path of ce_forward's stage-ring kernel
+ * (no page counterpart).  Runs that kernel on bf16 logits [T, V] (ld = V, 1 <= T <= 65536,
+ * V * 2 > 32768 bytes), ignore_index -100, reduction SUM, with its producer announcing 16 more
+ * bytes per stage than its copies deliver, so no stage ever completes.  Every wait is bounded
+ * by wait_ns (1 ms .. 2 s): the waiting warps give up and record their code, which the last
+ * CTA writes to *status (105, 106, 108, 110 or 112, see ce_forward) with no clearing before;
+ * the kernel returns, the context stays usable and the launch slot is left zero.  loss_rows,
+ * row_stats and *loss_out are undefined afterwards.  Returns VCE_ERR_ARG, enqueuing nothing,
+ * when the rows do not take the stage ring (V not a multiple of 8, logits not 16-byte aligned,
+ * rows of at most 32 KB).
+ */
+VCE_API int vce_test_ce_fwd_stall(const void* logits, int64_t T, int64_t V, const int64_t* labels,
+                                  float* loss_rows, float* row_stats, float* loss_out, uint64_t wait_ns,
+                                  int32_t* status, vce_stream_t s);
 
 /*
  * ce_merge_chunks -- CE forward (+ backward) over logits held as k column chunks

@@ -61,6 +61,13 @@ def test_argument_errors_need_no_gpu(lib):
     m = lib.ce_merge_chunks
     assert m(0, None, None, None, 1, 4, None, -100, 2, None, None, None, None, None, None, 1, None, None,
              None) == -8
+    st = lib.vce_test_ce_fwd_stall   # the forward ring's give-up hook: its host checks
+    st.argtypes = [P, i64, i64, P, P, P, P, ctypes.c_uint64, P, P]
+    assert st(x, 4, 20000, x, x, x, x, 50_000_000, None, None) == -1       # null status
+    assert st(x, 0, 20000, x, x, x, x, 50_000_000, x, None) == -3          # no rows
+    assert st(x, 70000, 20000, x, x, x, x, 50_000_000, x, None) == -3      # beyond the folded reduction
+    assert st(x, 4, 20000, x, x, x, x, 1000, x, None) == -8                # wait bound under 1 ms
+    assert st(x, 4, 8000, x, x, x, x, 50_000_000, x, None) == -8           # 16 KB rows: the warp kernel
 
 
 def test_linear_and_gemm_hook_argument_errors_need_no_gpu(lib):

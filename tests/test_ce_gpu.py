@@ -556,6 +556,43 @@ def test_ring_launches_on_two_streams(vce):
             assert torch.equal(rows, rows0) and torch.equal(out, out0) and torch.equal(grad, grad0)
 
 
+def test_forward_ring_stall_gives_up_and_the_slot_stays_usable(vce):
+    """Stages that never complete in ce_forward's stage ring (its producer announces 16 bytes more
+    per stage than its copies deliver): the bounded waits give up with a code that the kernel
+    itself writes into a status word filled with garbage, the call returns within seconds, and
+    the next 1100 calls -- one of them on the launch slot the stalled launch held -- are correct
+    with status 0."""
+    import time
+    T, V = 300, 20000
+    p = gen.custom(T, V, "bf16", seed=29, std=2.0, n_margin=4, n_ignore=10)
+    storage = p.full()
+    logits = to_device(storage, "bf16")
+    labels = torch.from_numpy(p.labels).cuda()
+    t0 = time.time()
+    st = vce.vce_test_ce_fwd_stall(logits, labels, wait_ns=50_000_000)
+    assert st in (105, 106, 108, 110, 112), st
+    assert "gave up" in vce.vce_status_string(st)
+    assert time.time() - t0 < 60
+    ref = O.ce(O.widen(storage, "bf16"), p.labels, "mean")
+    rows = torch.empty(T, dtype=torch.float32, device="cuda")
+    out = torch.empty(1, dtype=torch.float32, device="cuda")
+    stats = torch.empty(T, 4, dtype=torch.float32, device="cuda")
+    status = torch.empty(1, dtype=torch.int32, device="cuda")
+    first = None
+    for i in range(1100):
+        vce.ce_forward(logits, labels, reduction="mean", loss_rows=rows, loss_out=out, row_stats=stats,
+                       status=status)
+        if i % 100 and i != 1099:
+            continue
+        assert vce.vce_get_status(status) == 0, i
+        if first is None:
+            first = (rows.clone(), out.clone())
+            G.check_loss_rows(first[0].cpu().numpy(), ref["loss_rows"], ref["valid"])
+            G.check_reduced(first[1].item(), ref["loss_out"])
+        else:
+            assert torch.equal(rows, first[0]) and torch.equal(out, first[1]), i
+
+
 def test_forward_ring_beyond_the_folded_reduction(vce):
     """65540 rows of 32 KB + 16 B: more rows than the ring reduces in-kernel, so k_ce_reduce runs
     after it.  The MEAN call's loss is the fp64 mean of the same kernel's per-row losses (its

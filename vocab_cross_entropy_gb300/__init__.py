@@ -93,6 +93,8 @@ def _load(path=None):
             L.vce_test_gemm_skip.restype = i32
         L.vce_test_ce_fused_stall.argtypes = [p, i64, i64, p, p, p, p, p, ctypes.c_uint64, p, p]
         L.vce_test_ce_fused_stall.restype = i32
+        L.vce_test_ce_fwd_stall.argtypes = [p, i64, i64, p, p, p, p, ctypes.c_uint64, p, p]
+        L.vce_test_ce_fwd_stall.restype = i32
     for name in ("ce_forward", "ce_backward", "ce_forward_ls", "ce_backward_ls", "ce_forward_backward",
                  "ce_forward_backward_ls", "ce_merge_chunks_ls",
                  "ce_merge_chunks", "ce_merge_chunks_noalloc",
@@ -408,6 +410,21 @@ def vce_test_gemm_skip(A, B, skip_bits, *, stream=None):
     _check("vce_test_gemm_skip", _get().vce_test_gemm_skip(_ptr(A), _ptr(B), M, N, K, _ptr(skip_bits),
                                                         skip_bits.shape[1], _ptr(C), _stream(stream)))
     return C
+
+
+def vce_test_ce_fwd_stall(logits, labels, wait_ns=50_000_000, *, stream=None):
+    """Run ce_forward's stage-ring kernel with stages that never complete; returns the device
+    status word (written by the kernel itself: filled with garbage first)."""
+    T, V = logits.shape
+    dev = logits.device
+    loss_rows = torch.empty(T, dtype=torch.float32, device=dev)
+    row_stats = torch.empty(T, ROW_STATS, dtype=torch.float32, device=dev)
+    loss_out = torch.empty(1, dtype=torch.float32, device=dev)
+    status = torch.full((1,), 0x7FFF1234, dtype=torch.int32, device=dev)
+    _check("vce_test_ce_fwd_stall", _get().vce_test_ce_fwd_stall(
+        _ptr(logits), T, V, _ptr(labels), _ptr(loss_rows), _ptr(row_stats), _ptr(loss_out), int(wait_ns),
+        _ptr(status), _stream(stream)))
+    return vce_get_status(status, stream)
 
 
 def vce_test_ce_fused_stall(logits, labels, wait_ns=50_000_000, *, stream=None):

@@ -116,6 +116,7 @@ struct Args {
     int red;                           // vce_reduction
     float* loss_out;                   // the reduced loss (fold)
     int slot;                          // this launch's slot (ce_slots.cuh)
+    uint32_t tx_extra;                 // 0; > 0 only in the give-up test (a stage never completes)
 };
 
 __device__ __forceinline__ bool label_valid(const Args& a, int64_t t) {
@@ -201,7 +202,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_ce_fwd_ring(const __grid_consta
                     stop = true;
                     return;
                 }
-                tc::mbar_arrive_expect_tx(&ctl.full[st], nb);
+                tc::mbar_arrive_expect_tx(&ctl.full[st], nb + a.tx_extra);
                 tc::bulk_load(smem + st * kChunk, src + (int64_t)j * kChunk, nb, &ctl.full[st]);
                 q_copies = ++q;
             }
@@ -421,7 +422,8 @@ VCE_DEBUG_READER(debug_word_ce_fwd_ring)
 
 cudaError_t launch_fwd_ring(vce_dtype dt, const void* logits, int64_t T, int64_t V, int64_t ld, const int64_t* labels,
                             int64_t ignore_index, float eps, int red, float* loss_rows, float* loss_out,
-                            float* row_stats, int32_t* status, cudaStream_t s, bool* launched, bool* reduced) {
+                            float* row_stats, int32_t* status, cudaStream_t s, bool* launched, bool* reduced,
+                            uint64_t wait_ns, uint32_t tx_extra) {
     using namespace fring;
     *launched = false;
     *reduced = false;
@@ -429,8 +431,8 @@ cudaError_t launch_fwd_ring(vce_dtype dt, const void* logits, int64_t T, int64_t
     if (T < 1 || V % 8 || ld % 8 || !aligned(logits, 16) || V > (int64_t)1 << 30) return cudaSuccess;
     const bool in_kernel = red != VCE_RED_NONE && T <= fold::kMaxRows;
     Args args{logits,    T,   V,          ld,          labels,          ignore_index, loss_rows,
-              reinterpret_cast<float4*>(row_stats), status, eps, tc::kWaitNs, in_kernel ? 1 : 0, red, loss_out,
-              slots::next_slot()};
+              reinterpret_cast<float4*>(row_stats), status, eps, wait_ns, in_kernel ? 1 : 0, red, loss_out,
+              slots::next_slot(), tx_extra};
     const int sms = device_sm_count();
     const cudaError_t e = dt == VCE_BF16 ? launch<uint16_t>(args, sms, s) : launch<float>(args, sms, s);
     if (e == cudaSuccess) {
@@ -441,3 +443,24 @@ cudaError_t launch_fwd_ring(vce_dtype dt, const void* logits, int64_t T, int64_t
 }
 
 }  // namespace vce
+
+using namespace vce;
+
+extern "C" int vce_test_ce_fwd_stall(const void* logits, int64_t T, int64_t V, const int64_t* labels, float* loss_rows,
+                                     float* row_stats, float* loss_out, uint64_t wait_ns, int32_t* status,
+                                     vce_stream_t s) {
+    if (!logits || !labels || !loss_rows || !row_stats || !loss_out || !status) return VCE_ERR_NULL;
+    if (T < 1 || T > fold::kMaxRows || V < 1) return VCE_ERR_SHAPE;
+    if (wait_ns < 1000000ull || wait_ns > tc::kWaitNs) return VCE_ERR_ARG;
+    if (V * 2 <= 32768) return VCE_ERR_ARG;   // rows of at most 32 KB take the warp kernel
+    if (!aligned(row_stats, 16) || !aligned(labels, 8) || !aligned(loss_rows, 4) || !aligned(loss_out, 4))
+        return VCE_ERR_ALIGN;
+    int rc = require_sm100();
+    if (rc) return rc;
+    bool launched = false, reduced = false;
+    // 16 bytes announced beyond each copy: no stage ever completes
+    if (launch_fwd_ring(VCE_BF16, logits, T, V, V, labels, -100, 0.f, VCE_RED_SUM, loss_rows, loss_out, row_stats,
+                        status, s, &launched, &reduced, wait_ns, 16) != cudaSuccess)
+        return VCE_ERR_CUDA;
+    return launched ? VCE_OK : VCE_ERR_ARG;
+}

@@ -83,8 +83,11 @@ cudaError_t launch_bwd_ring(vce_dtype dt, vce_dtype gdt, const SegTable& tab, co
 // kernel also reduces the losses into *loss_out and writes the rows' weights, and sets
 // *reduced; the status word must then be 0 when the kernel starts (its high bits count the
 // finished CTAs).
+// wait_ns bounds every wait of the kernel; tx_extra > 0 (test hook only) announces that many
+// more bytes per stage than its copies deliver, so no stage completes.
 cudaError_t launch_fwd_ring(vce_dtype dt, const void* logits, int64_t T, int64_t V, int64_t ld, const int64_t* labels,
                             int64_t ignore_index, float eps, int red, float* loss_rows, float* loss_out,
-                            float* row_stats, int32_t* status, cudaStream_t s, bool* launched, bool* reduced);
+                            float* row_stats, int32_t* status, cudaStream_t s, bool* launched, bool* reduced,
+                            uint64_t wait_ns = 2000000000ull, uint32_t tx_extra = 0);
 
 }  // namespace vce

@@ -75,10 +75,10 @@ extern "C" const char* vce_status_string(int status) {
         case 102: return "a GEMM pipeline wait for a loaded shared-memory stage gave up";
         case 103: return "a GEMM pipeline wait for a free accumulator gave up";
         case 104: return "a GEMM pipeline wait for a finished accumulator gave up";
-        case 105: return "a one-pass CE wait for a free shared-memory stage gave up";
-        case 106: return "a one-pass CE wait for a loaded shared-memory stage gave up";
+        case 105: return "a CE stage-ring wait for a free shared-memory stage gave up";
+        case 106: return "a CE stage-ring wait for a loaded shared-memory stage gave up";
         case 107: return "a one-pass CE wait for the cluster's row statistics gave up";
-        case 108: return "a one-pass CE wait for the warps' partial row statistics gave up";
+        case 108: return "a CE stage-ring wait for the warps' partial row statistics gave up";
         case 109: return "a one-pass CE wait for a row's gradient coefficients gave up";
         case 110: return "a CE forward wait for free statistics slots gave up";
         case 111: return "a CE forward ring was launched with consumer groups for rows too long for them";
