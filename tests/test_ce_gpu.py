@@ -593,6 +593,28 @@ def test_forward_ring_stall_gives_up_and_the_slot_stays_usable(vce):
             assert torch.equal(rows, first[0]) and torch.equal(out, first[1]), i
 
 
+@pytest.mark.parametrize("V", [20000, 70000])
+def test_forward_ring_first_rows_ignored(vce, V):
+    """Rows 0..199 ignored: every CTA's first fixed rows (152 CTAs) are ignored ones, which the
+    producer skips and the statistics warp writes as +0 losses with zero statistics; the rest
+    match the oracle, the mean included."""
+    T = 600
+    p = gen.custom(T, V, "bf16", seed=V + 11, std=2.0, n_margin=10)
+    labels = p.labels.copy()
+    labels[:200] = -100
+    storage = p.full()
+    logits = to_device(storage, "bf16")
+    lab = torch.from_numpy(labels).cuda()
+    out, rows, stats, status = vce.ce_forward(logits, lab, -100, "mean")
+    torch.cuda.synchronize()
+    assert vce.vce_get_status(status) == 0
+    ref = O.ce(O.widen(storage, "bf16"), labels, "mean")
+    lr = rows.cpu().numpy()
+    assert np.all(lr[:200] == 0) and np.all(stats.cpu().numpy()[:200] == 0)
+    G.check_loss_rows(lr, ref["loss_rows"], ref["valid"])
+    G.check_reduced(out.item(), ref["loss_out"])
+
+
 def test_forward_ring_beyond_the_folded_reduction(vce):
     """65540 rows of 32 KB + 16 B: more rows than the ring reduces in-kernel, so k_ce_reduce runs
     after it.  The MEAN call's loss is the fp64 mean of the same kernel's per-row losses (its
