@@ -722,3 +722,39 @@ def test_empty_batch(vce, dtype):
             else:
                 assert lo.item() == want
         assert grad.shape == (0, 1000) and g2.shape == (0, 1000) and [g.shape for g in g3] == [(0, 300), (0, 700)]
+
+
+@pytest.mark.parametrize("seed", range(16))
+def test_random_shapes(vce, seed):
+    """Randomised shapes and options through the two-call path and the one-pass call: row counts
+    from 1 to 700 (fewer than, about and several times the 152 CTAs), vocabularies that take the
+    warp kernel, the stage ring with one or two consumer groups, the per-block kernel (not a
+    multiple of 8) and clusters in the one pass; bf16 or fp32 logits and gradients, each
+    reduction, ignored rows and raised targets.  Every output against the oracle."""
+    rng = np.random.default_rng(1000 + seed)
+    T = int(rng.choice([1, 7, 151, 152, 153])) if rng.random() < 0.4 else int(rng.integers(200, 700))
+    V = int(rng.choice([int(rng.integers(2, 4000)), int(rng.integers(16001, 16400)) * 2 // 2,
+                        int(rng.integers(4000, 8192)) * 8, int(rng.integers(8200, 12000)) * 8 + 3,
+                        70000]))
+    dtype = str(rng.choice(["bf16", "f32"]))
+    gdt = [None, torch.float32, torch.bfloat16][int(rng.integers(0, 3))]
+    reduction = str(rng.choice(["mean", "sum", "none"]))
+    n_ignore = int(rng.integers(0, max(1, T // 4)))
+    n_margin = int(rng.integers(0, max(1, T // 8)))
+    p = gen.custom(T, V, dtype, seed=seed, std=2.0, n_margin=n_margin, margin=(17.0, 50.0), n_ignore=n_ignore)
+    go = rng.uniform(0.25, 2.0, T) if reduction == "none" else float(rng.uniform(0.25, 2.0))
+    full_check(vce, p, reduction, go, gdt)
+    storage = p.full()
+    logits = to_device(storage, dtype)
+    labels = torch.from_numpy(p.labels).cuda()
+    g = torch.empty(T if reduction == "none" else 1, device="cuda")
+    g[:] = torch.as_tensor(go, dtype=torch.float32)
+    out, rows, stats, grad, status = vce.ce_forward_backward(logits, labels, reduction=reduction, grad_output=g,
+                                                             grad_dtype=gdt)
+    torch.cuda.synchronize()
+    assert vce.vce_get_status(status) == 0
+    ref = O.ce(O.widen(storage, dtype), p.labels, reduction, go)
+    G.check_loss_rows(rows.cpu().numpy(), ref["loss_rows"], ref["valid"])
+    if reduction != "none":
+        G.check_reduced(out.item(), ref["loss_out"])
+    grade_grad(grad, ref["grad"], p.margin_rows, p.labels)
