@@ -215,3 +215,21 @@ def test_full_size_sampled(vce):
     Gc = O.linear_ce_grad_columns(E, W, p.labels, fwd, c, cols)
     grade_sum(host(dW[torch.from_numpy(cols).cuda()]), Gc.T @ E, np.abs(Gc).T @ np.abs(E), "full-size dW rows",
               st["dW"])
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_shapes(vce, seed):
+    """Randomised linear-CE shapes and options against the fp64 oracle: one or many 128-row tiles
+    (single CTAs or CTA pairs), D giving an odd or an even number of 64-column K blocks (one or
+    two K blocks per pipeline stage), vocabularies inside one chunk or over several, each
+    reduction, bf16 or fp32 gradients, ignored rows."""
+    rng = np.random.default_rng(2000 + seed)
+    T = int(rng.choice([1, 100, 128, 129, 256])) if rng.random() < 0.4 else int(rng.integers(257, 1300))
+    D = 8 * int(rng.choice([1, 8, 16, 24, 48, int(rng.integers(1, 97))]))
+    V = int(rng.choice([1, int(rng.integers(2, 600)), int(rng.integers(600, 9000)), int(rng.integers(30000, 40000)),
+                        int(rng.integers(40000, 70000))]))
+    reduction = str(rng.choice(["mean", "sum", "none"]))
+    gdt = torch.bfloat16 if rng.random() < 0.7 else torch.float32
+    n_ignore = int(rng.integers(0, max(1, T // 5)))
+    go = rng.uniform(0.25, 2.0, T) if reduction == "none" else float(rng.uniform(0.25, 2.0))
+    full_check(vce, gen.linear_custom(T, D, V, seed=seed, n_ignore=n_ignore), reduction, go, gdt)
