@@ -131,3 +131,22 @@ def test_pages_chunked_matches_unchunked_and_oracle(vce):
     assert np.all(own.sum(0)[valid] == 1) and np.all(own.sum(0)[~valid] == 0)
     M = cs[:, rows, 0].max(axis=0)
     assert np.array_equal(M[fwd["valid"]].astype(np.float64), fwd["max_nt"][fwd["valid"]])
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_random_chunkings(vce, seed):
+    """Randomised chunkings against the oracle: 1 to 16 chunks, widths that are and are not
+    whole 16-byte vectors (the backward ring's items or the per-block kernel), row counts about
+    and beyond the 152 CTAs, either logits dtype, each reduction, ignored rows and raised
+    targets."""
+    rng = np.random.default_rng(3000 + seed)
+    k = int(rng.integers(1, 17))
+    widths = [int(rng.choice([int(rng.integers(1, 40)), 8 * int(rng.integers(1, 600)), int(rng.integers(1, 9000))]))
+              for _ in range(k)]
+    T = int(rng.choice([1, 152, 153])) if rng.random() < 0.3 else int(rng.integers(100, 600))
+    dtype = str(rng.choice(["bf16", "f32"]))
+    reduction = str(rng.choice(["mean", "sum", "none"]))
+    go = rng.uniform(0.25, 2.0, T) if reduction == "none" else float(rng.uniform(0.25, 2.0))
+    p = gen.custom(T, sum(widths), dtype, seed=seed, std=2.5, n_margin=int(rng.integers(0, max(1, T // 8))),
+                   margin=(17.0, 50.0), n_ignore=int(rng.integers(0, max(1, T // 5))))
+    chunk_check(vce, p, widths, reduction, go)
