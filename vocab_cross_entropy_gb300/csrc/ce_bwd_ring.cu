@@ -22,8 +22,8 @@
 //                   labels) among blockIdx.x, blockIdx.x + gridDim.x, ..., whose logits are not
 //                   read
 // Every wait is bounded (2 s).  A wait that gives up sets the CTA's abort flag; every role then
-// keeps its arrivals but skips the work and later waits.  ce_backward has no status word, so
-// the gradient is then undefined without a report.
+// stops at its next wait, and the producer lets its copies in flight land (bounded).
+// ce_backward has no status word, so the gradient is then undefined without a report.
 #include <cuda_runtime.h>
 #include <stdint.h>
 

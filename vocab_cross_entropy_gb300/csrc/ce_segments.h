@@ -52,8 +52,9 @@ cudaError_t launch_ce_bwd(vce_dtype dt, vce_dtype gdt, int nt, const SegTable& t
 // fits).  eps: label smoothing (0: none).  wait_ns bounds every wait of the kernel; tx_extra > 0
 // (tests only) announces that many bytes more per stage than each copy delivers, so no stage
 // completes and the waits give up.  reduced != null asks the kernel to reduce the losses into
-// *loss_out itself (SUM / MEAN over at most 65536 rows; inv_n is then unused and the status word
-// must be 0 when the kernel starts) and reports whether it does.
+// *loss_out itself (SUM / MEAN over at most 65536 rows; inv_n is then unused) and reports whether
+// it does.  The kernel writes *status itself at its end (the launch's first error code, or 0):
+// it needs no clearing before.
 cudaError_t launch_fused_ring(vce_dtype dt, vce_dtype gdt, const void* logits, int64_t T, int64_t V, int64_t ld,
                               const int64_t* labels, int64_t ignore_index, int red, const float* grad_output,
                               const float* inv_n, float* loss_rows, float* row_stats, void* grad, int64_t ld_g,
@@ -69,7 +70,8 @@ bool fused_ring_layout_ok(vce_dtype dt, int64_t T, int64_t V, int64_t ld, int64_
 bool fused_ring_reduces(int red, int64_t T);
 
 // The gradient of every (chunk, row) segment of `tab` with each segment streamed through a
-// shared-memory stage ring (ce_bwd_ring.cu): the same entries as launch_ce_bwd.  Leaves
+// shared-memory stage ring (ce_bwd_ring.cu; items claimed at run time, ce_slots.cuh): the same
+// entries as launch_ce_bwd.  Leaves
 // *launched false, enqueuing nothing, unless every input and output chunk row is whole 16-byte
 // vectors on a 16-byte boundary.
 cudaError_t launch_bwd_ring(vce_dtype dt, vce_dtype gdt, const SegTable& tab, const int64_t* labels,
@@ -81,9 +83,8 @@ cudaError_t launch_bwd_ring(vce_dtype dt, vce_dtype gdt, const SegTable& tab, co
 // enqueuing nothing, when the layout does not fit (rows or leading dimension not multiples of
 // 8 elements, logits not 16-byte aligned).  For red SUM / MEAN and at most 65536 rows the
 // kernel also reduces the losses into *loss_out and writes the rows' weights, and sets
-// *reduced; the status word must then be 0 when the kernel starts (its high bits count the
-// finished CTAs).
-// wait_ns bounds every wait of the kernel; tx_extra > 0 (test hook only) announces that many
+// *reduced.  The kernel writes *status itself at its end (the launch's first error code, or 0):
+// it needs no clearing before.  wait_ns bounds every wait of the kernel; tx_extra > 0 (test hook only) announces that many
 // more bytes per stage than its copies deliver, so no stage completes.
 cudaError_t launch_fwd_ring(vce_dtype dt, const void* logits, int64_t T, int64_t V, int64_t ld, const int64_t* labels,
                             int64_t ignore_index, float eps, int red, float* loss_rows, float* loss_out,
